@@ -1,0 +1,33 @@
+"""Budget accounting against the rows the settings tables print (tests/golden/table_budgets.json)."""
+import json
+import os
+
+import pytest
+
+from oracle import budgets
+from synth import SNAPKV_PREFILL_32K, QWEN3_30B_A3B_QUEST_128K, QWEN3_4B_QUEST_32K
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "table_budgets.json")))
+
+
+@pytest.mark.parametrize("row", GOLD["rows"], ids=lambda r: r["cite"])
+def test_total_is_selected_plus_sink_plus_recent(row):
+    assert budgets.total_kept_tokens(row["selected"], row["sink"], row["recent"]) == row["total"]
+    if "pages" in row:
+        assert budgets.selected_pages(row["selected"]) == row["pages"]
+
+
+def test_workload_budgets_follow_the_tables():
+    # 2,048 and 4,096 selected tokens are 128 and 256 sixteen-token pages.
+    assert QWEN3_4B_QUEST_32K.topk_pages == budgets.selected_pages(2048)
+    assert QWEN3_30B_A3B_QUEST_128K.topk_pages == budgets.selected_pages(4096)
+    s = GOLD["snapkv_longbench"]
+    wl = SNAPKV_PREFILL_32K
+    assert (wl.keep_topk, wl.window, wl.pool_kernel) == (s["selected"], s["recent"], s["pooling_kernel"])
+    assert s["scoring_window"] == wl.window
+    assert budgets.total_kept_tokens(wl.keep_topk, s["sink"], wl.window) == 2048
+
+
+def test_partial_page_budget_rejected():
+    with pytest.raises(ValueError):
+        budgets.selected_pages(2008)
