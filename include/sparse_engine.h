@@ -1,0 +1,219 @@
+/*
+ * sparse_engine.h -- C ABI of the GB300 (sm_103a) sparse decode attention library.
+ *
+ * The library implements the data-parallel hot path of a sparse-first serving
+ * engine as described in "SparseEngine: Sparse-First Inference Engine"
+ * (arXiv 2609.39068):
+ *   - Quest: query-aware selection of 16-token KV pages from per-page key
+ *     summaries, then attention over the selected pages only (Figure 2 caption,
+ *     Figure 3 caption, Tables 8-12, Table 14);
+ *   - SnapKV: eviction at the end of prefill from observation-window attention
+ *     scores with max-pooling, keeping the selected tokens plus the window in
+ *     compacted pages (Figure 2 caption, Table 8, Table 10, Table 15 note).
+ * The pages do not print either method's equations; each entry point below
+ * states the computation it performs.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named in a signature are DEVICE pointers unless the comment says
+ *    "host". Structs are passed by host pointer and read during the call only.
+ *  - The caller owns every buffer, including workspaces sized by the
+ *    *_workspace_size functions. The library allocates no device memory and
+ *    keeps no per-call state.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream). Results are valid once the stream has reached the call.
+ *  - Arguments are validated on the host before anything is launched: a bad
+ *    argument returns SE_ERR_INVALID_ARG (or SE_ERR_UNSUPPORTED for a shape
+ *    the kernels do not implement, SE_ERR_WORKSPACE for a short workspace) and
+ *    launches nothing. A launch failure returns SE_ERR_CUDA.
+ *  - Device pointers must be 16-byte aligned. Device-side contents (lengths,
+ *    page ids) are checked in the kernels: a value out of range sets a bit in the
+ *    library's device error word, and the offending page or request is skipped.
+ *    Read the word with se_read_device_error().
+ *  - bf16 is IEEE-style bfloat16 (1-8-7), stored as uint16.
+ *  - Page size is 16 tokens.
+ */
+#ifndef SPARSE_ENGINE_H
+#define SPARSE_ENGINE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SE_API __attribute__((visibility("default")))
+#else
+#define SE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SE_OK = 0,
+  SE_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned pointer, stride too small */
+  SE_ERR_UNSUPPORTED = 2,  /* valid arguments, shape not implemented (e.g. head_dim) */
+  SE_ERR_WORKSPACE = 3,    /* workspace_bytes smaller than the *_workspace_size answer */
+  SE_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+  SE_ERR_DEVICE = 5        /* the device error word is non-zero (se_read_device_error) */
+} se_status_t;
+
+/* Bits of the device error word. */
+#define SE_DEVERR_PAGE_RANGE   0x1u  /* a block-table entry outside [0, num_pages) */
+#define SE_DEVERR_LENGTH       0x2u  /* a length or selected-page id outside its declared bound */
+#define SE_DEVERR_WAIT_TIMEOUT 0x4u  /* a bounded wait on an mbarrier gave up */
+
+/*
+ * Paged KV cache view. Physical page p of KV head h holds tokens in slots
+ * 0..15; token slot t of (p, h) starts at element
+ *     ((p * num_kv_heads + h) * 16 + t) * row_stride
+ * of `k` (resp. `v`). Quest page summaries live beside the pages, indexed by
+ * the same physical page id ("the summaries required by Quest" kept with the
+ * KV blocks, SparseEngine, Figure 3 caption):
+ *     summary[((p * num_kv_heads + h) * 2 + 0) * head_dim + c] = min over the page's valid keys of channel c
+ *     summary[((p * num_kv_heads + h) * 2 + 1) * head_dim + c] = max over the same keys
+ * A latent (MLA-style) cache sets v == k with head_dim_v < head_dim: the value
+ * is the first head_dim_v dims of the key row.
+ */
+typedef struct {
+  void* k;                 /* bf16 */
+  void* v;                 /* bf16; may equal k */
+  void* summary;           /* bf16 [num_pages][num_kv_heads][2][head_dim]; may be NULL for calls that do not use it */
+  int32_t num_pages;       /* physical pages in the pool */
+  int32_t num_kv_heads;
+  int32_t page_size;       /* must be 16 */
+  int32_t head_dim;        /* key/query width: 128, or 576 for a latent cache */
+  int32_t head_dim_v;      /* value width: 128, or 512 for a latent cache */
+  int32_t row_stride_k;    /* elements between consecutive token rows of k (>= head_dim, multiple of 8) */
+  int32_t row_stride_v;    /* elements between consecutive token rows of v (>= head_dim_v, multiple of 8) */
+} se_paged_kv_t;
+
+/* Human-readable name of a status code (host, static storage). */
+SE_API const char* se_status_string(int status);
+
+/* Details of the last failing call on this host thread: entry point and reason
+ * (host, thread-local storage, valid until the next failing call). */
+SE_API const char* se_last_error_detail(void);
+
+/*
+ * Reads the library's device error word (SE_DEVERR_* bits) for the current
+ * device into *out (host) after synchronising the device; clears it when
+ * `clear` is non-zero. Returns SE_OK or SE_ERR_CUDA.
+ */
+SE_API se_status_t se_read_device_error(uint32_t* out, int clear);
+
+/*
+ * se_quest_build_summaries -- Quest page summaries from the cached keys.
+ * SparseEngine, Figure 3 caption (prefix caching keeps the Quest summaries with
+ * the KV blocks) and Table 8 (16-token pages).
+ * For every request b, every logical page p < ceil(seq_lens[b] / 16) and every
+ * KV head h, writes into kv->summary at physical page block_table[b][p] the
+ * per-channel minimum and maximum of the keys of the page's valid tokens
+ * (positions < seq_lens[b]); slots past the length are never read.
+ *   block_table: int32 [batch][bt_stride]; seq_lens: int32 [batch];
+ *   max_seq_len: host upper bound of seq_lens (sizes the grid; a larger device
+ *   value sets SE_DEVERR_LENGTH and the request is clipped to it).
+ */
+SE_API se_status_t se_quest_build_summaries(const se_paged_kv_t* kv, const int32_t* block_table, int32_t bt_stride,
+                                     const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                                     void* stream);
+
+/*
+ * se_quest_update_summaries -- KV append fused with the Quest summary update.
+ * SparseEngine, Figure 3 caption (summaries kept with the KV blocks); Table 7
+ * (the history of the current position includes the current token).
+ * For every request b and KV head h, writes k_new[b][h] (and v_new[b][h]) into
+ * the token slot of position seq_lens_before[b] (logical page pos / 16, slot
+ * pos % 16, physical page from block_table), and updates that page's summary:
+ * set to k_new when the token opens the page (slot 0), otherwise the running
+ * min and max with k_new. Re-running the same append is idempotent. The caller
+ * advances its lengths afterwards. Requests must not share the written page.
+ *   k_new: bf16 [batch][num_kv_heads][head_dim];
+ *   v_new: bf16 [batch][num_kv_heads][head_dim_v], or NULL when kv->v == kv->k
+ *   (latent cache: the value is part of the key row).
+ */
+SE_API se_status_t se_quest_update_summaries(const se_paged_kv_t* kv, const void* k_new, const void* v_new,
+                                      const int32_t* block_table, int32_t bt_stride,
+                                      const int32_t* seq_lens_before, int32_t batch, void* stream);
+
+/*
+ * se_quest_score_pages -- Quest upper-bound score of every candidate page.
+ * SparseEngine, Figure 2 caption and Table 14 (Quest, query-dependent page
+ * retrieval); the bound is the published Quest criterion.
+ * For request b, KV head h and candidate page p in [0, n_b - 2] with
+ * n_b = ceil(seq_lens[b] / 16):
+ *     scores[(b * num_kv_heads + h) * score_stride + p]
+ *         = sum over the query heads a of h's group, sum over channels c, of
+ *           max(q[b][a][c] * min_{p,c}, q[b][a][c] * max_{p,c})
+ * (computed as sum_c max_{p,c} * P_c + min_{p,c} * N_c with P_c, N_c the sums of
+ * the group's positive and negative query parts; fp32). The last page is not
+ * scored: it is always kept.
+ *   q: bf16 [batch][num_q_heads][head_dim]; num_q_heads a multiple of num_kv_heads;
+ *   scores: fp32, score_stride >= ceil(max_seq_len / 16).
+ */
+SE_API se_status_t se_quest_score_pages(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                 const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                 int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
+                                 void* stream);
+
+/*
+ * se_quest_topk_pages -- per-(request, KV head) page selection.
+ * SparseEngine, Table 10 caption (selected budgets exclude separately kept
+ * tokens) and Table 10, Quest (Vortex) row (2,048 selected tokens = 128 pages).
+ * Among the candidates 0..n_b-2 picks the topk_pages highest scores (equal
+ * scores: lower page id first), appends the last page n_b - 1, and writes the
+ * page ids in ascending order to out_pages[(b * num_kv_heads + h) * sel_stride
+ * + i] and the count to out_counts[b * num_kv_heads + h]. With no more than
+ * topk_pages candidates every page is selected (count n_b). A request of
+ * length 0 selects nothing (count 0).
+ *   sel_stride >= topk_pages + 1.
+ */
+SE_API se_status_t se_quest_topk_pages(const float* scores, int32_t score_stride, const int32_t* seq_lens,
+                                int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t topk_pages,
+                                int32_t* out_pages, int32_t* out_counts, int32_t sel_stride, void* stream);
+
+/*
+ * se_quest_select_pages -- se_quest_score_pages followed by se_quest_topk_pages,
+ * with the scores kept in the caller's workspace (size from
+ * se_quest_select_workspace_size).
+ */
+SE_API size_t se_quest_select_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len);
+SE_API se_status_t se_quest_select_pages(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                  const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                  int32_t batch, int32_t max_seq_len, int32_t topk_pages, int32_t* out_pages,
+                                  int32_t* out_counts, int32_t sel_stride, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * se_sparse_paged_decode -- attention of one decode query per request over the
+ * selected pages only.
+ * SparseEngine, Figure 2 caption (attention execution over the method's view of
+ * the cache) and Table 7 (logit z, weight alpha; the history includes the
+ * current token).
+ * For request b and query head a (KV head h = a / (num_q_heads / num_kv_heads)):
+ *     z_j = sm_scale * q[b][a] . k_j over the tokens j < seq_lens[b] of the pages
+ *           sel_pages[(b * num_kv_heads + h) * sel_stride + i], i < sel_counts[..]
+ *     out[b][a]  = sum_j softmax(z)_j v_j                       (bf16, round to nearest even)
+ *     out_lse[b][a] = log sum_j exp(z_j)                        (fp32, natural log; optional)
+ * A request with no selected page writes out = 0 and lse = -inf. The pages of
+ * one (request, KV head) are split across CTAs and the partial results merged
+ * by log-sum-exp in `workspace` (size from se_sparse_decode_workspace_size).
+ *   q: bf16 [batch][num_q_heads][head_dim]; out: bf16 [batch][num_q_heads][head_dim_v];
+ *   out_lse: fp32 [batch][num_q_heads] or NULL.
+ * Shapes: head_dim == head_dim_v == 128 with 1..16 query heads per KV head, or a
+ * latent cache (head_dim 576, head_dim_v 512, one KV head, 16..128 query heads
+ * in multiples of 16).
+ */
+SE_API size_t se_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim_v, int32_t sel_stride);
+SE_API se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                   const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                   int32_t batch, const int32_t* sel_pages, const int32_t* sel_counts,
+                                   int32_t sel_stride, float sm_scale, void* out, float* out_lse,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_ENGINE_H */

@@ -198,13 +198,16 @@ class QuestRequest:
         for h in range(self.num_kv_heads):
             qg = q[h * G:(h + 1) * G]
             m, M = self.summaries[h]
-            scores = group_page_scores(qg, m[:n - 1], M[:n - 1])
+            scores = group_page_scores(qg, m[:max(n - 1, 0)], M[:max(n - 1, 0)])
             pages = select_pages(scores, n, topk_pages)
             heads.append(HeadResult(scores, pages, kth_score(scores, n, topk_pages)))
             use = pages if pages_override is None else list(pages_override[h])
-            K = np.vstack([self.page_rows(h, p, value=False) for p in use])
-            V = np.vstack([self.page_rows(h, p, value=True) for p in use])
-            o, lse = softmax_attention(qg, K, V, sm_scale)
+            if not use:  # no token to attend to: the empty sum (zero output, lse = -inf)
+                o, lse = np.zeros((G, self.head_dim_v)), np.full(G, -np.inf)
+            else:
+                K = np.vstack([self.page_rows(h, p, value=False) for p in use])
+                V = np.vstack([self.page_rows(h, p, value=True) for p in use])
+                o, lse = softmax_attention(qg, K, V, sm_scale)
             outs.append(o)
             lses.append(lse)
         return RequestResult(heads, np.vstack(outs), np.concatenate(lses))

@@ -1,0 +1,212 @@
+"""Python binding of libsparse_engine.so, the sm_103a sparse decode attention library.
+
+The functions below carry the C ABI's names (include/sparse_engine.h) and do
+argument marshalling only: they check dtypes, devices and contiguity of the
+torch tensors that own the device memory, pass raw pointers and the current
+CUDA stream to the library, and raise ``SparseEngineError`` on any non-OK
+status. Every step of the computation runs in the library's CUDA kernels;
+there is no CPU path. If the library has not been built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "SparseEngineError", "SEPagedKV", "paged_kv", "load_library", "se_read_device_error",
+    "se_quest_build_summaries", "se_quest_update_summaries", "se_quest_score_pages",
+    "se_quest_topk_pages", "se_quest_select_workspace_size", "se_quest_select_pages",
+    "se_sparse_decode_workspace_size", "se_sparse_paged_decode", "exported_symbols",
+]
+
+SE_OK = 0
+DEVERR_PAGE_RANGE = 0x1
+DEVERR_LENGTH = 0x2
+DEVERR_WAIT_TIMEOUT = 0x4
+
+
+class SparseEngineError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{detail} [status {status}]")
+        self.status = status
+
+
+class SEPagedKV(ctypes.Structure):
+    """Mirror of se_paged_kv_t."""
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("summary", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("head_dim_v", ctypes.c_int32), ("row_stride_k", ctypes.c_int32),
+                ("row_stride_v", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_F = ctypes.c_float
+_Z = ctypes.c_size_t
+_KV = ctypes.POINTER(SEPagedKV)
+
+_SIGNATURES = {
+    "se_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "se_last_error_detail": (ctypes.c_char_p, []),
+    "se_read_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+    "se_quest_build_summaries": (ctypes.c_int, [_KV, _P, _I, _P, _I, _I, _P]),
+    "se_quest_update_summaries": (ctypes.c_int, [_KV, _P, _P, _P, _I, _P, _I, _P]),
+    "se_quest_score_pages": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _P, _I, _P]),
+    "se_quest_topk_pages": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I, _P]),
+    "se_quest_select_workspace_size": (_Z, [_I, _I, _I]),
+    "se_quest_select_pages": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _I, _P, _P, _I, _P, _Z, _P]),
+    "se_sparse_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "se_sparse_paged_decode": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _P, _P, _I, _F, _P, _P, _P, _Z, _P]),
+}
+
+_lib = None
+
+
+def exported_symbols():
+    return list(_SIGNATURES)
+
+
+def load_library():
+    """Load the in-tree library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = _build.lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with sparse_decode_attention_quest_gb300.build.build() "
+                               "(there is no fallback path)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != SE_OK:
+        lib = load_library()
+        raise SparseEngineError(status, lib.se_last_error_detail().decode())
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def paged_kv(k_cache: torch.Tensor, v_cache: Optional[torch.Tensor], summary: Optional[torch.Tensor],
+             head_dim_v: Optional[int] = None) -> SEPagedKV:
+    """se_paged_kv_t for bf16 caches [P][Hkv][16][row]. ``v_cache`` None = latent cache (v aliases k)."""
+    _ptr(k_cache, torch.bfloat16, "k_cache")
+    P, H, ps, row_k = k_cache.shape
+    if v_cache is None:
+        if head_dim_v is None:
+            raise ValueError("a latent cache needs head_dim_v")
+        v_ptr, row_v, dv = k_cache.data_ptr(), row_k, head_dim_v
+    else:
+        _ptr(v_cache, torch.bfloat16, "v_cache")
+        v_ptr, row_v, dv = v_cache.data_ptr(), v_cache.shape[-1], v_cache.shape[-1]
+    if summary is not None:
+        _ptr(summary, torch.bfloat16, "summary")
+    return SEPagedKV(k_cache.data_ptr(), v_ptr, None if summary is None else summary.data_ptr(),
+                     P, H, ps, row_k, dv, row_k, row_v)
+
+
+def se_read_device_error(clear: bool = True) -> int:
+    lib = load_library()
+    v = ctypes.c_uint32(0)
+    _check(lib.se_read_device_error(ctypes.byref(v), int(clear)))
+    return v.value
+
+
+def se_quest_build_summaries(kv: SEPagedKV, block_table, seq_lens, max_seq_len: int, stream=None):
+    lib = load_library()
+    _check(lib.se_quest_build_summaries(ctypes.byref(kv), _ptr(block_table, torch.int32, "block_table"),
+                                        block_table.shape[1], _ptr(seq_lens, torch.int32, "seq_lens"),
+                                        seq_lens.shape[0], int(max_seq_len), _stream(stream)))
+
+
+def se_quest_update_summaries(kv: SEPagedKV, k_new, v_new, block_table, seq_lens_before, stream=None):
+    lib = load_library()
+    _check(lib.se_quest_update_summaries(ctypes.byref(kv), _ptr(k_new, torch.bfloat16, "k_new"),
+                                         _ptr(v_new, torch.bfloat16, "v_new"),
+                                         _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                         _ptr(seq_lens_before, torch.int32, "seq_lens_before"),
+                                         seq_lens_before.shape[0], _stream(stream)))
+
+
+def se_quest_score_pages(kv: SEPagedKV, q, block_table, seq_lens, max_seq_len: int, scores, stream=None):
+    lib = load_library()
+    _check(lib.se_quest_score_pages(ctypes.byref(kv), _ptr(q, torch.bfloat16, "q"), q.shape[1],
+                                    _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                    _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0], int(max_seq_len),
+                                    _ptr(scores, torch.float32, "scores"), scores.shape[-1], _stream(stream)))
+
+
+def se_quest_topk_pages(scores, seq_lens, num_kv_heads: int, max_seq_len: int, topk_pages: int, out_pages,
+                        out_counts, stream=None):
+    lib = load_library()
+    _check(lib.se_quest_topk_pages(_ptr(scores, torch.float32, "scores"), scores.shape[-1],
+                                   _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0], int(num_kv_heads),
+                                   int(max_seq_len), int(topk_pages), _ptr(out_pages, torch.int32, "out_pages"),
+                                   _ptr(out_counts, torch.int32, "out_counts"), out_pages.shape[-1],
+                                   _stream(stream)))
+
+
+def se_quest_select_workspace_size(batch: int, num_kv_heads: int, max_seq_len: int) -> int:
+    return int(load_library().se_quest_select_workspace_size(batch, num_kv_heads, max_seq_len))
+
+
+def se_quest_select_pages(kv: SEPagedKV, q, block_table, seq_lens, max_seq_len: int, topk_pages: int, out_pages,
+                          out_counts, workspace, stream=None):
+    lib = load_library()
+    _check(lib.se_quest_select_pages(ctypes.byref(kv), _ptr(q, torch.bfloat16, "q"), q.shape[1],
+                                     _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                     _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0], int(max_seq_len),
+                                     int(topk_pages), _ptr(out_pages, torch.int32, "out_pages"),
+                                     _ptr(out_counts, torch.int32, "out_counts"), out_pages.shape[-1],
+                                     _ptr(workspace, torch.uint8, "workspace"),
+                                     0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
+def se_sparse_decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim_v: int,
+                                    sel_stride: int) -> int:
+    return int(load_library().se_sparse_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim_v,
+                                                              sel_stride))
+
+
+def se_sparse_paged_decode(kv: SEPagedKV, q, block_table, seq_lens, sel_pages, sel_counts, sm_scale: float, out,
+                           out_lse=None, workspace=None, stream=None):
+    lib = load_library()
+    _check(lib.se_sparse_paged_decode(ctypes.byref(kv), _ptr(q, torch.bfloat16, "q"), q.shape[1],
+                                      _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                      _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0],
+                                      _ptr(sel_pages, torch.int32, "sel_pages"),
+                                      _ptr(sel_counts, torch.int32, "sel_counts"), sel_pages.shape[-1],
+                                      float(sm_scale), _ptr(out, torch.bfloat16, "out"),
+                                      _ptr(out_lse, torch.float32, "out_lse"),
+                                      _ptr(workspace, torch.uint8, "workspace"),
+                                      0 if workspace is None else workspace.numel(), _stream(stream)))

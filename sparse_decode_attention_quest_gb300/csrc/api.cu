@@ -1,0 +1,338 @@
+// Host entry points of the C ABI declared in include/sparse_engine.h:
+// argument validation (before any launch), per-device cached properties,
+// tensor-map encoding for the TMA copies, and dispatch to the kernels.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "se_internal.h"
+
+// The library's device error word (SE_DEVERR_* bits), one per device context.
+__device__ unsigned se_device_error_word;
+
+namespace {
+
+using se::KvView;
+
+thread_local char g_detail[256] = "";
+
+se_status_t fail(se_status_t st, const char* fn, const char* what) {
+  std::snprintf(g_detail, sizeof(g_detail), "%s: %s", fn, what);
+  return st;
+}
+
+se_status_t cuda_fail(const char* fn, cudaError_t e) {
+  std::snprintf(g_detail, sizeof(g_detail), "%s: %s (%s)", fn, cudaGetErrorName(e), cudaGetErrorString(e));
+  return SE_ERR_CUDA;
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  unsigned* err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+// Properties of the current device, queried once per device.
+cudaError_t current_device(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), se_device_error_word);
+    if (e != cudaSuccess) return e;
+    d.ready = true;
+  }
+  *out = &d;
+  return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view of a paged cache as rows of `row_stride` bf16 (one row per token slot),
+// boxes of 64 columns x 16 rows with 128-byte swizzle.
+bool encode_page_map(CUtensorMap* map, const void* base, long long rows, int width, int row_stride) {
+  auto fn = encode_tiled();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_stride * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int pages_of(long long tokens) { return (int)((tokens + se::kPageSize - 1) / se::kPageSize); }
+
+// Common checks of a paged cache view.
+se_status_t check_kv(const char* fn, const se_paged_kv_t* kv, bool need_summary) {
+  if (!kv) return fail(SE_ERR_INVALID_ARG, fn, "kv is NULL");
+  if (!kv->k || !kv->v) return fail(SE_ERR_INVALID_ARG, fn, "kv->k / kv->v is NULL");
+  if (need_summary && !kv->summary) return fail(SE_ERR_INVALID_ARG, fn, "kv->summary is NULL");
+  if (!aligned16(kv->k) || !aligned16(kv->v) || (kv->summary && !aligned16(kv->summary)))
+    return fail(SE_ERR_INVALID_ARG, fn, "cache pointers must be 16-byte aligned");
+  if (kv->page_size != se::kPageSize) return fail(SE_ERR_INVALID_ARG, fn, "page_size must be 16");
+  if (kv->num_pages < 0 || kv->num_kv_heads < 1) return fail(SE_ERR_INVALID_ARG, fn, "bad num_pages/num_kv_heads");
+  if (kv->head_dim < 8 || kv->head_dim_v < 8 || (kv->head_dim % 8) || (kv->head_dim_v % 8))
+    return fail(SE_ERR_INVALID_ARG, fn, "head dims must be positive multiples of 8");
+  if (kv->row_stride_k < kv->head_dim || kv->row_stride_v < kv->head_dim_v || (kv->row_stride_k % 8) ||
+      (kv->row_stride_v % 8))
+    return fail(SE_ERR_INVALID_ARG, fn, "row strides must cover the head dims and be multiples of 8");
+  if ((long long)kv->num_pages * kv->num_kv_heads * se::kPageSize >= (1ll << 31))
+    return fail(SE_ERR_UNSUPPORTED, fn, "cache holds 2^31 or more token rows");
+  if (kv->head_dim != 128 && kv->head_dim != 576) return fail(SE_ERR_UNSUPPORTED, fn, "head_dim must be 128 or 576");
+  return SE_OK;
+}
+
+KvView view_of(const se_paged_kv_t* kv) {
+  KvView v;
+  v.k = static_cast<const uint16_t*>(kv->k);
+  v.v = static_cast<const uint16_t*>(kv->v);
+  v.summary = static_cast<uint16_t*>(kv->summary);
+  v.num_pages = kv->num_pages;
+  v.num_kv_heads = kv->num_kv_heads;
+  v.head_dim = kv->head_dim;
+  v.head_dim_v = kv->head_dim_v;
+  v.row_stride_k = kv->row_stride_k;
+  v.row_stride_v = kv->row_stride_v;
+  return v;
+}
+
+size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
+
+int score_stride_for(int max_seq_len) { return pages_of(max_seq_len) > 0 ? pages_of(max_seq_len) : 1; }
+
+se_status_t check_batch_common(const char* fn, const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* seq_lens, int32_t batch, int32_t max_seq_len) {
+  if (batch < 0) return fail(SE_ERR_INVALID_ARG, fn, "batch < 0");
+  if (max_seq_len < 0) return fail(SE_ERR_INVALID_ARG, fn, "max_seq_len < 0");
+  if (batch > 0 && (!block_table || !seq_lens)) return fail(SE_ERR_INVALID_ARG, fn, "block_table/seq_lens NULL");
+  if (bt_stride < pages_of(max_seq_len) || bt_stride < 1)
+    return fail(SE_ERR_INVALID_ARG, fn, "bt_stride < ceil(max_seq_len / 16)");
+  return SE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* se_status_string(int status) {
+  switch (status) {
+    case SE_OK: return "SE_OK";
+    case SE_ERR_INVALID_ARG: return "SE_ERR_INVALID_ARG";
+    case SE_ERR_UNSUPPORTED: return "SE_ERR_UNSUPPORTED";
+    case SE_ERR_WORKSPACE: return "SE_ERR_WORKSPACE";
+    case SE_ERR_CUDA: return "SE_ERR_CUDA";
+    case SE_ERR_DEVICE: return "SE_ERR_DEVICE";
+    default: return "SE_ERR_UNKNOWN";
+  }
+}
+
+const char* se_last_error_detail(void) { return g_detail; }
+
+se_status_t se_read_device_error(uint32_t* out, int clear) {
+  if (!out) return fail(SE_ERR_INVALID_ARG, "se_read_device_error", "out is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail("se_read_device_error", e);
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, se_device_error_word, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail("se_read_device_error", e);
+  if (clear) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(se_device_error_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail("se_read_device_error", e);
+  }
+  *out = v;
+  return SE_OK;
+}
+
+se_status_t se_quest_build_summaries(const se_paged_kv_t* kv, const int32_t* block_table, int32_t bt_stride,
+                                     const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                                     void* stream) {
+  static const char* fn = "se_quest_build_summaries";
+  se_status_t st = check_kv(fn, kv, true);
+  if (st != SE_OK) return st;
+  st = check_batch_common(fn, block_table, bt_stride, seq_lens, batch, max_seq_len);
+  if (st != SE_OK) return st;
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  e = se::launch_build_summaries(view_of(kv), block_table, bt_stride, seq_lens, batch, max_seq_len, d->err,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+se_status_t se_quest_update_summaries(const se_paged_kv_t* kv, const void* k_new, const void* v_new,
+                                      const int32_t* block_table, int32_t bt_stride,
+                                      const int32_t* seq_lens_before, int32_t batch, void* stream) {
+  static const char* fn = "se_quest_update_summaries";
+  se_status_t st = check_kv(fn, kv, true);
+  if (st != SE_OK) return st;
+  if (batch < 0) return fail(SE_ERR_INVALID_ARG, fn, "batch < 0");
+  if (batch > 0 && (!k_new || !block_table || !seq_lens_before))
+    return fail(SE_ERR_INVALID_ARG, fn, "k_new/block_table/seq_lens_before NULL");
+  if (bt_stride < 1) return fail(SE_ERR_INVALID_ARG, fn, "bt_stride < 1");
+  const bool latent = kv->v == kv->k;
+  if (!latent && batch > 0 && !v_new) return fail(SE_ERR_INVALID_ARG, fn, "v_new NULL for a separate value cache");
+  if (latent && v_new) return fail(SE_ERR_INVALID_ARG, fn, "v_new must be NULL when kv->v == kv->k");
+  if (!aligned16(k_new) || !aligned16(v_new)) return fail(SE_ERR_INVALID_ARG, fn, "k_new/v_new not 16-byte aligned");
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  e = se::launch_append_update(view_of(kv), static_cast<uint16_t*>(kv->k), static_cast<uint16_t*>(kv->v),
+                               static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new),
+                               block_table, bt_stride, seq_lens_before, batch, d->err,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+se_status_t se_quest_score_pages(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                 const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                 int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
+                                 void* stream) {
+  static const char* fn = "se_quest_score_pages";
+  se_status_t st = check_kv(fn, kv, true);
+  if (st != SE_OK) return st;
+  st = check_batch_common(fn, block_table, bt_stride, seq_lens, batch, max_seq_len);
+  if (st != SE_OK) return st;
+  if (num_q_heads < 1 || num_q_heads % kv->num_kv_heads)
+    return fail(SE_ERR_INVALID_ARG, fn, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (batch > 0 && (!q || !scores)) return fail(SE_ERR_INVALID_ARG, fn, "q/scores NULL");
+  if (!aligned16(q) || !aligned16(scores)) return fail(SE_ERR_INVALID_ARG, fn, "q/scores not 16-byte aligned");
+  if (score_stride < score_stride_for(max_seq_len)) return fail(SE_ERR_INVALID_ARG, fn, "score_stride too small");
+  if (kv->num_kv_heads * kv->head_dim > 2048)
+    return fail(SE_ERR_UNSUPPORTED, fn, "num_kv_heads * head_dim > 2048 (summary block over 8 KB)");
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  e = se::launch_score_pages(view_of(kv), static_cast<const uint16_t*>(q), num_q_heads, block_table, bt_stride,
+                             seq_lens, batch, max_seq_len, scores, score_stride, d->sm_count, d->err,
+                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+se_status_t se_quest_topk_pages(const float* scores, int32_t score_stride, const int32_t* seq_lens,
+                                int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t topk_pages,
+                                int32_t* out_pages, int32_t* out_counts, int32_t sel_stride, void* stream) {
+  static const char* fn = "se_quest_topk_pages";
+  if (batch < 0 || num_kv_heads < 1 || max_seq_len < 0) return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
+  if (topk_pages < 1) return fail(SE_ERR_INVALID_ARG, fn, "topk_pages < 1");
+  if (sel_stride < topk_pages + 1) return fail(SE_ERR_INVALID_ARG, fn, "sel_stride < topk_pages + 1");
+  if (score_stride < score_stride_for(max_seq_len)) return fail(SE_ERR_INVALID_ARG, fn, "score_stride too small");
+  if (batch > 0 && (!scores || !seq_lens || !out_pages || !out_counts))
+    return fail(SE_ERR_INVALID_ARG, fn, "NULL pointer");
+  if (!aligned16(scores) || !aligned16(out_pages) || !aligned16(out_counts))
+    return fail(SE_ERR_INVALID_ARG, fn, "pointers must be 16-byte aligned");
+  if (se::topk_smem_bytes(max_seq_len) > 200 * 1024)
+    return fail(SE_ERR_UNSUPPORTED, fn, "more than 51200 candidate pages per request");
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  e = se::launch_topk_pages(scores, score_stride, seq_lens, batch, num_kv_heads, max_seq_len, topk_pages,
+                            out_pages, out_counts, sel_stride, d->err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+size_t se_quest_select_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len) {
+  if (batch < 0 || num_kv_heads < 0 || max_seq_len < 0) return 0;
+  return round16((size_t)batch * num_kv_heads * score_stride_for(max_seq_len) * sizeof(float));
+}
+
+se_status_t se_quest_select_pages(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                  const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                  int32_t batch, int32_t max_seq_len, int32_t topk_pages, int32_t* out_pages,
+                                  int32_t* out_counts, int32_t sel_stride, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  static const char* fn = "se_quest_select_pages";
+  if (!kv) return fail(SE_ERR_INVALID_ARG, fn, "kv is NULL");
+  if (batch < 0 || max_seq_len < 0) return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
+  const size_t need = se_quest_select_workspace_size(batch, kv->num_kv_heads, max_seq_len);
+  if (workspace_bytes < need) return fail(SE_ERR_WORKSPACE, fn, "workspace too small");
+  if (need > 0 && !workspace) return fail(SE_ERR_INVALID_ARG, fn, "workspace NULL");
+  if (topk_pages < 1 || sel_stride < topk_pages + 1)
+    return fail(SE_ERR_INVALID_ARG, fn, "topk_pages < 1 or sel_stride < topk_pages + 1");
+  float* scores = static_cast<float*>(workspace);
+  const int stride = score_stride_for(max_seq_len);
+  se_status_t st = se_quest_score_pages(kv, q, num_q_heads, block_table, bt_stride, seq_lens, batch, max_seq_len,
+                                        scores, stride, stream);
+  if (st != SE_OK) return st;
+  return se_quest_topk_pages(scores, stride, seq_lens, batch, kv->num_kv_heads, max_seq_len, topk_pages, out_pages,
+                             out_counts, sel_stride, stream);
+}
+
+size_t se_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim_v, int32_t sel_stride) {
+  if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim_v < 1 || sel_stride < 1) return 0;
+  // Upper bound over devices: at least 8 selected pages per split.
+  const size_t max_split = (size_t)(sel_stride + 7) / 8;
+  return round16((size_t)batch * num_q_heads * max_split * ((size_t)head_dim_v + 1) * sizeof(float));
+}
+
+se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                   const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                   int32_t batch, const int32_t* sel_pages, const int32_t* sel_counts,
+                                   int32_t sel_stride, float sm_scale, void* out, float* out_lse,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  static const char* fn = "se_sparse_paged_decode";
+  se_status_t st = check_kv(fn, kv, false);
+  if (st != SE_OK) return st;
+  if (batch < 0) return fail(SE_ERR_INVALID_ARG, fn, "batch < 0");
+  if (num_q_heads < 1 || num_q_heads % kv->num_kv_heads)
+    return fail(SE_ERR_INVALID_ARG, fn, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (sel_stride < 1 || bt_stride < 1) return fail(SE_ERR_INVALID_ARG, fn, "sel_stride/bt_stride < 1");
+  if (batch > 0 && (!q || !block_table || !seq_lens || !sel_pages || !sel_counts || !out))
+    return fail(SE_ERR_INVALID_ARG, fn, "NULL pointer");
+  if (!aligned16(q) || !aligned16(out) || !aligned16(out_lse) || !aligned16(workspace) || !aligned16(sel_pages))
+    return fail(SE_ERR_INVALID_ARG, fn, "pointers must be 16-byte aligned");
+  if (!std::isfinite(sm_scale)) return fail(SE_ERR_INVALID_ARG, fn, "sm_scale not finite");
+  const int group = num_q_heads / kv->num_kv_heads;
+  const bool gqa = kv->head_dim == 128 && kv->head_dim_v == 128 && group <= 16;
+  if (!gqa) return fail(SE_ERR_UNSUPPORTED, fn, "only head_dim = head_dim_v = 128 with <= 16 query heads per KV head");
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  const se::DecodePlan plan = se::plan_gqa_decode(batch, kv->num_kv_heads, sel_stride, d->sm_count);
+  const size_t need = se::gqa_decode_workspace_bytes(batch, num_q_heads, kv->head_dim_v, plan);
+  if (workspace_bytes < need) return fail(SE_ERR_WORKSPACE, fn, "workspace too small");
+  if (need > 0 && !workspace) return fail(SE_ERR_INVALID_ARG, fn, "workspace NULL");
+  if (batch == 0) return SE_OK;
+  CUtensorMap kmap, vmap;
+  const long long rows = (long long)kv->num_pages * kv->num_kv_heads * se::kPageSize;
+  if (!encode_page_map(&kmap, kv->k, rows > 0 ? rows : 1, kv->head_dim, kv->row_stride_k) ||
+      !encode_page_map(&vmap, kv->v, rows > 0 ? rows : 1, kv->head_dim_v, kv->row_stride_v))
+    return fail(SE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
+  e = se::launch_gqa_decode(kmap, vmap, view_of(kv), static_cast<const uint16_t*>(q), num_q_heads, block_table,
+                            bt_stride, seq_lens, batch, sel_pages, sel_counts, sel_stride, sm_scale,
+                            static_cast<uint16_t*>(out), out_lse, workspace, plan, d->err,
+                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+}  // extern "C"

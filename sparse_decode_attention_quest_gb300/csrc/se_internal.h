@@ -1,0 +1,64 @@
+// Internal declarations shared by the host entry points (api.cu) and the
+// kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sparse_engine.h"
+
+namespace se {
+
+constexpr int kPageSize = 16;
+// Bounded waits: an mbarrier wait gives up after this much wall time or polls.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kWaitLimitIters = 1u << 28;
+
+// Device-visible copy of the cache layout (plain values, passed by value).
+struct KvView {
+  const uint16_t* k;
+  const uint16_t* v;
+  uint16_t* summary;
+  int32_t num_pages;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t head_dim_v;
+  int32_t row_stride_k;
+  int32_t row_stride_v;
+};
+
+// ---- quest_summary.cu
+cudaError_t launch_build_summaries(const KvView& kv, const int32_t* block_table, int32_t bt_stride,
+                                   const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, unsigned* err,
+                                   cudaStream_t stream);
+cudaError_t launch_append_update(const KvView& kv, uint16_t* k_mut, uint16_t* v_mut, const uint16_t* k_new,
+                                 const uint16_t* v_new, const int32_t* block_table, int32_t bt_stride,
+                                 const int32_t* seq_lens_before, int32_t batch, unsigned* err,
+                                 cudaStream_t stream);
+
+// ---- quest_select.cu
+cudaError_t launch_score_pages(const KvView& kv, const uint16_t* q, int32_t num_q_heads,
+                               const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                               int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
+                               int sm_count, unsigned* err, cudaStream_t stream);
+cudaError_t launch_topk_pages(const float* scores, int32_t score_stride, const int32_t* seq_lens, int32_t batch,
+                              int32_t num_kv_heads, int32_t max_seq_len, int32_t topk, int32_t* out_pages,
+                              int32_t* out_counts, int32_t sel_stride, unsigned* err, cudaStream_t stream);
+size_t topk_smem_bytes(int32_t max_seq_len);
+
+// ---- sparse_decode.cu
+struct DecodePlan {
+  int32_t nsplit;           // CTAs per (request, KV head)
+  int32_t pages_per_split;  // selected pages per CTA
+};
+DecodePlan plan_gqa_decode(int32_t batch, int32_t num_kv_heads, int32_t sel_stride, int sm_count);
+size_t gqa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim_v, const DecodePlan& plan);
+cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const KvView& kv,
+                              const uint16_t* q, int32_t num_q_heads, const int32_t* block_table,
+                              int32_t bt_stride, const int32_t* seq_lens, int32_t batch,
+                              const int32_t* sel_pages, const int32_t* sel_counts, int32_t sel_stride,
+                              float sm_scale, uint16_t* out, float* out_lse, void* workspace,
+                              const DecodePlan& plan, unsigned* err, cudaStream_t stream);
+
+}  // namespace se

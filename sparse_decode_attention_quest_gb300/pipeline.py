@@ -1,0 +1,88 @@
+"""One Quest decode step over a paged cache: buffers plus the C-ABI calls in order.
+
+Host orchestration only (allocation and call order); the work runs in the
+library's kernels:
+    se_quest_update_summaries   (optional KV append fused with the summary update)
+    se_quest_score_pages        (upper-bound score of every candidate page)
+    se_quest_topk_pages         (top-k pages + the last page, ascending)
+    se_sparse_paged_decode      (split-K flash-decode over the selected pages + merge)
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Sequence
+
+import torch
+
+from . import (paged_kv, se_quest_build_summaries, se_quest_score_pages, se_quest_topk_pages,
+               se_quest_update_summaries, se_sparse_decode_workspace_size, se_sparse_paged_decode)
+
+PAGE = 16
+
+
+def new_summary(k_cache: torch.Tensor) -> torch.Tensor:
+    """Summary storage beside a cache [P][Hkv][16][D]: bf16 [P][Hkv][2][D]."""
+    P, H, _, D = k_cache.shape
+    return torch.empty(P, H, 2, D, dtype=torch.bfloat16, device=k_cache.device)
+
+
+class QuestDecodeStep:
+    def __init__(self, k_cache: torch.Tensor, v_cache: Optional[torch.Tensor], summary: torch.Tensor,
+                 block_table: torch.Tensor, num_q_heads: int, topk_pages: int, max_seq_len: int,
+                 head_dim_v: Optional[int] = None, sm_scale: Optional[float] = None, sel_stride: Optional[int] = None):
+        self.k_cache, self.v_cache, self.summary = k_cache, v_cache, summary
+        self.block_table = block_table
+        self.kv = paged_kv(k_cache, v_cache, summary, head_dim_v)
+        dev = k_cache.device
+        self.B = block_table.shape[0]
+        self.H = k_cache.shape[1]
+        self.Hq = num_q_heads
+        self.D = k_cache.shape[-1]
+        self.Dv = self.kv.head_dim_v
+        self.topk = topk_pages
+        self.max_seq_len = max_seq_len
+        self.sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(self.D)
+        stride = max(1, (max_seq_len + PAGE - 1) // PAGE)
+        self.scores = torch.empty(self.B, self.H, stride, dtype=torch.float32, device=dev)
+        self.sel_stride = sel_stride if sel_stride is not None else topk_pages + 1
+        self.sel = torch.empty(self.B, self.H, self.sel_stride, dtype=torch.int32, device=dev)
+        self.counts = torch.empty(self.B, self.H, dtype=torch.int32, device=dev)
+        self.out = torch.empty(self.B, self.Hq, self.Dv, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=dev)
+        ws = se_sparse_decode_workspace_size(self.B, self.Hq, self.H, self.Dv, self.sel_stride)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+
+    def build_summaries(self, seq_lens: torch.Tensor, stream=None):
+        se_quest_build_summaries(self.kv, self.block_table, seq_lens, self.max_seq_len, stream)
+
+    def append(self, k_new, v_new, seq_lens_before, stream=None):
+        se_quest_update_summaries(self.kv, k_new, v_new, self.block_table, seq_lens_before, stream)
+
+    def select(self, q, seq_lens, stream=None):
+        se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, stream)
+        se_quest_topk_pages(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sel, self.counts, stream)
+
+    def attend(self, q, seq_lens, sel=None, counts=None, stream=None):
+        se_sparse_paged_decode(self.kv, q, self.block_table, seq_lens, self.sel if sel is None else sel,
+                               self.counts if counts is None else counts, self.sm_scale, self.out, self.lse,
+                               self.workspace, stream)
+
+    def run(self, q, seq_lens, k_new=None, v_new=None, seq_lens_before=None, stream=None,
+            events: Optional[Sequence] = None):
+        """Full step. ``events`` (4 CUDA events, optional) are recorded on ``stream`` before
+        the append, before scoring, before top-k and before decode, for per-kernel timing."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        if events is not None:
+            events[0].record(s)
+        if k_new is not None:
+            self.append(k_new, v_new, seq_lens_before, s)
+        if events is not None:
+            events[1].record(s)
+        se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, s)
+        if events is not None:
+            events[2].record(s)
+        se_quest_topk_pages(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sel, self.counts, s)
+        if events is not None:
+            events[3].record(s)
+        self.attend(q, seq_lens, stream=s)
+        return self.out

@@ -58,6 +58,7 @@ class QuestDecodeWorkload:
     outlier_scale: float = 8.0
     latent: bool = False     # one cache row holds the key; the value is its first head_dim_v dims
     page_size: int = PAGE_SIZE
+    lengths: tuple = ()      # explicit per-request lengths (override the uniform draw)
 
     @property
     def group(self) -> int:
@@ -117,6 +118,9 @@ class QuestDecodeInputs:
 
 
 def _draw_lengths(wl, g):
+    if wl.lengths:
+        assert len(wl.lengths) == wl.batch
+        return list(wl.lengths)
     if wl.context_min == wl.context_max:
         return [wl.context_min] * wl.batch
     return torch.randint(wl.context_min, wl.context_max + 1, (wl.batch,), generator=g).tolist()

@@ -175,6 +175,15 @@ def check_single_token_attention(quest):
     np.testing.assert_allclose(res.lse, 0.7 * (q @ Kl[0, 0]), rtol=1e-14)
 
 
+def check_empty_request(quest):
+    """A request with no token selects nothing and attends to nothing (empty sum)."""
+    kc = np.zeros((2, 1, PS, 4))
+    res = quest.QuestRequest(kc, kc.copy(), np.array([0]), 0, 1, 4, 4, PS).decode(np.ones((2, 4)), 3, 1.0)
+    assert res.heads[0].pages == [] and res.heads[0].threshold is None
+    np.testing.assert_array_equal(res.out, np.zeros((2, 4)))
+    assert np.all(np.isneginf(res.lse))
+
+
 def check_permutation_invariance(quest):
     rng = _rng(10)
     L, H, D = 11, 2, 4
@@ -298,7 +307,7 @@ def check_compaction_exact(snapkv):
 QUEST_CHECKS = [check_summary_bruteforce, check_append_matches_rebuild, check_bound_dominates_logits,
                 check_bound_single_token_exact, check_bound_sign_cases,
                 check_group_score_bounds_group_logit, check_select_bruteforce,
-                check_select_all_equals_dense, check_single_token_attention,
+                check_select_all_equals_dense, check_single_token_attention, check_empty_request,
                 check_permutation_invariance, check_latent_value_is_key_prefix,
                 check_selection_uses_the_bound]
 SNAPKV_CHECKS = [check_window_probabilities, check_candidate_scores, check_max_pool,

@@ -1,0 +1,282 @@
+"""Quest decode path on the GPU against the fp64 oracle (through the C ABI).
+
+Cases: the tiny 4K workload in full; oracle-sized cases with the 32K Qwen3-4B
+and ragged Qwen3-30B-A3B recipes that span several score chunks, top-k
+passes and decode splits, with ragged tails; every group size the GQA kernel
+takes; edge lengths (0, 1, 15, 16, 17 tokens, budget above the page count);
+invariants (summaries bit-exact, bound >= true logit, select-all = dense,
+block-table permutation, split count, append idempotence); device-side
+range checks; and the full-size workloads checked on sampled requests.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.quest as oq
+import sparse_decode_attention_quest_gb300 as se
+from sparse_decode_attention_quest_gb300.pipeline import QuestDecodeStep, new_summary
+from synth import (QWEN3_30B_A3B_QUEST_128K, QWEN3_4B_QUEST_32K, TINY_QUEST_4K, make_quest_decode_inputs)
+from tests.parity import OUT_ATOL, compare_decode, oracle_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _prepare(wl, dev, device_gen=False, sel_stride=None, poison=True):
+    x = make_quest_decode_inputs(wl, device=dev if device_gen else "cpu", poison_tail=poison)
+    k = x.k_cache.to(dev)
+    v = None if x.v_cache is None else x.v_cache.to(dev)
+    step = QuestDecodeStep(k, v, new_summary(k), x.block_table.to(dev), wl.num_q_heads, wl.topk_pages,
+                           max(max(x.seq_lens_after), 1), head_dim_v=wl.head_dim_v, sel_stride=sel_stride)
+    before = torch.tensor(x.seq_lens, dtype=torch.int32, device=dev)
+    after = torch.tensor(x.seq_lens_after, dtype=torch.int32, device=dev)
+    step.build_summaries(before)
+    return x, step, before, after
+
+
+def _run(x, step, before, after, dev):
+    q = x.q.to(dev)
+    if x.workload.append:
+        step.run(q, after, x.k_new.to(dev), x.v_new.to(dev), before)
+    else:
+        step.run(q, after)
+    torch.cuda.synchronize()
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors(se_lib, cuda_device):
+    se.se_read_device_error(clear=True)
+    yield
+    assert se.se_read_device_error(clear=True) == 0
+
+
+def _scale(wl):
+    return 1.0 / math.sqrt(wl.head_dim)
+
+
+def test_tiny_workload_full(cuda_device):
+    wl = TINY_QUEST_4K
+    x, step, b, a = _prepare(wl, cuda_device)
+    _run(x, step, b, a, cuda_device)
+    compare_decode(x, step, [0], _scale(wl), "tiny")
+
+
+def test_ragged_append_oracle_sized(cuda_device):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=5, context_min=900, context_max=4100, topk_pages=24)
+    x, step, b, a = _prepare(wl, cuda_device)
+    _run(x, step, b, a, cuda_device)
+    compare_decode(x, step, range(wl.batch), _scale(wl), "ragged")
+
+
+def test_qwen3_4b_recipe_oracle_sized(cuda_device):
+    wl = QWEN3_4B_QUEST_32K.scaled(batch=2, context_min=4096, context_max=4096, topk_pages=32)
+    x, step, b, a = _prepare(wl, cuda_device)
+    _run(x, step, b, a, cuda_device)
+    compare_decode(x, step, range(wl.batch), _scale(wl), "qwen3-4b")
+
+
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 2), (16, 2), (32, 2), (12, 4)])
+def test_group_sizes(cuda_device, hq, hkv):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=3, num_q_heads=hq, num_kv_heads=hkv, context_min=500,
+                                         context_max=1300, topk_pages=12, seed=11)
+    x, step, b, a = _prepare(wl, cuda_device)
+    _run(x, step, b, a, cuda_device)
+    compare_decode(x, step, range(wl.batch), _scale(wl), f"G={hq // hkv}")
+
+
+@pytest.mark.parametrize("append", [False, True])
+@pytest.mark.parametrize("sel_stride", [None, 64])  # one decode split per request, or several + merge
+def test_edge_lengths(cuda_device, append, sel_stride):
+    lens = (0, 1, 15, 16, 17, 31, 33, 160, 161, 700) if not append else (1, 15, 16, 17, 31, 33, 160, 161, 700, 0)
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=len(lens), lengths=lens, topk_pages=6, append=append, seed=5)
+    x, step, b, a = _prepare(wl, cuda_device, sel_stride=sel_stride)
+    _run(x, step, b, a, cuda_device)
+    compare_decode(x, step, range(wl.batch), _scale(wl), "edges")
+    counts = step.counts.cpu()
+    for i, L in enumerate(x.seq_lens_after):
+        n = math.ceil(L / 16)
+        assert int(counts[i, 0]) == min(n, wl.topk_pages + 1)
+    if not append:
+        out = step.out.float().cpu()
+        assert torch.equal(out[0], torch.zeros_like(out[0]))            # empty request
+        assert bool(torch.isneginf(step.lse[0].cpu()).all())
+
+
+def test_summaries_bit_exact(cuda_device):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=3, context_min=100, context_max=900, append=False, seed=7)
+    x, step, b, a = _prepare(wl, cuda_device)
+    torch.cuda.synchronize()
+    inp = oracle_inputs(x)
+    summ = step.summary.float().cpu().numpy()
+    bt = x.block_table.cpu().numpy()
+    for r in range(wl.batch):
+        req = oq.QuestRequest(inp["k_cache"], None, inp["block_table"][r], x.seq_lens[r], wl.num_kv_heads,
+                              wl.head_dim, wl.head_dim, 16)
+        for h in range(wl.num_kv_heads):
+            m, M = req.summaries[h]
+            for p in range(m.shape[0]):
+                np.testing.assert_array_equal(summ[bt[r, p], h, 0], m[p])
+                np.testing.assert_array_equal(summ[bt[r, p], h, 1], M[p])
+
+
+def test_append_matches_rebuild_and_is_idempotent(cuda_device):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=6, lengths=(15, 16, 17, 31, 32, 400), topk_pages=4, seed=9)
+    x, step, b, a = _prepare(wl, cuda_device)
+    step.append(x.k_new.to(cuda_device), x.v_new.to(cuda_device), b)
+    once = step.summary.clone()
+    step.append(x.k_new.to(cuda_device), x.v_new.to(cuda_device), b)
+    torch.cuda.synchronize()
+    assert torch.equal(once.view(torch.int16), step.summary.view(torch.int16))
+    fresh = new_summary(step.k_cache)
+    se.se_quest_build_summaries(se.paged_kv(step.k_cache, step.v_cache, fresh), step.block_table, a,
+                                step.max_seq_len)
+    torch.cuda.synchronize()
+    bt = x.block_table
+    for r in range(wl.batch):
+        n = x.pages_per_request[r]
+        idx = bt[r, :n].long().to(cuda_device)
+        assert torch.equal(fresh[idx].view(torch.int16), once[idx].view(torch.int16)), r
+
+
+def test_score_is_an_upper_bound_of_the_group_logit(cuda_device):
+    wl = QWEN3_4B_QUEST_32K.scaled(batch=2, context_min=1000, context_max=1000, seed=13)
+    x, step, b, a = _prepare(wl, cuda_device)
+    se.se_quest_score_pages(step.kv, x.q.to(cuda_device), step.block_table, a, step.max_seq_len, step.scores)
+    torch.cuda.synchronize()
+    scores = step.scores.double().cpu()
+    G = wl.group
+    for r in range(wl.batch):
+        n = x.pages_per_request[r]
+        for h in range(wl.num_kv_heads):
+            qg = x.q[r, h * G:(h + 1) * G].double().sum(0)
+            for p in range(n - 1):
+                keys = x.k_cache[int(x.block_table[r, p]), h].double()
+                true_max = float((keys @ qg).max())
+                # fp32 accumulation of ~256 products of magnitude <= ~50: allow 1e-3 relative slack
+                assert float(scores[r, h, p]) >= true_max - 1e-3 * max(1.0, abs(true_max)), (r, h, p)
+
+
+def test_select_all_equals_dense(cuda_device):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=3, context_min=300, context_max=1000, topk_pages=80,
+                                         append=False, seed=17)
+    x, step, b, a = _prepare(wl, cuda_device)
+    _run(x, step, b, a, cuda_device)
+    inp = oracle_inputs(x)
+    dense = {}
+    for r in range(wl.batch):
+        n = x.pages_per_request[r]
+        assert step.counts[r].tolist() == [n] * wl.num_kv_heads
+        dense[r] = [list(range(n))] * wl.num_kv_heads
+    ref = oq.decode_step(inp, wl.topk_pages, _scale(wl), pages_override=dense)
+    out = step.out.float().cpu().numpy()
+    for r in range(wl.batch):
+        assert np.abs(out[r] - ref[r].out).max() <= OUT_ATOL
+
+
+def test_decode_on_the_oracle_selection(cuda_device):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=3, context_min=1500, context_max=3000, topk_pages=20,
+                                         append=False, seed=19)
+    x, step, b, a = _prepare(wl, cuda_device)
+    inp = oracle_inputs(x)
+    ref = oq.decode_step(inp, wl.topk_pages, _scale(wl))
+    sel = torch.zeros(wl.batch, wl.num_kv_heads, wl.topk_pages + 1, dtype=torch.int32)
+    cnt = torch.zeros(wl.batch, wl.num_kv_heads, dtype=torch.int32)
+    for r in range(wl.batch):
+        for h in range(wl.num_kv_heads):
+            pg = ref[r].heads[h].pages
+            sel[r, h, :len(pg)] = torch.tensor(pg)
+            cnt[r, h] = len(pg)
+    step.attend(x.q.to(cuda_device), a, sel.to(cuda_device), cnt.to(cuda_device))
+    torch.cuda.synchronize()
+    out = step.out.float().cpu().numpy()
+    lse = step.lse.cpu().numpy()
+    for r in range(wl.batch):
+        assert np.abs(out[r] - ref[r].out).max() <= OUT_ATOL
+        assert np.abs(lse[r] - ref[r].lse).max() <= 1e-3
+
+
+def test_block_table_permutation_is_invisible(cuda_device):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=3, context_min=600, context_max=2000, topk_pages=10, seed=23)
+    x, step, b, a = _prepare(wl, cuda_device)
+    _run(x, step, b, a, cuda_device)
+    out1, sel1 = step.out.clone(), step.sel.clone()
+    # Same logical content at other physical pages.
+    P = x.num_pages
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(1))
+    inv = torch.argsort(perm)
+    k2 = x.k_cache[perm].to(cuda_device)
+    v2 = x.v_cache[perm].to(cuda_device)
+    bt2 = inv[x.block_table.long()].to(torch.int32)
+    step2 = QuestDecodeStep(k2, v2, new_summary(k2), bt2.to(cuda_device), wl.num_q_heads, wl.topk_pages,
+                            step.max_seq_len)
+    step2.build_summaries(b)
+    _run(x, step2, b, a, cuda_device)
+    assert torch.equal(sel1, step2.sel)
+    assert torch.equal(out1.view(torch.int16), step2.out.view(torch.int16))
+
+
+def test_split_count_does_not_change_the_result(cuda_device):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=2, context_min=3000, context_max=3000, topk_pages=40,
+                                         append=False, seed=29)
+    x, s1, b, a = _prepare(wl, cuda_device)
+    _run(x, s1, b, a, cuda_device)
+    x2, s2, b2, a2 = _prepare(wl, cuda_device, sel_stride=wl.topk_pages + 1 + 200)
+    _run(x2, s2, b2, a2, cuda_device)
+    assert torch.equal(s1.counts, s2.counts)
+    assert torch.equal(s1.sel, s2.sel[:, :, :wl.topk_pages + 1])
+    assert (s1.out.float() - s2.out.float()).abs().max().item() <= 1e-2
+    assert (s1.lse - s2.lse).abs().max().item() <= 1e-4
+
+
+def test_select_pages_entry_point_matches_the_two_calls(cuda_device):
+    wl = QWEN3_4B_QUEST_32K.scaled(batch=2, context_min=2000, context_max=2400, topk_pages=16, seed=31)
+    x, step, b, a = _prepare(wl, cuda_device)
+    q = x.q.to(cuda_device)
+    step.select(q, a)
+    ws = torch.empty(se.se_quest_select_workspace_size(wl.batch, wl.num_kv_heads, step.max_seq_len),
+                     dtype=torch.uint8, device=cuda_device)
+    sel = torch.empty_like(step.sel)
+    cnt = torch.empty_like(step.counts)
+    se.se_quest_select_pages(step.kv, q, step.block_table, a, step.max_seq_len, wl.topk_pages, sel, cnt, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(cnt, step.counts) and torch.equal(sel, step.sel)
+
+
+def test_out_of_range_page_id_sets_the_error_word(cuda_device):
+    wl = TINY_QUEST_4K.scaled(context_min=160, context_max=160, topk_pages=4)
+    x, step, b, a = _prepare(wl, cuda_device)
+    bad = step.block_table.clone()
+    bad[0, 3] = x.num_pages + 5          # outside the pool: every kernel checks and skips it
+    step.block_table = bad
+    step.kv = se.paged_kv(step.k_cache, step.v_cache, step.summary)
+    se.se_quest_score_pages(step.kv, x.q.to(cuda_device), bad, a, step.max_seq_len, step.scores)
+    torch.cuda.synchronize()
+    assert se.se_read_device_error(clear=True) & se.DEVERR_PAGE_RANGE
+    assert float(step.scores[0, 0, 3]) == float("-inf")
+
+
+def test_short_workspace_is_rejected(cuda_device):
+    wl = TINY_QUEST_4K
+    x, step, b, a = _prepare(wl, cuda_device)
+    with pytest.raises(se.SparseEngineError) as e:
+        se.se_sparse_paged_decode(step.kv, x.q.to(cuda_device), step.block_table, a, step.sel, step.counts, 0.1,
+                                  step.out, None, step.workspace[:16])
+    assert e.value.status == 3
+
+
+# ---------------------------------------------------------------- full size, sampled requests
+def test_full_qwen3_4b_32k_sampled(cuda_device):
+    wl = QWEN3_4B_QUEST_32K
+    x, step, b, a = _prepare(wl, cuda_device, device_gen=True)
+    _run(x, step, b, a, cuda_device)
+    compare_decode(x, step, [0, wl.batch - 1], _scale(wl), "qwen3-4b full")
+
+
+def test_full_qwen3_30b_a3b_128k_sampled(cuda_device):
+    wl = QWEN3_30B_A3B_QUEST_128K
+    x, step, b, a = _prepare(wl, cuda_device, device_gen=True)
+    _run(x, step, b, a, cuda_device)
+    longest = int(np.argmax(x.seq_lens))
+    shortest = int(np.argmin(x.seq_lens))
+    compare_decode(x, step, sorted({longest, shortest, 7}), _scale(wl), "qwen3-30b full")
