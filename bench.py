@@ -1,0 +1,426 @@
+"""Sparse decode attention bench: Quest select + sparse paged decode at 64K-128K context.
+
+Workload: the Qwen3-30B-A3B attention shape (32 query / 4 KV heads, head dim
+128), 32 requests with ragged contexts uniform in [65536, 131072] tokens,
+16-token pages on a randomly permuted block table, a 4096-token budget (256
+pages + the last page), one decode step per request that first appends the
+new token (KV write + summary update). bf16 cache, fp32 accumulation.
+
+One step = se_quest_update_summaries + se_quest_score_pages +
+se_quest_topk_pages + se_sparse_paged_decode over the whole batch (one layer).
+Inputs are resident in HBM; L2 is flushed (a 2x L2-sized write) between
+steps, outside the timed spans; every step is timed with CUDA events on the
+launching stream.
+
+Output: one JSON line (rank 0). ``--impl reference`` times the fp64 CPU
+oracle instead, on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode attn tokens/sec & achieved HBM GB/s (frac of 8 TB/s) at 128K, 1 GB300"
+UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+PAGE = 16
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+_BATCH_OVERRIDE = None
+
+
+def _workload():
+    """The 128K workload; ``--batch`` shrinks it only for profiler captures (never reported as the metric)."""
+    from synth import QWEN3_30B_A3B_QUEST_128K
+    wl = QWEN3_30B_A3B_QUEST_128K
+    return wl if _BATCH_OVERRIDE is None else wl.scaled(batch=_BATCH_OVERRIDE)
+
+
+def _config(wl, extra=None):
+    c = {"workload": wl.name, "model_shape": "Qwen3-30B-A3B attention (32 q / 4 kv heads, d 128)",
+         "batch": wl.batch, "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
+         "head_dim": wl.head_dim, "context": [wl.context_min, wl.context_max], "page_size": wl.page_size,
+         "topk_pages": wl.topk_pages, "kept_pages_per_kv_head": wl.topk_pages + 1,
+         "append_per_step": wl.append, "block_table": "random permutation",
+         "l2": "flushed between timed steps (write of 2x L2 size, outside the events)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# --------------------------------------------------------------------------- bytes
+def algorithmic_bytes(wl, lens_after, counts):
+    """Bytes each kernel must move (inputs read once, outputs written once)."""
+    B, Hq, H, D, Dv = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.head_dim_v
+    n = [math.ceil(L / PAGE) for L in lens_after]
+    cand = sum(max(x - 1, 0) for x in n)
+    summary_row = 2 * D * 2  # min + max, bf16
+    b = {}
+    # append: read k_new/v_new, write the K/V rows, read+write the summary rows
+    b["append"] = B * H * ((D + Dv) * 2 * 2 + summary_row * 2) if wl.append else 0
+    # score: candidate summaries + their block-table entries + q + scores out
+    b["score"] = cand * H * summary_row + cand * 4 + B * Hq * D * 2 + cand * H * 4
+    # top-k: scores in, selection out
+    b["topk"] = cand * H * 4 + B * H * (wl.topk_pages + 1) * 4
+    # decode: the selected K and V page blocks + q + bf16 output
+    sel_pages = int(sum(counts))
+    b["decode"] = sel_pages * PAGE * (D + Dv) * 2 + B * Hq * D * 2 + B * Hq * Dv * 2
+    return b
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def _oracle_worker(args):
+    """One request through the fp64 oracle: state (page summaries) untimed, then the
+    decode step (append + score + select + attend) timed."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import oracle.quest as oq
+    (k, v, n_tokens, H, D, Dv, q, k_new, v_new, topk, scale) = args
+    import numpy as np
+    req = oq.QuestRequest(k, v, np.arange(k.shape[0]), n_tokens, H, D, Dv, PAGE)
+    t0 = time.perf_counter()
+    if k_new is not None:
+        req.append(k_new, v_new)
+    req.decode(q, topk, scale)
+    return time.perf_counter() - t0
+
+
+def _sample_for_oracle(x, requests):
+    items = []
+    wl = x.workload
+    for b in requests:
+        n = x.pages_per_request[b]
+        idx = x.block_table[b, :n].long()
+        k = x.k_cache[idx].cpu().share_memory_()
+        v = x.v_cache[idx].cpu().share_memory_()
+        items.append((k, v, x.seq_lens[b], wl.num_kv_heads, wl.head_dim, wl.head_dim_v, x.q[b].cpu(),
+                      None if x.k_new is None else x.k_new[b].cpu(),
+                      None if x.v_new is None else x.v_new[b].cpu(), wl.topk_pages, 1.0 / math.sqrt(wl.head_dim)))
+    return items
+
+
+def cpu_oracle_throughput(x, n_requests=None, cores=None):
+    """tokens/s of the oracle over a sample of requests, one process per core (spawn)."""
+    import torch.multiprocessing as mp
+    cores = cores or len(os.sched_getaffinity(0))
+    wl = x.workload
+    n_requests = n_requests or min(wl.batch, max(2, 2 * cores))
+    reqs = list(range(n_requests))
+    items = _sample_for_oracle(x, reqs)
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+    ctx = mp.get_context("spawn")
+    workers = min(cores, len(items))
+    with ctx.Pool(workers) as pool:
+        times = pool.map(_oracle_worker, items)
+    busy = sum(times)  # seconds of single-core oracle work
+    value = len(items) / (busy / workers)  # requests (= tokens) per second on `workers` cores
+    return {"value": value, "unit": UNIT, "cores": workers, "kind": "oracle",
+            "sample": f"{len(items)} of the {wl.batch} requests (one decode token each; contexts "
+                      f"{[x.seq_lens[b] for b in reqs]}), append + score + select + attend timed per request, "
+                      f"page summaries prebuilt untimed; {busy:.1f} s of single-core work"}
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import sparse_decode_attention_quest_gb300 as se
+    from sparse_decode_attention_quest_gb300.pipeline import QuestDecodeStep, new_summary
+    from synth import make_quest_decode_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = _workload()
+    if rank:
+        wl = wl.scaled(seed=wl.seed + 1000 * rank)  # each replica decodes its own batch
+    x = make_quest_decode_inputs(wl, device=dev, poison_tail=False)
+    max_len = max(x.seq_lens_after)
+    step = QuestDecodeStep(x.k_cache, x.v_cache, new_summary(x.k_cache), x.block_table, wl.num_q_heads,
+                           wl.topk_pages, max_len)
+    before = torch.tensor(x.seq_lens, dtype=torch.int32, device=dev)
+    after = torch.tensor(x.seq_lens_after, dtype=torch.int32, device=dev)
+    step.build_summaries(before)
+    stream = torch.cuda.Stream(device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+
+    def one_step(ev=None):
+        step.run(x.q, after, x.k_new, x.v_new, before, stream=stream, events=ev)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            one_step()
+    torch.cuda.synchronize()
+    assert se.se_read_device_error() == 0
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.fill_(float(i))
+            one_step(evs[i][:4])
+            evs[i][4].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    spans = {"append": [], "score": [], "topk": [], "decode": []}
+    step_ms = []
+    for e in evs:
+        spans["append"].append(e[0].elapsed_time(e[1]))
+        spans["score"].append(e[1].elapsed_time(e[2]))
+        spans["topk"].append(e[2].elapsed_time(e[3]))
+        spans["decode"].append(e[3].elapsed_time(e[4]))
+        step_ms.append(e[0].elapsed_time(e[4]))
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    counts = step.counts.cpu().flatten().tolist()
+    abytes = algorithmic_bytes(wl, x.seq_lens_after, counts)
+    step_bytes = sum(abytes.values())
+    peak, peak_kind = _peaks()
+    kernels = {}
+    for name, v in spans.items():
+        ms = statistics.mean(v)
+        gbs = abytes[name] / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
+        kernels[name] = {"ms": round(ms, 5), "algorithmic_bytes": abytes[name], "gbs": round(gbs, 1),
+                         "frac_of_measured_hbm": round(gbs / peak, 4)}
+    dom = max(("score", "decode"), key=lambda k: kernels[k]["ms"])
+    traffic = _profile_traffic(dom)
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(args, step, x, before, after, stream, flush, dev)
+
+    result = {
+        "metric": METRIC, "value": wl.batch * world / (ms_per_step * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
+        "data": "synthetic (seeded N(0,1) bf16 keys/values/queries, 4 outlier key channels x8 per KV head)",
+        "config": _config(wl, {"parallelism": f"replicas x{world} (each GPU decodes its own batch)"}),
+        "hbm": {"step_algorithmic_bytes": step_bytes, "step_gbs": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
+                "frac_of_8tbs": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+                "frac_of_measured": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4)},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak, "unit": "GB/s",
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)" if peak_kind ==
+                     "measured" else "fallback 6.8 TB/s",
+                     "frac": round(kernels[dom]["gbs"] / peak, 4), "traffic": traffic},
+        "kernels": kernels,
+        "gpu_launches": K * step.launches_per_step(),
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            result["cpu_baseline"] = cpu_oracle_throughput(x, cores=args.cpu_cores)
+        except Exception as exc:  # reported, never silently replaced
+            result["cpu_baseline"] = {"error": repr(exc)}
+    return result
+
+
+def _profile_traffic(kernel):
+    """DRAM traffic per launch from the committed ncu summary, if it matches the current source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+        src = os.path.join(ROOT, "sparse_decode_attention_quest_gb300", "csrc", rec["source"])
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if digest != rec["source_sha256_16"]:
+            return None
+        return rec["bytes_per_launch_full_size"]
+    except Exception:
+        return None
+
+
+def _e2e(args, step, x, before, after, stream, flush, dev):
+    import torch
+    wl = x.workload
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_kn, h_vn = pin(x.q), pin(x.k_new), pin(x.v_new)
+    h_before = pin(before)
+    h_after = pin(after)
+    h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(x.q), torch.empty_like(x.k_new), torch.empty_like(x.v_new)
+    d_before, d_after = torch.empty_like(before), torch.empty_like(after)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_before, h_after))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step(ev0=None, ev1=None):
+        with torch.cuda.stream(stream):
+            if ev0 is not None:
+                ev0.record(stream)
+            d_q.copy_(h_q, non_blocking=True)
+            d_kn.copy_(h_kn, non_blocking=True)
+            d_vn.copy_(h_vn, non_blocking=True)
+            d_before.copy_(h_before, non_blocking=True)
+            d_after.copy_(h_after, non_blocking=True)
+            step.run(d_q, d_after, d_kn, d_vn, d_before, stream=stream)
+            h_out.copy_(step.out, non_blocking=True)
+            if ev1 is not None:
+                ev1.record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        e2e_step()
+    torch.cuda.synchronize()
+    n = max(10, args.steps // 4)
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        with torch.cuda.stream(stream):
+            flush.fill_(float(i))
+        e2e_step(*pairs[i])
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    return {"value": wl.batch / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": n,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "pinned host q/k_new/v_new/lengths -> device, the four C-ABI calls, output -> pinned host"}
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm: each step decodes a bounded sample of
+    the same workload's requests on the host cores."""
+    import torch
+    from synth import make_quest_decode_inputs
+    wl = _workload()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = make_quest_decode_inputs(wl, device=dev, poison_tail=False)
+    cores = args.cpu_cores or len(os.sched_getaffinity(0))
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_throughput(x, n_requests=min(wl.batch, cores), cores=cores)
+        if i >= args.warmup:
+            per_step.append(r)
+    value = statistics.mean(r["value"] for r in per_step)
+    ms = wl.batch / value * 1e3
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(wl, {"parallelism": "host cores"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": per_step[0]["cores"], "kind": "oracle",
+                             "sample": per_step[0]["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-cores", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=None, help="smaller batch for profiler captures only")
+    args = ap.parse_args()
+    global _BATCH_OVERRIDE
+    _BATCH_OVERRIDE = args.batch
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

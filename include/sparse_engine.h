@@ -204,6 +204,15 @@ SE_API se_status_t se_quest_select_pages(const se_paged_kv_t* kv, const void* q,
  * latent cache (head_dim 576, head_dim_v 512, one KV head, 16..128 query heads
  * in multiples of 16).
  */
+/*
+ * se_sparse_decode_plan -- how se_sparse_paged_decode splits the work on the
+ * current device for these sizes: *nsplit CTAs per (request, KV head), each
+ * taking up to *pages_per_split selected pages, and *launches kernels per call
+ * (the decode kernel, plus the log-sum-exp merge when *nsplit > 1). Host only.
+ */
+SE_API se_status_t se_sparse_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t head_dim_v, int32_t sel_stride,
+                                         int32_t* nsplit, int32_t* pages_per_split, int32_t* launches);
 SE_API size_t se_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim_v, int32_t sel_stride);
 SE_API se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,

@@ -21,7 +21,7 @@ __all__ = [
     "SparseEngineError", "SEPagedKV", "paged_kv", "load_library", "se_read_device_error",
     "se_quest_build_summaries", "se_quest_update_summaries", "se_quest_score_pages",
     "se_quest_topk_pages", "se_quest_select_workspace_size", "se_quest_select_pages",
-    "se_sparse_decode_workspace_size", "se_sparse_paged_decode", "exported_symbols",
+    "se_sparse_decode_workspace_size", "se_sparse_decode_plan", "se_sparse_paged_decode", "exported_symbols",
 ]
 
 SE_OK = 0
@@ -62,6 +62,8 @@ _SIGNATURES = {
     "se_quest_select_workspace_size": (_Z, [_I, _I, _I]),
     "se_quest_select_pages": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _I, _P, _P, _I, _P, _Z, _P]),
     "se_sparse_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "se_sparse_decode_plan": (ctypes.c_int, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                                             ctypes.POINTER(_I)]),
     "se_sparse_paged_decode": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _P, _P, _I, _F, _P, _P, _P, _Z, _P]),
 }
 
@@ -196,6 +198,16 @@ def se_sparse_decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: 
                                     sel_stride: int) -> int:
     return int(load_library().se_sparse_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim_v,
                                                               sel_stride))
+
+
+def se_sparse_decode_plan(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, head_dim_v: int,
+                          sel_stride: int):
+    """(nsplit, pages_per_split, launches) of se_sparse_paged_decode on the current device."""
+    lib = load_library()
+    a, b, c = _I(0), _I(0), _I(0)
+    _check(lib.se_sparse_decode_plan(batch, num_q_heads, num_kv_heads, head_dim, head_dim_v, sel_stride,
+                                     ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
 
 
 def se_sparse_paged_decode(kv: SEPagedKV, q, block_table, seq_lens, sel_pages, sel_counts, sm_scale: float, out,

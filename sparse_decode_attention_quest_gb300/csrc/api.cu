@@ -287,6 +287,25 @@ se_status_t se_quest_select_pages(const se_paged_kv_t* kv, const void* q, int32_
                              out_counts, sel_stride, stream);
 }
 
+se_status_t se_sparse_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t head_dim_v, int32_t sel_stride, int32_t* nsplit,
+                                  int32_t* pages_per_split, int32_t* launches) {
+  static const char* fn = "se_sparse_decode_plan";
+  if (!nsplit || !pages_per_split || !launches) return fail(SE_ERR_INVALID_ARG, fn, "NULL output");
+  if (batch < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads || sel_stride < 1)
+    return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
+  if (!(head_dim == 128 && head_dim_v == 128 && num_q_heads / num_kv_heads <= 16))
+    return fail(SE_ERR_UNSUPPORTED, fn, "shape not implemented");
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  const se::DecodePlan plan = se::plan_gqa_decode(batch, num_kv_heads, sel_stride, d->sm_count);
+  *nsplit = plan.nsplit;
+  *pages_per_split = plan.pages_per_split;
+  *launches = batch == 0 ? 0 : (plan.nsplit > 1 ? 2 : 1);
+  return SE_OK;
+}
+
 size_t se_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim_v, int32_t sel_stride) {
   if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim_v < 1 || sel_stride < 1) return 0;

@@ -15,7 +15,8 @@ from typing import Optional, Sequence
 import torch
 
 from . import (paged_kv, se_quest_build_summaries, se_quest_score_pages, se_quest_topk_pages,
-               se_quest_update_summaries, se_sparse_decode_workspace_size, se_sparse_paged_decode)
+               se_quest_update_summaries, se_sparse_decode_plan, se_sparse_decode_workspace_size,
+               se_sparse_paged_decode)
 
 PAGE = 16
 
@@ -51,6 +52,11 @@ class QuestDecodeStep:
         self.lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=dev)
         ws = se_sparse_decode_workspace_size(self.B, self.Hq, self.H, self.Dv, self.sel_stride)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+
+    def launches_per_step(self, append: bool = True) -> int:
+        """Kernels one run() launches: append, score, top-k, decode (+ split merge)."""
+        _, _, dec = se_sparse_decode_plan(self.B, self.Hq, self.H, self.D, self.Dv, self.sel_stride)
+        return (1 if append else 0) + 2 + dec
 
     def build_summaries(self, seq_lens: torch.Tensor, stream=None):
         se_quest_build_summaries(self.kv, self.block_table, seq_lens, self.max_seq_len, stream)

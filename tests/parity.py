@@ -104,6 +104,7 @@ def compare_decode(x, step, requests, sm_scale: float, what: str = ""):
         assert np.isfinite(out[b]).all(), f"{what} b={b}: non-finite output"
         worst = max(worst, float(err.max()))
         assert err.max() <= OUT_ATOL, f"{what} b={b}: max |out - oracle| = {err.max():.4g}"
-        lerr = np.abs(lse[b] - again[b].lse).max()
+        both_empty = np.isneginf(lse[b]) & np.isneginf(again[b].lse)  # empty request: -inf on both sides
+        lerr = np.where(both_empty, 0.0, np.abs(lse[b] - np.where(both_empty, 0.0, again[b].lse))).max()
         assert lerr <= LSE_ATOL, f"{what} b={b}: max |lse - oracle| = {lerr:.4g}"
     return worst
