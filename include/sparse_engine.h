@@ -221,6 +221,36 @@ SE_API se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q
                                    int32_t sel_stride, float sm_scale, void* out, float* out_lse,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * se_sparse_paged_decode_noalloc -- se_sparse_paged_decode for callers that
+ * cannot allocate device memory. The SparseEngine pages have no counterpart: this
+ * is a deployment variant of the decode above.
+ * Some callers have no way to provide the decode workspace: a plugin in an
+ * inference runtime that receives only its inputs and outputs, a process whose
+ * device memory is owned by another framework's caching allocator, or a serving
+ * loop that forbids cudaMalloc after start-up because it can synchronise the
+ * device. This call computes exactly what se_sparse_paged_decode computes, with
+ * the same arguments minus the workspace, and keeps the split partials in a
+ * fixed 8 MiB array inside the library (held on every GPU that loads the
+ * library until the process exits). It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *  - The first call on a device looks up the array's device address, with that
+ *    device current; make that first call before any stream capture.
+ *  - Sizes whose partials exceed 8 MiB are rejected with SE_ERR_WORKSPACE
+ *    (use se_sparse_paged_decode with a workspace instead); the bound is
+ *    batch * num_q_heads * splits * (head_dim_v + 1) * 4 bytes, splits from
+ *    se_sparse_decode_plan.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents (every partial read is first written by the same call, so nothing
+ *    needs clearing). Two calls that overlap on the GPU race on the array: order
+ *    them on one stream or with events.
+ */
+SE_API se_status_t se_sparse_paged_decode_noalloc(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                                  const int32_t* block_table, int32_t bt_stride,
+                                                  const int32_t* seq_lens, int32_t batch, const int32_t* sel_pages,
+                                                  const int32_t* sel_counts, int32_t sel_stride, float sm_scale,
+                                                  void* out, float* out_lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

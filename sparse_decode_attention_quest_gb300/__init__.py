@@ -21,7 +21,8 @@ __all__ = [
     "SparseEngineError", "SEPagedKV", "paged_kv", "load_library", "se_read_device_error",
     "se_quest_build_summaries", "se_quest_update_summaries", "se_quest_score_pages",
     "se_quest_topk_pages", "se_quest_select_workspace_size", "se_quest_select_pages",
-    "se_sparse_decode_workspace_size", "se_sparse_decode_plan", "se_sparse_paged_decode", "exported_symbols",
+    "se_sparse_decode_workspace_size", "se_sparse_decode_plan", "se_sparse_paged_decode",
+    "se_sparse_paged_decode_noalloc", "exported_symbols",
 ]
 
 SE_OK = 0
@@ -65,6 +66,7 @@ _SIGNATURES = {
     "se_sparse_decode_plan": (ctypes.c_int, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
                                              ctypes.POINTER(_I)]),
     "se_sparse_paged_decode": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _P, _P, _I, _F, _P, _P, _P, _Z, _P]),
+    "se_sparse_paged_decode_noalloc": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _P, _P, _I, _F, _P, _P, _P]),
 }
 
 _lib = None
@@ -222,3 +224,17 @@ def se_sparse_paged_decode(kv: SEPagedKV, q, block_table, seq_lens, sel_pages, s
                                       _ptr(out_lse, torch.float32, "out_lse"),
                                       _ptr(workspace, torch.uint8, "workspace"),
                                       0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
+def se_sparse_paged_decode_noalloc(kv: SEPagedKV, q, block_table, seq_lens, sel_pages, sel_counts, sm_scale: float,
+                                   out, out_lse=None, stream=None):
+    """se_sparse_paged_decode without a workspace, for callers that cannot allocate device memory:
+    the split partials live in a fixed 8 MiB array inside the library (see the C header)."""
+    lib = load_library()
+    _check(lib.se_sparse_paged_decode_noalloc(ctypes.byref(kv), _ptr(q, torch.bfloat16, "q"), q.shape[1],
+                                              _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                              _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0],
+                                              _ptr(sel_pages, torch.int32, "sel_pages"),
+                                              _ptr(sel_counts, torch.int32, "sel_counts"), sel_pages.shape[-1],
+                                              float(sm_scale), _ptr(out, torch.bfloat16, "out"),
+                                              _ptr(out_lse, torch.float32, "out_lse"), _stream(stream)))

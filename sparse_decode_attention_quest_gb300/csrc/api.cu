@@ -355,3 +355,23 @@ se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32
 }
 
 }  // extern "C"
+
+// Internal accessors for entry points defined in other translation units.
+namespace se {
+
+cudaError_t device_context(int* sm_count, unsigned** err) {
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return e;
+  *sm_count = d->sm_count;
+  *err = d->err;
+  return cudaSuccess;
+}
+
+bool encode_kv_page_map(CUtensorMap* map, const void* base, long long rows, int width, int row_stride) {
+  return encode_page_map(map, base, rows, width, row_stride);
+}
+
+void set_error_detail(const char* fn, const char* what) { fail(SE_OK, fn, what); }
+
+}  // namespace se

@@ -61,4 +61,9 @@ cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, 
                               float sm_scale, uint16_t* out, float* out_lse, void* workspace,
                               const DecodePlan& plan, unsigned* err, cudaStream_t stream);
 
+// ---- api.cu: per-device context and helpers shared with other entry points
+cudaError_t device_context(int* sm_count, unsigned** err);
+bool encode_kv_page_map(CUtensorMap* map, const void* base, long long rows, int width, int row_stride);
+void set_error_detail(const char* fn, const char* what);
+
 }  // namespace se
