@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_NAME = "libsparse_engine.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "quest_summary.cu", "quest_select.cu", "sparse_decode.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "quest_summary.cu", "quest_score.cu", "quest_topk.cu", "sparse_decode.cu",
+           "decode_noalloc.cu"]
 
 
 def _nvcc():

@@ -227,8 +227,9 @@ se_status_t se_quest_score_pages(const se_paged_kv_t* kv, const void* q, int32_t
   if (batch > 0 && (!q || !scores)) return fail(SE_ERR_INVALID_ARG, fn, "q/scores NULL");
   if (!aligned16(q) || !aligned16(scores)) return fail(SE_ERR_INVALID_ARG, fn, "q/scores not 16-byte aligned");
   if (score_stride < score_stride_for(max_seq_len)) return fail(SE_ERR_INVALID_ARG, fn, "score_stride too small");
-  if (kv->num_kv_heads * kv->head_dim > 2048)
-    return fail(SE_ERR_UNSUPPORTED, fn, "num_kv_heads * head_dim > 2048 (summary block over 8 KB)");
+  if (!se::score_pages_supported(kv->num_kv_heads, kv->head_dim))
+    return fail(SE_ERR_UNSUPPORTED, fn, "scoring needs head_dim 128 with 1..8 KV heads, or head_dim 576 with one");
+  if (batch > 16384) return fail(SE_ERR_UNSUPPORTED, fn, "batch > 16384");
   DeviceInfo* d = nullptr;
   cudaError_t e = current_device(&d);
   if (e != cudaSuccess) return cuda_fail(fn, e);

@@ -37,11 +37,13 @@ cudaError_t launch_append_update(const KvView& kv, uint16_t* k_mut, uint16_t* v_
                                  const int32_t* seq_lens_before, int32_t batch, unsigned* err,
                                  cudaStream_t stream);
 
-// ---- quest_select.cu
+// ---- quest_score.cu
+bool score_pages_supported(int num_kv_heads, int head_dim);
 cudaError_t launch_score_pages(const KvView& kv, const uint16_t* q, int32_t num_q_heads,
                                const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
                                int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
                                int sm_count, unsigned* err, cudaStream_t stream);
+// ---- quest_topk.cu
 cudaError_t launch_topk_pages(const float* scores, int32_t score_stride, const int32_t* seq_lens, int32_t batch,
                               int32_t num_kv_heads, int32_t max_seq_len, int32_t topk, int32_t* out_pages,
                               int32_t* out_counts, int32_t sel_stride, unsigned* err, cudaStream_t stream);
