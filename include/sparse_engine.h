@@ -206,9 +206,11 @@ SE_API se_status_t se_quest_select_pages(const se_paged_kv_t* kv, const void* q,
  */
 /*
  * se_sparse_decode_plan -- how se_sparse_paged_decode splits the work on the
- * current device for these sizes: *nsplit CTAs per (request, KV head), each
- * taking up to *pages_per_split selected pages, and *launches kernels per call
- * (the decode kernel, plus the log-sum-exp merge when *nsplit > 1). Host only.
+ * current device for these sizes. The selected pages of all (request, KV head)
+ * items are cut into equal slices of at least *pages_per_split pages, one per
+ * CTA; *nsplit is the most slices one item can span (the partial results kept
+ * per query-head row), and *launches the kernels per call (the decode kernel
+ * and the log-sum-exp merge). Host only.
  */
 SE_API se_status_t se_sparse_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t head_dim_v, int32_t sel_stride,

@@ -303,16 +303,16 @@ se_status_t se_sparse_decode_plan(int32_t batch, int32_t num_q_heads, int32_t nu
   const se::DecodePlan plan = se::plan_gqa_decode(batch, num_kv_heads, sel_stride, d->sm_count);
   *nsplit = plan.nsplit;
   *pages_per_split = plan.pages_per_split;
-  *launches = batch == 0 ? 0 : (plan.nsplit > 1 ? 2 : 1);
+  *launches = batch == 0 ? 0 : 2;  // the decode kernel and the split merge
   return SE_OK;
 }
 
 size_t se_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim_v, int32_t sel_stride) {
   if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim_v < 1 || sel_stride < 1) return 0;
-  // Upper bound over devices: at least 8 selected pages per split.
-  const size_t max_split = (size_t)(sel_stride + 7) / 8;
-  return round16((size_t)batch * num_q_heads * max_split * ((size_t)head_dim_v + 1) * sizeof(float));
+  // The split layout does not depend on the device.
+  const se::DecodePlan plan = se::plan_gqa_decode(batch, num_kv_heads, sel_stride, 1);
+  return round16(se::gqa_decode_workspace_bytes(batch, num_q_heads, head_dim_v, plan));
 }
 
 se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
@@ -342,14 +342,11 @@ se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32
   const size_t need = se::gqa_decode_workspace_bytes(batch, num_q_heads, kv->head_dim_v, plan);
   if (workspace_bytes < need) return fail(SE_ERR_WORKSPACE, fn, "workspace too small");
   if (need > 0 && !workspace) return fail(SE_ERR_INVALID_ARG, fn, "workspace NULL");
+  if ((size_t)batch * kv->num_kv_heads > se::gqa_decode_max_items())
+    return fail(SE_ERR_UNSUPPORTED, fn, "too many (request, KV head) items for one launch");
   if (batch == 0) return SE_OK;
-  CUtensorMap kmap, vmap;
-  const long long rows = (long long)kv->num_pages * kv->num_kv_heads * se::kPageSize;
-  if (!encode_page_map(&kmap, kv->k, rows > 0 ? rows : 1, kv->head_dim, kv->row_stride_k) ||
-      !encode_page_map(&vmap, kv->v, rows > 0 ? rows : 1, kv->head_dim_v, kv->row_stride_v))
-    return fail(SE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
-  e = se::launch_gqa_decode(kmap, vmap, view_of(kv), static_cast<const uint16_t*>(q), num_q_heads, block_table,
-                            bt_stride, seq_lens, batch, sel_pages, sel_counts, sel_stride, sm_scale,
+  e = se::launch_gqa_decode(view_of(kv), static_cast<const uint16_t*>(q), num_q_heads, block_table, bt_stride,
+                            seq_lens, batch, sel_pages, sel_counts, sel_stride, sm_scale,
                             static_cast<uint16_t*>(out), out_lse, workspace, plan, d->err,
                             static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);

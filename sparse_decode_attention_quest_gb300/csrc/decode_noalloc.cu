@@ -112,14 +112,11 @@ extern "C" se_status_t se_sparse_paged_decode_noalloc(const se_paged_kv_t* kv, c
   view.head_dim_v = kv->head_dim_v;
   view.row_stride_k = kv->row_stride_k;
   view.row_stride_v = kv->row_stride_v;
-  CUtensorMap kmap, vmap;
-  const long long rows = (long long)kv->num_pages * kv->num_kv_heads * se::kPageSize;
-  if (!se::encode_kv_page_map(&kmap, kv->k, rows > 0 ? rows : 1, kv->head_dim, kv->row_stride_k) ||
-      !se::encode_kv_page_map(&vmap, kv->v, rows > 0 ? rows : 1, kv->head_dim_v, kv->row_stride_v))
-    return reject(SE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-  e = se::launch_gqa_decode(kmap, vmap, view, static_cast<const uint16_t*>(q), num_q_heads, block_table, bt_stride,
-                            seq_lens, batch, sel_pages, sel_counts, sel_stride, sm_scale, static_cast<uint16_t*>(out),
-                            out_lse, scratch, plan, err, static_cast<cudaStream_t>(stream));
+  if ((size_t)batch * kv->num_kv_heads > se::gqa_decode_max_items())
+    return reject(SE_ERR_UNSUPPORTED, "too many (request, KV head) items for one launch");
+  e = se::launch_gqa_decode(view, static_cast<const uint16_t*>(q), num_q_heads, block_table, bt_stride, seq_lens,
+                            batch, sel_pages, sel_counts, sel_stride, sm_scale, static_cast<uint16_t*>(out), out_lse,
+                            scratch, plan, err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return reject(SE_ERR_CUDA, cudaGetErrorString(e));
   return SE_OK;
 }

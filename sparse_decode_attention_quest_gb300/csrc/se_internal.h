@@ -51,17 +51,18 @@ size_t topk_smem_bytes(int32_t max_seq_len);
 
 // ---- sparse_decode.cu
 struct DecodePlan {
-  int32_t nsplit;           // CTAs per (request, KV head)
-  int32_t pages_per_split;  // selected pages per CTA
+  int32_t nsplit;           // most CTAs whose slices one item's pages can span (partial slots per row)
+  int32_t pages_per_split;  // fewest selected pages per CTA slice
+  int32_t grid;             // CTAs launched
 };
 DecodePlan plan_gqa_decode(int32_t batch, int32_t num_kv_heads, int32_t sel_stride, int sm_count);
 size_t gqa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim_v, const DecodePlan& plan);
-cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const KvView& kv,
-                              const uint16_t* q, int32_t num_q_heads, const int32_t* block_table,
-                              int32_t bt_stride, const int32_t* seq_lens, int32_t batch,
-                              const int32_t* sel_pages, const int32_t* sel_counts, int32_t sel_stride,
-                              float sm_scale, uint16_t* out, float* out_lse, void* workspace,
-                              const DecodePlan& plan, unsigned* err, cudaStream_t stream);
+size_t gqa_decode_max_items();
+cudaError_t launch_gqa_decode(const KvView& kv, const uint16_t* q, int32_t num_q_heads, const int32_t* block_table,
+                              int32_t bt_stride, const int32_t* seq_lens, int32_t batch, const int32_t* sel_pages,
+                              const int32_t* sel_counts, int32_t sel_stride, float sm_scale, uint16_t* out,
+                              float* out_lse, void* workspace, const DecodePlan& plan, unsigned* err,
+                              cudaStream_t stream);
 
 // ---- api.cu: per-device context and helpers shared with other entry points
 cudaError_t device_context(int* sm_count, unsigned** err);

@@ -4,175 +4,219 @@
 // history includes the current token).
 //
 // GQA path (head_dim = head_dim_v = 128, 1..16 query heads per KV head):
-//  * one CTA per (request, KV head, split of the selected pages) serves the whole
-//    query group, so every selected (page, head) block is read from HBM once;
-//  * a producer warp streams each page's K and V blocks (4 KB each) into a
-//    12-stage shared-memory ring with tiled TMA copies (two 64-column boxes per
-//    block, 128-byte swizzle so the ldmatrix reads below are conflict-free),
-//    completion tracked by mbarriers;
-//  * four consumer warps each take every fourth page of the split and run an
-//    online softmax: S = Q K^T and O += P V on the tensor cores with the
-//    m16n8k16 bf16 MMA (query heads are the 16 rows, G <= 16), fp32 accumulate;
-//  * the warps' states merge in shared memory; a split writes its normalised
-//    partial output and log-sum-exp, and combine_kernel merges the splits
-//    (o = sum_s exp(lse_s - LSE) o_s). With one split the CTA writes the output.
-// Tokens at positions >= seq_len on a request's last page are masked, and their
-// value rows are zeroed in shared memory, so stale cache contents (even NaN)
-// never reach the output.
+//  * the selected pages of all (request, KV head) items form one flattened
+//    range; every CTA takes an equal slice (at least 16 pages), so ragged
+//    selections balance. A slice is cut at item boundaries into segments;
+//  * one CTA serves a whole query group, so every selected (page, head) block
+//    is read from HBM once. The four warps of a CTA take every fourth page of a
+//    segment; each warp streams its pages through its own 3-stage ring with
+//    16-byte cp.async copies (two pages in flight while it computes a third).
+//    The copies write the 128-byte-swizzled layout that makes the ldmatrix
+//    reads conflict-free, and token rows at or past the request's length are
+//    zero-filled instead of read, so stale cache slots (even NaN) never reach
+//    the output;
+//  * per page: S = Q K^T and O += P V on the tensor cores with the m16n8k16
+//    bf16 MMA (query heads are the 16 rows), an online softmax in the log2
+//    domain, fp32 accumulation;
+//  * at the end of a segment the four warps' states merge in shared memory. An
+//    item held by one CTA writes its output directly; an item spread over
+//    several CTAs writes normalised partials (output, log-sum-exp) and
+//    combine_kernel merges them: o = sum_s exp(lse_s - LSE) o_s.
 #include "se_ptx.cuh"
 
 namespace se {
 namespace {
 
 constexpr int kHeadDim = 128;
-constexpr int kConsumerWarps = 4;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 12;
-constexpr int kHalfBytes = 16 * 64 * 2;     // one 64-column box of a (page, head) block
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+constexpr int kHalfBytes = 16 * 64 * 2;     // one 64-column half of a (page, head) block
 constexpr int kTileBytes = 2 * kHalfBytes;  // one (page, head) block of K or V
-constexpr int kStageBytes = 2 * kTileBytes; // K block then V block
-constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kDecodeSmem = kRingBytes + kStages * 8 * 2 + kStages * 4 + 1024;  // + barriers, meta, alignment
+constexpr int kPageBytes = 2 * kTileBytes;  // K block then V block
+constexpr int kWarpRing = kStages * kPageBytes;
+constexpr int kRingBytes = kWarps * kWarpRing;
+constexpr int kMinPagesPerCta = 16;
+constexpr int kCtasPerSm = 2;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct DecodeArgs {
+  const uint16_t* k;
+  const uint16_t* v;
+  int32_t row_stride_k;
+  int32_t row_stride_v;
   const uint16_t* q;
   int32_t group;
   int32_t num_kv_heads;
+  int32_t batch;
   const int32_t* block_table;
   int32_t bt_stride;
   const int32_t* seq_lens;
   const int32_t* sel;
   const int32_t* sel_counts;
   int32_t sel_stride;
-  int32_t pages_per_split;
-  int32_t nsplit;
+  int32_t max_splits;
   int32_t num_pages;
   float scale_log2;  // sm_scale * log2(e)
   uint16_t* out;
   float* out_lse;
-  float* o_part;     // [B][Hq][nsplit][128]
-  float* lse_part;   // [B][Hq][nsplit], log2 domain
+  float* o_part;     // [B * Hq][max_splits][128]
+  float* lse_part;   // [B * Hq][max_splits], log2 domain
+  int32_t* item_ns;  // [B * H]: CTAs holding each item's pages
   unsigned* err;
 };
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Largest i in [0, n - 1] with prefix[i] <= x: the item whose page range holds x.
+__device__ __forceinline__ int find_item(const int* prefix, int n, int x) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Copy one (page, head) K block and V block into a stage; rows >= valid are
+// zero-filled without reading the cache.
+__device__ __forceinline__ void issue_page(const DecodeArgs& a, uint32_t stage, int phys, int h, int valid,
+                                           int lane) {
+  const size_t blk = ((size_t)phys * a.num_kv_heads + h) * kPageSize;
+  const uint16_t* kp = a.k + blk * a.row_stride_k;
+  const uint16_t* vp = a.v + blk * a.row_stride_v;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int c = lane + 32 * it;  // 16-byte chunk 0..255 of the 16 x 256-byte block
+    const int r = c >> 4, q16 = c & 15;
+    const uint32_t off = (uint32_t)(q16 >> 3) * kHalfBytes + swz128(r, q16 & 7);
+    const bool in = r < valid;
+    const uint32_t bytes = in ? 16u : 0u;
+    cp_async16(stage + off, kp + (size_t)(in ? r : 0) * a.row_stride_k + q16 * 8, bytes);
+    cp_async16(stage + kTileBytes + off, vp + (size_t)(in ? r : 0) * a.row_stride_v + q16 * 8, bytes);
+  }
+}
+
 template <bool kHiRows>
-__global__ void __launch_bounds__(kDecodeThreads, 2) gqa_decode_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                      const __grid_constant__ CUtensorMap vmap,
-                                                                      const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kRingBytes);
-  uint64_t* empty = full + kStages;
-  int* meta = reinterpret_cast<int*>(empty + kStages);
-
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  int* prefix = reinterpret_cast<int*>(ring + kRingBytes);  // [items + 1]
   const int H = a.num_kv_heads, G = a.group, Hq = H * G;
+  const int items = a.batch * H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  int L = a.seq_lens[b];
-  if (L < 0) {
-    if (threadIdx.x == 0) raise_error(a.err, SE_DEVERR_LENGTH);
-    L = 0;
-  }
-  int n_b = (L + kPageSize - 1) / kPageSize;
-  if (n_b > a.bt_stride) {  // a length beyond the block table: clip to it
-    if (threadIdx.x == 0) raise_error(a.err, SE_DEVERR_LENGTH);
-    n_b = a.bt_stride;
-    L = n_b * kPageSize;
-  }
-  int cnt_total = a.sel_counts[b * H + h];
-  if (cnt_total < 0 || cnt_total > a.sel_stride) {
-    if (threadIdx.x == 0 && split == 0) raise_error(a.err, SE_DEVERR_LENGTH);
-    cnt_total = cnt_total < 0 ? 0 : a.sel_stride;
-  }
-  const int start = split * a.pages_per_split;
-  const int cnt = min(a.pages_per_split, cnt_total - start);
-  if (cnt <= 0) {
-    if (split == 0 && a.nsplit == 1) {  // nothing selected: zero output, lse = -inf
-      for (int i = threadIdx.x; i < G * kHeadDim; i += kDecodeThreads) {
-        a.out[((size_t)b * Hq + h * G + i / kHeadDim) * kHeadDim + i % kHeadDim] = 0;
-        if (a.out_lse && i % kHeadDim == 0) a.out_lse[(size_t)b * Hq + h * G + i / kHeadDim] = -INFINITY;
-      }
+  // Selected pages per item, then an exclusive prefix.
+  for (int i = threadIdx.x; i < items; i += kThreads) {
+    int c = a.sel_counts[i];
+    if (c < 0 || c > a.sel_stride) {
+      raise_error(a.err, SE_DEVERR_LENGTH);
+      c = c < 0 ? 0 : a.sel_stride;
     }
-    return;
-  }
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_fence_init();
+    prefix[i + 1] = c;
   }
   __syncthreads();
-
-  // Consumer state (rows g and g + 8 of the MMA tile; unused by the producer warp).
-  const int g = lane >> 2, t = lane & 3;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float o[16][4];
+  if (warp == 0) {
+    const int per = (items + 31) / 32;
+    const int lo = min(items, lane * per), hi = min(items, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += prefix[i + 1];
+    int incl = sum;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int run = incl - sum;
+    if (lane == 0) prefix[0] = 0;
+    for (int i = lo; i < hi; ++i) {
+      run += prefix[i + 1];
+      prefix[i + 1] = run;
+    }
+  }
+  __syncthreads();
+  const int total = prefix[items];
+  const int per_cta = max(kMinPagesPerCta, (total + (int)gridDim.x - 1) / (int)gridDim.x);
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < items; i += kThreads) {
+      const int p0 = prefix[i], cnt = prefix[i + 1] - p0;
+      a.item_ns[i] = cnt == 0 ? 0 : (p0 + cnt - 1) / per_cta - p0 / per_cta + 1;
+    }
+  }
+  const int start = blockIdx.x * per_cta;
+  const int end = min(total, start + per_cta);
+  if (start >= end) return;
 
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_map(&kmap);
-      tma_prefetch_map(&vmap);
+  const uint32_t wring = smem_addr(ring) + warp * kWarpRing;
+  const int g = lane >> 2, t = lane & 3;
+  const int i_first = find_item(prefix, items, start);
+  const int i_last = find_item(prefix, items, end - 1);
+  for (int item = i_first; item <= i_last; ++item) {
+    const int p0 = prefix[item];
+    const int lo = max(start, p0) - p0, hi = min(end, prefix[item + 1]) - p0;  // item-local pages
+    if (lo >= hi) continue;
+    const int b = item / H, h = item % H;
+    int L = a.seq_lens[b];
+    if (L < 0) {
+      if (lane == 0) raise_error(a.err, SE_DEVERR_LENGTH);
+      L = 0;
     }
-    const uint64_t policy = l2_evict_first_policy();
-    const int32_t* sel_row = a.sel + ((size_t)b * H + h) * a.sel_stride + start;
-    const int32_t* bt = a.block_table + (size_t)b * a.bt_stride;
-    bool ok = true;
-    int issued = 0;
-    for (int base = 0; base < cnt && ok; base += 32) {
-      int phys = -1, valid = 0;
-      if (base + lane < cnt) {
-        const int logical = sel_row[base + lane];
+    int n_b = (L + kPageSize - 1) / kPageSize;
+    if (n_b > a.bt_stride) {
+      if (lane == 0) raise_error(a.err, SE_DEVERR_LENGTH);
+      n_b = a.bt_stride;
+      L = n_b * kPageSize;
+    }
+    // This warp's pages of the segment: lo + warp + 4 k, k < np.
+    const int np = (hi - lo > warp) ? (hi - lo - warp + kWarps - 1) / kWarps : 0;
+    const int32_t* sel_row = a.sel + (size_t)item * a.sel_stride + lo + warp;
+    const int32_t* bt_row = a.block_table + (size_t)b * a.bt_stride;
+    // Metadata of page k (physical page, valid tokens), one page per lane.
+    auto meta = [&](int k, int& phys, int& valid) {
+      phys = 0;
+      valid = 0;
+      if (k < np) {
+        const int logical = sel_row[kWarps * k];
         if (logical >= 0 && logical < n_b) {
-          phys = bt[logical];
-          valid = min(kPageSize, L - logical * kPageSize);
-        }
-      }
-      const int m = min(32, cnt - base);
-      for (int j = 0; j < m; ++j) {
-        const int ph = __shfl_sync(0xffffffffu, phys, j);
-        const int v = __shfl_sync(0xffffffffu, valid, j);
-        const int i = base + j, s = i % kStages;
-        if (lane == 0) {
-          if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1)) {
-            raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
-            ok = false;
-          } else if (v <= 0 || ph < 0 || ph >= a.num_pages) {
-            raise_error(a.err, v <= 0 ? SE_DEVERR_LENGTH : SE_DEVERR_PAGE_RANGE);
-            meta[s] = 0;
-            mbar_arrive(&full[s]);
-            ++issued;
+          const int ph = bt_row[logical];
+          if (ph >= 0 && ph < a.num_pages) {
+            phys = ph;
+            valid = min(kPageSize, L - logical * kPageSize);
           } else {
-            meta[s] = v;
-            mbar_arrive_expect_tx(&full[s], kStageBytes);
-            const int y = (ph * H + h) * kPageSize;
-            uint8_t* st = ring + s * kStageBytes;
-            tma_load_2d(st, &kmap, 0, y, &full[s], policy);
-            tma_load_2d(st + kHalfBytes, &kmap, 64, y, &full[s], policy);
-            tma_load_2d(st + kTileBytes, &vmap, 0, y, &full[s], policy);
-            tma_load_2d(st + kTileBytes + kHalfBytes, &vmap, 64, y, &full[s], policy);
-            ++issued;
+            raise_error(a.err, SE_DEVERR_PAGE_RANGE);
           }
+        } else {
+          raise_error(a.err, SE_DEVERR_LENGTH);
         }
-        ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
-        if (!ok) break;
       }
-    }
-    // Drain: every copy this CTA issued has landed before any thread leaves.
-    if (lane == 0) {
-      for (int i = max(0, issued - kStages); i < issued; ++i) {
-        if (!mbar_wait(&full[i % kStages], (i / kStages) & 1)) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+    };
+    // Two batches of 32 pages: [base, base + 32) in *_cur, the next 32 in *_nxt.
+    int base = 0, ph_cur, va_cur, ph_nxt, va_nxt;
+    meta(lane, ph_cur, va_cur);
+    meta(lane + 32, ph_nxt, va_nxt);
+    auto lookup = [&](int k, int& phys, int& valid) {
+      const int pc = __shfl_sync(0xffffffffu, ph_cur, k & 31), vc = __shfl_sync(0xffffffffu, va_cur, k & 31);
+      const int pn = __shfl_sync(0xffffffffu, ph_nxt, k & 31), vn = __shfl_sync(0xffffffffu, va_nxt, k & 31);
+      const bool in_cur = k < base + 32;
+      phys = in_cur ? pc : pn;
+      valid = in_cur ? vc : vn;
+    };
+
+    // Prologue: the first kStages - 1 pages in flight, then the query fragments.
+#pragma unroll
+    for (int k = 0; k < kStages - 1; ++k) {
+      if (k < np) {
+        int ph, va;
+        lookup(k, ph, va);
+        issue_page(a, wring + (k % kStages) * kPageBytes, ph, h, va, lane);
       }
+      cp_async_commit();
     }
-  } else {
-    // ------------------------------------------------------------ consumers
-    // Query fragments (A operand, rows = query heads of the group, zero past G).
     uint32_t qa[8][4];
     {
       const uint16_t* qrow0 = a.q + ((size_t)b * Hq + h * G + g) * kHeadDim;
@@ -187,49 +231,52 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) gqa_decode_kernel(const __g
         qa[ks][3] = r1 ? *reinterpret_cast<const uint32_t*>(qrow1 + c + 8) : 0u;
       }
     }
-    const uint32_t ring_addr = smem_addr(ring);
-    for (int i = warp; i < cnt; i += kConsumerWarps) {
-      const int s = i % kStages;
-      if (!mbar_wait(&full[s], (i / kStages) & 1)) {
-        if (lane == 0) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
-        break;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[16][4];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+    for (int k = 0; k < np; ++k) {
+      const int kn = k + kStages - 1;
+      if (kn == base + 32 + 32) {  // the next batch is needed by the copy ahead: rotate
+        base += 32;
+        ph_cur = ph_nxt;
+        va_cur = va_nxt;
+        meta(base + 32 + lane, ph_nxt, va_nxt);
       }
-      const int valid = meta[s];
+      if (kn < np) {
+        int ph, va;
+        lookup(kn, ph, va);
+        issue_page(a, wring + (kn % kStages) * kPageBytes, ph, h, va, lane);
+      }
+      cp_async_commit();
+      cp_async_wait<kStages - 1>();  // page k has landed (this thread's copies)
+      __syncwarp();                  // ... and every lane's
+      int ph_k, valid;
+      lookup(k, ph_k, valid);
+      (void)ph_k;
       if (valid > 0) {
-        const uint32_t kt = ring_addr + s * kStageBytes;
+        const uint32_t kt = wring + (k % kStages) * kPageBytes;
         const uint32_t vt = kt + kTileBytes;
-        if (valid < kPageSize) {
-          // Zero value rows past the length in both 64-column boxes.
-          uint4* vrow = reinterpret_cast<uint4*>(ring + s * kStageBytes + kTileBytes);
-          const int nchunk = (kPageSize - valid) * 8;  // 16-byte chunks per box
-          for (int c = lane; c < 2 * nchunk; c += 32) {
-            const int box = c / nchunk, r = c % nchunk;
-            vrow[box * (kHalfBytes / 16) + valid * 8 + r] = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
         // S = Q K^T : two n-tiles of 8 tokens, 8 k-steps of 16 dims.
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int krow = (lane & 7) + ((lane >> 4) << 3);
         const int ksub = (lane >> 3) & 1;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t addr = kt + (ks >> 2) * kHalfBytes + swz128(krow, ((ks & 3) << 1) + ksub);
           uint32_t r0, r1, r2, r3;
-          ldmatrix_x4(r0, r1, r2, r3, addr);
+          ldmatrix_x4(r0, r1, r2, r3, kt + (ks >> 2) * kHalfBytes + swz128(krow, ((ks & 3) << 1) + ksub));
           mma_bf16_16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], r0, r1);
           mma_bf16_16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], r2, r3);
         }
-        // Online softmax in the log2 domain.
+        // Online softmax in the log2 domain; tokens >= valid are masked.
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int tok = nt * 8 + 2 * t + (e & 1);
             sc[nt][e] = tok < valid ? sc[nt][e] * a.scale_log2 : -INFINITY;
           }
-        }
         float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
         float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -261,33 +308,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) gqa_decode_kernel(const __g
         const uint32_t pa1 = pack_bf16x2(p[0][2], p[0][3]);
         const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]);
         const uint32_t pa3 = pack_bf16x2(p[1][2], p[1][3]);
-        // O += P V : 16 n-tiles of 8 dims, one k-step of 16 tokens.
+        // O += P V : 16 n-tiles of 8 dims, one k-step of 16 tokens (zero rows past valid).
         const int vtok = (lane & 7) + (((lane >> 3) & 1) << 3);
         const int vsub = lane >> 4;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int chunk = 2 * j + vsub;  // 16-byte chunk of 8 dims, 0..15
-          const uint32_t addr = vt + (chunk >> 3) * kHalfBytes + swz128(vtok, chunk & 7);
+          const int chunk = 2 * j + vsub;
           uint32_t r0, r1, r2, r3;
-          ldmatrix_x4_trans(r0, r1, r2, r3, addr);
+          ldmatrix_x4_trans(r0, r1, r2, r3, vt + (chunk >> 3) * kHalfBytes + swz128(vtok, chunk & 7));
           mma_bf16_16816(o[2 * j], pa0, pa1, pa2, pa3, r0, r1);
           mma_bf16_16816(o[2 * j + 1], pa0, pa1, pa2, pa3, r2, r3);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      __syncwarp();  // every lane is done with this stage before it is refilled
     }
+    cp_async_wait<0>();
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  }
 
-  __syncthreads();  // every warp is done with the ring (all copies drained): reuse it for the merge
-  if (warp < kConsumerWarps) {
-    float* red_m = reinterpret_cast<float*>(ring);         // [4][16]
-    float* red_l = red_m + kConsumerWarps * 16;            // [4][16]
-    float* red_o = red_l + kConsumerWarps * 16;            // [4][16][128]
+    // ---- merge the four warps' states (the rings are idle: reuse them)
+    __syncthreads();
+    float* red_m = reinterpret_cast<float*>(ring);  // [4][16]
+    float* red_l = red_m + kWarps * 16;             // [4][16]
+    float* red_o = red_l + kWarps * 16;             // [4][16][128]
     if (t == 0) {
       red_m[warp * 16 + g] = m0;
       red_l[warp * 16 + g] = l0;
@@ -296,151 +341,156 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) gqa_decode_kernel(const __g
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      float* r0p = red_o + ((size_t)warp * 16 + g) * kHeadDim + j * 8 + 2 * t;
-      float* r1p = red_o + ((size_t)warp * 16 + g + 8) * kHeadDim + j * 8 + 2 * t;
-      *reinterpret_cast<float2*>(r0p) = make_float2(o[j][0], o[j][1]);
-      *reinterpret_cast<float2*>(r1p) = make_float2(o[j][2], o[j][3]);
+      *reinterpret_cast<float2*>(red_o + ((size_t)warp * 16 + g) * kHeadDim + j * 8 + 2 * t) =
+          make_float2(o[j][0], o[j][1]);
+      *reinterpret_cast<float2*>(red_o + ((size_t)warp * 16 + g + 8) * kHeadDim + j * 8 + 2 * t) =
+          make_float2(o[j][2], o[j][3]);
     }
-  }
-  __syncthreads();  // merge inputs written
-
-  const float* red_m = reinterpret_cast<const float*>(ring);
-  const float* red_l = red_m + kConsumerWarps * 16;
-  const float* red_o = red_l + kConsumerWarps * 16;
-  for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kDecodeThreads) {
-    const int r = idx / kHeadDim, d = idx % kHeadDim;
-    float M = -INFINITY;
+    __syncthreads();
+    const int cnt = prefix[item + 1] - p0;
+    const int first_cta = p0 / per_cta;
+    const int ns = (p0 + cnt - 1) / per_cta - first_cta + 1;
+    const int slot = blockIdx.x - first_cta;
+    for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kThreads) {
+      const int r = idx / kHeadDim, d = idx % kHeadDim;
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * 16 + r]);
-    float lsum = 0.f, acc = 0.f;
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * 16 + r]);
+      float lsum = 0.f, acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float mw = red_m[w * 16 + r];
-      const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-      lsum += f * red_l[w * 16 + r];
-      acc += f * red_o[((size_t)w * 16 + r) * kHeadDim + d];
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = red_m[w * 16 + r];
+        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        lsum += f * red_l[w * 16 + r];
+        acc += f * red_o[((size_t)w * 16 + r) * kHeadDim + d];
+      }
+      const bool empty_row = !(lsum > 0.f);
+      const float val = empty_row ? 0.f : acc / lsum;
+      const float lse2 = empty_row ? -INFINITY : M + log2f(lsum);
+      const size_t row = (size_t)b * Hq + h * G + r;
+      if (ns == 1) {
+        a.out[row * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+        if (a.out_lse && d == 0) a.out_lse[row] = lse2 * kLn2;
+      } else {
+        a.o_part[(row * a.max_splits + slot) * kHeadDim + d] = val;
+        if (d == 0) a.lse_part[row * a.max_splits + slot] = lse2;
+      }
     }
-    const bool empty_row = !(lsum > 0.f);
-    const float val = empty_row ? 0.f : acc / lsum;
-    const float lse2 = empty_row ? -INFINITY : M + log2f(lsum);
-    const size_t row = (size_t)b * Hq + h * G + r;
-    if (a.nsplit == 1) {
-      a.out[row * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-      if (a.out_lse && d == 0) a.out_lse[row] = lse2 * kLn2;
-    } else {
-      a.o_part[(row * a.nsplit + split) * kHeadDim + d] = val;
-      if (d == 0) a.lse_part[row * a.nsplit + split] = lse2;
-    }
+    __syncthreads();  // the rings are refilled by the next segment
   }
 }
 
-// Merge the split partials of one (request, query head) per warp.
+// Merge the partials of the items spread over several CTAs; one warp per
+// (request, query head). Items held by one CTA were written directly; items
+// with no selected page get a zero output and lse = -inf.
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ o_part,
                                                       const float* __restrict__ lse_part,
-                                                      const int32_t* __restrict__ sel_counts, int32_t batch,
-                                                      int32_t Hq, int32_t group, int32_t sel_stride,
-                                                      int32_t pages_per_split, int32_t nsplit, int32_t Dv,
-                                                      uint16_t* __restrict__ out, float* __restrict__ out_lse) {
+                                                      const int32_t* __restrict__ item_ns, int32_t batch, int32_t Hq,
+                                                      int32_t group, int32_t max_splits, uint16_t* __restrict__ out,
+                                                      float* __restrict__ out_lse) {
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= batch * Hq) return;
   const int lane = threadIdx.x & 31;
   const int b = row / Hq, h = (row % Hq) / group, H = Hq / group;
-  int cnt = sel_counts[b * H + h];
-  cnt = cnt < 0 ? 0 : (cnt > sel_stride ? sel_stride : cnt);
-  const int ns = min(nsplit, (cnt + pages_per_split - 1) / pages_per_split);
-  const float* lp = lse_part + (size_t)row * nsplit;
+  const int ns = min(item_ns[b * H + h], max_splits);
+  if (ns == 1) return;
+  const float* lp = lse_part + (size_t)row * max_splits;
   float M = -INFINITY;
   for (int s = 0; s < ns; ++s) M = fmaxf(M, lp[s]);
   float wsum = 0.f;
   for (int s = 0; s < ns; ++s) wsum += (lp[s] == -INFINITY) ? 0.f : exp2f(lp[s] - M);
   const bool empty_row = !(wsum > 0.f);
-  for (int d = lane * 4; d < Dv; d += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < ns; ++s) {
-      if (lp[s] == -INFINITY) continue;
-      const float f = exp2f(lp[s] - M);
-      const float4 v = *reinterpret_cast<const float4*>(o_part + ((size_t)row * nsplit + s) * Dv + d);
-      acc.x += f * v.x;
-      acc.y += f * v.y;
-      acc.z += f * v.z;
-      acc.w += f * v.w;
-    }
-    const float inv = empty_row ? 0.f : 1.f / wsum;
-    uint2 pk;
-    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(out + (size_t)row * Dv + d) = pk;
+  const float inv = empty_row ? 0.f : 1.f / wsum;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int d = lane * 4;
+  for (int s = 0; s < ns; ++s) {
+    if (lp[s] == -INFINITY) continue;
+    const float f = exp2f(lp[s] - M);
+    const float4 v = *reinterpret_cast<const float4*>(o_part + ((size_t)row * max_splits + s) * kHeadDim + d);
+    acc.x += f * v.x;
+    acc.y += f * v.y;
+    acc.z += f * v.z;
+    acc.w += f * v.w;
   }
+  uint2 pk;
+  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(out + (size_t)row * kHeadDim + d) = pk;
   if (out_lse && lane == 0) out_lse[row] = empty_row ? -INFINITY : (M + log2f(wsum)) * kLn2;
 }
+
+size_t decode_smem_bytes(int items) { return (size_t)kRingBytes + 1024 + (size_t)(items + 1) * 4; }
 
 }  // namespace
 
 DecodePlan plan_gqa_decode(int32_t batch, int32_t num_kv_heads, int32_t sel_stride, int sm_count) {
-  const long long items = (long long)batch * num_kv_heads;
-  const long long target = (long long)sm_count * 2 * 4;  // about 4 waves of 2 CTAs per SM
-  long long ns = items > 0 ? (target + items - 1) / items : 1;
-  if (ns < 1) ns = 1;
-  if (ns > sel_stride) ns = sel_stride;
-  int pps = (int)((sel_stride + ns - 1) / ns);
-  pps = ((pps + 3) / 4) * 4;
-  if (pps < 8) pps = 8;
+  (void)batch;
+  (void)num_kv_heads;
   DecodePlan p;
-  p.pages_per_split = pps;
-  p.nsplit = (sel_stride + pps - 1) / pps;
-  if (p.nsplit < 1) p.nsplit = 1;
+  p.pages_per_split = kMinPagesPerCta;
+  p.nsplit = (sel_stride + kMinPagesPerCta - 1) / kMinPagesPerCta + 1;  // CTAs one item can span
+  p.grid = sm_count * kCtasPerSm;
   return p;
 }
 
 size_t gqa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim_v, const DecodePlan& plan) {
-  if (plan.nsplit <= 1) return 0;
-  return (size_t)batch * num_q_heads * plan.nsplit * ((size_t)head_dim_v + 1) * sizeof(float);
+  const size_t rows = (size_t)batch * num_q_heads;
+  const size_t part = rows * plan.nsplit * ((size_t)head_dim_v + 1) * sizeof(float);
+  return ((part + 15) & ~size_t(15)) + rows * sizeof(int32_t);  // + item_ns (at most one per row)
 }
 
-cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const KvView& kv,
-                              const uint16_t* q, int32_t num_q_heads, const int32_t* block_table,
-                              int32_t bt_stride, const int32_t* seq_lens, int32_t batch,
-                              const int32_t* sel_pages, const int32_t* sel_counts, int32_t sel_stride,
-                              float sm_scale, uint16_t* out, float* out_lse, void* workspace,
-                              const DecodePlan& plan, unsigned* err, cudaStream_t stream) {
+size_t gqa_decode_max_items() { return (227 * 1024 - (size_t)kRingBytes - 1024) / 4 - 1; }
+
+cudaError_t launch_gqa_decode(const KvView& kv, const uint16_t* q, int32_t num_q_heads, const int32_t* block_table,
+                              int32_t bt_stride, const int32_t* seq_lens, int32_t batch, const int32_t* sel_pages,
+                              const int32_t* sel_counts, int32_t sel_stride, float sm_scale, uint16_t* out,
+                              float* out_lse, void* workspace, const DecodePlan& plan, unsigned* err,
+                              cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
   const int H = kv.num_kv_heads;
   DecodeArgs a;
+  a.k = kv.k;
+  a.v = kv.v;
+  a.row_stride_k = kv.row_stride_k;
+  a.row_stride_v = kv.row_stride_v;
   a.q = q;
   a.group = num_q_heads / H;
   a.num_kv_heads = H;
+  a.batch = batch;
   a.block_table = block_table;
   a.bt_stride = bt_stride;
   a.seq_lens = seq_lens;
   a.sel = sel_pages;
   a.sel_counts = sel_counts;
   a.sel_stride = sel_stride;
-  a.pages_per_split = plan.pages_per_split;
-  a.nsplit = plan.nsplit;
+  a.max_splits = plan.nsplit;
   a.num_pages = kv.num_pages;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.out = out;
   a.out_lse = out_lse;
-  a.o_part = reinterpret_cast<float*>(workspace);
-  a.lse_part = a.o_part ? a.o_part + (size_t)batch * num_q_heads * plan.nsplit * kHeadDim : nullptr;
+  const size_t rows = (size_t)batch * num_q_heads;
+  const size_t part = rows * plan.nsplit * ((size_t)kHeadDim + 1) * sizeof(float);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.o_part = reinterpret_cast<float*>(ws);
+  a.lse_part = a.o_part + rows * plan.nsplit * kHeadDim;
+  a.item_ns = reinterpret_cast<int32_t*>(ws + ((part + 15) & ~size_t(15)));
   a.err = err;
-  dim3 grid(plan.nsplit, H, batch);
+  const size_t smem = decode_smem_bytes(batch * H);
   cudaError_t e;
   if (a.group > 8) {
-    e = cudaFuncSetAttribute(gqa_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+    e = cudaFuncSetAttribute(gqa_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    gqa_decode_kernel<true><<<grid, kDecodeThreads, kDecodeSmem, stream>>>(kmap, vmap, a);
+    gqa_decode_kernel<true><<<plan.grid, kThreads, smem, stream>>>(a);
   } else {
-    e = cudaFuncSetAttribute(gqa_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+    e = cudaFuncSetAttribute(gqa_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    gqa_decode_kernel<false><<<grid, kDecodeThreads, kDecodeSmem, stream>>>(kmap, vmap, a);
+    gqa_decode_kernel<false><<<plan.grid, kThreads, smem, stream>>>(a);
   }
   e = cudaGetLastError();
-  if (e != cudaSuccess || plan.nsplit == 1) return e;
-  const int rows = batch * num_q_heads;
-  combine_kernel<<<(rows + 3) / 4, 128, 0, stream>>>(a.o_part, a.lse_part, sel_counts, batch, num_q_heads, a.group,
-                                                    sel_stride, plan.pages_per_split, plan.nsplit, kHeadDim, out,
-                                                    out_lse);
+  if (e != cudaSuccess) return e;
+  const int nrows = batch * num_q_heads;
+  combine_kernel<<<(nrows + 3) / 4, 128, 0, stream>>>(a.o_part, a.lse_part, a.item_ns, batch, num_q_heads, a.group,
+                                                     plan.nsplit, out, out_lse);
   return cudaGetLastError();
 }
 

@@ -120,8 +120,9 @@ def test_decode_validation(se_lib):
 
 
 def test_decode_workspace_size(se_lib):
-    # upper bound: at least 8 pages per split, (Dv + 1) floats per (row, split)
-    assert se_lib.se_sparse_decode_workspace_size(32, 32, 4, 128, 257) == 32 * 32 * 33 * 129 * 4
+    # slices of >= 16 pages: an item of 257 pages spans at most 18; (Dv + 1) floats per (row, slice)
+    # plus one int per row for the per-item slice counts
+    assert se_lib.se_sparse_decode_workspace_size(32, 32, 4, 128, 257) == 32 * 32 * 18 * 129 * 4 + 32 * 32 * 4
     assert se_lib.se_sparse_decode_workspace_size(-1, 32, 4, 128, 257) == 0
 
 
