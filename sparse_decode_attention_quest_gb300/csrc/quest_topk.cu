@@ -10,9 +10,10 @@
 // page. All integer work: the result is exact for the given fp32 scores.
 //
 //  * topk_pages_reg_kernel (up to 8192 candidates): 1024 threads, each holding
-//    8 consecutive keys in registers; one barrier per radix pass (three
-//    rotating histograms, the digit search done redundantly by every warp) and
-//    two block scans for the ordered output.
+//    8 consecutive scores in registers; a 1024-bucket histogram between the
+//    scores' min and max finds the bucket of the k-th largest, whose members
+//    are then ranked exactly (a radix select restricted to that bucket when it
+//    is crowded), and two block scans write the ordered output.
 //  * topk_pages_smem_kernel (longer contexts): keys in dynamic shared memory.
 #include "se_ptx.cuh"
 
@@ -74,12 +75,51 @@ __device__ __forceinline__ void find_digit(const int* hist, int remaining, int l
   above = __shfl_sync(0xffffffffu, a, src);
 }
 
+constexpr int kBuckets = 1024;
+constexpr int kMaxMembers = 1024;
+
+// Block-wide exclusive prefix of one int per thread, in thread order (two barriers).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* wtot, int warp, int lane, int& total) {
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) wtot[warp] = incl;
+  __syncthreads();
+  int before = incl - v;
+  total = 0;
+  for (int w = 0; w < kTopkWarps; ++w) {
+    const int x = wtot[w];
+    before += (w < warp) ? x : 0;
+    total += x;
+  }
+  __syncthreads();
+  return before;
+}
+
+// Up to 8192 candidates, 8 consecutive scores per thread in registers.
+//  1. min and max of the finite scores; 1024 linear buckets between them (the
+//     bucket index is monotone in the score, so the order is kept);
+//  2. histogram, and the bucket B holding the k-th largest score: every score
+//     in a higher bucket is selected;
+//  3. the members of bucket B are ranked exactly (score, then lower page id)
+//     by brute force; if B holds more than 1024 members (near-identical scores)
+//     a 4-pass radix select restricted to B finds the exact threshold instead;
+//  4. the selected page ids are written in ascending order (block scan).
 __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ seq_lens, int32_t H,
     int32_t max_seq_len, int32_t k, int32_t* __restrict__ out_pages, int32_t* __restrict__ out_counts,
     int32_t sel_stride, unsigned* err) {
-  __shared__ int hist[3][257];
-  __shared__ int wtot_eq[kTopkWarps], wtot_sel[kTopkWarps];
+  __shared__ int hist[kBuckets];
+  __shared__ float s_min[kTopkWarps], s_max[kTopkWarps];
+  __shared__ int wtot[kTopkWarps];
+  __shared__ float mem_val[kMaxMembers];
+  __shared__ int mem_idx[kMaxMembers];
+  __shared__ unsigned selbits[kRegMaxCand / 32];
+  __shared__ int rhist[3][257];
+  __shared__ int s_info[4];  // bucket B, keys above B, members collected
   const int bh = blockIdx.x, b = bh / H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int L = clamp_len(seq_lens[b], max_seq_len, err);
@@ -92,94 +132,152 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
     return;
   }
   const float* sc = scores + (size_t)bh * score_stride;
-  uint32_t key[kKeysPerThread];
+  float x[kKeysPerThread];
+  float lmin = INFINITY, lmax = -INFINITY;
 #pragma unroll
   for (int e = 0; e < kKeysPerThread; ++e) {
     const int i = tid * kKeysPerThread + e;
-    key[e] = i < C ? order_key(sc[i]) : 0u;
+    x[e] = i < C ? sc[i] : -INFINITY;
+    if (i < C && isfinite(x[e])) {
+      lmin = fminf(lmin, x[e]);
+      lmax = fmaxf(lmax, x[e]);
+    }
   }
-  for (int i = tid; i < 2 * 257; i += kTopkThreads) (&hist[0][0])[i] = 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lmin = fminf(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
+    lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+  }
+  if (lane == 0) {
+    s_min[warp] = lmin;
+    s_max[warp] = lmax;
+  }
+  hist[tid] = 0;
+  if (tid < kRegMaxCand / 32) selbits[tid] = 0u;
+  if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
+  if (tid == 0) s_info[2] = 0;
   __syncthreads();
-
-  uint32_t prefix = 0, mask = 0;
-  int remaining = k;
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    int* h = hist[pass % 3];
-    if (pass >= 1)  // buffer of the next pass; its last readers passed the previous barrier
-      for (int i = tid; i < 257; i += kTopkThreads) hist[(pass + 1) % 3][i] = 0;
+  float mn = INFINITY, mx = -INFINITY;
+  for (int w = 0; w < kTopkWarps; ++w) {
+    mn = fminf(mn, s_min[w]);
+    mx = fmaxf(mx, s_max[w]);
+  }
+  const float scale = (mx > mn) ? (float)kBuckets / (mx - mn) : 0.f;
+  int bk[kKeysPerThread];
+#pragma unroll
+  for (int e = 0; e < kKeysPerThread; ++e) {
+    int bb = 0;
+    if (isfinite(x[e])) bb = min(kBuckets - 1, max(0, (int)((x[e] - mn) * scale)));
+    else if (x[e] > 0.f) bb = kBuckets - 1;  // +inf; -inf and NaN stay in bucket 0
+    bk[e] = bb;
+    if (tid * kKeysPerThread + e < C) atomicAdd(&hist[bb], 1);
+  }
+  __syncthreads();
+  // Suffix counts over the buckets (thread i owns bucket i): keys in buckets >= i.
+  const int hc = hist[tid];
+  int incl = hc;  // within the warp, from the top: lanes above hold higher buckets
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += t;
+  }
+  if (lane == 0) wtot[warp] = incl;
+  __syncthreads();
+  for (int w = warp + 1; w < kTopkWarps; ++w) incl += wtot[w];
+  if (incl - hc < k && k <= incl) {
+    s_info[0] = tid;
+    s_info[1] = incl - hc;
+  }
+  __syncthreads();
+  const int B = s_info[0];
+  const int need = k - s_info[1];  // members of bucket B to take, >= 1
+  const int m = hist[B];
+  if (m <= kMaxMembers) {
+    // Exact ranking of the members of bucket B.
 #pragma unroll
     for (int e = 0; e < kKeysPerThread; ++e) {
       const int i = tid * kKeysPerThread + e;
-      const bool in = i < C && (key[e] & mask) == prefix;
-      const int digit = in ? (int)((key[e] >> shift) & 255u) : 256;
-      const unsigned peers = __match_any_sync(0xffffffffu, digit);
-      if (in && lane == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
+      if (i < C && bk[e] == B) {
+        const int slot = atomicAdd(&s_info[2], 1);
+        mem_val[slot] = x[e];
+        mem_idx[slot] = i;
+      }
     }
     __syncthreads();
-    int d, above;
-    find_digit(h, remaining, lane, d, above);
-    remaining -= above;
-    prefix |= (uint32_t)d << shift;
-    mask |= 255u << shift;
-  }
-
-  // Output in ascending index order: every key above T, then the first
-  // `need_eq` keys equal to T.
-  const uint32_t T = prefix;
-  const int need_eq = remaining;
-  int n_eq = 0;
-#pragma unroll
-  for (int e = 0; e < kKeysPerThread; ++e) n_eq += (tid * kKeysPerThread + e < C && key[e] == T) ? 1 : 0;
-  int incl = n_eq;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) wtot_eq[warp] = incl;
-  __syncthreads();
-  int eq_rank = incl - n_eq;
-  for (int w = 0; w < warp; ++w) eq_rank += wtot_eq[w];
-  int n_sel = 0;
-  {
-    int r = eq_rank;
-#pragma unroll
-    for (int e = 0; e < kKeysPerThread; ++e) {
-      const bool in = tid * kKeysPerThread + e < C;
-      if (in && key[e] > T) ++n_sel;
-      if (in && key[e] == T) {
-        if (r < need_eq) ++n_sel;
-        ++r;
+    if (tid < m) {
+      const float v = mem_val[tid];
+      const int id = mem_idx[tid];
+      const uint32_t kv = order_key(v);
+      int rank = 0;
+      for (int j = 0; j < m; ++j) {
+        const uint32_t kj = order_key(mem_val[j]);
+        rank += (kj > kv || (kj == kv && mem_idx[j] < id)) ? 1 : 0;
       }
+      if (rank < need) atomicOr(&selbits[id >> 5], 1u << (id & 31));
     }
-  }
-  incl = n_sel;
+    __syncthreads();
+  } else {
+    // Radix select among the members of bucket B (4 passes x 8 bits).
+    uint32_t key[kKeysPerThread];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) wtot_sel[warp] = incl;
-  __syncthreads();
-  int pos = incl - n_sel;
-  for (int w = 0; w < warp; ++w) pos += wtot_sel[w];
-  {
-    int r = eq_rank;
+    for (int e = 0; e < kKeysPerThread; ++e) key[e] = order_key(x[e]);
+    uint32_t prefix = 0, mask = 0;
+    int remaining = need;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      int* hh = rhist[pass % 3];
+      if (pass >= 1)
+        for (int i = tid; i < 257; i += kTopkThreads) rhist[(pass + 1) % 3][i] = 0;
+#pragma unroll
+      for (int e = 0; e < kKeysPerThread; ++e) {
+        const int i = tid * kKeysPerThread + e;
+        if (i < C && bk[e] == B && (key[e] & mask) == prefix) atomicAdd(&hh[(key[e] >> shift) & 255u], 1);
+      }
+      __syncthreads();
+      int d, above;
+      find_digit(hh, remaining, lane, d, above);
+      remaining -= above;
+      prefix |= (uint32_t)d << shift;
+      mask |= 255u << shift;
+    }
+    // Members above the threshold key, then the first `remaining` equal to it.
+    int n_eq = 0;
+#pragma unroll
+    for (int e = 0; e < kKeysPerThread; ++e)
+      n_eq += (tid * kKeysPerThread + e < C && bk[e] == B && key[e] == prefix) ? 1 : 0;
+    int tot;
+    int r = block_exclusive_scan(n_eq, wtot, warp, lane, tot);
 #pragma unroll
     for (int e = 0; e < kKeysPerThread; ++e) {
       const int i = tid * kKeysPerThread + e;
-      const bool in = i < C;
-      bool take = in && key[e] > T;
-      if (in && key[e] == T) {
-        take = r < need_eq;
-        ++r;
+      if (i < C && bk[e] == B) {
+        bool take = key[e] > prefix;
+        if (key[e] == prefix) {
+          take = r < remaining;
+          ++r;
+        }
+        if (take) atomicOr(&selbits[i >> 5], 1u << (i & 31));
       }
-      if (take) {
-        if (pos < k) out[pos] = i;
-        ++pos;
-      }
+    }
+    __syncthreads();
+  }
+  // Output in ascending page order.
+  bool selv[kKeysPerThread];
+  int n_sel = 0;
+#pragma unroll
+  for (int e = 0; e < kKeysPerThread; ++e) {
+    const int i = tid * kKeysPerThread + e;
+    selv[e] = i < C && (bk[e] > B || (bk[e] == B && ((selbits[i >> 5] >> (i & 31)) & 1u)));
+    n_sel += selv[e] ? 1 : 0;
+  }
+  int tot;
+  int pos = block_exclusive_scan(n_sel, wtot, warp, lane, tot);
+#pragma unroll
+  for (int e = 0; e < kKeysPerThread; ++e) {
+    if (selv[e]) {
+      if (pos < k) out[pos] = tid * kKeysPerThread + e;
+      ++pos;
     }
   }
   if (tid == 0) {
@@ -187,7 +285,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
     out_counts[bh] = k + 1;
   }
 }
-
 
 __global__ void __launch_bounds__(kTopkThreads) topk_pages_smem_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ seq_lens, int32_t H,

@@ -280,3 +280,52 @@ def test_full_qwen3_30b_a3b_128k_sampled(cuda_device):
     longest = int(np.argmax(x.seq_lens))
     shortest = int(np.argmin(x.seq_lens))
     compare_decode(x, step, sorted({longest, shortest, 7}), _scale(wl), "qwen3-30b full")
+
+
+# ---------------------------------------------------------------- top-k on crafted scores
+def _topk_case(scores_rows, lens, k, dev):
+    """Run se_quest_topk_pages on given fp32 scores [B][1][stride]; compare with the oracle exactly."""
+    B = len(lens)
+    stride = scores_rows.shape[-1]
+    max_len = max(lens)
+    sc = scores_rows.to(dev)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=dev)
+    sel = torch.full((B, 1, k + 1), -7, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(B, 1, dtype=torch.int32, device=dev)
+    se.se_quest_topk_pages(sc, lens_t, 1, max_len, k, sel, cnt)
+    torch.cuda.synchronize()
+    for b, L in enumerate(lens):
+        n = math.ceil(L / 16)
+        ref = oq.select_pages(scores_rows[b, 0].double().numpy(), n, k)
+        got = sel[b, 0, :int(cnt[b, 0])].tolist()
+        assert got == ref, (b, L, got[:8], ref[:8])
+
+
+@pytest.mark.parametrize("kind", ["distinct", "all_equal", "few_values", "with_neg_inf", "near_ties"])
+def test_topk_exact_on_crafted_scores(cuda_device, kind):
+    g = torch.Generator().manual_seed(3)
+    lens = [16 * 300, 16 * 2000 + 5, 16 * 6145, 16 * 8193, 16 * 40 + 1]
+    stride = max(math.ceil(L / 16) for L in lens)
+    B = len(lens)
+    if kind == "distinct":
+        s = torch.randn(B, 1, stride, generator=g)
+    elif kind == "all_equal":
+        s = torch.full((B, 1, stride), 1.25)
+    elif kind == "few_values":
+        s = torch.randint(0, 5, (B, 1, stride), generator=g).float()
+    elif kind == "with_neg_inf":
+        s = torch.randn(B, 1, stride, generator=g)
+        s[torch.rand(B, 1, stride, generator=g) < 0.3] = float("-inf")
+    else:  # many scores within a few ulps of each other: crowded buckets, exact order still defined
+        s = 100.0 + torch.randint(0, 3000, (B, 1, stride), generator=g).float() * 1e-5
+    for k in (1, 37, 256):
+        _topk_case(s, lens, k, cuda_device)
+
+
+def test_topk_beyond_8192_candidates_uses_the_shared_memory_kernel(cuda_device):
+    g = torch.Generator().manual_seed(4)
+    lens = [16 * 10000, 16 * 9000 + 3]
+    stride = 10000
+    s = torch.randn(2, 1, stride, generator=g)
+    s[0, 0, ::7] = 0.5  # ties
+    _topk_case(s, lens, 300, cuda_device)
