@@ -224,6 +224,67 @@ SE_API se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * SnapKV eviction at the end of prefill (SparseEngine: Sparse-First Inference
+ * Engine, Table 8: 32-query scoring window, pooling kernel 7, 2,016 selected +
+ * 32 recent tokens; Table 10: probability-based prefill scores; Table 15 note:
+ * physical eviction releases KV storage; Figure 3 caption: the compacted state
+ * is what Chain Cache resumes from).
+ * For request b (prompt length n = prompt_lens[b] >= window) and KV head h, the
+ * window queries are the last `window` prompt positions: q_window[b][w][a] is
+ * the query of head a at position n - window + w (bf16 [batch][window][Hq][128]).
+ * Row r = (w, g) of h's group sees keys j <= n - window + w, with logits
+ * z = sm_scale q . k_j. Shapes: head_dim 128 and window * (Hq / Hkv) <= 128.
+ *
+ * se_snapkv_window_scores: for every candidate j < n - window,
+ *     scores[(b * Hkv + h) * score_stride + j] = sum over the window rows and the
+ *     group's query heads of softmax_j(z)  (fp32; the softmax of each row is over
+ *     all the keys it sees, window keys included),
+ *   and optionally row_lse[(b * Hkv + h) * window * G + r] = log sum_j exp(z_rj)
+ *   (NULL to skip). score_stride >= max_prompt_len - window. Workspace: the
+ *   per-slice row statistics, se_snapkv_workspace_size bytes (any larger size
+ *   is fine; the scores buffer of se_snapkv_score_and_compact is not needed
+ *   here).
+ * se_snapkv_select: max-pools each row of scores with an odd pool_kernel
+ *   (stride 1, window clipped to the candidates), keeps the keep_topk best
+ *   candidates (equal pooled scores: lower position first) in ascending order,
+ *   then appends the window positions n - window .. n - 1; with at most
+ *   keep_topk candidates every position is kept. kept_pos int32
+ *   [batch][Hkv][kept_stride] (kept_stride >= keep_topk + window), kept_counts
+ *   int32 [batch][Hkv]. Up to 45056 candidates per request.
+ * se_snapkv_compact: copies the kept K and V rows unchanged into the destination
+ *   cache: kept token t of (b, h) goes to page dst_block_table[b][t / 16],
+ *   slot t % 16, head h (destination rows dense, 128 wide). The destination
+ *   table must map ceil(kept_counts / 16) pages; a kept token past
+ *   dst_bt_stride * 16 or a page id out of range sets the device error word
+ *   and is skipped.
+ * se_snapkv_score_and_compact: the three steps, the scores kept in `workspace`
+ *   (se_snapkv_workspace_size bytes).
+ */
+SE_API size_t se_snapkv_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t window,
+                                       int32_t max_prompt_len);
+SE_API se_status_t se_snapkv_window_scores(const se_paged_kv_t* src, const void* q_window, int32_t num_q_heads,
+                                           int32_t window, const int32_t* block_table, int32_t bt_stride,
+                                           const int32_t* prompt_lens, int32_t batch, int32_t max_prompt_len,
+                                           float sm_scale, float* scores, int32_t score_stride, float* row_lse,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+SE_API se_status_t se_snapkv_select(const float* scores, int32_t score_stride, const int32_t* prompt_lens,
+                                    int32_t batch, int32_t num_kv_heads, int32_t window, int32_t max_prompt_len,
+                                    int32_t pool_kernel, int32_t keep_topk, int32_t* kept_pos, int32_t kept_stride,
+                                    int32_t* kept_counts, void* stream);
+SE_API se_status_t se_snapkv_compact(const se_paged_kv_t* src, const int32_t* src_block_table, int32_t src_bt_stride,
+                                     const int32_t* prompt_lens, int32_t batch, const se_paged_kv_t* dst,
+                                     const int32_t* dst_block_table, int32_t dst_bt_stride, const int32_t* kept_pos,
+                                     int32_t kept_stride, const int32_t* kept_counts, void* stream);
+SE_API se_status_t se_snapkv_score_and_compact(const se_paged_kv_t* src, const void* q_window, int32_t num_q_heads,
+                                               int32_t window, const int32_t* src_block_table,
+                                               int32_t src_bt_stride, const int32_t* prompt_lens, int32_t batch,
+                                               int32_t max_prompt_len, int32_t pool_kernel, int32_t keep_topk,
+                                               float sm_scale, const se_paged_kv_t* dst,
+                                               const int32_t* dst_block_table, int32_t dst_bt_stride,
+                                               int32_t* kept_pos, int32_t kept_stride, int32_t* kept_counts,
+                                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * se_sparse_paged_decode_noalloc -- se_sparse_paged_decode for callers that
  * cannot allocate device memory. The SparseEngine pages have no counterpart: this
  * is a deployment variant of the decode above.

@@ -51,6 +51,17 @@ def window_probabilities(q_win: np.ndarray, K: np.ndarray, sm_scale: float) -> n
     return e / e.sum(axis=2, keepdims=True)
 
 
+def window_lse(q_win: np.ndarray, K: np.ndarray, sm_scale: float) -> np.ndarray:
+    """LSE [W][G]: log sum_j exp(sm_scale * q_{w,g} . k_j) over the keys row w sees (j <= n-W+w)."""
+    W = q_win.shape[0]
+    n = K.shape[0]
+    z = sm_scale * np.einsum("wgd,jd->wgj", q_win, K)
+    hidden = np.arange(n)[None, :] > (n - W + np.arange(W))[:, None]
+    z = np.where(hidden[:, None, :], -np.inf, z)
+    zmax = z.max(axis=2, keepdims=True)
+    return zmax[:, :, 0] + np.log(np.exp(z - zmax).sum(axis=2))
+
+
 def candidate_scores(alpha: np.ndarray) -> np.ndarray:
     """s_j = sum_w sum_h alpha_{w,h,j} over the candidates j < n-W."""
     W, _, n = alpha.shape
@@ -97,7 +108,8 @@ def snapkv_head(q_win_group, k_cache, block_table_row, h: int, n: int, window: i
     s = candidate_scores(alpha)
     pooled = max_pool_clipped(s, pool_kernel)
     return {"scores": s, "pooled": pooled, "threshold": kth_pooled(pooled, keep),
-            "kept": keep_positions(pooled, n, window, keep), "alpha_total": alpha.sum()}
+            "kept": keep_positions(pooled, n, window, keep), "alpha_total": alpha.sum(),
+            "lse": window_lse(f64(q_win_group), K, sm_scale)}
 
 
 def compact_rows(cache, block_table_row, h: int, kept: list, page_size: int = 16):

@@ -22,7 +22,8 @@ __all__ = [
     "se_quest_build_summaries", "se_quest_update_summaries", "se_quest_score_pages",
     "se_quest_topk_pages", "se_quest_select_workspace_size", "se_quest_select_pages",
     "se_sparse_decode_workspace_size", "se_sparse_decode_plan", "se_sparse_paged_decode",
-    "se_sparse_paged_decode_noalloc", "exported_symbols",
+    "se_sparse_paged_decode_noalloc", "se_snapkv_workspace_size", "se_snapkv_window_scores", "se_snapkv_select",
+    "se_snapkv_compact", "se_snapkv_score_and_compact", "exported_symbols",
 ]
 
 SE_OK = 0
@@ -67,6 +68,12 @@ _SIGNATURES = {
                                              ctypes.POINTER(_I)]),
     "se_sparse_paged_decode": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _P, _P, _I, _F, _P, _P, _P, _Z, _P]),
     "se_sparse_paged_decode_noalloc": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _P, _P, _I, _F, _P, _P, _P]),
+    "se_snapkv_workspace_size": (_Z, [_I, _I, _I, _I]),
+    "se_snapkv_window_scores": (ctypes.c_int, [_KV, _P, _I, _I, _P, _I, _P, _I, _I, _F, _P, _I, _P, _P, _Z, _P]),
+    "se_snapkv_select": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
+    "se_snapkv_compact": (ctypes.c_int, [_KV, _P, _I, _P, _I, _KV, _P, _I, _P, _I, _P, _P]),
+    "se_snapkv_score_and_compact": (ctypes.c_int, [_KV, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _F, _KV, _P, _I, _P,
+                                                   _I, _P, _P, _Z, _P]),
 }
 
 _lib = None
@@ -238,3 +245,59 @@ def se_sparse_paged_decode_noalloc(kv: SEPagedKV, q, block_table, seq_lens, sel_
                                               _ptr(sel_counts, torch.int32, "sel_counts"), sel_pages.shape[-1],
                                               float(sm_scale), _ptr(out, torch.bfloat16, "out"),
                                               _ptr(out_lse, torch.float32, "out_lse"), _stream(stream)))
+
+
+# ---------------------------------------------------------------- SnapKV
+def se_snapkv_workspace_size(batch: int, num_kv_heads: int, window: int, max_prompt_len: int) -> int:
+    return int(load_library().se_snapkv_workspace_size(batch, num_kv_heads, window, max_prompt_len))
+
+
+def se_snapkv_window_scores(src: SEPagedKV, q_window, block_table, prompt_lens, max_prompt_len: int, sm_scale: float,
+                            scores, row_lse=None, workspace=None, stream=None):
+    lib = load_library()
+    _check(lib.se_snapkv_window_scores(ctypes.byref(src), _ptr(q_window, torch.bfloat16, "q_window"),
+                                       q_window.shape[2], q_window.shape[1],
+                                       _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                       _ptr(prompt_lens, torch.int32, "prompt_lens"), prompt_lens.shape[0],
+                                       int(max_prompt_len), float(sm_scale), _ptr(scores, torch.float32, "scores"),
+                                       scores.shape[-1], _ptr(row_lse, torch.float32, "row_lse"),
+                                       _ptr(workspace, torch.uint8, "workspace"),
+                                       0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
+def se_snapkv_select(scores, prompt_lens, num_kv_heads: int, window: int, max_prompt_len: int, pool_kernel: int,
+                     keep_topk: int, kept_pos, kept_counts, stream=None):
+    lib = load_library()
+    _check(lib.se_snapkv_select(_ptr(scores, torch.float32, "scores"), scores.shape[-1],
+                                _ptr(prompt_lens, torch.int32, "prompt_lens"), prompt_lens.shape[0], int(num_kv_heads),
+                                int(window), int(max_prompt_len), int(pool_kernel), int(keep_topk),
+                                _ptr(kept_pos, torch.int32, "kept_pos"), kept_pos.shape[-1],
+                                _ptr(kept_counts, torch.int32, "kept_counts"), _stream(stream)))
+
+
+def se_snapkv_compact(src: SEPagedKV, src_block_table, prompt_lens, dst: SEPagedKV, dst_block_table, kept_pos,
+                      kept_counts, stream=None):
+    lib = load_library()
+    _check(lib.se_snapkv_compact(ctypes.byref(src), _ptr(src_block_table, torch.int32, "src_block_table"),
+                                 src_block_table.shape[1], _ptr(prompt_lens, torch.int32, "prompt_lens"),
+                                 prompt_lens.shape[0], ctypes.byref(dst),
+                                 _ptr(dst_block_table, torch.int32, "dst_block_table"), dst_block_table.shape[1],
+                                 _ptr(kept_pos, torch.int32, "kept_pos"), kept_pos.shape[-1],
+                                 _ptr(kept_counts, torch.int32, "kept_counts"), _stream(stream)))
+
+
+def se_snapkv_score_and_compact(src: SEPagedKV, q_window, src_block_table, prompt_lens, max_prompt_len: int,
+                                pool_kernel: int, keep_topk: int, sm_scale: float, dst: SEPagedKV, dst_block_table,
+                                kept_pos, kept_counts, workspace, stream=None):
+    lib = load_library()
+    _check(lib.se_snapkv_score_and_compact(ctypes.byref(src), _ptr(q_window, torch.bfloat16, "q_window"),
+                                           q_window.shape[2], q_window.shape[1],
+                                           _ptr(src_block_table, torch.int32, "src_block_table"),
+                                           src_block_table.shape[1], _ptr(prompt_lens, torch.int32, "prompt_lens"),
+                                           prompt_lens.shape[0], int(max_prompt_len), int(pool_kernel),
+                                           int(keep_topk), float(sm_scale), ctypes.byref(dst),
+                                           _ptr(dst_block_table, torch.int32, "dst_block_table"),
+                                           dst_block_table.shape[1], _ptr(kept_pos, torch.int32, "kept_pos"),
+                                           kept_pos.shape[-1], _ptr(kept_counts, torch.int32, "kept_counts"),
+                                           _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                           _stream(stream)))

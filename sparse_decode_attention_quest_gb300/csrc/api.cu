@@ -352,6 +352,156 @@ se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
 }
 
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ SnapKV
+namespace {
+
+se_status_t check_snapkv_shape(const char* fn, const se_paged_kv_t* kv, int32_t num_q_heads, int32_t window,
+                               int32_t batch, int32_t max_len) {
+  se_status_t st = check_kv(fn, kv, false);
+  if (st != SE_OK) return st;
+  if (kv->head_dim != 128 || kv->head_dim_v != 128)
+    return fail(SE_ERR_UNSUPPORTED, fn, "SnapKV needs head_dim = head_dim_v = 128");
+  if (num_q_heads < 1 || num_q_heads % kv->num_kv_heads)
+    return fail(SE_ERR_INVALID_ARG, fn, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (window < 1) return fail(SE_ERR_INVALID_ARG, fn, "window < 1");
+  if (window * (num_q_heads / kv->num_kv_heads) > 128)
+    return fail(SE_ERR_UNSUPPORTED, fn, "window x query heads per KV head must be <= 128");
+  if (batch < 0 || max_len < 0) return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
+  if ((long long)batch * kv->num_kv_heads > 4096) return fail(SE_ERR_UNSUPPORTED, fn, "more than 4096 pairs");
+  return SE_OK;
+}
+
+int snap_score_stride(int max_len, int window) { return max_len - window > 1 ? max_len - window : 1; }
+
+}  // namespace
+
+extern "C" {
+
+size_t se_snapkv_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t window, int32_t max_prompt_len) {
+  if (batch < 0 || num_kv_heads < 1 || window < 1 || max_prompt_len < 0) return 0;
+  const int pairs = batch * num_kv_heads;
+  return round16(se::snapkv_part_bytes(pairs, max_prompt_len)) +
+         round16((size_t)pairs * snap_score_stride(max_prompt_len, window) * sizeof(float));
+}
+
+se_status_t se_snapkv_window_scores(const se_paged_kv_t* src, const void* q_window, int32_t num_q_heads,
+                                    int32_t window, const int32_t* block_table, int32_t bt_stride,
+                                    const int32_t* prompt_lens, int32_t batch, int32_t max_prompt_len, float sm_scale,
+                                    float* scores, int32_t score_stride, float* row_lse, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  static const char* fn = "se_snapkv_window_scores";
+  se_status_t st = check_snapkv_shape(fn, src, num_q_heads, window, batch, max_prompt_len);
+  if (st != SE_OK) return st;
+  st = check_batch_common(fn, block_table, bt_stride, prompt_lens, batch, max_prompt_len);
+  if (st != SE_OK) return st;
+  if (batch > 0 && (!q_window || !scores)) return fail(SE_ERR_INVALID_ARG, fn, "q_window/scores NULL");
+  if (!aligned16(q_window) || !aligned16(scores) || !aligned16(row_lse) || !aligned16(workspace))
+    return fail(SE_ERR_INVALID_ARG, fn, "pointers must be 16-byte aligned");
+  if (score_stride < snap_score_stride(max_prompt_len, window))
+    return fail(SE_ERR_INVALID_ARG, fn, "score_stride < max_prompt_len - window");
+  if (!std::isfinite(sm_scale)) return fail(SE_ERR_INVALID_ARG, fn, "sm_scale not finite");
+  const size_t need = se::snapkv_part_bytes(batch * src->num_kv_heads, max_prompt_len);
+  if (workspace_bytes < need) return fail(SE_ERR_WORKSPACE, fn, "workspace too small");
+  if (need > 0 && !workspace) return fail(SE_ERR_INVALID_ARG, fn, "workspace NULL");
+  if (batch == 0) return SE_OK;
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  CUtensorMap kmap;
+  const long long rows = (long long)src->num_pages * src->num_kv_heads * se::kPageSize;
+  if (!encode_page_map(&kmap, src->k, rows > 0 ? rows : 1, src->head_dim, src->row_stride_k))
+    return fail(SE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
+  e = se::launch_snapkv_scores(kmap, view_of(src), static_cast<const uint16_t*>(q_window), num_q_heads, window,
+                               block_table, bt_stride, prompt_lens, batch, max_prompt_len, sm_scale, scores,
+                               score_stride, row_lse, workspace, d->sm_count, d->err,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+se_status_t se_snapkv_select(const float* scores, int32_t score_stride, const int32_t* prompt_lens, int32_t batch,
+                             int32_t num_kv_heads, int32_t window, int32_t max_prompt_len, int32_t pool_kernel,
+                             int32_t keep_topk, int32_t* kept_pos, int32_t kept_stride, int32_t* kept_counts,
+                             void* stream) {
+  static const char* fn = "se_snapkv_select";
+  if (batch < 0 || num_kv_heads < 1 || window < 1 || max_prompt_len < 0) return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
+  if (pool_kernel < 1 || pool_kernel % 2 == 0) return fail(SE_ERR_INVALID_ARG, fn, "pool_kernel must be odd");
+  if (keep_topk < 1) return fail(SE_ERR_INVALID_ARG, fn, "keep_topk < 1");
+  if (kept_stride < keep_topk + window) return fail(SE_ERR_INVALID_ARG, fn, "kept_stride < keep_topk + window");
+  if (score_stride < snap_score_stride(max_prompt_len, window))
+    return fail(SE_ERR_INVALID_ARG, fn, "score_stride < max_prompt_len - window");
+  if (max_prompt_len - window > se::snapkv_select_max_candidates())
+    return fail(SE_ERR_UNSUPPORTED, fn, "more than 45056 candidate positions per request");
+  if (batch > 0 && (!scores || !prompt_lens || !kept_pos || !kept_counts))
+    return fail(SE_ERR_INVALID_ARG, fn, "NULL pointer");
+  if (!aligned16(scores) || !aligned16(kept_pos) || !aligned16(kept_counts))
+    return fail(SE_ERR_INVALID_ARG, fn, "pointers must be 16-byte aligned");
+  if (batch == 0) return SE_OK;
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  e = se::launch_snapkv_select(scores, score_stride, prompt_lens, batch, num_kv_heads, window, max_prompt_len,
+                               pool_kernel, keep_topk, kept_pos, kept_stride, kept_counts, d->err,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+se_status_t se_snapkv_compact(const se_paged_kv_t* src, const int32_t* src_block_table, int32_t src_bt_stride,
+                              const int32_t* prompt_lens, int32_t batch, const se_paged_kv_t* dst,
+                              const int32_t* dst_block_table, int32_t dst_bt_stride, const int32_t* kept_pos,
+                              int32_t kept_stride, const int32_t* kept_counts, void* stream) {
+  static const char* fn = "se_snapkv_compact";
+  se_status_t st = check_kv(fn, src, false);
+  if (st != SE_OK) return st;
+  st = check_kv(fn, dst, false);
+  if (st != SE_OK) return st;
+  if (src->head_dim != 128 || src->head_dim_v != 128 || dst->head_dim != 128 || dst->head_dim_v != 128 ||
+      dst->row_stride_k != 128 || dst->row_stride_v != 128 || dst->num_kv_heads != src->num_kv_heads)
+    return fail(SE_ERR_UNSUPPORTED, fn, "compaction needs d 128 caches with dense destination rows");
+  if (batch < 0 || kept_stride < 1 || src_bt_stride < 1 || dst_bt_stride < 1)
+    return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
+  if (batch > 0 && (!src_block_table || !prompt_lens || !dst_block_table || !kept_pos || !kept_counts))
+    return fail(SE_ERR_INVALID_ARG, fn, "NULL pointer");
+  if (batch == 0) return SE_OK;
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  e = se::launch_snapkv_gather(view_of(src), static_cast<uint16_t*>(dst->k), static_cast<uint16_t*>(dst->v),
+                               dst->num_pages, src_block_table, src_bt_stride, dst_block_table, dst_bt_stride,
+                               prompt_lens, batch, kept_pos, kept_stride, kept_counts, d->err,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+se_status_t se_snapkv_score_and_compact(const se_paged_kv_t* src, const void* q_window, int32_t num_q_heads,
+                                        int32_t window, const int32_t* src_block_table, int32_t src_bt_stride,
+                                        const int32_t* prompt_lens, int32_t batch, int32_t max_prompt_len,
+                                        int32_t pool_kernel, int32_t keep_topk, float sm_scale,
+                                        const se_paged_kv_t* dst, const int32_t* dst_block_table,
+                                        int32_t dst_bt_stride, int32_t* kept_pos, int32_t kept_stride,
+                                        int32_t* kept_counts, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  static const char* fn = "se_snapkv_score_and_compact";
+  if (!src) return fail(SE_ERR_INVALID_ARG, fn, "src is NULL");
+  const size_t need = se_snapkv_workspace_size(batch, src->num_kv_heads, window, max_prompt_len);
+  if (workspace_bytes < need) return fail(SE_ERR_WORKSPACE, fn, "workspace too small");
+  if (need > 0 && !workspace) return fail(SE_ERR_INVALID_ARG, fn, "workspace NULL");
+  const size_t part = round16(se::snapkv_part_bytes(batch * src->num_kv_heads, max_prompt_len));
+  float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + part);
+  const int stride = snap_score_stride(max_prompt_len, window);
+  se_status_t st = se_snapkv_window_scores(src, q_window, num_q_heads, window, src_block_table, src_bt_stride,
+                                           prompt_lens, batch, max_prompt_len, sm_scale, scores, stride, nullptr,
+                                           workspace, part, stream);
+  if (st != SE_OK) return st;
+  st = se_snapkv_select(scores, stride, prompt_lens, batch, src->num_kv_heads, window, max_prompt_len, pool_kernel,
+                        keep_topk, kept_pos, kept_stride, kept_counts, stream);
+  if (st != SE_OK) return st;
+  return se_snapkv_compact(src, src_block_table, src_bt_stride, prompt_lens, batch, dst, dst_block_table,
+                           dst_bt_stride, kept_pos, kept_stride, kept_counts, stream);
+}
+
 }  // extern "C"
 
 // Internal accessors for entry points defined in other translation units.

@@ -64,6 +64,23 @@ cudaError_t launch_gqa_decode(const KvView& kv, const uint16_t* q, int32_t num_q
                               float* out_lse, void* workspace, const DecodePlan& plan, unsigned* err,
                               cudaStream_t stream);
 
+// ---- snapkv.cu
+int snapkv_max_slices(int max_len);
+size_t snapkv_part_bytes(int pairs, int max_len);
+int snapkv_select_max_candidates();
+cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const KvView& kv, const uint16_t* qwin, int32_t num_q_heads,
+                                 int32_t window, const int32_t* bt, int32_t bt_stride, const int32_t* lens,
+                                 int32_t batch, int32_t max_len, float sm_scale, float* scores, int32_t score_stride,
+                                 float* row_lse, void* part_ws, int sm_count, unsigned* err, cudaStream_t stream);
+cudaError_t launch_snapkv_select(const float* scores, int32_t score_stride, const int32_t* lens, int32_t batch,
+                                 int32_t num_kv_heads, int32_t window, int32_t max_len, int32_t pool, int32_t keep,
+                                 int32_t* kept, int32_t kept_stride, int32_t* kept_counts, unsigned* err,
+                                 cudaStream_t stream);
+cudaError_t launch_snapkv_gather(const KvView& src, uint16_t* dk, uint16_t* dv, int32_t dst_num_pages,
+                                 const int32_t* src_bt, int32_t src_bt_stride, const int32_t* dst_bt,
+                                 int32_t dst_bt_stride, const int32_t* lens, int32_t batch, const int32_t* kept,
+                                 int32_t kept_stride, const int32_t* kept_counts, unsigned* err, cudaStream_t stream);
+
 // ---- api.cu: per-device context and helpers shared with other entry points
 cudaError_t device_context(int* sm_count, unsigned** err);
 bool encode_kv_page_map(CUtensorMap* map, const void* base, long long rows, int width, int row_stride);

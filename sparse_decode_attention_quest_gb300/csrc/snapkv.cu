@@ -1,0 +1,728 @@
+// SnapKV-style eviction at the end of prefill (SparseEngine: Sparse-First
+// Inference Engine, Table 8: 32-query scoring window, pooling kernel 7, 2,016
+// selected + 32 recent tokens; Table 10: probability-based prefill scores;
+// Table 15 note: eviction releases storage, so kept tokens are compacted).
+//
+// Per (request b, KV head h) with prompt length n and window W, the R = W * G
+// window query rows r = (w, g) (query head g of h's group at position
+// n - W + w) attend causally to keys j <= n - W + w:
+//   pass 1   LSE_r = log sum_j exp(z_rj),         z_rj = sm_scale q_r . k_j
+//   pass 2   s_j   = sum_r exp(z_rj - LSE_r)      for candidates j < n - W
+//   select   s'_j  = max of s over [j - p/2, j + p/2] clipped to the candidates;
+//            keep the top k of s' (ties: lower j) ascending, then n - W .. n - 1
+//   compact  kept token t -> page t / 16, slot t % 16 of the destination table
+//
+// The logits are the one dense contraction of the path: 128 query rows x 128
+// keys x 128 dims per tile, on the 5th-generation tensor cores. Warp roles:
+//   warp 0      TMA producer: the 8 pages of a 128-key tile, two 64-column
+//               boxes each with 128-byte swizzle, into a 4-stage ring;
+//   warp 1      allocates 256 TMEM columns (two fp32 128x128 accumulators)
+//               and issues the tcgen05.mma (M 128, N 128, K 16) x 8 per tile;
+//   warps 2-5   epilogue: thread r owns TMEM lane r = query row r; it loads
+//               its row of the accumulator, applies the causal mask and the
+//               online max/sum (pass 1) or exp(z - LSE) (pass 2). Pass 2 sums
+//               the columns with a warp transpose-reduce and a fixed-order
+//               merge of the four warps through shared memory (deterministic).
+// The tiles of all (request, KV head) pairs form one flattened range; every
+// CTA takes an equal slice. Pass 1 writes per-slice partial (max, sum) per row
+// that pass 2 merges.
+#include "se_ptx.cuh"
+
+namespace se {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTileN = 128;                   // keys per tile
+constexpr int kPagesPerTile = kTileN / kPageSize;
+constexpr int kHalfBytes = kTileN * 128;      // 128 rows x 128 bytes (64 dims)
+constexpr int kTileBytes = 2 * kHalfBytes;    // 32 KB
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kMinTilesPerCta = 4;
+constexpr int kTmemCols = 256;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Dynamic shared memory: [K ring 4 x 32 KB][Q 2 x 32 KB][colsum 2 x 4 x 128 fp32][prefix][barriers]
+constexpr int kRingOff = 0;
+constexpr int kQOff = kStages * kTileBytes;
+constexpr int kColOff = kQOff + 2 * kTileBytes;
+constexpr int kPrefixOff = kColOff + 2 * 4 * 128 * 4;
+
+struct SnapArgs {
+  const uint16_t* qwin;  // [B][W][Hq][D]
+  int32_t W, G, H, B;
+  const int32_t* bt;
+  int32_t bt_stride;
+  const int32_t* lens;
+  int32_t max_len;
+  int32_t num_pages;
+  float scale_log2;
+  float* part;         // pass 1: [pairs][max_slices][128] x (max, sum), log2 domain
+  int32_t* pair_ns;    // pass 1: slices per pair
+  int32_t max_slices;
+  float* row_lse;      // pass 2, optional: [pairs][R] natural log
+  float* scores;       // pass 2: [pairs][score_stride]
+  int32_t score_stride;
+  unsigned* err;
+};
+
+__device__ __forceinline__ int find_pair(const int* prefix, int n, int x) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void named_barrier_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Tiles of pair (b, h) for the pass: all keys (pass 1) or the candidates only (pass 2).
+__device__ __forceinline__ int pair_tiles(int n, int W, int pass) {
+  const int cols = pass == 1 ? n : max(n - W, 0);
+  return (cols + kTileN - 1) / kTileN;
+}
+
+template <int PASS>
+__global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                   const SnapArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int pairs = a.B * a.H;
+  int* prefix = reinterpret_cast<int*>(smem + kPrefixOff);  // [pairs + 1]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPrefixOff + ((pairs + 2) & ~1) * 4);
+  uint64_t* full = bars;                 // [4]
+  uint64_t* empty = full + kStages;      // [4]
+  uint64_t* acc_full = empty + kStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;    // [2]
+  uint64_t* q_full = acc_empty + 2;      // [2]
+  uint64_t* q_empty = q_full + 2;        // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_empty + 2);
+  float* colsum = reinterpret_cast<float*>(smem + kColOff);  // [2][4][128]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = a.W * a.G;
+
+  // Tiles per pair and their exclusive prefix.
+  for (int p = threadIdx.x; p < pairs; p += kThreads) {
+    int n = a.lens[p / a.H];
+    if (n < a.W || n > a.max_len) {
+      raise_error(a.err, SE_DEVERR_LENGTH);
+      n = n < a.W ? 0 : a.max_len;
+    }
+    prefix[p + 1] = pair_tiles(n, a.W, PASS);
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+      mbar_init(&q_full[i], 128);
+      mbar_init(&q_empty[i], 1);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (pairs + 31) / 32;
+    const int lo = min(pairs, lane * per), hi = min(pairs, lo + per);
+    int sum = 0;
+    for (int p = lo; p < hi; ++p) sum += prefix[p + 1];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int run = incl - sum;
+    if (lane == 0) prefix[0] = 0;
+    for (int p = lo; p < hi; ++p) {
+      run += prefix[p + 1];
+      prefix[p + 1] = run;
+    }
+  }
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total = prefix[pairs];
+  const int per_cta = max(kMinTilesPerCta, (total + (int)gridDim.x - 1) / (int)gridDim.x);
+  if (PASS == 1 && blockIdx.x == 0) {
+    for (int p = threadIdx.x; p < pairs; p += kThreads) {
+      const int p0 = prefix[p], cnt = prefix[p + 1] - p0;
+      a.pair_ns[p] = cnt == 0 ? 0 : (p0 + cnt - 1) / per_cta - p0 / per_cta + 1;
+    }
+  }
+  const int start = blockIdx.x * per_cta;
+  const int end = min(total, start + per_cta);
+  bool dead = false;  // a bounded wait gave up: finish without further waits
+
+  if (start < end) {
+    const int p_first = find_pair(prefix, pairs, start);
+    const int p_last = find_pair(prefix, pairs, end - 1);
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      const uint64_t policy = l2_evict_first_policy();
+      int it = 0;
+      for (int p = p_first; p <= p_last; ++p) {
+        const int t0 = max(start, prefix[p]) - prefix[p], t1 = min(end, prefix[p + 1]) - prefix[p];
+        const int b = p / a.H, h = p % a.H;
+        const int n = min(a.lens[b], a.max_len);
+        const int npages = (n + kPageSize - 1) / kPageSize;
+        for (int t = t0; t < t1; ++t, ++it) {
+          const int s = it % kStages;
+          if (it >= kStages && !dead && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1)) {
+            if (lane == 0) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+            dead = true;
+          }
+          const int page = t * kPagesPerTile + lane;
+          int phys = -1;
+          if (lane < kPagesPerTile && page < npages) {
+            phys = a.bt[(size_t)b * a.bt_stride + page];
+            if (phys < 0 || phys >= a.num_pages) {
+              raise_error(a.err, SE_DEVERR_PAGE_RANGE);
+              phys = -1;
+            }
+          }
+          const unsigned live = __ballot_sync(0xffffffffu, phys >= 0);
+          if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(live) * 2 * kPageSize * 128);
+          __syncwarp();
+          if (phys >= 0 && !dead) {
+            uint8_t* st = smem + kRingOff + s * kTileBytes + lane * kPageSize * 128;
+            const int y = (phys * a.H + h) * kPageSize;
+            tma_load_2d(st, &kmap, 0, y, &full[s], policy);
+            tma_load_2d(st + kHalfBytes, &kmap, 64, y, &full[s], policy);
+          }
+        }
+      }
+      // Drain: every copy issued by this CTA has landed.
+      if (lane == 0)
+        for (int i = max(0, it - kStages); i < it && !dead; ++i)
+          if (!mbar_wait(&full[i % kStages], (i / kStages) & 1)) dead = true;
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc = umma_idesc_bf16(128, kTileN);
+      int it = 0, acc_it = 0, seg = 0;
+      for (int p = p_first; p <= p_last; ++p, ++seg) {
+        const int t0 = max(start, prefix[p]) - prefix[p], t1 = min(end, prefix[p + 1]) - prefix[p];
+        if (t0 >= t1) {
+          --seg;
+          continue;
+        }
+        const int qb = seg & 1;
+        if (lane == 0 && !dead && !mbar_wait(&q_full[qb], (seg >> 1) & 1)) {
+          raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+          dead = true;
+        }
+        dead = __shfl_sync(0xffffffffu, (int)dead, 0) != 0;
+        tc05_fence_after();
+        const uint32_t qaddr = smem_addr(smem + kQOff + qb * kTileBytes);
+        for (int t = t0; t < t1; ++t, ++it, ++acc_it) {
+          const int s = it % kStages, ab = acc_it & 1;
+          if (lane == 0 && !dead) {
+            if (!mbar_wait(&full[s], (it / kStages) & 1)) dead = true;
+            if (!dead && acc_it >= 2 && !mbar_wait(&acc_empty[ab], ((acc_it >> 1) - 1) & 1)) dead = true;
+            if (dead) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+          }
+          dead = __shfl_sync(0xffffffffu, (int)dead, 0) != 0;
+          tc05_fence_after();
+          if (lane == 0) {
+            if (!dead) {
+              const uint32_t kaddr = smem_addr(smem + kRingOff + s * kTileBytes);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                tc05_mma_bf16(tmem + ab * kTileN, umma_desc_sw128(qaddr + koff), umma_desc_sw128(kaddr + koff),
+                              idesc, kk > 0 ? 1u : 0u);
+              }
+            }
+            tc05_commit(&empty[s]);
+            tc05_commit(&acc_full[ab]);
+            if (t == t1 - 1) tc05_commit(&q_empty[qb]);
+          }
+          __syncwarp();
+        }
+      }
+    } else {
+      // ------------------------------------------------------------ epilogue
+      const int wg = warp & 3;            // TMEM lane group of this warp
+      const int r = wg * 32 + lane;       // query row = TMEM lane
+      const int w_pos = r / a.G, g = r % a.G;
+      const bool row_live = r < R;
+      int acc_it = 0, seg = 0, tile_ctr = 0;
+      for (int p = p_first; p <= p_last; ++p) {
+        const int t0 = max(start, prefix[p]) - prefix[p], t1 = min(end, prefix[p + 1]) - prefix[p];
+        if (t0 >= t1) continue;
+        const int b = p / a.H, h = p % a.H;
+        const int n = min(a.lens[b], a.max_len);
+        const int qb = seg & 1;
+        // Query row r of this pair into Q buffer qb (128-byte swizzled, zero past R).
+        if (seg >= 2 && !dead && !mbar_wait(&q_empty[qb], ((seg >> 1) - 1) & 1)) {
+          raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+          dead = true;
+        }
+        {
+          uint8_t* qt = smem + kQOff + qb * kTileBytes;
+          const uint16_t* qrow = a.qwin + (((size_t)b * a.W + w_pos) * (a.H * a.G) + h * a.G + g) * kD;
+#pragma unroll
+          for (int q16 = 0; q16 < 16; ++q16) {
+            const uint4 v = row_live ? *reinterpret_cast<const uint4*>(qrow + q16 * 8) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(qt + (q16 >> 3) * kHalfBytes + swz128(r, q16 & 7)) = v;
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&q_full[qb]);
+        }
+        // Row statistics: pass 1 accumulates them; pass 2 merges pass 1's slices.
+        float m_run = -INFINITY, l_run = 0.f, lse2 = INFINITY;
+        if (PASS == 2) {
+          const int ns = min(a.pair_ns[p], a.max_slices);
+          float M = -INFINITY;
+          for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, a.part[(((size_t)p * a.max_slices + s2) * 128 + r) * 2]);
+          float L = 0.f;
+          for (int s2 = 0; s2 < ns; ++s2) {
+            const float mm = a.part[(((size_t)p * a.max_slices + s2) * 128 + r) * 2];
+            if (mm != -INFINITY) L += a.part[(((size_t)p * a.max_slices + s2) * 128 + r) * 2 + 1] * exp2f(mm - M);
+          }
+          lse2 = (L > 0.f) ? M + log2f(L) : INFINITY;  // +inf: the row contributes nothing
+          if (a.row_lse && t0 == 0 && row_live) a.row_lse[(size_t)p * R + r] = (L > 0.f) ? lse2 * kLn2 : -INFINITY;
+        }
+        const int limit = n - a.W + w_pos;  // last visible key of this row
+        for (int t = t0; t < t1; ++t, ++acc_it, ++tile_ctr) {
+          const int ab = acc_it & 1;
+          if (!dead && !mbar_wait(&acc_full[ab], (acc_it >> 1) & 1)) {
+            raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+            dead = true;
+          }
+          tc05_fence_after();
+          const int j0 = t * kTileN;
+          float* cs = colsum + (tile_ctr & 1) * 4 * 128 + wg * 128;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kTileN; c0 += 32) {
+            uint32_t raw[32];
+            tmem_ld32(tmem + ((uint32_t)(wg * 32) << 16) + ab * kTileN + c0, raw);
+            tmem_ld_wait();
+            if (PASS == 1) {
+              float mx = -INFINITY;
+              float x[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int j = j0 + c0 + c;
+                x[c] = (row_live && j <= limit && j < n) ? __uint_as_float(raw[c]) * a.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x[c]);
+              }
+              const float mn = fmaxf(m_run, mx);
+              if (mn != -INFINITY) {
+                float sum = 0.f;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) sum += exp2f(x[c] - mn);
+                l_run = l_run * exp2f(m_run - mn) + sum;
+                m_run = mn;
+              }
+            } else {
+              float e[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int j = j0 + c0 + c;
+                e[c] = (j < n - a.W) ? exp2f(__uint_as_float(raw[c]) * a.scale_log2 - lse2) : 0.f;
+              }
+              // Warp transpose-reduce: afterwards lane l holds the column c0 + l sum over the warp's rows.
+#pragma unroll
+              for (int k = 0; k < 5; ++k) {
+                const int off = 16 >> k, half = 16 >> k;
+                const bool upper = (lane & off) != 0;
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                  const float lo_v = e[i], hi_v = e[i + half];
+                  const float send = upper ? lo_v : hi_v;
+                  e[i] = (upper ? hi_v : lo_v) + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+              }
+              cs[c0 + lane] = e[0];
+            }
+          }
+          tc05_fence_before();
+          mbar_arrive(&acc_empty[ab]);
+          if (PASS == 2) {
+            named_barrier_epi();  // the four warps' column partials of this tile are in
+            const float* cb = colsum + (tile_ctr & 1) * 4 * 128;
+            const int c = wg * 32 + lane;  // one column per epilogue thread
+            const float v = ((cb[c] + cb[128 + c]) + cb[256 + c]) + cb[384 + c];
+            const int j = j0 + c;
+            if (j < n - a.W) a.scores[(size_t)p * a.score_stride + j] = v;
+          }
+        }
+        if (PASS == 1) {
+          const int first_cta = prefix[p] / per_cta;
+          const int slot = blockIdx.x - first_cta;
+          float* dst = a.part + (((size_t)p * a.max_slices + slot) * 128 + r) * 2;
+          dst[0] = m_run;
+          dst[1] = l_run;
+        }
+        ++seg;
+      }
+    }
+  }
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ selection
+constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kBuckets = 1024;
+constexpr int kMaxMembers = 1024;
+constexpr int kSelMaxCand = 45056;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ int block_scan_excl(int v, int* wtot, int warp, int lane) {
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) wtot[warp] = incl;
+  __syncthreads();
+  int before = incl - v;
+  for (int w = 0; w < warp; ++w) before += wtot[w];
+  __syncthreads();
+  return before;
+}
+
+// Max-pool of the scores, then the top `keep` candidates by pooled score (ties:
+// lower position) in ascending order, then the window positions. One CTA per
+// (request, KV head); pooled scores in shared memory.
+__global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
+    const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ lens, int32_t H, int32_t W,
+    int32_t max_len, int32_t pool, int32_t keep, int32_t* __restrict__ kept, int32_t kept_stride,
+    int32_t* __restrict__ kept_counts, unsigned* err) {
+  extern __shared__ float pooled[];  // [C]
+  __shared__ int hist[kBuckets];
+  __shared__ float s_min[kSelWarps], s_max[kSelWarps];
+  __shared__ int wtot[kSelWarps];
+  __shared__ float mem_val[kMaxMembers];
+  __shared__ int mem_idx[kMaxMembers];
+  __shared__ int s_info[4];
+  __shared__ int rhist[3][257];
+  const int pair = blockIdx.x, b = pair / H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int n = lens[b];
+  if (n < W || n > max_len) {
+    if (tid == 0) raise_error(err, SE_DEVERR_LENGTH);
+    if (tid == 0) kept_counts[pair] = 0;
+    return;
+  }
+  const int C = n - W;
+  int32_t* out = kept + (size_t)pair * kept_stride;
+  if (C <= keep) {
+    for (int i = tid; i < n; i += kSelThreads) out[i] = i;
+    if (tid == 0) kept_counts[pair] = n;
+    return;
+  }
+  const float* sc = scores + (size_t)pair * score_stride;
+  const int half = pool / 2;
+  const int kpt = (C + kSelThreads - 1) / kSelThreads;  // contiguous candidates per thread
+  const int i0 = min(C, tid * kpt), i1 = min(C, i0 + kpt);
+  float lmin = INFINITY, lmax = -INFINITY;
+  for (int i = i0; i < i1; ++i) {
+    float m = -INFINITY;
+    for (int t = max(0, i - half); t <= min(C - 1, i + half); ++t) m = fmaxf(m, sc[t]);
+    pooled[i] = m;
+    if (isfinite(m)) {
+      lmin = fminf(lmin, m);
+      lmax = fmaxf(lmax, m);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lmin = fminf(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
+    lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+  }
+  if (lane == 0) {
+    s_min[warp] = lmin;
+    s_max[warp] = lmax;
+  }
+  hist[tid] = 0;
+  if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
+  if (tid == 0) s_info[2] = 0;
+  __syncthreads();
+  float mn = INFINITY, mx = -INFINITY;
+  for (int w = 0; w < kSelWarps; ++w) {
+    mn = fminf(mn, s_min[w]);
+    mx = fmaxf(mx, s_max[w]);
+  }
+  const float scale = (mx > mn) ? (float)kBuckets / (mx - mn) : 0.f;
+  auto bucket = [&](float v) {
+    if (isfinite(v)) return min(kBuckets - 1, max(0, (int)((v - mn) * scale)));
+    return v > 0.f ? kBuckets - 1 : 0;
+  };
+  for (int i = i0; i < i1; ++i) atomicAdd(&hist[bucket(pooled[i])], 1);
+  __syncthreads();
+  const int hc = hist[tid];
+  int incl = hc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += t;
+  }
+  if (lane == 0) wtot[warp] = incl;
+  __syncthreads();
+  for (int w = warp + 1; w < kSelWarps; ++w) incl += wtot[w];
+  if (incl - hc < keep && keep <= incl) {
+    s_info[0] = tid;
+    s_info[1] = incl - hc;
+  }
+  __syncthreads();
+  const int B = s_info[0];
+  const int need = keep - s_info[1];
+  const int m = hist[B];
+  // Selected members of bucket B are marked by setting the sign bit of an
+  // extra flag array would cost memory; instead the threshold (key T, count of
+  // equal keys to take) is found and applied below.
+  uint32_t T;
+  int need_eq;
+  if (m <= kMaxMembers) {
+    for (int i = i0; i < i1; ++i) {
+      if (bucket(pooled[i]) == B) {
+        const int slot = atomicAdd(&s_info[2], 1);
+        mem_val[slot] = pooled[i];
+        mem_idx[slot] = i;
+      }
+    }
+    __syncthreads();
+    // The member of rank need - 1 (score desc, position asc) sets the threshold.
+    if (tid < m) {
+      const uint32_t kv = order_key(mem_val[tid]);
+      const int id = mem_idx[tid];
+      int rank = 0, above = 0;
+      for (int j = 0; j < m; ++j) {
+        const uint32_t kj = order_key(mem_val[j]);
+        rank += (kj > kv || (kj == kv && mem_idx[j] < id)) ? 1 : 0;
+        above += kj > kv ? 1 : 0;
+      }
+      if (rank == need - 1) {
+        s_info[0] = (int)kv;
+        s_info[1] = need - above;  // keys equal to kv to take, lowest positions first
+      }
+    }
+    __syncthreads();
+    T = (uint32_t)s_info[0];
+    need_eq = s_info[1];
+  } else {
+    uint32_t prefix = 0, mask = 0;
+    int remaining = need;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      int* hh = rhist[pass % 3];
+      if (pass >= 1)
+        for (int i = tid; i < 257; i += kSelThreads) rhist[(pass + 1) % 3][i] = 0;
+      for (int i = i0; i < i1; ++i) {
+        const float v = pooled[i];
+        const uint32_t key = order_key(v);
+        if (bucket(v) == B && (key & mask) == prefix) atomicAdd(&hh[(key >> shift) & 255u], 1);
+      }
+      __syncthreads();
+      // The digit holding the remaining-th largest member key (every warp computes it).
+      int g8[8], gsum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        g8[j] = hh[lane * 8 + j];
+        gsum += g8[j];
+      }
+      int inc2 = gsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, inc2, o);
+        if (lane + o < 32) inc2 += t;
+      }
+      const int up = inc2 - gsum;
+      const bool mine = up < remaining && remaining <= inc2;
+      int d = 0, ab = 0;
+      if (mine) {
+        int cum = up;
+        for (int j = 7; j >= 0; --j) {
+          if (cum + g8[j] >= remaining) {
+            d = lane * 8 + j;
+            ab = cum;
+            break;
+          }
+          cum += g8[j];
+        }
+      }
+      const unsigned who = __ballot_sync(0xffffffffu, mine);
+      const int src = who ? __ffs(who) - 1 : 0;
+      d = __shfl_sync(0xffffffffu, d, src);
+      ab = __shfl_sync(0xffffffffu, ab, src);
+      remaining -= ab;
+      prefix |= (uint32_t)d << shift;
+      mask |= 255u << shift;
+    }
+    T = prefix;
+    need_eq = remaining;
+  }
+  // Selection: pooled key above T, or equal to T among the first need_eq (by position).
+  int n_eq = 0;
+  for (int i = i0; i < i1; ++i) n_eq += order_key(pooled[i]) == T ? 1 : 0;
+  int r = block_scan_excl(n_eq, wtot, warp, lane);
+  int n_sel = 0;
+  {
+    int rr = r;
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t key = order_key(pooled[i]);
+      if (key > T) ++n_sel;
+      else if (key == T) {
+        if (rr < need_eq) ++n_sel;
+        ++rr;
+      }
+    }
+  }
+  int pos = block_scan_excl(n_sel, wtot, warp, lane);
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = order_key(pooled[i]);
+    bool take = key > T;
+    if (key == T) {
+      take = r < need_eq;
+      ++r;
+    }
+    if (take) {
+      if (pos < keep) out[pos] = i;
+      ++pos;
+    }
+  }
+  for (int w = tid; w < W; w += kSelThreads) out[keep + w] = C + w;
+  if (tid == 0) kept_counts[pair] = keep + W;
+}
+
+// ------------------------------------------------------------------ compaction
+// Kept token t of pair (b, h) goes to destination page dst_bt[b][t / 16], slot t % 16.
+// One half-warp copies one 256-byte row (16 x 16 bytes); K and V rows alternate.
+__global__ void __launch_bounds__(256) snapkv_gather_kernel(KvView src, uint16_t* __restrict__ dk,
+                                                            uint16_t* __restrict__ dv, int32_t dst_num_pages,
+                                                            const int32_t* __restrict__ src_bt, int32_t src_bt_stride,
+                                                            const int32_t* __restrict__ dst_bt, int32_t dst_bt_stride,
+                                                            const int32_t* __restrict__ lens, int32_t pairs,
+                                                            const int32_t* __restrict__ kept, int32_t kept_stride,
+                                                            const int32_t* __restrict__ kept_counts, unsigned* err) {
+  const long long unit = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);  // (pair, t, K|V)
+  const int sub = threadIdx.x & 15;
+  const long long rows = (long long)pairs * kept_stride * 2;
+  if (unit >= rows) return;
+  const int kvsel = (int)(unit & 1);
+  const long long pt = unit >> 1;
+  const int pair = (int)(pt / kept_stride), t = (int)(pt % kept_stride);
+  const int H = src.num_kv_heads;
+  const int b = pair / H, h = pair % H;
+  const int cnt = kept_counts[pair];
+  if (t >= cnt || cnt > kept_stride) return;
+  const int pos = kept[(size_t)pair * kept_stride + t];
+  const int n = lens[b];
+  if (pos < 0 || pos >= n || pos / kPageSize >= src_bt_stride || t / kPageSize >= dst_bt_stride) {
+    if (sub == 0) raise_error(err, SE_DEVERR_LENGTH);
+    return;
+  }
+  const int sp = src_bt[(size_t)b * src_bt_stride + pos / kPageSize];
+  const int dp = dst_bt[(size_t)b * dst_bt_stride + t / kPageSize];
+  if (sp < 0 || sp >= src.num_pages || dp < 0 || dp >= dst_num_pages) {
+    if (sub == 0) raise_error(err, SE_DEVERR_PAGE_RANGE);
+    return;
+  }
+  const uint16_t* s = (kvsel ? src.v : src.k) + (((size_t)sp * H + h) * kPageSize + pos % kPageSize) *
+                                                     (kvsel ? src.row_stride_v : src.row_stride_k);
+  uint16_t* d = (kvsel ? dv : dk) + (((size_t)dp * H + h) * kPageSize + t % kPageSize) * kD;
+  reinterpret_cast<uint4*>(d)[sub] = reinterpret_cast<const uint4*>(s)[sub];
+}
+
+size_t scores_smem_bytes(int pairs) {
+  return 1024 + (size_t)kPrefixOff + (size_t)((pairs + 2) & ~1) * 4 + 16 * 8 + 16;
+}
+
+}  // namespace
+
+int snapkv_max_slices(int max_len) {
+  const int tiles = (max_len + kTileN - 1) / kTileN;
+  return (tiles + kMinTilesPerCta - 1) / kMinTilesPerCta + 1;
+}
+
+size_t snapkv_part_bytes(int pairs, int max_len) {
+  const size_t part = (size_t)pairs * snapkv_max_slices(max_len) * 128 * 2 * sizeof(float);
+  return ((part + 15) & ~size_t(15)) + (((size_t)pairs * sizeof(int32_t) + 15) & ~size_t(15));
+}
+
+int snapkv_select_max_candidates() { return kSelMaxCand; }
+
+cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const KvView& kv, const uint16_t* qwin, int32_t num_q_heads,
+                                 int32_t window, const int32_t* bt, int32_t bt_stride, const int32_t* lens,
+                                 int32_t batch, int32_t max_len, float sm_scale, float* scores, int32_t score_stride,
+                                 float* row_lse, void* part_ws, int sm_count, unsigned* err, cudaStream_t stream) {
+  if (batch == 0) return cudaSuccess;
+  SnapArgs a;
+  a.qwin = qwin;
+  a.W = window;
+  a.H = kv.num_kv_heads;
+  a.G = num_q_heads / kv.num_kv_heads;
+  a.B = batch;
+  a.bt = bt;
+  a.bt_stride = bt_stride;
+  a.lens = lens;
+  a.max_len = max_len;
+  a.num_pages = kv.num_pages;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  const int pairs = batch * kv.num_kv_heads;
+  a.max_slices = snapkv_max_slices(max_len);
+  const size_t part = (size_t)pairs * a.max_slices * 128 * 2 * sizeof(float);
+  a.part = static_cast<float*>(part_ws);
+  a.pair_ns = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(part_ws) + ((part + 15) & ~size_t(15)));
+  a.row_lse = row_lse;
+  a.scores = scores;
+  a.score_stride = score_stride;
+  a.err = err;
+  const size_t smem = scores_smem_bytes(pairs);
+  cudaError_t e = cudaFuncSetAttribute(snapkv_scores_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(snapkv_scores_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  snapkv_scores_kernel<1><<<sm_count, kThreads, smem, stream>>>(kmap, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  snapkv_scores_kernel<2><<<sm_count, kThreads, smem, stream>>>(kmap, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_snapkv_select(const float* scores, int32_t score_stride, const int32_t* lens, int32_t batch,
+                                 int32_t num_kv_heads, int32_t window, int32_t max_len, int32_t pool, int32_t keep,
+                                 int32_t* kept, int32_t kept_stride, int32_t* kept_counts, unsigned* err,
+                                 cudaStream_t stream) {
+  if (batch == 0) return cudaSuccess;
+  const int maxc = max(max_len - window, 1);
+  const size_t smem = (size_t)maxc * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(snapkv_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  snapkv_select_kernel<<<batch * num_kv_heads, kSelThreads, smem, stream>>>(
+      scores, score_stride, lens, num_kv_heads, window, max_len, pool, keep, kept, kept_stride, kept_counts, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_snapkv_gather(const KvView& src, uint16_t* dk, uint16_t* dv, int32_t dst_num_pages,
+                                 const int32_t* src_bt, int32_t src_bt_stride, const int32_t* dst_bt,
+                                 int32_t dst_bt_stride, const int32_t* lens, int32_t batch, const int32_t* kept,
+                                 int32_t kept_stride, const int32_t* kept_counts, unsigned* err, cudaStream_t stream) {
+  const int pairs = batch * src.num_kv_heads;
+  const long long rows = (long long)pairs * kept_stride * 2;
+  if (rows == 0) return cudaSuccess;
+  snapkv_gather_kernel<<<(unsigned)((rows + 15) / 16), 256, 0, stream>>>(
+      src, dk, dv, dst_num_pages, src_bt, src_bt_stride, dst_bt, dst_bt_stride, lens, pairs, kept, kept_stride,
+      kept_counts, err);
+  return cudaGetLastError();
+}
+
+}  // namespace se

@@ -244,6 +244,17 @@ def check_window_probabilities(snapkv):
         np.testing.assert_allclose(a.sum(axis=2), np.ones((W, 3)), rtol=1e-13)
 
 
+def check_window_lse(snapkv):
+    rng = _rng(18)
+    for n, W in ((6, 2), (20, 8), (9, 9)):
+        q = rng.standard_normal((W, 2, 5))
+        K = rng.standard_normal((n, 5))
+        z = 0.3 * torch.einsum("wgd,jd->wgj", torch.from_numpy(q), torch.from_numpy(K))
+        mask = torch.ones(n, n, dtype=torch.bool).tril()[n - W:]
+        ref = torch.logsumexp(z.masked_fill(~mask[:, None, :], float("-inf")), dim=-1).numpy()
+        np.testing.assert_allclose(snapkv.window_lse(q, K, 0.3), ref, rtol=1e-12)
+
+
 def check_candidate_scores(snapkv):
     rng = _rng(13)
     n, W, G = 11, 3, 2
@@ -310,5 +321,5 @@ QUEST_CHECKS = [check_summary_bruteforce, check_append_matches_rebuild, check_bo
                 check_select_all_equals_dense, check_single_token_attention, check_empty_request,
                 check_permutation_invariance, check_latent_value_is_key_prefix,
                 check_selection_uses_the_bound]
-SNAPKV_CHECKS = [check_window_probabilities, check_candidate_scores, check_max_pool,
+SNAPKV_CHECKS = [check_window_probabilities, check_window_lse, check_candidate_scores, check_max_pool,
                  check_keep_positions, check_snapkv_head_end_to_end, check_compaction_exact]

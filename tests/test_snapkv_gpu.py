@@ -1,0 +1,180 @@
+"""SnapKV eviction on the GPU against the fp64 oracle (through the C ABI).
+
+Window row log-sum-exps and candidate scores against the oracle's softmax
+definition; kept positions under the selection rule (exempt within 1e-3
+relative of the keep-th pooled score); compaction byte-exact; the selection
+kernel alone on crafted scores (ties, crowded buckets) bit-exact; the full
+32K workload on sampled (request, KV head) pairs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.snapkv as osk
+import sparse_decode_attention_quest_gb300 as se
+from synth import SNAPKV_PREFILL_32K, make_snapkv_inputs
+from tests.parity import exempt
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors(se_lib, cuda_device):
+    se.se_read_device_error(clear=True)
+    yield
+    assert se.se_read_device_error(clear=True) == 0
+
+
+def _run(x, dev, keep=None, pool=None):
+    wl = x.workload
+    keep = wl.keep_topk if keep is None else keep
+    pool = wl.pool_kernel if pool is None else pool
+    k, v = x.k_cache.to(dev), x.v_cache.to(dev)
+    src = se.paged_kv(k, v, None)
+    bt = x.src_block_table.to(dev)
+    lens = torch.tensor(x.prompt_lens, dtype=torch.int32, device=dev)
+    max_len = max(x.prompt_lens)
+    W, G, H, B = wl.window, wl.group, wl.num_kv_heads, wl.batch
+    stride = max(max_len - W, 1)
+    scores = torch.full((B, H, stride), float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full((B, H, W * G), float("nan"), dtype=torch.float32, device=dev)
+    ws = torch.empty(se.se_snapkv_workspace_size(B, H, W, max_len), dtype=torch.uint8, device=dev)
+    qw = x.q_window.to(dev)
+    scale = 1.0 / math.sqrt(wl.head_dim)
+    se.se_snapkv_window_scores(src, qw, bt, lens, max_len, scale, scores, lse, ws)
+    kept = torch.full((B, H, keep + W), -1, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(B, H, dtype=torch.int32, device=dev)
+    se.se_snapkv_select(scores, lens, H, W, max_len, pool, keep, kept, cnt)
+    dk = torch.full((x.dst_num_pages, H, 16, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    dv = torch.full_like(dk, float("nan"))
+    dst = se.paged_kv(dk, dv, None)
+    dbt = x.dst_block_table.to(dev)
+    se.se_snapkv_compact(src, bt, lens, dst, dbt, kept, cnt)
+    torch.cuda.synchronize()
+    return dict(scores=scores.cpu(), lse=lse.cpu(), kept=kept.cpu(), cnt=cnt.cpu(), dk=dk.cpu(), dv=dv.cpu(),
+                ws=ws, src=src, qw=qw, bt=bt, lens=lens, dst=dst, dbt=dbt, scale=scale, keep=keep, pool=pool)
+
+
+def _check_pair(x, res, b, h):
+    wl = x.workload
+    W, G = wl.window, wl.group
+    n = x.prompt_lens[b]
+    ref = osk.snapkv_head(x.q_window[b, :, h * G:(h + 1) * G, :], x.k_cache, x.src_block_table[b], h, n, W,
+                          res["pool"], res["keep"], res["scale"])
+    # row log-sum-exp (fp32 sums of exact bf16 products)
+    np.testing.assert_allclose(res["lse"][b, h].numpy(), ref["lse"].reshape(-1), rtol=0, atol=2e-3)
+    # candidate scores (probability sums, fp32)
+    got = res["scores"][b, h, :n - W].double().numpy()
+    np.testing.assert_allclose(got, ref["scores"], rtol=2e-3, atol=1e-6)
+    # kept positions: exact except candidates within 1e-3 of the keep-th pooled score
+    cnt = int(res["cnt"][b, h])
+    assert cnt == len(ref["kept"]), (cnt, len(ref["kept"]))
+    kept = res["kept"][b, h, :cnt].tolist()
+    assert kept == sorted(set(kept)) and kept[-W:] == list(range(n - W, n))
+    gs, rs = set(kept), set(ref["kept"])
+    for j in range(n - W):
+        if (j in gs) != (j in rs):
+            assert exempt(ref["pooled"][j], ref["threshold"]), (b, h, j, ref["pooled"][j], ref["threshold"])
+    # compaction: kept token t is byte-identical at (dst page t // 16, slot t % 16)
+    src_rows_k = torch.stack([x.k_cache[int(x.src_block_table[b, j // 16]), h, j % 16] for j in kept])
+    src_rows_v = torch.stack([x.v_cache[int(x.src_block_table[b, j // 16]), h, j % 16] for j in kept])
+    dst_k = torch.stack([res["dk"][int(x.dst_block_table[b, t // 16]), h, t % 16] for t in range(cnt)])
+    dst_v = torch.stack([res["dv"][int(x.dst_block_table[b, t // 16]), h, t % 16] for t in range(cnt)])
+    assert torch.equal(src_rows_k.view(torch.int16), dst_k.view(torch.int16))
+    assert torch.equal(src_rows_v.view(torch.int16), dst_v.view(torch.int16))
+
+
+def test_snapkv_oracle_sized_ragged(cuda_device):
+    wl = SNAPKV_PREFILL_32K.scaled(batch=2, prompt_min=700, prompt_max=2600, keep_topk=96)
+    x = make_snapkv_inputs(wl)
+    res = _run(x, cuda_device)
+    for b in range(wl.batch):
+        for h in range(wl.num_kv_heads):
+            _check_pair(x, res, b, h)
+
+
+@pytest.mark.parametrize("pool", [1, 3])
+def test_snapkv_pool_sizes_and_small_windows(cuda_device, pool):
+    wl = SNAPKV_PREFILL_32K.scaled(batch=2, num_q_heads=16, num_kv_heads=4, window=16, prompt_min=300,
+                                   prompt_max=1000, keep_topk=40, seed=8)
+    x = make_snapkv_inputs(wl)
+    res = _run(x, cuda_device, pool=pool)
+    for b in range(wl.batch):
+        for h in range(wl.num_kv_heads):
+            _check_pair(x, res, b, h)
+
+
+@pytest.mark.parametrize("n", [2048, 32])
+def test_snapkv_short_prompts_keep_everything(cuda_device, n):
+    # n - W == keep: every position is kept; n == W: only the window (no candidate).
+    wl = SNAPKV_PREFILL_32K.scaled(batch=2, prompt_min=n, prompt_max=n, keep_topk=2016, seed=9)
+    x = make_snapkv_inputs(wl)
+    res = _run(x, cuda_device)
+    for b in range(wl.batch):
+        for h in range(wl.num_kv_heads):
+            assert int(res["cnt"][b, h]) == n
+            assert res["kept"][b, h, :n].tolist() == list(range(n))
+            _check_pair(x, res, b, h)
+
+
+def test_snapkv_score_and_compact_matches_the_steps(cuda_device):
+    wl = SNAPKV_PREFILL_32K.scaled(batch=2, prompt_min=1500, prompt_max=3000, keep_topk=128, seed=10)
+    x = make_snapkv_inputs(wl)
+    res = _run(x, cuda_device)
+    B, H, W = wl.batch, wl.num_kv_heads, wl.window
+    max_len = max(x.prompt_lens)
+    ws = torch.empty(se.se_snapkv_workspace_size(B, H, W, max_len), dtype=torch.uint8, device=cuda_device)
+    kept = torch.full((B, H, 128 + W), -1, dtype=torch.int32, device=cuda_device)
+    cnt = torch.zeros(B, H, dtype=torch.int32, device=cuda_device)
+    dk = torch.zeros((x.dst_num_pages, H, 16, 128), dtype=torch.bfloat16, device=cuda_device)
+    dv = torch.zeros_like(dk)
+    se.se_snapkv_score_and_compact(res["src"], res["qw"], res["bt"], res["lens"], max_len, wl.pool_kernel, 128,
+                                   res["scale"], se.paged_kv(dk, dv, None), res["dbt"], kept, cnt, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(kept.cpu(), res["kept"]) and torch.equal(cnt.cpu(), res["cnt"])
+    for b in range(B):
+        n_pages = x.dst_pages_per_request[b]
+        idx = x.dst_block_table[b, :n_pages].long()
+        assert torch.equal(dk.cpu()[idx].view(torch.int16), res["dk"][idx].view(torch.int16))
+
+
+@pytest.mark.parametrize("kind", ["distinct", "ties", "flat"])
+def test_snapkv_select_exact_on_crafted_scores(cuda_device, kind):
+    g = torch.Generator().manual_seed(11)
+    W, H = 32, 2
+    lens = [5000, 30000]
+    stride = max(lens) - W
+    if kind == "distinct":
+        s = torch.rand(2, H, stride, generator=g)
+    elif kind == "ties":
+        s = torch.randint(0, 4, (2, H, stride), generator=g).float() * 0.25
+    else:
+        s = torch.full((2, H, stride), 0.125)
+    keep = 2016
+    dev = cuda_device
+    kept = torch.full((2, H, keep + W), -1, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(2, H, dtype=torch.int32, device=dev)
+    se.se_snapkv_select(s.to(dev), torch.tensor(lens, dtype=torch.int32, device=dev), H, W, max(lens), 7, keep,
+                        kept, cnt)
+    torch.cuda.synchronize()
+    for b, n in enumerate(lens):
+        for h in range(H):
+            pooled = osk.max_pool_clipped(s[b, h, :n - W].double().numpy(), 7)
+            ref = osk.keep_positions(pooled, n, W, keep)
+            assert kept[b, h, :int(cnt[b, h])].tolist() == ref, (kind, b, h)
+
+
+def test_snapkv_full_32k_sampled(cuda_device):
+    wl = SNAPKV_PREFILL_32K
+    x = make_snapkv_inputs(wl, device=cuda_device)
+    res = _run(x, cuda_device)
+    xc = x  # inputs stay on the device; copy the sampled pairs' data for the oracle
+    xc.k_cache = x.k_cache.cpu()
+    xc.v_cache = x.v_cache.cpu()
+    xc.q_window = x.q_window.cpu()
+    xc.src_block_table = x.src_block_table.cpu()
+    xc.dst_block_table = x.dst_block_table.cpu()
+    for b, h in ((0, 0), (wl.batch - 1, wl.num_kv_heads - 1), (1, 3)):
+        _check_pair(xc, res, b, h)
