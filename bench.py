@@ -316,6 +316,8 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "e2e": e2e,
     }
+    if rank == 0 and not args.no_extra:
+        result["extra_workloads"] = {"snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, stream)}
     if rank == 0 and not args.no_cpu_baseline:
         try:
             result["cpu_baseline"] = cpu_oracle_throughput(x, cores=args.cpu_cores)
@@ -338,6 +340,61 @@ def _profile_traffic(kernel):
         return rec["bytes_per_launch_full_size"]
     except Exception:
         return None
+
+
+def _snapkv_extra(args, dev, flush, stream):
+    """SnapKV eviction at the end of a 32K prefill (4 requests, 32 q / 8 kv heads): one
+    se_snapkv_score_and_compact call per step (window scores on the tensor cores,
+    pool + top-k, compaction), timed with events; L2 flushed between steps."""
+    import torch
+    import sparse_decode_attention_quest_gb300 as se
+    from synth import SNAPKV_PREFILL_32K, make_snapkv_inputs
+    wl = SNAPKV_PREFILL_32K
+    x = make_snapkv_inputs(wl, device=dev, poison_tail=False)
+    B, H, W, G = wl.batch, wl.num_kv_heads, wl.window, wl.group
+    max_len = max(x.prompt_lens)
+    src = se.paged_kv(x.k_cache, x.v_cache, None)
+    lens = torch.tensor(x.prompt_lens, dtype=torch.int32, device=dev)
+    dk = torch.empty((x.dst_num_pages, H, 16, 128), dtype=torch.bfloat16, device=dev)
+    dv = torch.empty_like(dk)
+    dst = se.paged_kv(dk, dv, None)
+    kept = torch.empty((B, H, wl.keep_topk + W), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, H), dtype=torch.int32, device=dev)
+    ws = torch.empty(se.se_snapkv_workspace_size(B, H, W, max_len), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(wl.head_dim)
+
+    def call():
+        se.se_snapkv_score_and_compact(src, x.q_window, x.src_block_table, lens, max_len, wl.pool_kernel,
+                                       wl.keep_topk, scale, dst, x.dst_block_table, kept, cnt, ws, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.fill_(1.0)
+            call()
+    n = max(5, args.steps // 20)
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            flush.fill_(float(i))
+            pairs[i][0].record(stream)
+            call()
+            pairs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    kbytes = sum(x.prompt_lens) * H * 128 * 2                  # the prompt keys
+    kept_rows = int(cnt.sum().item())
+    gather = kept_rows * 256 * 2 * 2                           # K and V rows read and written
+    flops = 2 * sum(x.prompt_lens) * H * (W * G) * 128 * 2     # two passes of the window x prompt QK^T
+    peak_hbm, _ = _peaks()
+    try:
+        peak_tf = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+    except Exception:
+        peak_tf = 1900.0
+    return {"ms_per_call": ms, "steps": n, "requests_per_s": B / (ms * 1e-3),
+            "keys_read_bytes_per_pass": kbytes, "gather_bytes": gather,
+            "hbm_gbs_two_key_passes": round((2 * kbytes + gather) / (ms * 1e-3) / 1e9, 1),
+            "tensor_tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+            "tensor_frac_of_measured_bf16": round(flops / (ms * 1e-3) / 1e12 / peak_tf, 4)}
 
 
 def _e2e(args, step, x, before, after, stream, flush, dev):
@@ -419,6 +476,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary SnapKV measurement")
+    ap.add_argument("--snapkv-only", action="store_true", help="only the SnapKV measurement (for profiler captures)")
     ap.add_argument("--cpu-cores", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None, help="smaller batch for profiler captures only")
     args = ap.parse_args()
@@ -432,6 +491,12 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.snapkv_only:  # profiler captures of the SnapKV kernels alone (never the reported metric)
+        import torch
+        dev = torch.device("cuda", local_rank)
+        flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4, device=dev)
+        print(json.dumps({"snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, torch.cuda.Stream(dev))}))
         return
     if world > 1:
         import torch

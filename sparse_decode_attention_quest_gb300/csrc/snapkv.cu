@@ -18,11 +18,12 @@
 //               boxes each with 128-byte swizzle, into a 4-stage ring;
 //   warp 1      allocates 256 TMEM columns (two fp32 128x128 accumulators)
 //               and issues the tcgen05.mma (M 128, N 128, K 16) x 8 per tile;
-//   warps 2-5   epilogue: thread r owns TMEM lane r = query row r; it loads
-//               its row of the accumulator, applies the causal mask and the
-//               online max/sum (pass 1) or exp(z - LSE) (pass 2). Pass 2 sums
-//               the columns with a warp transpose-reduce and a fixed-order
-//               merge of the four warps through shared memory (deterministic).
+//   warps 2-9   epilogue, two warps per TMEM lane quarter: a thread owns query
+//               row r (TMEM lane r) and 64 of the tile's 128 columns; it applies
+//               the causal mask (boundary tiles only) and the online max/sum
+//               (pass 1) or exp(z - LSE) (pass 2). Pass 2 sums the columns with
+//               a warp transpose-reduce and a fixed-order merge of the four lane
+//               quarters through shared memory (deterministic).
 // The tiles of all (request, KV head) pairs form one flattened range; every
 // CTA takes an equal slice. Pass 1 writes per-slice partial (max, sum) per row
 // that pass 2 merges.
@@ -37,7 +38,8 @@ constexpr int kPagesPerTile = kTileN / kPageSize;
 constexpr int kHalfBytes = kTileN * 128;      // 128 rows x 128 bytes (64 dims)
 constexpr int kTileBytes = 2 * kHalfBytes;    // 32 KB
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
 constexpr int kMinTilesPerCta = 4;
 constexpr int kTmemCols = 256;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -46,7 +48,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kRingOff = 0;
 constexpr int kQOff = kStages * kTileBytes;
 constexpr int kColOff = kQOff + 2 * kTileBytes;
-constexpr int kPrefixOff = kColOff + 2 * 4 * 128 * 4;
+constexpr int kStatOff = kColOff + 2 * 4 * 128 * 4;   // pass 1: [128 rows][2] (max, sum) of column half 1
+constexpr int kPrefixOff = kStatOff + 128 * 2 * 4;
 
 struct SnapArgs {
   const uint16_t* qwin;  // [B][W][Hq][D]
@@ -75,7 +78,21 @@ __device__ __forceinline__ int find_pair(const int* prefix, int n, int x) {
   return lo;
 }
 
-__device__ __forceinline__ void named_barrier_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void named_barrier_epi() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Row r's log2-domain log-sum-exp of pair p from pass 1's per-slice (max, sum); +inf when the row saw no key.
+__device__ __forceinline__ float merged_lse2(const SnapArgs& a, int p, int r) {
+  const int ns = min(a.pair_ns[p], a.max_slices);
+  const float* pr = a.part + ((size_t)p * a.max_slices * 128 + r) * 2;
+  float M = -INFINITY;
+  for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, pr[(size_t)s2 * 256]);
+  float L = 0.f;
+  for (int s2 = 0; s2 < ns; ++s2) {
+    const float mm = pr[(size_t)s2 * 256];
+    if (mm != -INFINITY) L += pr[(size_t)s2 * 256 + 1] * exp2f(mm - M);
+  }
+  return (L > 0.f) ? M + log2f(L) : INFINITY;
+}
 
 // Tiles of pair (b, h) for the pass: all keys (pass 1) or the candidates only (pass 2).
 __device__ __forceinline__ int pair_tiles(int n, int W, int pass) {
@@ -118,8 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
-      mbar_init(&q_full[i], 128);
+      mbar_init(&acc_empty[i], kEpiThreads);
+      mbar_init(&q_full[i], kEpiThreads);
       mbar_init(&q_empty[i], 1);
     }
     mbar_fence_init();
@@ -248,10 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
       }
     } else {
       // ------------------------------------------------------------ epilogue
-      const int wg = warp & 3;            // TMEM lane group of this warp
-      const int r = wg * 32 + lane;       // query row = TMEM lane
+      const int wg = warp & 3;              // TMEM lane quarter of this warp
+      const int chalf = (warp - 2) >> 2;    // which 64 of the tile's 128 columns
+      const int r = wg * 32 + lane;         // query row = TMEM lane
       const int w_pos = r / a.G, g = r % a.G;
       const bool row_live = r < R;
+      float* stat = reinterpret_cast<float*>(smem + kStatOff);
       int acc_it = 0, seg = 0, tile_ctr = 0;
       for (int p = p_first; p <= p_last; ++p) {
         const int t0 = max(start, prefix[p]) - prefix[p], t1 = min(end, prefix[p + 1]) - prefix[p];
@@ -259,37 +278,29 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
         const int b = p / a.H, h = p % a.H;
         const int n = min(a.lens[b], a.max_len);
         const int qb = seg & 1;
-        // Query row r of this pair into Q buffer qb (128-byte swizzled, zero past R).
+        // Query row r, dims [64 chalf, 64 chalf + 64), into Q buffer qb (swizzled, zero past R).
         if (seg >= 2 && !dead && !mbar_wait(&q_empty[qb], ((seg >> 1) - 1) & 1)) {
           raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
           dead = true;
         }
         {
-          uint8_t* qt = smem + kQOff + qb * kTileBytes;
-          const uint16_t* qrow = a.qwin + (((size_t)b * a.W + w_pos) * (a.H * a.G) + h * a.G + g) * kD;
+          uint8_t* qt = smem + kQOff + qb * kTileBytes + chalf * kHalfBytes;
+          const uint16_t* qrow = a.qwin + (((size_t)b * a.W + w_pos) * (a.H * a.G) + h * a.G + g) * kD + chalf * 64;
 #pragma unroll
-          for (int q16 = 0; q16 < 16; ++q16) {
-            const uint4 v = row_live ? *reinterpret_cast<const uint4*>(qrow + q16 * 8) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(qt + (q16 >> 3) * kHalfBytes + swz128(r, q16 & 7)) = v;
+          for (int q8 = 0; q8 < 8; ++q8) {
+            const uint4 v = row_live ? *reinterpret_cast<const uint4*>(qrow + q8 * 8) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(qt + swz128(r, q8)) = v;
           }
           fence_proxy_async_smem();
           mbar_arrive(&q_full[qb]);
         }
-        // Row statistics: pass 1 accumulates them; pass 2 merges pass 1's slices.
         float m_run = -INFINITY, l_run = 0.f, lse2 = INFINITY;
         if (PASS == 2) {
-          const int ns = min(a.pair_ns[p], a.max_slices);
-          float M = -INFINITY;
-          for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, a.part[(((size_t)p * a.max_slices + s2) * 128 + r) * 2]);
-          float L = 0.f;
-          for (int s2 = 0; s2 < ns; ++s2) {
-            const float mm = a.part[(((size_t)p * a.max_slices + s2) * 128 + r) * 2];
-            if (mm != -INFINITY) L += a.part[(((size_t)p * a.max_slices + s2) * 128 + r) * 2 + 1] * exp2f(mm - M);
-          }
-          lse2 = (L > 0.f) ? M + log2f(L) : INFINITY;  // +inf: the row contributes nothing
-          if (a.row_lse && t0 == 0 && row_live) a.row_lse[(size_t)p * R + r] = (L > 0.f) ? lse2 * kLn2 : -INFINITY;
+          lse2 = merged_lse2(a, p, r);  // +inf: the row contributes nothing
+          if (a.row_lse && t0 == 0 && row_live && chalf == 0)
+            a.row_lse[(size_t)p * R + r] = lse2 != INFINITY ? lse2 * kLn2 : -INFINITY;
         }
-        const int limit = n - a.W + w_pos;  // last visible key of this row
+        const int limit = n - a.W + w_pos;  // last key this row sees
         for (int t = t0; t < t1; ++t, ++acc_it, ++tile_ctr) {
           const int ab = acc_it & 1;
           if (!dead && !mbar_wait(&acc_full[ab], (acc_it >> 1) & 1)) {
@@ -297,38 +308,50 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
             dead = true;
           }
           tc05_fence_after();
-          const int j0 = t * kTileN;
-          float* cs = colsum + (tile_ctr & 1) * 4 * 128 + wg * 128;
-#pragma unroll 1
-          for (int c0 = 0; c0 < kTileN; c0 += 32) {
-            uint32_t raw[32];
-            tmem_ld32(tmem + ((uint32_t)(wg * 32) << 16) + ab * kTileN + c0, raw);
+          const int jc = t * kTileN + chalf * 64;  // first column of this thread's half
+          uint32_t raw[2][32];
+          {
+            const uint32_t row_addr = tmem + ((uint32_t)(wg * 32) << 16) + ab * kTileN + chalf * 64;
+            tmem_ld32(row_addr, raw[0]);
+            tmem_ld32(row_addr + 32, raw[1]);
             tmem_ld_wait();
-            if (PASS == 1) {
-              float mx = -INFINITY;
-              float x[32];
+          }
+          tc05_fence_before();
+          mbar_arrive(&acc_empty[ab]);  // the accumulator can take the next tile's MMA
+          if (PASS == 1) {
+            const bool interior = row_live && jc + 63 <= limit;  // every column visible
+            float x[64];
 #pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const int j = j0 + c0 + c;
-                x[c] = (row_live && j <= limit && j < n) ? __uint_as_float(raw[c]) * a.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x[c]);
-              }
-              const float mn = fmaxf(m_run, mx);
-              if (mn != -INFINITY) {
-                float sum = 0.f;
+            for (int c = 0; c < 64; ++c) {
+              const float z = __uint_as_float(raw[c >> 5][c & 31]) * a.scale_log2;
+              x[c] = (interior || (row_live && jc + c <= limit)) ? z : -INFINITY;
+            }
+            float mx = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) sum += exp2f(x[c] - mn);
-                l_run = l_run * exp2f(m_run - mn) + sum;
-                m_run = mn;
+            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
+            const float mn = fmaxf(m_run, mx);
+            if (mn != -INFINITY) {
+              float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+              for (int c = 0; c < 64; c += 2) {
+                s0 += fast_exp2(x[c] - mn);
+                s1 += fast_exp2(x[c + 1] - mn);
               }
-            } else {
+              l_run = l_run * fast_exp2(m_run - mn) + (s0 + s1);
+              m_run = mn;
+            }
+          } else {
+            float* cs = colsum + (tile_ctr & 1) * 4 * 128 + wg * 128 + chalf * 64;
+            const bool interior = jc + 63 < n - a.W;  // every column a candidate
+#pragma unroll
+            for (int chk = 0; chk < 2; ++chk) {
               float e[32];
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
-                const int j = j0 + c0 + c;
-                e[c] = (j < n - a.W) ? exp2f(__uint_as_float(raw[c]) * a.scale_log2 - lse2) : 0.f;
+                const float v = fast_exp2(__uint_as_float(raw[chk][c]) * a.scale_log2 - lse2);
+                e[c] = (interior || jc + chk * 32 + c < n - a.W) ? v : 0.f;
               }
-              // Warp transpose-reduce: afterwards lane l holds the column c0 + l sum over the warp's rows.
+              // Warp transpose-reduce: afterwards lane l holds column (32 chk + l) summed over the warp's rows.
 #pragma unroll
               for (int k = 0; k < 5; ++k) {
                 const int off = 16 >> k, half = 16 >> k;
@@ -340,29 +363,52 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
                   e[i] = (upper ? hi_v : lo_v) + __shfl_xor_sync(0xffffffffu, send, off);
                 }
               }
-              cs[c0 + lane] = e[0];
+              cs[chk * 32 + lane] = e[0];
             }
-          }
-          tc05_fence_before();
-          mbar_arrive(&acc_empty[ab]);
-          if (PASS == 2) {
-            named_barrier_epi();  // the four warps' column partials of this tile are in
-            const float* cb = colsum + (tile_ctr & 1) * 4 * 128;
-            const int c = wg * 32 + lane;  // one column per epilogue thread
-            const float v = ((cb[c] + cb[128 + c]) + cb[256 + c]) + cb[384 + c];
-            const int j = j0 + c;
-            if (j < n - a.W) a.scores[(size_t)p * a.score_stride + j] = v;
+            named_barrier_epi();  // the lane quarters' column partials of this tile are in
+            const int et = threadIdx.x - 64;  // 0 .. 255
+            if (et < kTileN) {
+              const float* cb = colsum + (tile_ctr & 1) * 4 * 128;
+              const float v = ((cb[et] + cb[128 + et]) + cb[256 + et]) + cb[384 + et];
+              const int j = t * kTileN + et;
+              if (j < n - a.W) a.scores[(size_t)p * a.score_stride + j] = v;
+            }
           }
         }
         if (PASS == 1) {
-          const int first_cta = prefix[p] / per_cta;
-          const int slot = blockIdx.x - first_cta;
-          float* dst = a.part + (((size_t)p * a.max_slices + slot) * 128 + r) * 2;
-          dst[0] = m_run;
-          dst[1] = l_run;
+          // Merge the two column halves of each row, then write this slice's partial.
+          if (chalf == 1) {
+            stat[r * 2] = m_run;
+            stat[r * 2 + 1] = l_run;
+          }
+          named_barrier_epi();
+          if (chalf == 0) {
+            const float m1 = stat[r * 2], l1 = stat[r * 2 + 1];
+            const float M = fmaxf(m_run, m1);
+            float L = 0.f;
+            if (M != -INFINITY) L = l_run * fast_exp2(m_run - M) + l1 * fast_exp2(m1 - M);
+            const int first_cta = prefix[p] / per_cta;
+            const int slot = blockIdx.x - first_cta;
+            float* dst = a.part + (((size_t)p * a.max_slices + slot) * 128 + r) * 2;
+            dst[0] = M;
+            dst[1] = L;
+          }
+          named_barrier_epi();  // stat is reused by the next segment
         }
         ++seg;
       }
+    }
+  }
+  // Pairs whose prompt holds no candidate (n == window) have no pass-2 tile:
+  // CTA 0 writes their row log-sum-exps.
+  if (PASS == 2 && blockIdx.x == 0 && a.row_lse && warp >= 2 && warp < 6) {
+    const int r = (warp & 3) * 32 + lane;
+    for (int p = 0; p < pairs; ++p) {
+      if (prefix[p + 1] != prefix[p] || r >= R) continue;
+      const int n = a.lens[p / a.H];
+      if (n < a.W || n > a.max_len) continue;
+      const float l2 = merged_lse2(a, p, r);
+      a.row_lse[(size_t)p * R + r] = l2 != INFINITY ? l2 * kLn2 : -INFINITY;
     }
   }
   tc05_fence_before();
@@ -376,31 +422,50 @@ constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBuckets = 1024;
 constexpr int kMaxMembers = 1024;
-constexpr int kSelMaxCand = 45056;
+constexpr int kSelPer = 44;                          // candidates per thread
+constexpr int kSelMaxCand = kSelThreads * kSelPer;   // 45056
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ int block_scan_excl(int v, int* wtot, int warp, int lane) {
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
+// Exclusive prefix, in index order, of flagged candidates. Thread t owns
+// candidates t + 1024 e, so index order is (e, warp, lane): per (e, warp)
+// counts from ballots, one prefix over them (warp 0). Afterwards the rank of
+// owned candidate e is cnt[e * 32 + warp] + popc(ballot(flag) & lanes below).
+__device__ __forceinline__ void index_order_prefix(uint64_t flags, int E, int* cnt, int warp, int lane) {
+  for (int e = 0; e < E; ++e) {
+    const unsigned ball = __ballot_sync(0xffffffffu, (flags >> e) & 1ull);
+    if (lane == 0) cnt[e * 32 + warp] = __popc(ball);
   }
-  if (lane == 31) wtot[warp] = incl;
   __syncthreads();
-  int before = incl - v;
-  for (int w = 0; w < warp; ++w) before += wtot[w];
+  if (warp == 0) {
+    const int per = E;  // E * 32 entries over 32 lanes
+    const int lo = lane * per, hi = lo + per;
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += cnt[i];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int run = incl - sum;
+    for (int i = lo; i < hi; ++i) {
+      const int c = cnt[i];
+      cnt[i] = run;
+      run += c;
+    }
+  }
   __syncthreads();
-  return before;
 }
 
 // Max-pool of the scores, then the top `keep` candidates by pooled score (ties:
 // lower position) in ascending order, then the window positions. One CTA per
-// (request, KV head); pooled scores in shared memory.
+// (request, KV head); thread t owns candidates t + 1024 e (coalesced pooling
+// reads, conflict-free shared-memory accesses); pooled scores live in shared
+// memory, per-candidate flags in a 64-bit mask.
 __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ lens, int32_t H, int32_t W,
     int32_t max_len, int32_t pool, int32_t keep, int32_t* __restrict__ kept, int32_t kept_stride,
@@ -411,14 +476,18 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   __shared__ int wtot[kSelWarps];
   __shared__ float mem_val[kMaxMembers];
   __shared__ int mem_idx[kMaxMembers];
+  __shared__ int cnt[kSelPer * 32];
   __shared__ int s_info[4];
   __shared__ int rhist[3][257];
   const int pair = blockIdx.x, b = pair / H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int n = lens[b];
+  const unsigned lt = (1u << lane) - 1u;
+  const int n = lens[b];
   if (n < W || n > max_len) {
-    if (tid == 0) raise_error(err, SE_DEVERR_LENGTH);
-    if (tid == 0) kept_counts[pair] = 0;
+    if (tid == 0) {
+      raise_error(err, SE_DEVERR_LENGTH);
+      kept_counts[pair] = 0;
+    }
     return;
   }
   const int C = n - W;
@@ -429,19 +498,24 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     return;
   }
   const float* sc = scores + (size_t)pair * score_stride;
+  const int E = (C + kSelThreads - 1) / kSelThreads;
   const int half = pool / 2;
-  const int kpt = (C + kSelThreads - 1) / kSelThreads;  // contiguous candidates per thread
-  const int i0 = min(C, tid * kpt), i1 = min(C, i0 + kpt);
   float lmin = INFINITY, lmax = -INFINITY;
-  for (int i = i0; i < i1; ++i) {
-    float m = -INFINITY;
-    for (int t = max(0, i - half); t <= min(C - 1, i + half); ++t) m = fmaxf(m, sc[t]);
-    pooled[i] = m;
-    if (isfinite(m)) {
-      lmin = fminf(lmin, m);
-      lmax = fmaxf(lmax, m);
+  for (int e = 0; e < E; ++e) {
+    const int i = tid + e * kSelThreads;
+    if (i < C) {
+      float m = -INFINITY;
+      for (int t = max(0, i - half); t <= min(C - 1, i + half); ++t) m = fmaxf(m, sc[t]);
+      pooled[i] = m;
+      if (isfinite(m)) {
+        lmin = fminf(lmin, m);
+        lmax = fmaxf(lmax, m);
+      }
     }
   }
+  hist[tid] = 0;
+  if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
+  if (tid == 0) s_info[2] = 0;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     lmin = fminf(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
@@ -451,9 +525,6 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     s_min[warp] = lmin;
     s_max[warp] = lmax;
   }
-  hist[tid] = 0;
-  if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
-  if (tid == 0) s_info[2] = 0;
   __syncthreads();
   float mn = INFINITY, mx = -INFINITY;
   for (int w = 0; w < kSelWarps; ++w) {
@@ -465,7 +536,10 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     if (isfinite(v)) return min(kBuckets - 1, max(0, (int)((v - mn) * scale)));
     return v > 0.f ? kBuckets - 1 : 0;
   };
-  for (int i = i0; i < i1; ++i) atomicAdd(&hist[bucket(pooled[i])], 1);
+  for (int e = 0; e < E; ++e) {
+    const int i = tid + e * kSelThreads;
+    if (i < C) atomicAdd(&hist[bucket(pooled[i])], 1);
+  }
   __syncthreads();
   const int hc = hist[tid];
   int incl = hc;
@@ -485,21 +559,20 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   const int B = s_info[0];
   const int need = keep - s_info[1];
   const int m = hist[B];
-  // Selected members of bucket B are marked by setting the sign bit of an
-  // extra flag array would cost memory; instead the threshold (key T, count of
-  // equal keys to take) is found and applied below.
+  __syncthreads();  // s_info is rewritten below
   uint32_t T;
   int need_eq;
   if (m <= kMaxMembers) {
-    for (int i = i0; i < i1; ++i) {
-      if (bucket(pooled[i]) == B) {
+    for (int e = 0; e < E; ++e) {
+      const int i = tid + e * kSelThreads;
+      if (i < C && bucket(pooled[i]) == B) {
         const int slot = atomicAdd(&s_info[2], 1);
         mem_val[slot] = pooled[i];
         mem_idx[slot] = i;
       }
     }
     __syncthreads();
-    // The member of rank need - 1 (score desc, position asc) sets the threshold.
+    // The member of rank need - 1 (score desc, position asc) fixes the threshold.
     if (tid < m) {
       const uint32_t kv = order_key(mem_val[tid]);
       const int id = mem_idx[tid];
@@ -511,7 +584,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
       }
       if (rank == need - 1) {
         s_info[0] = (int)kv;
-        s_info[1] = need - above;  // keys equal to kv to take, lowest positions first
+        s_info[1] = need - above;
       }
     }
     __syncthreads();
@@ -526,13 +599,15 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
       int* hh = rhist[pass % 3];
       if (pass >= 1)
         for (int i = tid; i < 257; i += kSelThreads) rhist[(pass + 1) % 3][i] = 0;
-      for (int i = i0; i < i1; ++i) {
-        const float v = pooled[i];
-        const uint32_t key = order_key(v);
-        if (bucket(v) == B && (key & mask) == prefix) atomicAdd(&hh[(key >> shift) & 255u], 1);
+      for (int e = 0; e < E; ++e) {
+        const int i = tid + e * kSelThreads;
+        if (i < C) {
+          const float v = pooled[i];
+          const uint32_t key = order_key(v);
+          if (bucket(v) == B && (key & mask) == prefix) atomicAdd(&hh[(key >> shift) & 255u], 1);
+        }
       }
       __syncthreads();
-      // The digit holding the remaining-th largest member key (every warp computes it).
       int g8[8], gsum = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -570,33 +645,30 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     T = prefix;
     need_eq = remaining;
   }
-  // Selection: pooled key above T, or equal to T among the first need_eq (by position).
-  int n_eq = 0;
-  for (int i = i0; i < i1; ++i) n_eq += order_key(pooled[i]) == T ? 1 : 0;
-  int r = block_scan_excl(n_eq, wtot, warp, lane);
-  int n_sel = 0;
-  {
-    int rr = r;
-    for (int i = i0; i < i1; ++i) {
+  // Selected: pooled key above T, or equal to T among the first need_eq by position.
+  uint64_t eqf = 0;
+  for (int e = 0; e < E; ++e) {
+    const int i = tid + e * kSelThreads;
+    if (i < C && order_key(pooled[i]) == T) eqf |= 1ull << e;
+  }
+  index_order_prefix(eqf, E, cnt, warp, lane);
+  uint64_t self = 0;
+  for (int e = 0; e < E; ++e) {
+    const int i = tid + e * kSelThreads;
+    const unsigned ball = __ballot_sync(0xffffffffu, (eqf >> e) & 1ull);
+    const int eq_rank = cnt[e * 32 + warp] + __popc(ball & lt);
+    if (i < C) {
       const uint32_t key = order_key(pooled[i]);
-      if (key > T) ++n_sel;
-      else if (key == T) {
-        if (rr < need_eq) ++n_sel;
-        ++rr;
-      }
+      if (key > T || (key == T && eq_rank < need_eq)) self |= 1ull << e;
     }
   }
-  int pos = block_scan_excl(n_sel, wtot, warp, lane);
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = order_key(pooled[i]);
-    bool take = key > T;
-    if (key == T) {
-      take = r < need_eq;
-      ++r;
-    }
-    if (take) {
-      if (pos < keep) out[pos] = i;
-      ++pos;
+  __syncthreads();  // cnt is reused
+  index_order_prefix(self, E, cnt, warp, lane);
+  for (int e = 0; e < E; ++e) {
+    const unsigned ball = __ballot_sync(0xffffffffu, (self >> e) & 1ull);
+    if ((self >> e) & 1ull) {
+      const int pos = cnt[e * 32 + warp] + __popc(ball & lt);
+      if (pos < keep) out[pos] = tid + e * kSelThreads;
     }
   }
   for (int w = tid; w < W; w += kSelThreads) out[keep + w] = C + w;

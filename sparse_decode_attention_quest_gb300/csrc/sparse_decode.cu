@@ -284,16 +284,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
         const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float c0 = exp2f(m0 - n0), c1 = exp2f(m1 - n1);
+        const float c0 = fast_exp2(m0 - n0), c1 = fast_exp2(m1 - n1);
         m0 = n0;
         m1 = n1;
         float p[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          p[nt][0] = exp2f(sc[nt][0] - n0);
-          p[nt][1] = exp2f(sc[nt][1] - n0);
-          p[nt][2] = exp2f(sc[nt][2] - n1);
-          p[nt][3] = exp2f(sc[nt][3] - n1);
+          p[nt][0] = fast_exp2(sc[nt][0] - n0);
+          p[nt][1] = fast_exp2(sc[nt][1] - n0);
+          p[nt][2] = fast_exp2(sc[nt][2] - n1);
+          p[nt][3] = fast_exp2(sc[nt][3] - n1);
         }
         l0 = l0 * c0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
         l1 = l1 * c1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const float mw = red_m[w * 16 + r];
-        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
         lsum += f * red_l[w * 16 + r];
         acc += f * red_o[((size_t)w * 16 + r) * kHeadDim + d];
       }
@@ -398,14 +398,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   float M = -INFINITY;
   for (int s = 0; s < ns; ++s) M = fmaxf(M, lp[s]);
   float wsum = 0.f;
-  for (int s = 0; s < ns; ++s) wsum += (lp[s] == -INFINITY) ? 0.f : exp2f(lp[s] - M);
+  for (int s = 0; s < ns; ++s) wsum += (lp[s] == -INFINITY) ? 0.f : fast_exp2(lp[s] - M);
   const bool empty_row = !(wsum > 0.f);
   const float inv = empty_row ? 0.f : 1.f / wsum;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int d = lane * 4;
   for (int s = 0; s < ns; ++s) {
     if (lp[s] == -INFINITY) continue;
-    const float f = exp2f(lp[s] - M);
+    const float f = fast_exp2(lp[s] - M);
     const float4 v = *reinterpret_cast<const float4*>(o_part + ((size_t)row * max_splits + s) * kHeadDim + d);
     acc.x += f * v.x;
     acc.y += f * v.y;
