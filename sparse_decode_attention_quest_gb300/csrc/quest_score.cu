@@ -12,10 +12,11 @@
 // Work split: the candidate pages of all requests form one flattened range
 // (request-major). Each CTA takes an equal slice, so ragged lengths balance.
 // The slice is cut at request boundaries into segments. For each segment the
-// CTA first computes P and N of the request together (double-buffered in shared
-// memory); every lane then keeps the multipliers of its own 16-byte chunks in
-// registers. Warps take every eighth page of the segment and load U pages at a
-// time with 16-byte loads straight into registers, so U page blocks per warp
+// CTA first computes P and N of the request together (all threads, the group
+// cut into runs; double-buffered in shared memory); every lane then keeps the
+// multipliers of its own 16-byte chunks in registers. Warps take every eighth
+// page of the segment and load U pages at a time with 16-byte loads straight
+// into registers, so U page blocks per warp
 // are in flight (a page block holds all KV heads of the page, contiguous).
 // A page costs T 16-byte loads and 8 T multiply-adds per lane plus a butterfly
 // reduce-scatter across the KV heads. Scattered page blocks read this way reach
@@ -67,6 +68,24 @@ __device__ __forceinline__ float dot8(const uint4 v, const float (&m)[8], float 
   return acc;
 }
 
+// Runs of query heads the group is cut into for the P/N pre-reduction: about
+// two tasks of (KV head, 8 channels, run) per thread, at most one head per run.
+__host__ __device__ __forceinline__ int pn_slices(int items, int group) {
+  const int s = (2 * kThreads + items - 1) / items;
+  return s < group ? s : group;
+}
+
+// Positive and negative parts of 8 bf16 query values, accumulated.
+__device__ __forceinline__ void add_pos_neg(const uint4 v, float (&P)[8], float (&N)[8]) {
+  const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    P[e] += fmaxf(x[e], 0.f);
+    N[e] += fminf(x[e], 0.f);
+  }
+}
+
 // Warp sums of T per-lane values (one per KV head), stored by the lanes that
 // end up holding them: a butterfly reduce-scatter for T = 1, 2, 4, 8.
 template <int T>
@@ -104,12 +123,16 @@ __device__ __forceinline__ void reduce_and_store(float (&acc)[T], int lane, floa
 // (D = 576, one KV head) every chunk belongs to the one head.
 template <int D, int T, int U, int MIN_BLOCKS>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) score_pages_kernel(const ScoreArgs a) {
+  // The block-table window of 32 pages is refreshed when k0 crosses a multiple
+  // of 32, which k0 (a multiple of U) only hits exactly when U divides 32.
+  static_assert(32 % U == 0, "U must divide 32");
   constexpr bool HEAD_PER_CHUNK = (D == 128);
   extern __shared__ __align__(16) uint8_t smem[];
   const int H = a.kv.num_kv_heads;
   const int chunks = H * D / 4;  // 16-byte chunks per page block
-  float* pn = reinterpret_cast<float*>(smem);                // [2][H][2][D]
-  int* prefix = reinterpret_cast<int*>(pn + 2 * H * 2 * D);  // [batch + 1]
+  float* pn = reinterpret_cast<float*>(smem);                  // [2][H][2][D]
+  float* slice_part = pn + 2 * H * 2 * D;                      // [slices][H][2][D]
+  int* prefix = reinterpret_cast<int*>(slice_part + pn_slices(H * D / 8, a.group) * H * 2 * D);  // [batch + 1]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // Candidate pages per request, then an exclusive prefix (one warp, chunked).
@@ -153,31 +176,45 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) score_pages_kernel(const
   for (int b = b_first; b <= b_last; ++b) {
     const int lo = max(start, prefix[b]), hi = min(end, prefix[b + 1]);  // flattened ids
     if (lo >= hi) continue;
-    // ---- P and N of request b into buffer seg & 1 (all threads); the other
-    // buffer may still be in use by nobody: each lane copies its multipliers
-    // into registers right after the barrier below.
+    // ---- P and N of request b into buffer seg & 1. The group is cut into
+    // `slices` runs of query heads so that every thread has a few independent
+    // loads in flight; slice partials are then added in slice order (fixed
+    // order: the result does not depend on timing). The other buffer may still
+    // be read by nobody: each lane copies its multipliers into registers right
+    // after the barrier below.
     float* buf = pn + (seg & 1) * H * 2 * D;
     const uint16_t* qb = a.q + (size_t)b * H * a.group * D;
-    for (int task = threadIdx.x; task < H * D / 8; task += kThreads) {
-      const int h = task / (D / 8), c0 = (task % (D / 8)) * 8;
+    const int items = H * D / 8;
+    const int slices = pn_slices(items, a.group);
+    for (int task = threadIdx.x; task < items * slices; task += kThreads) {
+      const int it = task % items, sl = task / items;
+      const int h = it / (D / 8), c0 = (it % (D / 8)) * 8;
+      const int g0 = sl * a.group / slices, g1 = (sl + 1) * a.group / slices;
       float P[8], N[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) P[e] = N[e] = 0.f;
-      for (int g = 0; g < a.group; ++g) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qb + (size_t)(h * a.group + g) * D + c0);
-        const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+      const uint16_t* qh = qb + (size_t)h * a.group * D + c0;
+      int g = g0;
+      for (; g + 4 <= g1; g += 4) {
+        uint4 v[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          P[e] += fmaxf(x[e], 0.f);
-          N[e] += fminf(x[e], 0.f);
-        }
+        for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const uint4*>(qh + (size_t)(g + u) * D);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) add_pos_neg(v[u], P, N);
       }
+      for (; g < g1; ++g) add_pos_neg(*reinterpret_cast<const uint4*>(qh + (size_t)g * D), P, N);
+      float* part = slice_part + (size_t)sl * H * 2 * D;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        buf[(h * 2 + 0) * D + c0 + e] = N[e];  // multiplies the min row
-        buf[(h * 2 + 1) * D + c0 + e] = P[e];  // multiplies the max row
+        part[(h * 2 + 0) * D + c0 + e] = N[e];  // multiplies the min row
+        part[(h * 2 + 1) * D + c0 + e] = P[e];  // multiplies the max row
       }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < H * 2 * D; i += kThreads) {
+      float acc = slice_part[i];
+      for (int sl = 1; sl < slices; ++sl) acc += slice_part[(size_t)sl * H * 2 * D + i];
+      buf[i] = acc;
     }
     __syncthreads();
     float mult[T][8];
@@ -249,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) score_pages_kernel(const
 template <int D, int T, int U, int MIN_BLOCKS>
 cudaError_t launch_t(const ScoreArgs& a, int sm_count, cudaStream_t stream) {
   const int H = a.kv.num_kv_heads;
-  const size_t smem = (size_t)2 * H * 2 * D * 4 + (size_t)(a.batch + 1) * 4;
+  const size_t smem = (size_t)(2 + pn_slices(H * D / 8, a.group)) * H * 2 * D * 4 + (size_t)(a.batch + 1) * 4;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(score_pages_kernel<D, T, U, MIN_BLOCKS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -284,14 +321,14 @@ cudaError_t launch_score_pages(const KvView& kv, const uint16_t* q, int32_t num_
   a.score_stride = score_stride;
   a.err = err;
   // U pages in flight per warp keep about 16 16-byte loads per lane outstanding.
-  if (kv.head_dim == 576) return launch_t<576, 5, 3, 1>(a, sm_count, stream);
+  if (kv.head_dim == 576) return launch_t<576, 5, 4, 1>(a, sm_count, stream);
   switch (kv.num_kv_heads) {
     case 1: return launch_t<128, 1, 16, 2>(a, sm_count, stream);
     case 2: return launch_t<128, 2, 8, 2>(a, sm_count, stream);
-    case 3: return launch_t<128, 3, 5, 2>(a, sm_count, stream);
+    case 3: return launch_t<128, 3, 4, 2>(a, sm_count, stream);
     case 4: return launch_t<128, 4, 4, 2>(a, sm_count, stream);
-    case 5: return launch_t<128, 5, 3, 1>(a, sm_count, stream);
-    case 6: return launch_t<128, 6, 3, 1>(a, sm_count, stream);
+    case 5: return launch_t<128, 5, 4, 1>(a, sm_count, stream);
+    case 6: return launch_t<128, 6, 4, 1>(a, sm_count, stream);
     case 7: return launch_t<128, 7, 2, 1>(a, sm_count, stream);
     default: return launch_t<128, 8, 2, 1>(a, sm_count, stream);
   }

@@ -17,7 +17,8 @@ import torch
 import oracle.quest as oq
 import sparse_decode_attention_quest_gb300 as se
 from sparse_decode_attention_quest_gb300.pipeline import QuestDecodeStep, new_summary
-from synth import (QWEN3_30B_A3B_QUEST_128K, QWEN3_4B_QUEST_32K, TINY_QUEST_4K, make_quest_decode_inputs)
+from synth import (MLA_GLM_QUEST_32K, QWEN3_30B_A3B_QUEST_128K, QWEN3_4B_QUEST_32K, TINY_QUEST_4K,
+                   make_quest_decode_inputs)
 from tests.parity import OUT_ATOL, compare_decode, oracle_inputs
 
 pytestmark = pytest.mark.gpu
@@ -280,6 +281,41 @@ def test_full_qwen3_30b_a3b_128k_sampled(cuda_device):
     longest = int(np.argmax(x.seq_lens))
     shortest = int(np.argmin(x.seq_lens))
     compare_decode(x, step, sorted({longest, shortest, 7}), _scale(wl), "qwen3-30b full")
+
+
+# ---------------------------------------------------------------- scores of a large batch, sampled pages
+@pytest.mark.parametrize("hkv,head_dim", [(1, 128), (2, 128), (3, 128), (4, 128), (5, 128), (6, 128), (7, 128),
+                                          (8, 128), (1, 576)])
+def test_scores_on_sampled_pages_of_a_large_batch(cuda_device, hkv, head_dim):
+    """About 100K candidate pages, so that every CTA's slice holds more than 256
+    pages of one request and each scoring warp walks past its first 32-page
+    block-table window; scores of sampled pages (the window edges included)
+    against the oracle bound recomputed from those pages' keys."""
+    if head_dim == 576:
+        wl = MLA_GLM_QUEST_32K.scaled(batch=50, seed=61)
+    else:
+        wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=25, num_kv_heads=hkv, num_q_heads=4 * hkv,
+                                             context_min=64000, context_max=64000, append=False, seed=60 + hkv)
+    x, step, b, a = _prepare(wl, cuda_device, device_gen=True)
+    step.select(x.q, a)
+    torch.cuda.synchronize()
+    scores = step.scores.cpu().numpy()
+    G = wl.num_q_heads // wl.num_kv_heads
+    rng = np.random.default_rng(0)
+    q = x.q.float().cpu().numpy().astype(np.float64)
+    for r in range(wl.batch):
+        n = math.ceil(x.seq_lens_after[r] / wl.page_size)
+        pages = {0, 255, 256, 257, 263, 264, 511, 512, n - 2} | set(rng.integers(0, n - 1, 12).tolist())
+        for p in sorted(pg for pg in pages if 0 <= pg < n - 1):
+            phys = int(x.block_table[r, p])
+            blk = x.k_cache[phys].double().cpu().numpy()          # [Hkv][16][D], a full page
+            for h in range(wl.num_kv_heads):
+                m, M = oq.page_summary(blk[h])
+                qg = q[r, h * G:(h + 1) * G]
+                want = oq.group_page_scores(qg, m[None, :], M[None, :])[0]
+                scale = np.maximum(np.abs(qg * m), np.abs(qg * M)).sum()
+                got = float(scores[r, h, p])
+                assert abs(got - want) <= 2e-5 * scale + 1e-6, (r, h, p, got, want)
 
 
 # ---------------------------------------------------------------- top-k on crafted scores
