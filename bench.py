@@ -69,6 +69,28 @@ def _config(wl, extra=None):
     return c
 
 
+# --------------------------------------------------------------------------- ranks
+def rank_workload(wl, rank):
+    """Replica ``rank`` decodes its own batch: the same recipe, seed offset by 1000 x rank."""
+    return wl if rank == 0 else wl.scaled(seed=wl.seed + 1000 * rank)
+
+
+def max_over_ranks(value, world, device="cpu"):
+    """The largest ``value`` over all ranks (every rank gets it); the identity at world 1."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(batch, world, ms_per_step):
+    """Whole-job tokens/s: every rank decodes ``batch`` requests per step of ``ms_per_step``."""
+    return batch * world / (ms_per_step * 1e-3)
+
+
 # --------------------------------------------------------------------------- bytes
 def algorithmic_bytes(wl, lens_after, counts):
     """Bytes each kernel must move (inputs read once, outputs written once)."""
@@ -83,9 +105,10 @@ def algorithmic_bytes(wl, lens_after, counts):
     b["score"] = cand * H * summary_row + cand * 4 + B * Hq * D * 2 + cand * H * 4
     # top-k: scores in, selection out
     b["topk"] = cand * H * 4 + B * H * (wl.topk_pages + 1) * 4
-    # decode: the selected K and V page blocks + q + bf16 output
+    # decode: the selected K and V page blocks + q + bf16 output (a latent row is key and value at once)
     sel_pages = int(sum(counts))
-    b["decode"] = sel_pages * PAGE * (D + Dv) * 2 + B * Hq * D * 2 + B * Hq * Dv * 2
+    row = D if wl.latent else D + Dv
+    b["decode"] = sel_pages * PAGE * row * 2 + B * Hq * D * 2 + B * Hq * Dv * 2
     return b
 
 
@@ -200,9 +223,7 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    wl = _workload()
-    if rank:
-        wl = wl.scaled(seed=wl.seed + 1000 * rank)  # each replica decodes its own batch
+    wl = rank_workload(_workload(), rank)
     x = make_quest_decode_inputs(wl, device=dev, poison_tail=False)
     max_len = max(x.seq_lens_after)
     step = QuestDecodeStep(x.k_cache, x.v_cache, new_summary(x.k_cache), x.block_table, wl.num_q_heads,
@@ -270,11 +291,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    total_ms = sum(a.elapsed_time(b) for a, b in pairs)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in pairs), world, dev)
     ms_per_step = total_ms / K
     assert se.se_read_device_error() == 0
     counts = step.counts.cpu().flatten().tolist()
@@ -296,7 +313,7 @@ def run_ours(args, rank, world, local_rank):
         e2e = _e2e(args, step, x, before, after, stream, flush, dev)
 
     result = {
-        "metric": METRIC, "value": wl.batch * world / (ms_per_step * 1e-3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": job_throughput(wl.batch, world, ms_per_step), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
         "data": "synthetic (seeded N(0,1) bf16 keys/values/queries, 4 outlier key channels x8 per KV head)",
@@ -317,7 +334,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
     }
     if rank == 0 and not args.no_extra:
-        result["extra_workloads"] = {"snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, stream)}
+        result["extra_workloads"] = {"snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, stream),
+                                     "mla_glm_quest_b64_32k": _mla_extra(args, dev, flush, stream)}
     if rank == 0 and not args.no_cpu_baseline:
         try:
             result["cpu_baseline"] = cpu_oracle_throughput(x, cores=args.cpu_cores)
@@ -395,6 +413,69 @@ def _snapkv_extra(args, dev, flush, stream):
             "hbm_gbs_two_key_passes": round((2 * kbytes + gather) / (ms * 1e-3) / 1e9, 1),
             "tensor_tflops": round(flops / (ms * 1e-3) / 1e12, 1),
             "tensor_frac_of_measured_bf16": round(flops / (ms * 1e-3) / 1e12 / peak_tf, 4)}
+
+
+def _mla_extra(args, dev, flush, stream):
+    """Quest decode over a latent cache: GLM-4.7-Flash-like MLA shape (64 query heads
+    sharing one 576-dim latent row, value = its first 512 dims), 64 requests at 32K,
+    a 2048-token budget. One step = score + top-k + decode, captured in a CUDA graph
+    and replayed (L2 flushed between replays); per-kernel spans from an eager pass."""
+    import torch
+    import sparse_decode_attention_quest_gb300 as se
+    from sparse_decode_attention_quest_gb300.pipeline import QuestDecodeStep, new_summary
+    from synth import MLA_GLM_QUEST_32K, make_quest_decode_inputs
+    wl = MLA_GLM_QUEST_32K
+    x = make_quest_decode_inputs(wl, device=dev, poison_tail=False)
+    max_len = max(x.seq_lens_after)
+    step = QuestDecodeStep(x.k_cache, None, new_summary(x.k_cache), x.block_table, wl.num_q_heads,
+                           wl.topk_pages, max_len, head_dim_v=wl.head_dim_v)
+    lens = torch.tensor(x.seq_lens_after, dtype=torch.int32, device=dev)
+    step.build_summaries(lens)
+    n = max(5, args.steps // 10)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.fill_(1.0)
+            step.run(x.q, lens, stream=stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            flush.fill_(float(i))
+            step.run(x.q, lens, stream=stream, events=evs[i][:4])
+            evs[i][4].record(stream)
+    torch.cuda.synchronize()
+    spans = {k: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+             for j, k in ((1, "score"), (2, "topk"), (3, "decode"))}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        step.run(x.q, lens, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.fill_(1.0)
+            graph.replay()
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            flush.fill_(float(i))
+            pairs[i][0].record(stream)
+            graph.replay()
+            pairs[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert se.se_read_device_error() == 0
+    ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    abytes = algorithmic_bytes(wl, x.seq_lens_after, step.counts.cpu().flatten().tolist())
+    peak, _ = _peaks()
+    kern = {k: {"ms": round(v, 5), "algorithmic_bytes": abytes[k],
+                "gbs": round(abytes[k] / (v * 1e-3) / 1e9, 1),
+                "frac_of_measured_hbm": round(abytes[k] / (v * 1e-3) / 1e9 / peak, 4)} for k, v in spans.items()}
+    step_bytes = abytes["score"] + abytes["topk"] + abytes["decode"]
+    # QK^T over 576 dims and PV over 512 for every selected token and query head
+    flops = 2 * int(step.counts.sum().item()) * PAGE * wl.num_q_heads * (wl.head_dim + wl.head_dim_v)
+    kern["decode"]["tflops"] = round(flops / (spans["decode"] * 1e-3) / 1e12, 1)
+    return {"ms_per_step": ms, "steps": n, "tokens_per_s": wl.batch / (ms * 1e-3),
+            "step_gbs": round(step_bytes / (ms * 1e-3) / 1e9, 1),
+            "step_frac_of_measured_hbm": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4), "kernels": kern,
+            "shape": {"batch": wl.batch, "num_q_heads": wl.num_q_heads, "head_dim": wl.head_dim,
+                      "head_dim_v": wl.head_dim_v, "context": wl.context_max, "topk_pages": wl.topk_pages}}
 
 
 def _e2e(args, step, x, before, after, stream, flush, dev):
@@ -478,6 +559,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary SnapKV measurement")
     ap.add_argument("--snapkv-only", action="store_true", help="only the SnapKV measurement (for profiler captures)")
+    ap.add_argument("--mla-only", action="store_true", help="only the latent-cache measurement (for profiler captures)")
     ap.add_argument("--cpu-cores", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None, help="smaller batch for profiler captures only")
     args = ap.parse_args()
@@ -497,6 +579,12 @@ def main():
         dev = torch.device("cuda", local_rank)
         flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4, device=dev)
         print(json.dumps({"snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, torch.cuda.Stream(dev))}))
+        return
+    if args.mla_only:  # profiler captures of the latent-cache kernels alone (never the reported metric)
+        import torch
+        dev = torch.device("cuda", local_rank)
+        flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4, device=dev)
+        print(json.dumps({"mla_glm_quest_b64_32k": _mla_extra(args, dev, flush, torch.cuda.Stream(dev))}))
         return
     if world > 1:
         import torch

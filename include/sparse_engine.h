@@ -201,8 +201,8 @@ SE_API se_status_t se_quest_select_pages(const se_paged_kv_t* kv, const void* q,
  *   q: bf16 [batch][num_q_heads][head_dim]; out: bf16 [batch][num_q_heads][head_dim_v];
  *   out_lse: fp32 [batch][num_q_heads] or NULL.
  * Shapes: head_dim == head_dim_v == 128 with 1..16 query heads per KV head, or a
- * latent cache (head_dim 576, head_dim_v 512, one KV head, 16..128 query heads
- * in multiples of 16).
+ * latent cache (head_dim 576, head_dim_v 512, one KV head, kv->v == kv->k,
+ * 16..64 query heads in multiples of 16).
  */
 /*
  * se_sparse_decode_plan -- how se_sparse_paged_decode splits the work on the

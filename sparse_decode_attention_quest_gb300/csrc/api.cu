@@ -295,12 +295,14 @@ se_status_t se_sparse_decode_plan(int32_t batch, int32_t num_q_heads, int32_t nu
   if (!nsplit || !pages_per_split || !launches) return fail(SE_ERR_INVALID_ARG, fn, "NULL output");
   if (batch < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads || sel_stride < 1)
     return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
-  if (!(head_dim == 128 && head_dim_v == 128 && num_q_heads / num_kv_heads <= 16))
+  const bool mla = se::mla_decode_supported(num_kv_heads, head_dim, head_dim_v, num_q_heads);
+  if (!(head_dim == 128 && head_dim_v == 128 && num_q_heads / num_kv_heads <= 16) && !mla)
     return fail(SE_ERR_UNSUPPORTED, fn, "shape not implemented");
   DeviceInfo* d = nullptr;
   cudaError_t e = current_device(&d);
   if (e != cudaSuccess) return cuda_fail(fn, e);
-  const se::DecodePlan plan = se::plan_gqa_decode(batch, num_kv_heads, sel_stride, d->sm_count);
+  const se::DecodePlan plan = mla ? se::plan_mla_decode(sel_stride, d->sm_count)
+                                  : se::plan_gqa_decode(batch, num_kv_heads, sel_stride, d->sm_count);
   *nsplit = plan.nsplit;
   *pages_per_split = plan.pages_per_split;
   *launches = batch == 0 ? 0 : 2;  // the decode kernel and the split merge
@@ -310,7 +312,10 @@ se_status_t se_sparse_decode_plan(int32_t batch, int32_t num_q_heads, int32_t nu
 size_t se_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim_v, int32_t sel_stride) {
   if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim_v < 1 || sel_stride < 1) return 0;
-  // The split layout does not depend on the device.
+  // The split layout does not depend on the device. A latent cache is the one
+  // shape with a 512-wide value and one KV head.
+  if (num_kv_heads == 1 && head_dim_v == 512 && se::mla_decode_supported(1, 576, 512, num_q_heads))
+    return round16(se::mla_decode_workspace_bytes(batch, num_q_heads, se::plan_mla_decode(sel_stride, 1)));
   const se::DecodePlan plan = se::plan_gqa_decode(batch, num_kv_heads, sel_stride, 1);
   return round16(se::gqa_decode_workspace_bytes(batch, num_q_heads, head_dim_v, plan));
 }
@@ -334,10 +339,29 @@ se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32
   if (!std::isfinite(sm_scale)) return fail(SE_ERR_INVALID_ARG, fn, "sm_scale not finite");
   const int group = num_q_heads / kv->num_kv_heads;
   const bool gqa = kv->head_dim == 128 && kv->head_dim_v == 128 && group <= 16;
-  if (!gqa) return fail(SE_ERR_UNSUPPORTED, fn, "only head_dim = head_dim_v = 128 with <= 16 query heads per KV head");
+  const bool mla = se::mla_decode_supported(kv->num_kv_heads, kv->head_dim, kv->head_dim_v, num_q_heads);
+  if (!gqa && !mla)
+    return fail(SE_ERR_UNSUPPORTED, fn,
+                "head_dim = head_dim_v = 128 with <= 16 query heads per KV head, or a latent cache (576/512, one "
+                "KV head, 16..64 query heads in multiples of 16)");
+  if (mla && kv->v != kv->k) return fail(SE_ERR_INVALID_ARG, fn, "a latent cache needs kv->v == kv->k");
   DeviceInfo* d = nullptr;
   cudaError_t e = current_device(&d);
   if (e != cudaSuccess) return cuda_fail(fn, e);
+  if (mla) {
+    const se::DecodePlan plan = se::plan_mla_decode(sel_stride, d->sm_count);
+    const size_t need = se::mla_decode_workspace_bytes(batch, num_q_heads, plan);
+    if (workspace_bytes < need) return fail(SE_ERR_WORKSPACE, fn, "workspace too small");
+    if (need > 0 && !workspace) return fail(SE_ERR_INVALID_ARG, fn, "workspace NULL");
+    if ((size_t)batch > se::mla_decode_max_items())
+      return fail(SE_ERR_UNSUPPORTED, fn, "too many requests for one launch");
+    if (batch == 0) return SE_OK;
+    e = se::launch_mla_decode(view_of(kv), static_cast<const uint16_t*>(q), num_q_heads, block_table, bt_stride,
+                              seq_lens, batch, sel_pages, sel_counts, sel_stride, sm_scale,
+                              static_cast<uint16_t*>(out), out_lse, workspace, plan, d->err,
+                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+  }
   const se::DecodePlan plan = se::plan_gqa_decode(batch, kv->num_kv_heads, sel_stride, d->sm_count);
   const size_t need = se::gqa_decode_workspace_bytes(batch, num_q_heads, kv->head_dim_v, plan);
   if (workspace_bytes < need) return fail(SE_ERR_WORKSPACE, fn, "workspace too small");

@@ -64,6 +64,17 @@ cudaError_t launch_gqa_decode(const KvView& kv, const uint16_t* q, int32_t num_q
                               float* out_lse, void* workspace, const DecodePlan& plan, unsigned* err,
                               cudaStream_t stream);
 
+// ---- mla_decode.cu (latent cache: head_dim 576, value = first 512 dims, one KV head)
+bool mla_decode_supported(int num_kv_heads, int head_dim, int head_dim_v, int num_q_heads);
+DecodePlan plan_mla_decode(int32_t sel_stride, int sm_count);
+size_t mla_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, const DecodePlan& plan);
+size_t mla_decode_max_items();
+cudaError_t launch_mla_decode(const KvView& kv, const uint16_t* q, int32_t num_q_heads, const int32_t* block_table,
+                              int32_t bt_stride, const int32_t* seq_lens, int32_t batch, const int32_t* sel_pages,
+                              const int32_t* sel_counts, int32_t sel_stride, float sm_scale, uint16_t* out,
+                              float* out_lse, void* workspace, const DecodePlan& plan, unsigned* err,
+                              cudaStream_t stream);
+
 // ---- snapkv.cu
 int snapkv_max_slices(int max_len);
 size_t snapkv_part_bytes(int pairs, int max_len);

@@ -117,12 +117,20 @@ def test_decode_validation(se_lib):
     wide = _kv(head_dim=576, head_dim_v=512, row_stride_k=576, row_stride_v=576, num_kv_heads=1)
     assert f(ctypes.byref(wide), FAKE, 8, FAKE, 64, FAKE, 2, FAKE, FAKE, 9, 0.1, FAKE, None, FAKE, 1 << 20,
              None) == UNSUPPORTED  # latent cache with 8 query heads
+    assert f(ctypes.byref(wide), FAKE, 128, FAKE, 64, FAKE, 2, FAKE, FAKE, 9, 0.1, FAKE, None, FAKE, 1 << 30,
+             None) == UNSUPPORTED  # latent cache with 128 query heads
+    split = _kv(head_dim=576, head_dim_v=512, row_stride_k=576, row_stride_v=576, num_kv_heads=1)
+    split.v = FAKE + 4096
+    assert f(ctypes.byref(split), FAKE, 64, FAKE, 64, FAKE, 2, FAKE, FAKE, 9, 0.1, FAKE, None, FAKE, 1 << 30,
+             None) == INVALID  # a latent cache reads the value from the key row: v must be k
 
 
 def test_decode_workspace_size(se_lib):
     # slices of >= 16 pages: an item of 257 pages spans at most 18; (Dv + 1) floats per (row, slice)
     # plus one int per row for the per-item slice counts
     assert se_lib.se_sparse_decode_workspace_size(32, 32, 4, 128, 257) == 32 * 32 * 18 * 129 * 4 + 32 * 32 * 4
+    # latent cache (one KV head, 512-wide value): 129 selected pages span at most 10 slices; one int per request
+    assert se_lib.se_sparse_decode_workspace_size(64, 64, 1, 512, 129) == 64 * 64 * 10 * 513 * 4 + 64 * 4
     assert se_lib.se_sparse_decode_workspace_size(-1, 32, 4, 128, 257) == 0
 
 
