@@ -8,7 +8,7 @@ new token (KV write + summary update). bf16 cache, fp32 accumulation.
 
 One step = se_quest_update_summaries + se_quest_score_pages +
 se_quest_topk_pages + se_sparse_paged_decode over the whole batch (one layer).
-Inputs are resident in HBM; L2 is flushed (a 2x L2-sized write) between
+Inputs are resident in HBM; L2 is flushed (a 2x L2-sized write, then a 2x L2 read) between
 steps, outside the timed spans; every step is timed with CUDA events on the
 launching stream.
 
@@ -63,7 +63,8 @@ def _config(wl, extra=None):
          "head_dim": wl.head_dim, "context": [wl.context_min, wl.context_max], "page_size": wl.page_size,
          "topk_pages": wl.topk_pages, "kept_pages_per_kv_head": wl.topk_pages + 1,
          "append_per_step": wl.append, "block_table": "random permutation",
-         "l2": "flushed between timed steps (write of 2x L2 size, outside the events)"}
+         "l2": "flushed between timed steps, outside the events: a write of 2x L2 size, then a read of "
+               "another 2x L2 buffer (no dirty flush lines left behind)"}
     if extra:
         c.update(extra)
     return c
@@ -110,6 +111,23 @@ def algorithmic_bytes(wl, lens_after, counts):
     row = D if wl.latent else D + Dv
     b["decode"] = sel_pages * PAGE * row * 2 + B * Hq * D * 2 + B * Hq * Dv * 2
     return b
+
+
+# --------------------------------------------------------------------------- L2
+class L2Flush:
+    """Between timed steps: write a buffer of twice the L2 size (evicts the step's
+    data), then read a second one of the same size, so that no dirty line of the
+    written buffer is left for the next step's first kernel to write back."""
+
+    def __init__(self, dev):
+        import torch
+        n = 2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4 + 1024
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.ones(n, dtype=torch.float32, device=dev)
+
+    def __call__(self, value):
+        self.w.fill_(value)
+        self.r.sum()
 
 
 # --------------------------------------------------------------------------- clocks
@@ -232,8 +250,7 @@ def run_ours(args, rank, world, local_rank):
     after = torch.tensor(x.seq_lens_after, dtype=torch.int32, device=dev)
     step.build_summaries(before)
     stream = torch.cuda.Stream(device=dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
 
     def one_step(ev=None):
         step.run(x.q, after, x.k_new, x.v_new, before, stream=stream, events=ev)
@@ -241,7 +258,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            flush.fill_(1.0)
+            flush(1.0)
             one_step()
     torch.cuda.synchronize()
     assert se.se_read_device_error() == 0
@@ -254,7 +271,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(K):
-            flush.fill_(float(i))
+            flush(float(i))
             one_step(evs[i][:4])
             evs[i][4].record(stream)
     torch.cuda.synchronize()
@@ -274,7 +291,7 @@ def run_ours(args, rank, world, local_rank):
         step.run(x.q, after, x.k_new, x.v_new, before, stream=stream)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            flush.fill_(1.0)
+            flush(1.0)
             graph.replay()
     pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
@@ -283,7 +300,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(K):
-            flush.fill_(float(i))
+            flush(float(i))
             pairs[i][0].record(stream)
             graph.replay()
             pairs[i][1].record(stream)
@@ -387,13 +404,13 @@ def _snapkv_extra(args, dev, flush, stream):
 
     with torch.cuda.stream(stream):
         for _ in range(3):
-            flush.fill_(1.0)
+            flush(1.0)
             call()
     n = max(5, args.steps // 20)
     pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     with torch.cuda.stream(stream):
         for i in range(n):
-            flush.fill_(float(i))
+            flush(float(i))
             pairs[i][0].record(stream)
             call()
             pairs[i][1].record(stream)
@@ -434,12 +451,12 @@ def _mla_extra(args, dev, flush, stream):
     n = max(5, args.steps // 10)
     with torch.cuda.stream(stream):
         for _ in range(3):
-            flush.fill_(1.0)
+            flush(1.0)
             step.run(x.q, lens, stream=stream)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
     with torch.cuda.stream(stream):
         for i in range(n):
-            flush.fill_(float(i))
+            flush(float(i))
             step.run(x.q, lens, stream=stream, events=evs[i][:4])
             evs[i][4].record(stream)
     torch.cuda.synchronize()
@@ -450,12 +467,12 @@ def _mla_extra(args, dev, flush, stream):
         step.run(x.q, lens, stream=stream)
     with torch.cuda.stream(stream):
         for _ in range(3):
-            flush.fill_(1.0)
+            flush(1.0)
             graph.replay()
     pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     with torch.cuda.stream(stream):
         for i in range(n):
-            flush.fill_(float(i))
+            flush(float(i))
             pairs[i][0].record(stream)
             graph.replay()
             pairs[i][1].record(stream)
@@ -506,14 +523,14 @@ def _e2e(args, step, x, before, after, stream, flush, dev):
                 ev1.record(stream)
 
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush(1.0)
         e2e_step()
     torch.cuda.synchronize()
     n = max(10, args.steps // 4)
     pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for i in range(n):
         with torch.cuda.stream(stream):
-            flush.fill_(float(i))
+            flush(float(i))
         e2e_step(*pairs[i])
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
@@ -577,13 +594,13 @@ def main():
     if args.snapkv_only:  # profiler captures of the SnapKV kernels alone (never the reported metric)
         import torch
         dev = torch.device("cuda", local_rank)
-        flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4, device=dev)
+        flush = L2Flush(dev)
         print(json.dumps({"snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, torch.cuda.Stream(dev))}))
         return
     if args.mla_only:  # profiler captures of the latent-cache kernels alone (never the reported metric)
         import torch
         dev = torch.device("cuda", local_rank)
-        flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4, device=dev)
+        flush = L2Flush(dev)
         print(json.dumps({"mla_glm_quest_b64_32k": _mla_extra(args, dev, flush, torch.cuda.Stream(dev))}))
         return
     if world > 1:

@@ -11,17 +11,24 @@
 //
 // Work split: the candidate pages of all requests form one flattened range
 // (request-major). Each CTA takes an equal slice, so ragged lengths balance.
-// The slice is cut at request boundaries into segments. For each segment the
-// CTA first computes P and N of the request together (all threads, the group
-// cut into runs; double-buffered in shared memory); every lane then keeps the
-// multipliers of its own 16-byte chunks in registers. Warps take every eighth
-// page of the segment and load U pages at a time with 16-byte loads straight
-// into registers, so U page blocks per warp
-// are in flight (a page block holds all KV heads of the page, contiguous).
-// A page costs T 16-byte loads and 8 T multiply-adds per lane plus a butterfly
-// reduce-scatter across the KV heads. Scattered page blocks read this way reach
-// close to full HBM bandwidth on GB300, where one issuing warp feeding a
-// bulk-copy ring is limited by its per-copy issue cost.
+// The slice is cut at request boundaries into segments. Each of the 8 warps
+// takes every eighth page of a segment and streams the pages' summary blocks
+// (all KV heads of a page, contiguous) through its own ring of R stages in
+// shared memory with 16-byte cp.async copies, R - 1 blocks in flight; the
+// physical page ids sit in lanes, two 32-page windows per warp. The first
+// copies of a segment go out before the CTA computes P and N of the request
+// (all threads; double-buffered in shared memory); every lane then keeps its
+// share of the multipliers in registers as MMA operands. The dot product of a
+// page block with the multipliers runs on the m16n8k16 bf16 MMA: for each KV
+// head, B holds the 2 D summary channels as 8 x (2 D / 8) blocks, A the
+// matching multipliers split into a bf16 high part (rows 0-7) and low part
+// (rows 8-15), and the score is the sum of the diagonals of the two 8x8 halves
+// of D (exact bf16 products, fp32 sums; the split keeps about 17 bits of each
+// multiplier). A page of H heads costs H ldmatrix and 2 H MMAs (d 128) plus a
+// butterfly reduce-scatter across the KV heads. On GB300, random 2 KB blocks gathered by
+// every warp through its own ring reach close to the copy bandwidth; loads
+// batched into registers do not, because a warp drains its batch before it
+// issues the next one.
 #include "se_ptx.cuh"
 
 namespace se {
@@ -55,26 +62,6 @@ __device__ __forceinline__ int find_request(const int* prefix, int n, int x) {
   return lo;
 }
 
-// 8 bf16 values (one 16-byte chunk) times 8 fp32 multipliers, accumulated.
-__device__ __forceinline__ float dot8(const uint4 v, const float (&m)[8], float acc) {
-  acc = fmaf(bf16_lo(v.x), m[0], acc);
-  acc = fmaf(bf16_hi(v.x), m[1], acc);
-  acc = fmaf(bf16_lo(v.y), m[2], acc);
-  acc = fmaf(bf16_hi(v.y), m[3], acc);
-  acc = fmaf(bf16_lo(v.z), m[4], acc);
-  acc = fmaf(bf16_hi(v.z), m[5], acc);
-  acc = fmaf(bf16_lo(v.w), m[6], acc);
-  acc = fmaf(bf16_hi(v.w), m[7], acc);
-  return acc;
-}
-
-// Runs of query heads the group is cut into for the P/N pre-reduction: about
-// two tasks of (KV head, 8 channels, run) per thread, at most one head per run.
-__host__ __device__ __forceinline__ int pn_slices(int items, int group) {
-  const int s = (2 * kThreads + items - 1) / items;
-  return s < group ? s : group;
-}
-
 // Positive and negative parts of 8 bf16 query values, accumulated.
 __device__ __forceinline__ void add_pos_neg(const uint4 v, float (&P)[8], float (&N)[8]) {
   const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
@@ -85,6 +72,24 @@ __device__ __forceinline__ void add_pos_neg(const uint4 v, float (&P)[8], float 
     N[e] += fminf(x[e], 0.f);
   }
 }
+
+// Two 8x8 bf16 matrices from shared memory (lanes 0-15 give the row addresses).
+__device__ __forceinline__ void ldmatrix_x2(uint32_t& r0, uint32_t& r1, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+// An fp32 multiplier as the sum of two bf16 values (high part, then the
+// rounded remainder): the pair carries about 17 bits of the mantissa.
+__device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
+  hi = __bfloat162float(__float2bfloat16_rn(x));
+  lo = x - hi;
+}
+
+// Channel of a head's 2 D summary channels (min row, then max row) that the
+// MMA below pairs with k-index k of row n: 8-channel runs, n-major inside each
+// block of 64, so the eight rows of one 8x8 operand matrix are 128 contiguous
+// bytes (conflict-free ldmatrix).
+__device__ __forceinline__ int chan(int k, int n) { return (k >> 3) * 64 + n * 8 + (k & 7); }
 
 // Warp sums of T per-lane values (one per KV head), stored by the lanes that
 // end up holding them: a butterfly reduce-scatter for T = 1, 2, 4, 8.
@@ -118,22 +123,38 @@ __device__ __forceinline__ void reduce_and_store(float (&acc)[T], int lane, floa
   }
 }
 
-// D: head dim; T: 16-byte chunks per lane per page; U: pages in flight per warp.
+// cp.async of 16 bytes into shared memory, and its group bookkeeping.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Lanes per (KV head, 8 channels) item in the P/N pre-reduction: the group's
+// query heads are cut into S runs summed by S adjacent lanes.
+__device__ __forceinline__ int pn_lanes(int group) { return group >= 8 ? 8 : group >= 4 ? 4 : group >= 2 ? 2 : 1; }
+
+// D: head dim; T: 16-byte chunks per lane per page block (= KV heads at d 128);
+// R: ring stages per warp.
 // For D = 128 chunk t of every lane belongs to KV head t; for the latent cache
 // (D = 576, one KV head) every chunk belongs to the one head.
-template <int D, int T, int U, int MIN_BLOCKS>
-__global__ void __launch_bounds__(kThreads, MIN_BLOCKS) score_pages_kernel(const ScoreArgs a) {
-  // The block-table window of 32 pages is refreshed when k0 crosses a multiple
-  // of 32, which k0 (a multiple of U) only hits exactly when U divides 32.
-  static_assert(32 % U == 0, "U must divide 32");
-  constexpr bool HEAD_PER_CHUNK = (D == 128);
+template <int D, int T, int R>
+__global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArgs a) {
+  // Page i + R - 1 is looked up while page i is consumed, inside the two
+  // 32-page block-table windows [base, base + 64) a warp holds.
+  static_assert(R >= 2 && R <= 17, "ring depth");
+  constexpr int kHeads = D == 128 ? T : 1;      // KV heads in a page's summary block
+  constexpr int kKsPerHead = 2 * D / 128;        // MMA k-steps over a head's 2 D channels
+  constexpr int kBlk = kHeads * 2 * D * 2;       // bytes of one page's summary block
+  constexpr int kChunks = kBlk / 16;
   extern __shared__ __align__(16) uint8_t smem[];
   const int H = a.kv.num_kv_heads;
-  const int chunks = H * D / 4;  // 16-byte chunks per page block
-  float* pn = reinterpret_cast<float*>(smem);                  // [2][H][2][D]
-  float* slice_part = pn + 2 * H * 2 * D;                      // [slices][H][2][D]
-  int* prefix = reinterpret_cast<int*>(slice_part + pn_slices(H * D / 8, a.group) * H * 2 * D);  // [batch + 1]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + (size_t)warp * R * kBlk;                            // [warp][R][kBlk]
+  float* pn = reinterpret_cast<float*>(smem + (size_t)kWarps * R * kBlk);    // [2][H][2][D]
+  int* prefix = reinterpret_cast<int*>(pn + 2 * H * 2 * D);                 // [batch + 1]
+  const uint32_t ring_addr = smem_addr(ring);
 
   // Candidate pages per request, then an exclusive prefix (one warp, chunked).
   for (int b = threadIdx.x; b < a.batch; b += kThreads) {
@@ -176,123 +197,175 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) score_pages_kernel(const
   for (int b = b_first; b <= b_last; ++b) {
     const int lo = max(start, prefix[b]), hi = min(end, prefix[b + 1]);  // flattened ids
     if (lo >= hi) continue;
-    // ---- P and N of request b into buffer seg & 1. The group is cut into
-    // `slices` runs of query heads so that every thread has a few independent
-    // loads in flight; slice partials are then added in slice order (fixed
-    // order: the result does not depend on timing). The other buffer may still
-    // be read by nobody: each lane copies its multipliers into registers right
-    // after the barrier below.
-    float* buf = pn + (seg & 1) * H * 2 * D;
-    const uint16_t* qb = a.q + (size_t)b * H * a.group * D;
-    const int items = H * D / 8;
-    const int slices = pn_slices(items, a.group);
-    for (int task = threadIdx.x; task < items * slices; task += kThreads) {
-      const int it = task % items, sl = task / items;
-      const int h = it / (D / 8), c0 = (it % (D / 8)) * 8;
-      const int g0 = sl * a.group / slices, g1 = (sl + 1) * a.group / slices;
-      float P[8], N[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) P[e] = N[e] = 0.f;
-      const uint16_t* qh = qb + (size_t)h * a.group * D + c0;
-      int g = g0;
-      for (; g + 4 <= g1; g += 4) {
-        uint4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const uint4*>(qh + (size_t)(g + u) * D);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) add_pos_neg(v[u], P, N);
-      }
-      for (; g < g1; ++g) add_pos_neg(*reinterpret_cast<const uint4*>(qh + (size_t)g * D), P, N);
-      float* part = slice_part + (size_t)sl * H * 2 * D;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        part[(h * 2 + 0) * D + c0 + e] = N[e];  // multiplies the min row
-        part[(h * 2 + 1) * D + c0 + e] = P[e];  // multiplies the max row
-      }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < H * 2 * D; i += kThreads) {
-      float acc = slice_part[i];
-      for (int sl = 1; sl < slices; ++sl) acc += slice_part[(size_t)sl * H * 2 * D + i];
-      buf[i] = acc;
-    }
-    __syncthreads();
-    float mult[T][8];
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const int j = lane + 32 * t;
-      const bool in = j < chunks;
-      const int h = in ? j / (D / 4) : 0;
-      const int row = in ? (j % (D / 4)) / (D / 8) : 0;
-      const int c0 = in ? (j % (D / 8)) * 8 : 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mult[t][e] = in ? buf[(h * 2 + row) * D + c0 + e] : 0.f;
-    }
-    ++seg;
 
-    // ---- this warp's pages of the segment: lo + warp, lo + warp + 8, ...
+    // ---- this warp's pages of the segment: lo + warp, lo + warp + 8, ...;
+    // their physical ids sit in lanes, two windows of 32 pages.
     const int first = lo + warp;
     const int npages = first < hi ? (hi - first + kWarps - 1) / kWarps : 0;
     const int32_t* bt_row = a.block_table + (size_t)b * a.bt_stride;
     const int p_first = first - prefix[b];  // page id of this warp's first page
-    float* out_b = a.scores + (size_t)b * H * a.score_stride;
-    // Block-table entries for 32 of this warp's pages at a time; the next 32 prefetched.
-    int phys_cur = lane < npages ? bt_row[p_first + kWarps * lane] : -1;
-    int phys_nxt = lane + 32 < npages ? bt_row[p_first + kWarps * (lane + 32)] : -1;
-    for (int k0 = 0; k0 < npages; k0 += U) {
-      if (k0 > 0 && (k0 & 31) == 0) {
-        phys_cur = phys_nxt;
-        phys_nxt = k0 + 32 + lane < npages ? bt_row[p_first + kWarps * (k0 + 32 + lane)] : -1;
-      }
-      uint4 v[U][T];
-      int ph[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        ph[u] = __shfl_sync(0xffffffffu, phys_cur, (k0 + u) & 31);
-        const bool live = k0 + u < npages && ph[u] >= 0 && ph[u] < a.kv.num_pages;
-        const uint4* blk = reinterpret_cast<const uint4*>(a.kv.summary + (size_t)(live ? ph[u] : 0) * H * 2 * D);
+    auto phys_of = [&](int i) { return i < npages ? bt_row[p_first + kWarps * i] : -1; };
+    int base = 0;
+    int ph_cur = phys_of(lane), ph_nxt = phys_of(lane + 32);
+    auto lookup = [&](int i) {
+      const int c = __shfl_sync(0xffffffffu, ph_cur, i & 31), n = __shfl_sync(0xffffffffu, ph_nxt, i & 31);
+      return i < base + 32 ? c : n;
+    };
+    // Copies of page i into stage i % R; a page id outside the pool is not read.
+    auto issue = [&](int i) {
+      const int ph = lookup(i);
+      if (ph >= 0 && ph < a.kv.num_pages) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(a.kv.summary) + (size_t)ph * kBlk;
+        const uint32_t dst = ring_addr + (i % R) * kBlk;
 #pragma unroll
         for (int t = 0; t < T; ++t) {
           const int j = lane + 32 * t;
-          v[u][t] = (live && j < chunks) ? ld_stream_v4(blk + j) : make_uint4(0, 0, 0, 0);
+          if (j < kChunks) cp_async16(dst + j * 16, src + j * 16);
         }
       }
+    };
+    // The first R - 1 pages go out before the pre-reduction below.
+#pragma unroll 1
+    for (int i = 0; i < R - 1; ++i) {
+      if (i < npages) issue(i);
+      cp_async_commit();
+    }
+
+    // ---- P and N of request b into buffer seg & 1. Each (KV head, 8 channels)
+    // item is summed by S adjacent lanes over S runs of the group's query heads
+    // and the runs are added with a fixed butterfly (the result does not depend
+    // on timing). The other buffer may still be read by nobody: each lane copies
+    // its multipliers into registers right after the barrier below.
+    float* buf = pn + (seg & 1) * H * 2 * D;
+    {
+      const uint16_t* qb = a.q + (size_t)b * H * a.group * D;
+      const int S = pn_lanes(a.group);
+      const int tasks = H * (D / 8) * S;
+      for (int t0 = warp * 32; t0 < tasks; t0 += kThreads) {  // warp-uniform
+        const int task = t0 + lane;
+        const bool live = task < tasks;
+        const int it = task / S, sl = task % S;
+        const int h = it / (D / 8), c0 = (it % (D / 8)) * 8;
+        float P[8], N[8];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (k0 + u < npages) {
-          const bool good = ph[u] >= 0 && ph[u] < a.kv.num_pages;
-          if (!good && lane == 0) raise_error(a.err, SE_DEVERR_PAGE_RANGE);
-          float acc[T];
+        for (int e = 0; e < 8; ++e) P[e] = N[e] = 0.f;
+        if (live) {
+          const int g0 = sl * a.group / S, g1 = (sl + 1) * a.group / S;
+          const uint16_t* qh = qb + (size_t)h * a.group * D + c0;
+          int g = g0;
+          for (; g + 4 <= g1; g += 4) {
+            uint4 v[4];
 #pragma unroll
-          for (int t = 0; t < T; ++t) acc[t] = 0.f;
+            for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const uint4*>(qh + (size_t)(g + u) * D);
 #pragma unroll
-          for (int t = 0; t < T; ++t) {
-            if (HEAD_PER_CHUNK) acc[t] = dot8(v[u][t], mult[t], acc[t]);
-            else acc[0] = dot8(v[u][t], mult[t], acc[0]);
+            for (int u = 0; u < 4; ++u) add_pos_neg(v[u], P, N);
           }
-          float* out = out_b + p_first + kWarps * (k0 + u);
-          if (HEAD_PER_CHUNK) {
-            reduce_and_store<T>(acc, lane, out, a.score_stride, good);
-          } else {
-            float r[1] = {acc[0]};
-            reduce_and_store<1>(r, lane, out, a.score_stride, good);
+          for (; g < g1; ++g) add_pos_neg(*reinterpret_cast<const uint4*>(qh + (size_t)g * D), P, N);
+        }
+        for (int o = 1; o < S; o <<= 1) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            P[e] += __shfl_xor_sync(0xffffffffu, P[e], o);
+            N[e] += __shfl_xor_sync(0xffffffffu, N[e], o);
+          }
+        }
+        if (live && sl == 0) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            buf[(h * 2 + 0) * D + c0 + e] = N[e];  // multiplies the min row
+            buf[(h * 2 + 1) * D + c0 + e] = P[e];  // multiplies the max row
           }
         }
       }
     }
+    __syncthreads();
+    // A fragments of the m16n8k16 MMA: row n < 8 holds the high parts and row
+    // n + 8 the low parts of the multipliers of channels chan(k, n); k-step s
+    // of head h covers the head's channels 128 s .. 128 s + 127.
+    uint32_t afrag[kHeads * kKsPerHead][4];
+    {
+      const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h)
+#pragma unroll
+        for (int s = 0; s < kKsPerHead; ++s) {
+          const float* mh = buf + h * 2 * D;
+          float hi[4], lo[4];
+          const int k0 = 16 * s + 2 * t;
+          split_bf16(mh[chan(k0, g)], hi[0], lo[0]);
+          split_bf16(mh[chan(k0 + 1, g)], hi[1], lo[1]);
+          split_bf16(mh[chan(k0 + 8, g)], hi[2], lo[2]);
+          split_bf16(mh[chan(k0 + 9, g)], hi[3], lo[3]);
+          uint32_t* f = afrag[h * kKsPerHead + s];
+          f[0] = pack_bf16x2(hi[0], hi[1]);
+          f[1] = pack_bf16x2(lo[0], lo[1]);
+          f[2] = pack_bf16x2(hi[2], hi[3]);
+          f[3] = pack_bf16x2(lo[2], lo[3]);
+        }
+    }
+    ++seg;
+
+    float* out_b = a.scores + (size_t)b * H * a.score_stride;
+    for (int i = 0; i < npages; ++i) {
+      // Page i has left the first window: rotate; the new window is first
+      // looked up about 32 - R pages later.
+      if (i == base + 32) {
+        base += 32;
+        ph_cur = ph_nxt;
+        ph_nxt = phys_of(base + 32 + lane);
+      }
+      if (i + R - 1 < npages) issue(i + R - 1);
+      cp_async_commit();
+      cp_async_wait<R - 1>();  // page i has landed (this lane's copies)
+      __syncwarp();            // ... and every lane's
+      const int ph = lookup(i);
+      const bool good = ph >= 0 && ph < a.kv.num_pages;
+      if (!good && lane == 0) raise_error(a.err, SE_DEVERR_PAGE_RANGE);
+      // Per head: D = A B with B[k][n] = summary channel chan(k, n); the head's
+      // score is the sum of the diagonal of D's two 8x8 halves (high and low).
+      const uint32_t st = ring_addr + (i % R) * kBlk;
+      float acc[kHeads];
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t hb = st + h * 4 * D;
+#pragma unroll
+        for (int s = 0; s + 1 < kKsPerHead; s += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(b0, b1, b2, b3, hb + s * 256 + (lane >> 3) * 128 + (lane & 7) * 16);
+          const uint32_t* f0 = afrag[h * kKsPerHead + s];
+          const uint32_t* f1 = afrag[h * kKsPerHead + s + 1];
+          mma_bf16_16816(d, f0[0], f0[1], f0[2], f0[3], b0, b1);
+          mma_bf16_16816(d, f1[0], f1[1], f1[2], f1[3], b2, b3);
+        }
+        if (kKsPerHead & 1) {  // the last, unpaired k-step
+          constexpr int s = kKsPerHead - 1;
+          uint32_t b0, b1;
+          ldmatrix_x2(b0, b1, hb + s * 256 + ((lane >> 3) & 1) * 128 + (lane & 7) * 16);
+          const uint32_t* f = afrag[h * kKsPerHead + s];
+          mma_bf16_16816(d, f[0], f[1], f[2], f[3], b0, b1);
+        }
+        const int g = lane >> 2, t = lane & 3;
+        acc[h] = (2 * t == g ? d[0] + d[2] : 0.f) + (2 * t + 1 == g ? d[1] + d[3] : 0.f);
+      }
+      __syncwarp();  // every lane has read stage i % R before it is refilled
+      float* out = out_b + p_first + kWarps * i;
+      reduce_and_store<kHeads>(acc, lane, out, a.score_stride, good);
+    }
+    cp_async_wait<0>();  // nothing of this segment is in flight when the ring is reused
+    __syncwarp();
   }
 }
 
-template <int D, int T, int U, int MIN_BLOCKS>
+template <int D, int T, int R>
 cudaError_t launch_t(const ScoreArgs& a, int sm_count, cudaStream_t stream) {
   const int H = a.kv.num_kv_heads;
-  const size_t smem = (size_t)(2 + pn_slices(H * D / 8, a.group)) * H * 2 * D * 4 + (size_t)(a.batch + 1) * 4;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(score_pages_kernel<D, T, U, MIN_BLOCKS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  score_pages_kernel<D, T, U, MIN_BLOCKS><<<sm_count * MIN_BLOCKS, kThreads, smem, stream>>>(a);
+  constexpr int kBlk = D == 128 ? T * 512 : 2 * D * 2;
+  const size_t smem = (size_t)kWarps * R * kBlk + (size_t)2 * H * 2 * D * 4 + (size_t)(a.batch + 1) * 4;
+  cudaError_t e = cudaFuncSetAttribute(score_pages_kernel<D, T, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  score_pages_kernel<D, T, R><<<sm_count * 2, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -320,17 +393,18 @@ cudaError_t launch_score_pages(const KvView& kv, const uint16_t* q, int32_t num_
   a.scores = scores;
   a.score_stride = score_stride;
   a.err = err;
-  // U pages in flight per warp keep about 16 16-byte loads per lane outstanding.
-  if (kv.head_dim == 576) return launch_t<576, 5, 4, 1>(a, sm_count, stream);
+  // Ring depth per head count: about 96 KB of summary blocks in flight per CTA,
+  // two CTAs per SM.
+  if (kv.head_dim == 576) return launch_t<576, 5, 5>(a, sm_count, stream);
   switch (kv.num_kv_heads) {
-    case 1: return launch_t<128, 1, 16, 2>(a, sm_count, stream);
-    case 2: return launch_t<128, 2, 8, 2>(a, sm_count, stream);
-    case 3: return launch_t<128, 3, 4, 2>(a, sm_count, stream);
-    case 4: return launch_t<128, 4, 4, 2>(a, sm_count, stream);
-    case 5: return launch_t<128, 5, 4, 1>(a, sm_count, stream);
-    case 6: return launch_t<128, 6, 4, 1>(a, sm_count, stream);
-    case 7: return launch_t<128, 7, 2, 1>(a, sm_count, stream);
-    default: return launch_t<128, 8, 2, 1>(a, sm_count, stream);
+    case 1: return launch_t<128, 1, 16>(a, sm_count, stream);
+    case 2: return launch_t<128, 2, 12>(a, sm_count, stream);
+    case 3: return launch_t<128, 3, 8>(a, sm_count, stream);
+    case 4: return launch_t<128, 4, 6>(a, sm_count, stream);
+    case 5: return launch_t<128, 5, 4>(a, sm_count, stream);
+    case 6: return launch_t<128, 6, 4>(a, sm_count, stream);
+    case 7: return launch_t<128, 7, 3>(a, sm_count, stream);
+    default: return launch_t<128, 8, 3>(a, sm_count, stream);
   }
 }
 
