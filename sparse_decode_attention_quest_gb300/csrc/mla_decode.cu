@@ -82,6 +82,7 @@ __device__ __forceinline__ void pair_barrier(int hg) {
 
 template <int HG>
 __global__ void __launch_bounds__(64 * HG, 1) mla_decode_kernel(const MlaArgs a) {
+  pdl_enter();
   constexpr int kThreads = 64 * HG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -359,6 +360,7 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
                                                           const int32_t* __restrict__ item_ns, int32_t batch,
                                                           int32_t Hq, int32_t max_splits, uint16_t* __restrict__ out,
                                                           float* __restrict__ out_lse) {
+  pdl_enter();
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= batch * Hq) return;
   const int lane = threadIdx.x & 31;
@@ -398,7 +400,10 @@ template <int HG>
 cudaError_t launch_hg(const MlaArgs& a, int grid, size_t smem, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  mla_decode_kernel<HG><<<grid, 64 * HG, smem, stream>>>(a);
+  {
+    const cudaError_t le = launch_pdl(mla_decode_kernel<HG>, dim3(grid), dim3(64 * HG), smem, stream, a);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -467,8 +472,11 @@ cudaError_t launch_mla_decode(const KvView& kv, const uint16_t* q, int32_t num_q
     default: e = launch_hg<4>(a, plan.grid, smem, stream); break;
   }
   if (e != cudaSuccess) return e;
-  mla_combine_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(a.o_part, a.lse_part, a.item_ns, batch,
-                                                                     num_q_heads, plan.nsplit, out, out_lse);
+  {
+    const cudaError_t le = launch_pdl(mla_combine_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, stream,
+                                      a.o_part, a.lse_part, a.item_ns, batch, num_q_heads, plan.nsplit, out, out_lse);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

@@ -141,6 +141,7 @@ __device__ __forceinline__ int pn_lanes(int group) { return group >= 8 ? 8 : gro
 // (D = 576, one KV head) every chunk belongs to the one head.
 template <int D, int T, int R>
 __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArgs a) {
+  pdl_enter();
   // Page i + R - 1 is looked up while page i is consumed, inside the two
   // 32-page block-table windows [base, base + 64) a warp holds.
   static_assert(R >= 2 && R <= 17, "ring depth");
@@ -365,7 +366,11 @@ cudaError_t launch_t(const ScoreArgs& a, int sm_count, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(score_pages_kernel<D, T, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  score_pages_kernel<D, T, R><<<sm_count * 2, kThreads, smem, stream>>>(a);
+  {
+    const cudaError_t le = launch_pdl(score_pages_kernel<D, T, R>, dim3(sm_count * 2), dim3(kThreads), smem, stream,
+                                      a);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

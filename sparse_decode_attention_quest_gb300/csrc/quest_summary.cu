@@ -27,6 +27,7 @@ __device__ __forceinline__ int clamp_len(int L, int max_len, unsigned* err) {
 __global__ void __launch_bounds__(kBuildWarps * 32) build_summaries_kernel(
     KvView kv, const int32_t* __restrict__ block_table, int32_t bt_stride, const int32_t* __restrict__ seq_lens,
     int32_t max_seq_len, unsigned* err) {
+  pdl_enter();
   const int b = blockIdx.y;
   const int L = clamp_len(seq_lens[b], max_seq_len, err);
   const int n_pages = (L + kPageSize - 1) / kPageSize;
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(256) append_update_kernel(KvView kv, uint16_t*
                                                             int32_t bt_stride,
                                                             const int32_t* __restrict__ seq_lens_before,
                                                             int32_t batch, unsigned* err) {
+  pdl_enter();
   const int H = kv.num_kv_heads;
   const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (item >= batch * H) return;
@@ -120,8 +122,11 @@ cudaError_t launch_build_summaries(const KvView& kv, const int32_t* block_table,
   const int max_pages = (max_seq_len + kPageSize - 1) / kPageSize;
   if (batch == 0 || max_pages == 0) return cudaSuccess;
   dim3 grid((max_pages + kBuildPagesPerCta - 1) / kBuildPagesPerCta, batch);
-  build_summaries_kernel<<<grid, kBuildWarps * 32, 0, stream>>>(kv, block_table, bt_stride, seq_lens,
-                                                                 max_seq_len, err);
+  {
+    const cudaError_t le = launch_pdl(build_summaries_kernel, dim3(grid), dim3(kBuildWarps * 32), 0, stream, kv,
+                                      block_table, bt_stride, seq_lens, max_seq_len, err);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -131,8 +136,11 @@ cudaError_t launch_append_update(const KvView& kv, uint16_t* k_mut, uint16_t* v_
                                  cudaStream_t stream) {
   const int items = batch * kv.num_kv_heads;
   if (items == 0) return cudaSuccess;
-  append_update_kernel<<<(items + 7) / 8, 256, 0, stream>>>(kv, k_mut, v_mut, k_new, v_new, block_table,
-                                                            bt_stride, seq_lens_before, batch, err);
+  {
+    const cudaError_t le = launch_pdl(append_update_kernel, dim3((items + 7) / 8), dim3(256), 0, stream, kv, k_mut,
+                                      v_mut, k_new, v_new, block_table, bt_stride, seq_lens_before, batch, err);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

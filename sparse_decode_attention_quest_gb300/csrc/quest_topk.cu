@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ seq_lens, int32_t H,
     int32_t max_seq_len, int32_t k, int32_t* __restrict__ out_pages, int32_t* __restrict__ out_counts,
     int32_t sel_stride, unsigned* err) {
+  pdl_enter();
   __shared__ int hist[kBuckets];
   __shared__ float s_min[kTopkWarps], s_max[kTopkWarps];
   __shared__ int wtot[kTopkWarps];
@@ -290,6 +291,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_smem_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ seq_lens, int32_t H,
     int32_t max_seq_len, int32_t k, int32_t* __restrict__ out_pages, int32_t* __restrict__ out_counts,
     int32_t sel_stride, unsigned* err) {
+  pdl_enter();
   extern __shared__ uint32_t keys[];
   __shared__ int hist[257];
   __shared__ int warp_tot[kTopkWarps];
@@ -413,8 +415,12 @@ cudaError_t launch_topk_pages(const float* scores, int32_t score_stride, const i
   if (batch == 0) return cudaSuccess;
   const int max_cand = (max_seq_len + kPageSize - 1) / kPageSize - 1;
   if (max_cand <= kRegMaxCand) {
-    topk_pages_reg_kernel<<<batch * num_kv_heads, kTopkThreads, 0, stream>>>(
-        scores, score_stride, seq_lens, num_kv_heads, max_seq_len, topk, out_pages, out_counts, sel_stride, err);
+    {
+      const cudaError_t le = launch_pdl(topk_pages_reg_kernel, dim3(batch * num_kv_heads), dim3(kTopkThreads), 0,
+                                        stream, scores, score_stride, seq_lens, num_kv_heads, max_seq_len, topk,
+                                        out_pages, out_counts, sel_stride, err);
+      if (le != cudaSuccess) return le;
+    }
     return cudaGetLastError();
   }
   const size_t smem = topk_smem_bytes(max_seq_len);
@@ -423,8 +429,12 @@ cudaError_t launch_topk_pages(const float* scores, int32_t score_stride, const i
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  topk_pages_smem_kernel<<<batch * num_kv_heads, kTopkThreads, smem, stream>>>(
-      scores, score_stride, seq_lens, num_kv_heads, max_seq_len, topk, out_pages, out_counts, sel_stride, err);
+  {
+    const cudaError_t le = launch_pdl(topk_pages_smem_kernel, dim3(batch * num_kv_heads), dim3(kTopkThreads), smem,
+                                      stream, scores, score_stride, seq_lens, num_kv_heads, max_seq_len, topk,
+                                      out_pages, out_counts, sel_stride, err);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

@@ -10,6 +10,19 @@
 
 namespace se {
 
+// Programmatic dependent launch. Every kernel of the library calls pdl_wait()
+// before its first global-memory access: it returns once the work before it
+// in the stream has completed and its writes are visible (at once when the
+// launch did not ask for the overlap), so the order of the stream is kept;
+// only the launch and the start of the CTAs overlap the previous kernel.
+// pdl_launch_dependents() lets the next kernel in the stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -103,6 +103,7 @@ __device__ __forceinline__ int pair_tiles(int n, int W, int pass) {
 template <int PASS>
 __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                    const SnapArgs a) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int pairs = a.B * a.H;
@@ -470,6 +471,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ lens, int32_t H, int32_t W,
     int32_t max_len, int32_t pool, int32_t keep, int32_t* __restrict__ kept, int32_t kept_stride,
     int32_t* __restrict__ kept_counts, unsigned* err) {
+  pdl_enter();
   extern __shared__ float pooled[];  // [C]
   __shared__ int hist[kBuckets];
   __shared__ float s_min[kSelWarps], s_max[kSelWarps];
@@ -685,6 +687,7 @@ __global__ void __launch_bounds__(256) snapkv_gather_kernel(KvView src, uint16_t
                                                             const int32_t* __restrict__ lens, int32_t pairs,
                                                             const int32_t* __restrict__ kept, int32_t kept_stride,
                                                             const int32_t* __restrict__ kept_counts, unsigned* err) {
+  pdl_enter();
   const long long unit = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);  // (pair, t, K|V)
   const int sub = threadIdx.x & 15;
   const long long rows = (long long)pairs * kept_stride * 2;
@@ -763,10 +766,16 @@ cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const KvView& kv, cons
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(snapkv_scores_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  snapkv_scores_kernel<1><<<sm_count, kThreads, smem, stream>>>(kmap, a);
+  {
+    const cudaError_t le = launch_pdl(snapkv_scores_kernel<1>, dim3(sm_count), dim3(kThreads), smem, stream, kmap, a);
+    if (le != cudaSuccess) return le;
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  snapkv_scores_kernel<2><<<sm_count, kThreads, smem, stream>>>(kmap, a);
+  {
+    const cudaError_t le = launch_pdl(snapkv_scores_kernel<2>, dim3(sm_count), dim3(kThreads), smem, stream, kmap, a);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -779,8 +788,12 @@ cudaError_t launch_snapkv_select(const float* scores, int32_t score_stride, cons
   const size_t smem = (size_t)maxc * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(snapkv_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  snapkv_select_kernel<<<batch * num_kv_heads, kSelThreads, smem, stream>>>(
-      scores, score_stride, lens, num_kv_heads, window, max_len, pool, keep, kept, kept_stride, kept_counts, err);
+  {
+    const cudaError_t le = launch_pdl(snapkv_select_kernel, dim3(batch * num_kv_heads), dim3(kSelThreads), smem,
+                                      stream, scores, score_stride, lens, num_kv_heads, window, max_len, pool, keep,
+                                      kept, kept_stride, kept_counts, err);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -791,9 +804,12 @@ cudaError_t launch_snapkv_gather(const KvView& src, uint16_t* dk, uint16_t* dv, 
   const int pairs = batch * src.num_kv_heads;
   const long long rows = (long long)pairs * kept_stride * 2;
   if (rows == 0) return cudaSuccess;
-  snapkv_gather_kernel<<<(unsigned)((rows + 15) / 16), 256, 0, stream>>>(
-      src, dk, dv, dst_num_pages, src_bt, src_bt_stride, dst_bt, dst_bt_stride, lens, pairs, kept, kept_stride,
-      kept_counts, err);
+  {
+    const cudaError_t le = launch_pdl(snapkv_gather_kernel, dim3((unsigned)((rows + 15) / 16)), dim3(256), 0, stream,
+                                      src, dk, dv, dst_num_pages, src_bt, src_bt_stride, dst_bt, dst_bt_stride, lens,
+                                      pairs, kept, kept_stride, kept_counts, err);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

@@ -104,6 +104,7 @@ __device__ __forceinline__ void issue_page(const DecodeArgs& a, uint32_t stage, 
 
 template <bool kHiRows>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const DecodeArgs a) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   int* prefix = reinterpret_cast<int*>(ring + kRingBytes);  // [items + 1]
@@ -388,6 +389,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ item_ns, int32_t batch, int32_t Hq,
                                                       int32_t group, int32_t max_splits, uint16_t* __restrict__ out,
                                                       float* __restrict__ out_lse) {
+  pdl_enter();
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= batch * Hq) return;
   const int lane = threadIdx.x & 31;
@@ -480,17 +482,26 @@ cudaError_t launch_gqa_decode(const KvView& kv, const uint16_t* q, int32_t num_q
   if (a.group > 8) {
     e = cudaFuncSetAttribute(gqa_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    gqa_decode_kernel<true><<<plan.grid, kThreads, smem, stream>>>(a);
+    {
+      const cudaError_t le = launch_pdl(gqa_decode_kernel<true>, dim3(plan.grid), dim3(kThreads), smem, stream, a);
+      if (le != cudaSuccess) return le;
+    }
   } else {
     e = cudaFuncSetAttribute(gqa_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    gqa_decode_kernel<false><<<plan.grid, kThreads, smem, stream>>>(a);
+    {
+      const cudaError_t le = launch_pdl(gqa_decode_kernel<false>, dim3(plan.grid), dim3(kThreads), smem, stream, a);
+      if (le != cudaSuccess) return le;
+    }
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int nrows = batch * num_q_heads;
-  combine_kernel<<<(nrows + 3) / 4, 128, 0, stream>>>(a.o_part, a.lse_part, a.item_ns, batch, num_q_heads, a.group,
-                                                     plan.nsplit, out, out_lse);
+  {
+    const cudaError_t le = launch_pdl(combine_kernel, dim3((nrows + 3) / 4), dim3(128), 0, stream, a.o_part,
+                                      a.lse_part, a.item_ns, batch, num_q_heads, a.group, plan.nsplit, out, out_lse);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
