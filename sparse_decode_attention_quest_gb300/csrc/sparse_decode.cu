@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  int* prefix = reinterpret_cast<int*>(ring + kRingBytes);  // [items + 1]
+  float* red_ml = reinterpret_cast<float*>(ring + kRingBytes);       // [2][kWarps][16]: (m, l) per warp and row
+  int* prefix = reinterpret_cast<int*>(red_ml + 2 * kWarps * 16);    // [items + 1]
   const int H = a.num_kv_heads, G = a.group, Hq = H * G;
   const int items = a.batch * H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -154,61 +155,79 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
   if (start >= end) return;
 
   const uint32_t wring = smem_addr(ring) + warp * kWarpRing;
+  // This warp's state at the end of a segment waits for the merge in the last
+  // stage of its ring (16 rows x 128 fp32 = one stage); the next segment's
+  // prologue only fills the other stages, so its copies are in flight while
+  // the CTA merges the previous segment.
+  float* my_red = reinterpret_cast<float*>(ring + warp * kWarpRing + (kStages - 1) * kPageBytes);
   const int g = lane >> 2, t = lane & 3;
   const int i_first = find_item(prefix, items, start);
   const int i_last = find_item(prefix, items, end - 1);
-  for (int item = i_first; item <= i_last; ++item) {
-    const int p0 = prefix[item];
-    const int lo = max(start, p0) - p0, hi = min(end, prefix[item + 1]) - p0;  // item-local pages
-    if (lo >= hi) continue;
-    const int b = item / H, h = item % H;
-    int L = a.seq_lens[b];
+  auto nonempty_from = [&](int it) {
+    for (; it <= i_last; ++it)
+      if (max(start, prefix[it]) < min(end, prefix[it + 1])) return it;
+    return -1;
+  };
+
+  // Per-segment values (the segment = this CTA's pages of one item).
+  int item = nonempty_from(i_first);
+  int b = 0, h = 0, n_b = 0, L = 0, np = 0;
+  const int32_t* sel_row = nullptr;
+  const int32_t* bt_row = nullptr;
+  int base = 0, ph_cur = 0, va_cur = 0, ph_nxt = 0, va_nxt = 0;
+  uint32_t qa[8][4];
+  // Metadata of page k of this warp (physical page, valid tokens), one page per lane.
+  auto meta = [&](int k, int& phys, int& valid) {
+    phys = 0;
+    valid = 0;
+    if (k < np) {
+      const int logical = sel_row[kWarps * k];
+      if (logical >= 0 && logical < n_b) {
+        const int ph = bt_row[logical];
+        if (ph >= 0 && ph < a.num_pages) {
+          phys = ph;
+          valid = min(kPageSize, L - logical * kPageSize);
+        } else {
+          raise_error(a.err, SE_DEVERR_PAGE_RANGE);
+        }
+      } else {
+        raise_error(a.err, SE_DEVERR_LENGTH);
+      }
+    }
+  };
+  // Two batches of 32 pages: [base, base + 32) in *_cur, the next 32 in *_nxt.
+  auto lookup = [&](int k, int& phys, int& valid) {
+    const int pc = __shfl_sync(0xffffffffu, ph_cur, k & 31), vc = __shfl_sync(0xffffffffu, va_cur, k & 31);
+    const int pn = __shfl_sync(0xffffffffu, ph_nxt, k & 31), vn = __shfl_sync(0xffffffffu, va_nxt, k & 31);
+    const bool in_cur = k < base + 32;
+    phys = in_cur ? pc : pn;
+    valid = in_cur ? vc : vn;
+  };
+  // Opens segment `it`: its values, metadata windows, the first kStages - 1
+  // pages in flight (stages 0 .. kStages - 2) and the query fragments.
+  auto open_segment = [&](int it) {
+    const int p0 = prefix[it];
+    const int lo = max(start, p0) - p0, hi = min(end, prefix[it + 1]) - p0;  // item-local pages
+    b = it / H;
+    h = it % H;
+    L = a.seq_lens[b];
     if (L < 0) {
       if (lane == 0) raise_error(a.err, SE_DEVERR_LENGTH);
       L = 0;
     }
-    int n_b = (L + kPageSize - 1) / kPageSize;
+    n_b = (L + kPageSize - 1) / kPageSize;
     if (n_b > a.bt_stride) {
       if (lane == 0) raise_error(a.err, SE_DEVERR_LENGTH);
       n_b = a.bt_stride;
       L = n_b * kPageSize;
     }
-    // This warp's pages of the segment: lo + warp + 4 k, k < np.
-    const int np = (hi - lo > warp) ? (hi - lo - warp + kWarps - 1) / kWarps : 0;
-    const int32_t* sel_row = a.sel + (size_t)item * a.sel_stride + lo + warp;
-    const int32_t* bt_row = a.block_table + (size_t)b * a.bt_stride;
-    // Metadata of page k (physical page, valid tokens), one page per lane.
-    auto meta = [&](int k, int& phys, int& valid) {
-      phys = 0;
-      valid = 0;
-      if (k < np) {
-        const int logical = sel_row[kWarps * k];
-        if (logical >= 0 && logical < n_b) {
-          const int ph = bt_row[logical];
-          if (ph >= 0 && ph < a.num_pages) {
-            phys = ph;
-            valid = min(kPageSize, L - logical * kPageSize);
-          } else {
-            raise_error(a.err, SE_DEVERR_PAGE_RANGE);
-          }
-        } else {
-          raise_error(a.err, SE_DEVERR_LENGTH);
-        }
-      }
-    };
-    // Two batches of 32 pages: [base, base + 32) in *_cur, the next 32 in *_nxt.
-    int base = 0, ph_cur, va_cur, ph_nxt, va_nxt;
+    // This warp's pages of the segment: lo + warp + kWarps k, k < np.
+    np = (hi - lo > warp) ? (hi - lo - warp + kWarps - 1) / kWarps : 0;
+    sel_row = a.sel + (size_t)it * a.sel_stride + lo + warp;
+    bt_row = a.block_table + (size_t)b * a.bt_stride;
+    base = 0;
     meta(lane, ph_cur, va_cur);
     meta(lane + 32, ph_nxt, va_nxt);
-    auto lookup = [&](int k, int& phys, int& valid) {
-      const int pc = __shfl_sync(0xffffffffu, ph_cur, k & 31), vc = __shfl_sync(0xffffffffu, va_cur, k & 31);
-      const int pn = __shfl_sync(0xffffffffu, ph_nxt, k & 31), vn = __shfl_sync(0xffffffffu, va_nxt, k & 31);
-      const bool in_cur = k < base + 32;
-      phys = in_cur ? pc : pn;
-      valid = in_cur ? vc : vn;
-    };
-
-    // Prologue: the first kStages - 1 pages in flight, then the query fragments.
 #pragma unroll
     for (int k = 0; k < kStages - 1; ++k) {
       if (k < np) {
@@ -218,20 +237,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
       }
       cp_async_commit();
     }
-    uint32_t qa[8][4];
-    {
-      const uint16_t* qrow0 = a.q + ((size_t)b * Hq + h * G + g) * kHeadDim;
-      const uint16_t* qrow1 = a.q + ((size_t)b * Hq + h * G + g + 8) * kHeadDim;
-      const bool r0 = g < G, r1 = kHiRows && (g + 8 < G);
+    const uint16_t* qrow0 = a.q + ((size_t)b * Hq + h * G + g) * kHeadDim;
+    const uint16_t* qrow1 = a.q + ((size_t)b * Hq + h * G + g + 8) * kHeadDim;
+    const bool r0 = g < G, r1 = kHiRows && (g + 8 < G);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int c = ks * 16 + 2 * t;
-        qa[ks][0] = r0 ? *reinterpret_cast<const uint32_t*>(qrow0 + c) : 0u;
-        qa[ks][2] = r0 ? *reinterpret_cast<const uint32_t*>(qrow0 + c + 8) : 0u;
-        qa[ks][1] = r1 ? *reinterpret_cast<const uint32_t*>(qrow1 + c) : 0u;
-        qa[ks][3] = r1 ? *reinterpret_cast<const uint32_t*>(qrow1 + c + 8) : 0u;
-      }
+    for (int ks = 0; ks < 8; ++ks) {
+      const int c = ks * 16 + 2 * t;
+      qa[ks][0] = r0 ? *reinterpret_cast<const uint32_t*>(qrow0 + c) : 0u;
+      qa[ks][2] = r0 ? *reinterpret_cast<const uint32_t*>(qrow0 + c + 8) : 0u;
+      qa[ks][1] = r1 ? *reinterpret_cast<const uint32_t*>(qrow1 + c) : 0u;
+      qa[ks][3] = r1 ? *reinterpret_cast<const uint32_t*>(qrow1 + c + 8) : 0u;
     }
+  };
+
+  open_segment(item);
+  while (true) {
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[16][4];
 #pragma unroll
@@ -323,32 +343,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
       }
       __syncwarp();  // every lane is done with this stage before it is refilled
     }
-    cp_async_wait<0>();
+    cp_async_wait<0>();  // every copy of this warp has landed: the ring is idle
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-    // ---- merge the four warps' states (the rings are idle: reuse them)
-    __syncthreads();
-    float* red_m = reinterpret_cast<float*>(ring);  // [4][16]
-    float* red_l = red_m + kWarps * 16;             // [4][16]
-    float* red_o = red_l + kWarps * 16;             // [4][16][128]
     if (t == 0) {
-      red_m[warp * 16 + g] = m0;
-      red_l[warp * 16 + g] = l0;
-      red_m[warp * 16 + g + 8] = m1;
-      red_l[warp * 16 + g + 8] = l1;
+      red_ml[warp * 16 + g] = m0;
+      red_ml[kWarps * 16 + warp * 16 + g] = l0;
+      red_ml[warp * 16 + g + 8] = m1;
+      red_ml[kWarps * 16 + warp * 16 + g + 8] = l1;
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      *reinterpret_cast<float2*>(red_o + ((size_t)warp * 16 + g) * kHeadDim + j * 8 + 2 * t) =
-          make_float2(o[j][0], o[j][1]);
-      *reinterpret_cast<float2*>(red_o + ((size_t)warp * 16 + g + 8) * kHeadDim + j * 8 + 2 * t) =
-          make_float2(o[j][2], o[j][3]);
+      *reinterpret_cast<float2*>(my_red + g * kHeadDim + j * 8 + 2 * t) = make_float2(o[j][0], o[j][1]);
+      *reinterpret_cast<float2*>(my_red + (g + 8) * kHeadDim + j * 8 + 2 * t) = make_float2(o[j][2], o[j][3]);
     }
-    __syncthreads();
-    const int cnt = prefix[item + 1] - p0;
+    // The segment's values are needed by the merge after the next one opens.
+    const int cur = item, cur_b = b, cur_h = h;
+    const int next = nonempty_from(item + 1);
+    if (next >= 0) open_segment(next);
+    __syncthreads();  // every warp's state is staged
+
+    // ---- merge the warps' states of segment `cur`
+    const int p0 = prefix[cur];
+    const int cnt = prefix[cur + 1] - p0;
     const int first_cta = p0 / per_cta;
     const int ns = (p0 + cnt - 1) / per_cta - first_cta + 1;
     const int slot = blockIdx.x - first_cta;
@@ -356,19 +375,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
       const int r = idx / kHeadDim, d = idx % kHeadDim;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * 16 + r]);
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_ml[w * 16 + r]);
       float lsum = 0.f, acc = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float mw = red_m[w * 16 + r];
+        const float mw = red_ml[w * 16 + r];
         const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-        lsum += f * red_l[w * 16 + r];
-        acc += f * red_o[((size_t)w * 16 + r) * kHeadDim + d];
+        lsum += f * red_ml[kWarps * 16 + w * 16 + r];
+        const float* wred = reinterpret_cast<const float*>(ring + w * kWarpRing + (kStages - 1) * kPageBytes);
+        acc += f * wred[r * kHeadDim + d];
       }
       const bool empty_row = !(lsum > 0.f);
       const float val = empty_row ? 0.f : acc / lsum;
       const float lse2 = empty_row ? -INFINITY : M + log2f(lsum);
-      const size_t row = (size_t)b * Hq + h * G + r;
+      const size_t row = (size_t)cur_b * Hq + cur_h * G + r;
       if (ns == 1) {
         a.out[row * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
         if (a.out_lse && d == 0) a.out_lse[row] = lse2 * kLn2;
@@ -377,7 +397,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
         if (d == 0) a.lse_part[row * a.max_splits + slot] = lse2;
       }
     }
-    __syncthreads();  // the rings are refilled by the next segment
+    __syncthreads();  // the staged states are read: the last stages may be refilled
+    if (next < 0) break;
+    item = next;
   }
 }
 
@@ -421,7 +443,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   if (out_lse && lane == 0) out_lse[row] = empty_row ? -INFINITY : (M + log2f(wsum)) * kLn2;
 }
 
-size_t decode_smem_bytes(int items) { return (size_t)kRingBytes + 1024 + (size_t)(items + 1) * 4; }
+size_t decode_smem_bytes(int items) {
+  return (size_t)kRingBytes + 1024 + 2 * kWarps * 16 * 4 + (size_t)(items + 1) * 4;
+}
 
 }  // namespace
 
@@ -441,7 +465,7 @@ size_t gqa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t he
   return ((part + 15) & ~size_t(15)) + rows * sizeof(int32_t);  // + item_ns (at most one per row)
 }
 
-size_t gqa_decode_max_items() { return (227 * 1024 - (size_t)kRingBytes - 1024) / 4 - 1; }
+size_t gqa_decode_max_items() { return (227 * 1024 - (size_t)kRingBytes - 1024 - 2 * kWarps * 16 * 4) / 4 - 1; }
 
 cudaError_t launch_gqa_decode(const KvView& kv, const uint16_t* q, int32_t num_q_heads, const int32_t* block_table,
                               int32_t bt_stride, const int32_t* seq_lens, int32_t batch, const int32_t* sel_pages,
