@@ -351,8 +351,10 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
     }
     if rank == 0 and not args.no_extra:
-        result["extra_workloads"] = {"snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, stream),
-                                     "mla_glm_quest_b64_32k": _mla_extra(args, dev, flush, stream)}
+        result["extra_workloads"] = {
+            "snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, stream),
+            "mla_glm_quest_b64_32k": _mla_extra(args, dev, flush, stream),
+            "qwen3_30b_a3b_quest_sink64_recent512_b32_128k": _windows_extra(args, dev, flush, stream)}
     if rank == 0 and not args.no_cpu_baseline:
         try:
             result["cpu_baseline"] = cpu_oracle_throughput(x, cores=args.cpu_cores)
@@ -432,39 +434,42 @@ def _snapkv_extra(args, dev, flush, stream):
             "tensor_frac_of_measured_bf16": round(flops / (ms * 1e-3) / 1e12 / peak_tf, 4)}
 
 
-def _mla_extra(args, dev, flush, stream):
-    """Quest decode over a latent cache: GLM-4.7-Flash-like MLA shape (64 query heads
-    sharing one 576-dim latent row, value = its first 512 dims), 64 requests at 32K,
-    a 2048-token budget. One step = score + top-k + decode, captured in a CUDA graph
-    and replayed (L2 flushed between replays); per-kernel spans from an eager pass."""
+def _quest_extra(args, dev, flush, stream, wl, sink=0, recent=0):
+    """One Quest decode step of workload ``wl`` (append if the workload appends, score, top-k
+    with the keep windows ``sink``/``recent``, decode), captured in a CUDA graph and replayed
+    (L2 flushed between replays); per-kernel spans from an eager pass."""
     import torch
     import sparse_decode_attention_quest_gb300 as se
     from sparse_decode_attention_quest_gb300.pipeline import QuestDecodeStep, new_summary
-    from synth import MLA_GLM_QUEST_32K, make_quest_decode_inputs
-    wl = MLA_GLM_QUEST_32K
+    from synth import make_quest_decode_inputs
     x = make_quest_decode_inputs(wl, device=dev, poison_tail=False)
     max_len = max(x.seq_lens_after)
-    step = QuestDecodeStep(x.k_cache, None, new_summary(x.k_cache), x.block_table, wl.num_q_heads,
-                           wl.topk_pages, max_len, head_dim_v=wl.head_dim_v)
-    lens = torch.tensor(x.seq_lens_after, dtype=torch.int32, device=dev)
-    step.build_summaries(lens)
+    step = QuestDecodeStep(x.k_cache, x.v_cache, new_summary(x.k_cache), x.block_table, wl.num_q_heads,
+                           wl.topk_pages, max_len, head_dim_v=wl.head_dim_v, sink_tokens=sink, recent_tokens=recent)
+    before = torch.tensor(x.seq_lens, dtype=torch.int32, device=dev)
+    after = torch.tensor(x.seq_lens_after, dtype=torch.int32, device=dev)
+    step.build_summaries(before)
+    if wl.append:
+        run = lambda ev=None: step.run(x.q, after, x.k_new, x.v_new, before, stream=stream, events=ev)
+    else:
+        run = lambda ev=None: step.run(x.q, after, stream=stream, events=ev)
     n = max(5, args.steps // 10)
     with torch.cuda.stream(stream):
         for _ in range(3):
             flush(1.0)
-            step.run(x.q, lens, stream=stream)
+            run()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
     with torch.cuda.stream(stream):
         for i in range(n):
             flush(float(i))
-            step.run(x.q, lens, stream=stream, events=evs[i][:4])
+            run(evs[i][:4])
             evs[i][4].record(stream)
     torch.cuda.synchronize()
     spans = {k: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
-             for j, k in ((1, "score"), (2, "topk"), (3, "decode"))}
+             for j, k in ((0, "append"), (1, "score"), (2, "topk"), (3, "decode"))}
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
-        step.run(x.q, lens, stream=stream)
+        run()
     with torch.cuda.stream(stream):
         for _ in range(3):
             flush(1.0)
@@ -482,17 +487,37 @@ def _mla_extra(args, dev, flush, stream):
     abytes = algorithmic_bytes(wl, x.seq_lens_after, step.counts.cpu().flatten().tolist())
     peak, _ = _peaks()
     kern = {k: {"ms": round(v, 5), "algorithmic_bytes": abytes[k],
-                "gbs": round(abytes[k] / (v * 1e-3) / 1e9, 1),
-                "frac_of_measured_hbm": round(abytes[k] / (v * 1e-3) / 1e9 / peak, 4)} for k, v in spans.items()}
-    step_bytes = abytes["score"] + abytes["topk"] + abytes["decode"]
-    # QK^T over 576 dims and PV over 512 for every selected token and query head
-    flops = 2 * int(step.counts.sum().item()) * PAGE * wl.num_q_heads * (wl.head_dim + wl.head_dim_v)
+                "gbs": round(abytes[k] / (v * 1e-3) / 1e9, 1) if v > 0 else 0.0,
+                "frac_of_measured_hbm": round(abytes[k] / (v * 1e-3) / 1e9 / peak, 4) if v > 0 else 0.0}
+            for k, v in spans.items() if abytes[k] > 0}
+    step_bytes = sum(abytes.values())
+    # QK^T over head_dim and PV over head_dim_v for every selected token and query head
+    G = wl.num_q_heads // wl.num_kv_heads
+    flops = 2 * int(step.counts.sum().item()) * PAGE * G * (wl.head_dim + wl.head_dim_v)
     kern["decode"]["tflops"] = round(flops / (spans["decode"] * 1e-3) / 1e12, 1)
     return {"ms_per_step": ms, "steps": n, "tokens_per_s": wl.batch / (ms * 1e-3),
             "step_gbs": round(step_bytes / (ms * 1e-3) / 1e9, 1),
             "step_frac_of_measured_hbm": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4), "kernels": kern,
-            "shape": {"batch": wl.batch, "num_q_heads": wl.num_q_heads, "head_dim": wl.head_dim,
-                      "head_dim_v": wl.head_dim_v, "context": wl.context_max, "topk_pages": wl.topk_pages}}
+            "kept_pages_per_kv_head": round(float(step.counts.float().mean().item()), 2),
+            "shape": {"workload": wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
+                      "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "head_dim_v": wl.head_dim_v,
+                      "context": [wl.context_min, wl.context_max], "topk_pages": wl.topk_pages,
+                      "sink_tokens": sink, "recent_tokens": recent, "append": wl.append}}
+
+
+def _mla_extra(args, dev, flush, stream):
+    """Quest decode over a latent cache: GLM-4.7-Flash-like MLA shape (64 query heads sharing
+    one 576-dim latent row, value = its first 512 dims), 64 requests at 32K, a 2,048-token
+    budget."""
+    from synth import MLA_GLM_QUEST_32K
+    return _quest_extra(args, dev, flush, stream, MLA_GLM_QUEST_32K)
+
+
+def _windows_extra(args, dev, flush, stream):
+    """The 128K workload with the decode-time keep windows of the throughput runs: sink 64,
+    recent 512, 1,472 selected tokens (92 pages), 2,048 kept in total."""
+    from synth import QWEN3_30B_A3B_QUEST_128K
+    return _quest_extra(args, dev, flush, stream, QWEN3_30B_A3B_QUEST_128K.scaled(topk_pages=92), 64, 512)
 
 
 def _e2e(args, step, x, before, after, stream, flush, dev):

@@ -173,6 +173,30 @@ SE_API se_status_t se_quest_topk_pages(const float* scores, int32_t score_stride
                                 int32_t* out_pages, int32_t* out_counts, int32_t sel_stride, void* stream);
 
 /*
+ * se_quest_topk_pages_windowed -- se_quest_topk_pages with sink and recent keep
+ * windows. SparseEngine, Tables 9-12: Quest keeps sink and recent tokens
+ * beside its selected budget (e.g. sink 64, recent 512, 1,472 selected =
+ * 2,048 total, Tables 11 and 12; sink 64, recent 256, 4,096 selected =
+ * 4,416 total, Table 9), and the budget excludes them (Table 10 caption).
+ * Page-granular: the pages holding any of the first sink_tokens tokens and
+ * the pages holding any of the last recent_tokens tokens are always kept, as
+ * is the last page; topk_pages pages are selected among the pages between
+ * them (equal scores: lower page id first). Output, ascending: the sink pages,
+ * the selected pages, the recent pages; count = all of them (every page when
+ * no more than topk_pages candidates remain). sink_tokens = recent_tokens = 0
+ * is se_quest_topk_pages.
+ *   sel_stride >= se_quest_kept_pages_max(topk_pages, sink_tokens, recent_tokens)
+ *               = ceil(sink/16) + topk_pages + ceil(recent/16) + 1.
+ */
+SE_API se_status_t se_quest_topk_pages_windowed(const float* scores, int32_t score_stride, const int32_t* seq_lens,
+                                                int32_t batch, int32_t num_kv_heads, int32_t max_seq_len,
+                                                int32_t topk_pages, int32_t sink_tokens, int32_t recent_tokens,
+                                                int32_t* out_pages, int32_t* out_counts, int32_t sel_stride,
+                                                void* stream);
+/* Most pages one (request, KV head) can keep with these windows (-1 for a negative argument). Host only. */
+SE_API long long se_quest_kept_pages_max(int32_t topk_pages, int32_t sink_tokens, int32_t recent_tokens);
+
+/*
  * se_quest_select_pages -- se_quest_score_pages followed by se_quest_topk_pages,
  * with the scores kept in the caller's workspace (size from
  * se_quest_select_workspace_size).
@@ -183,6 +207,13 @@ SE_API se_status_t se_quest_select_pages(const se_paged_kv_t* kv, const void* q,
                                   int32_t batch, int32_t max_seq_len, int32_t topk_pages, int32_t* out_pages,
                                   int32_t* out_counts, int32_t sel_stride, void* workspace,
                                   size_t workspace_bytes, void* stream);
+/* se_quest_select_pages with the keep windows of se_quest_topk_pages_windowed. */
+SE_API se_status_t se_quest_select_pages_windowed(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                                  const int32_t* block_table, int32_t bt_stride,
+                                                  const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                                                  int32_t topk_pages, int32_t sink_tokens, int32_t recent_tokens,
+                                                  int32_t* out_pages, int32_t* out_counts, int32_t sel_stride,
+                                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * se_sparse_paged_decode -- attention of one decode query per request over the

@@ -29,6 +29,12 @@ Quest method, written from its definition:
 4. selection: the ``topk`` best-scoring pages among 0..n-2 (reading: ties go
    to the lower page index), plus the last page n-1, which holds the newest
    tokens and is always kept outside the budget; ascending page ids;
+4b. keep windows (Tables 9-12: Quest with sink and recent tokens beside the
+   selected budget, e.g. sink 64, recent 512, 1,472 selected = 2,048 total;
+   reading: page-granular): the pages holding any of the first S tokens and
+   the pages holding any of the last R tokens are always kept, as is the last
+   page; the ``topk`` best pages are chosen among the pages that are in neither
+   window (ties to the lower page index). S = R = 0 is step 4;
 5. attention over the selected pages: z_j = sm_scale * q_h . k_j for the
    tokens j < L of those pages, alpha = softmax(z), o_h = sum_j alpha_j v_j and
    lse_h = log sum_j exp(z_j).
@@ -102,6 +108,39 @@ def kth_score(scores, n_pages: int, topk: int):
     if len(cands) <= topk:
         return None
     return sorted(cands, reverse=True)[topk - 1]
+
+
+def keep_windows(n_tokens: int, page_size: int, sink_tokens: int, recent_tokens: int):
+    """(always-kept pages, candidate pages), both ascending: a page is always kept if it
+    holds one of the first ``sink_tokens`` tokens, one of the last ``recent_tokens`` tokens,
+    or is the last page."""
+    n = num_pages(n_tokens, page_size)
+    sink = set(range(min(sink_tokens, n_tokens)))
+    recent = set(range(max(0, n_tokens - recent_tokens), n_tokens))
+    kept, cands = [], []
+    for p in range(n):
+        tokens = range(p * page_size, min((p + 1) * page_size, n_tokens))
+        if p == n - 1 or any(t in sink or t in recent for t in tokens):
+            kept.append(p)
+        else:
+            cands.append(p)
+    return kept, cands
+
+
+def select_pages_windowed(scores, n_tokens: int, page_size: int, topk: int, sink_tokens: int,
+                          recent_tokens: int) -> list:
+    """Ascending page ids: the kept windows plus the ``topk`` best candidates between them."""
+    kept, cands = keep_windows(n_tokens, page_size, sink_tokens, recent_tokens)
+    ranked = sorted(cands, key=lambda p: (-scores[p], p))
+    return sorted(set(kept) | set(ranked[:topk]))
+
+
+def kth_score_windowed(scores, n_tokens: int, page_size: int, topk: int, sink_tokens: int, recent_tokens: int):
+    """The k-th largest candidate score, or None when every candidate is kept."""
+    _, cands = keep_windows(n_tokens, page_size, sink_tokens, recent_tokens)
+    if len(cands) <= topk:
+        return None
+    return sorted((scores[p] for p in cands), reverse=True)[topk - 1]
 
 
 # ---------------------------------------------------------------- step 5
@@ -189,8 +228,10 @@ class QuestRequest:
             m[page], M[page] = append_to_summary(m[page], M[page], kn[h], off)
             self.summaries[h] = (m, M)
 
-    def decode(self, q, topk_pages: int, sm_scale: float, pages_override=None) -> RequestResult:
-        """Select pages per KV head and attend. ``pages_override[h]`` replaces the selection."""
+    def decode(self, q, topk_pages: int, sm_scale: float, pages_override=None, sink_tokens: int = 0,
+               recent_tokens: int = 0) -> RequestResult:
+        """Select pages per KV head (with the keep windows of step 4b) and attend.
+        ``pages_override[h]`` replaces the selection."""
         q = f64(q)
         G = q.shape[0] // self.num_kv_heads
         n = num_pages(self.n_tokens, self.page_size)
@@ -199,8 +240,14 @@ class QuestRequest:
             qg = q[h * G:(h + 1) * G]
             m, M = self.summaries[h]
             scores = group_page_scores(qg, m[:max(n - 1, 0)], M[:max(n - 1, 0)])
-            pages = select_pages(scores, n, topk_pages)
-            heads.append(HeadResult(scores, pages, kth_score(scores, n, topk_pages)))
+            if sink_tokens == 0 and recent_tokens == 0:
+                pages = select_pages(scores, n, topk_pages)
+                tau = kth_score(scores, n, topk_pages)
+            else:
+                ps = self.page_size
+                pages = select_pages_windowed(scores, self.n_tokens, ps, topk_pages, sink_tokens, recent_tokens)
+                tau = kth_score_windowed(scores, self.n_tokens, ps, topk_pages, sink_tokens, recent_tokens)
+            heads.append(HeadResult(scores, pages, tau))
             use = pages if pages_override is None else list(pages_override[h])
             if not use:  # no token to attend to: the empty sum (zero output, lse = -inf)
                 o, lse = np.zeros((G, self.head_dim_v)), np.full(G, -np.inf)
@@ -213,7 +260,8 @@ class QuestRequest:
         return RequestResult(heads, np.vstack(outs), np.concatenate(lses))
 
 
-def decode_step(inputs, topk_pages: int, sm_scale: float, requests=None, pages_override=None):
+def decode_step(inputs, topk_pages: int, sm_scale: float, requests=None, pages_override=None, sink_tokens: int = 0,
+                recent_tokens: int = 0):
     """Oracle decode step over the requests of a batch (all by default).
 
     ``inputs`` carries CPU copies of: k_cache, v_cache (or None), block_table [B][w],
@@ -230,5 +278,5 @@ def decode_step(inputs, topk_pages: int, sm_scale: float, requests=None, pages_o
             vn = inputs["v_new"][b] if inputs.get("v_new") is not None else None
             req.append(inputs["k_new"][b], vn)
         po = None if pages_override is None else pages_override[b]
-        out[b] = req.decode(inputs["q"][b], topk_pages, sm_scale, po)
+        out[b] = req.decode(inputs["q"][b], topk_pages, sm_scale, po, sink_tokens, recent_tokens)
     return out

@@ -20,7 +20,8 @@ from . import build as _build
 __all__ = [
     "SparseEngineError", "SEPagedKV", "paged_kv", "load_library", "se_read_device_error",
     "se_quest_build_summaries", "se_quest_update_summaries", "se_quest_score_pages",
-    "se_quest_topk_pages", "se_quest_select_workspace_size", "se_quest_select_pages",
+    "se_quest_topk_pages", "se_quest_topk_pages_windowed", "se_quest_kept_pages_max",
+    "se_quest_select_workspace_size", "se_quest_select_pages", "se_quest_select_pages_windowed",
     "se_sparse_decode_workspace_size", "se_sparse_decode_plan", "se_sparse_paged_decode",
     "se_sparse_paged_decode_noalloc", "se_snapkv_workspace_size", "se_snapkv_window_scores", "se_snapkv_select",
     "se_snapkv_compact", "se_snapkv_score_and_compact", "exported_symbols",
@@ -61,8 +62,12 @@ _SIGNATURES = {
     "se_quest_update_summaries": (ctypes.c_int, [_KV, _P, _P, _P, _I, _P, _I, _P]),
     "se_quest_score_pages": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _P, _I, _P]),
     "se_quest_topk_pages": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I, _P]),
+    "se_quest_topk_pages_windowed": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P]),
+    "se_quest_kept_pages_max": (ctypes.c_longlong, [_I, _I, _I]),
     "se_quest_select_workspace_size": (_Z, [_I, _I, _I]),
     "se_quest_select_pages": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _I, _P, _P, _I, _P, _Z, _P]),
+    "se_quest_select_pages_windowed": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P,
+                                                      _Z, _P]),
     "se_sparse_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "se_sparse_decode_plan": (ctypes.c_int, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
                                              ctypes.POINTER(_I)]),
@@ -187,6 +192,21 @@ def se_quest_topk_pages(scores, seq_lens, num_kv_heads: int, max_seq_len: int, t
                                    _stream(stream)))
 
 
+def se_quest_topk_pages_windowed(scores, seq_lens, num_kv_heads: int, max_seq_len: int, topk_pages: int,
+                                 sink_tokens: int, recent_tokens: int, out_pages, out_counts, stream=None):
+    lib = load_library()
+    _check(lib.se_quest_topk_pages_windowed(_ptr(scores, torch.float32, "scores"), scores.shape[-1],
+                                            _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0],
+                                            int(num_kv_heads), int(max_seq_len), int(topk_pages), int(sink_tokens),
+                                            int(recent_tokens), _ptr(out_pages, torch.int32, "out_pages"),
+                                            _ptr(out_counts, torch.int32, "out_counts"), out_pages.shape[-1],
+                                            _stream(stream)))
+
+
+def se_quest_kept_pages_max(topk_pages: int, sink_tokens: int, recent_tokens: int) -> int:
+    return int(load_library().se_quest_kept_pages_max(topk_pages, sink_tokens, recent_tokens))
+
+
 def se_quest_select_workspace_size(batch: int, num_kv_heads: int, max_seq_len: int) -> int:
     return int(load_library().se_quest_select_workspace_size(batch, num_kv_heads, max_seq_len))
 
@@ -201,6 +221,20 @@ def se_quest_select_pages(kv: SEPagedKV, q, block_table, seq_lens, max_seq_len: 
                                      _ptr(out_counts, torch.int32, "out_counts"), out_pages.shape[-1],
                                      _ptr(workspace, torch.uint8, "workspace"),
                                      0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
+def se_quest_select_pages_windowed(kv: SEPagedKV, q, block_table, seq_lens, max_seq_len: int, topk_pages: int,
+                                   sink_tokens: int, recent_tokens: int, out_pages, out_counts, workspace,
+                                   stream=None):
+    lib = load_library()
+    _check(lib.se_quest_select_pages_windowed(ctypes.byref(kv), _ptr(q, torch.bfloat16, "q"), q.shape[1],
+                                              _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                              _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0],
+                                              int(max_seq_len), int(topk_pages), int(sink_tokens),
+                                              int(recent_tokens), _ptr(out_pages, torch.int32, "out_pages"),
+                                              _ptr(out_counts, torch.int32, "out_counts"), out_pages.shape[-1],
+                                              _ptr(workspace, torch.uint8, "workspace"),
+                                              0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
 def se_sparse_decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim_v: int,

@@ -239,13 +239,17 @@ se_status_t se_quest_score_pages(const se_paged_kv_t* kv, const void* q, int32_t
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
 }
 
-se_status_t se_quest_topk_pages(const float* scores, int32_t score_stride, const int32_t* seq_lens,
-                                int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t topk_pages,
-                                int32_t* out_pages, int32_t* out_counts, int32_t sel_stride, void* stream) {
-  static const char* fn = "se_quest_topk_pages";
+se_status_t se_quest_topk_pages_windowed(const float* scores, int32_t score_stride, const int32_t* seq_lens,
+                                         int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t topk_pages,
+                                         int32_t sink_tokens, int32_t recent_tokens, int32_t* out_pages,
+                                         int32_t* out_counts, int32_t sel_stride, void* stream) {
+  static const char* fn = "se_quest_topk_pages_windowed";
   if (batch < 0 || num_kv_heads < 1 || max_seq_len < 0) return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
   if (topk_pages < 1) return fail(SE_ERR_INVALID_ARG, fn, "topk_pages < 1");
-  if (sel_stride < topk_pages + 1) return fail(SE_ERR_INVALID_ARG, fn, "sel_stride < topk_pages + 1");
+  if (sink_tokens < 0 || recent_tokens < 0 || sink_tokens > (1 << 30) || recent_tokens > (1 << 30))
+    return fail(SE_ERR_INVALID_ARG, fn, "sink_tokens / recent_tokens out of range");
+  if ((long long)sel_stride < se_quest_kept_pages_max(topk_pages, sink_tokens, recent_tokens))
+    return fail(SE_ERR_INVALID_ARG, fn, "sel_stride < se_quest_kept_pages_max(topk_pages, sink, recent)");
   if (score_stride < score_stride_for(max_seq_len)) return fail(SE_ERR_INVALID_ARG, fn, "score_stride too small");
   if (batch > 0 && (!scores || !seq_lens || !out_pages || !out_counts))
     return fail(SE_ERR_INVALID_ARG, fn, "NULL pointer");
@@ -257,8 +261,22 @@ se_status_t se_quest_topk_pages(const float* scores, int32_t score_stride, const
   cudaError_t e = current_device(&d);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   e = se::launch_topk_pages(scores, score_stride, seq_lens, batch, num_kv_heads, max_seq_len, topk_pages,
-                            out_pages, out_counts, sel_stride, d->err, static_cast<cudaStream_t>(stream));
+                            sink_tokens, recent_tokens, out_pages, out_counts, sel_stride, d->err,
+                            static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+se_status_t se_quest_topk_pages(const float* scores, int32_t score_stride, const int32_t* seq_lens,
+                                int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t topk_pages,
+                                int32_t* out_pages, int32_t* out_counts, int32_t sel_stride, void* stream) {
+  return se_quest_topk_pages_windowed(scores, score_stride, seq_lens, batch, num_kv_heads, max_seq_len, topk_pages,
+                                      0, 0, out_pages, out_counts, sel_stride, stream);
+}
+
+long long se_quest_kept_pages_max(int32_t topk_pages, int32_t sink_tokens, int32_t recent_tokens) {
+  if (topk_pages < 0 || sink_tokens < 0 || recent_tokens < 0) return -1;
+  const long long ps = se::kPageSize;
+  return (sink_tokens + ps - 1) / ps + topk_pages + (recent_tokens + ps - 1) / ps + 1;
 }
 
 size_t se_quest_select_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len) {
@@ -266,26 +284,38 @@ size_t se_quest_select_workspace_size(int32_t batch, int32_t num_kv_heads, int32
   return round16((size_t)batch * num_kv_heads * score_stride_for(max_seq_len) * sizeof(float));
 }
 
-se_status_t se_quest_select_pages(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
-                                  const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
-                                  int32_t batch, int32_t max_seq_len, int32_t topk_pages, int32_t* out_pages,
-                                  int32_t* out_counts, int32_t sel_stride, void* workspace,
-                                  size_t workspace_bytes, void* stream) {
-  static const char* fn = "se_quest_select_pages";
+se_status_t se_quest_select_pages_windowed(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                           const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                           int32_t batch, int32_t max_seq_len, int32_t topk_pages,
+                                           int32_t sink_tokens, int32_t recent_tokens, int32_t* out_pages,
+                                           int32_t* out_counts, int32_t sel_stride, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  static const char* fn = "se_quest_select_pages_windowed";
   if (!kv) return fail(SE_ERR_INVALID_ARG, fn, "kv is NULL");
   if (batch < 0 || max_seq_len < 0) return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
   const size_t need = se_quest_select_workspace_size(batch, kv->num_kv_heads, max_seq_len);
   if (workspace_bytes < need) return fail(SE_ERR_WORKSPACE, fn, "workspace too small");
   if (need > 0 && !workspace) return fail(SE_ERR_INVALID_ARG, fn, "workspace NULL");
-  if (topk_pages < 1 || sel_stride < topk_pages + 1)
-    return fail(SE_ERR_INVALID_ARG, fn, "topk_pages < 1 or sel_stride < topk_pages + 1");
+  if (topk_pages < 1 || sink_tokens < 0 || recent_tokens < 0 ||
+      (long long)sel_stride < se_quest_kept_pages_max(topk_pages, sink_tokens, recent_tokens))
+    return fail(SE_ERR_INVALID_ARG, fn, "topk_pages < 1, negative window or sel_stride too small");
   float* scores = static_cast<float*>(workspace);
   const int stride = score_stride_for(max_seq_len);
   se_status_t st = se_quest_score_pages(kv, q, num_q_heads, block_table, bt_stride, seq_lens, batch, max_seq_len,
                                         scores, stride, stream);
   if (st != SE_OK) return st;
-  return se_quest_topk_pages(scores, stride, seq_lens, batch, kv->num_kv_heads, max_seq_len, topk_pages, out_pages,
-                             out_counts, sel_stride, stream);
+  return se_quest_topk_pages_windowed(scores, stride, seq_lens, batch, kv->num_kv_heads, max_seq_len, topk_pages,
+                                      sink_tokens, recent_tokens, out_pages, out_counts, sel_stride, stream);
+}
+
+se_status_t se_quest_select_pages(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                  const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                  int32_t batch, int32_t max_seq_len, int32_t topk_pages, int32_t* out_pages,
+                                  int32_t* out_counts, int32_t sel_stride, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return se_quest_select_pages_windowed(kv, q, num_q_heads, block_table, bt_stride, seq_lens, batch, max_seq_len,
+                                        topk_pages, 0, 0, out_pages, out_counts, sel_stride, workspace,
+                                        workspace_bytes, stream);
 }
 
 se_status_t se_sparse_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

@@ -33,6 +33,22 @@ __device__ __forceinline__ int clamp_len(int L, int max_len, unsigned* err) {
   return L;
 }
 
+// Candidate pages [c0, c1) of a request of L tokens in n pages: the pages that
+// hold none of the first `sink` tokens and none of the last `recent` tokens;
+// the last page (the newest token) is always kept, so c1 <= n - 1.
+__device__ __forceinline__ void candidate_window(int L, int n, int sink, int recent, int& c0, int& c1) {
+  const int rf = L > recent ? (L - recent) / kPageSize : 0;
+  c1 = max(0, min(rf, n - 1));
+  c0 = min((min(sink, L) + kPageSize - 1) / kPageSize, c1);
+}
+
+// Writes the kept pages outside the window: 0 .. c0 - 1 first, c1 .. n - 1
+// after the k selected ones.
+__device__ __forceinline__ void write_kept_windows(int32_t* out, int c0, int c1, int n, int k, int tid) {
+  for (int i = tid; i < c0; i += kTopkThreads) out[i] = i;
+  for (int j = tid; j < n - c1; j += kTopkThreads) out[c0 + k + j] = c1 + j;
+}
+
 // Larger float -> larger key (IEEE order; -0 sorts just below +0).
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
@@ -110,8 +126,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* wtot, int warp, 
 //  4. the selected page ids are written in ascending order (block scan).
 __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ seq_lens, int32_t H,
-    int32_t max_seq_len, int32_t k, int32_t* __restrict__ out_pages, int32_t* __restrict__ out_counts,
-    int32_t sel_stride, unsigned* err) {
+    int32_t max_seq_len, int32_t k, int32_t sink, int32_t recent, int32_t* __restrict__ out_pages,
+    int32_t* __restrict__ out_counts, int32_t sel_stride, unsigned* err) {
   pdl_enter();
   __shared__ int hist[kBuckets];
   __shared__ float s_min[kTopkWarps], s_max[kTopkWarps];
@@ -125,14 +141,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int L = clamp_len(seq_lens[b], max_seq_len, err);
   const int n = (L + kPageSize - 1) / kPageSize;
-  const int C = min(max(n - 1, 0), kRegMaxCand);
+  int c0, c1;
+  candidate_window(L, n, sink, recent, c0, c1);
+  const int C = min(c1 - c0, kRegMaxCand);  // candidate i is page c0 + i
   int32_t* out = out_pages + (size_t)bh * sel_stride;
   if (C <= k) {
     for (int i = tid; i < n; i += kTopkThreads) out[i] = i;
     if (tid == 0) out_counts[bh] = n;
     return;
   }
-  const float* sc = scores + (size_t)bh * score_stride;
+  write_kept_windows(out, c0, c1, n, k, tid);
+  const float* sc = scores + (size_t)bh * score_stride + c0;
   float x[kKeysPerThread];
   float lmin = INFINITY, lmax = -INFINITY;
 #pragma unroll
@@ -277,20 +296,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
 #pragma unroll
   for (int e = 0; e < kKeysPerThread; ++e) {
     if (selv[e]) {
-      if (pos < k) out[pos] = tid * kKeysPerThread + e;
+      if (pos < k) out[c0 + pos] = c0 + tid * kKeysPerThread + e;
       ++pos;
     }
   }
-  if (tid == 0) {
-    out[k] = n - 1;
-    out_counts[bh] = k + 1;
-  }
+  if (tid == 0) out_counts[bh] = c0 + k + (n - c1);
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_pages_smem_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ seq_lens, int32_t H,
-    int32_t max_seq_len, int32_t k, int32_t* __restrict__ out_pages, int32_t* __restrict__ out_counts,
-    int32_t sel_stride, unsigned* err) {
+    int32_t max_seq_len, int32_t k, int32_t sink, int32_t recent, int32_t* __restrict__ out_pages,
+    int32_t* __restrict__ out_counts, int32_t sel_stride, unsigned* err) {
   pdl_enter();
   extern __shared__ uint32_t keys[];
   __shared__ int hist[257];
@@ -300,14 +316,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_smem_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int L = clamp_len(seq_lens[b], max_seq_len, err);
   const int n = (L + kPageSize - 1) / kPageSize;
-  const int C = max(n - 1, 0);
+  int c0, c1;
+  candidate_window(L, n, sink, recent, c0, c1);
+  const int C = c1 - c0;  // candidate i is page c0 + i
   int32_t* out = out_pages + (size_t)bh * sel_stride;
   if (C <= k) {
     for (int i = tid; i < n; i += kTopkThreads) out[i] = i;
     if (tid == 0) out_counts[bh] = n;
     return;
   }
-  const float* sc = scores + (size_t)bh * score_stride;
+  write_kept_windows(out, c0, c1, n, k, tid);
+  const float* sc = scores + (size_t)bh * score_stride + c0;
   for (int i = tid; i < C; i += kTopkThreads) keys[i] = order_key(sc[i]);
 
   uint32_t prefix = 0, mask = 0;
@@ -391,15 +410,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_smem_kernel(
       sel_total += v;
     }
     const int pos = base_out + sel_before + __popc(bsel & lt_mask);
-    if (sel && pos < k) out[pos] = i;
+    if (sel && pos < k) out[c0 + pos] = c0 + i;
     base_out += sel_total;
     eq_seen += eq_total;
     __syncthreads();
   }
-  if (tid == 0) {
-    out[k] = n - 1;
-    out_counts[bh] = k + 1;
-  }
+  if (tid == 0) out_counts[bh] = c0 + k + (n - c1);
 }
 
 }  // namespace
@@ -410,15 +426,16 @@ size_t topk_smem_bytes(int32_t max_seq_len) {
 }
 
 cudaError_t launch_topk_pages(const float* scores, int32_t score_stride, const int32_t* seq_lens, int32_t batch,
-                              int32_t num_kv_heads, int32_t max_seq_len, int32_t topk, int32_t* out_pages,
-                              int32_t* out_counts, int32_t sel_stride, unsigned* err, cudaStream_t stream) {
+                              int32_t num_kv_heads, int32_t max_seq_len, int32_t topk, int32_t sink_tokens,
+                              int32_t recent_tokens, int32_t* out_pages, int32_t* out_counts, int32_t sel_stride,
+                              unsigned* err, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
   const int max_cand = (max_seq_len + kPageSize - 1) / kPageSize - 1;
   if (max_cand <= kRegMaxCand) {
     {
       const cudaError_t le = launch_pdl(topk_pages_reg_kernel, dim3(batch * num_kv_heads), dim3(kTopkThreads), 0,
                                         stream, scores, score_stride, seq_lens, num_kv_heads, max_seq_len, topk,
-                                        out_pages, out_counts, sel_stride, err);
+                                        sink_tokens, recent_tokens, out_pages, out_counts, sel_stride, err);
       if (le != cudaSuccess) return le;
     }
     return cudaGetLastError();
@@ -432,7 +449,7 @@ cudaError_t launch_topk_pages(const float* scores, int32_t score_stride, const i
   {
     const cudaError_t le = launch_pdl(topk_pages_smem_kernel, dim3(batch * num_kv_heads), dim3(kTopkThreads), smem,
                                       stream, scores, score_stride, seq_lens, num_kv_heads, max_seq_len, topk,
-                                      out_pages, out_counts, sel_stride, err);
+                                      sink_tokens, recent_tokens, out_pages, out_counts, sel_stride, err);
     if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();

@@ -65,9 +65,13 @@ cudaError_t launch_score_pages(const KvView& kv, const uint16_t* q, int32_t num_
                                int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
                                int sm_count, unsigned* err, cudaStream_t stream);
 // ---- quest_topk.cu
+// Top-k of the candidate pages: those holding none of the first sink_tokens and
+// none of the last recent_tokens tokens (the last page always kept); the kept
+// windows are written around the selection.
 cudaError_t launch_topk_pages(const float* scores, int32_t score_stride, const int32_t* seq_lens, int32_t batch,
-                              int32_t num_kv_heads, int32_t max_seq_len, int32_t topk, int32_t* out_pages,
-                              int32_t* out_counts, int32_t sel_stride, unsigned* err, cudaStream_t stream);
+                              int32_t num_kv_heads, int32_t max_seq_len, int32_t topk, int32_t sink_tokens,
+                              int32_t recent_tokens, int32_t* out_pages, int32_t* out_counts, int32_t sel_stride,
+                              unsigned* err, cudaStream_t stream);
 size_t topk_smem_bytes(int32_t max_seq_len);
 
 // ---- sparse_decode.cu

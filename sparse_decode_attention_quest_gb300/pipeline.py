@@ -4,7 +4,7 @@ Host orchestration only (allocation and call order); the work runs in the
 library's kernels:
     se_quest_update_summaries   (optional KV append fused with the summary update)
     se_quest_score_pages        (upper-bound score of every candidate page)
-    se_quest_topk_pages         (top-k pages + the last page, ascending)
+    se_quest_topk_pages_windowed (top-k pages + the sink/recent windows + the last page, ascending)
     se_sparse_paged_decode      (split-K flash-decode over the selected pages + merge)
 """
 from __future__ import annotations
@@ -14,9 +14,9 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (paged_kv, se_quest_build_summaries, se_quest_score_pages, se_quest_topk_pages,
-               se_quest_update_summaries, se_sparse_decode_plan, se_sparse_decode_workspace_size,
-               se_sparse_paged_decode)
+from . import (paged_kv, se_quest_build_summaries, se_quest_kept_pages_max, se_quest_score_pages,
+               se_quest_topk_pages_windowed, se_quest_update_summaries, se_sparse_decode_plan,
+               se_sparse_decode_workspace_size, se_sparse_paged_decode)
 
 PAGE = 16
 
@@ -30,7 +30,8 @@ def new_summary(k_cache: torch.Tensor) -> torch.Tensor:
 class QuestDecodeStep:
     def __init__(self, k_cache: torch.Tensor, v_cache: Optional[torch.Tensor], summary: torch.Tensor,
                  block_table: torch.Tensor, num_q_heads: int, topk_pages: int, max_seq_len: int,
-                 head_dim_v: Optional[int] = None, sm_scale: Optional[float] = None, sel_stride: Optional[int] = None):
+                 head_dim_v: Optional[int] = None, sm_scale: Optional[float] = None, sel_stride: Optional[int] = None,
+                 sink_tokens: int = 0, recent_tokens: int = 0):
         self.k_cache, self.v_cache, self.summary = k_cache, v_cache, summary
         self.block_table = block_table
         self.kv = paged_kv(k_cache, v_cache, summary, head_dim_v)
@@ -45,7 +46,9 @@ class QuestDecodeStep:
         self.sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(self.D)
         stride = max(1, (max_seq_len + PAGE - 1) // PAGE)
         self.scores = torch.empty(self.B, self.H, stride, dtype=torch.float32, device=dev)
-        self.sel_stride = sel_stride if sel_stride is not None else topk_pages + 1
+        self.sink, self.recent = sink_tokens, recent_tokens
+        kept_max = se_quest_kept_pages_max(topk_pages, sink_tokens, recent_tokens)
+        self.sel_stride = sel_stride if sel_stride is not None else kept_max
         self.sel = torch.empty(self.B, self.H, self.sel_stride, dtype=torch.int32, device=dev)
         self.counts = torch.empty(self.B, self.H, dtype=torch.int32, device=dev)
         self.out = torch.empty(self.B, self.Hq, self.Dv, dtype=torch.bfloat16, device=dev)
@@ -66,7 +69,8 @@ class QuestDecodeStep:
 
     def select(self, q, seq_lens, stream=None):
         se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, stream)
-        se_quest_topk_pages(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sel, self.counts, stream)
+        se_quest_topk_pages_windowed(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sink,
+                                     self.recent, self.sel, self.counts, stream)
 
     def attend(self, q, seq_lens, sel=None, counts=None, stream=None):
         se_sparse_paged_decode(self.kv, q, self.block_table, seq_lens, self.sel if sel is None else sel,
@@ -87,7 +91,8 @@ class QuestDecodeStep:
         se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, s)
         if events is not None:
             events[2].record(s)
-        se_quest_topk_pages(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sel, self.counts, s)
+        se_quest_topk_pages_windowed(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sink,
+                                     self.recent, self.sel, self.counts, s)
         if events is not None:
             events[3].record(s)
         self.attend(q, seq_lens, stream=s)

@@ -139,6 +139,47 @@ def check_select_bruteforce(quest):
     assert quest.select_pages(np.arange(5.0), 6, 10) == list(range(6))
 
 
+# ------------------------------------------------------------------ keep windows
+def _window_rank_select(scores, n_tokens, ps, k, S, R):
+    """Brute force from the token-level definition: page p is kept when it holds one of the
+    first S tokens, one of the last R tokens, or is the last page; among the other pages, p
+    is selected when fewer than k of them beat it (higher score, or equal and lower index)."""
+    n = -(-n_tokens // ps)
+
+    def kept(p):
+        first, last = p * ps, min((p + 1) * ps, n_tokens) - 1
+        return p == n - 1 or first < S or last >= n_tokens - R
+
+    cands = [p for p in range(n) if not kept(p)]
+    sel = [p for p in cands
+           if sum(1 for r in cands if scores[r] > scores[p] or (scores[r] == scores[p] and r < p)) < k]
+    return sorted([p for p in range(n) if kept(p)] + sel)
+
+
+def check_select_windowed_bruteforce(quest):
+    rng = _rng(17)
+    for _ in range(200):
+        L = int(rng.integers(0, 90))
+        S, R, k = int(rng.integers(0, 20)), int(rng.integers(0, 30)), int(rng.integers(1, 6))
+        n = -(-L // PS)
+        scores = rng.integers(-2, 3, size=max(n - 1, 0)).astype(float)  # many ties
+        assert quest.select_pages_windowed(scores, L, PS, k, S, R) == _window_rank_select(scores, L, PS, k, S, R), \
+            (L, S, R, k, scores)
+    # Windows that cover every page keep every page.
+    assert quest.select_pages_windowed(np.zeros(9), 40, PS, 1, 20, 20) == list(range(10))
+
+
+def check_select_windowed_reduces_to_plain(quest):
+    rng = _rng(19)
+    for _ in range(50):
+        L = int(rng.integers(1, 90))
+        n = -(-L // PS)
+        k = int(rng.integers(1, 8))
+        scores = rng.standard_normal(max(n - 1, 0))
+        assert quest.select_pages_windowed(scores, L, PS, k, 0, 0) == quest.select_pages(scores, n, k)
+        assert quest.kth_score_windowed(scores, L, PS, k, 0, 0) == quest.kth_score(scores, n, k)
+
+
 # ------------------------------------------------------------------ attention
 def _sdpa(qg, K, V, scale):
     q = torch.from_numpy(qg)[None, :, None, :]          # [1][G][1][D]
@@ -320,6 +361,7 @@ QUEST_CHECKS = [check_summary_bruteforce, check_append_matches_rebuild, check_bo
                 check_group_score_bounds_group_logit, check_select_bruteforce,
                 check_select_all_equals_dense, check_single_token_attention, check_empty_request,
                 check_permutation_invariance, check_latent_value_is_key_prefix,
-                check_selection_uses_the_bound]
+                check_selection_uses_the_bound, check_select_windowed_bruteforce,
+                check_select_windowed_reduces_to_plain]
 SNAPKV_CHECKS = [check_window_probabilities, check_window_lse, check_candidate_scores, check_max_pool,
                  check_keep_positions, check_snapkv_head_end_to_end, check_compaction_exact]

@@ -78,14 +78,17 @@ def oracle_inputs(x, requests=None):
     }
 
 
-def compare_decode(x, step, requests, sm_scale: float, what: str = ""):
-    """Selection and output of ``step`` (after run) against the oracle on ``requests``.
+def compare_decode(x, step, requests, sm_scale: float, what: str = "", sink_tokens: int = 0,
+                   recent_tokens: int = 0):
+    """Selection and output of ``step`` (after run) against the oracle on ``requests``
+    (with the keep windows ``sink_tokens`` / ``recent_tokens``).
 
     Returns the maximum absolute output error seen.
     """
     wl = x.workload
     inp = oracle_inputs(x, requests)
-    ref = oq.decode_step(inp, wl.topk_pages, sm_scale, requests=requests)
+    ref = oq.decode_step(inp, wl.topk_pages, sm_scale, requests=requests, sink_tokens=sink_tokens,
+                         recent_tokens=recent_tokens)
     sel = step.sel.cpu().numpy()
     cnt = step.counts.cpu().numpy()
     out = step.out.float().cpu().numpy()

@@ -4,7 +4,10 @@ import os
 
 import pytest
 
+import numpy as np
+
 from oracle import budgets
+from oracle import quest
 from synth import SNAPKV_PREFILL_32K, QWEN3_30B_A3B_QUEST_128K, QWEN3_4B_QUEST_32K
 
 GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "table_budgets.json")))
@@ -31,3 +34,15 @@ def test_workload_budgets_follow_the_tables():
 def test_partial_page_budget_rejected():
     with pytest.raises(ValueError):
         budgets.selected_pages(2008)
+
+
+@pytest.mark.parametrize("row", [r for r in GOLD["rows"] if r["method"] == "Quest"], ids=lambda r: r["cite"])
+def test_windowed_selection_keeps_the_printed_total(row):
+    # At a page-aligned 128K length the sink, the selected pages and the recent window add up
+    # to the total the table prints (16-token pages).
+    L, ps = 131072, 16
+    n = L // ps
+    scores = np.random.default_rng(0).standard_normal(n - 1)
+    pages = quest.select_pages_windowed(scores, L, ps, budgets.selected_pages(row["selected"]), row["sink"],
+                                        row["recent"])
+    assert len(pages) * ps == row["total"]

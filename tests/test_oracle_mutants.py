@@ -91,6 +91,21 @@ def _s_keep_ties_high(pooled, n, W, keep):
     return chosen + list(range(c, n))
 
 
+def _q_windows_recent_whole_pages(n_tokens, page_size, sink_tokens, recent_tokens):
+    # recent window counted as whole pages from the end (misses the partial page at its start)
+    n = -(-n_tokens // page_size)
+    rp = recent_tokens // page_size
+    sp = -(-min(sink_tokens, n_tokens) // page_size)
+    kept = sorted(set(range(min(sp, n))) | set(range(max(n - max(rp, 1), 0), n)))
+    return kept, [p for p in range(n) if p not in kept]
+
+
+def _q_windowed_sink_in_budget(scores, n_tokens, page_size, topk, sink_tokens, recent_tokens):
+    kept, cands = quest.keep_windows(n_tokens, page_size, sink_tokens, recent_tokens)
+    k = max(topk - -(-sink_tokens // page_size), 0)
+    return sorted(set(kept) | set(sorted(cands, key=lambda p: (-scores[p], p))[:k]))
+
+
 MUTANTS = [
     (quest, "page_summary", _q_summary_swapped, pins.QUEST_CHECKS),
     (quest, "append_to_summary", _q_append_never_resets, pins.QUEST_CHECKS),
@@ -101,6 +116,8 @@ MUTANTS = [
     (quest, "select_pages", _q_select_no_last, pins.QUEST_CHECKS),
     (quest, "select_pages", _q_select_last_in_budget, pins.QUEST_CHECKS),
     (quest, "softmax_attention", _q_attention_no_scale, pins.QUEST_CHECKS),
+    (quest, "keep_windows", _q_windows_recent_whole_pages, pins.QUEST_CHECKS),
+    (quest, "select_pages_windowed", _q_windowed_sink_in_budget, pins.QUEST_CHECKS),
     (snapkv, "window_probabilities", _s_mask_off_by_one, pins.SNAPKV_CHECKS),
     (snapkv, "candidate_scores", _s_scores_include_window, pins.SNAPKV_CHECKS),
     (snapkv, "max_pool_clipped", _s_pool_right_only, pins.SNAPKV_CHECKS),

@@ -24,12 +24,13 @@ from tests.parity import OUT_ATOL, compare_decode, oracle_inputs
 pytestmark = pytest.mark.gpu
 
 
-def _prepare(wl, dev, device_gen=False, sel_stride=None, poison=True):
+def _prepare(wl, dev, device_gen=False, sel_stride=None, poison=True, sink=0, recent=0):
     x = make_quest_decode_inputs(wl, device=dev if device_gen else "cpu", poison_tail=poison)
     k = x.k_cache.to(dev)
     v = None if x.v_cache is None else x.v_cache.to(dev)
     step = QuestDecodeStep(k, v, new_summary(k), x.block_table.to(dev), wl.num_q_heads, wl.topk_pages,
-                           max(max(x.seq_lens_after), 1), head_dim_v=wl.head_dim_v, sel_stride=sel_stride)
+                           max(max(x.seq_lens_after), 1), head_dim_v=wl.head_dim_v, sel_stride=sel_stride,
+                           sink_tokens=sink, recent_tokens=recent)
     before = torch.tensor(x.seq_lens, dtype=torch.int32, device=dev)
     after = torch.tensor(x.seq_lens_after, dtype=torch.int32, device=dev)
     step.build_summaries(before)
@@ -318,21 +319,53 @@ def test_scores_on_sampled_pages_of_a_large_batch(cuda_device, hkv, head_dim):
                 assert abs(got - want) <= 2e-5 * scale + 1e-6, (r, h, p, got, want)
 
 
+# ---------------------------------------------------------------- sink / recent keep windows
+@pytest.mark.parametrize("sink,recent", [(64, 512), (16, 64), (64, 256), (0, 512), (64, 0), (100, 37)])
+def test_windowed_selection_oracle_sized(cuda_device, sink, recent):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=4, context_min=900, context_max=4100, topk_pages=24, seed=71)
+    x, step, b, a = _prepare(wl, cuda_device, sink=sink, recent=recent)
+    _run(x, step, b, a, cuda_device)
+    compare_decode(x, step, range(wl.batch), _scale(wl), f"windows {sink}/{recent}", sink, recent)
+
+
+@pytest.mark.parametrize("sel_stride", [None, 80])
+def test_windowed_edge_lengths(cuda_device, sel_stride):
+    # windows that overlap each other or cover the whole request, unaligned lengths
+    lens = (0, 1, 15, 16, 17, 63, 64, 65, 130, 600)
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=len(lens), lengths=lens, topk_pages=2, append=False, seed=73)
+    x, step, b, a = _prepare(wl, cuda_device, sel_stride=sel_stride, sink=64, recent=64)
+    _run(x, step, b, a, cuda_device)
+    compare_decode(x, step, range(wl.batch), _scale(wl), "windowed edges", 64, 64)
+
+
+def test_windowed_full_qwen3_30b_a3b_128k_sampled(cuda_device):
+    # The decode-time keep settings of the throughput runs: sink 64, recent 512, 1,472 selected.
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(topk_pages=92)
+    x, step, b, a = _prepare(wl, cuda_device, device_gen=True, sink=64, recent=512)
+    _run(x, step, b, a, cuda_device)
+    compare_decode(x, step, [0, 9, wl.batch - 1], _scale(wl), "windowed 128k", 64, 512)
+
+
 # ---------------------------------------------------------------- top-k on crafted scores
-def _topk_case(scores_rows, lens, k, dev):
-    """Run se_quest_topk_pages on given fp32 scores [B][1][stride]; compare with the oracle exactly."""
+def _topk_case(scores_rows, lens, k, dev, sink=0, recent=0):
+    """Run the top-k entry point on given fp32 scores [B][1][stride]; compare with the oracle exactly."""
     B = len(lens)
     stride = scores_rows.shape[-1]
     max_len = max(lens)
     sc = scores_rows.to(dev)
     lens_t = torch.tensor(lens, dtype=torch.int32, device=dev)
-    sel = torch.full((B, 1, k + 1), -7, dtype=torch.int32, device=dev)
+    sel = torch.full((B, 1, se.se_quest_kept_pages_max(k, sink, recent)), -7, dtype=torch.int32, device=dev)
     cnt = torch.zeros(B, 1, dtype=torch.int32, device=dev)
-    se.se_quest_topk_pages(sc, lens_t, 1, max_len, k, sel, cnt)
+    if sink == 0 and recent == 0:
+        se.se_quest_topk_pages(sc, lens_t, 1, max_len, k, sel, cnt)
+    else:
+        se.se_quest_topk_pages_windowed(sc, lens_t, 1, max_len, k, sink, recent, sel, cnt)
     torch.cuda.synchronize()
     for b, L in enumerate(lens):
         n = math.ceil(L / 16)
-        ref = oq.select_pages(scores_rows[b, 0].double().numpy(), n, k)
+        s = scores_rows[b, 0].double().numpy()
+        ref = oq.select_pages(s, n, k) if sink == 0 and recent == 0 else \
+            oq.select_pages_windowed(s, L, 16, k, sink, recent)
         got = sel[b, 0, :int(cnt[b, 0])].tolist()
         assert got == ref, (b, L, got[:8], ref[:8])
 
@@ -356,6 +389,7 @@ def test_topk_exact_on_crafted_scores(cuda_device, kind):
         s = 100.0 + torch.randint(0, 3000, (B, 1, stride), generator=g).float() * 1e-5
     for k in (1, 37, 256):
         _topk_case(s, lens, k, cuda_device)
+        _topk_case(s, lens, k, cuda_device, sink=64, recent=512)
 
 
 def test_topk_beyond_8192_candidates_uses_the_shared_memory_kernel(cuda_device):
@@ -365,3 +399,4 @@ def test_topk_beyond_8192_candidates_uses_the_shared_memory_kernel(cuda_device):
     s = torch.randn(2, 1, stride, generator=g)
     s[0, 0, ::7] = 0.5  # ties
     _topk_case(s, lens, 300, cuda_device)
+    _topk_case(s, lens, 300, cuda_device, sink=100, recent=700)
