@@ -353,6 +353,8 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_extra:
         result["extra_workloads"] = {
             "snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, stream),
+            "snapkv_aime_b4_32k": _snapkv_extra(args, dev, flush, stream, _snapkv_wl("SNAPKV_AIME_32K")),
+            "snapkv_agent_b4_32k": _snapkv_extra(args, dev, flush, stream, _snapkv_wl("SNAPKV_AGENT_32K")),
             "mla_glm_quest_b64_32k": _mla_extra(args, dev, flush, stream),
             "qwen3_30b_a3b_quest_sink64_recent512_b32_128k": _windows_extra(args, dev, flush, stream)}
     if rank == 0 and not args.no_cpu_baseline:
@@ -379,14 +381,15 @@ def _profile_traffic(kernel):
         return None
 
 
-def _snapkv_extra(args, dev, flush, stream):
+def _snapkv_extra(args, dev, flush, stream, wl=None):
     """SnapKV eviction at the end of a 32K prefill (4 requests, 32 q / 8 kv heads): one
-    se_snapkv_score_and_compact call per step (window scores on the tensor cores,
-    pool + top-k, compaction), timed with events; L2 flushed between steps."""
+    se_snapkv_score_and_compact_windowed call per step (window scores on the tensor cores,
+    pool + top-k with the workload's keep windows, compaction), timed with events; L2
+    flushed between steps."""
     import torch
     import sparse_decode_attention_quest_gb300 as se
     from synth import SNAPKV_PREFILL_32K, make_snapkv_inputs
-    wl = SNAPKV_PREFILL_32K
+    wl = SNAPKV_PREFILL_32K if wl is None else wl
     x = make_snapkv_inputs(wl, device=dev, poison_tail=False)
     B, H, W, G = wl.batch, wl.num_kv_heads, wl.window, wl.group
     max_len = max(x.prompt_lens)
@@ -395,14 +398,15 @@ def _snapkv_extra(args, dev, flush, stream):
     dk = torch.empty((x.dst_num_pages, H, 16, 128), dtype=torch.bfloat16, device=dev)
     dv = torch.empty_like(dk)
     dst = se.paged_kv(dk, dv, None)
-    kept = torch.empty((B, H, wl.keep_topk + W), dtype=torch.int32, device=dev)
+    kept = torch.empty((B, H, wl.keep_sink + wl.keep_topk + wl.recent), dtype=torch.int32, device=dev)
     cnt = torch.empty((B, H), dtype=torch.int32, device=dev)
     ws = torch.empty(se.se_snapkv_workspace_size(B, H, W, max_len), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(wl.head_dim)
 
     def call():
-        se.se_snapkv_score_and_compact(src, x.q_window, x.src_block_table, lens, max_len, wl.pool_kernel,
-                                       wl.keep_topk, scale, dst, x.dst_block_table, kept, cnt, ws, stream)
+        se.se_snapkv_score_and_compact_windowed(src, x.q_window, x.src_block_table, lens, max_len, wl.pool_kernel,
+                                                wl.keep_topk, wl.keep_sink, wl.recent, scale, dst,
+                                                x.dst_block_table, kept, cnt, ws, stream)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -428,6 +432,8 @@ def _snapkv_extra(args, dev, flush, stream):
     except Exception:
         peak_tf = 1900.0
     return {"ms_per_call": ms, "steps": n, "requests_per_s": B / (ms * 1e-3),
+            "settings": {"window": W, "pool_kernel": wl.pool_kernel, "sink": wl.keep_sink, "recent": wl.recent,
+                         "selected": wl.keep_topk, "kept_per_pair": int(cnt[0, 0].item())},
             "keys_read_bytes_per_pass": kbytes, "gather_bytes": gather,
             "hbm_gbs_two_key_passes": round((2 * kbytes + gather) / (ms * 1e-3) / 1e9, 1),
             "tensor_tflops": round(flops / (ms * 1e-3) / 1e12, 1),
@@ -518,6 +524,11 @@ def _windows_extra(args, dev, flush, stream):
     recent 512, 1,472 selected tokens (92 pages), 2,048 kept in total."""
     from synth import QWEN3_30B_A3B_QUEST_128K
     return _quest_extra(args, dev, flush, stream, QWEN3_30B_A3B_QUEST_128K.scaled(topk_pages=92), 64, 512)
+
+
+def _snapkv_wl(name):
+    import synth
+    return getattr(synth, name)
 
 
 def _e2e(args, step, x, before, after, stream, flush, dev):

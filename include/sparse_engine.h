@@ -290,6 +290,18 @@ SE_API se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q
  *   and is skipped.
  * se_snapkv_score_and_compact: the three steps, the scores kept in `workspace`
  *   (se_snapkv_workspace_size bytes).
+ * se_snapkv_select_windowed / se_snapkv_score_and_compact_windowed: the same
+ *   with explicit keep windows (SparseEngine, Tables 9-12: SnapKV with sink
+ *   0/16/64 and recent 64/256/512 tokens beside 4,096 or 15,808 selected, a
+ *   16-query observation window in Table 10; Table 10 caption: the budget
+ *   excludes them). Positions 0 .. sink_tokens - 1 and n - recent_tokens ..
+ *   n - 1 are always kept (recent_tokens >= window); the keep_topk best pooled
+ *   candidates among the positions between them are kept in ascending order;
+ *   the scores and the pooling are those above (every position before the
+ *   window is scored and pooled). Output: sink positions, selected, recent
+ *   positions; every position when no more than keep_topk candidates remain.
+ *   kept_stride >= sink_tokens + keep_topk + recent_tokens. sink_tokens = 0,
+ *   recent_tokens = window is the plain call.
  */
 SE_API size_t se_snapkv_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t window,
                                        int32_t max_prompt_len);
@@ -302,6 +314,11 @@ SE_API se_status_t se_snapkv_select(const float* scores, int32_t score_stride, c
                                     int32_t batch, int32_t num_kv_heads, int32_t window, int32_t max_prompt_len,
                                     int32_t pool_kernel, int32_t keep_topk, int32_t* kept_pos, int32_t kept_stride,
                                     int32_t* kept_counts, void* stream);
+SE_API se_status_t se_snapkv_select_windowed(const float* scores, int32_t score_stride, const int32_t* prompt_lens,
+                                             int32_t batch, int32_t num_kv_heads, int32_t window,
+                                             int32_t max_prompt_len, int32_t pool_kernel, int32_t keep_topk,
+                                             int32_t sink_tokens, int32_t recent_tokens, int32_t* kept_pos,
+                                             int32_t kept_stride, int32_t* kept_counts, void* stream);
 SE_API se_status_t se_snapkv_compact(const se_paged_kv_t* src, const int32_t* src_block_table, int32_t src_bt_stride,
                                      const int32_t* prompt_lens, int32_t batch, const se_paged_kv_t* dst,
                                      const int32_t* dst_block_table, int32_t dst_bt_stride, const int32_t* kept_pos,
@@ -314,6 +331,17 @@ SE_API se_status_t se_snapkv_score_and_compact(const se_paged_kv_t* src, const v
                                                const int32_t* dst_block_table, int32_t dst_bt_stride,
                                                int32_t* kept_pos, int32_t kept_stride, int32_t* kept_counts,
                                                void* workspace, size_t workspace_bytes, void* stream);
+SE_API se_status_t se_snapkv_score_and_compact_windowed(const se_paged_kv_t* src, const void* q_window,
+                                                        int32_t num_q_heads, int32_t window,
+                                                        const int32_t* src_block_table, int32_t src_bt_stride,
+                                                        const int32_t* prompt_lens, int32_t batch,
+                                                        int32_t max_prompt_len, int32_t pool_kernel,
+                                                        int32_t keep_topk, int32_t sink_tokens,
+                                                        int32_t recent_tokens, float sm_scale,
+                                                        const se_paged_kv_t* dst, const int32_t* dst_block_table,
+                                                        int32_t dst_bt_stride, int32_t* kept_pos,
+                                                        int32_t kept_stride, int32_t* kept_counts, void* workspace,
+                                                        size_t workspace_bytes, void* stream);
 
 /*
  * se_sparse_paged_decode_noalloc -- se_sparse_paged_decode for callers that

@@ -30,6 +30,14 @@ method written from its definition, with these readings:
    than ``keep`` candidates every position is kept;
 6. the kept rows are copied unchanged into compacted pages, kept token t landing
    in logical page t // page_size, slot t % page_size.
+
+Keep windows (Tables 9-12: SnapKV with sink 0/16/64 and recent 64/256/512
+tokens beside 4,096 or 15,808 selected, a 16-query observation window in
+Table 10; the budget excludes them, Table 10 caption). Reading: the first S
+positions and the last R positions (R >= W) are always kept; the ``keep``
+best pooled candidates among the positions between them are added; the scores
+and their pooling are those of steps 3-4 (every position before the window).
+S = 0, R = W is step 5.
 """
 from __future__ import annotations
 
@@ -84,6 +92,26 @@ def keep_positions(pooled: np.ndarray, n: int, window: int, keep: int) -> list:
     return chosen + list(range(cands, n))
 
 
+def keep_positions_windowed(pooled: np.ndarray, n: int, window: int, keep: int, sink: int, recent: int) -> list:
+    """Ascending: the first ``sink`` and last ``recent`` positions, plus the ``keep`` best pooled
+    candidates between them (ties: lower j); every position when no more than ``keep`` remain."""
+    always = set(range(min(sink, n))) | set(range(max(0, n - recent), n))
+    cands = [j for j in range(n - window) if j not in always]
+    if len(cands) <= keep:
+        return list(range(n))
+    chosen = sorted(cands, key=lambda j: (-pooled[j], j))[:keep]
+    return sorted(always | set(chosen))
+
+
+def kth_pooled_windowed(pooled: np.ndarray, n: int, window: int, keep: int, sink: int, recent: int):
+    """The keep-th largest pooled candidate score, or None when every position is kept."""
+    always = set(range(min(sink, n))) | set(range(max(0, n - recent), n))
+    cands = [pooled[j] for j in range(n - window) if j not in always]
+    if len(cands) <= keep:
+        return None
+    return sorted(cands, reverse=True)[keep - 1]
+
+
 def kth_pooled(pooled: np.ndarray, keep: int):
     """The keep-th largest pooled score (selection threshold), or None when all are kept."""
     if len(pooled) <= keep:
@@ -101,14 +129,20 @@ def request_keys(cache, block_table_row, h: int, n: int, page_size: int) -> np.n
 
 
 def snapkv_head(q_win_group, k_cache, block_table_row, h: int, n: int, window: int,
-                pool_kernel: int, keep: int, sm_scale: float, page_size: int = 16) -> dict:
-    """Scores, pooled scores, threshold and kept positions of one (request, KV head)."""
+                pool_kernel: int, keep: int, sm_scale: float, page_size: int = 16, sink: int = 0,
+                recent: int = None) -> dict:
+    """Scores, pooled scores, threshold and kept positions of one (request, KV head)
+    (keep windows ``sink`` / ``recent``; recent None is the observation window)."""
     K = request_keys(k_cache, block_table_row, h, n, page_size)
     alpha = window_probabilities(f64(q_win_group), K, sm_scale)
     s = candidate_scores(alpha)
     pooled = max_pool_clipped(s, pool_kernel)
-    return {"scores": s, "pooled": pooled, "threshold": kth_pooled(pooled, keep),
-            "kept": keep_positions(pooled, n, window, keep), "alpha_total": alpha.sum(),
+    if sink == 0 and recent in (None, window):
+        kept, tau = keep_positions(pooled, n, window, keep), kth_pooled(pooled, keep)
+    else:
+        kept = keep_positions_windowed(pooled, n, window, keep, sink, recent)
+        tau = kth_pooled_windowed(pooled, n, window, keep, sink, recent)
+    return {"scores": s, "pooled": pooled, "threshold": tau, "kept": kept, "alpha_total": alpha.sum(),
             "lse": window_lse(f64(q_win_group), K, sm_scale)}
 
 
@@ -131,5 +165,5 @@ def snapkv_step(inputs, requests=None, heads=None) -> dict:
             out[(b, h)] = snapkv_head(qg, inputs["k_cache"], inputs["block_table"][b], h,
                                       int(inputs["prompt_lens"][b]), inputs["window"],
                                       inputs["pool_kernel"], inputs["keep_topk"], inputs["sm_scale"],
-                                      inputs.get("page_size", 16))
+                                      inputs.get("page_size", 16), inputs.get("sink", 0), inputs.get("recent"))
     return out

@@ -24,7 +24,8 @@ __all__ = [
     "se_quest_select_workspace_size", "se_quest_select_pages", "se_quest_select_pages_windowed",
     "se_sparse_decode_workspace_size", "se_sparse_decode_plan", "se_sparse_paged_decode",
     "se_sparse_paged_decode_noalloc", "se_snapkv_workspace_size", "se_snapkv_window_scores", "se_snapkv_select",
-    "se_snapkv_compact", "se_snapkv_score_and_compact", "exported_symbols",
+    "se_snapkv_compact", "se_snapkv_score_and_compact", "se_snapkv_select_windowed",
+    "se_snapkv_score_and_compact_windowed", "exported_symbols",
 ]
 
 SE_OK = 0
@@ -76,9 +77,12 @@ _SIGNATURES = {
     "se_snapkv_workspace_size": (_Z, [_I, _I, _I, _I]),
     "se_snapkv_window_scores": (ctypes.c_int, [_KV, _P, _I, _I, _P, _I, _P, _I, _I, _F, _P, _I, _P, _P, _Z, _P]),
     "se_snapkv_select": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
+    "se_snapkv_select_windowed": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
     "se_snapkv_compact": (ctypes.c_int, [_KV, _P, _I, _P, _I, _KV, _P, _I, _P, _I, _P, _P]),
     "se_snapkv_score_and_compact": (ctypes.c_int, [_KV, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _F, _KV, _P, _I, _P,
                                                    _I, _P, _P, _Z, _P]),
+    "se_snapkv_score_and_compact_windowed": (ctypes.c_int, [_KV, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F,
+                                                            _KV, _P, _I, _P, _I, _P, _P, _Z, _P]),
 }
 
 _lib = None
@@ -309,6 +313,18 @@ def se_snapkv_select(scores, prompt_lens, num_kv_heads: int, window: int, max_pr
                                 _ptr(kept_counts, torch.int32, "kept_counts"), _stream(stream)))
 
 
+def se_snapkv_select_windowed(scores, prompt_lens, num_kv_heads: int, window: int, max_prompt_len: int,
+                              pool_kernel: int, keep_topk: int, sink_tokens: int, recent_tokens: int, kept_pos,
+                              kept_counts, stream=None):
+    lib = load_library()
+    _check(lib.se_snapkv_select_windowed(_ptr(scores, torch.float32, "scores"), scores.shape[-1],
+                                         _ptr(prompt_lens, torch.int32, "prompt_lens"), prompt_lens.shape[0],
+                                         int(num_kv_heads), int(window), int(max_prompt_len), int(pool_kernel),
+                                         int(keep_topk), int(sink_tokens), int(recent_tokens),
+                                         _ptr(kept_pos, torch.int32, "kept_pos"), kept_pos.shape[-1],
+                                         _ptr(kept_counts, torch.int32, "kept_counts"), _stream(stream)))
+
+
 def se_snapkv_compact(src: SEPagedKV, src_block_table, prompt_lens, dst: SEPagedKV, dst_block_table, kept_pos,
                       kept_counts, stream=None):
     lib = load_library()
@@ -335,3 +351,18 @@ def se_snapkv_score_and_compact(src: SEPagedKV, q_window, src_block_table, promp
                                            kept_pos.shape[-1], _ptr(kept_counts, torch.int32, "kept_counts"),
                                            _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                                            _stream(stream)))
+
+
+def se_snapkv_score_and_compact_windowed(src: SEPagedKV, q_window, src_block_table, prompt_lens, max_prompt_len: int,
+                                         pool_kernel: int, keep_topk: int, sink_tokens: int, recent_tokens: int,
+                                         sm_scale: float, dst: SEPagedKV, dst_block_table, kept_pos, kept_counts,
+                                         workspace, stream=None):
+    lib = load_library()
+    _check(lib.se_snapkv_score_and_compact_windowed(
+        ctypes.byref(src), _ptr(q_window, torch.bfloat16, "q_window"), q_window.shape[2], q_window.shape[1],
+        _ptr(src_block_table, torch.int32, "src_block_table"), src_block_table.shape[1],
+        _ptr(prompt_lens, torch.int32, "prompt_lens"), prompt_lens.shape[0], int(max_prompt_len), int(pool_kernel),
+        int(keep_topk), int(sink_tokens), int(recent_tokens), float(sm_scale), ctypes.byref(dst),
+        _ptr(dst_block_table, torch.int32, "dst_block_table"), dst_block_table.shape[1],
+        _ptr(kept_pos, torch.int32, "kept_pos"), kept_pos.shape[-1], _ptr(kept_counts, torch.int32, "kept_counts"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))

@@ -475,15 +475,19 @@ se_status_t se_snapkv_window_scores(const se_paged_kv_t* src, const void* q_wind
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
 }
 
-se_status_t se_snapkv_select(const float* scores, int32_t score_stride, const int32_t* prompt_lens, int32_t batch,
-                             int32_t num_kv_heads, int32_t window, int32_t max_prompt_len, int32_t pool_kernel,
-                             int32_t keep_topk, int32_t* kept_pos, int32_t kept_stride, int32_t* kept_counts,
-                             void* stream) {
-  static const char* fn = "se_snapkv_select";
+se_status_t se_snapkv_select_windowed(const float* scores, int32_t score_stride, const int32_t* prompt_lens,
+                                      int32_t batch, int32_t num_kv_heads, int32_t window, int32_t max_prompt_len,
+                                      int32_t pool_kernel, int32_t keep_topk, int32_t sink_tokens,
+                                      int32_t recent_tokens, int32_t* kept_pos, int32_t kept_stride,
+                                      int32_t* kept_counts, void* stream) {
+  static const char* fn = "se_snapkv_select_windowed";
   if (batch < 0 || num_kv_heads < 1 || window < 1 || max_prompt_len < 0) return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
   if (pool_kernel < 1 || pool_kernel % 2 == 0) return fail(SE_ERR_INVALID_ARG, fn, "pool_kernel must be odd");
   if (keep_topk < 1) return fail(SE_ERR_INVALID_ARG, fn, "keep_topk < 1");
-  if (kept_stride < keep_topk + window) return fail(SE_ERR_INVALID_ARG, fn, "kept_stride < keep_topk + window");
+  if (sink_tokens < 0 || recent_tokens < window || sink_tokens > (1 << 30) || recent_tokens > (1 << 30))
+    return fail(SE_ERR_INVALID_ARG, fn, "sink_tokens < 0 or recent_tokens < window");
+  if ((long long)kept_stride < (long long)sink_tokens + keep_topk + recent_tokens)
+    return fail(SE_ERR_INVALID_ARG, fn, "kept_stride < sink_tokens + keep_topk + recent_tokens");
   if (score_stride < snap_score_stride(max_prompt_len, window))
     return fail(SE_ERR_INVALID_ARG, fn, "score_stride < max_prompt_len - window");
   if (max_prompt_len - window > se::snapkv_select_max_candidates())
@@ -497,9 +501,17 @@ se_status_t se_snapkv_select(const float* scores, int32_t score_stride, const in
   cudaError_t e = current_device(&d);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   e = se::launch_snapkv_select(scores, score_stride, prompt_lens, batch, num_kv_heads, window, max_prompt_len,
-                               pool_kernel, keep_topk, kept_pos, kept_stride, kept_counts, d->err,
-                               static_cast<cudaStream_t>(stream));
+                               pool_kernel, keep_topk, sink_tokens, recent_tokens, kept_pos, kept_stride, kept_counts,
+                               d->err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+se_status_t se_snapkv_select(const float* scores, int32_t score_stride, const int32_t* prompt_lens, int32_t batch,
+                             int32_t num_kv_heads, int32_t window, int32_t max_prompt_len, int32_t pool_kernel,
+                             int32_t keep_topk, int32_t* kept_pos, int32_t kept_stride, int32_t* kept_counts,
+                             void* stream) {
+  return se_snapkv_select_windowed(scores, score_stride, prompt_lens, batch, num_kv_heads, window, max_prompt_len,
+                                   pool_kernel, keep_topk, 0, window, kept_pos, kept_stride, kept_counts, stream);
 }
 
 se_status_t se_snapkv_compact(const se_paged_kv_t* src, const int32_t* src_block_table, int32_t src_bt_stride,
@@ -529,15 +541,16 @@ se_status_t se_snapkv_compact(const se_paged_kv_t* src, const int32_t* src_block
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
 }
 
-se_status_t se_snapkv_score_and_compact(const se_paged_kv_t* src, const void* q_window, int32_t num_q_heads,
-                                        int32_t window, const int32_t* src_block_table, int32_t src_bt_stride,
-                                        const int32_t* prompt_lens, int32_t batch, int32_t max_prompt_len,
-                                        int32_t pool_kernel, int32_t keep_topk, float sm_scale,
-                                        const se_paged_kv_t* dst, const int32_t* dst_block_table,
-                                        int32_t dst_bt_stride, int32_t* kept_pos, int32_t kept_stride,
-                                        int32_t* kept_counts, void* workspace, size_t workspace_bytes,
-                                        void* stream) {
-  static const char* fn = "se_snapkv_score_and_compact";
+se_status_t se_snapkv_score_and_compact_windowed(const se_paged_kv_t* src, const void* q_window,
+                                                 int32_t num_q_heads, int32_t window, const int32_t* src_block_table,
+                                                 int32_t src_bt_stride, const int32_t* prompt_lens, int32_t batch,
+                                                 int32_t max_prompt_len, int32_t pool_kernel, int32_t keep_topk,
+                                                 int32_t sink_tokens, int32_t recent_tokens, float sm_scale,
+                                                 const se_paged_kv_t* dst, const int32_t* dst_block_table,
+                                                 int32_t dst_bt_stride, int32_t* kept_pos, int32_t kept_stride,
+                                                 int32_t* kept_counts, void* workspace, size_t workspace_bytes,
+                                                 void* stream) {
+  static const char* fn = "se_snapkv_score_and_compact_windowed";
   if (!src) return fail(SE_ERR_INVALID_ARG, fn, "src is NULL");
   const size_t need = se_snapkv_workspace_size(batch, src->num_kv_heads, window, max_prompt_len);
   if (workspace_bytes < need) return fail(SE_ERR_WORKSPACE, fn, "workspace too small");
@@ -549,11 +562,26 @@ se_status_t se_snapkv_score_and_compact(const se_paged_kv_t* src, const void* q_
                                            prompt_lens, batch, max_prompt_len, sm_scale, scores, stride, nullptr,
                                            workspace, part, stream);
   if (st != SE_OK) return st;
-  st = se_snapkv_select(scores, stride, prompt_lens, batch, src->num_kv_heads, window, max_prompt_len, pool_kernel,
-                        keep_topk, kept_pos, kept_stride, kept_counts, stream);
+  st = se_snapkv_select_windowed(scores, stride, prompt_lens, batch, src->num_kv_heads, window, max_prompt_len,
+                                 pool_kernel, keep_topk, sink_tokens, recent_tokens, kept_pos, kept_stride,
+                                 kept_counts, stream);
   if (st != SE_OK) return st;
   return se_snapkv_compact(src, src_block_table, src_bt_stride, prompt_lens, batch, dst, dst_block_table,
                            dst_bt_stride, kept_pos, kept_stride, kept_counts, stream);
+}
+
+se_status_t se_snapkv_score_and_compact(const se_paged_kv_t* src, const void* q_window, int32_t num_q_heads,
+                                        int32_t window, const int32_t* src_block_table, int32_t src_bt_stride,
+                                        const int32_t* prompt_lens, int32_t batch, int32_t max_prompt_len,
+                                        int32_t pool_kernel, int32_t keep_topk, float sm_scale,
+                                        const se_paged_kv_t* dst, const int32_t* dst_block_table,
+                                        int32_t dst_bt_stride, int32_t* kept_pos, int32_t kept_stride,
+                                        int32_t* kept_counts, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  return se_snapkv_score_and_compact_windowed(src, q_window, num_q_heads, window, src_block_table, src_bt_stride,
+                                              prompt_lens, batch, max_prompt_len, pool_kernel, keep_topk, 0, window,
+                                              sm_scale, dst, dst_block_table, dst_bt_stride, kept_pos, kept_stride,
+                                              kept_counts, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

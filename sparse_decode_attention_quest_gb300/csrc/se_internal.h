@@ -108,10 +108,12 @@ cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const KvView& kv, cons
                                  int32_t window, const int32_t* bt, int32_t bt_stride, const int32_t* lens,
                                  int32_t batch, int32_t max_len, float sm_scale, float* scores, int32_t score_stride,
                                  float* row_lse, void* part_ws, int sm_count, unsigned* err, cudaStream_t stream);
+// Keeps positions 0 .. sink - 1 and n - recent .. n - 1 (recent >= window) and the keep best
+// pooled candidates between them.
 cudaError_t launch_snapkv_select(const float* scores, int32_t score_stride, const int32_t* lens, int32_t batch,
                                  int32_t num_kv_heads, int32_t window, int32_t max_len, int32_t pool, int32_t keep,
-                                 int32_t* kept, int32_t kept_stride, int32_t* kept_counts, unsigned* err,
-                                 cudaStream_t stream);
+                                 int32_t sink, int32_t recent, int32_t* kept, int32_t kept_stride,
+                                 int32_t* kept_counts, unsigned* err, cudaStream_t stream);
 cudaError_t launch_snapkv_gather(const KvView& src, uint16_t* dk, uint16_t* dv, int32_t dst_num_pages,
                                  const int32_t* src_bt, int32_t src_bt_stride, const int32_t* dst_bt,
                                  int32_t dst_bt_stride, const int32_t* lens, int32_t batch, const int32_t* kept,

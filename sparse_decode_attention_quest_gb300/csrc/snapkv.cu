@@ -469,10 +469,10 @@ __device__ __forceinline__ void index_order_prefix(uint64_t flags, int E, int* c
 // memory, per-candidate flags in a 64-bit mask.
 __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ lens, int32_t H, int32_t W,
-    int32_t max_len, int32_t pool, int32_t keep, int32_t* __restrict__ kept, int32_t kept_stride,
-    int32_t* __restrict__ kept_counts, unsigned* err) {
+    int32_t max_len, int32_t pool, int32_t keep, int32_t sink, int32_t recent, int32_t* __restrict__ kept,
+    int32_t kept_stride, int32_t* __restrict__ kept_counts, unsigned* err) {
   pdl_enter();
-  extern __shared__ float pooled[];  // [C]
+  extern __shared__ float pooled[];  // [n - W]
   __shared__ int hist[kBuckets];
   __shared__ float s_min[kSelWarps], s_max[kSelWarps];
   __shared__ int wtot[kSelWarps];
@@ -492,7 +492,11 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     }
     return;
   }
-  const int C = n - W;
+  // Scored positions [0, n - W); candidates [c0, c1): neither among the first
+  // `sink` positions nor among the last `recent` (>= W) ones.
+  const int CS = n - W;
+  const int c1 = max(0, n - recent), c0 = min(sink, c1);
+  const int C = c1 - c0;  // candidate j is position c0 + j
   int32_t* out = kept + (size_t)pair * kept_stride;
   if (C <= keep) {
     for (int i = tid; i < n; i += kSelThreads) out[i] = i;
@@ -500,19 +504,22 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     return;
   }
   const float* sc = scores + (size_t)pair * score_stride;
-  const int E = (C + kSelThreads - 1) / kSelThreads;
   const int half = pool / 2;
+  // Max-pool over the scored positions (window clipped to them).
+  for (int i = tid; i < CS; i += kSelThreads) {
+    float m = -INFINITY;
+    for (int t = max(0, i - half); t <= min(CS - 1, i + half); ++t) m = fmaxf(m, sc[t]);
+    pooled[i] = m;
+  }
+  __syncthreads();
+  const float* pc = pooled + c0;  // pooled score of candidate j
+  const int E = (C + kSelThreads - 1) / kSelThreads;
   float lmin = INFINITY, lmax = -INFINITY;
   for (int e = 0; e < E; ++e) {
     const int i = tid + e * kSelThreads;
-    if (i < C) {
-      float m = -INFINITY;
-      for (int t = max(0, i - half); t <= min(C - 1, i + half); ++t) m = fmaxf(m, sc[t]);
-      pooled[i] = m;
-      if (isfinite(m)) {
-        lmin = fminf(lmin, m);
-        lmax = fmaxf(lmax, m);
-      }
+    if (i < C && isfinite(pc[i])) {
+      lmin = fminf(lmin, pc[i]);
+      lmax = fmaxf(lmax, pc[i]);
     }
   }
   hist[tid] = 0;
@@ -540,7 +547,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   };
   for (int e = 0; e < E; ++e) {
     const int i = tid + e * kSelThreads;
-    if (i < C) atomicAdd(&hist[bucket(pooled[i])], 1);
+    if (i < C) atomicAdd(&hist[bucket(pc[i])], 1);
   }
   __syncthreads();
   const int hc = hist[tid];
@@ -567,9 +574,9 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   if (m <= kMaxMembers) {
     for (int e = 0; e < E; ++e) {
       const int i = tid + e * kSelThreads;
-      if (i < C && bucket(pooled[i]) == B) {
+      if (i < C && bucket(pc[i]) == B) {
         const int slot = atomicAdd(&s_info[2], 1);
-        mem_val[slot] = pooled[i];
+        mem_val[slot] = pc[i];
         mem_idx[slot] = i;
       }
     }
@@ -604,7 +611,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
       for (int e = 0; e < E; ++e) {
         const int i = tid + e * kSelThreads;
         if (i < C) {
-          const float v = pooled[i];
+          const float v = pc[i];
           const uint32_t key = order_key(v);
           if (bucket(v) == B && (key & mask) == prefix) atomicAdd(&hh[(key >> shift) & 255u], 1);
         }
@@ -651,7 +658,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   uint64_t eqf = 0;
   for (int e = 0; e < E; ++e) {
     const int i = tid + e * kSelThreads;
-    if (i < C && order_key(pooled[i]) == T) eqf |= 1ull << e;
+    if (i < C && order_key(pc[i]) == T) eqf |= 1ull << e;
   }
   index_order_prefix(eqf, E, cnt, warp, lane);
   uint64_t self = 0;
@@ -660,7 +667,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     const unsigned ball = __ballot_sync(0xffffffffu, (eqf >> e) & 1ull);
     const int eq_rank = cnt[e * 32 + warp] + __popc(ball & lt);
     if (i < C) {
-      const uint32_t key = order_key(pooled[i]);
+      const uint32_t key = order_key(pc[i]);
       if (key > T || (key == T && eq_rank < need_eq)) self |= 1ull << e;
     }
   }
@@ -670,11 +677,12 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     const unsigned ball = __ballot_sync(0xffffffffu, (self >> e) & 1ull);
     if ((self >> e) & 1ull) {
       const int pos = cnt[e * 32 + warp] + __popc(ball & lt);
-      if (pos < keep) out[pos] = tid + e * kSelThreads;
+      if (pos < keep) out[c0 + pos] = c0 + tid + e * kSelThreads;
     }
   }
-  for (int w = tid; w < W; w += kSelThreads) out[keep + w] = C + w;
-  if (tid == 0) kept_counts[pair] = keep + W;
+  for (int i = tid; i < c0; i += kSelThreads) out[i] = i;
+  for (int w = tid; w < n - c1; w += kSelThreads) out[c0 + keep + w] = c1 + w;
+  if (tid == 0) kept_counts[pair] = c0 + keep + (n - c1);
 }
 
 // ------------------------------------------------------------------ compaction
@@ -781,8 +789,8 @@ cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const KvView& kv, cons
 
 cudaError_t launch_snapkv_select(const float* scores, int32_t score_stride, const int32_t* lens, int32_t batch,
                                  int32_t num_kv_heads, int32_t window, int32_t max_len, int32_t pool, int32_t keep,
-                                 int32_t* kept, int32_t kept_stride, int32_t* kept_counts, unsigned* err,
-                                 cudaStream_t stream) {
+                                 int32_t sink, int32_t recent, int32_t* kept, int32_t kept_stride,
+                                 int32_t* kept_counts, unsigned* err, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
   const int maxc = max(max_len - window, 1);
   const size_t smem = (size_t)maxc * sizeof(float);
@@ -791,7 +799,7 @@ cudaError_t launch_snapkv_select(const float* scores, int32_t score_stride, cons
   {
     const cudaError_t le = launch_pdl(snapkv_select_kernel, dim3(batch * num_kv_heads), dim3(kSelThreads), smem,
                                       stream, scores, score_stride, lens, num_kv_heads, window, max_len, pool, keep,
-                                      kept, kept_stride, kept_counts, err);
+                                      sink, recent, kept, kept_stride, kept_counts, err);
     if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();

@@ -14,6 +14,8 @@ from .workloads import (  # noqa: F401
     QWEN3_4B_QUEST_32K,
     QWEN3_30B_A3B_QUEST_128K,
     SNAPKV_PREFILL_32K,
+    SNAPKV_AIME_32K,
+    SNAPKV_AGENT_32K,
     MLA_GLM_QUEST_32K,
     QUEST_WORKLOADS,
     make_quest_decode_inputs,

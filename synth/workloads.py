@@ -216,7 +216,9 @@ class SnapKVWorkload:
     prompt_max: int
     window: int = 32             # observation window (last queries of the prompt)
     pool_kernel: int = 7
-    keep_topk: int = 2016        # positions kept besides the window
+    keep_topk: int = 2016        # positions selected besides the kept windows
+    keep_sink: int = 0           # first positions always kept
+    keep_recent: int = 0         # last positions always kept (0: the observation window)
     sink_fraction: float = 0.05  # share of key positions given the sink direction
     sink_logit_shift: float = 3.0
     permuted_table: bool = True
@@ -225,6 +227,10 @@ class SnapKVWorkload:
     @property
     def group(self) -> int:
         return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def recent(self) -> int:
+        return self.keep_recent or self.window
 
     def scaled(self, **kw) -> "SnapKVWorkload":
         return replace(self, **kw)
@@ -235,6 +241,18 @@ class SnapKVWorkload:
 SNAPKV_PREFILL_32K = SnapKVWorkload(
     name="snapkv_prefill_b4_32k", seed=3, batch=4, num_q_heads=32, num_kv_heads=8, head_dim=128,
     prompt_min=32768, prompt_max=32768)
+
+
+# The same shape with the AIME-run SnapKV settings: 16-query observation window, sink 16,
+# recent 64, 4,096 selected (4,176 kept).
+SNAPKV_AIME_32K = SnapKVWorkload(
+    name="snapkv_aime_b4_32k", seed=5, batch=4, num_q_heads=32, num_kv_heads=8, head_dim=128,
+    prompt_min=32768, prompt_max=32768, window=16, keep_topk=4096, keep_sink=16, keep_recent=64)
+
+# ... and with the agent-run settings: 32-query window, sink 64, recent 512, 15,808 selected.
+SNAPKV_AGENT_32K = SnapKVWorkload(
+    name="snapkv_agent_b4_32k", seed=6, batch=4, num_q_heads=32, num_kv_heads=8, head_dim=128,
+    prompt_min=32768, prompt_max=32768, window=32, keep_topk=15808, keep_sink=64, keep_recent=512)
 
 
 @dataclass
@@ -261,7 +279,7 @@ def make_snapkv_inputs(wl: SnapKVWorkload, device="cpu", poison_tail=True) -> Sn
         lens = torch.randint(wl.prompt_min, wl.prompt_max + 1, (wl.batch,), generator=cpu_g).tolist()
     ppr = [pages_for_tokens(n, wl.page_size) for n in lens]
     bt, num_pages = _block_table(ppr, wl.permuted_table, cpu_g)
-    kept = [min(n, wl.keep_topk + wl.window) for n in lens]
+    kept = [min(n, wl.keep_sink + wl.keep_topk + wl.recent) for n in lens]
     dppr = [pages_for_tokens(k, wl.page_size) for k in kept]
     dbt, dst_pages = _block_table(dppr, wl.permuted_table, cpu_g)
 

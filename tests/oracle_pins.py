@@ -330,6 +330,28 @@ def check_keep_positions(snapkv):
         assert len(got) == min(n, keep + W)
 
 
+def check_keep_positions_windowed(snapkv):
+    """Rank counting from the definition: j is kept when j < S, j >= n - R, or (j < n - W and
+    fewer than keep other candidates beat it); every position when keep covers the candidates."""
+    rng = _rng(23)
+    for _ in range(200):
+        n = int(rng.integers(2, 40))
+        W = int(rng.integers(1, n + 1))
+        R = int(rng.integers(W, n + 3))
+        S = int(rng.integers(0, 12))
+        keep = int(rng.integers(1, 8))
+        pooled = rng.integers(0, 4, size=n - W).astype(float)
+        cands = [j for j in range(n - W) if j >= S and j < n - R]
+        if len(cands) <= keep:
+            ref = list(range(n))
+        else:
+            ref = [j for j in range(n) if j < S or j >= n - R or (j in cands and sum(
+                1 for r in cands if pooled[r] > pooled[j] or (pooled[r] == pooled[j] and r < j)) < keep)]
+        assert snapkv.keep_positions_windowed(pooled, n, W, keep, S, R) == ref, (n, W, R, S, keep)
+        if S == 0 and R == W:
+            assert ref == snapkv.keep_positions(pooled, n, W, keep)
+
+
 def check_snapkv_head_end_to_end(snapkv):
     """Whole head against torch routines: softmax, max_pool1d and a stable sort."""
     rng = _rng(16)
@@ -364,4 +386,4 @@ QUEST_CHECKS = [check_summary_bruteforce, check_append_matches_rebuild, check_bo
                 check_selection_uses_the_bound, check_select_windowed_bruteforce,
                 check_select_windowed_reduces_to_plain]
 SNAPKV_CHECKS = [check_window_probabilities, check_window_lse, check_candidate_scores, check_max_pool,
-                 check_keep_positions, check_snapkv_head_end_to_end, check_compaction_exact]
+                 check_keep_positions, check_keep_positions_windowed, check_snapkv_head_end_to_end, check_compaction_exact]

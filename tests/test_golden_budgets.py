@@ -8,6 +8,7 @@ import numpy as np
 
 from oracle import budgets
 from oracle import quest
+from oracle import snapkv
 from synth import SNAPKV_PREFILL_32K, QWEN3_30B_A3B_QUEST_128K, QWEN3_4B_QUEST_32K
 
 GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "table_budgets.json")))
@@ -46,3 +47,22 @@ def test_windowed_selection_keeps_the_printed_total(row):
     pages = quest.select_pages_windowed(scores, L, ps, budgets.selected_pages(row["selected"]), row["sink"],
                                         row["recent"])
     assert len(pages) * ps == row["total"]
+
+
+@pytest.mark.parametrize("row", [r for r in GOLD["rows"] if r["method"] == "SnapKV"], ids=lambda r: r["cite"])
+def test_snapkv_windows_keep_the_printed_total(row):
+    # A 32K prompt, the 16-query observation window of that run: sink + selected + recent.
+    n, W = 32768, 16
+    pooled = np.random.default_rng(1).standard_normal(n - W)
+    kept = snapkv.keep_positions_windowed(pooled, n, W, row["selected"], row["sink"], row["recent"])
+    assert len(kept) == row["total"]
+
+
+def test_snapkv_workloads_follow_the_tables():
+    from synth import SNAPKV_AGENT_32K, SNAPKV_AIME_32K
+    aime = [r for r in GOLD["rows"] if r["method"] == "SnapKV"][0]
+    wl = SNAPKV_AIME_32K
+    assert (wl.keep_sink, wl.keep_recent, wl.keep_topk, wl.window) == (aime["sink"], aime["recent"],
+                                                                       aime["selected"], 16)
+    wl = SNAPKV_AGENT_32K
+    assert (wl.keep_sink, wl.keep_recent, wl.keep_topk) == (64, 512, 15808)

@@ -106,6 +106,12 @@ def _q_windowed_sink_in_budget(scores, n_tokens, page_size, topk, sink_tokens, r
     return sorted(set(kept) | set(sorted(cands, key=lambda p: (-scores[p], p))[:k]))
 
 
+def _s_windowed_recent_is_window(pooled, n, window, keep, sink, recent):
+    # recent window taken as the observation window (the larger recent window ignored)
+    return snapkv.keep_positions(pooled, n, window, keep) if sink == 0 else \
+        sorted(set(range(min(sink, n))) | set(snapkv.keep_positions(pooled, n, window, keep)))
+
+
 MUTANTS = [
     (quest, "page_summary", _q_summary_swapped, pins.QUEST_CHECKS),
     (quest, "append_to_summary", _q_append_never_resets, pins.QUEST_CHECKS),
@@ -122,6 +128,7 @@ MUTANTS = [
     (snapkv, "candidate_scores", _s_scores_include_window, pins.SNAPKV_CHECKS),
     (snapkv, "max_pool_clipped", _s_pool_right_only, pins.SNAPKV_CHECKS),
     (snapkv, "keep_positions", _s_keep_ties_high, pins.SNAPKV_CHECKS),
+    (snapkv, "keep_positions_windowed", _s_windowed_recent_is_window, pins.SNAPKV_CHECKS),
 ]
 
 

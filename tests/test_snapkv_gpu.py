@@ -14,7 +14,7 @@ import torch
 
 import oracle.snapkv as osk
 import sparse_decode_attention_quest_gb300 as se
-from synth import SNAPKV_PREFILL_32K, make_snapkv_inputs
+from synth import SNAPKV_AGENT_32K, SNAPKV_AIME_32K, SNAPKV_PREFILL_32K, make_snapkv_inputs
 from tests.parity import exempt
 
 pytestmark = pytest.mark.gpu
@@ -44,9 +44,13 @@ def _run(x, dev, keep=None, pool=None):
     qw = x.q_window.to(dev)
     scale = 1.0 / math.sqrt(wl.head_dim)
     se.se_snapkv_window_scores(src, qw, bt, lens, max_len, scale, scores, lse, ws)
-    kept = torch.full((B, H, keep + W), -1, dtype=torch.int32, device=dev)
+    S, R = wl.keep_sink, wl.recent
+    kept = torch.full((B, H, S + keep + R), -1, dtype=torch.int32, device=dev)
     cnt = torch.zeros(B, H, dtype=torch.int32, device=dev)
-    se.se_snapkv_select(scores, lens, H, W, max_len, pool, keep, kept, cnt)
+    if S == 0 and R == W:
+        se.se_snapkv_select(scores, lens, H, W, max_len, pool, keep, kept, cnt)
+    else:
+        se.se_snapkv_select_windowed(scores, lens, H, W, max_len, pool, keep, S, R, kept, cnt)
     dk = torch.full((x.dst_num_pages, H, 16, 128), float("nan"), dtype=torch.bfloat16, device=dev)
     dv = torch.full_like(dk, float("nan"))
     dst = se.paged_kv(dk, dv, None)
@@ -54,7 +58,8 @@ def _run(x, dev, keep=None, pool=None):
     se.se_snapkv_compact(src, bt, lens, dst, dbt, kept, cnt)
     torch.cuda.synchronize()
     return dict(scores=scores.cpu(), lse=lse.cpu(), kept=kept.cpu(), cnt=cnt.cpu(), dk=dk.cpu(), dv=dv.cpu(),
-                ws=ws, src=src, qw=qw, bt=bt, lens=lens, dst=dst, dbt=dbt, scale=scale, keep=keep, pool=pool)
+                ws=ws, src=src, qw=qw, bt=bt, lens=lens, dst=dst, dbt=dbt, scale=scale, keep=keep, pool=pool,
+                sink=S, recent=R)
 
 
 def _check_pair(x, res, b, h):
@@ -62,7 +67,7 @@ def _check_pair(x, res, b, h):
     W, G = wl.window, wl.group
     n = x.prompt_lens[b]
     ref = osk.snapkv_head(x.q_window[b, :, h * G:(h + 1) * G, :], x.k_cache, x.src_block_table[b], h, n, W,
-                          res["pool"], res["keep"], res["scale"])
+                          res["pool"], res["keep"], res["scale"], sink=res["sink"], recent=res["recent"])
     # row log-sum-exp (fp32 sums of exact bf16 products)
     np.testing.assert_allclose(res["lse"][b, h].numpy(), ref["lse"].reshape(-1), rtol=0, atol=2e-3)
     # candidate scores (probability sums, fp32)
@@ -72,7 +77,8 @@ def _check_pair(x, res, b, h):
     cnt = int(res["cnt"][b, h])
     assert cnt == len(ref["kept"]), (cnt, len(ref["kept"]))
     kept = res["kept"][b, h, :cnt].tolist()
-    assert kept == sorted(set(kept)) and kept[-W:] == list(range(n - W, n))
+    assert kept == sorted(set(kept))
+    assert set(range(max(0, n - res["recent"]), n)) <= set(kept) and set(range(min(res["sink"], n))) <= set(kept)
     gs, rs = set(kept), set(ref["kept"])
     for j in range(n - W):
         if (j in gs) != (j in rs):
@@ -178,3 +184,55 @@ def test_snapkv_full_32k_sampled(cuda_device):
     xc.dst_block_table = x.dst_block_table.cpu()
     for b, h in ((0, 0), (wl.batch - 1, wl.num_kv_heads - 1), (1, 3)):
         _check_pair(xc, res, b, h)
+
+
+# ---------------------------------------------------------------- keep windows (sink / recent)
+@pytest.mark.parametrize("W,S,R,keep", [(16, 16, 64, 96), (32, 64, 512, 300), (32, 0, 256, 200), (32, 64, 32, 100)])
+def test_snapkv_windows_oracle_sized(cuda_device, W, S, R, keep):
+    wl = SNAPKV_PREFILL_32K.scaled(batch=2, prompt_min=700, prompt_max=2600, window=W, keep_topk=keep, keep_sink=S,
+                                   keep_recent=R, seed=12)
+    x = make_snapkv_inputs(wl)
+    res = _run(x, cuda_device)
+    for b in range(wl.batch):
+        for h in range(wl.num_kv_heads):
+            _check_pair(x, res, b, h)
+
+
+@pytest.mark.parametrize("kind", ["distinct", "ties"])
+def test_snapkv_windowed_select_exact_on_crafted_scores(cuda_device, kind):
+    g = torch.Generator().manual_seed(13)
+    W, H, S, R, keep = 16, 2, 64, 512, 4096
+    lens = [5000, 30000, 600]
+    stride = max(lens) - W
+    s = torch.rand(3, H, stride, generator=g) if kind == "distinct" else \
+        torch.randint(0, 4, (3, H, stride), generator=g).float() * 0.25
+    dev = cuda_device
+    kept = torch.full((3, H, S + keep + R), -1, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(3, H, dtype=torch.int32, device=dev)
+    se.se_snapkv_select_windowed(s.to(dev), torch.tensor(lens, dtype=torch.int32, device=dev), H, W, max(lens), 7,
+                                 keep, S, R, kept, cnt)
+    torch.cuda.synchronize()
+    for b, n in enumerate(lens):
+        for h in range(H):
+            pooled = osk.max_pool_clipped(s[b, h, :n - W].double().numpy(), 7)
+            ref = osk.keep_positions_windowed(pooled, n, W, keep, S, R)
+            assert kept[b, h, :int(cnt[b, h])].tolist() == ref, (kind, b, h)
+
+
+def _full_sampled(wl, dev, pairs):
+    x = make_snapkv_inputs(wl, device=dev)
+    res = _run(x, dev)
+    x.k_cache, x.v_cache, x.q_window = x.k_cache.cpu(), x.v_cache.cpu(), x.q_window.cpu()
+    x.src_block_table, x.dst_block_table = x.src_block_table.cpu(), x.dst_block_table.cpu()
+    for b, h in pairs:
+        _check_pair(x, res, b, h)
+
+
+def test_snapkv_aime_budget_full_32k_sampled(cuda_device):
+    # 16-query window, sink 16, recent 64, 4,096 selected
+    _full_sampled(SNAPKV_AIME_32K, cuda_device, ((0, 0), (3, 7)))
+
+
+def test_snapkv_agent_budget_full_32k_sampled(cuda_device):
+    # sink 64, recent 512, 15,808 selected: half of each 32K prompt kept
+    _full_sampled(SNAPKV_AGENT_32K, cuda_device, ((1, 2), (2, 5)))
