@@ -355,6 +355,7 @@ def run_ours(args, rank, world, local_rank):
             "snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, stream),
             "snapkv_aime_b4_32k": _snapkv_extra(args, dev, flush, stream, _snapkv_wl("SNAPKV_AIME_32K")),
             "snapkv_agent_b4_32k": _snapkv_extra(args, dev, flush, stream, _snapkv_wl("SNAPKV_AGENT_32K")),
+            "snapkv_periodic_evict_aime_b4": _periodic_evict_extra(args, dev, flush, stream),
             "mla_glm_quest_b64_32k": _mla_extra(args, dev, flush, stream),
             "qwen3_30b_a3b_quest_sink64_recent512_b32_128k": _windows_extra(args, dev, flush, stream)}
     if rank == 0 and not args.no_cpu_baseline:
@@ -524,6 +525,22 @@ def _windows_extra(args, dev, flush, stream):
     recent 512, 1,472 selected tokens (92 pages), 2,048 kept in total."""
     from synth import QWEN3_30B_A3B_QUEST_128K
     return _quest_extra(args, dev, flush, stream, QWEN3_30B_A3B_QUEST_128K.scaled(topk_pages=92), 64, 512)
+
+
+def _periodic_evict_extra(args, dev, flush, stream):
+    """Decode-time SnapKV eviction with the AIME-run settings (Table 10: window 16, sink 16,
+    recent 64, 4,096 selected, every 1,024 decode steps): one eviction over the compacted
+    4,176 positions plus the 1,024 appended since the last one, and its cost spread over the
+    1,024 decode steps of a period."""
+    from synth import SNAPKV_AIME_32K
+    period = 1024
+    n = SNAPKV_AIME_32K.keep_sink + SNAPKV_AIME_32K.keep_topk + SNAPKV_AIME_32K.recent + period
+    r = _snapkv_extra(args, dev, flush, stream,
+                      SNAPKV_AIME_32K.scaled(name="snapkv_periodic_aime_b4", prompt_min=n, prompt_max=n))
+    r["period_decode_steps"] = period
+    r["positions_before_eviction"] = n
+    r["amortized_us_per_decode_step"] = round(r["ms_per_call"] * 1e3 / period, 4)
+    return r
 
 
 def _snapkv_wl(name):

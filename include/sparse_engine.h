@@ -131,6 +131,9 @@ SE_API se_status_t se_quest_build_summaries(const se_paged_kv_t* kv, const int32
  *   k_new: bf16 [batch][num_kv_heads][head_dim];
  *   v_new: bf16 [batch][num_kv_heads][head_dim_v], or NULL when kv->v == kv->k
  *   (latent cache: the value is part of the key row).
+ * With kv->summary NULL only the K/V rows are written: the decode-time append of
+ * a cache that keeps no Quest summaries (a SnapKV-compacted cache between its
+ * periodic evictions, Table 10: eviction every 1,024 decode steps).
  */
 SE_API se_status_t se_quest_update_summaries(const se_paged_kv_t* kv, const void* k_new, const void* v_new,
                                       const int32_t* block_table, int32_t bt_stride,

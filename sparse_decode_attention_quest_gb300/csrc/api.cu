@@ -193,7 +193,7 @@ se_status_t se_quest_update_summaries(const se_paged_kv_t* kv, const void* k_new
                                       const int32_t* block_table, int32_t bt_stride,
                                       const int32_t* seq_lens_before, int32_t batch, void* stream) {
   static const char* fn = "se_quest_update_summaries";
-  se_status_t st = check_kv(fn, kv, true);
+  se_status_t st = check_kv(fn, kv, false);  // summary NULL: the K/V rows only
   if (st != SE_OK) return st;
   if (batch < 0) return fail(SE_ERR_INVALID_ARG, fn, "batch < 0");
   if (batch > 0 && (!k_new || !block_table || !seq_lens_before))

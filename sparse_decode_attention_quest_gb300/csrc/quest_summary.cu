@@ -93,11 +93,13 @@ __global__ void __launch_bounds__(256) append_update_kernel(KvView kv, uint16_t*
   const size_t blk = (size_t)phys * H + h;
   const uint32_t* src = reinterpret_cast<const uint32_t*>(k_new + (size_t)item * D);
   uint32_t* dst = reinterpret_cast<uint32_t*>(k_mut + (blk * kPageSize + slot) * kv.row_stride_k);
-  uint32_t* smin = reinterpret_cast<uint32_t*>(kv.summary + blk * 2 * D);
+  // A cache without Quest summaries (e.g. a SnapKV-compacted one) only gets the rows.
+  uint32_t* smin = kv.summary ? reinterpret_cast<uint32_t*>(kv.summary + blk * 2 * D) : nullptr;
   uint32_t* smax = smin + (D >> 1);
   for (int c = lane; c < (D >> 1); c += 32) {
     const uint32_t x = src[c];
     dst[c] = x;
+    if (smin == nullptr) continue;
     if (slot == 0) {
       smin[c] = x;
       smax[c] = x;

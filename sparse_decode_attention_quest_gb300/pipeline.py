@@ -15,8 +15,9 @@ from typing import Optional, Sequence
 import torch
 
 from . import (paged_kv, se_quest_build_summaries, se_quest_kept_pages_max, se_quest_score_pages,
-               se_quest_topk_pages_windowed, se_quest_update_summaries, se_sparse_decode_plan,
-               se_sparse_decode_workspace_size, se_sparse_paged_decode)
+               se_quest_topk_pages_windowed, se_quest_update_summaries, se_snapkv_score_and_compact_windowed,
+               se_snapkv_workspace_size, se_sparse_decode_plan, se_sparse_decode_workspace_size,
+               se_sparse_paged_decode)
 
 PAGE = 16
 
@@ -97,3 +98,72 @@ class QuestDecodeStep:
             events[3].record(s)
         self.attend(q, seq_lens, stream=s)
         return self.out
+
+
+class SnapKVDecodeCache:
+    """A SnapKV-compacted paged cache through decode: the prefill eviction, then every
+    ``period`` decode steps another eviction over the compacted pages (SparseEngine, Table 10:
+    SnapKV with a 16-query observation window, sink 16, recent 64, 4,096 selected, eviction
+    every 1,024 decode steps).
+
+    Two page pools of the same size, the live one and the one the next eviction compacts
+    into; request b owns pages b * P .. b * P + P - 1 of each (P = pages for sink + keep +
+    recent + period tokens). A decode step appends its token's K/V rows to the live pool and
+    keeps its query if it is among the last ``window`` of the period, in order: the
+    observation window of the next eviction. Host orchestration only; appends and
+    evictions run in the library's kernels.
+    """
+
+    def __init__(self, batch: int, num_kv_heads: int, num_q_heads: int, head_dim: int, window: int,
+                 pool_kernel: int, keep_topk: int, sink_tokens: int, recent_tokens: int, period: int, device,
+                 sm_scale: Optional[float] = None):
+        if period < window:
+            raise ValueError("period must cover the observation window")
+        self.B, self.H, self.Hq, self.D = batch, num_kv_heads, num_q_heads, head_dim
+        self.W, self.pool, self.keep = window, pool_kernel, keep_topk
+        self.sink, self.recent, self.period = sink_tokens, recent_tokens, period
+        self.sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(head_dim)
+        self.kept_max = sink_tokens + keep_topk + recent_tokens
+        self.max_len = self.kept_max + period
+        self.P = (self.max_len + PAGE - 1) // PAGE
+        shape = (batch * self.P, num_kv_heads, PAGE, head_dim)
+        self.k = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.v = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.block_table = torch.arange(batch * self.P, dtype=torch.int32, device=device).view(batch, self.P)
+        self.live = 0
+        self.lens = torch.zeros(batch, dtype=torch.int32, device=device)
+        self.q_window = torch.zeros(batch, window, num_q_heads, head_dim, dtype=torch.bfloat16, device=device)
+        self.kept = torch.empty(batch, num_kv_heads, self.kept_max, dtype=torch.int32, device=device)
+        self.counts = torch.empty(batch, num_kv_heads, dtype=torch.int32, device=device)
+        self.steps = 0
+        self.evictions = 0
+
+    def kv(self, pool: Optional[int] = None):
+        i = self.live if pool is None else pool
+        return paged_kv(self.k[i], self.v[i], None)
+
+    def evict_from(self, src_kv, src_block_table, lens, q_window, max_len: int, stream=None):
+        """Compacts (cache, lengths, the window's queries) into the pool that is not live and
+        makes it live: the prefill eviction (the prompt's cache) and every periodic one."""
+        dst = 1 - self.live
+        ws = torch.empty(max(se_snapkv_workspace_size(self.B, self.H, self.W, max_len), 16), dtype=torch.uint8,
+                         device=self.lens.device)
+        se_snapkv_score_and_compact_windowed(src_kv, q_window, src_block_table, lens, max_len, self.pool, self.keep,
+                                             self.sink, self.recent, self.sm_scale, self.kv(dst), self.block_table,
+                                             self.kept, self.counts, ws, stream)
+        self.lens = self.counts[:, 0].contiguous()  # every KV head of a request keeps as many positions
+        self.live = dst
+        self.steps = 0
+        self.evictions += 1
+
+    def append(self, k_new, v_new, q, stream=None):
+        """One decode step: K/V rows of the new token (k_new, v_new [B][Hkv][D]) and its query
+        q [B][Hq][D]; evicts when the period is complete."""
+        se_quest_update_summaries(self.kv(), k_new, v_new, self.block_table, self.lens, stream)
+        first = self.period - self.W
+        if self.steps >= first:
+            self.q_window[:, self.steps - first].copy_(q)
+        self.lens = self.lens + 1
+        self.steps += 1
+        if self.steps == self.period:
+            self.evict_from(self.kv(), self.block_table, self.lens, self.q_window, self.max_len, stream)

@@ -236,3 +236,68 @@ def test_snapkv_aime_budget_full_32k_sampled(cuda_device):
 def test_snapkv_agent_budget_full_32k_sampled(cuda_device):
     # sink 64, recent 512, 15,808 selected: half of each 32K prompt kept
     _full_sampled(SNAPKV_AGENT_32K, cuda_device, ((1, 2), (2, 5)))
+
+
+# ---------------------------------------------------------------- periodic eviction during decode
+def test_periodic_decode_eviction_over_compacted_pages(cuda_device):
+    """Prefill eviction (3,000-token prompts, window 16, sink 16, recent 64, 400 selected), then
+    one period of 64 decode steps appended to the compacted pages, then the periodic eviction
+    over them; the second eviction is checked against the oracle on the logical sequence
+    (prefill-kept rows, then the appended rows) with the last 16 decode queries as window."""
+    from sparse_decode_attention_quest_gb300.pipeline import SnapKVDecodeCache
+    dev = cuda_device
+    wl = SNAPKV_AIME_32K.scaled(batch=2, prompt_min=3000, prompt_max=3000, keep_topk=400, seed=14)
+    x = make_snapkv_inputs(wl)
+    B, H, Hq, D, W = wl.batch, wl.num_kv_heads, wl.num_q_heads, wl.head_dim, wl.window
+    S, R, K, pool, period = wl.keep_sink, wl.recent, wl.keep_topk, wl.pool_kernel, 64
+    scale = 1.0 / math.sqrt(D)
+    cache = SnapKVDecodeCache(B, H, Hq, D, W, pool, K, S, R, period, dev)
+    lens = torch.tensor(x.prompt_lens, dtype=torch.int32, device=dev)
+    cache.evict_from(se.paged_kv(x.k_cache.to(dev), x.v_cache.to(dev), None), x.src_block_table.to(dev), lens,
+                     x.q_window.to(dev), max(x.prompt_lens))
+    torch.cuda.synchronize()
+    G = wl.group
+    n0 = x.prompt_lens[0]
+    kept0 = {}
+    for b in range(B):
+        for h in range(H):
+            ref = osk.snapkv_head(x.q_window[b, :, h * G:(h + 1) * G, :], x.k_cache, x.src_block_table[b], h, n0, W,
+                                  pool, K, scale, sink=S, recent=R)
+            got = cache.kept[b, h, :int(cache.counts[b, h])].tolist()
+            assert got == ref["kept"], (b, h)  # no ties at the threshold for this seed
+            kept0[(b, h)] = ref["kept"]
+    g = torch.Generator().manual_seed(15)
+    k_app = torch.randn(period, B, H, D, generator=g).to(torch.bfloat16)
+    v_app = torch.randn(period, B, H, D, generator=g).to(torch.bfloat16)
+    q_dec = torch.randn(period, B, Hq, D, generator=g).to(torch.bfloat16)
+    for t in range(period):
+        cache.append(k_app[t].to(dev), v_app[t].to(dev), q_dec[t].to(dev))
+    torch.cuda.synchronize()
+    assert cache.evictions == 2 and cache.steps == 0
+    kk, kv_ = cache.k[cache.live].cpu(), cache.v[cache.live].cpu()
+    for b in range(B):
+        for h in range(H):
+            rows_k = [x.k_cache[int(x.src_block_table[b, j // 16]), h, j % 16] for j in kept0[(b, h)]]
+            rows_k += [k_app[t, b, h] for t in range(period)]
+            rows_v = [x.v_cache[int(x.src_block_table[b, j // 16]), h, j % 16] for j in kept0[(b, h)]]
+            rows_v += [v_app[t, b, h] for t in range(period)]
+            n1 = len(rows_k)
+            npg = -(-n1 // 16)
+            logical = torch.zeros(npg, H, 16, D, dtype=torch.bfloat16)
+            padded = torch.zeros(npg * 16, D, dtype=torch.bfloat16)
+            padded[:n1] = torch.stack(rows_k)
+            logical[:, h] = padded.view(npg, 16, D)
+            qw = q_dec[period - W:, b, h * G:(h + 1) * G, :]          # [W][G][D], oldest first
+            ref = osk.snapkv_head(qw, logical, torch.arange(npg), h, n1, W, pool, K, scale, sink=S, recent=R)
+            cnt = int(cache.counts[b, h])
+            got = cache.kept[b, h, :cnt].tolist()
+            assert cnt == len(ref["kept"])
+            gs, rs = set(got), set(ref["kept"])
+            for j in range(n1 - W):
+                if (j in gs) != (j in rs):
+                    assert exempt(ref["pooled"][j], ref["threshold"]), (b, h, j)
+            # the compacted rows are the logical rows at the kept positions, bit for bit
+            for t, j in enumerate(got):
+                page = int(cache.block_table[b, t // 16])
+                assert torch.equal(kk[page, h, t % 16].view(torch.int16), rows_k[j].view(torch.int16))
+                assert torch.equal(kv_[page, h, t % 16].view(torch.int16), rows_v[j].view(torch.int16))
