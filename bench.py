@@ -356,6 +356,13 @@ def run_ours(args, rank, world, local_rank):
             "snapkv_aime_b4_32k": _snapkv_extra(args, dev, flush, stream, _snapkv_wl("SNAPKV_AIME_32K")),
             "snapkv_agent_b4_32k": _snapkv_extra(args, dev, flush, stream, _snapkv_wl("SNAPKV_AGENT_32K")),
             "snapkv_periodic_evict_aime_b4": _periodic_evict_extra(args, dev, flush, stream),
+            "tiny_quest_b1_g4_4k": _quest_extra(args, dev, flush, stream, _snapkv_wl("TINY_QUEST_4K")),
+            "qwen3_4b_quest_b8_32k": _quest_extra(args, dev, flush, stream, _snapkv_wl("QWEN3_4B_QUEST_32K")),
+            "tiny_quest_b1_g4_4k_fused": _quest_extra(args, dev, flush, stream, _snapkv_wl("TINY_QUEST_4K"),
+                                                      fused=True),
+            "qwen3_4b_quest_b8_32k_fused": _quest_extra(args, dev, flush, stream, _snapkv_wl("QWEN3_4B_QUEST_32K"),
+                                                        fused=True),
+            "qwen3_30b_a3b_quest_b32_128k_fused": _quest_extra(args, dev, flush, stream, wl, fused=True),
             "mla_glm_quest_b64_32k": _mla_extra(args, dev, flush, stream),
             "qwen3_30b_a3b_quest_sink64_recent512_b32_128k": _windows_extra(args, dev, flush, stream)}
     if rank == 0 and not args.no_cpu_baseline:
@@ -441,10 +448,11 @@ def _snapkv_extra(args, dev, flush, stream, wl=None):
             "tensor_frac_of_measured_bf16": round(flops / (ms * 1e-3) / 1e12 / peak_tf, 4)}
 
 
-def _quest_extra(args, dev, flush, stream, wl, sink=0, recent=0):
+def _quest_extra(args, dev, flush, stream, wl, sink=0, recent=0, fused=False):
     """One Quest decode step of workload ``wl`` (append if the workload appends, score, top-k
     with the keep windows ``sink``/``recent``, decode), captured in a CUDA graph and replayed
-    (L2 flushed between replays); per-kernel spans from an eager pass."""
+    (L2 flushed between replays); per-kernel spans from an eager pass. ``fused``: the step as
+    one se_quest_fused_step launch (its span is the whole step)."""
     import torch
     import sparse_decode_attention_quest_gb300 as se
     from sparse_decode_attention_quest_gb300.pipeline import QuestDecodeStep, new_summary
@@ -456,7 +464,18 @@ def _quest_extra(args, dev, flush, stream, wl, sink=0, recent=0):
     before = torch.tensor(x.seq_lens, dtype=torch.int32, device=dev)
     after = torch.tensor(x.seq_lens_after, dtype=torch.int32, device=dev)
     step.build_summaries(before)
-    if wl.append:
+    if fused:
+        def run(ev=None):
+            if ev is not None:
+                for e in ev[:3]:
+                    e.record(stream)
+            if wl.append:
+                step.run_fused(x.q, after, x.k_new, x.v_new, stream=stream)
+            else:
+                step.run_fused(x.q, after, stream=stream)
+            if ev is not None:
+                ev[3].record(stream)
+    elif wl.append:
         run = lambda ev=None: step.run(x.q, after, x.k_new, x.v_new, before, stream=stream, events=ev)
     else:
         run = lambda ev=None: step.run(x.q, after, stream=stream, events=ev)
@@ -493,15 +512,19 @@ def _quest_extra(args, dev, flush, stream, wl, sink=0, recent=0):
     ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
     abytes = algorithmic_bytes(wl, x.seq_lens_after, step.counts.cpu().flatten().tolist())
     peak, _ = _peaks()
+    step_bytes = sum(abytes.values())
+    if fused:
+        spans = {"fused_step": spans["decode"]}
+        abytes = {"fused_step": step_bytes}
     kern = {k: {"ms": round(v, 5), "algorithmic_bytes": abytes[k],
                 "gbs": round(abytes[k] / (v * 1e-3) / 1e9, 1) if v > 0 else 0.0,
                 "frac_of_measured_hbm": round(abytes[k] / (v * 1e-3) / 1e9 / peak, 4) if v > 0 else 0.0}
             for k, v in spans.items() if abytes[k] > 0}
-    step_bytes = sum(abytes.values())
     # QK^T over head_dim and PV over head_dim_v for every selected token and query head
     G = wl.num_q_heads // wl.num_kv_heads
     flops = 2 * int(step.counts.sum().item()) * PAGE * G * (wl.head_dim + wl.head_dim_v)
-    kern["decode"]["tflops"] = round(flops / (spans["decode"] * 1e-3) / 1e12, 1)
+    dk = "fused_step" if fused else "decode"
+    kern[dk]["tflops"] = round(flops / (spans[dk] * 1e-3) / 1e12, 1)
     return {"ms_per_step": ms, "steps": n, "tokens_per_s": wl.batch / (ms * 1e-3),
             "step_gbs": round(step_bytes / (ms * 1e-3) / 1e9, 1),
             "step_frac_of_measured_hbm": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4), "kernels": kern,
@@ -509,7 +532,8 @@ def _quest_extra(args, dev, flush, stream, wl, sink=0, recent=0):
             "shape": {"workload": wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
                       "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "head_dim_v": wl.head_dim_v,
                       "context": [wl.context_min, wl.context_max], "topk_pages": wl.topk_pages,
-                      "sink_tokens": sink, "recent_tokens": recent, "append": wl.append}}
+                      "sink_tokens": sink, "recent_tokens": recent, "append": wl.append},
+            "launches_per_step": 1 if fused else step.launches_per_step(wl.append)}
 
 
 def _mla_extra(args, dev, flush, stream):
@@ -544,6 +568,7 @@ def _periodic_evict_extra(args, dev, flush, stream):
 
 
 def _snapkv_wl(name):
+    """A workload of the synth package by name."""
     import synth
     return getattr(synth, name)
 

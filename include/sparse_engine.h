@@ -219,6 +219,31 @@ SE_API se_status_t se_quest_select_pages_windowed(const se_paged_kv_t* kv, const
                                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * se_quest_fused_step -- one Quest decode step in a single launch: the optional
+ * KV append with its summary update, the page scores, the windowed top-k and
+ * the sparse decode, with the scores kept in on-chip memory (a cluster of CTAs
+ * per (request, KV head) shares them over distributed shared memory).
+ * SparseEngine, Figure 2 and Figure 3 captions; Tables 9-12 (keep windows);
+ * Table 7 (the history includes the current token). The results equal
+ * se_quest_update_summaries + se_quest_score_pages +
+ * se_quest_topk_pages_windowed + se_sparse_paged_decode:
+ *   seq_lens: lengths INCLUDING the new token; with k_new/v_new (bf16
+ *     [batch][num_kv_heads][128], both or neither) the token at position
+ *     seq_lens[b] - 1 is appended first (no append when both are NULL);
+ *   sel_pages / sel_counts: the kept pages as se_quest_topk_pages_windowed writes them;
+ *   out: bf16 [batch][num_q_heads][128]; out_lse: fp32 [batch][num_q_heads] or NULL.
+ * Shapes: head_dim = head_dim_v = 128, separate K and V caches, up to 16 query
+ * heads per KV head, up to 8192 candidate pages per request and 2048 kept pages
+ * (se_quest_kept_pages_max); sel_stride >= se_quest_kept_pages_max(...). No workspace.
+ */
+SE_API se_status_t se_quest_fused_step(const se_paged_kv_t* kv, const void* k_new, const void* v_new, const void* q,
+                                       int32_t num_q_heads, const int32_t* block_table, int32_t bt_stride,
+                                       const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                                       int32_t topk_pages, int32_t sink_tokens, int32_t recent_tokens, float sm_scale,
+                                       void* out, float* out_lse, int32_t* sel_pages, int32_t* sel_counts,
+                                       int32_t sel_stride, void* stream);
+
+/*
  * se_sparse_paged_decode -- attention of one decode query per request over the
  * selected pages only.
  * SparseEngine, Figure 2 caption (attention execution over the method's view of

@@ -22,6 +22,7 @@ __all__ = [
     "se_quest_build_summaries", "se_quest_update_summaries", "se_quest_score_pages",
     "se_quest_topk_pages", "se_quest_topk_pages_windowed", "se_quest_kept_pages_max",
     "se_quest_select_workspace_size", "se_quest_select_pages", "se_quest_select_pages_windowed",
+    "se_quest_fused_step",
     "se_sparse_decode_workspace_size", "se_sparse_decode_plan", "se_sparse_paged_decode",
     "se_sparse_paged_decode_noalloc", "se_snapkv_workspace_size", "se_snapkv_window_scores", "se_snapkv_select",
     "se_snapkv_compact", "se_snapkv_score_and_compact", "se_snapkv_select_windowed",
@@ -69,6 +70,8 @@ _SIGNATURES = {
     "se_quest_select_pages": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _I, _P, _P, _I, _P, _Z, _P]),
     "se_quest_select_pages_windowed": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P,
                                                       _Z, _P]),
+    "se_quest_fused_step": (ctypes.c_int, [_KV, _P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P,
+                                           _I, _P]),
     "se_sparse_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "se_sparse_decode_plan": (ctypes.c_int, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
                                              ctypes.POINTER(_I)]),
@@ -239,6 +242,20 @@ def se_quest_select_pages_windowed(kv: SEPagedKV, q, block_table, seq_lens, max_
                                               _ptr(out_counts, torch.int32, "out_counts"), out_pages.shape[-1],
                                               _ptr(workspace, torch.uint8, "workspace"),
                                               0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
+def se_quest_fused_step(kv: SEPagedKV, k_new, v_new, q, block_table, seq_lens, max_seq_len: int, topk_pages: int,
+                        sink_tokens: int, recent_tokens: int, sm_scale: float, out, out_lse, sel_pages, sel_counts,
+                        stream=None):
+    lib = load_library()
+    _check(lib.se_quest_fused_step(ctypes.byref(kv), _ptr(k_new, torch.bfloat16, "k_new"),
+                                   _ptr(v_new, torch.bfloat16, "v_new"), _ptr(q, torch.bfloat16, "q"), q.shape[1],
+                                   _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                   _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0], int(max_seq_len),
+                                   int(topk_pages), int(sink_tokens), int(recent_tokens), float(sm_scale),
+                                   _ptr(out, torch.bfloat16, "out"), _ptr(out_lse, torch.float32, "out_lse"),
+                                   _ptr(sel_pages, torch.int32, "sel_pages"), _ptr(sel_counts, torch.int32, "sel_counts"),
+                                   sel_pages.shape[-1], _stream(stream)))
 
 
 def se_sparse_decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim_v: int,

@@ -318,6 +318,48 @@ se_status_t se_quest_select_pages(const se_paged_kv_t* kv, const void* q, int32_
                                         workspace_bytes, stream);
 }
 
+se_status_t se_quest_fused_step(const se_paged_kv_t* kv, const void* k_new, const void* v_new, const void* q,
+                                int32_t num_q_heads, const int32_t* block_table, int32_t bt_stride,
+                                const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t topk_pages,
+                                int32_t sink_tokens, int32_t recent_tokens, float sm_scale, void* out,
+                                float* out_lse, int32_t* sel_pages, int32_t* sel_counts, int32_t sel_stride,
+                                void* stream) {
+  static const char* fn = "se_quest_fused_step";
+  se_status_t st = check_kv(fn, kv, true);
+  if (st != SE_OK) return st;
+  if (batch < 0 || max_seq_len < 0 || bt_stride < 1) return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
+  if (num_q_heads < 1 || num_q_heads % kv->num_kv_heads)
+    return fail(SE_ERR_INVALID_ARG, fn, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (kv->head_dim != 128 || kv->head_dim_v != 128 || kv->v == kv->k || num_q_heads / kv->num_kv_heads > 16)
+    return fail(SE_ERR_UNSUPPORTED, fn, "head_dim = head_dim_v = 128, separate K and V, <= 16 query heads per KV head");
+  if (topk_pages < 1 || sink_tokens < 0 || recent_tokens < 0)
+    return fail(SE_ERR_INVALID_ARG, fn, "topk_pages < 1 or negative window");
+  const long long kept_max = se_quest_kept_pages_max(topk_pages, sink_tokens, recent_tokens);
+  if ((long long)sel_stride < kept_max) return fail(SE_ERR_INVALID_ARG, fn, "sel_stride < se_quest_kept_pages_max");
+  if (kept_max > se::fused_max_kept()) return fail(SE_ERR_UNSUPPORTED, fn, "more than 2048 kept pages");
+  if (pages_of(max_seq_len) - 1 > se::fused_max_candidates())
+    return fail(SE_ERR_UNSUPPORTED, fn, "more than 8192 candidate pages per request");
+  if (bt_stride < pages_of(max_seq_len)) return fail(SE_ERR_INVALID_ARG, fn, "bt_stride < pages of max_seq_len");
+  if ((k_new == nullptr) != (v_new == nullptr)) return fail(SE_ERR_INVALID_ARG, fn, "k_new and v_new: both or neither");
+  if (batch > 0 && (!q || !block_table || !seq_lens || !out || !sel_pages || !sel_counts))
+    return fail(SE_ERR_INVALID_ARG, fn, "NULL pointer");
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(sel_pages) ||
+      !aligned16(out_lse))
+    return fail(SE_ERR_INVALID_ARG, fn, "pointers must be 16-byte aligned");
+  if (!std::isfinite(sm_scale)) return fail(SE_ERR_INVALID_ARG, fn, "sm_scale not finite");
+  if (batch == 0) return SE_OK;
+  DeviceInfo* d = nullptr;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  e = se::launch_quest_fused(view_of(kv), static_cast<uint16_t*>(kv->k), static_cast<uint16_t*>(kv->v),
+                             static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new),
+                             static_cast<const uint16_t*>(q), num_q_heads, block_table, bt_stride, seq_lens, batch,
+                             max_seq_len, topk_pages, sink_tokens, recent_tokens, sm_scale,
+                             static_cast<uint16_t*>(out), out_lse, sel_pages, sel_counts, sel_stride, d->sm_count,
+                             d->err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
 se_status_t se_sparse_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t head_dim_v, int32_t sel_stride, int32_t* nsplit,
                                   int32_t* pages_per_split, int32_t* launches) {

@@ -100,6 +100,17 @@ cudaError_t launch_mla_decode(const KvView& kv, const uint16_t* q, int32_t num_q
                               float* out_lse, void* workspace, const DecodePlan& plan, unsigned* err,
                               cudaStream_t stream);
 
+// ---- quest_fused.cu: append + score + top-k + decode in one launch (a cluster per item)
+int fused_max_candidates();
+int fused_max_kept();
+int fused_cluster_size(int items, int sm_count);
+cudaError_t launch_quest_fused(const KvView& kv, uint16_t* k_mut, uint16_t* v_mut, const uint16_t* k_new,
+                               const uint16_t* v_new, const uint16_t* q, int32_t num_q_heads,
+                               const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens, int32_t batch,
+                               int32_t max_seq_len, int32_t topk, int32_t sink_tokens, int32_t recent_tokens,
+                               float sm_scale, uint16_t* out, float* out_lse, int32_t* sel, int32_t* sel_counts,
+                               int32_t sel_stride, int sm_count, unsigned* err, cudaStream_t stream);
+
 // ---- snapkv.cu
 int snapkv_max_slices(int max_len);
 size_t snapkv_part_bytes(int pairs, int max_len);

@@ -6,6 +6,7 @@ library's kernels:
     se_quest_score_pages        (upper-bound score of every candidate page)
     se_quest_topk_pages_windowed (top-k pages + the sink/recent windows + the last page, ascending)
     se_sparse_paged_decode      (split-K flash-decode over the selected pages + merge)
+or all four in one launch (se_quest_fused_step, run_fused).
 """
 from __future__ import annotations
 
@@ -14,7 +15,7 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (paged_kv, se_quest_build_summaries, se_quest_kept_pages_max, se_quest_score_pages,
+from . import (paged_kv, se_quest_build_summaries, se_quest_fused_step, se_quest_kept_pages_max, se_quest_score_pages,
                se_quest_topk_pages_windowed, se_quest_update_summaries, se_snapkv_score_and_compact_windowed,
                se_snapkv_workspace_size, se_sparse_decode_plan, se_sparse_decode_workspace_size,
                se_sparse_paged_decode)
@@ -77,6 +78,13 @@ class QuestDecodeStep:
         se_sparse_paged_decode(self.kv, q, self.block_table, seq_lens, self.sel if sel is None else sel,
                                self.counts if counts is None else counts, self.sm_scale, self.out, self.lse,
                                self.workspace, stream)
+
+    def run_fused(self, q, seq_lens, k_new=None, v_new=None, stream=None):
+        """The whole step in one launch (se_quest_fused_step): ``seq_lens`` are the lengths
+        after the append; with k_new/v_new the token at seq_lens - 1 is appended first."""
+        se_quest_fused_step(self.kv, k_new, v_new, q, self.block_table, seq_lens, self.max_seq_len, self.topk,
+                            self.sink, self.recent, self.sm_scale, self.out, self.lse, self.sel, self.counts, stream)
+        return self.out
 
     def run(self, q, seq_lens, k_new=None, v_new=None, seq_lens_before=None, stream=None,
             events: Optional[Sequence] = None):

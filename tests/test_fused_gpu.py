@@ -1,0 +1,109 @@
+"""The one-launch Quest step (se_quest_fused_step) on the GPU against the fp64 oracle.
+
+Same comparison rules as the four-call path (selection exact outside the 1e-3
+band around the k-th score, output within 2e-2, lse within 1e-3): the tiny
+workload, ragged appends with and without keep windows, every group-size
+class, edge lengths, the appended token bit-exact against the append entry
+point, and the full 32K and 128K workloads on sampled requests.
+"""
+import math
+
+import pytest
+import torch
+
+import sparse_decode_attention_quest_gb300 as se
+from sparse_decode_attention_quest_gb300.pipeline import QuestDecodeStep, new_summary
+from synth import QWEN3_30B_A3B_QUEST_128K, QWEN3_4B_QUEST_32K, TINY_QUEST_4K, make_quest_decode_inputs
+from tests.parity import compare_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors(se_lib, cuda_device):
+    se.se_read_device_error(clear=True)
+    yield
+    assert se.se_read_device_error(clear=True) == 0
+
+
+def _prepare(wl, dev, device_gen=False, sink=0, recent=0):
+    x = make_quest_decode_inputs(wl, device=dev if device_gen else "cpu", poison_tail=True)
+    k = x.k_cache.to(dev)
+    v = x.v_cache.to(dev)
+    step = QuestDecodeStep(k, v, new_summary(k), x.block_table.to(dev), wl.num_q_heads, wl.topk_pages,
+                           max(max(x.seq_lens_after), 1), sink_tokens=sink, recent_tokens=recent)
+    before = torch.tensor(x.seq_lens, dtype=torch.int32, device=dev)
+    after = torch.tensor(x.seq_lens_after, dtype=torch.int32, device=dev)
+    step.build_summaries(before)
+    return x, step, after
+
+
+def _run_fused(x, step, after, dev):
+    if x.workload.append:
+        step.run_fused(x.q.to(dev), after, x.k_new.to(dev), x.v_new.to(dev))
+    else:
+        step.run_fused(x.q.to(dev), after)
+    torch.cuda.synchronize()
+
+
+def _scale(wl):
+    return 1.0 / math.sqrt(wl.head_dim)
+
+
+def test_fused_tiny_workload(cuda_device):
+    wl = TINY_QUEST_4K
+    x, step, a = _prepare(wl, cuda_device)
+    _run_fused(x, step, a, cuda_device)
+    compare_decode(x, step, [0], _scale(wl), "fused tiny")
+
+
+@pytest.mark.parametrize("sink,recent", [(0, 0), (64, 512), (16, 64)])
+def test_fused_ragged_append(cuda_device, sink, recent):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=5, context_min=900, context_max=4100, topk_pages=24, seed=81)
+    x, step, a = _prepare(wl, cuda_device, sink=sink, recent=recent)
+    _run_fused(x, step, a, cuda_device)
+    compare_decode(x, step, range(wl.batch), _scale(wl), f"fused ragged {sink}/{recent}", sink, recent)
+
+
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (16, 2), (32, 2), (12, 4)])
+def test_fused_group_sizes(cuda_device, hq, hkv):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=3, num_q_heads=hq, num_kv_heads=hkv, context_min=500,
+                                         context_max=2500, topk_pages=16, seed=83 + hq)
+    x, step, a = _prepare(wl, cuda_device)
+    _run_fused(x, step, a, cuda_device)
+    compare_decode(x, step, range(wl.batch), _scale(wl), f"fused g={hq // hkv}")
+
+
+def test_fused_edge_lengths(cuda_device):
+    lens = (0, 1, 15, 16, 17, 31, 33, 160, 161, 700)
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=len(lens), lengths=lens, topk_pages=6, seed=87)
+    x, step, a = _prepare(wl, cuda_device)
+    _run_fused(x, step, a, cuda_device)
+    compare_decode(x, step, range(wl.batch), _scale(wl), "fused edges")
+
+
+def test_fused_append_equals_the_append_entry_point(cuda_device):
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=6, lengths=(15, 16, 17, 31, 32, 400), topk_pages=4, seed=89)
+    x, s1, a = _prepare(wl, cuda_device)
+    x2, s2, a2 = _prepare(wl, cuda_device)
+    _run_fused(x, s1, a, cuda_device)
+    before = torch.tensor(x2.seq_lens, dtype=torch.int32, device=cuda_device)
+    s2.append(x2.k_new.to(cuda_device), x2.v_new.to(cuda_device), before)
+    torch.cuda.synchronize()
+    assert torch.equal(s1.k_cache.view(torch.int16), s2.k_cache.view(torch.int16))
+    assert torch.equal(s1.v_cache.view(torch.int16), s2.v_cache.view(torch.int16))
+    assert torch.equal(s1.summary.view(torch.int16), s2.summary.view(torch.int16))
+
+
+def test_fused_full_qwen3_4b_32k_sampled(cuda_device):
+    wl = QWEN3_4B_QUEST_32K
+    x, step, a = _prepare(wl, cuda_device, device_gen=True)
+    _run_fused(x, step, a, cuda_device)
+    compare_decode(x, step, [0, wl.batch - 1], _scale(wl), "fused qwen3-4b full")
+
+
+def test_fused_full_qwen3_30b_a3b_128k_sampled(cuda_device):
+    wl = QWEN3_30B_A3B_QUEST_128K
+    x, step, a = _prepare(wl, cuda_device, device_gen=True)
+    _run_fused(x, step, a, cuda_device)
+    compare_decode(x, step, [0, 13, wl.batch - 1], _scale(wl), "fused qwen3-30b full")
