@@ -72,14 +72,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
   return fn;
 }
 
-// 2-D view of a paged cache as rows of `row_stride` bf16 (one row per token slot),
-// boxes of 64 columns x 16 rows with 128-byte swizzle.
-bool encode_page_map(CUtensorMap* map, const void* base, long long rows, int width, int row_stride) {
+// 2-D view of a paged cache (or any row-major bf16 matrix) as rows of
+// `row_stride` bf16, boxes of 64 columns x `box_rows` rows with 128-byte swizzle.
+bool encode_page_map(CUtensorMap* map, const void* base, long long rows, int width, int row_stride,
+                     int box_rows = se::kPageSize) {
   auto fn = encode_tiled();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)row_stride * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -428,7 +429,13 @@ se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32
     if ((size_t)batch > se::mla_decode_max_items())
       return fail(SE_ERR_UNSUPPORTED, fn, "too many requests for one launch");
     if (batch == 0) return SE_OK;
-    e = se::launch_mla_decode(view_of(kv), static_cast<const uint16_t*>(q), num_q_heads, block_table, bt_stride,
+    // Tile copies: 64 dims x 16 rows (one page) of the cache, 64 dims x all heads of the queries.
+    CUtensorMap kvmap, qmap;
+    if (!encode_page_map(&kvmap, kv->k, (long long)kv->num_pages * se::kPageSize, kv->head_dim, kv->row_stride_k) ||
+        !encode_page_map(&qmap, q, (long long)batch * num_q_heads, kv->head_dim, kv->head_dim, num_q_heads))
+      return fail(SE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
+    e = se::launch_mla_decode(kvmap, qmap, view_of(kv), static_cast<const uint16_t*>(q), num_q_heads, block_table,
+                              bt_stride,
                               seq_lens, batch, sel_pages, sel_counts, sel_stride, sm_scale,
                               static_cast<uint16_t*>(out), out_lse, workspace, plan, d->err,
                               static_cast<cudaStream_t>(stream));
@@ -640,9 +647,6 @@ cudaError_t device_context(int* sm_count, unsigned** err) {
   return cudaSuccess;
 }
 
-bool encode_kv_page_map(CUtensorMap* map, const void* base, long long rows, int width, int row_stride) {
-  return encode_page_map(map, base, rows, width, row_stride);
-}
 
 void set_error_detail(const char* fn, const char* what) { fail(SE_OK, fn, what); }
 

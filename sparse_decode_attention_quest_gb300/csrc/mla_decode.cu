@@ -3,23 +3,33 @@
 // decoding at 32K/128K; Table 7: logit z and weight alpha over the history).
 //
 // One cache row per token holds 576 dims (512 latent + 64 RoPE) and serves as
-// the key; its first 512 dims are the value. All 16 x HG query heads share the
+// the key; its first 512 dims are the value. All query heads (16..64) share the
 // one KV head, so every selected page (16 rows x 1152 bytes) is read once and
-// used by all heads.
+// used by all heads: with 64 heads both products are dense contractions, and
+// they run on the 5th-generation tensor cores with the scores and the output
+// accumulated in tensor memory (TMEM).
 //
 //  * Work split as in the GQA decode: the selected pages of all requests form
 //    one flattened range and every CTA takes an equal slice (>= 16 pages).
-//  * 2 x HG warps: warp (hg, dh) owns query heads 16 hg .. 16 hg + 15 and output
-//    dims 256 dh .. 256 dh + 255, so its output accumulator is 128 registers. Its
-//    query fragments cover dims 288 dh .. 288 dh + 287 (72 registers); the two
-//    warps of a head group add their partial logits through shared memory, so
-//    both see the full 576-dim logits and run the same online softmax.
-//  * A CTA-wide 8-stage ring of pages, filled with 16-byte cp.async copies into
-//    a layout of nine 64-dim chunks per page, 128-byte swizzled; rows at or past
-//    the request's length are zero-filled, never read. Page metadata (physical
-//    page, valid rows) sits in lanes, two windows of 32 pages per warp, loaded
-//    25 pages before the copies need it.
-//  * S = Q K^T and O += P V use the m16n8k16 bf16 MMA with fp32 accumulation.
+//  * A tile is 64 tokens (4 pages) in nine 64-dim chunks of 64 rows x 128 bytes,
+//    128-byte swizzled; two tiles are in flight. One thread copies each page of
+//    a tile with nine TMA boxes (64 dims x 16 rows); pages not selected are not
+//    copied, and the value dims of rows at or past the request's length are
+//    zeroed in shared memory by the softmax warps before the PV MMAs read them.
+//  * One thread issues all MMAs, S^T of the next tile as soon as it has landed
+//    and PV of the oldest tile as soon as its P is written.
+//  * S^T = K Q^T: one M = 64 tcgen05.mma per 16 dims (36 per tile) with the tile
+//    as the K-major A operand and the request's queries (64 rows x 576 dims in
+//    shared memory) as B; S^T lands in TMEM, token r in lane 32 (r / 16) + r % 16.
+//  * Eight softmax warps, two per page of the tile, read S^T (each thread one
+//    token x 16 heads), take per-head tile maxima, keep a running maximum per
+//    head that moves only when a tile exceeds it by 2^8 (then the output
+//    accumulator columns of the heads that moved are rescaled in TMEM), and
+//    write P as bf16 over the tile's RoPE chunk, which S^T no longer needs.
+//  * O^T += V^T P^T: four M = 128 MMAs per 16 tokens (dims 128 mt ..), A = the
+//    tile's first 512 dims read MN-major, B = P read MN-major; O^T of all 64
+//    heads is 4 x 64 TMEM columns. The epilogue divides by the softmax sums
+//    and writes the output (one slice) or a partial for the combine kernel.
 #include "se_ptx.cuh"
 
 namespace se {
@@ -27,14 +37,41 @@ namespace {
 
 constexpr int kD = 576;
 constexpr int kDv = 512;
-constexpr int kChunks = kD / 64;                      // 9 chunks of 64 dims
-constexpr int kChunkBytes = kPageSize * 128;          // 16 rows x 128 bytes
-constexpr int kPageBytes = kChunks * kChunkBytes;     // 18 KB
-constexpr int kStages = 8;
-constexpr int kRingBytes = kStages * kPageBytes;
+constexpr int kChunks = kD / 64;                        // 9 chunks of 64 dims
 constexpr int kMinPagesPerCta = 16;
-constexpr int kKStepsPerHalf = kD / 2 / 16;           // 18
 constexpr float kLn2 = 0.6931471805599453f;
+
+constexpr int kTileTok = 64;                            // 4 pages per tile
+constexpr int kTilePages = kTileTok / kPageSize;
+constexpr int kChunkBytes = kTileTok * 128;             // 64 rows x 64 dims
+constexpr int kStageBytes = kChunks * kChunkBytes;      // 72 KB
+constexpr int kStages = 2;
+constexpr int kQRows = 64;
+constexpr int kQBytes = kChunks * kQRows * 128;         // 64 heads x 576 dims
+constexpr int kPOff = 8 * kChunkBytes;                  // P of a tile: over its RoPE chunk
+constexpr int kQOff = kStages * kStageBytes;
+constexpr int kMiscOff = kQOff + kQBytes;
+constexpr int kThreads = 320;
+constexpr int kSoftThreads = 256;                       // warps 0-7: softmax + epilogue
+constexpr int kMmaWarp = 8;                             // lane 0 issues every MMA
+constexpr int kLoadWarp = 9;                            // lane 0 issues the TMA copies
+constexpr int kTmemCols = 512;
+constexpr int kSCol = 0;                                // S^T buffers: columns 0, 64
+constexpr int kOCol = 128;                              // O^T M-tile mt: columns 128 + 64 mt
+constexpr float kRescaleLog2 = 8.f;                     // running max moves when exceeded by 2^8
+constexpr uint32_t kSoftBar = 1;                        // named barrier of the softmax warps
+
+// Shared memory after the Q buffer.
+constexpr int kBarOff = 0;        // 31 mbarriers
+constexpr int kTmemSlotOff = 256;
+constexpr int kValidOff = 272;    // [2 stages][4 pages] valid rows
+constexpr int kXmaxOff = 512;     // [4 pages][64 heads] tile maxima
+constexpr int kFacOff = 1536;     // [64] rescale factors
+constexpr int kLsumOff = 1792;    // [4 pages][64] softmax sums
+constexpr int kMrowOff = 2816;    // [64] running maxima
+constexpr int kLinvOff = 3072;    // [64] 1 / sum
+constexpr int kLseOff = 3328;     // [64] log2-sum-exp2
+constexpr int kPrefixOff = 3584;  // [batch + 1]
 
 struct MlaArgs {
   const uint16_t* kv;
@@ -59,12 +96,9 @@ struct MlaArgs {
   unsigned* err;
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ int find_item(const int* prefix, int n, int x) {
   int lo = 0, hi = n;
@@ -75,23 +109,97 @@ __device__ __forceinline__ int find_item(const int* prefix, int n, int x) {
   return lo;
 }
 
-// Barrier of the two warps of head group hg (named barriers 1 .. HG).
-__device__ __forceinline__ void pair_barrier(int hg) {
-  asm volatile("bar.sync %0, 64;" ::"r"(1 + hg) : "memory");
+// Reduction of 16 values over the 16 lanes of a half-warp by halving exchanges
+// (xor 1, 2, 4, 8: 15 shuffles). Afterwards v[0] holds the result for the value
+// with index reduced_index(lane).
+template <bool kMax>
+__device__ __forceinline__ void half_warp_reduce16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const int b = 1 << st, w = 8 >> st;
+    const bool up = (lane & b) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = up ? v[i] : v[i + w];
+      const float keep = up ? v[i + w] : v[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, b);
+      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+}
+__device__ __forceinline__ int reduced_index(int lane) {
+  return 8 * (lane & 1) + 4 * ((lane >> 1) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 3) & 1);
 }
 
-template <int HG>
-__global__ void __launch_bounds__(64 * HG, 1) mla_decode_kernel(const MlaArgs a) {
+// Walks the tiles of a CTA's slice in order: request segments (the part of a
+// request's selected pages inside the slice), each cut into tiles of 4 pages.
+struct TileCursor {
+  const int* prefix;
+  int start, end, i_last;
+  int item, lo, hi, ntiles, t, seg, j;
+  bool valid;
+  __device__ void open(int it) {
+    for (item = it; item <= i_last; ++item) {
+      const int p0 = prefix[item];
+      lo = max(start, p0) - p0;
+      hi = min(end, prefix[item + 1]) - p0;
+      if (lo < hi) {
+        ntiles = (hi - lo + kTilePages - 1) / kTilePages;
+        t = 0;
+        valid = true;
+        return;
+      }
+    }
+    valid = false;
+  }
+  __device__ void init(const int* pf, int st, int en, int i_first, int il) {
+    prefix = pf;
+    start = st;
+    end = en;
+    i_last = il;
+    seg = 0;
+    j = 0;
+    open(i_first);
+  }
+  __device__ bool last() const { return t == ntiles - 1; }
+  __device__ void next() {
+    ++j;
+    if (++t == ntiles) {
+      ++seg;
+      open(item + 1);
+    }
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_constant__ CUtensorMap kvmap,
+                                                                 const __grid_constant__ CUtensorMap qmap,
+                                                                 const MlaArgs a) {
   pdl_enter();
-  constexpr int kThreads = 64 * HG;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* xbuf = reinterpret_cast<float*>(ring + kRingBytes);  // [2 parity][HG][2 dh][32 lanes][8]
-  int* prefix = reinterpret_cast<int*>(xbuf + 2 * HG * 2 * 32 * 8);
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* misc = smem + kMiscOff;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc + kBarOff);
+  uint64_t* full = bars;          // [2 stages][9 chunks] a chunk of a tile landed (TMA transaction count)
+  uint64_t* empty = bars + 18;    // [2] the PV MMAs of the stage's tile are done
+  uint64_t* s_full = bars + 20;   // [2] S^T of a tile is in TMEM
+  uint64_t* s_free = bars + 22;   // [2] S^T read by the softmax threads
+  uint64_t* p_full = bars + 24;   // [2] P written, V rows past the length zeroed, O^T rescaled
+  uint64_t* o_done = bars + 26;   // the PV MMAs of a tile are done
+  uint64_t* o_free = bars + 27;   // O^T read by the epilogue (softmax threads)
+  uint64_t* q_full = bars + 28;   // the request's queries landed
+  uint64_t* q_empty = bars + 29;  // the last S^T MMA of a request's segment is done
+  uint64_t* fin = bars + 30;      // every MMA of the CTA is done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + kTmemSlotOff);
+  int* tile_valid = reinterpret_cast<int*>(misc + kValidOff);
+  float* xmax = reinterpret_cast<float*>(misc + kXmaxOff);
+  float* fac_s = reinterpret_cast<float*>(misc + kFacOff);
+  float* lsum = reinterpret_cast<float*>(misc + kLsumOff);
+  float* mrow = reinterpret_cast<float*>(misc + kMrowOff);
+  float* linv = reinterpret_cast<float*>(misc + kLinvOff);
+  float* lse_s = reinterpret_cast<float*>(misc + kLseOff);
+  int* prefix = reinterpret_cast<int*>(misc + kPrefixOff);
   const int items = a.batch;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hg = warp >> 1, dh = warp & 1;
-  const int g = lane >> 2, t = lane & 3;
 
   for (int i = threadIdx.x; i < items; i += kThreads) {
     int c = a.sel_counts[i];
@@ -133,35 +241,48 @@ __global__ void __launch_bounds__(64 * HG, 1) mla_decode_kernel(const MlaArgs a)
   const int end = min(total, start + per_cta);
   if (start >= end) return;
 
-  const uint32_t ring_addr = smem_addr(ring);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages * kChunks; ++i) mbar_init(&full[i], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], kSoftThreads);
+      mbar_init(&p_full[s], kSoftThreads);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(o_free, kSoftThreads);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(fin, 1);
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t smem0 = smem_addr(smem);
   const int i_first = find_item(prefix, items, start);
   const int i_last = find_item(prefix, items, end - 1);
-  int page_ctr = 0;  // pages processed by this CTA (exchange buffer parity)
-  for (int item = i_first; item <= i_last; ++item) {
-    const int p0 = prefix[item];
-    const int lo = max(start, p0) - p0, hi = min(end, prefix[item + 1]) - p0;
-    if (lo >= hi) continue;
-    const int b = item;
-    int L = a.seq_lens[b];
-    if (L < 0) {
-      if (threadIdx.x == 0) raise_error(a.err, SE_DEVERR_LENGTH);
-      L = 0;
-    }
-    int n_b = (L + kPageSize - 1) / kPageSize;
-    if (n_b > a.bt_stride) {
-      if (threadIdx.x == 0) raise_error(a.err, SE_DEVERR_LENGTH);
-      n_b = a.bt_stride;
-      L = n_b * kPageSize;
-    }
-    const int np = hi - lo;
-    const int32_t* sel_row = a.sel + (size_t)item * a.sel_stride + lo;
-    const int32_t* bt_row = a.block_table + (size_t)b * a.bt_stride;
-    // Metadata of page k (physical page, valid rows; 0 rows: skip), one page per
-    // lane: every warp holds pages [base, base + 32) and [base + 32, base + 64).
+  const int Hq = a.Hq;
+  bool dead = false;  // a bounded wait gave up: leave the loops, no further waits
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer
+    // Lane 0 issues the copies, chunk by chunk (each chunk signals its own
+    // barrier, so that the S^T MMAs of a chunk start as soon as it is in); the
+    // lanes hold the page metadata.
+    const uint64_t policy = l2_evict_first_policy();
+    TileCursor c;
+    c.init(prefix, start, end, i_first, i_last);
+    int base = 0, ph_cur = 0, va_cur = 0, ph_nxt = 0, va_nxt = 0, n_b = 0, L = 0;
+    const int32_t* sel_row = nullptr;
+    const int32_t* bt_row = nullptr;
+    // Metadata of page k of the segment (physical page, valid rows; 0 rows: not copied).
     auto meta = [&](int k, int& phys, int& valid) {
       phys = 0;
       valid = 0;
-      if (k < np) {
+      if (k < c.hi - c.lo) {
         const int logical = sel_row[k];
         if (logical >= 0 && logical < n_b) {
           const int ph = bt_row[logical];
@@ -176,181 +297,338 @@ __global__ void __launch_bounds__(64 * HG, 1) mla_decode_kernel(const MlaArgs a)
         }
       }
     };
-    int base = 0, ph_cur, va_cur, ph_nxt, va_nxt;
-    meta(lane, ph_cur, va_cur);
-    meta(lane + 32, ph_nxt, va_nxt);
-    auto lookup = [&](int k, int& phys, int& valid) {
-      const int pc = __shfl_sync(0xffffffffu, ph_cur, k & 31), vc = __shfl_sync(0xffffffffu, va_cur, k & 31);
-      const int pn = __shfl_sync(0xffffffffu, ph_nxt, k & 31), vn = __shfl_sync(0xffffffffu, va_nxt, k & 31);
-      const bool in_cur = k < base + 32;
-      phys = in_cur ? pc : pn;
-      valid = in_cur ? vc : vn;
-    };
-    auto issue = [&](int k) {
-      int phys, valid;
-      lookup(k, phys, valid);
-      const uint32_t st = ring_addr + (k % kStages) * kPageBytes;
-      const uint16_t* src = a.kv + (size_t)phys * kPageSize * a.row_stride;
-      for (int c = threadIdx.x; c < kPageSize * kChunks * 8; c += kThreads) {  // 1152 16-byte pieces
-        const int r = c / (kChunks * 8), q = c % (kChunks * 8);
-        const bool in = r < valid;
-        cp_async16(st + (q >> 3) * kChunkBytes + swz128(r, q & 7),
-                   src + (size_t)(in ? r : 0) * a.row_stride + q * 8, in ? 16u : 0u);
-      }
-    };
-#pragma unroll 1
-    for (int k = 0; k < kStages - 1; ++k) {
-      if (k < np) issue(k);
-      cp_async_commit();
-    }
-    // Query fragments: heads 16 hg + {g, g + 8}, k-steps over dims 288 dh ..
-    uint32_t qa[kKStepsPerHalf][4];
-    {
-      const uint16_t* q0 = a.q + ((size_t)b * a.Hq + hg * 16 + g) * kD;
-      const uint16_t* q1 = q0 + 8 * kD;
-#pragma unroll
-      for (int ks = 0; ks < kKStepsPerHalf; ++ks) {
-        const int c = (dh * kKStepsPerHalf + ks) * 16 + 2 * t;
-        qa[ks][0] = *reinterpret_cast<const uint32_t*>(q0 + c);
-        qa[ks][2] = *reinterpret_cast<const uint32_t*>(q0 + c + 8);
-        qa[ks][1] = *reinterpret_cast<const uint32_t*>(q1 + c);
-        qa[ks][3] = *reinterpret_cast<const uint32_t*>(q1 + c + 8);
-      }
-    }
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[32][4];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    const int krow = (lane & 7) + ((lane >> 4) << 3), ksub = (lane >> 3) & 1;
-    const int vtok = (lane & 7) + (((lane >> 3) & 1) << 3), vsub = lane >> 4;
-
-    for (int k = 0; k < np; ++k, ++page_ctr) {
-      // Page k has left the first window: rotate. The window loaded here is
-      // first needed 25 pages later (the copies run kStages - 1 pages ahead).
-      if (k == base + 32) {
+    for (; c.valid; c.next()) {
+      const int s = c.j & 1;
+      if (c.t == 0) {
+        const int b = c.item;
+        L = a.seq_lens[b];
+        if (L < 0) {
+          if (lane == 0) raise_error(a.err, SE_DEVERR_LENGTH);
+          L = 0;
+        }
+        n_b = (L + kPageSize - 1) / kPageSize;
+        if (n_b > a.bt_stride) {
+          if (lane == 0) raise_error(a.err, SE_DEVERR_LENGTH);
+          n_b = a.bt_stride;
+          L = n_b * kPageSize;
+        }
+        sel_row = a.sel + (size_t)c.item * a.sel_stride + c.lo;
+        bt_row = a.block_table + (size_t)b * a.bt_stride;
+        base = 0;
+        meta(lane, ph_cur, va_cur);
+        meta(lane + 32, ph_nxt, va_nxt);
+      } else if (c.t * kTilePages == base + 32) {
+        // The tile has left the first window: rotate (the new one is used 8 tiles later).
         base += 32;
         ph_cur = ph_nxt;
         va_cur = va_nxt;
         meta(base + 32 + lane, ph_nxt, va_nxt);
       }
-      if (k + kStages - 1 < np) issue(k + kStages - 1);
-      cp_async_commit();
-      cp_async_wait<kStages - 1>();
-      __syncthreads();  // page k is in shared memory (every thread's copies)
-      int phys_k, valid;
-      lookup(k, phys_k, valid);
-      (void)phys_k;
-      if (valid > 0) {
-        const uint32_t st = ring_addr + (k % kStages) * kPageBytes;
-        // Partial S over this warp's 288 dims.
-        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      int phys[kTilePages], valid[kTilePages], live = 0;
 #pragma unroll
-        for (int ks = 0; ks < kKStepsPerHalf; ++ks) {
-          const int d0 = (dh * kKStepsPerHalf + ks) * 16;
-          uint32_t r0, r1, r2, r3;
-          ldmatrix_x4(r0, r1, r2, r3, st + (d0 >> 6) * kChunkBytes + swz128(krow, ((d0 & 63) >> 3) + ksub));
-          mma_bf16_16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], r0, r1);
-          mma_bf16_16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], r2, r3);
-        }
-        // Add the partner warp's partial (same head group, other half of the dims).
-        float* mine = xbuf + ((((page_ctr & 1) * HG + hg) * 2 + dh) * 32 + lane) * 8;
-        const float* other = xbuf + ((((page_ctr & 1) * HG + hg) * 2 + (dh ^ 1)) * 32 + lane) * 8;
+      for (int pg = 0; pg < kTilePages; ++pg) {
+        const int k = c.t * kTilePages + pg;
+        const int pc = __shfl_sync(0xffffffffu, ph_cur, k & 31), vc = __shfl_sync(0xffffffffu, va_cur, k & 31);
+        const int pn = __shfl_sync(0xffffffffu, ph_nxt, k & 31), vn = __shfl_sync(0xffffffffu, va_nxt, k & 31);
+        const bool in_cur = k < base + 32;
+        phys[pg] = in_cur ? pc : pn;
+        valid[pg] = in_cur ? vc : vn;
+        live += valid[pg] > 0;
+      }
+      if (lane == 0) {
+        if (c.j >= 2 && !mbar_wait(&empty[s], ((c.j >> 1) - 1) & 1)) dead = true;
+        if (!dead) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mine[e] = sc[e >> 2][e & 3];
-        pair_barrier(hg);
+          for (int pg = 0; pg < kTilePages; ++pg) tile_valid[s * kTilePages + pg] = valid[pg];
+          uint8_t* st = smem + s * kStageBytes;
+#pragma unroll 1
+          for (int ch = 0; ch < kChunks; ++ch) {
+            mbar_arrive_expect_tx(&full[s * kChunks + ch], (uint32_t)live * kPageSize * 128);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) sc[e >> 2][e & 3] += other[e];
-        // Online softmax in the log2 domain (identical in both warps of the pair).
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = nt * 8 + 2 * t + (e & 1);
-            sc[nt][e] = tok < valid ? sc[nt][e] * a.scale_log2 : -INFINITY;
+            for (int pg = 0; pg < kTilePages; ++pg)
+              if (valid[pg] > 0)
+                tma_load_2d(st + ch * kChunkBytes + pg * kPageSize * 128, &kvmap, ch * 64, phys[pg] * kPageSize,
+                            &full[s * kChunks + ch], policy);
           }
-        float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-        float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float c0 = fast_exp2(m0 - n0), c1 = fast_exp2(m1 - n1);
-        m0 = n0;
-        m1 = n1;
-        float p[2][4];
+          if (c.t == 0) {
+            // The request's queries, once the previous segment's S^T MMAs are done with the buffer.
+            if (c.seg >= 1 && !mbar_wait(q_empty, (c.seg - 1) & 1)) dead = true;
+            if (!dead) {
+              mbar_arrive_expect_tx(q_full, (uint32_t)Hq * kD * 2);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          p[nt][0] = fast_exp2(sc[nt][0] - n0);
-          p[nt][1] = fast_exp2(sc[nt][1] - n0);
-          p[nt][2] = fast_exp2(sc[nt][2] - n1);
-          p[nt][3] = fast_exp2(sc[nt][3] - n1);
-        }
-        l0 = l0 * c0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-        l1 = l1 * c1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          o[j][0] *= c0;
-          o[j][1] *= c0;
-          o[j][2] *= c1;
-          o[j][3] *= c1;
-        }
-        const uint32_t pa0 = pack_bf16x2(p[0][0], p[0][1]);
-        const uint32_t pa1 = pack_bf16x2(p[0][2], p[0][3]);
-        const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]);
-        const uint32_t pa3 = pack_bf16x2(p[1][2], p[1][3]);
-        // O[:, 256 dh + 16 j ..] += P V (value = first 512 dims of the row).
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n0d = dh * 256 + 16 * j;
-          const int q = ((n0d & 63) >> 3) + vsub;
-          uint32_t r0, r1, r2, r3;
-          ldmatrix_x4_trans(r0, r1, r2, r3, st + (n0d >> 6) * kChunkBytes + swz128(vtok, q));
-          mma_bf16_16816(o[2 * j], pa0, pa1, pa2, pa3, r0, r1);
-          mma_bf16_16816(o[2 * j + 1], pa0, pa1, pa2, pa3, r2, r3);
+              for (int ch = 0; ch < kChunks; ++ch)
+                tma_load_2d(smem + kQOff + ch * kQRows * 128, &qmap, ch * 64, c.item * Hq, q_full, policy);
+            }
+          }
         }
       }
-      __syncthreads();  // stage k % kStages is refilled next
+      if (__shfl_sync(0xffffffffu, (int)dead, 0)) {
+        dead = true;
+        break;
+      }
     }
-    cp_async_wait<0>();
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    // Output rows of this warp: heads 16 hg + g (m0, l0) and + g + 8 (m1, l1).
-    const int cnt = prefix[item + 1] - p0;
-    const int first_cta = p0 / per_cta;
-    const int ns = (p0 + cnt - 1) / per_cta - first_cta + 1;
-    const int slot = blockIdx.x - first_cta;
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    const size_t row0 = (size_t)b * a.Hq + hg * 16 + g, row1 = row0 + 8;
+    if (dead && lane == 0) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    // Two cursors: the S^T MMAs of the next tile chunk by chunk as the chunks
+    // land, the PV MMAs of the oldest tile as soon as its P is written, in
+    // whichever order they come.
+    if (lane == 0) {
+      const uint32_t idesc_s = umma_idesc_bf16(64, Hq);
+      const uint32_t idesc_o = umma_idesc_bf16_mn(128, 64);
+      TileCursor cs, cp;
+      cs.init(prefix, start, end, i_first, i_last);
+      cp.init(prefix, start, end, i_first, i_last);
+      bool q_ok = false, sf_ok = false, o_ok = false;
+      int ch = 0;  // next chunk of the current S^T
+      uint64_t t_last = global_timer_ns();
+      uint32_t idle = 0;
+      while (cp.valid) {
+        bool progress = false;
+        if (cs.valid) {
+          const int s = cs.j & 1;
+          if (cs.t == 0 && !q_ok) q_ok = mbar_try_wait(q_full, cs.seg & 1);
+          if (!sf_ok) sf_ok = cs.j < 2 || mbar_try_wait(&s_free[s], ((cs.j >> 1) - 1) & 1);
+          if ((cs.t != 0 || q_ok) && sf_ok) {
+            const uint32_t st = smem0 + s * kStageBytes;
+            while (ch < kChunks && mbar_try_wait(&full[s * kChunks + ch], (cs.j >> 1) & 1)) {
+              tc05_fence_after();
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int d = dh * 256 + 8 * j + 2 * t;
-      if (ns == 1) {
-        *reinterpret_cast<uint32_t*>(a.out + row0 * kDv + d) = pack_bf16x2(o[j][0] * inv0, o[j][1] * inv0);
-        *reinterpret_cast<uint32_t*>(a.out + row1 * kDv + d) = pack_bf16x2(o[j][2] * inv1, o[j][3] * inv1);
+              for (int kk = 0; kk < 4; ++kk)
+                tc05_mma_bf16(tmem + kSCol + s * 64, umma_desc_sw128(st + ch * kChunkBytes + kk * 32),
+                              umma_desc_sw128(smem0 + kQOff + ch * (kQRows * 128) + kk * 32), idesc_s,
+                              (ch | kk) != 0 ? 1u : 0u);
+              ++ch;
+              progress = true;
+            }
+            if (ch == kChunks) {
+              tc05_commit(&s_full[s]);
+              if (cs.last()) tc05_commit(q_empty);
+              q_ok = sf_ok = false;
+              ch = 0;
+              cs.next();
+            }
+          }
+        }
+        if (cp.j < cs.j) {
+          const int s = cp.j & 1;
+          const bool first = cp.t == 0;
+          if (!o_ok) o_ok = !(first && cp.seg >= 1) || mbar_try_wait(o_free, (cp.seg - 1) & 1);
+          if (o_ok && mbar_try_wait(&p_full[s], (cp.j >> 1) & 1)) {
+            tc05_fence_after();
+            const uint32_t st = smem0 + s * kStageBytes, pb = st + kPOff;
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc05_mma_bf16(tmem + kOCol + mt * 64,
+                              umma_desc_sw128_mn(st + 2 * mt * kChunkBytes + kk * 2048, kChunkBytes),
+                              umma_desc_sw128_mn(pb + kk * 2048, kChunkBytes), idesc_o, (first && kk == 0) ? 0u : 1u);
+            tc05_commit(&empty[s]);
+            tc05_commit(o_done);
+            o_ok = false;
+            cp.next();
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle = 0;
+          t_last = global_timer_ns();
+        } else if (++idle >= kWaitLimitIters || ((idle & 63u) == 0 && global_timer_ns() - t_last > kWaitLimitNs)) {
+          dead = true;
+          break;
+        }
+      }
+      if (dead) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+      tc05_commit(fin);
+      if (!mbar_wait(fin, 0)) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    // Warp w: page w % 4 of the tile (its TMEM lane quarter), heads 32 (w / 4) ..;
+    // thread: token `tok` of the page, heads hh .. hh + 15.
+    const int q4 = warp & 3;
+    const int tok = lane & 15, hh = 32 * (warp >> 2) + 16 * (lane >> 4);
+    const int hr = hh + reduced_index(lane);  // head of this thread's reduction results
+    const int row = q4 * kPageSize + tok;     // token row of the tile
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    float m_h[16], l_h[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m_h[i] = l_h[i] = 0.f;
+    TileCursor c;
+    c.init(prefix, start, end, i_first, i_last);
+    for (; c.valid; c.next()) {
+      const int j = c.j, t = c.t, s = j & 1;
+      const bool ok_s = __all_sync(0xffffffffu, mbar_wait(&s_full[s], (j >> 1) & 1));
+      uint32_t r[16];
+      if (ok_s) {
+        tc05_fence_after();
+        tmem_ld16x2_16(tmem + lane_base + kSCol + s * 64 + 32 * (warp >> 2), r);
+        tmem_ld_wait();
       } else {
-        *reinterpret_cast<float2*>(a.o_part + (row0 * a.max_splits + slot) * kDv + d) =
-            make_float2(o[j][0] * inv0, o[j][1] * inv0);
-        *reinterpret_cast<float2*>(a.o_part + (row1 * a.max_splits + slot) * kDv + d) =
-            make_float2(o[j][2] * inv1, o[j][3] * inv1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = 0u;
       }
-    }
-    if (dh == 0 && t == 0) {
-      const float lse0 = l0 > 0.f ? m0 + log2f(l0) : -INFINITY, lse1 = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
-      if (ns == 1) {
-        if (a.out_lse) {
-          a.out_lse[row0] = lse0 * kLn2;
-          a.out_lse[row1] = lse1 * kLn2;
+      tc05_fence_before();
+      mbar_arrive(&s_free[s]);
+      const bool ok_f = mbar_wait(&full[s * kChunks], (j >> 1) & 1);  // valid rows of the tile
+      dead = dead || !ok_s || !ok_f;
+      const bool tok_ok = tok < tile_valid[s * kTilePages + q4];
+      float x[16], v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        x[i] = (tok_ok && hh + i < Hq) ? __uint_as_float(r[i]) * a.scale_log2 : -INFINITY;
+        v[i] = x[i];
+      }
+      if (!tok_ok && (warp >> 2) == 0) {
+        // Rows past the request's length (or of pages not copied) hold stale
+        // data: zero their value dims so that P = 0 times them stays 0.
+        const uint32_t st = smem0 + s * kStageBytes;
+#pragma unroll 1
+        for (int ch = 4 * (lane >> 4); ch < 4 * (lane >> 4) + 4; ++ch)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) st_shared_v4(st + ch * kChunkBytes + swz128(row, k), 0u, 0u, 0u, 0u);
+      }
+      half_warp_reduce16<true>(v, lane);
+      xmax[q4 * 64 + hr] = v[0];
+      if (bar_red_or(kSoftBar, kSoftThreads, dead)) {  // also publishes xmax
+        dead = true;
+        break;
+      }
+      // Running maximum per head: set by the segment's first tile, then moved
+      // only when a tile exceeds it by 2^8 (so P stays <= 256).
+      float mo[16];
+      bool moved = false;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 w0 = *reinterpret_cast<const float4*>(xmax + hh + 4 * k);
+        const float4 w1 = *reinterpret_cast<const float4*>(xmax + 64 + hh + 4 * k);
+        const float4 w2 = *reinterpret_cast<const float4*>(xmax + 128 + hh + 4 * k);
+        const float4 w3 = *reinterpret_cast<const float4*>(xmax + 192 + hh + 4 * k);
+        const float tm[4] = {fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x)), fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y)),
+                             fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z)), fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w))};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * k + e;
+          mo[i] = m_h[i];
+          const float mn = (t == 0 || tm[e] > mo[i] + kRescaleLog2) ? tm[e] : mo[i];
+          moved = moved || (t > 0 && mn != mo[i]);
+          m_h[i] = mn;
+          if (t == 0) l_h[i] = 0.f;
         }
-      } else {
-        a.lse_part[row0 * a.max_splits + slot] = lse0;
-        a.lse_part[row1 * a.max_splits + slot] = lse1;
+      }
+      if (bar_red_or(kSoftBar, kSoftThreads, moved)) {
+        // Rare: bring l and the O^T columns of the heads that moved to the new maxima.
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float f = m_h[i] == mo[i] ? 1.f : fast_exp2(mo[i] - m_h[i]);
+          l_h[i] *= f;
+          if (q4 == 0 && tok == 0) fac_s[hh + i] = f;
+        }
+        named_bar_sync(kSoftBar, kSoftThreads);
+        const bool ok_o = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1));
+        if (ok_o) {
+          tc05_fence_after();
+#pragma unroll 1
+          for (int mt = 0; mt < 4; ++mt) {
+            const uint32_t ta = tmem + lane_base + kOCol + mt * 64 + 32 * (warp >> 2);
+            uint32_t o[32];
+            tmem_ld32(ta, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc)
+              o[cc] = __float_as_uint(__uint_as_float(o[cc]) * fac_s[32 * (warp >> 2) + cc]);
+            tmem_st32(ta, o);
+          }
+          tmem_st_wait();
+        } else {
+          dead = true;
+        }
+      }
+      // P of this token for heads hh .. hh + 15 into row `row` of the tile's
+      // RoPE chunk (64 heads per 128-byte row).
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float ma = m_h[2 * i] == -INFINITY ? 0.f : m_h[2 * i];
+        const float mb = m_h[2 * i + 1] == -INFINITY ? 0.f : m_h[2 * i + 1];
+        const float pa = fast_exp2(x[2 * i] - ma), pb = fast_exp2(x[2 * i + 1] - mb);
+        l_h[2 * i] += pa;
+        l_h[2 * i + 1] += pb;
+        pk[i] = pack_bf16x2(pa, pb);
+      }
+      const uint32_t prow = smem0 + s * kStageBytes + kPOff;
+      st_shared_v4(prow + swz128(row, hh >> 3), pk[0], pk[1], pk[2], pk[3]);
+      st_shared_v4(prow + swz128(row, (hh >> 3) + 1), pk[4], pk[5], pk[6], pk[7]);
+      fence_proxy_async_smem();
+      tc05_fence_before();
+      mbar_arrive(&p_full[s]);
+
+      if (c.last()) {
+        // ---- epilogue of the segment: O = O^T / l per head, or a partial
+        const int b = c.item;
+        const bool ok_e = __all_sync(0xffffffffu, mbar_wait(o_done, j & 1));
+        dead = dead || !ok_e;
+        float w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = l_h[i];
+        half_warp_reduce16<false>(w, lane);
+        lsum[q4 * 64 + hr] = w[0];
+        if (q4 == 0 && tok == 0)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) mrow[hh + i] = m_h[i];
+        named_bar_sync(kSoftBar, kSoftThreads);
+        if (threadIdx.x < 64) {
+          const int h = threadIdx.x;
+          const float l = (lsum[h] + lsum[64 + h]) + (lsum[128 + h] + lsum[192 + h]);
+          linv[h] = l > 0.f ? 1.f / l : 0.f;
+          lse_s[h] = l > 0.f ? mrow[h] + log2f(l) : -INFINITY;
+        }
+        named_bar_sync(kSoftBar, kSoftThreads);
+        const int p0 = prefix[b], cnt = prefix[b + 1] - p0;
+        const int first_cta = p0 / per_cta;
+        const int ns = (p0 + cnt - 1) / per_cta - first_cta + 1;
+        const int slot = blockIdx.x - first_cta;
+        if (ok_e) {
+          tc05_fence_after();
+#pragma unroll 1
+          for (int mt = 0; mt < 4; ++mt) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + kOCol + mt * 64 + 32 * (warp >> 2), o);
+            tmem_ld_wait();
+            const int d = mt * 128 + 32 * q4 + lane;
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+              const int h = 32 * (warp >> 2) + cc;
+              if (h < Hq) {
+                const float val = __uint_as_float(o[cc]) * linv[h];
+                const size_t orow = (size_t)b * Hq + h;
+                if (ns == 1)
+                  a.out[orow * kDv + d] = (uint16_t)(pack_bf16x2(val, 0.f) & 0xffffu);
+                else
+                  a.o_part[(orow * a.max_splits + slot) * kDv + d] = val;
+              }
+            }
+          }
+        }
+        if (threadIdx.x < Hq) {
+          const size_t orow = (size_t)b * Hq + threadIdx.x;
+          if (ns == 1) {
+            if (a.out_lse) a.out_lse[orow] = lse_s[threadIdx.x] * kLn2;
+          } else {
+            a.lse_part[orow * a.max_splits + slot] = lse_s[threadIdx.x];
+          }
+        }
+        tc05_fence_before();
+        mbar_arrive(o_free);
       }
     }
-    __syncthreads();  // the ring is refilled by the next segment
   }
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 // Merge of the partials of requests spread over several CTAs (one warp per
@@ -392,20 +670,7 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
   if (out_lse && lane == 0) out_lse[row] = empty_row ? -INFINITY : (M + log2f(wsum)) * kLn2;
 }
 
-size_t smem_bytes(int HG, int32_t batch) {
-  return (size_t)kRingBytes + 1024 + (size_t)2 * HG * 2 * 32 * 8 * 4 + (size_t)(batch + 1) * 4;
-}
-
-template <int HG>
-cudaError_t launch_hg(const MlaArgs& a, int grid, size_t smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  {
-    const cudaError_t le = launch_pdl(mla_decode_kernel<HG>, dim3(grid), dim3(64 * HG), smem, stream, a);
-    if (le != cudaSuccess) return le;
-  }
-  return cudaGetLastError();
-}
+size_t smem_bytes(int32_t batch) { return 1024 + (size_t)kMiscOff + kPrefixOff + (size_t)(batch + 1) * 4; }
 
 }  // namespace
 
@@ -428,11 +693,12 @@ size_t mla_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, const Deco
   return ((part + 15) & ~size_t(15)) + (size_t)batch * sizeof(int32_t);
 }
 
-// Requests one launch takes: the per-request prefix must fit beside the ring
-// in shared memory (at 64 query heads).
-size_t mla_decode_max_items() { return (227 * 1024 - smem_bytes(4, 0)) / 4; }
+// Requests one launch takes: the per-request prefix must fit beside the two
+// tiles and the queries in shared memory.
+size_t mla_decode_max_items() { return (227 * 1024 - smem_bytes(0)) / 4; }
 
-cudaError_t launch_mla_decode(const KvView& kv, const uint16_t* q, int32_t num_q_heads, const int32_t* block_table,
+cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const CUtensorMap& qmap, const KvView& kv, const uint16_t* q,
+                              int32_t num_q_heads, const int32_t* block_table,
                               int32_t bt_stride, const int32_t* seq_lens, int32_t batch, const int32_t* sel_pages,
                               const int32_t* sel_counts, int32_t sel_stride, float sm_scale, uint16_t* out,
                               float* out_lse, void* workspace, const DecodePlan& plan, unsigned* err,
@@ -462,21 +728,14 @@ cudaError_t launch_mla_decode(const KvView& kv, const uint16_t* q, int32_t num_q
   a.lse_part = a.o_part + rows * plan.nsplit * kDv;
   a.item_ns = reinterpret_cast<int32_t*>(ws + ((part + 15) & ~size_t(15)));
   a.err = err;
-  const int HG = num_q_heads / 16;
-  const size_t smem = smem_bytes(HG, batch);
-  cudaError_t e;
-  switch (HG) {
-    case 1: e = launch_hg<1>(a, plan.grid, smem, stream); break;
-    case 2: e = launch_hg<2>(a, plan.grid, smem, stream); break;
-    case 3: e = launch_hg<3>(a, plan.grid, smem, stream); break;
-    default: e = launch_hg<4>(a, plan.grid, smem, stream); break;
-  }
+  const size_t smem = smem_bytes(batch);
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  {
-    const cudaError_t le = launch_pdl(mla_combine_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, stream,
-                                      a.o_part, a.lse_part, a.item_ns, batch, num_q_heads, plan.nsplit, out, out_lse);
-    if (le != cudaSuccess) return le;
-  }
+  e = launch_pdl(mla_decode_kernel, dim3(plan.grid), dim3(kThreads), smem, stream, kvmap, qmap, a);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(mla_combine_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, stream, a.o_part, a.lse_part,
+                 a.item_ns, batch, num_q_heads, plan.nsplit, out, out_lse);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

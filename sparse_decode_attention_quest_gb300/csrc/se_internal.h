@@ -94,7 +94,10 @@ bool mla_decode_supported(int num_kv_heads, int head_dim, int head_dim_v, int nu
 DecodePlan plan_mla_decode(int32_t sel_stride, int sm_count);
 size_t mla_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, const DecodePlan& plan);
 size_t mla_decode_max_items();
-cudaError_t launch_mla_decode(const KvView& kv, const uint16_t* q, int32_t num_q_heads, const int32_t* block_table,
+// kvmap: the cache as rows of 576 bf16, boxes of 64 x 16; qmap: the queries as
+// batch x num_q_heads rows of 576, boxes of 64 x num_q_heads (both 128-byte swizzle).
+cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const CUtensorMap& qmap, const KvView& kv, const uint16_t* q,
+                              int32_t num_q_heads, const int32_t* block_table,
                               int32_t bt_stride, const int32_t* seq_lens, int32_t batch, const int32_t* sel_pages,
                               const int32_t* sel_counts, int32_t sel_stride, float sm_scale, uint16_t* out,
                               float* out_lse, void* workspace, const DecodePlan& plan, unsigned* err,
@@ -132,7 +135,6 @@ cudaError_t launch_snapkv_gather(const KvView& src, uint16_t* dk, uint16_t* dv, 
 
 // ---- api.cu: per-device context and helpers shared with other entry points
 cudaError_t device_context(int* sm_count, unsigned** err);
-bool encode_kv_page_map(CUtensorMap* map, const void* base, long long rows, int width, int row_stride);
 void set_error_detail(const char* fn, const char* what);
 
 }  // namespace se
