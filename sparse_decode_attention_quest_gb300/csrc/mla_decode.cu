@@ -16,8 +16,8 @@
 //    a tile with nine TMA boxes (64 dims x 16 rows); pages not selected are not
 //    copied, and the value dims of rows at or past the request's length are
 //    zeroed in shared memory by the softmax warps before the PV MMAs read them.
-//  * One thread issues all MMAs, S^T of the next tile as soon as it has landed
-//    and PV of the oldest tile as soon as its P is written.
+//  * Two threads issue the MMAs: one the S^T MMAs of each tile chunk by chunk as
+//    the chunks land, the other the PV MMAs of each tile once its P is written.
 //  * S^T = K Q^T: one M = 64 tcgen05.mma per 16 dims (36 per tile) with the tile
 //    as the K-major A operand and the request's queries (64 rows x 576 dims in
 //    shared memory) as B; S^T lands in TMEM, token r in lane 32 (r / 16) + r % 16.
@@ -51,10 +51,11 @@ constexpr int kQBytes = kChunks * kQRows * 128;         // 64 heads x 576 dims
 constexpr int kPOff = 8 * kChunkBytes;                  // P of a tile: over its RoPE chunk
 constexpr int kQOff = kStages * kStageBytes;
 constexpr int kMiscOff = kQOff + kQBytes;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftThreads = 256;                       // warps 0-7: softmax + epilogue
-constexpr int kMmaWarp = 8;                             // lane 0 issues every MMA
+constexpr int kMmaWarp = 8;                             // lane 0 issues the S^T MMAs (and owns TMEM)
 constexpr int kLoadWarp = 9;                            // lane 0 issues the TMA copies
+constexpr int kPvWarp = 10;                             // lane 0 issues the PV MMAs
 constexpr int kTmemCols = 512;
 constexpr int kSCol = 0;                                // S^T buffers: columns 0, 64
 constexpr int kOCol = 128;                              // O^T M-tile mt: columns 128 + 64 mt
@@ -65,13 +66,12 @@ constexpr uint32_t kSoftBar = 1;                        // named barrier of the 
 constexpr int kBarOff = 0;        // 31 mbarriers
 constexpr int kTmemSlotOff = 256;
 constexpr int kValidOff = 272;    // [2 stages][4 pages] valid rows
-constexpr int kXmaxOff = 512;     // [4 pages][64 heads] tile maxima
-constexpr int kFacOff = 1536;     // [64] rescale factors
-constexpr int kLsumOff = 1792;    // [4 pages][64] softmax sums
-constexpr int kMrowOff = 2816;    // [64] running maxima
-constexpr int kLinvOff = 3072;    // [64] 1 / sum
-constexpr int kLseOff = 3328;     // [64] log2-sum-exp2
-constexpr int kPrefixOff = 3584;  // [batch + 1]
+constexpr int kXmaxOff = 512;     // [2 tile parities][4 pages][64 heads] tile maxima
+constexpr int kLsumOff = 2560;    // [4 pages][64] softmax sums
+constexpr int kMrowOff = 3584;    // [64] running maxima
+constexpr int kLinvOff = 3840;    // [64] 1 / sum
+constexpr int kLseOff = 4096;     // [64] log2-sum-exp2
+constexpr int kPrefixOff = 4352;  // [batch + 1]
 
 struct MlaArgs {
   const uint16_t* kv;
@@ -188,11 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
   uint64_t* o_free = bars + 27;   // O^T read by the epilogue (softmax threads)
   uint64_t* q_full = bars + 28;   // the request's queries landed
   uint64_t* q_empty = bars + 29;  // the last S^T MMA of a request's segment is done
-  uint64_t* fin = bars + 30;      // every MMA of the CTA is done
+  uint64_t* fin = bars + 30;      // every MMA of the CTA is done (both issuers)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + kTmemSlotOff);
   int* tile_valid = reinterpret_cast<int*>(misc + kValidOff);
   float* xmax = reinterpret_cast<float*>(misc + kXmaxOff);
-  float* fac_s = reinterpret_cast<float*>(misc + kFacOff);
   float* lsum = reinterpret_cast<float*>(misc + kLsumOff);
   float* mrow = reinterpret_cast<float*>(misc + kMrowOff);
   float* linv = reinterpret_cast<float*>(misc + kLinvOff);
@@ -253,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     mbar_init(o_free, kSoftThreads);
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    mbar_init(fin, 1);
+    mbar_init(fin, 2);
     mbar_fence_init();
   }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
@@ -369,79 +368,82 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     }
     if (dead && lane == 0) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // Two cursors: the S^T MMAs of the next tile chunk by chunk as the chunks
-    // land, the PV MMAs of the oldest tile as soon as its P is written, in
-    // whichever order they come.
+    // ------------------------------------------------------------ S^T issuer
+    // The score MMAs of each tile, chunk by chunk as the chunks land.
     if (lane == 0) {
       const uint32_t idesc_s = umma_idesc_bf16(64, Hq);
-      const uint32_t idesc_o = umma_idesc_bf16_mn(128, 64);
-      TileCursor cs, cp;
-      cs.init(prefix, start, end, i_first, i_last);
-      cp.init(prefix, start, end, i_first, i_last);
-      bool q_ok = false, sf_ok = false, o_ok = false;
-      int ch = 0;  // next chunk of the current S^T
-      uint64_t t_last = global_timer_ns();
-      uint32_t idle = 0;
-      while (cp.valid) {
-        bool progress = false;
-        if (cs.valid) {
-          const int s = cs.j & 1;
-          if (cs.t == 0 && !q_ok) q_ok = mbar_try_wait(q_full, cs.seg & 1);
-          if (!sf_ok) sf_ok = cs.j < 2 || mbar_try_wait(&s_free[s], ((cs.j >> 1) - 1) & 1);
-          if ((cs.t != 0 || q_ok) && sf_ok) {
-            const uint32_t st = smem0 + s * kStageBytes;
-            while (ch < kChunks && mbar_try_wait(&full[s * kChunks + ch], (cs.j >> 1) & 1)) {
-              tc05_fence_after();
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                tc05_mma_bf16(tmem + kSCol + s * 64, umma_desc_sw128(st + ch * kChunkBytes + kk * 32),
-                              umma_desc_sw128(smem0 + kQOff + ch * (kQRows * 128) + kk * 32), idesc_s,
-                              (ch | kk) != 0 ? 1u : 0u);
-              ++ch;
-              progress = true;
-            }
-            if (ch == kChunks) {
-              tc05_commit(&s_full[s]);
-              if (cs.last()) tc05_commit(q_empty);
-              q_ok = sf_ok = false;
-              ch = 0;
-              cs.next();
-            }
-          }
-        }
-        if (cp.j < cs.j) {
-          const int s = cp.j & 1;
-          const bool first = cp.t == 0;
-          if (!o_ok) o_ok = !(first && cp.seg >= 1) || mbar_try_wait(o_free, (cp.seg - 1) & 1);
-          if (o_ok && mbar_try_wait(&p_full[s], (cp.j >> 1) & 1)) {
-            tc05_fence_after();
-            const uint32_t st = smem0 + s * kStageBytes, pb = st + kPOff;
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                tc05_mma_bf16(tmem + kOCol + mt * 64,
-                              umma_desc_sw128_mn(st + 2 * mt * kChunkBytes + kk * 2048, kChunkBytes),
-                              umma_desc_sw128_mn(pb + kk * 2048, kChunkBytes), idesc_o, (first && kk == 0) ? 0u : 1u);
-            tc05_commit(&empty[s]);
-            tc05_commit(o_done);
-            o_ok = false;
-            cp.next();
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle = 0;
-          t_last = global_timer_ns();
-        } else if (++idle >= kWaitLimitIters || ((idle & 63u) == 0 && global_timer_ns() - t_last > kWaitLimitNs)) {
+      // Operand descriptors of the bases; an MMA adds a constant offset (the
+      // address field is bits 0-13 of (address >> 4), and every shared address
+      // here is below 256 KB, so the additions never carry out of it).
+      const uint64_t desc_k0 = umma_desc_sw128(smem0);
+      const uint64_t desc_q = umma_desc_sw128(smem0 + kQOff);
+      constexpr uint64_t kStageDesc = kStageBytes >> 4;
+      TileCursor c;
+      c.init(prefix, start, end, i_first, i_last);
+      for (; c.valid && !dead; c.next()) {
+        const int s = c.j & 1;
+        if ((c.t == 0 && !mbar_wait(q_full, c.seg & 1)) || (c.j >= 2 && !mbar_wait(&s_free[s], ((c.j >> 1) - 1) & 1))) {
           dead = true;
           break;
         }
+        tc05_fence_after();  // after the softmax's read of this S^T buffer
+        const uint32_t d_s = tmem + kSCol + s * 64;
+        const uint64_t dk = desc_k0 + (s ? kStageDesc : 0);
+#pragma unroll 1
+        for (int ch = 0; ch < kChunks; ++ch) {
+          if (!mbar_wait(&full[s * kChunks + ch], (c.j >> 1) & 1)) {
+            dead = true;
+            break;
+          }
+          // 16 dims = 32 bytes = 2 per K step; a chunk is (chunk bytes >> 4) further.
+          const uint64_t da = dk + (uint64_t)(ch * (kChunkBytes >> 4));
+          const uint64_t dq = desc_q + (uint64_t)(ch * ((kQRows * 128) >> 4));
+          tc05_mma_bf16(d_s, da, dq, idesc_s, ch != 0 ? 1u : 0u);
+          tc05_mma_bf16(d_s, da + 2, dq + 2, idesc_s, 1u);
+          tc05_mma_bf16(d_s, da + 4, dq + 4, idesc_s, 1u);
+          tc05_mma_bf16(d_s, da + 6, dq + 6, idesc_s, 1u);
+        }
+        if (dead) break;
+        tc05_commit(&s_full[s]);
+        if (c.last()) tc05_commit(q_empty);
       }
       if (dead) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
       tc05_commit(fin);
-      if (!mbar_wait(fin, 0)) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ PV issuer
+    // O^T += V^T P^T of each tile once its P is written.
+    if (lane == 0) {
+      const uint32_t idesc_o = umma_idesc_bf16_mn(128, 64);
+      const uint64_t desc_v0 = umma_desc_sw128_mn(smem0, kChunkBytes);
+      constexpr uint64_t kStageDesc = kStageBytes >> 4, kPDesc = kPOff >> 4;
+      TileCursor c;
+      c.init(prefix, start, end, i_first, i_last);
+      for (; c.valid; c.next()) {
+        const int s = c.j & 1;
+        const bool first = c.t == 0;
+        if (!mbar_wait(&p_full[s], (c.j >> 1) & 1) || (first && c.seg >= 1 && !mbar_wait(o_free, (c.seg - 1) & 1))) {
+          dead = true;
+          break;
+        }
+        tc05_fence_after();
+        // 16 tokens = 2048 bytes = 128 per K step; 128 dims = 2 chunks = 1024 per M-tile.
+        const uint64_t dv = desc_v0 + (s ? kStageDesc : 0), dp = dv + kPDesc;
+        const uint32_t acc0 = first ? 0u : 1u;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const uint32_t d_o = tmem + kOCol + mt * 64;
+          tc05_mma_bf16(d_o, dv + mt * 1024, dp, idesc_o, acc0);
+          tc05_mma_bf16(d_o, dv + mt * 1024 + 128, dp + 128, idesc_o, 1u);
+          tc05_mma_bf16(d_o, dv + mt * 1024 + 256, dp + 256, idesc_o, 1u);
+          tc05_mma_bf16(d_o, dv + mt * 1024 + 384, dp + 384, idesc_o, 1u);
+        }
+        tc05_commit(&empty[s]);
+        tc05_commit(o_done);
+      }
+      if (dead) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+      tc05_commit(fin);
     }
     __syncwarp();
   } else {
@@ -491,44 +493,46 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
           for (int k = 0; k < 8; ++k) st_shared_v4(st + ch * kChunkBytes + swz128(row, k), 0u, 0u, 0u, 0u);
       }
       half_warp_reduce16<true>(v, lane);
-      xmax[q4 * 64 + hr] = v[0];
+      // Two buffers by tile parity: the one barrier per tile keeps every thread
+      // within one tile of the others.
+      float* xm = xmax + s * 256;
+      xm[q4 * 64 + hr] = v[0];
       if (bar_red_or(kSoftBar, kSoftThreads, dead)) {  // also publishes xmax
         dead = true;
         break;
       }
       // Running maximum per head: set by the segment's first tile, then moved
-      // only when a tile exceeds it by 2^8 (so P stays <= 256).
-      float mo[16];
+      // only when a tile exceeds it by 2^8 (so P stays <= 256). Every warp of a
+      // head half computes the same maxima from the same tile maxima.
+      float f[16];
       bool moved = false;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float4 w0 = *reinterpret_cast<const float4*>(xmax + hh + 4 * k);
-        const float4 w1 = *reinterpret_cast<const float4*>(xmax + 64 + hh + 4 * k);
-        const float4 w2 = *reinterpret_cast<const float4*>(xmax + 128 + hh + 4 * k);
-        const float4 w3 = *reinterpret_cast<const float4*>(xmax + 192 + hh + 4 * k);
+        const float4 w0 = *reinterpret_cast<const float4*>(xm + hh + 4 * k);
+        const float4 w1 = *reinterpret_cast<const float4*>(xm + 64 + hh + 4 * k);
+        const float4 w2 = *reinterpret_cast<const float4*>(xm + 128 + hh + 4 * k);
+        const float4 w3 = *reinterpret_cast<const float4*>(xm + 192 + hh + 4 * k);
         const float tm[4] = {fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x)), fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y)),
                              fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z)), fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w))};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = 4 * k + e;
-          mo[i] = m_h[i];
-          const float mn = (t == 0 || tm[e] > mo[i] + kRescaleLog2) ? tm[e] : mo[i];
-          moved = moved || (t > 0 && mn != mo[i]);
+          const float mo = m_h[i];
+          const float mn = (t == 0 || tm[e] > mo + kRescaleLog2) ? tm[e] : mo;
+          const bool mv = t > 0 && mn != mo;
+          f[i] = mv ? fast_exp2(mo - mn) : 1.f;
+          moved = moved || mv;
           m_h[i] = mn;
-          if (t == 0) l_h[i] = 0.f;
+          l_h[i] = t == 0 ? 0.f : l_h[i] * f[i];
         }
       }
-      if (bar_red_or(kSoftBar, kSoftThreads, moved)) {
-        // Rare: bring l and the O^T columns of the heads that moved to the new maxima.
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float f = m_h[i] == mo[i] ? 1.f : fast_exp2(mo[i] - m_h[i]);
-          l_h[i] *= f;
-          if (q4 == 0 && tok == 0) fac_s[hh + i] = f;
-        }
-        named_bar_sync(kSoftBar, kSoftThreads);
+      if (__any_sync(0xffffffffu, moved)) {
+        // Rare: the O^T columns of this warp's head half (its lane quarter) to the new maxima.
         const bool ok_o = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1));
         if (ok_o) {
+          float fc[32];  // factor of column c of the half: lanes 0-15 hold heads 0-15, lanes 16-31 heads 16-31
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) fc[cc] = __shfl_sync(0xffffffffu, f[cc & 15], (cc >> 4) * 16);
           tc05_fence_after();
 #pragma unroll 1
           for (int mt = 0; mt < 4; ++mt) {
@@ -537,8 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
             tmem_ld32(ta, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc)
-              o[cc] = __float_as_uint(__uint_as_float(o[cc]) * fac_s[32 * (warp >> 2) + cc]);
+            for (int cc = 0; cc < 32; ++cc) o[cc] = __float_as_uint(__uint_as_float(o[cc]) * fc[cc]);
             tmem_st32(ta, o);
           }
           tmem_st_wait();
@@ -625,6 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
       }
     }
   }
+  if (warp == kMmaWarp && lane == 0 && !mbar_wait(fin, 0)) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
   tc05_fence_before();
   __syncthreads();
   tc05_fence_after();
