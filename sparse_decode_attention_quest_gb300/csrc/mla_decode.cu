@@ -492,61 +492,70 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
 #pragma unroll
           for (int k = 0; k < 8; ++k) st_shared_v4(st + ch * kChunkBytes + swz128(row, k), 0u, 0u, 0u, 0u);
       }
-      half_warp_reduce16<true>(v, lane);
-      // Two buffers by tile parity: the one barrier per tile keeps every thread
-      // within one tile of the others.
-      float* xm = xmax + s * 256;
-      xm[q4 * 64 + hr] = v[0];
-      if (bar_red_or(kSoftBar, kSoftThreads, dead)) {  // also publishes xmax
-        dead = true;
-        break;
-      }
-      // Running maximum per head: set by the segment's first tile, then moved
-      // only when a tile exceeds it by 2^8 (so P stays <= 256). Every warp of a
-      // head half computes the same maxima from the same tile maxima.
-      float f[16];
-      bool moved = false;
+      // Fast path: after the segment's first tile, a tile whose scores all stay
+      // within 2^8 of the running maxima changes nothing but P and l. Otherwise
+      // (first tile, a larger score, or a failed wait) the tile maxima are
+      // exchanged and the running maxima recomputed.
+      bool need = t == 0 || dead;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 w0 = *reinterpret_cast<const float4*>(xm + hh + 4 * k);
-        const float4 w1 = *reinterpret_cast<const float4*>(xm + 64 + hh + 4 * k);
-        const float4 w2 = *reinterpret_cast<const float4*>(xm + 128 + hh + 4 * k);
-        const float4 w3 = *reinterpret_cast<const float4*>(xm + 192 + hh + 4 * k);
-        const float tm[4] = {fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x)), fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y)),
-                             fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z)), fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w))};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 4 * k + e;
-          const float mo = m_h[i];
-          const float mn = (t == 0 || tm[e] > mo + kRescaleLog2) ? tm[e] : mo;
-          const bool mv = t > 0 && mn != mo;
-          f[i] = mv ? fast_exp2(mo - mn) : 1.f;
-          moved = moved || mv;
-          m_h[i] = mn;
-          l_h[i] = t == 0 ? 0.f : l_h[i] * f[i];
-        }
-      }
-      if (__any_sync(0xffffffffu, moved)) {
-        // Rare: the O^T columns of this warp's head half (its lane quarter) to the new maxima.
-        const bool ok_o = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1));
-        if (ok_o) {
-          float fc[32];  // factor of column c of the half: lanes 0-15 hold heads 0-15, lanes 16-31 heads 16-31
-#pragma unroll
-          for (int cc = 0; cc < 32; ++cc) fc[cc] = __shfl_sync(0xffffffffu, f[cc & 15], (cc >> 4) * 16);
-          tc05_fence_after();
-#pragma unroll 1
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint32_t ta = tmem + lane_base + kOCol + mt * 64 + 32 * (warp >> 2);
-            uint32_t o[32];
-            tmem_ld32(ta, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc) o[cc] = __float_as_uint(__uint_as_float(o[cc]) * fc[cc]);
-            tmem_st32(ta, o);
-          }
-          tmem_st_wait();
-        } else {
+      for (int i = 0; i < 16; ++i) need = need || x[i] > m_h[i] + kRescaleLog2;
+      if (bar_red_or(kSoftBar, kSoftThreads, need)) {
+        half_warp_reduce16<true>(v, lane);
+        // Two buffers by tile parity: the barriers keep every thread within one
+        // tile of the others.
+        float* xm = xmax + s * 256;
+        xm[q4 * 64 + hr] = v[0];
+        if (bar_red_or(kSoftBar, kSoftThreads, dead)) {  // also publishes xmax
           dead = true;
+          break;
+        }
+        // Running maximum per head: set by the segment's first tile, then moved
+        // only when a tile exceeds it by 2^8 (so P stays <= 256). Every warp of
+        // a head half computes the same maxima from the same tile maxima.
+        float f[16];
+        bool moved = false;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 w0 = *reinterpret_cast<const float4*>(xm + hh + 4 * k);
+          const float4 w1 = *reinterpret_cast<const float4*>(xm + 64 + hh + 4 * k);
+          const float4 w2 = *reinterpret_cast<const float4*>(xm + 128 + hh + 4 * k);
+          const float4 w3 = *reinterpret_cast<const float4*>(xm + 192 + hh + 4 * k);
+          const float tm[4] = {fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x)), fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y)),
+                               fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z)), fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w))};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * k + e;
+            const float mo = m_h[i];
+            const float mn = (t == 0 || tm[e] > mo + kRescaleLog2) ? tm[e] : mo;
+            const bool mv = t > 0 && mn != mo;
+            f[i] = mv ? fast_exp2(mo - mn) : 1.f;
+            moved = moved || mv;
+            m_h[i] = mn;
+            l_h[i] = t == 0 ? 0.f : l_h[i] * f[i];
+          }
+        }
+        if (__any_sync(0xffffffffu, moved)) {
+          // The O^T columns of this warp's head half (its lane quarter) to the new maxima.
+          const bool ok_o = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1));
+          if (ok_o) {
+            float fc[32];  // factor of column c of the half: lanes 0-15 hold heads 0-15, lanes 16-31 heads 16-31
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) fc[cc] = __shfl_sync(0xffffffffu, f[cc & 15], (cc >> 4) * 16);
+            tc05_fence_after();
+#pragma unroll 1
+            for (int mt = 0; mt < 4; ++mt) {
+              const uint32_t ta = tmem + lane_base + kOCol + mt * 64 + 32 * (warp >> 2);
+              uint32_t o[32];
+              tmem_ld32(ta, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int cc = 0; cc < 32; ++cc) o[cc] = __float_as_uint(__uint_as_float(o[cc]) * fc[cc]);
+              tmem_st32(ta, o);
+            }
+            tmem_st_wait();
+          } else {
+            dead = true;
+          }
         }
       }
       // P of this token for heads hh .. hh + 15 into row `row` of the tile's

@@ -124,3 +124,41 @@ def test_full_mla_glm_32k_sampled(cuda_device):
     x, step, lens = _prepare(wl, cuda_device, device_gen=True)
     _run(x, step, lens, cuda_device)
     compare_decode(x, step, [0, 31, wl.batch - 1], _scale(wl), "mla-glm full")
+
+
+def test_latent_growing_scores_rescale_every_tile(cuda_device):
+    """Scores that grow by more than 2^8 (log2 units) from one 4-page tile to the
+    next, so that the decode's running maxima move on every tile and the output
+    accumulators are rescaled each time. The RoPE dims of page p carry p times a
+    direction shared by every query head; the value dims (the latent part) are
+    left as generated. The decode attends over every page in order (an explicit
+    selection), against the oracle on the same pages; the last page is ragged."""
+    wl = MLA_GLM_QUEST_32K.scaled(batch=2, context_min=2040, context_max=2040, topk_pages=8, seed=71)
+    x = make_quest_decode_inputs(wl, device="cpu", poison_tail=True)
+    gen = torch.Generator().manual_seed(72)
+    u = torch.randn(64, generator=gen)
+    n = x.pages_per_request[0]
+    for b in range(wl.batch):
+        for p in range(n):
+            phys = int(x.block_table[b, p])
+            rows = x.k_cache[phys, 0, :, 512:].float() + 0.6 * p * u
+            x.k_cache[phys, 0, :, 512:] = rows.to(torch.bfloat16)
+    x.q[..., 512:] = (u + 0.05 * torch.randn(x.q[..., 512:].shape, generator=gen)).to(x.q.dtype)
+    dev = cuda_device
+    k = x.k_cache.to(dev)
+    step = QuestDecodeStep(k, None, new_summary(k), x.block_table.to(dev), wl.num_q_heads, wl.topk_pages,
+                           max(x.seq_lens_after), head_dim_v=wl.head_dim_v, sel_stride=n)
+    lens = torch.tensor(x.seq_lens_after, dtype=torch.int32, device=dev)
+    sel = torch.arange(n, dtype=torch.int32).repeat(wl.batch, 1, 1)
+    cnt = torch.full((wl.batch, 1), n, dtype=torch.int32)
+    step.attend(x.q.to(dev), lens, sel.to(dev), cnt.to(dev))
+    torch.cuda.synchronize()
+    inp = oracle_inputs(x)
+    ref = oq.decode_step(inp, wl.topk_pages, _scale(wl), pages_override=[[list(range(n))]] * wl.batch)
+    out = step.out.float().cpu().numpy()
+    lse = step.lse.cpu().numpy()
+    # the shared component alone raises the logits by more than 8 (log2 units) per tile
+    assert 4 * 0.6 * float(u.square().sum()) * _scale(wl) / math.log(2) > 8
+    for r in range(wl.batch):
+        assert np.abs(out[r] - ref[r].out).max() <= OUT_ATOL
+        assert np.abs(lse[r] - ref[r].lse).max() <= LSE_ATOL
