@@ -541,7 +541,8 @@ def _mla_extra(args, dev, flush, stream):
     one 576-dim latent row, value = its first 512 dims), 64 requests at 32K, a 2,048-token
     budget."""
     from synth import MLA_GLM_QUEST_32K
-    return _quest_extra(args, dev, flush, stream, MLA_GLM_QUEST_32K)
+    wl = MLA_GLM_QUEST_32K if _BATCH_OVERRIDE is None else MLA_GLM_QUEST_32K.scaled(batch=_BATCH_OVERRIDE)
+    return _quest_extra(args, dev, flush, stream, wl)
 
 
 def _windows_extra(args, dev, flush, stream):
@@ -656,7 +657,8 @@ def main():
     ap.add_argument("--snapkv-only", action="store_true", help="only the SnapKV measurement (for profiler captures)")
     ap.add_argument("--mla-only", action="store_true", help="only the latent-cache measurement (for profiler captures)")
     ap.add_argument("--cpu-cores", type=int, default=None)
-    ap.add_argument("--batch", type=int, default=None, help="smaller batch for profiler captures only")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="smaller batch (the 128K or, with --mla-only, the latent workload) for profiler captures only")
     args = ap.parse_args()
     global _BATCH_OVERRIDE
     _BATCH_OVERRIDE = args.batch
