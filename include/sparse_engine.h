@@ -140,6 +140,24 @@ SE_API se_status_t se_quest_update_summaries(const se_paged_kv_t* kv, const void
                                       const int32_t* seq_lens_before, int32_t batch, void* stream);
 
 /*
+ * se_quest_update_summaries_ex -- se_quest_update_summaries with flags.
+ *   flags: 0, or SE_APPEND_OVERLAP_PREVIOUS: the append's kernel may start
+ *   while the previous kernel of `stream` still runs (programmatic dependent
+ *   launch, when that kernel allows it) and completes only after it, so work
+ *   queued after the call still sees the previous kernel's results. The caller
+ *   guarantees that the previous kernel neither reads nor writes anything the
+ *   append touches (the written K/V slots and the summary of their page),
+ *   e.g. the page selection of the same step: the page a token lands in is the
+ *   request's last page, which is never scored (it is always kept). Other bits:
+ *   SE_ERR_INVALID_ARG.
+ */
+#define SE_APPEND_OVERLAP_PREVIOUS 0x1u
+SE_API se_status_t se_quest_update_summaries_ex(const se_paged_kv_t* kv, const void* k_new, const void* v_new,
+                                                const int32_t* block_table, int32_t bt_stride,
+                                                const int32_t* seq_lens_before, int32_t batch, uint32_t flags,
+                                                void* stream);
+
+/*
  * se_quest_score_pages -- Quest upper-bound score of every candidate page.
  * SparseEngine, Figure 2 caption and Table 14 (Quest, query-dependent page
  * retrieval); the bound is the published Quest criterion.

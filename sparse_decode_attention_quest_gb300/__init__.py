@@ -19,7 +19,8 @@ from . import build as _build
 
 __all__ = [
     "SparseEngineError", "SEPagedKV", "paged_kv", "load_library", "se_read_device_error",
-    "se_quest_build_summaries", "se_quest_update_summaries", "se_quest_score_pages",
+    "se_quest_build_summaries", "se_quest_update_summaries", "se_quest_update_summaries_ex",
+    "APPEND_OVERLAP_PREVIOUS", "se_quest_score_pages",
     "se_quest_topk_pages", "se_quest_topk_pages_windowed", "se_quest_kept_pages_max",
     "se_quest_select_workspace_size", "se_quest_select_pages", "se_quest_select_pages_windowed",
     "se_quest_fused_step",
@@ -33,6 +34,7 @@ SE_OK = 0
 DEVERR_PAGE_RANGE = 0x1
 DEVERR_LENGTH = 0x2
 DEVERR_WAIT_TIMEOUT = 0x4
+APPEND_OVERLAP_PREVIOUS = 0x1  # se_quest_update_summaries_ex: may run alongside the previous kernel
 
 
 class SparseEngineError(RuntimeError):
@@ -62,6 +64,7 @@ _SIGNATURES = {
     "se_read_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "se_quest_build_summaries": (ctypes.c_int, [_KV, _P, _I, _P, _I, _I, _P]),
     "se_quest_update_summaries": (ctypes.c_int, [_KV, _P, _P, _P, _I, _P, _I, _P]),
+    "se_quest_update_summaries_ex": (ctypes.c_int, [_KV, _P, _P, _P, _I, _P, _I, ctypes.c_uint32, _P]),
     "se_quest_score_pages": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _P, _I, _P]),
     "se_quest_topk_pages": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I, _P]),
     "se_quest_topk_pages_windowed": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P]),
@@ -179,6 +182,16 @@ def se_quest_update_summaries(kv: SEPagedKV, k_new, v_new, block_table, seq_lens
                                          _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
                                          _ptr(seq_lens_before, torch.int32, "seq_lens_before"),
                                          seq_lens_before.shape[0], _stream(stream)))
+
+
+def se_quest_update_summaries_ex(kv: SEPagedKV, k_new, v_new, block_table, seq_lens_before, flags: int = 0,
+                                 stream=None):
+    lib = load_library()
+    _check(lib.se_quest_update_summaries_ex(ctypes.byref(kv), _ptr(k_new, torch.bfloat16, "k_new"),
+                                            _ptr(v_new, torch.bfloat16, "v_new"),
+                                            _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                            _ptr(seq_lens_before, torch.int32, "seq_lens_before"),
+                                            seq_lens_before.shape[0], int(flags), _stream(stream)))
 
 
 def se_quest_score_pages(kv: SEPagedKV, q, block_table, seq_lens, max_seq_len: int, scores, stream=None):

@@ -193,7 +193,15 @@ se_status_t se_quest_build_summaries(const se_paged_kv_t* kv, const int32_t* blo
 se_status_t se_quest_update_summaries(const se_paged_kv_t* kv, const void* k_new, const void* v_new,
                                       const int32_t* block_table, int32_t bt_stride,
                                       const int32_t* seq_lens_before, int32_t batch, void* stream) {
-  static const char* fn = "se_quest_update_summaries";
+  return se_quest_update_summaries_ex(kv, k_new, v_new, block_table, bt_stride, seq_lens_before, batch, 0u, stream);
+}
+
+se_status_t se_quest_update_summaries_ex(const se_paged_kv_t* kv, const void* k_new, const void* v_new,
+                                         const int32_t* block_table, int32_t bt_stride,
+                                         const int32_t* seq_lens_before, int32_t batch, uint32_t flags,
+                                         void* stream) {
+  static const char* fn = "se_quest_update_summaries_ex";
+  if (flags & ~(uint32_t)SE_APPEND_OVERLAP_PREVIOUS) return fail(SE_ERR_INVALID_ARG, fn, "unknown flags");
   se_status_t st = check_kv(fn, kv, false);  // summary NULL: the K/V rows only
   if (st != SE_OK) return st;
   if (batch < 0) return fail(SE_ERR_INVALID_ARG, fn, "batch < 0");
@@ -209,8 +217,8 @@ se_status_t se_quest_update_summaries(const se_paged_kv_t* kv, const void* k_new
   if (e != cudaSuccess) return cuda_fail(fn, e);
   e = se::launch_append_update(view_of(kv), static_cast<uint16_t*>(kv->k), static_cast<uint16_t*>(kv->v),
                                static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new),
-                               block_table, bt_stride, seq_lens_before, batch, d->err,
-                               static_cast<cudaStream_t>(stream));
+                               block_table, bt_stride, seq_lens_before, batch,
+                               (flags & SE_APPEND_OVERLAP_PREVIOUS) != 0, d->err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
 }
 

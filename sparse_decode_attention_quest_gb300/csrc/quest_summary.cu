@@ -64,6 +64,11 @@ __global__ void __launch_bounds__(kBuildWarps * 32) build_summaries_kernel(
   }
 }
 
+// kOverlap: the kernel may start while the previous kernel of the stream still
+// runs (programmatic dependent launch); it touches nothing that kernel reads or
+// writes, and waits for it only before it exits, so that the kernels after it
+// still see everything before it complete.
+template <bool kOverlap>
 __global__ void __launch_bounds__(256) append_update_kernel(KvView kv, uint16_t* __restrict__ k_mut,
                                                             uint16_t* __restrict__ v_mut,
                                                             const uint16_t* __restrict__ k_new,
@@ -72,48 +77,54 @@ __global__ void __launch_bounds__(256) append_update_kernel(KvView kv, uint16_t*
                                                             int32_t bt_stride,
                                                             const int32_t* __restrict__ seq_lens_before,
                                                             int32_t batch, unsigned* err) {
-  pdl_enter();
+  if (kOverlap)
+    pdl_launch_dependents();
+  else
+    pdl_enter();
   const int H = kv.num_kv_heads;
   const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (item >= batch * H) return;
   const int lane = threadIdx.x & 31;
-  const int b = item / H, h = item % H;
-  const int pos = seq_lens_before[b];
-  if (pos < 0 || pos / kPageSize >= bt_stride) {
-    if (lane == 0) raise_error(err, SE_DEVERR_LENGTH);
-    return;
-  }
-  const int page = pos / kPageSize, slot = pos % kPageSize;
-  const int phys = block_table[(size_t)b * bt_stride + page];
-  if (phys < 0 || phys >= kv.num_pages) {
-    if (lane == 0) raise_error(err, SE_DEVERR_PAGE_RANGE);
-    return;
-  }
-  const int D = kv.head_dim, Dv = kv.head_dim_v;
-  const size_t blk = (size_t)phys * H + h;
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(k_new + (size_t)item * D);
-  uint32_t* dst = reinterpret_cast<uint32_t*>(k_mut + (blk * kPageSize + slot) * kv.row_stride_k);
-  // A cache without Quest summaries (e.g. a SnapKV-compacted one) only gets the rows.
-  uint32_t* smin = kv.summary ? reinterpret_cast<uint32_t*>(kv.summary + blk * 2 * D) : nullptr;
-  uint32_t* smax = smin + (D >> 1);
-  for (int c = lane; c < (D >> 1); c += 32) {
-    const uint32_t x = src[c];
-    dst[c] = x;
-    if (smin == nullptr) continue;
-    if (slot == 0) {
-      smin[c] = x;
-      smax[c] = x;
-    } else {
-      const uint32_t a = smin[c], z = smax[c];
-      smin[c] = pack_bf16x2(fminf(bf16_lo(a), bf16_lo(x)), fminf(bf16_hi(a), bf16_hi(x)));
-      smax[c] = pack_bf16x2(fmaxf(bf16_lo(z), bf16_lo(x)), fmaxf(bf16_hi(z), bf16_hi(x)));
+  do {
+    if (item >= batch * H) break;
+    const int b = item / H, h = item % H;
+    const int pos = seq_lens_before[b];
+    if (pos < 0 || pos / kPageSize >= bt_stride) {
+      if (lane == 0) raise_error(err, SE_DEVERR_LENGTH);
+      break;
     }
-  }
-  if (v_new != nullptr) {
-    const uint32_t* vs = reinterpret_cast<const uint32_t*>(v_new + (size_t)item * Dv);
-    uint32_t* vd = reinterpret_cast<uint32_t*>(v_mut + (blk * kPageSize + slot) * kv.row_stride_v);
-    for (int c = lane; c < (Dv >> 1); c += 32) vd[c] = vs[c];
-  }
+    const int page = pos / kPageSize, slot = pos % kPageSize;
+    const int phys = block_table[(size_t)b * bt_stride + page];
+    if (phys < 0 || phys >= kv.num_pages) {
+      if (lane == 0) raise_error(err, SE_DEVERR_PAGE_RANGE);
+      break;
+    }
+    const int D = kv.head_dim, Dv = kv.head_dim_v;
+    const size_t blk = (size_t)phys * H + h;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(k_new + (size_t)item * D);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(k_mut + (blk * kPageSize + slot) * kv.row_stride_k);
+    // A cache without Quest summaries (e.g. a SnapKV-compacted one) only gets the rows.
+    uint32_t* smin = kv.summary ? reinterpret_cast<uint32_t*>(kv.summary + blk * 2 * D) : nullptr;
+    uint32_t* smax = smin + (D >> 1);
+    for (int c = lane; c < (D >> 1); c += 32) {
+      const uint32_t x = src[c];
+      dst[c] = x;
+      if (smin == nullptr) continue;
+      if (slot == 0) {
+        smin[c] = x;
+        smax[c] = x;
+      } else {
+        const uint32_t a = smin[c], z = smax[c];
+        smin[c] = pack_bf16x2(fminf(bf16_lo(a), bf16_lo(x)), fminf(bf16_hi(a), bf16_hi(x)));
+        smax[c] = pack_bf16x2(fmaxf(bf16_lo(z), bf16_lo(x)), fmaxf(bf16_hi(z), bf16_hi(x)));
+      }
+    }
+    if (v_new != nullptr) {
+      const uint32_t* vs = reinterpret_cast<const uint32_t*>(v_new + (size_t)item * Dv);
+      uint32_t* vd = reinterpret_cast<uint32_t*>(v_mut + (blk * kPageSize + slot) * kv.row_stride_v);
+      for (int c = lane; c < (Dv >> 1); c += 32) vd[c] = vs[c];
+    }
+  } while (false);
+  if (kOverlap) pdl_wait();  // every thread: the grid completes only after the previous one
 }
 
 }  // namespace
@@ -134,15 +145,17 @@ cudaError_t launch_build_summaries(const KvView& kv, const int32_t* block_table,
 
 cudaError_t launch_append_update(const KvView& kv, uint16_t* k_mut, uint16_t* v_mut, const uint16_t* k_new,
                                  const uint16_t* v_new, const int32_t* block_table, int32_t bt_stride,
-                                 const int32_t* seq_lens_before, int32_t batch, unsigned* err,
-                                 cudaStream_t stream) {
+                                 const int32_t* seq_lens_before, int32_t batch, bool overlap_previous,
+                                 unsigned* err, cudaStream_t stream) {
   const int items = batch * kv.num_kv_heads;
   if (items == 0) return cudaSuccess;
-  {
-    const cudaError_t le = launch_pdl(append_update_kernel, dim3((items + 7) / 8), dim3(256), 0, stream, kv, k_mut,
-                                      v_mut, k_new, v_new, block_table, bt_stride, seq_lens_before, batch, err);
-    if (le != cudaSuccess) return le;
-  }
+  const cudaError_t le =
+      overlap_previous
+          ? launch_pdl(append_update_kernel<true>, dim3((items + 7) / 8), dim3(256), 0, stream, kv, k_mut, v_mut,
+                       k_new, v_new, block_table, bt_stride, seq_lens_before, batch, err)
+          : launch_pdl(append_update_kernel<false>, dim3((items + 7) / 8), dim3(256), 0, stream, kv, k_mut, v_mut,
+                       k_new, v_new, block_table, bt_stride, seq_lens_before, batch, err);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

@@ -53,10 +53,12 @@ struct KvView {
 cudaError_t launch_build_summaries(const KvView& kv, const int32_t* block_table, int32_t bt_stride,
                                    const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, unsigned* err,
                                    cudaStream_t stream);
+// overlap_previous: the kernel may run alongside the previous kernel of the
+// stream (it must touch nothing that kernel reads or writes) and completes after it.
 cudaError_t launch_append_update(const KvView& kv, uint16_t* k_mut, uint16_t* v_mut, const uint16_t* k_new,
                                  const uint16_t* v_new, const int32_t* block_table, int32_t bt_stride,
-                                 const int32_t* seq_lens_before, int32_t batch, unsigned* err,
-                                 cudaStream_t stream);
+                                 const int32_t* seq_lens_before, int32_t batch, bool overlap_previous,
+                                 unsigned* err, cudaStream_t stream);
 
 // ---- quest_score.cu
 bool score_pages_supported(int num_kv_heads, int head_dim);

@@ -15,8 +15,9 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (paged_kv, se_quest_build_summaries, se_quest_fused_step, se_quest_kept_pages_max, se_quest_score_pages,
-               se_quest_topk_pages_windowed, se_quest_update_summaries, se_snapkv_score_and_compact_windowed,
+from . import (APPEND_OVERLAP_PREVIOUS, paged_kv, se_quest_build_summaries, se_quest_fused_step, se_quest_kept_pages_max,
+               se_quest_score_pages, se_quest_topk_pages_windowed, se_quest_update_summaries,
+               se_quest_update_summaries_ex, se_snapkv_score_and_compact_windowed,
                se_snapkv_workspace_size, se_sparse_decode_plan, se_sparse_decode_workspace_size,
                se_sparse_paged_decode)
 
@@ -66,8 +67,9 @@ class QuestDecodeStep:
     def build_summaries(self, seq_lens: torch.Tensor, stream=None):
         se_quest_build_summaries(self.kv, self.block_table, seq_lens, self.max_seq_len, stream)
 
-    def append(self, k_new, v_new, seq_lens_before, stream=None):
-        se_quest_update_summaries(self.kv, k_new, v_new, self.block_table, seq_lens_before, stream)
+    def append(self, k_new, v_new, seq_lens_before, stream=None, overlap_previous=False):
+        se_quest_update_summaries_ex(self.kv, k_new, v_new, self.block_table, seq_lens_before,
+                                     APPEND_OVERLAP_PREVIOUS if overlap_previous else 0, stream)
 
     def select(self, q, seq_lens, stream=None):
         se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, stream)
@@ -88,22 +90,33 @@ class QuestDecodeStep:
 
     def run(self, q, seq_lens, k_new=None, v_new=None, seq_lens_before=None, stream=None,
             events: Optional[Sequence] = None):
-        """Full step. ``events`` (4 CUDA events, optional) are recorded on ``stream`` before
-        the append, before scoring, before top-k and before decode, for per-kernel timing."""
+        """Full step. ``seq_lens``: lengths including the new token; with k_new/v_new the token
+        at ``seq_lens_before`` is appended.
+
+        Without ``events`` the kernels run score, top-k, append, decode: the token lands in its
+        request's last page, which is never scored (it is always kept), so the append may run
+        alongside the top-k (se_quest_update_summaries_ex, SE_APPEND_OVERLAP_PREVIOUS) and only
+        the decode waits for it. With ``events`` (4 CUDA events) they run append, score, top-k,
+        decode one after another, with the events recorded on ``stream`` before each, for
+        per-kernel timing."""
         s = stream if stream is not None else torch.cuda.current_stream()
-        if events is not None:
-            events[0].record(s)
+        if events is None:
+            se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, s)
+            se_quest_topk_pages_windowed(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sink,
+                                         self.recent, self.sel, self.counts, s)
+            if k_new is not None:
+                self.append(k_new, v_new, seq_lens_before, s, overlap_previous=True)
+            self.attend(q, seq_lens, stream=s)
+            return self.out
+        events[0].record(s)
         if k_new is not None:
             self.append(k_new, v_new, seq_lens_before, s)
-        if events is not None:
-            events[1].record(s)
+        events[1].record(s)
         se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, s)
-        if events is not None:
-            events[2].record(s)
+        events[2].record(s)
         se_quest_topk_pages_windowed(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sink,
                                      self.recent, self.sel, self.counts, s)
-        if events is not None:
-            events[3].record(s)
+        events[3].record(s)
         self.attend(q, seq_lens, stream=s)
         return self.out
 

@@ -146,3 +146,11 @@ def test_update_validation(se_lib):
 def test_failure_detail(se_lib):
     assert _build(_kv(page_size=8)) == INVALID
     assert b"page_size" in se_lib.se_last_error_detail()
+
+
+def test_update_ex_validation(se_lib):
+    f = se_lib.se_quest_update_summaries_ex
+    kv = _kv()
+    assert f(ctypes.byref(kv), FAKE, FAKE, FAKE, 64, FAKE, 2, 0x2, None) == INVALID   # unknown flag
+    assert b"flags" in se_lib.se_last_error_detail()
+    assert f(ctypes.byref(kv), FAKE, None, FAKE, 64, FAKE, 2, se.APPEND_OVERLAP_PREVIOUS, None) == INVALID  # v_new
