@@ -400,3 +400,42 @@ def test_topk_beyond_8192_candidates_uses_the_shared_memory_kernel(cuda_device):
     s[0, 0, ::7] = 0.5  # ties
     _topk_case(s, lens, 300, cuda_device)
     _topk_case(s, lens, 300, cuda_device, sink=100, recent=700)
+
+
+def test_overlapped_append_serial_order_and_graph_replay_agree(cuda_device):
+    """The step without events runs score, top-k, append (alongside the top-k), decode; with
+    events it runs append, score, top-k, decode; captured in a CUDA graph it runs the first
+    order under programmatic dependent launch. All three give the same selection, output
+    and lse, bit for bit (the append is idempotent, so they share one cache)."""
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=6, context_min=3000, context_max=9000, topk_pages=24, seed=83)
+    x, step, before, after = _prepare(wl, cuda_device)
+    dev = cuda_device
+    q, kn, vn = x.q.to(dev), x.k_new.to(dev), x.v_new.to(dev)
+    s = torch.cuda.Stream(dev)
+    results = []
+    with torch.cuda.stream(s):
+        step.run(q, after, kn, vn, before, stream=s)                      # overlapped
+    s.synchronize()
+    results.append((step.sel.clone(), step.counts.clone(), step.out.clone(), step.lse.clone()))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    with torch.cuda.stream(s):
+        step.run(q, after, kn, vn, before, stream=s, events=ev)           # serial
+    s.synchronize()
+    results.append((step.sel.clone(), step.counts.clone(), step.out.clone(), step.lse.clone()))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
+        step.run(q, after, kn, vn, before, stream=s)
+    for _ in range(3):
+        step.out.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    results.append((step.sel.clone(), step.counts.clone(), step.out.clone(), step.lse.clone()))
+    for r in results[1:]:
+        assert torch.equal(r[1], results[0][1])
+        for bh in range(wl.batch * wl.num_kv_heads):
+            n = int(r[1].view(-1)[bh])
+            assert torch.equal(r[0].view(wl.batch * wl.num_kv_heads, -1)[bh, :n],
+                               results[0][0].view(wl.batch * wl.num_kv_heads, -1)[bh, :n])
+        assert torch.equal(r[2], results[0][2])
+        assert torch.equal(r[3], results[0][3])
+    compare_decode(x, step, range(wl.batch), _scale(wl), "graph-replayed overlapped step")
