@@ -190,20 +190,35 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
         const int b = p / a.H, h = p % a.H;
         const int n = min(a.lens[b], a.max_len);
         const int npages = (n + kPageSize - 1) / kPageSize;
+        // Block-table entries of 4 tiles per window (lane l: page l % 8 of tile
+        // wb + l / 8); the next window is read 4 tiles before it is needed, so no
+        // tile waits on a table lookup.
+        const int32_t* bt_row = a.bt + (size_t)b * a.bt_stride;
+        auto load_window = [&](int wt) {
+          const int tt = wt + (lane >> 3), page = tt * kPagesPerTile + (lane & 7);
+          int ph = -1;
+          if (tt < t1 && page < npages) {
+            ph = bt_row[page];
+            if (ph < 0 || ph >= a.num_pages) {
+              raise_error(a.err, SE_DEVERR_PAGE_RANGE);
+              ph = -1;
+            }
+          }
+          return ph;
+        };
+        int wb = t0, win_cur = load_window(t0), win_nxt = load_window(t0 + 4);
         for (int t = t0; t < t1; ++t, ++it) {
           const int s = it % kStages;
+          if (t == wb + 4) {
+            wb += 4;
+            win_cur = win_nxt;
+            win_nxt = load_window(wb + 4);
+          }
+          int phys = __shfl_sync(0xffffffffu, win_cur, (t - wb) * kPagesPerTile + (lane & 7));
+          if (lane >= kPagesPerTile) phys = -1;
           if (it >= kStages && !dead && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1)) {
             if (lane == 0) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
             dead = true;
-          }
-          const int page = t * kPagesPerTile + lane;
-          int phys = -1;
-          if (lane < kPagesPerTile && page < npages) {
-            phys = a.bt[(size_t)b * a.bt_stride + page];
-            if (phys < 0 || phys >= a.num_pages) {
-              raise_error(a.err, SE_DEVERR_PAGE_RANGE);
-              phys = -1;
-            }
           }
           const unsigned live = __ballot_sync(0xffffffffu, phys >= 0);
           if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(live) * 2 * kPageSize * 128);
