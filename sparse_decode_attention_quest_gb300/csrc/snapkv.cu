@@ -237,48 +237,50 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
           if (!mbar_wait(&full[i % kStages], (i / kStages) & 1)) dead = true;
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = umma_idesc_bf16(128, kTileN);
-      int it = 0, acc_it = 0, seg = 0;
-      for (int p = p_first; p <= p_last; ++p, ++seg) {
-        const int t0 = max(start, prefix[p]) - prefix[p], t1 = min(end, prefix[p + 1]) - prefix[p];
-        if (t0 >= t1) {
-          --seg;
-          continue;
-        }
-        const int qb = seg & 1;
-        if (lane == 0 && !dead && !mbar_wait(&q_full[qb], (seg >> 1) & 1)) {
-          raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
-          dead = true;
-        }
-        dead = __shfl_sync(0xffffffffu, (int)dead, 0) != 0;
-        tc05_fence_after();
-        const uint32_t qaddr = smem_addr(smem + kQOff + qb * kTileBytes);
-        for (int t = t0; t < t1; ++t, ++it, ++acc_it) {
-          const int s = it % kStages, ab = acc_it & 1;
-          if (lane == 0 && !dead) {
-            if (!mbar_wait(&full[s], (it / kStages) & 1)) dead = true;
-            if (!dead && acc_it >= 2 && !mbar_wait(&acc_empty[ab], ((acc_it >> 1) - 1) & 1)) dead = true;
-            if (dead) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+      // Lane 0 alone: descriptors built once per Q buffer and stage, advanced by
+      // constant offsets ((bytes >> 4) in the address field, no carry: every
+      // shared address is below 256 KB).
+      if (lane == 0) {
+        const uint32_t idesc = umma_idesc_bf16(128, kTileN);
+        int it = 0, acc_it = 0, seg = 0;
+        // After a failed wait the loop goes on without MMAs but keeps committing,
+        // so that the other roles' waits still complete.
+        for (int p = p_first; p <= p_last; ++p) {
+          const int t0 = max(start, prefix[p]) - prefix[p], t1 = min(end, prefix[p + 1]) - prefix[p];
+          if (t0 >= t1) continue;
+          const int qb = seg & 1;
+          if (!dead && !mbar_wait(&q_full[qb], (seg >> 1) & 1)) {
+            raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+            dead = true;
           }
-          dead = __shfl_sync(0xffffffffu, (int)dead, 0) != 0;
           tc05_fence_after();
-          if (lane == 0) {
+          const uint64_t dq = umma_desc_sw128(smem_addr(smem + kQOff + qb * kTileBytes));
+          for (int t = t0; t < t1; ++t, ++it, ++acc_it) {
+            const int s = it % kStages, ab = acc_it & 1;
+            if (!dead && (!mbar_wait(&full[s], (it / kStages) & 1) ||
+                          (acc_it >= 2 && !mbar_wait(&acc_empty[ab], ((acc_it >> 1) - 1) & 1)))) {
+              raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+              dead = true;
+            }
+            tc05_fence_after();
             if (!dead) {
-              const uint32_t kaddr = smem_addr(smem + kRingOff + s * kTileBytes);
+              const uint64_t dk = umma_desc_sw128(smem_addr(smem + kRingOff + s * kTileBytes));
+              const uint32_t d = tmem + ab * kTileN;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                tc05_mma_bf16(tmem + ab * kTileN, umma_desc_sw128(qaddr + koff), umma_desc_sw128(kaddr + koff),
-                              idesc, kk > 0 ? 1u : 0u);
+                constexpr uint64_t kHalfDesc = kHalfBytes >> 4;
+                const uint64_t off = (uint64_t)(kk >> 2) * kHalfDesc + (uint64_t)(kk & 3) * 2;  // 32 bytes = 2
+                tc05_mma_bf16(d, dq + off, dk + off, idesc, kk > 0 ? 1u : 0u);
               }
             }
             tc05_commit(&empty[s]);
             tc05_commit(&acc_full[ab]);
             if (t == t1 - 1) tc05_commit(&q_empty[qb]);
           }
-          __syncwarp();
+          ++seg;
         }
       }
+      __syncwarp();
     } else {
       // ------------------------------------------------------------ epilogue
       const int wg = warp & 3;              // TMEM lane quarter of this warp
