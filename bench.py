@@ -6,7 +6,8 @@ Workload: the Qwen3-30B-A3B attention shape (32 query / 4 KV heads, head dim
 pages + the last page), one decode step per request that first appends the
 new token (KV write + summary update). bf16 cache, fp32 accumulation.
 
-One step = se_quest_score_pages + se_quest_topk_pages + se_quest_update_summaries_ex
+One step = se_quest_score_pages_ws (a kernel summing each request's queries, then the
+page scoring) + se_quest_topk_pages + se_quest_update_summaries_ex
 (the append, overlapping the top-k: the token lands in the always-kept last page) +
 se_sparse_paged_decode over the whole batch (one layer).
 Inputs are resident in HBM; L2 is flushed (a 2x L2-sized write, then a 2x L2 read) between

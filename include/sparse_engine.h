@@ -178,6 +178,33 @@ SE_API se_status_t se_quest_score_pages(const se_paged_kv_t* kv, const void* q, 
                                  void* stream);
 
 /*
+ * se_quest_score_workspace_size -- bytes of the workspace of
+ * se_quest_score_pages_ws: the group sums P_c and N_c of every request and KV
+ * head (fp32, batch * num_kv_heads * 2 * head_dim values). 0 for negative sizes.
+ */
+SE_API size_t se_quest_score_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * se_quest_score_pages_ws -- se_quest_score_pages with a workspace for the
+ * query multipliers. Same scores, bit for bit. A first kernel sums every
+ * request's queries into P_c and N_c once; the scoring kernel then reads them
+ * instead of summing the queries of each request in every CTA that scores part
+ * of it. That summing waits on the memory latency of the query loads while the
+ * summary reads keep HBM busy; with the workspace, a CTA's switch to another
+ * request costs one read of the sums. The largest gain is for the latent cache
+ * (64 query heads of 576 channels per request).
+ *   workspace: device memory the caller owns, 16-byte aligned, at least
+ *   se_quest_score_workspace_size(batch, kv->num_kv_heads, kv->head_dim) bytes
+ *   (SE_ERR_WORKSPACE when smaller, SE_ERR_INVALID_ARG when NULL or
+ *   misaligned); its contents on entry do not matter and are overwritten.
+ * The other arguments and errors are those of se_quest_score_pages.
+ */
+SE_API se_status_t se_quest_score_pages_ws(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                           const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                           int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * se_quest_topk_pages -- per-(request, KV head) page selection.
  * SparseEngine, Table 10 caption (selected budgets exclude separately kept
  * tokens) and Table 10, Quest (Vortex) row (2,048 selected tokens = 128 pages).

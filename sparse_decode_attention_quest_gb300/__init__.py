@@ -20,7 +20,7 @@ from . import build as _build
 __all__ = [
     "SparseEngineError", "SEPagedKV", "paged_kv", "load_library", "se_read_device_error",
     "se_quest_build_summaries", "se_quest_update_summaries", "se_quest_update_summaries_ex",
-    "APPEND_OVERLAP_PREVIOUS", "se_quest_score_pages",
+    "APPEND_OVERLAP_PREVIOUS", "se_quest_score_pages", "se_quest_score_workspace_size", "se_quest_score_pages_ws",
     "se_quest_topk_pages", "se_quest_topk_pages_windowed", "se_quest_kept_pages_max",
     "se_quest_select_workspace_size", "se_quest_select_pages", "se_quest_select_pages_windowed",
     "se_quest_fused_step",
@@ -66,6 +66,8 @@ _SIGNATURES = {
     "se_quest_update_summaries": (ctypes.c_int, [_KV, _P, _P, _P, _I, _P, _I, _P]),
     "se_quest_update_summaries_ex": (ctypes.c_int, [_KV, _P, _P, _P, _I, _P, _I, ctypes.c_uint32, _P]),
     "se_quest_score_pages": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _P, _I, _P]),
+    "se_quest_score_workspace_size": (_Z, [_I, _I, _I]),
+    "se_quest_score_pages_ws": (ctypes.c_int, [_KV, _P, _I, _P, _I, _P, _I, _I, _P, _I, _P, _Z, _P]),
     "se_quest_topk_pages": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I, _P]),
     "se_quest_topk_pages_windowed": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P]),
     "se_quest_kept_pages_max": (ctypes.c_longlong, [_I, _I, _I]),
@@ -200,6 +202,21 @@ def se_quest_score_pages(kv: SEPagedKV, q, block_table, seq_lens, max_seq_len: i
                                     _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
                                     _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0], int(max_seq_len),
                                     _ptr(scores, torch.float32, "scores"), scores.shape[-1], _stream(stream)))
+
+
+def se_quest_score_workspace_size(batch: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(load_library().se_quest_score_workspace_size(batch, num_kv_heads, head_dim))
+
+
+def se_quest_score_pages_ws(kv: SEPagedKV, q, block_table, seq_lens, max_seq_len: int, scores, workspace,
+                            stream=None):
+    lib = load_library()
+    _check(lib.se_quest_score_pages_ws(ctypes.byref(kv), _ptr(q, torch.bfloat16, "q"), q.shape[1],
+                                       _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                       _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0], int(max_seq_len),
+                                       _ptr(scores, torch.float32, "scores"), scores.shape[-1],
+                                       _ptr(workspace, torch.uint8, "workspace"),
+                                       0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
 def se_quest_topk_pages(scores, seq_lens, num_kv_heads: int, max_seq_len: int, topk_pages: int, out_pages,

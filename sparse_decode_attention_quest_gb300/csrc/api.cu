@@ -222,11 +222,13 @@ se_status_t se_quest_update_summaries_ex(const se_paged_kv_t* kv, const void* k_
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
 }
 
-se_status_t se_quest_score_pages(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
-                                 const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
-                                 int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
-                                 void* stream) {
-  static const char* fn = "se_quest_score_pages";
+namespace {
+
+// Shared body of se_quest_score_pages and se_quest_score_pages_ws (pn: the
+// multiplier workspace, or null).
+se_status_t score_pages_impl(const char* fn, const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                             const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens, int32_t batch,
+                             int32_t max_seq_len, float* scores, int32_t score_stride, float* pn, void* stream) {
   se_status_t st = check_kv(fn, kv, true);
   if (st != SE_OK) return st;
   st = check_batch_common(fn, block_table, bt_stride, seq_lens, batch, max_seq_len);
@@ -243,9 +245,39 @@ se_status_t se_quest_score_pages(const se_paged_kv_t* kv, const void* q, int32_t
   cudaError_t e = current_device(&d);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   e = se::launch_score_pages(view_of(kv), static_cast<const uint16_t*>(q), num_q_heads, block_table, bt_stride,
-                             seq_lens, batch, max_seq_len, scores, score_stride, d->sm_count, d->err,
+                             seq_lens, batch, max_seq_len, scores, score_stride, pn, d->sm_count, d->err,
                              static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+}  // namespace
+
+se_status_t se_quest_score_pages(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                 const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                 int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
+                                 void* stream) {
+  return score_pages_impl("se_quest_score_pages", kv, q, num_q_heads, block_table, bt_stride, seq_lens, batch,
+                          max_seq_len, scores, score_stride, nullptr, stream);
+}
+
+size_t se_quest_score_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t head_dim) {
+  if (batch < 0 || num_kv_heads < 0 || head_dim < 0) return 0;
+  return round16(se::score_pn_bytes(batch, num_kv_heads, head_dim));
+}
+
+se_status_t se_quest_score_pages_ws(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                                    const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                    int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  static const char* fn = "se_quest_score_pages_ws";
+  if (!kv) return fail(SE_ERR_INVALID_ARG, fn, "kv is NULL");
+  if (batch < 0) return fail(SE_ERR_INVALID_ARG, fn, "bad sizes");
+  const size_t need = se_quest_score_workspace_size(batch, kv->num_kv_heads, kv->head_dim);
+  if (workspace_bytes < need) return fail(SE_ERR_WORKSPACE, fn, "workspace too small");
+  if (need > 0 && !workspace) return fail(SE_ERR_INVALID_ARG, fn, "workspace NULL");
+  if (!aligned16(workspace)) return fail(SE_ERR_INVALID_ARG, fn, "workspace not 16-byte aligned");
+  return score_pages_impl(fn, kv, q, num_q_heads, block_table, bt_stride, seq_lens, batch, max_seq_len, scores,
+                          score_stride, need > 0 ? static_cast<float*>(workspace) : nullptr, stream);
 }
 
 se_status_t se_quest_topk_pages_windowed(const float* scores, int32_t score_stride, const int32_t* seq_lens,

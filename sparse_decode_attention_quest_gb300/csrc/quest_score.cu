@@ -29,6 +29,14 @@
 // every warp through its own ring reach close to the copy bandwidth; loads
 // batched into registers do not, because a warp drains its batch before it
 // issues the next one.
+//
+// With a workspace (se_quest_score_pages_ws) pn_kernel first writes P and N of
+// every request, and the scoring kernel reads them (an L2 hit) instead of
+// reducing the group's queries in every CTA that scores part of a request.
+// That in-CTA reduction waits on query loads that queue behind the summary
+// reads of the other CTAs: measured on GB300, 12.7 us at the start of the
+// latent kernel (64 query heads x 576 channels per request) and 15 us again in
+// the CTAs whose slice reaches a second request, which then finish last.
 #include "se_ptx.cuh"
 
 namespace se {
@@ -48,6 +56,7 @@ struct ScoreArgs {
   int32_t max_seq_len;
   float* scores;
   int32_t score_stride;
+  const float* pn_pre;  // P and N per request, [batch][H][2][D], from pn_kernel (or null)
   unsigned* err;
 };
 
@@ -133,13 +142,16 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 // Lanes per (KV head, 8 channels) item in the P/N pre-reduction: the group's
 // query heads are cut into S runs summed by S adjacent lanes.
-__device__ __forceinline__ int pn_lanes(int group) { return group >= 8 ? 8 : group >= 4 ? 4 : group >= 2 ? 2 : 1; }
+__host__ __device__ __forceinline__ int pn_lanes(int group) { return group >= 8 ? 8 : group >= 4 ? 4 : group >= 2 ? 2 : 1; }
 
 // D: head dim; T: 16-byte chunks per lane per page block (= KV heads at d 128);
 // R: ring stages per warp.
 // For D = 128 chunk t of every lane belongs to KV head t; for the latent cache
 // (D = 576, one KV head) every chunk belongs to the one head.
-template <int D, int T, int R>
+// kPre: the multipliers of every request were written by pn_kernel before
+// this kernel; a segment reads them from global memory (an L2 hit) instead of
+// reducing the group's queries itself, and no CTA barrier is needed.
+template <int D, int T, int R, bool kPre>
 __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArgs a) {
   pdl_enter();
   // Page i + R - 1 is looked up while page i is consumed, inside the two
@@ -153,8 +165,8 @@ __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArg
   const int H = a.kv.num_kv_heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + (size_t)warp * R * kBlk;                            // [warp][R][kBlk]
-  float* pn = reinterpret_cast<float*>(smem + (size_t)kWarps * R * kBlk);    // [2][H][2][D]
-  int* prefix = reinterpret_cast<int*>(pn + 2 * H * 2 * D);                 // [batch + 1]
+  float* pn = reinterpret_cast<float*>(smem + (size_t)kWarps * R * kBlk);    // [2][H][2][D] (not with kPre)
+  int* prefix = reinterpret_cast<int*>(pn + (kPre ? 0 : 2 * H * 2 * D));   // [batch + 1]
   const uint32_t ring_addr = smem_addr(ring);
 
   // Candidate pages per request, then an exclusive prefix (one warp, chunked).
@@ -232,13 +244,18 @@ __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArg
       cp_async_commit();
     }
 
-    // ---- P and N of request b into buffer seg & 1. Each (KV head, 8 channels)
-    // item is summed by S adjacent lanes over S runs of the group's query heads
-    // and the runs are added with a fixed butterfly (the result does not depend
-    // on timing). The other buffer may still be read by nobody: each lane copies
-    // its multipliers into registers right after the barrier below.
-    float* buf = pn + (seg & 1) * H * 2 * D;
-    {
+    // ---- P and N of request b: precomputed (kPre), or reduced here into
+    // buffer seg & 1. Each (KV head, 8 channels) item is summed by S adjacent
+    // lanes over S runs of the group's query heads and the runs are added with
+    // a fixed butterfly (the result does not depend on timing). The other
+    // buffer may still be read by nobody: each lane copies its multipliers
+    // into registers right after the barrier below.
+    const float* buf;
+    if (kPre) {
+      buf = a.pn_pre + (size_t)b * H * 2 * D;
+    } else {
+      float* wbuf = pn + (seg & 1) * H * 2 * D;
+      buf = wbuf;
       const uint16_t* qb = a.q + (size_t)b * H * a.group * D;
       const int S = pn_lanes(a.group);
       const int tasks = H * (D / 8) * S;
@@ -273,13 +290,13 @@ __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArg
         if (live && sl == 0) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            buf[(h * 2 + 0) * D + c0 + e] = N[e];  // multiplies the min row
-            buf[(h * 2 + 1) * D + c0 + e] = P[e];  // multiplies the max row
+            wbuf[(h * 2 + 0) * D + c0 + e] = N[e];  // multiplies the min row
+            wbuf[(h * 2 + 1) * D + c0 + e] = P[e];  // multiplies the max row
           }
         }
       }
+      __syncthreads();
     }
-    __syncthreads();
     // A fragments of the m16n8k16 MMA: row n < 8 holds the high parts and row
     // n + 8 the low parts of the multipliers of channels chan(k, n); k-step s
     // of head h covers the head's channels 128 s .. 128 s + 127.
@@ -358,23 +375,96 @@ __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArg
   }
 }
 
-template <int D, int T, int R>
-cudaError_t launch_t(const ScoreArgs& a, int sm_count, cudaStream_t stream) {
+constexpr int kPnThreads = 640;  // up to 640 tasks in one round (d 128 with 5 KV heads; the latent 576)
+
+// P and N of every request into pn_out [batch][H][2][D]: one CTA per request,
+// the same tasks, lanes and summation order as the pre-reduction inside
+// score_pages_kernel, so both give bit-identical multipliers. All loads of a
+// task's run are issued before the first is summed.
+template <int D>
+__global__ void __launch_bounds__(kPnThreads) pn_kernel(const uint16_t* __restrict__ q, int32_t H, int32_t group,
+                                                  float* __restrict__ pn_out) {
+  pdl_enter();
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int S = pn_lanes(group);
+  const int tasks = H * (D / 8) * S;
+  const uint16_t* qb = q + (size_t)b * H * group * D;
+  float* dst = pn_out + (size_t)b * H * 2 * D;
+  for (int t0 = threadIdx.x - lane; t0 < tasks; t0 += blockDim.x) {  // warp-uniform
+    const int task = t0 + lane;
+    const bool live = task < tasks;
+    const int it = task / S, sl = task % S;
+    const int h = it / (D / 8), c0 = (it % (D / 8)) * 8;
+    float P[8], N[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) P[e] = N[e] = 0.f;
+    if (live) {
+      const int g0 = sl * group / S, g1 = (sl + 1) * group / S;
+      const uint16_t* qh = qb + (size_t)h * group * D + c0;
+      for (int g = g0; g < g1; g += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (g + u < g1) v[u] = *reinterpret_cast<const uint4*>(qh + (size_t)(g + u) * D);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (g + u < g1) add_pos_neg(v[u], P, N);
+      }
+    }
+    for (int o = 1; o < S; o <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        P[e] += __shfl_xor_sync(0xffffffffu, P[e], o);
+        N[e] += __shfl_xor_sync(0xffffffffu, N[e], o);
+      }
+    }
+    if (live && sl == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        dst[(h * 2 + 0) * D + c0 + e] = N[e];
+        dst[(h * 2 + 1) * D + c0 + e] = P[e];
+      }
+    }
+  }
+}
+
+template <int D, int T, int R, bool kPre>
+cudaError_t launch_score(const ScoreArgs& a, int sm_count, cudaStream_t stream) {
   const int H = a.kv.num_kv_heads;
   constexpr int kBlk = D == 128 ? T * 512 : 2 * D * 2;
-  const size_t smem = (size_t)kWarps * R * kBlk + (size_t)2 * H * 2 * D * 4 + (size_t)(a.batch + 1) * 4;
-  cudaError_t e = cudaFuncSetAttribute(score_pages_kernel<D, T, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  const size_t smem =
+      (size_t)kWarps * R * kBlk + (kPre ? 0 : (size_t)2 * H * 2 * D * 4) + (size_t)(a.batch + 1) * 4;
+  cudaError_t e = cudaFuncSetAttribute(score_pages_kernel<D, T, R, kPre>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   {
-    const cudaError_t le = launch_pdl(score_pages_kernel<D, T, R>, dim3(sm_count * 2), dim3(kThreads), smem, stream,
-                                      a);
+    const cudaError_t le = launch_pdl(score_pages_kernel<D, T, R, kPre>, dim3(sm_count * 2), dim3(kThreads), smem,
+                                      stream, a);
     if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();
 }
 
+template <int D, int T, int R>
+cudaError_t launch_t(const ScoreArgs& a, int sm_count, cudaStream_t stream) {
+  if (!a.pn_pre) return launch_score<D, T, R, false>(a, sm_count, stream);
+  const int H = a.kv.num_kv_heads;
+  const int tasks = H * (D / 8) * pn_lanes(a.group);
+  const int threads = min(kPnThreads, (tasks + 31) / 32 * 32);
+  {
+    const cudaError_t le = launch_pdl(pn_kernel<D>, dim3(a.batch), dim3(threads), 0, stream, a.q, H, a.group,
+                                      const_cast<float*>(a.pn_pre));
+    if (le != cudaSuccess) return le;
+  }
+  return launch_score<D, T, R, true>(a, sm_count, stream);
+}
+
 }  // namespace
+
+size_t score_pn_bytes(int32_t batch, int32_t num_kv_heads, int32_t head_dim) {
+  return (size_t)batch * num_kv_heads * 2 * head_dim * sizeof(float);
+}
 
 bool score_pages_supported(int num_kv_heads, int head_dim) {
   return (head_dim == 128 && num_kv_heads >= 1 && num_kv_heads <= 8) || (head_dim == 576 && num_kv_heads == 1);
@@ -383,7 +473,7 @@ bool score_pages_supported(int num_kv_heads, int head_dim) {
 cudaError_t launch_score_pages(const KvView& kv, const uint16_t* q, int32_t num_q_heads,
                                const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
                                int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
-                               int sm_count, unsigned* err, cudaStream_t stream) {
+                               float* pn_ws, int sm_count, unsigned* err, cudaStream_t stream) {
   const int max_cand = (max_seq_len + kPageSize - 1) / kPageSize - 1;
   if (batch == 0 || max_cand <= 0) return cudaSuccess;
   ScoreArgs a;
@@ -397,6 +487,7 @@ cudaError_t launch_score_pages(const KvView& kv, const uint16_t* q, int32_t num_
   a.max_seq_len = max_seq_len;
   a.scores = scores;
   a.score_stride = score_stride;
+  a.pn_pre = pn_ws;
   a.err = err;
   // Ring depth per head count: about 96 KB of summary blocks in flight per CTA,
   // two CTAs per SM.

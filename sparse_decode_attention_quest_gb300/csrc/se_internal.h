@@ -62,10 +62,15 @@ cudaError_t launch_append_update(const KvView& kv, uint16_t* k_mut, uint16_t* v_
 
 // ---- quest_score.cu
 bool score_pages_supported(int num_kv_heads, int head_dim);
+// Bytes of the per-request multipliers (P and N) that pn_ws holds.
+size_t score_pn_bytes(int32_t batch, int32_t num_kv_heads, int32_t head_dim);
+// pn_ws (score_pn_bytes, 16-byte aligned) or null: with it, a first kernel
+// reduces every request's queries once and the scoring kernel reads the result;
+// without it, every CTA reduces the queries of the requests it scores.
 cudaError_t launch_score_pages(const KvView& kv, const uint16_t* q, int32_t num_q_heads,
                                const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
                                int32_t batch, int32_t max_seq_len, float* scores, int32_t score_stride,
-                               int sm_count, unsigned* err, cudaStream_t stream);
+                               float* pn_ws, int sm_count, unsigned* err, cudaStream_t stream);
 // ---- quest_topk.cu
 // Top-k of the candidate pages: those holding none of the first sink_tokens and
 // none of the last recent_tokens tokens (the last page always kept); the kept

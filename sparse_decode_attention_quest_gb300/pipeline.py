@@ -3,7 +3,8 @@
 Host orchestration only (allocation and call order); the work runs in the
 library's kernels:
     se_quest_update_summaries   (optional KV append fused with the summary update)
-    se_quest_score_pages        (upper-bound score of every candidate page)
+    se_quest_score_pages_ws     (upper-bound score of every candidate page; the group's query
+                                 sums computed once per request into a workspace)
     se_quest_topk_pages_windowed (top-k pages + the sink/recent windows + the last page, ascending)
     se_sparse_paged_decode      (split-K flash-decode over the selected pages + merge)
 or all four in one launch (se_quest_fused_step, run_fused).
@@ -16,7 +17,8 @@ from typing import Optional, Sequence
 import torch
 
 from . import (APPEND_OVERLAP_PREVIOUS, paged_kv, se_quest_build_summaries, se_quest_fused_step, se_quest_kept_pages_max,
-               se_quest_score_pages, se_quest_topk_pages_windowed, se_quest_update_summaries,
+               se_quest_score_pages, se_quest_score_pages_ws, se_quest_score_workspace_size,
+               se_quest_topk_pages_windowed, se_quest_update_summaries,
                se_quest_update_summaries_ex, se_snapkv_score_and_compact_windowed,
                se_snapkv_workspace_size, se_sparse_decode_plan, se_sparse_decode_workspace_size,
                se_sparse_paged_decode)
@@ -34,7 +36,10 @@ class QuestDecodeStep:
     def __init__(self, k_cache: torch.Tensor, v_cache: Optional[torch.Tensor], summary: torch.Tensor,
                  block_table: torch.Tensor, num_q_heads: int, topk_pages: int, max_seq_len: int,
                  head_dim_v: Optional[int] = None, sm_scale: Optional[float] = None, sel_stride: Optional[int] = None,
-                 sink_tokens: int = 0, recent_tokens: int = 0):
+                 sink_tokens: int = 0, recent_tokens: int = 0, score_workspace: bool = True):
+        """score_workspace: score through se_quest_score_pages_ws (the query sums of every
+        request computed once, in a workspace of batch x KV heads x 2 x head_dim floats)
+        rather than se_quest_score_pages; both give the same scores."""
         self.k_cache, self.v_cache, self.summary = k_cache, v_cache, summary
         self.block_table = block_table
         self.kv = paged_kv(k_cache, v_cache, summary, head_dim_v)
@@ -58,11 +63,15 @@ class QuestDecodeStep:
         self.lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=dev)
         ws = se_sparse_decode_workspace_size(self.B, self.Hq, self.H, self.Dv, self.sel_stride)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.score_ws = None
+        if score_workspace:
+            sws = se_quest_score_workspace_size(self.B, self.H, self.D)
+            self.score_ws = torch.empty(max(sws, 16), dtype=torch.uint8, device=dev)
 
     def launches_per_step(self, append: bool = True) -> int:
-        """Kernels one run() launches: append, score, top-k, decode (+ split merge)."""
+        """Kernels one run() launches: append, (query sums,) score, top-k, decode (+ split merge)."""
         _, _, dec = se_sparse_decode_plan(self.B, self.Hq, self.H, self.D, self.Dv, self.sel_stride)
-        return (1 if append else 0) + 2 + dec
+        return (1 if append else 0) + (3 if self.score_ws is not None else 2) + dec
 
     def build_summaries(self, seq_lens: torch.Tensor, stream=None):
         se_quest_build_summaries(self.kv, self.block_table, seq_lens, self.max_seq_len, stream)
@@ -71,8 +80,15 @@ class QuestDecodeStep:
         se_quest_update_summaries_ex(self.kv, k_new, v_new, self.block_table, seq_lens_before,
                                      APPEND_OVERLAP_PREVIOUS if overlap_previous else 0, stream)
 
+    def score(self, q, seq_lens, stream=None):
+        if self.score_ws is not None:
+            se_quest_score_pages_ws(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores,
+                                    self.score_ws, stream)
+        else:
+            se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, stream)
+
     def select(self, q, seq_lens, stream=None):
-        se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, stream)
+        self.score(q, seq_lens, stream)
         se_quest_topk_pages_windowed(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sink,
                                      self.recent, self.sel, self.counts, stream)
 
@@ -101,7 +117,7 @@ class QuestDecodeStep:
         per-kernel timing."""
         s = stream if stream is not None else torch.cuda.current_stream()
         if events is None:
-            se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, s)
+            self.score(q, seq_lens, s)
             se_quest_topk_pages_windowed(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sink,
                                          self.recent, self.sel, self.counts, s)
             if k_new is not None:
@@ -112,7 +128,7 @@ class QuestDecodeStep:
         if k_new is not None:
             self.append(k_new, v_new, seq_lens_before, s)
         events[1].record(s)
-        se_quest_score_pages(self.kv, q, self.block_table, seq_lens, self.max_seq_len, self.scores, s)
+        self.score(q, seq_lens, s)
         events[2].record(s)
         se_quest_topk_pages_windowed(self.scores, seq_lens, self.H, self.max_seq_len, self.topk, self.sink,
                                      self.recent, self.sel, self.counts, s)

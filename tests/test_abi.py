@@ -88,6 +88,23 @@ def test_score_validation(se_lib):
     assert f(ctypes.byref(big), FAKE, 32, FAKE, 64, FAKE, 2, 1000, FAKE, 63, None) == UNSUPPORTED
 
 
+def test_score_workspace_validation(se_lib):
+    # the group sums P and N: batch x KV heads x 2 x head_dim floats
+    assert se_lib.se_quest_score_workspace_size(2, 4, 128) == 2 * 4 * 2 * 128 * 4
+    assert se_lib.se_quest_score_workspace_size(64, 1, 576) == 64 * 2 * 576 * 4
+    assert se_lib.se_quest_score_workspace_size(-1, 4, 128) == 0
+    f = se_lib.se_quest_score_pages_ws
+    kv = _kv()
+    need = se_lib.se_quest_score_workspace_size(2, 4, 128)
+    args = lambda ws=FAKE, n=need, hq=32: (ctypes.byref(kv), FAKE, hq, FAKE, 64, FAKE, 2, 1000, FAKE, 63, ws, n,
+                                           None)
+    assert f(*args(n=need - 1)) == WORKSPACE
+    assert f(*args(ws=None)) == INVALID
+    assert f(*args(ws=FAKE + 4)) == INVALID                 # misaligned
+    assert f(*args(hq=30)) == INVALID                       # the checks of se_quest_score_pages follow
+    assert f(None, FAKE, 32, FAKE, 64, FAKE, 2, 1000, FAKE, 63, FAKE, need, None) == INVALID
+
+
 def test_topk_validation(se_lib):
     f = se_lib.se_quest_topk_pages
     assert f(FAKE, 63, FAKE, 2, 4, 1000, 0, FAKE, FAKE, 8, None) == INVALID        # k = 0

@@ -159,6 +159,45 @@ def test_score_is_an_upper_bound_of_the_group_logit(cuda_device):
                 assert float(scores[r, h, p]) >= true_max - 1e-3 * max(1.0, abs(true_max)), (r, h, p)
 
 
+def _scores_both_ways(wl, dev):
+    """Scores of one workload through se_quest_score_pages and se_quest_score_pages_ws."""
+    x, step, b, a = _prepare(wl, dev)
+    q = x.q.to(dev)
+    plain = torch.full_like(step.scores, float("nan"))
+    pre = torch.full_like(step.scores, float("nan"))
+    se.se_quest_score_pages(step.kv, q, step.block_table, a, step.max_seq_len, plain)
+    ws = torch.empty(se.se_quest_score_workspace_size(wl.batch, wl.num_kv_heads, wl.head_dim), dtype=torch.uint8,
+                     device=dev)
+    se.se_quest_score_pages_ws(step.kv, q, step.block_table, a, step.max_seq_len, pre, ws)
+    torch.cuda.synchronize()
+    return x, plain.cpu(), pre.cpu()
+
+
+def _check_same_scores(x, plain, pre):
+    for r, n in enumerate(x.pages_per_request):
+        got, ref = pre[r, :, :max(n - 1, 0)], plain[r, :, :max(n - 1, 0)]
+        assert torch.isfinite(ref).all(), r
+        assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), r
+
+
+@pytest.mark.parametrize("kv_heads,group", [(1, 4), (2, 8), (3, 2), (4, 8), (5, 1), (6, 3), (7, 16), (8, 4)])
+def test_score_workspace_gives_the_same_scores(cuda_device, kv_heads, group):
+    # every KV-head count of the d-128 kernel; ragged lengths over several CTA slices
+    wl = QWEN3_4B_QUEST_32K.scaled(batch=5, num_kv_heads=kv_heads, num_q_heads=kv_heads * group,
+                                   context_min=700, context_max=5000, seed=60 + kv_heads)
+    _check_same_scores(*_scores_both_ways(wl, cuda_device))
+
+
+def test_score_workspace_latent_and_many_requests_per_slice(cuda_device):
+    # the latent cache (64 query heads of 576 channels); then 1,200 short requests, so that
+    # every CTA slice crosses several requests and reads several requests' sums
+    wl = MLA_GLM_QUEST_32K.scaled(batch=6, context_min=900, context_max=9000, topk_pages=12, seed=71)
+    _check_same_scores(*_scores_both_ways(wl, cuda_device))
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=1200, context_min=17, context_max=120, topk_pages=2,
+                                         append=False, seed=72)
+    _check_same_scores(*_scores_both_ways(wl, cuda_device))
+
+
 def test_select_all_equals_dense(cuda_device):
     wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=3, context_min=300, context_max=1000, topk_pages=80,
                                          append=False, seed=17)
