@@ -94,8 +94,25 @@ __device__ __forceinline__ void find_digit(const int* hist, int remaining, int l
 constexpr int kBuckets = 1024;
 constexpr int kMaxMembers = 1024;
 
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sums over the per-warp values wtot[0..31] (one per warp of the block, in
+// shared memory): lane l of every warp reads wtot[l] and the warp adds them up
+// with shuffles, instead of every thread reading all 32. Returns the sum over
+// the warps before `warp`; `total` gets the sum over all of them.
+__device__ __forceinline__ int warps_before(const int* wtot, int warp, int lane, int& total) {
+  const int x = wtot[lane];
+  total = warp_sum(x);
+  return warp_sum(lane < warp ? x : 0);
+}
+
 // Block-wide exclusive prefix of one int per thread, in thread order (two barriers).
 __device__ __forceinline__ int block_exclusive_scan(int v, int* wtot, int warp, int lane, int& total) {
+  static_assert(kTopkWarps == 32, "one warp total per lane");
   int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -104,13 +121,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* wtot, int warp, 
   }
   if (lane == 31) wtot[warp] = incl;
   __syncthreads();
-  int before = incl - v;
-  total = 0;
-  for (int w = 0; w < kTopkWarps; ++w) {
-    const int x = wtot[w];
-    before += (w < warp) ? x : 0;
-    total += x;
-  }
+  const int before = incl - v + warps_before(wtot, warp, lane, total);
   __syncthreads();
   return before;
 }
@@ -177,10 +188,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
   if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
   if (tid == 0) s_info[2] = 0;
   __syncthreads();
-  float mn = INFINITY, mx = -INFINITY;
-  for (int w = 0; w < kTopkWarps; ++w) {
-    mn = fminf(mn, s_min[w]);
-    mx = fmaxf(mx, s_max[w]);
+  float mn = s_min[lane], mx = s_max[lane];  // min and max over the warps, by shuffles
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
   const float scale = (mx > mn) ? (float)kBuckets / (mx - mn) : 0.f;
   int bk[kKeysPerThread];
@@ -203,7 +215,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
   }
   if (lane == 0) wtot[warp] = incl;
   __syncthreads();
-  for (int w = warp + 1; w < kTopkWarps; ++w) incl += wtot[w];
+  {
+    const int x = wtot[lane];
+    incl += warp_sum(lane > warp ? x : 0);  // keys in the buckets of the warps above
+  }
   if (incl - hc < k && k <= incl) {
     s_info[0] = tid;
     s_info[1] = incl - hc;
@@ -391,24 +406,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_smem_kernel(
     const unsigned beq = __ballot_sync(0xffffffffu, eq);
     if (lane == 0) warp_tot[warp] = __popc(beq);
     __syncthreads();
-    int eq_before = 0, eq_total = 0;
-    for (int w = 0; w < kTopkWarps; ++w) {
-      const int v = warp_tot[w];
-      eq_before += (w < warp) ? v : 0;
-      eq_total += v;
-    }
+    int eq_total;
+    const int eq_before = warps_before(warp_tot, warp, lane, eq_total);
     __syncthreads();
     const int eq_rank = eq_seen + eq_before + __popc(beq & lt_mask);
     const bool sel = gt || (eq && eq_rank < need_eq);
     const unsigned bsel = __ballot_sync(0xffffffffu, sel);
     if (lane == 0) warp_tot[warp] = __popc(bsel);
     __syncthreads();
-    int sel_before = 0, sel_total = 0;
-    for (int w = 0; w < kTopkWarps; ++w) {
-      const int v = warp_tot[w];
-      sel_before += (w < warp) ? v : 0;
-      sel_total += v;
-    }
+    int sel_total;
+    const int sel_before = warps_before(warp_tot, warp, lane, sel_total);
     const int pos = base_out + sel_before + __popc(bsel & lt_mask);
     if (sel && pos < k) out[c0 + pos] = c0 + i;
     base_out += sel_total;
