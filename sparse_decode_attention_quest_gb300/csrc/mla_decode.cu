@@ -63,7 +63,7 @@ constexpr float kRescaleLog2 = 8.f;                     // running max moves whe
 constexpr uint32_t kSoftBar = 1;                        // named barrier of the softmax warps
 
 // Shared memory after the Q buffer.
-constexpr int kBarOff = 0;        // 31 mbarriers
+constexpr int kBarOff = 0;        // 32 mbarriers
 constexpr int kTmemSlotOff = 256;
 constexpr int kValidOff = 272;    // [2 stages][4 pages] valid rows
 constexpr int kXmaxOff = 512;     // [2 tile parities][4 pages][64 heads] tile maxima
@@ -189,6 +189,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
   uint64_t* q_full = bars + 28;   // the request's queries landed
   uint64_t* q_empty = bars + 29;  // the last S^T MMA of a request's segment is done
   uint64_t* fin = bars + 30;      // every MMA of the CTA is done (both issuers)
+  // The PV MMAs of a segment's last tile are done (one phase per segment).
+  // The epilogue cannot wait for that on o_done: the softmax threads do not
+  // wait for every tile's PV, so when they finish the last tile j, o_done may
+  // still be in phase j - 1; a parity wait may only name the current or the
+  // preceding phase, and phase j has the parity of the completed phase j - 2.
+  uint64_t* o_last = bars + 31;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + kTmemSlotOff);
   int* tile_valid = reinterpret_cast<int*>(misc + kValidOff);
   float* xmax = reinterpret_cast<float*>(misc + kXmaxOff);
@@ -253,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(fin, 2);
+    mbar_init(o_last, 1);
     mbar_fence_init();
   }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
@@ -441,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
         }
         tc05_commit(&empty[s]);
         tc05_commit(o_done);
+        if (c.last()) tc05_commit(o_last);
       }
       if (dead) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
       tc05_commit(fin);
@@ -580,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
       if (c.last()) {
         // ---- epilogue of the segment: O = O^T / l per head, or a partial
         const int b = c.item;
-        const bool ok_e = __all_sync(0xffffffffu, mbar_wait(o_done, j & 1));
+        const bool ok_e = __all_sync(0xffffffffu, mbar_wait(o_last, c.seg & 1));
         dead = dead || !ok_e;
         float w[16];
 #pragma unroll

@@ -126,6 +126,25 @@ def test_full_mla_glm_32k_sampled(cuda_device):
     compare_decode(x, step, [0, 31, wl.batch - 1], _scale(wl), "mla-glm full")
 
 
+def test_latent_decode_is_repeatable(cuda_device):
+    """The full 64 x 32K decode run again and again gives bit-identical outputs and
+    log-sum-exps. A decode pipeline whose epilogue read the output accumulators before
+    the last tiles' PV MMAs had landed gave a request output that changed from one run
+    to the next (with the exact log-sum-exp, and within the output tolerance)."""
+    wl = MLA_GLM_QUEST_32K
+    x, step, lens = _prepare(wl, cuda_device, device_gen=True)
+    q = x.q.to(cuda_device)
+    step.select(q, lens)
+    step.attend(q, lens)
+    torch.cuda.synchronize()
+    out0, lse0 = step.out.clone(), step.lse.clone()
+    for _ in range(12):
+        step.attend(q, lens)
+        torch.cuda.synchronize()
+        assert torch.equal(step.out.view(torch.int16), out0.view(torch.int16))
+        assert torch.equal(step.lse, lse0)
+
+
 def test_latent_growing_scores_rescale_every_tile(cuda_device):
     """Scores that grow by more than 2^8 (log2 units) from one 4-page tile to the
     next, so that the decode's running maxima move on every tile and the output
