@@ -186,6 +186,19 @@ def test_snapkv_full_32k_sampled(cuda_device):
         _check_pair(xc, res, b, h)
 
 
+def test_snapkv_is_repeatable(cuda_device):
+    # the full 4 x 32K eviction (tcgen05 score passes, selection, gather) run again gives
+    # bit-identical scores, row log-sum-exps, kept positions and compacted rows
+    x = make_snapkv_inputs(SNAPKV_PREFILL_32K, device=cuda_device)
+    first = _run(x, cuda_device)
+    for _ in range(4):
+        again = _run(x, cuda_device)
+        for key in ("scores", "lse", "kept", "cnt"):
+            assert torch.equal(first[key].view(torch.int32), again[key].view(torch.int32)), key
+        for key in ("dk", "dv"):
+            assert torch.equal(first[key].view(torch.int16), again[key].view(torch.int16)), key
+
+
 # ---------------------------------------------------------------- keep windows (sink / recent)
 @pytest.mark.parametrize("W,S,R,keep", [(16, 16, 64, 96), (32, 64, 512, 300), (32, 0, 256, 200), (32, 64, 32, 100)])
 def test_snapkv_windows_oracle_sized(cuda_device, W, S, R, keep):
