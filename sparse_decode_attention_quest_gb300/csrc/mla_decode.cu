@@ -652,8 +652,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Merge of the partials of requests spread over several CTAs (one warp per
-// row); rows of requests with no selected page get 0 and lse = -inf.
+// Merge the partials of the items spread over several CTAs; one warp per
+// (request, query head) row. The log-sum-exps of up to 32 splits come in one
+// round trip (lane s reads split s); the partial outputs are read split by
+// split, the 4 column chunks of a lane and two splits at a time in flight, and
+// added in split order. Items held by one CTA were written directly; rows of
+// requests with no selected page get 0 and lse = -inf.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restrict__ o_part,
                                                           const float* __restrict__ lse_part,
                                                           const int32_t* __restrict__ item_ns, int32_t batch,
@@ -666,27 +670,47 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
   const int ns = min(item_ns[row / Hq], max_splits);
   if (ns == 1) return;
   const float* lp = lse_part + (size_t)row * max_splits;
+  const float* op = o_part + (size_t)row * max_splits * kDv + lane * 4;
   float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, lp[s]);
+  for (int s0 = 0; s0 < ns; s0 += 32) M = fmaxf(M, s0 + lane < ns ? lp[s0 + lane] : -INFINITY);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float wsum = 0.f;
-  for (int s = 0; s < ns; ++s) wsum += (lp[s] == -INFINITY) ? 0.f : fast_exp2(lp[s] - M);
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto add = [&](float l, const float4 (&v)[4]) {
+    if (l == -INFINITY) return;
+    const float f = fast_exp2(l - M);
+    wsum += f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j].x += f * v[j].x;
+      acc[j].y += f * v[j].y;
+      acc[j].z += f * v[j].z;
+      acc[j].w += f * v[j].w;
+    }
+  };
+  for (int s = 0; s < ns; s += 2) {
+    const bool two = s + 1 < ns;
+    float4 v0[4], v1[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v0[j] = *reinterpret_cast<const float4*>(op + (size_t)s * kDv + 128 * j);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      v1[j] = two ? *reinterpret_cast<const float4*>(op + (size_t)(s + 1) * kDv + 128 * j)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    add(lp[s], v0);
+    if (two) add(lp[s + 1], v1);
+  }
   const bool empty_row = !(wsum > 0.f);
   const float inv = empty_row ? 0.f : 1.f / wsum;
-  for (int d = lane * 4; d < kDv; d += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < ns; ++s) {
-      if (lp[s] == -INFINITY) continue;
-      const float f = fast_exp2(lp[s] - M);
-      const float4 v = *reinterpret_cast<const float4*>(o_part + ((size_t)row * max_splits + s) * kDv + d);
-      acc.x += f * v.x;
-      acc.y += f * v.y;
-      acc.z += f * v.z;
-      acc.w += f * v.w;
-    }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
     uint2 pk;
-    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(out + (size_t)row * kDv + d) = pk;
+    pk.x = pack_bf16x2(acc[j].x * inv, acc[j].y * inv);
+    pk.y = pack_bf16x2(acc[j].z * inv, acc[j].w * inv);
+    *reinterpret_cast<uint2*>(out + (size_t)row * kDv + lane * 4 + 128 * j) = pk;
   }
   if (out_lse && lane == 0) out_lse[row] = empty_row ? -INFINITY : (M + log2f(wsum)) * kLn2;
 }
