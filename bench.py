@@ -516,7 +516,9 @@ def _quest_extra(args, dev, flush, stream, wl, sink=0, recent=0, fused=False):
     peak, _ = _peaks()
     step_bytes = sum(abytes.values())
     if fused:
-        spans = {"fused_step": spans["decode"]}
+        # events 0-2 are recorded before the one launch and event 3 after it: its span is
+        # the third interval (the one the four-kernel step names "topk")
+        spans = {"fused_step": spans["topk"]}
         abytes = {"fused_step": step_bytes}
     kern = {k: {"ms": round(v, 5), "algorithmic_bytes": abytes[k],
                 "gbs": round(abytes[k] / (v * 1e-3) / 1e9, 1) if v > 0 else 0.0,
