@@ -107,3 +107,23 @@ def test_fused_full_qwen3_30b_a3b_128k_sampled(cuda_device):
     x, step, a = _prepare(wl, cuda_device, device_gen=True)
     _run_fused(x, step, a, cuda_device)
     compare_decode(x, step, [0, 13, wl.batch - 1], _scale(wl), "fused qwen3-30b full")
+
+
+def test_fused_step_is_repeatable(cuda_device):
+    # the one-launch step (cluster-wide scores, selection and split merge over distributed
+    # shared memory) run again on the same inputs gives bit-identical selections, outputs and
+    # log-sum-exps; without an append, every run sees the same cache
+    wl = QWEN3_4B_QUEST_32K.scaled(batch=4, context_min=6000, context_max=12000, topk_pages=64, append=False,
+                                   seed=81)
+    x, step, a = _prepare(wl, cuda_device)
+    _run_fused(x, step, a, cuda_device)
+    sel0, cnt0, out0, lse0 = step.sel.clone(), step.counts.clone(), step.out.clone(), step.lse.clone()
+    for _ in range(8):
+        _run_fused(x, step, a, cuda_device)
+        assert torch.equal(step.counts, cnt0)
+        for b in range(wl.batch):
+            for h in range(wl.num_kv_heads):
+                n = int(cnt0[b, h])
+                assert torch.equal(step.sel[b, h, :n], sel0[b, h, :n])
+        assert torch.equal(step.out.view(torch.int16), out0.view(torch.int16))
+        assert torch.equal(step.lse, lse0)
