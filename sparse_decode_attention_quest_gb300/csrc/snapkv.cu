@@ -441,6 +441,7 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBuckets = 1024;
 constexpr int kMaxMembers = 1024;
 constexpr int kSelPer = 44;                          // candidates per thread
+constexpr int kPoolHalfMax = 8;                      // pooling windows up to 17 wide by shuffles
 constexpr int kSelMaxCand = kSelThreads * kSelPer;   // 45056
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -452,30 +453,40 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // candidates t + 1024 e, so index order is (e, warp, lane): per (e, warp)
 // counts from ballots, one prefix over them (warp 0). Afterwards the rank of
 // owned candidate e is cnt[e * 32 + warp] + popc(ballot(flag) & lanes below).
-__device__ __forceinline__ void index_order_prefix(uint64_t flags, int E, int* cnt, int warp, int lane) {
+__device__ __forceinline__ int sel_warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Per-candidate flags (bit e of thread t: candidate t + 1024 e) to the exclusive
+// count, in candidate order, of the flagged candidates before each warp's group
+// of 32: cnt[e * 32 + warp]. Every thread scans up to two of the E x 32 group
+// counts, then the block adds the threads' sums with two warp-level scans.
+__device__ __forceinline__ void index_order_prefix(uint64_t flags, int E, int* cnt, int* wtot, int warp,
+                                                   int lane) {
   for (int e = 0; e < E; ++e) {
     const unsigned ball = __ballot_sync(0xffffffffu, (flags >> e) & 1ull);
     if (lane == 0) cnt[e * 32 + warp] = __popc(ball);
   }
   __syncthreads();
-  if (warp == 0) {
-    const int per = E;  // E * 32 entries over 32 lanes
-    const int lo = lane * per, hi = lo + per;
-    int sum = 0;
-    for (int i = lo; i < hi; ++i) sum += cnt[i];
-    int incl = sum;
+  const int N = E * 32;               // <= 2 * kSelThreads
+  const int tid = warp * 32 + lane;
+  const int i0 = 2 * tid;
+  const int c0 = i0 < N ? cnt[i0] : 0, c1 = i0 + 1 < N ? cnt[i0 + 1] : 0;
+  const int v = c0 + c1;
+  int incl = v;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    int run = incl - sum;
-    for (int i = lo; i < hi; ++i) {
-      const int c = cnt[i];
-      cnt[i] = run;
-      run += c;
-    }
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
   }
+  if (lane == 31) wtot[warp] = incl;
+  __syncthreads();
+  const int x = wtot[lane];
+  const int before = incl - v + sel_warp_sum(lane < warp ? x : 0);
+  if (i0 < N) cnt[i0] = before;
+  if (i0 + 1 < N) cnt[i0 + 1] = before + c0;
   __syncthreads();
 }
 
@@ -522,11 +533,38 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   }
   const float* sc = scores + (size_t)pair * score_stride;
   const int half = pool / 2;
-  // Max-pool over the scored positions (window clipped to them).
-  for (int i = tid; i < CS; i += kSelThreads) {
-    float m = -INFINITY;
-    for (int t = max(0, i - half); t <= min(CS - 1, i + half); ++t) m = fmaxf(m, sc[t]);
-    pooled[i] = m;
+  // Max-pool over the scored positions (window clipped to them). A warp takes
+  // 32 consecutive positions; a lane reads its own score, the three lanes at
+  // each end also the score `half` places beyond the warp's range, and the
+  // window comes from the neighbouring lanes by shuffles.
+  if (half <= kPoolHalfMax) {
+    for (int base = warp * 32; base < CS; base += kSelThreads) {  // warp-uniform
+      const int p = base + lane;
+      const float own = p < CS ? sc[p] : -INFINITY;
+      const int pl = base - half + lane, ph = base + 32 + lane - (32 - half);
+      const float lo = (lane < half && pl >= 0) ? sc[pl] : -INFINITY;            // position base - half + lane
+      const float hi = (lane >= 32 - half && ph < CS) ? sc[ph] : -INFINITY;      // position base + 32 + lane - (32 - half)
+      float m = own;
+#pragma unroll
+      for (int d = 1; d <= kPoolHalfMax; ++d) {
+        if (d <= half) {
+          const int dn = lane - d, up = lane + d;  // lanes holding p - d and p + d
+          const float a = __shfl_sync(0xffffffffu, own, dn & 31);
+          const float al = __shfl_sync(0xffffffffu, lo, (dn + half) & 31);
+          const float bu = __shfl_sync(0xffffffffu, own, up & 31);
+          const float bh = __shfl_sync(0xffffffffu, hi, (up - 32 + 32 - half) & 31);
+          m = fmaxf(m, dn >= 0 ? a : al);
+          m = fmaxf(m, up < 32 ? bu : bh);
+        }
+      }
+      if (p < CS) pooled[p] = m;
+    }
+  } else {
+    for (int i = tid; i < CS; i += kSelThreads) {
+      float m = -INFINITY;
+      for (int t = max(0, i - half); t <= min(CS - 1, i + half); ++t) m = fmaxf(m, sc[t]);
+      pooled[i] = m;
+    }
   }
   __syncthreads();
   const float* pc = pooled + c0;  // pooled score of candidate j
@@ -552,10 +590,11 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     s_max[warp] = lmax;
   }
   __syncthreads();
-  float mn = INFINITY, mx = -INFINITY;
-  for (int w = 0; w < kSelWarps; ++w) {
-    mn = fminf(mn, s_min[w]);
-    mx = fmaxf(mx, s_max[w]);
+  float mn = s_min[lane], mx = s_max[lane];  // min and max over the warps, by shuffles
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
   const float scale = (mx > mn) ? (float)kBuckets / (mx - mn) : 0.f;
   auto bucket = [&](float v) {
@@ -576,7 +615,10 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   }
   if (lane == 0) wtot[warp] = incl;
   __syncthreads();
-  for (int w = warp + 1; w < kSelWarps; ++w) incl += wtot[w];
+  {
+    const int x = wtot[lane];
+    incl += sel_warp_sum(lane > warp ? x : 0);  // candidates in the buckets of the warps above
+  }
   if (incl - hc < keep && keep <= incl) {
     s_info[0] = tid;
     s_info[1] = incl - hc;
@@ -677,7 +719,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     const int i = tid + e * kSelThreads;
     if (i < C && order_key(pc[i]) == T) eqf |= 1ull << e;
   }
-  index_order_prefix(eqf, E, cnt, warp, lane);
+  index_order_prefix(eqf, E, cnt, wtot, warp, lane);
   uint64_t self = 0;
   for (int e = 0; e < E; ++e) {
     const int i = tid + e * kSelThreads;
@@ -689,7 +731,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     }
   }
   __syncthreads();  // cnt is reused
-  index_order_prefix(self, E, cnt, warp, lane);
+  index_order_prefix(self, E, cnt, wtot, warp, lane);
   for (int e = 0; e < E; ++e) {
     const unsigned ball = __ballot_sync(0xffffffffu, (self >> e) & 1ull);
     if ((self >> e) & 1ull) {
