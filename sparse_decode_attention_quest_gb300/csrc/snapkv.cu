@@ -442,6 +442,7 @@ constexpr int kBuckets = 1024;
 constexpr int kMaxMembers = 1024;
 constexpr int kSelPer = 44;                          // candidates per thread
 constexpr int kPoolHalfMax = 8;                      // pooling windows up to 17 wide by shuffles
+constexpr int kPoolUnroll = 4;                       // chunks of 32 positions a warp loads at once
 constexpr int kSelMaxCand = kSelThreads * kSelPer;   // 45056
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -538,26 +539,38 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   // each end also the score `half` places beyond the warp's range, and the
   // window comes from the neighbouring lanes by shuffles.
   if (half <= kPoolHalfMax) {
-    for (int base = warp * 32; base < CS; base += kSelThreads) {  // warp-uniform
-      const int p = base + lane;
-      const float own = p < CS ? sc[p] : -INFINITY;
-      const int pl = base - half + lane, ph = base + 32 + lane - (32 - half);
-      const float lo = (lane < half && pl >= 0) ? sc[pl] : -INFINITY;            // position base - half + lane
-      const float hi = (lane >= 32 - half && ph < CS) ? sc[ph] : -INFINITY;      // position base + 32 + lane - (32 - half)
-      float m = own;
+    // kPoolUnroll chunks of a warp are loaded before the first is pooled, so that
+    // their memory latency overlaps.
+    for (int base0 = warp * 32; base0 < CS; base0 += kPoolUnroll * kSelThreads) {  // warp-uniform
+      float own[kPoolUnroll], lo[kPoolUnroll], hi[kPoolUnroll];
 #pragma unroll
-      for (int d = 1; d <= kPoolHalfMax; ++d) {
-        if (d <= half) {
-          const int dn = lane - d, up = lane + d;  // lanes holding p - d and p + d
-          const float a = __shfl_sync(0xffffffffu, own, dn & 31);
-          const float al = __shfl_sync(0xffffffffu, lo, (dn + half) & 31);
-          const float bu = __shfl_sync(0xffffffffu, own, up & 31);
-          const float bh = __shfl_sync(0xffffffffu, hi, (up - 32 + 32 - half) & 31);
-          m = fmaxf(m, dn >= 0 ? a : al);
-          m = fmaxf(m, up < 32 ? bu : bh);
+      for (int u = 0; u < kPoolUnroll; ++u) {
+        const int base = base0 + u * kSelThreads, p = base + lane;
+        const int pl = base - half + lane, ph = base + lane + half;
+        own[u] = p < CS ? sc[p] : -INFINITY;
+        lo[u] = (lane < half && pl >= 0 && pl < CS) ? sc[pl] : -INFINITY;     // position base - half + lane
+        hi[u] = (lane >= 32 - half && ph < CS) ? sc[ph] : -INFINITY;          // position base + lane + half
+      }
+#pragma unroll
+      for (int u = 0; u < kPoolUnroll; ++u) {
+        const int base = base0 + u * kSelThreads, p = base + lane;
+        if (base < CS) {  // warp-uniform
+          float m = own[u];
+#pragma unroll
+          for (int d = 1; d <= kPoolHalfMax; ++d) {
+            if (d <= half) {
+              const int dn = lane - d, up = lane + d;  // lanes holding p - d and p + d
+              const float a = __shfl_sync(0xffffffffu, own[u], dn & 31);
+              const float al = __shfl_sync(0xffffffffu, lo[u], (dn + half) & 31);
+              const float bu = __shfl_sync(0xffffffffu, own[u], up & 31);
+              const float bh = __shfl_sync(0xffffffffu, hi[u], (up - half) & 31);
+              m = fmaxf(m, dn >= 0 ? a : al);
+              m = fmaxf(m, up < 32 ? bu : bh);
+            }
+          }
+          if (p < CS) pooled[p] = m;
         }
       }
-      if (p < CS) pooled[p] = m;
     }
   } else {
     for (int i = tid; i < CS; i += kSelThreads) {
