@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   }
   hist[tid] = 0;
   if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
-  if (tid == 0) s_info[2] = 0;
+  if (tid == 0) s_info[2] = s_info[3] = 0;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     lmin = fminf(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
@@ -727,23 +727,33 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     need_eq = remaining;
   }
   // Selected: pooled key above T, or equal to T among the first need_eq by position.
-  uint64_t eqf = 0;
+  uint64_t self = 0, eqf = 0;
+  int n_eq = 0;
   for (int e = 0; e < E; ++e) {
     const int i = tid + e * kSelThreads;
-    if (i < C && order_key(pc[i]) == T) eqf |= 1ull << e;
-  }
-  index_order_prefix(eqf, E, cnt, wtot, warp, lane);
-  uint64_t self = 0;
-  for (int e = 0; e < E; ++e) {
-    const int i = tid + e * kSelThreads;
-    const unsigned ball = __ballot_sync(0xffffffffu, (eqf >> e) & 1ull);
-    const int eq_rank = cnt[e * 32 + warp] + __popc(ball & lt);
     if (i < C) {
       const uint32_t key = order_key(pc[i]);
-      if (key > T || (key == T && eq_rank < need_eq)) self |= 1ull << e;
+      if (key > T) {
+        self |= 1ull << e;
+      } else if (key == T) {
+        eqf |= 1ull << e;
+        ++n_eq;
+      }
     }
   }
-  __syncthreads();  // cnt is reused
+  if (n_eq) atomicAdd(&s_info[3], n_eq);
+  __syncthreads();
+  if (s_info[3] <= need_eq) {  // block-uniform: every key equal to T is taken (the usual case)
+    self |= eqf;
+  } else {                     // more ties than places: the first need_eq by position
+    index_order_prefix(eqf, E, cnt, wtot, warp, lane);
+    for (int e = 0; e < E; ++e) {
+      const unsigned ball = __ballot_sync(0xffffffffu, (eqf >> e) & 1ull);
+      const int eq_rank = cnt[e * 32 + warp] + __popc(ball & lt);
+      if (((eqf >> e) & 1ull) && eq_rank < need_eq) self |= 1ull << e;
+    }
+    __syncthreads();  // cnt is reused
+  }
   index_order_prefix(self, E, cnt, wtot, warp, lane);
   for (int e = 0; e < E; ++e) {
     const unsigned ball = __ballot_sync(0xffffffffu, (self >> e) & 1ull);
