@@ -534,10 +534,12 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   }
   const float* sc = scores + (size_t)pair * score_stride;
   const int half = pool / 2;
-  // Max-pool over the scored positions (window clipped to them). A warp takes
-  // 32 consecutive positions; a lane reads its own score, the three lanes at
-  // each end also the score `half` places beyond the warp's range, and the
-  // window comes from the neighbouring lanes by shuffles.
+  float lmin = INFINITY, lmax = -INFINITY;  // over the finite pooled scores of the candidates
+  // Max-pool over the scored positions (window clipped to them), and the min and
+  // max of the candidates' pooled scores on the way. A warp takes 32
+  // consecutive positions; a lane reads its own score, the `half` lanes at each
+  // end also the score `half` places beyond the warp's range, and the window
+  // comes from the neighbouring lanes by shuffles.
   if (half <= kPoolHalfMax) {
     // kPoolUnroll chunks of a warp are loaded before the first is pooled, so that
     // their memory latency overlaps.
@@ -569,6 +571,10 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
             }
           }
           if (p < CS) pooled[p] = m;
+          if (p >= c0 && p < c1 && isfinite(m)) {
+            lmin = fminf(lmin, m);
+            lmax = fmaxf(lmax, m);
+          }
         }
       }
     }
@@ -577,19 +583,15 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
       float m = -INFINITY;
       for (int t = max(0, i - half); t <= min(CS - 1, i + half); ++t) m = fmaxf(m, sc[t]);
       pooled[i] = m;
+      if (i >= c0 && i < c1 && isfinite(m)) {
+        lmin = fminf(lmin, m);
+        lmax = fmaxf(lmax, m);
+      }
     }
   }
   __syncthreads();
   const float* pc = pooled + c0;  // pooled score of candidate j
   const int E = (C + kSelThreads - 1) / kSelThreads;
-  float lmin = INFINITY, lmax = -INFINITY;
-  for (int e = 0; e < E; ++e) {
-    const int i = tid + e * kSelThreads;
-    if (i < C && isfinite(pc[i])) {
-      lmin = fminf(lmin, pc[i]);
-      lmax = fmaxf(lmax, pc[i]);
-    }
-  }
   hist[tid] = 0;
   if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
   if (tid == 0) s_info[2] = s_info[3] = 0;
