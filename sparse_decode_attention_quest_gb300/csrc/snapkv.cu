@@ -27,6 +27,8 @@
 // The tiles of all (request, KV head) pairs form one flattened range; every
 // CTA takes an equal slice. Pass 1 writes per-slice partial (max, sum) per row
 // that pass 2 merges.
+#include <cooperative_groups.h>
+
 #include "se_ptx.cuh"
 
 namespace se {
@@ -443,6 +445,7 @@ constexpr int kMaxMembers = 1024;
 constexpr int kSelPer = 44;                          // candidates per thread
 constexpr int kPoolHalfMax = 8;                      // pooling windows up to 17 wide by shuffles
 constexpr int kPoolUnroll = 4;                       // chunks of 32 positions a warp loads at once
+constexpr int kSelCluster = 4;                       // CTAs per (request, KV head): the pooling is shared
 constexpr int kSelMaxCand = kSelThreads * kSelPer;   // 45056
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -492,10 +495,11 @@ __device__ __forceinline__ void index_order_prefix(uint64_t flags, int E, int* c
 }
 
 // Max-pool of the scores, then the top `keep` candidates by pooled score (ties:
-// lower position) in ascending order, then the window positions. One CTA per
-// (request, KV head); thread t owns candidates t + 1024 e (coalesced pooling
-// reads, conflict-free shared-memory accesses); pooled scores live in shared
-// memory, per-candidate flags in a 64-bit mask.
+// lower position) in ascending order, then the window positions. A cluster of
+// kSelCluster CTAs per (request, KV head) pools the positions into rank 0's
+// shared memory, and rank 0 selects: its thread t owns candidates t + 1024 e
+// (conflict-free shared-memory accesses); per-candidate flags sit in a 64-bit
+// mask.
 __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ lens, int32_t H, int32_t W,
     int32_t max_len, int32_t pool, int32_t keep, int32_t sink, int32_t recent, int32_t* __restrict__ kept,
@@ -508,14 +512,18 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   __shared__ float mem_val[kMaxMembers];
   __shared__ int mem_idx[kMaxMembers];
   __shared__ int cnt[kSelPer * 32];
-  __shared__ int s_info[4];
+  __shared__ int s_info[4];  // bucket B, keys above B, members collected, keys equal to the threshold
   __shared__ int rhist[3][257];
-  const int pair = blockIdx.x, b = pair / H;
+  __shared__ float cl_mm[2 * kSelCluster];  // rank 0: every rank's min and max of its pooled candidates
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int pair = blockIdx.x / kSelCluster, b = pair / H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const unsigned lt = (1u << lane) - 1u;
   const int n = lens[b];
-  if (n < W || n > max_len) {
-    if (tid == 0) {
+  if (n < W || n > max_len) {  // the same decision in every rank of the cluster
+    if (tid == 0 && rank == 0) {
       raise_error(err, SE_DEVERR_LENGTH);
       kept_counts[pair] = 0;
     }
@@ -528,10 +536,17 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   const int C = c1 - c0;  // candidate j is position c0 + j
   int32_t* out = kept + (size_t)pair * kept_stride;
   if (C <= keep) {
-    for (int i = tid; i < n; i += kSelThreads) out[i] = i;
-    if (tid == 0) kept_counts[pair] = n;
+    if (rank == 0) {
+      for (int i = tid; i < n; i += kSelThreads) out[i] = i;
+      if (tid == 0) kept_counts[pair] = n;
+    }
     return;
   }
+  // The ranks of the cluster pool the positions together, into rank 0's shared
+  // memory; rank 0 alone then selects. Every rank has started before any writes
+  // into rank 0's shared memory.
+  cluster.sync();
+  float* pooled0 = cluster.map_shared_rank(pooled, 0);
   const float* sc = scores + (size_t)pair * score_stride;
   const int half = pool / 2;
   float lmin = INFINITY, lmax = -INFINITY;  // over the finite pooled scores of the candidates
@@ -543,11 +558,12 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   if (half <= kPoolHalfMax) {
     // kPoolUnroll chunks of a warp are loaded before the first is pooled, so that
     // their memory latency overlaps.
-    for (int base0 = warp * 32; base0 < CS; base0 += kPoolUnroll * kSelThreads) {  // warp-uniform
+    constexpr int kStride = kSelCluster * kSelThreads;  // positions the cluster's warps cover per round
+    for (int base0 = (rank * kSelWarps + warp) * 32; base0 < CS; base0 += kPoolUnroll * kStride) {  // warp-uniform
       float own[kPoolUnroll], lo[kPoolUnroll], hi[kPoolUnroll];
 #pragma unroll
       for (int u = 0; u < kPoolUnroll; ++u) {
-        const int base = base0 + u * kSelThreads, p = base + lane;
+        const int base = base0 + u * kStride, p = base + lane;
         const int pl = base - half + lane, ph = base + lane + half;
         own[u] = p < CS ? sc[p] : -INFINITY;
         lo[u] = (lane < half && pl >= 0 && pl < CS) ? sc[pl] : -INFINITY;     // position base - half + lane
@@ -555,7 +571,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
       }
 #pragma unroll
       for (int u = 0; u < kPoolUnroll; ++u) {
-        const int base = base0 + u * kSelThreads, p = base + lane;
+        const int base = base0 + u * kStride, p = base + lane;
         if (base < CS) {  // warp-uniform
           float m = own[u];
 #pragma unroll
@@ -570,7 +586,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
               m = fmaxf(m, up < 32 ? bu : bh);
             }
           }
-          if (p < CS) pooled[p] = m;
+          if (p < CS) pooled0[p] = m;
           if (p >= c0 && p < c1 && isfinite(m)) {
             lmin = fminf(lmin, m);
             lmax = fmaxf(lmax, m);
@@ -579,10 +595,10 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
       }
     }
   } else {
-    for (int i = tid; i < CS; i += kSelThreads) {
+    for (int i = rank * kSelThreads + tid; i < CS; i += kSelCluster * kSelThreads) {
       float m = -INFINITY;
       for (int t = max(0, i - half); t <= min(CS - 1, i + half); ++t) m = fmaxf(m, sc[t]);
-      pooled[i] = m;
+      pooled0[i] = m;
       if (i >= c0 && i < c1 && isfinite(m)) {
         lmin = fminf(lmin, m);
         lmax = fmaxf(lmax, m);
@@ -610,6 +626,18 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   for (int o = 16; o > 0; o >>= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (tid == 0) {
+    float* mm0 = cluster.map_shared_rank(cl_mm, 0);
+    mm0[2 * rank] = mn;
+    mm0[2 * rank + 1] = mx;
+  }
+  cluster.sync();  // rank 0 holds every pooled score and every rank's min and max
+  if (rank != 0) return;
+#pragma unroll
+  for (int r = 0; r < kSelCluster; ++r) {
+    mn = fminf(mn, cl_mm[2 * r]);
+    mx = fmaxf(mx, cl_mm[2 * r + 1]);
   }
   const float scale = (mx > mn) ? (float)kBuckets / (mx - mn) : 0.f;
   auto bucket = [&](float v) {
@@ -880,12 +908,25 @@ cudaError_t launch_snapkv_select(const float* scores, int32_t score_stride, cons
   const size_t smem = (size_t)maxc * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(snapkv_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  {
-    const cudaError_t le = launch_pdl(snapkv_select_kernel, dim3(batch * num_kv_heads), dim3(kSelThreads), smem,
-                                      stream, scores, score_stride, lens, num_kv_heads, window, max_len, pool, keep,
-                                      sink, recent, kept, kept_stride, kept_counts, err);
-    if (le != cudaSuccess) return le;
-  }
+  // A cluster of kSelCluster CTAs per (request, KV head), launched with
+  // programmatic dependent launch like every other kernel of the library.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch * num_kv_heads * kSelCluster);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kSelCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, snapkv_select_kernel, scores, score_stride, lens, num_kv_heads, window, max_len, pool,
+                         keep, sink, recent, kept, kept_stride, kept_counts, err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
