@@ -799,7 +799,10 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
 
 // ------------------------------------------------------------------ compaction
 // Kept token t of pair (b, h) goes to destination page dst_bt[b][t / 16], slot t % 16.
-// One half-warp copies one 256-byte row (16 x 16 bytes); K and V rows alternate.
+// A half-warp copies the K and V rows (256 bytes each, 16 x 16 bytes) of
+// kGatherTok consecutive kept tokens of one pair: their positions and page ids
+// are looked up together and their 2 kGatherTok row loads are in flight at once.
+constexpr int kGatherTok = 4;
 __global__ void __launch_bounds__(256) snapkv_gather_kernel(KvView src, uint16_t* __restrict__ dk,
                                                             uint16_t* __restrict__ dv, int32_t dst_num_pages,
                                                             const int32_t* __restrict__ src_bt, int32_t src_bt_stride,
@@ -808,33 +811,50 @@ __global__ void __launch_bounds__(256) snapkv_gather_kernel(KvView src, uint16_t
                                                             const int32_t* __restrict__ kept, int32_t kept_stride,
                                                             const int32_t* __restrict__ kept_counts, unsigned* err) {
   pdl_enter();
-  const long long unit = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);  // (pair, t, K|V)
+  const long long unit = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);  // (pair, group of kGatherTok tokens)
   const int sub = threadIdx.x & 15;
-  const long long rows = (long long)pairs * kept_stride * 2;
-  if (unit >= rows) return;
-  const int kvsel = (int)(unit & 1);
-  const long long pt = unit >> 1;
-  const int pair = (int)(pt / kept_stride), t = (int)(pt % kept_stride);
+  const int groups = (kept_stride + kGatherTok - 1) / kGatherTok;
+  if (unit >= (long long)pairs * groups) return;
+  const int pair = (int)(unit / groups), t0 = (int)(unit % groups) * kGatherTok;
   const int H = src.num_kv_heads;
   const int b = pair / H, h = pair % H;
   const int cnt = kept_counts[pair];
-  if (t >= cnt || cnt > kept_stride) return;
-  const int pos = kept[(size_t)pair * kept_stride + t];
+  if (cnt > kept_stride) return;
   const int n = lens[b];
-  if (pos < 0 || pos >= n || pos / kPageSize >= src_bt_stride || t / kPageSize >= dst_bt_stride) {
-    if (sub == 0) raise_error(err, SE_DEVERR_LENGTH);
-    return;
+  // (page, head, slot) row of each token in the source and the destination cache; -1: not copied
+  long long srow[kGatherTok], drow[kGatherTok];
+#pragma unroll
+  for (int u = 0; u < kGatherTok; ++u) {
+    srow[u] = drow[u] = -1;
+    const int t = t0 + u;
+    if (t >= cnt) continue;
+    const int pos = kept[(size_t)pair * kept_stride + t];
+    if (pos < 0 || pos >= n || pos / kPageSize >= src_bt_stride || t / kPageSize >= dst_bt_stride) {
+      if (sub == 0) raise_error(err, SE_DEVERR_LENGTH);
+      continue;
+    }
+    const int sp = src_bt[(size_t)b * src_bt_stride + pos / kPageSize];
+    const int dp = dst_bt[(size_t)b * dst_bt_stride + t / kPageSize];
+    if (sp < 0 || sp >= src.num_pages || dp < 0 || dp >= dst_num_pages) {
+      if (sub == 0) raise_error(err, SE_DEVERR_PAGE_RANGE);
+      continue;
+    }
+    srow[u] = ((long long)sp * H + h) * kPageSize + pos % kPageSize;
+    drow[u] = ((long long)dp * H + h) * kPageSize + t % kPageSize;
   }
-  const int sp = src_bt[(size_t)b * src_bt_stride + pos / kPageSize];
-  const int dp = dst_bt[(size_t)b * dst_bt_stride + t / kPageSize];
-  if (sp < 0 || sp >= src.num_pages || dp < 0 || dp >= dst_num_pages) {
-    if (sub == 0) raise_error(err, SE_DEVERR_PAGE_RANGE);
-    return;
+  uint4 kr[kGatherTok], vr[kGatherTok];
+#pragma unroll
+  for (int u = 0; u < kGatherTok; ++u) {
+    if (srow[u] < 0) continue;
+    kr[u] = reinterpret_cast<const uint4*>(src.k + (size_t)srow[u] * src.row_stride_k)[sub];
+    vr[u] = reinterpret_cast<const uint4*>(src.v + (size_t)srow[u] * src.row_stride_v)[sub];
   }
-  const uint16_t* s = (kvsel ? src.v : src.k) + (((size_t)sp * H + h) * kPageSize + pos % kPageSize) *
-                                                     (kvsel ? src.row_stride_v : src.row_stride_k);
-  uint16_t* d = (kvsel ? dv : dk) + (((size_t)dp * H + h) * kPageSize + t % kPageSize) * kD;
-  reinterpret_cast<uint4*>(d)[sub] = reinterpret_cast<const uint4*>(s)[sub];
+#pragma unroll
+  for (int u = 0; u < kGatherTok; ++u) {
+    if (drow[u] < 0) continue;
+    reinterpret_cast<uint4*>(dk + (size_t)drow[u] * kD)[sub] = kr[u];
+    reinterpret_cast<uint4*>(dv + (size_t)drow[u] * kD)[sub] = vr[u];
+  }
 }
 
 size_t scores_smem_bytes(int pairs) {
@@ -935,10 +955,10 @@ cudaError_t launch_snapkv_gather(const KvView& src, uint16_t* dk, uint16_t* dv, 
                                  int32_t dst_bt_stride, const int32_t* lens, int32_t batch, const int32_t* kept,
                                  int32_t kept_stride, const int32_t* kept_counts, unsigned* err, cudaStream_t stream) {
   const int pairs = batch * src.num_kv_heads;
-  const long long rows = (long long)pairs * kept_stride * 2;
-  if (rows == 0) return cudaSuccess;
+  const long long units = (long long)pairs * ((kept_stride + kGatherTok - 1) / kGatherTok);
+  if (units == 0) return cudaSuccess;
   {
-    const cudaError_t le = launch_pdl(snapkv_gather_kernel, dim3((unsigned)((rows + 15) / 16)), dim3(256), 0, stream,
+    const cudaError_t le = launch_pdl(snapkv_gather_kernel, dim3((unsigned)((units + 15) / 16)), dim3(256), 0, stream,
                                       src, dk, dv, dst_num_pages, src_bt, src_bt_stride, dst_bt, dst_bt_stride, lens,
                                       pairs, kept, kept_stride, kept_counts, err);
     if (le != cudaSuccess) return le;
