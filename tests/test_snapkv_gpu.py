@@ -101,7 +101,7 @@ def test_snapkv_oracle_sized_ragged(cuda_device):
             _check_pair(x, res, b, h)
 
 
-@pytest.mark.parametrize("pool", [1, 3])
+@pytest.mark.parametrize("pool", [1, 3, 17, 21])  # 17: the widest window pooled by shuffles; 21: the loop
 def test_snapkv_pool_sizes_and_small_windows(cuda_device, pool):
     wl = SNAPKV_PREFILL_32K.scaled(batch=2, num_q_heads=16, num_kv_heads=4, window=16, prompt_min=300,
                                    prompt_max=1000, keep_topk=40, seed=8)
