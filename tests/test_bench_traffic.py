@@ -4,8 +4,6 @@ import hashlib
 import json
 import os
 
-import pytest
-
 import bench
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
