@@ -669,7 +669,8 @@ def main():
     ap.add_argument("--mla-only", action="store_true", help="only the latent-cache measurement (for profiler captures)")
     ap.add_argument("--cpu-cores", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None,
-                    help="smaller batch (the 128K or, with --mla-only, the latent workload) for profiler captures only")
+                    help="smaller batch (the 128K or, with --mla-only / --snapkv-only, the latent or SnapKV workload) "
+                         "for profiler captures only")
     args = ap.parse_args()
     global _BATCH_OVERRIDE
     _BATCH_OVERRIDE = args.batch
@@ -686,7 +687,9 @@ def main():
         import torch
         dev = torch.device("cuda", local_rank)
         flush = L2Flush(dev)
-        print(json.dumps({"snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, torch.cuda.Stream(dev))}))
+        from synth import SNAPKV_PREFILL_32K
+        wl = SNAPKV_PREFILL_32K if args.batch is None else SNAPKV_PREFILL_32K.scaled(batch=args.batch)
+        print(json.dumps({wl.name: _snapkv_extra(args, dev, flush, torch.cuda.Stream(dev), wl)}))
         return
     if args.mla_only:  # profiler captures of the latent-cache kernels alone (never the reported metric)
         import torch

@@ -180,6 +180,70 @@ def check_select_windowed_reduces_to_plain(quest):
         assert quest.kth_score_windowed(scores, L, PS, k, 0, 0) == quest.kth_score(scores, n, k)
 
 
+# ------------------------------------------------------------------ selection thresholds
+# tau, the k-th largest candidate score, centres the exemption band of the parity
+# rule. Pinned by rank counting from its definition: tau is the score of the one
+# candidate that exactly k - 1 candidates rank before (higher score, or equal score
+# and lower index); with no more candidates than k every candidate is kept and there
+# is no threshold.
+def _rank_k_score(scores, cands, k):
+    cands = list(cands)
+    if len(cands) <= k:
+        return None
+    hits = [scores[p] for p in cands
+            if sum(1 for r in cands if scores[r] > scores[p] or (scores[r] == scores[p] and r < p)) == k - 1]
+    assert len(hits) == 1
+    return hits[0]
+
+
+def _window_candidates(n_tokens, ps, S, R):
+    """Pages in neither keep window (token-level definition), the last page excluded."""
+    n = -(-n_tokens // ps)
+    return [p for p in range(n) if not (p == n - 1 or p * ps < S or min((p + 1) * ps, n_tokens) - 1 >= n_tokens - R)]
+
+
+def check_kth_score_rank_counting(quest):
+    rng = _rng(27)
+    for _ in range(150):
+        n = int(rng.integers(0, 24))
+        k = int(rng.integers(1, 9))
+        scores = rng.integers(-3, 4, size=max(n - 1, 0)).astype(float)  # many ties
+        assert quest.kth_score(scores, n, k) == _rank_k_score(scores, range(n - 1), k), (n, k, scores)
+    # distinct scores: tau is the k-th value counted from the top
+    assert quest.kth_score(np.array([5.0, 1.0, 4.0, 2.0, 3.0]), 6, 2) == 4.0
+    assert quest.kth_score(np.array([5.0, 1.0, 4.0]), 4, 3) is None       # 3 candidates, k = 3: all kept
+    assert quest.kth_score(np.array([5.0, 1.0, 4.0, 2.0]), 5, 4) is None
+
+
+def check_kth_score_windowed_rank_counting(quest):
+    rng = _rng(29)
+    for _ in range(200):
+        L = int(rng.integers(0, 90))
+        S, R, k = int(rng.integers(0, 20)), int(rng.integers(0, 30)), int(rng.integers(1, 6))
+        n = -(-L // PS)
+        scores = rng.integers(-2, 3, size=max(n - 1, 0)).astype(float)
+        ref = _rank_k_score(scores, _window_candidates(L, PS, S, R), k)
+        assert quest.kth_score_windowed(scores, L, PS, k, S, R) == ref, (L, S, R, k, scores)
+
+
+def check_decode_threshold_is_lowest_selected_score(quest):
+    """The threshold a decode reports is the lowest score among its selected candidates
+    (the top k by score hold the k-th largest as their minimum)."""
+    rng = _rng(31)
+    H, G, D = 2, 2, 4
+    for L, k, S, R in ((37, 3, 0, 0), (41, 2, 0, 0), (61, 4, 5, 9), (64, 3, 4, 8), (9, 4, 0, 0)):
+        kc, vc, bt, _, _ = _paged(rng, L, H, D)
+        q = rng.standard_normal((H * G, D))
+        res = quest.QuestRequest(kc, vc, bt, L, H, D, D, PS).decode(q, k, 0.5, sink_tokens=S, recent_tokens=R)
+        cands = _window_candidates(L, PS, S, R)
+        for hr in res.heads:
+            chosen = [p for p in hr.pages if p in cands]
+            if len(cands) <= k:
+                assert hr.threshold is None
+            else:
+                assert len(chosen) == k and hr.threshold == min(hr.scores[p] for p in chosen), (L, k, S, R)
+
+
 # ------------------------------------------------------------------ attention
 def _sdpa(qg, K, V, scale):
     q = torch.from_numpy(qg)[None, :, None, :]          # [1][G][1][D]
@@ -352,6 +416,48 @@ def check_keep_positions_windowed(snapkv):
             assert ref == snapkv.keep_positions(pooled, n, W, keep)
 
 
+def check_kth_pooled_rank_counting(snapkv):
+    rng = _rng(33)
+    for _ in range(150):
+        c = int(rng.integers(0, 24))
+        keep = int(rng.integers(1, 9))
+        pooled = rng.integers(0, 4, size=c).astype(float)
+        assert snapkv.kth_pooled(pooled, keep) == _rank_k_score(pooled, range(c), keep), (c, keep, pooled)
+    assert snapkv.kth_pooled(np.array([0.1, 0.7, 0.3, 0.5]), 3) == 0.3
+    assert snapkv.kth_pooled(np.array([0.1, 0.7, 0.3]), 3) is None
+
+
+def check_kth_pooled_windowed_rank_counting(snapkv):
+    rng = _rng(35)
+    for _ in range(200):
+        n = int(rng.integers(2, 40))
+        W = int(rng.integers(1, n + 1))
+        R = int(rng.integers(W, n + 3))
+        S = int(rng.integers(0, 12))
+        keep = int(rng.integers(1, 8))
+        pooled = rng.integers(0, 4, size=n - W).astype(float)
+        cands = [j for j in range(n - W) if S <= j < n - R]
+        assert snapkv.kth_pooled_windowed(pooled, n, W, keep, S, R) == _rank_k_score(pooled, cands, keep), \
+            (n, W, R, S, keep)
+
+
+def check_snapkv_threshold_is_lowest_kept_score(snapkv):
+    """The threshold of a head is the lowest pooled score among its chosen candidates."""
+    rng = _rng(37)
+    D, G = 6, 2
+    for n, W, keep, S, R in ((40, 4, 5, 0, None), (45, 3, 6, 4, 9), (12, 4, 9, 0, None), (30, 2, 3, 3, 2)):
+        kc, _, bt, _, _ = _paged(rng, n, 1, D)
+        q = rng.standard_normal((W, G, D))
+        res = snapkv.snapkv_head(q, kc, bt, 0, n, W, 3, keep, 0.4, PS, sink=S, recent=R)
+        RR = W if R is None else R
+        cands = [j for j in range(n - W) if S <= j < n - RR]
+        chosen = [j for j in res["kept"] if j in cands]
+        if len(cands) <= keep:
+            assert res["threshold"] is None
+        else:
+            assert len(chosen) == keep and res["threshold"] == min(res["pooled"][j] for j in chosen), (n, W, keep)
+
+
 def check_snapkv_head_end_to_end(snapkv):
     """Whole head against torch routines: softmax, max_pool1d and a stable sort."""
     rng = _rng(16)
@@ -384,6 +490,9 @@ QUEST_CHECKS = [check_summary_bruteforce, check_append_matches_rebuild, check_bo
                 check_select_all_equals_dense, check_single_token_attention, check_empty_request,
                 check_permutation_invariance, check_latent_value_is_key_prefix,
                 check_selection_uses_the_bound, check_select_windowed_bruteforce,
-                check_select_windowed_reduces_to_plain]
+                check_select_windowed_reduces_to_plain, check_kth_score_rank_counting,
+                check_kth_score_windowed_rank_counting, check_decode_threshold_is_lowest_selected_score]
 SNAPKV_CHECKS = [check_window_probabilities, check_window_lse, check_candidate_scores, check_max_pool,
-                 check_keep_positions, check_keep_positions_windowed, check_snapkv_head_end_to_end, check_compaction_exact]
+                 check_keep_positions, check_keep_positions_windowed, check_kth_pooled_rank_counting,
+                 check_kth_pooled_windowed_rank_counting, check_snapkv_threshold_is_lowest_kept_score,
+                 check_snapkv_head_end_to_end, check_compaction_exact]

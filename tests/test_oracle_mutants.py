@@ -112,6 +112,78 @@ def _s_windowed_recent_is_window(pooled, n, window, keep, sink, recent):
         sorted(set(range(min(sink, n))) | set(snapkv.keep_positions(pooled, n, window, keep)))
 
 
+def _q_kth_off_by_one(scores, n_pages, topk):
+    cands = [scores[p] for p in range(n_pages - 1)]
+    if len(cands) <= topk:
+        return None
+    return sorted(cands, reverse=True)[min(topk, len(cands) - 1)]
+
+
+def _q_kth_ascending(scores, n_pages, topk):
+    cands = [scores[p] for p in range(n_pages - 1)]
+    if len(cands) <= topk:
+        return None
+    return sorted(cands)[topk - 1]
+
+
+def _q_kth_last_page_a_candidate(scores, n_pages, topk):
+    cands = [scores[p] for p in range(min(n_pages, len(scores)))] + ([float("inf")] if n_pages > 0 else [])
+    if len(cands) <= topk:
+        return None
+    return sorted(cands, reverse=True)[topk - 1]
+
+
+def _q_kth_all_kept_when_equal(scores, n_pages, topk):
+    cands = [scores[p] for p in range(n_pages - 1)]
+    if len(cands) < topk:
+        return None
+    return sorted(cands, reverse=True)[topk - 1]
+
+
+def _q_kth_windowed_counts_kept(scores, n_tokens, page_size, topk, sink_tokens, recent_tokens):
+    # the kept windows ranked with the candidates
+    n = -(-n_tokens // page_size)
+    cands = list(range(max(n - 1, 0)))
+    if len(cands) <= topk:
+        return None
+    return sorted((scores[p] for p in cands), reverse=True)[topk - 1]
+
+
+def _q_kth_windowed_off_by_one(scores, n_tokens, page_size, topk, sink_tokens, recent_tokens):
+    _, cands = quest.keep_windows(n_tokens, page_size, sink_tokens, recent_tokens)
+    if len(cands) <= topk:
+        return None
+    return sorted((scores[p] for p in cands), reverse=True)[topk - 2 if topk > 1 else 0]
+
+
+def _s_kth_off_by_one(pooled, keep):
+    if len(pooled) <= keep:
+        return None
+    return sorted(pooled.tolist(), reverse=True)[keep]
+
+
+def _s_kth_ascending(pooled, keep):
+    if len(pooled) <= keep:
+        return None
+    return sorted(pooled.tolist())[keep - 1]
+
+
+def _s_kth_windowed_counts_sink(pooled, n, window, keep, sink, recent):
+    # the sink and recent positions ranked with the candidates
+    cands = [pooled[j] for j in range(n - window)]
+    if len(cands) <= keep:
+        return None
+    return sorted(cands, reverse=True)[keep - 1]
+
+
+def _s_kth_windowed_off_by_one(pooled, n, window, keep, sink, recent):
+    always = set(range(min(sink, n))) | set(range(max(0, n - recent), n))
+    cands = [pooled[j] for j in range(n - window) if j not in always]
+    if len(cands) <= keep:
+        return None
+    return sorted(cands, reverse=True)[min(keep, len(cands) - 1)]
+
+
 MUTANTS = [
     (quest, "page_summary", _q_summary_swapped, pins.QUEST_CHECKS),
     (quest, "append_to_summary", _q_append_never_resets, pins.QUEST_CHECKS),
@@ -124,11 +196,21 @@ MUTANTS = [
     (quest, "softmax_attention", _q_attention_no_scale, pins.QUEST_CHECKS),
     (quest, "keep_windows", _q_windows_recent_whole_pages, pins.QUEST_CHECKS),
     (quest, "select_pages_windowed", _q_windowed_sink_in_budget, pins.QUEST_CHECKS),
+    (quest, "kth_score", _q_kth_off_by_one, pins.QUEST_CHECKS),
+    (quest, "kth_score", _q_kth_ascending, pins.QUEST_CHECKS),
+    (quest, "kth_score", _q_kth_last_page_a_candidate, pins.QUEST_CHECKS),
+    (quest, "kth_score", _q_kth_all_kept_when_equal, pins.QUEST_CHECKS),
+    (quest, "kth_score_windowed", _q_kth_windowed_counts_kept, pins.QUEST_CHECKS),
+    (quest, "kth_score_windowed", _q_kth_windowed_off_by_one, pins.QUEST_CHECKS),
     (snapkv, "window_probabilities", _s_mask_off_by_one, pins.SNAPKV_CHECKS),
     (snapkv, "candidate_scores", _s_scores_include_window, pins.SNAPKV_CHECKS),
     (snapkv, "max_pool_clipped", _s_pool_right_only, pins.SNAPKV_CHECKS),
     (snapkv, "keep_positions", _s_keep_ties_high, pins.SNAPKV_CHECKS),
     (snapkv, "keep_positions_windowed", _s_windowed_recent_is_window, pins.SNAPKV_CHECKS),
+    (snapkv, "kth_pooled", _s_kth_off_by_one, pins.SNAPKV_CHECKS),
+    (snapkv, "kth_pooled", _s_kth_ascending, pins.SNAPKV_CHECKS),
+    (snapkv, "kth_pooled_windowed", _s_kth_windowed_counts_sink, pins.SNAPKV_CHECKS),
+    (snapkv, "kth_pooled_windowed", _s_kth_windowed_off_by_one, pins.SNAPKV_CHECKS),
 ]
 
 
