@@ -188,50 +188,94 @@ def _oracle_worker(args):
     decode step (append + score + select + attend) timed."""
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     import oracle.quest as oq
-    (k, v, n_tokens, H, D, Dv, q, k_new, v_new, topk, scale) = args
+    (k, v, n_tokens, H, D, Dv, q, k_new, v_new, topk, scale, sink, recent) = args
     import numpy as np
     req = oq.QuestRequest(k, v, np.arange(k.shape[0]), n_tokens, H, D, Dv, PAGE)
     t0 = time.perf_counter()
     if k_new is not None:
         req.append(k_new, v_new)
-    req.decode(q, topk, scale)
+    req.decode(q, topk, scale, sink_tokens=sink, recent_tokens=recent)
     return time.perf_counter() - t0
 
 
-def _sample_for_oracle(x, requests):
+def _sample_for_oracle(x, requests, sink=0, recent=0):
     items = []
     wl = x.workload
     for b in requests:
         n = x.pages_per_request[b]
         idx = x.block_table[b, :n].long()
         k = x.k_cache[idx].cpu().share_memory_()
-        v = x.v_cache[idx].cpu().share_memory_()
+        v = None if x.v_cache is None else x.v_cache[idx].cpu().share_memory_()
         items.append((k, v, x.seq_lens[b], wl.num_kv_heads, wl.head_dim, wl.head_dim_v, x.q[b].cpu(),
                       None if x.k_new is None else x.k_new[b].cpu(),
-                      None if x.v_new is None else x.v_new[b].cpu(), wl.topk_pages, 1.0 / math.sqrt(wl.head_dim)))
+                      None if x.v_new is None else x.v_new[b].cpu(), wl.topk_pages, 1.0 / math.sqrt(wl.head_dim),
+                      sink, recent))
     return items
 
 
-def cpu_oracle_throughput(x, n_requests=None, cores=None):
-    """tokens/s of the oracle over a sample of requests, one process per core (spawn)."""
+def _pool_times(worker, items, cores):
+    """Per-item single-core seconds of ``worker`` over ``items``, one process per core (spawn)."""
     import torch.multiprocessing as mp
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+    workers = min(cores, len(items))
+    with mp.get_context("spawn").Pool(workers) as pool:
+        return pool.map(worker, items), workers
+
+
+def cpu_oracle_throughput(x, n_requests=None, cores=None, sink=0, recent=0):
+    """tokens/s of the oracle over a sample of requests, one process per core (spawn)."""
     cores = cores or len(os.sched_getaffinity(0))
     wl = x.workload
     n_requests = n_requests or min(wl.batch, max(2, 2 * cores))
     reqs = list(range(n_requests))
-    items = _sample_for_oracle(x, reqs)
-    os.environ["OPENBLAS_NUM_THREADS"] = "1"
-    os.environ["OMP_NUM_THREADS"] = "1"
-    ctx = mp.get_context("spawn")
-    workers = min(cores, len(items))
-    with ctx.Pool(workers) as pool:
-        times = pool.map(_oracle_worker, items)
+    items = _sample_for_oracle(x, reqs, sink, recent)
+    times, workers = _pool_times(_oracle_worker, items, cores)
     busy = sum(times)  # seconds of single-core oracle work
     value = len(items) / (busy / workers)  # requests (= tokens) per second on `workers` cores
+    what = "append + score + select + attend" if x.k_new is not None else "score + select + attend"
     return {"value": value, "unit": UNIT, "cores": workers, "kind": "oracle",
             "sample": f"{len(items)} of the {wl.batch} requests (one decode token each; contexts "
-                      f"{[x.seq_lens[b] for b in reqs]}), append + score + select + attend timed per request, "
+                      f"{[x.seq_lens[b] for b in reqs]}), {what} timed per request, "
                       f"page summaries prebuilt untimed; {busy:.1f} s of single-core work"}
+
+
+def _snapkv_oracle_worker(args):
+    """One (request, KV head) pair of a SnapKV eviction through the fp64 oracle, timed:
+    window probabilities and row log-sum-exps, column scores, pooling, the kept positions,
+    then the kept K and V rows gathered."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import numpy as np
+    import oracle.snapkv as osk
+    (k, v, n, qg, W, pool, keep, scale, sink, recent) = args
+    t0 = time.perf_counter()
+    res = osk.snapkv_head(qg, k, np.arange(k.shape[0]), 0, n, W, pool, keep, scale, PAGE, sink=sink, recent=recent)
+    osk.compact_rows(k, np.arange(k.shape[0]), 0, res["kept"], PAGE)
+    osk.compact_rows(v, np.arange(k.shape[0]), 0, res["kept"], PAGE)
+    return time.perf_counter() - t0
+
+
+def snapkv_cpu_baseline(x, cores=None, n_pairs=None):
+    """Evictions (requests) per second of the oracle over a sample of (request, KV head) pairs."""
+    cores = cores or len(os.sched_getaffinity(0))
+    wl = x.workload
+    H, G = wl.num_kv_heads, wl.group
+    pairs = [(b, h) for b in range(wl.batch) for h in range(H)][:n_pairs or min(wl.batch * H, cores)]
+    items = []
+    for b, h in pairs:
+        n = x.prompt_lens[b]
+        idx = x.src_block_table[b, :x.src_pages_per_request[b]].long()
+        k = x.k_cache[idx][:, h:h + 1].cpu().share_memory_()
+        v = x.v_cache[idx][:, h:h + 1].cpu().share_memory_()
+        items.append((k, v, n, x.q_window[b, :, h * G:(h + 1) * G, :].cpu(), wl.window, wl.pool_kernel,
+                      wl.keep_topk, 1.0 / math.sqrt(wl.head_dim), wl.keep_sink, wl.recent))
+    times, workers = _pool_times(_snapkv_oracle_worker, items, cores)
+    busy = sum(times)
+    pairs_per_s = len(items) / (busy / workers)
+    return {"value": pairs_per_s / H, "unit": "requests/s", "cores": workers, "kind": "oracle",
+            "sample": f"{len(items)} of the {wl.batch * H} (request, KV head) pairs ({wl.batch} prompts of "
+                      f"{x.prompt_lens[0]} tokens): scores, pooling, selection and the gather of the kept rows "
+                      f"timed per pair, requests/s = pairs/s / {H} KV heads; {busy:.1f} s of single-core work"}
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -354,12 +398,15 @@ def run_ours(args, rank, world, local_rank):
     }
     if rank == 0 and not args.no_extra:
         result["extra_workloads"] = {
+            "qwen3_30b_a3b_quest_b32_128k_fixed": _fixed_128k_extra(args, dev, flush, stream),
             "snapkv_prefill_b4_32k": _snapkv_extra(args, dev, flush, stream),
             "snapkv_aime_b4_32k": _snapkv_extra(args, dev, flush, stream, _snapkv_wl("SNAPKV_AIME_32K")),
             "snapkv_agent_b4_32k": _snapkv_extra(args, dev, flush, stream, _snapkv_wl("SNAPKV_AGENT_32K")),
             "snapkv_periodic_evict_aime_b4": _periodic_evict_extra(args, dev, flush, stream),
-            "tiny_quest_b1_g4_4k": _quest_extra(args, dev, flush, stream, _snapkv_wl("TINY_QUEST_4K")),
-            "qwen3_4b_quest_b8_32k": _quest_extra(args, dev, flush, stream, _snapkv_wl("QWEN3_4B_QUEST_32K")),
+            "tiny_quest_b1_g4_4k": _quest_extra(args, dev, flush, stream, _snapkv_wl("TINY_QUEST_4K"),
+                                                cpu_requests=1),
+            "qwen3_4b_quest_b8_32k": _quest_extra(args, dev, flush, stream, _snapkv_wl("QWEN3_4B_QUEST_32K"),
+                                                  cpu_requests=8),
             "tiny_quest_b1_g4_4k_fused": _quest_extra(args, dev, flush, stream, _snapkv_wl("TINY_QUEST_4K"),
                                                       fused=True),
             "qwen3_4b_quest_b8_32k_fused": _quest_extra(args, dev, flush, stream, _snapkv_wl("QWEN3_4B_QUEST_32K"),
@@ -391,7 +438,7 @@ def _profile_traffic(kernel):
         return None
 
 
-def _snapkv_extra(args, dev, flush, stream, wl=None):
+def _snapkv_extra(args, dev, flush, stream, wl=None, cpu_baseline=True):
     """SnapKV eviction at the end of a 32K prefill (4 requests, 32 q / 8 kv heads): one
     se_snapkv_score_and_compact_windowed call per step (window scores on the tensor cores,
     pool + top-k with the workload's keep windows, compaction), timed with events; L2
@@ -441,7 +488,13 @@ def _snapkv_extra(args, dev, flush, stream, wl=None):
         peak_tf = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
     except Exception:
         peak_tf = 1900.0
-    return {"ms_per_call": ms, "steps": n, "requests_per_s": B / (ms * 1e-3),
+    cpu = None
+    if cpu_baseline and not args.no_cpu_baseline:
+        try:
+            cpu = snapkv_cpu_baseline(x, cores=args.cpu_cores)
+        except Exception as exc:  # reported, never silently replaced
+            cpu = {"error": repr(exc)}
+    return {"ms_per_call": ms, "steps": n, "requests_per_s": B / (ms * 1e-3), "cpu_baseline": cpu,
             "settings": {"window": W, "pool_kernel": wl.pool_kernel, "sink": wl.keep_sink, "recent": wl.recent,
                          "selected": wl.keep_topk, "kept_per_pair": int(cnt[0, 0].item())},
             "keys_read_bytes_per_pass": kbytes, "gather_bytes": gather,
@@ -450,7 +503,7 @@ def _snapkv_extra(args, dev, flush, stream, wl=None):
             "tensor_frac_of_measured_bf16": round(flops / (ms * 1e-3) / 1e12 / peak_tf, 4)}
 
 
-def _quest_extra(args, dev, flush, stream, wl, sink=0, recent=0, fused=False):
+def _quest_extra(args, dev, flush, stream, wl, sink=0, recent=0, fused=False, cpu_requests=None):
     """One Quest decode step of workload ``wl`` (append if the workload appends, score, top-k
     with the keep windows ``sink``/``recent``, decode), captured in a CUDA graph and replayed
     (L2 flushed between replays); per-kernel spans from an eager pass. ``fused``: the step as
@@ -529,7 +582,14 @@ def _quest_extra(args, dev, flush, stream, wl, sink=0, recent=0, fused=False):
     flops = 2 * int(step.counts.sum().item()) * PAGE * G * (wl.head_dim + wl.head_dim_v)
     dk = "fused_step" if fused else "decode"
     kern[dk]["tflops"] = round(flops / (spans[dk] * 1e-3) / 1e12, 1)
-    return {"ms_per_step": ms, "steps": n, "tokens_per_s": wl.batch / (ms * 1e-3),
+    cpu = None
+    if cpu_requests and not args.no_cpu_baseline:
+        try:
+            cpu = cpu_oracle_throughput(x, n_requests=min(wl.batch, cpu_requests), cores=args.cpu_cores, sink=sink,
+                                        recent=recent)
+        except Exception as exc:  # reported, never silently replaced
+            cpu = {"error": repr(exc)}
+    return {"ms_per_step": ms, "steps": n, "tokens_per_s": wl.batch / (ms * 1e-3), "cpu_baseline": cpu,
             "step_gbs": round(step_bytes / (ms * 1e-3) / 1e9, 1),
             "step_frac_of_measured_hbm": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4), "kernels": kern,
             "kept_pages_per_kv_head": round(float(step.counts.float().mean().item()), 2),
@@ -546,14 +606,24 @@ def _mla_extra(args, dev, flush, stream):
     budget."""
     from synth import MLA_GLM_QUEST_32K
     wl = MLA_GLM_QUEST_32K if _BATCH_OVERRIDE is None else MLA_GLM_QUEST_32K.scaled(batch=_BATCH_OVERRIDE)
-    return _quest_extra(args, dev, flush, stream, wl)
+    return _quest_extra(args, dev, flush, stream, wl, cpu_requests=16)
 
 
 def _windows_extra(args, dev, flush, stream):
     """The 128K workload with the decode-time keep windows of the throughput runs: sink 64,
     recent 512, 1,472 selected tokens (92 pages), 2,048 kept in total."""
     from synth import QWEN3_30B_A3B_QUEST_128K
-    return _quest_extra(args, dev, flush, stream, QWEN3_30B_A3B_QUEST_128K.scaled(topk_pages=92), 64, 512)
+    return _quest_extra(args, dev, flush, stream, QWEN3_30B_A3B_QUEST_128K.scaled(topk_pages=92), 64, 512,
+                        cpu_requests=16)
+
+
+def _fixed_128k_extra(args, dev, flush, stream):
+    """The 128K workload with every request at exactly 131,072 tokens after the append
+    (131,071 before it): 8,192 pages per request, 8,191 candidates per KV head."""
+    from synth import QWEN3_30B_A3B_QUEST_128K
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(name="qwen3_30b_a3b_quest_b32_128k_fixed", context_min=131071,
+                                         context_max=131071)
+    return _quest_extra(args, dev, flush, stream, wl, cpu_requests=16)
 
 
 def _periodic_evict_extra(args, dev, flush, stream):
@@ -565,7 +635,8 @@ def _periodic_evict_extra(args, dev, flush, stream):
     period = 1024
     n = SNAPKV_AIME_32K.keep_sink + SNAPKV_AIME_32K.keep_topk + SNAPKV_AIME_32K.recent + period
     r = _snapkv_extra(args, dev, flush, stream,
-                      SNAPKV_AIME_32K.scaled(name="snapkv_periodic_aime_b4", prompt_min=n, prompt_max=n))
+                      SNAPKV_AIME_32K.scaled(name="snapkv_periodic_aime_b4", prompt_min=n, prompt_max=n),
+                      cpu_baseline=False)
     r["period_decode_steps"] = period
     r["positions_before_eviction"] = n
     r["amortized_us_per_decode_step"] = round(r["ms_per_call"] * 1e3 / period, 4)
@@ -617,14 +688,24 @@ def _e2e(args, step, x, before, after, stream, flush, dev):
     torch.cuda.synchronize()
     n = max(10, args.steps // 4)
     pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    host_ms = []
     for i in range(n):
         with torch.cuda.stream(stream):
             flush(float(i))
+        stream.synchronize()  # the flush is done before the clock starts
+        t0 = time.perf_counter()
         e2e_step(*pairs[i])
+        stream.synchronize()  # the output is in host memory
+        host_ms.append((time.perf_counter() - t0) * 1e3)
     torch.cuda.synchronize()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    ms = statistics.mean(host_ms)
+    stream_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
     return {"value": wl.batch / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": n,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "timing": "host wall clock per step: from before the host-to-device copy is enqueued to the return of "
+                      "a stream synchronize after the device-to-host copy of the output (argument marshalling, "
+                      "launches, copies and kernels included; the L2 flush before it excluded)",
+            "stream_ms_per_step": stream_ms,
             "path": "pinned host q/k_new/v_new/lengths (one packed buffer, one copy) -> device, the four C-ABI "
                     "calls, output -> pinned host"}
 
@@ -676,6 +757,8 @@ def main():
     _BATCH_OVERRIDE = args.batch
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.snapkv_only or args.mla_only:
+        args.no_cpu_baseline = True
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -689,7 +772,7 @@ def main():
         flush = L2Flush(dev)
         from synth import SNAPKV_PREFILL_32K
         wl = SNAPKV_PREFILL_32K if args.batch is None else SNAPKV_PREFILL_32K.scaled(batch=args.batch)
-        print(json.dumps({wl.name: _snapkv_extra(args, dev, flush, torch.cuda.Stream(dev), wl)}))
+        print(json.dumps({wl.name: _snapkv_extra(args, dev, flush, torch.cuda.Stream(dev), wl, cpu_baseline=False)}))
         return
     if args.mla_only:  # profiler captures of the latent-cache kernels alone (never the reported metric)
         import torch

@@ -61,7 +61,7 @@ typedef enum {
 /* Bits of the device error word. */
 #define SE_DEVERR_PAGE_RANGE   0x1u  /* a block-table entry outside [0, num_pages) */
 #define SE_DEVERR_LENGTH       0x2u  /* a length or selected-page id outside its declared bound */
-#define SE_DEVERR_WAIT_TIMEOUT 0x4u  /* a bounded wait on an mbarrier gave up */
+#define SE_DEVERR_WAIT_TIMEOUT 0x4u  /* a bounded wait (an mbarrier, or another CTA's counter) gave up */
 
 /*
  * Paged KV cache view. Physical page p of KV head h holds tokens in slots
@@ -302,6 +302,11 @@ SE_API se_status_t se_quest_fused_step(const se_paged_kv_t* kv, const void* k_ne
  * A request with no selected page writes out = 0 and lse = -inf. The pages of
  * one (request, KV head) are split across CTAs and the partial results merged
  * by log-sum-exp in `workspace` (size from se_sparse_decode_workspace_size).
+ * The workspace must be zero-filled before its first use (one cudaMemset after
+ * allocating it): for head_dim 128 it holds per-item arrival counters that the
+ * CTA publishing an item's last partial reads and resets, so every call leaves
+ * them zero for the next one; the rest is overwritten by each call. Calls that
+ * share a workspace must not overlap on the GPU.
  *   q: bf16 [batch][num_q_heads][head_dim]; out: bf16 [batch][num_q_heads][head_dim_v];
  *   out_lse: fp32 [batch][num_q_heads] or NULL.
  * Shapes: head_dim == head_dim_v == 128 with 1..16 query heads per KV head, or a
@@ -313,8 +318,9 @@ SE_API se_status_t se_quest_fused_step(const se_paged_kv_t* kv, const void* k_ne
  * current device for these sizes. The selected pages of all (request, KV head)
  * items are cut into equal slices of at least *pages_per_split pages, one per
  * CTA; *nsplit is the most slices one item can span (the partial results kept
- * per query-head row), and *launches the kernels per call (the decode kernel
- * and the log-sum-exp merge). Host only.
+ * per query-head row), and *launches the kernels per call: 1 for head_dim 128
+ * (the decode kernel merges the split partials itself), 2 for a latent cache
+ * (the decode kernel and the log-sum-exp merge). Host only.
  */
 SE_API se_status_t se_sparse_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t head_dim_v, int32_t sel_stride,
@@ -417,6 +423,19 @@ SE_API se_status_t se_snapkv_score_and_compact_windowed(const se_paged_kv_t* src
                                                         size_t workspace_bytes, void* stream);
 
 /*
+ * se_debug_snapkv_wait_probe -- test hook for the bounded waits; it computes
+ * nothing (the pages have no counterpart). In the next se_snapkv_window_scores
+ * call issued from this host thread (also inside se_snapkv_score_and_compact*),
+ * the first score kernel's MMA-issuing thread of every CTA first waits on an
+ * mbarrier phase that nothing completes, and gives up after limit_us
+ * microseconds (1 .. 1000000). The kernel then sets SE_DEVERR_WAIT_TIMEOUT in
+ * the device error word and issues no tensor-core work for the rest of that
+ * launch; its copies still drain and it frees its tensor memory, so the context
+ * stays usable. The call's scores are not valid. Later calls are unaffected.
+ */
+SE_API se_status_t se_debug_snapkv_wait_probe(uint32_t limit_us);
+
+/*
  * se_sparse_paged_decode_noalloc -- se_sparse_paged_decode for callers that
  * cannot allocate device memory. The SparseEngine pages have no counterpart: this
  * is a deployment variant of the decode above.
@@ -424,21 +443,27 @@ SE_API se_status_t se_snapkv_score_and_compact_windowed(const se_paged_kv_t* src
  * inference runtime that receives only its inputs and outputs, a process whose
  * device memory is owned by another framework's caching allocator, or a serving
  * loop that forbids cudaMalloc after start-up because it can synchronise the
- * device. This call computes exactly what se_sparse_paged_decode computes, with
- * the same arguments minus the workspace, and keeps the split partials in a
- * fixed 8 MiB array inside the library (held on every GPU that loads the
- * library until the process exits). It calls no cudaMalloc, cudaFree or other
- * allocating routine.
+ * device. For head_dim = head_dim_v = 128 with up to 16 query heads per KV
+ * head, this call computes what se_sparse_paged_decode computes, with the same
+ * arguments minus the workspace, and keeps the split partials in a fixed 8 MiB
+ * array inside the library (held on every GPU that loads the library until the
+ * process exits). A latent cache (576/512) is rejected with SE_ERR_UNSUPPORTED:
+ * it needs se_sparse_paged_decode with a caller workspace. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
  *  - The first call on a device looks up the array's device address, with that
- *    device current; make that first call before any stream capture.
+ *    device current; make that first call before any stream capture. The address
+ *    is kept for the life of the process: after cudaDeviceReset, do not call the
+ *    library on that device again.
  *  - Sizes whose partials exceed 8 MiB are rejected with SE_ERR_WORKSPACE
  *    (use se_sparse_paged_decode with a workspace instead); the bound is
- *    batch * num_q_heads * splits * (head_dim_v + 1) * 4 bytes, splits from
- *    se_sparse_decode_plan.
+ *    batch * num_q_heads * splits * (head_dim_v + 1) * 4 bytes plus
+ *    batch * num_q_heads * 4, splits from se_sparse_decode_plan.
  *  - All calls on a device share the array and it keeps the last call's
- *    contents (every partial read is first written by the same call, so nothing
- *    needs clearing). Two calls that overlap on the GPU race on the array: order
- *    them on one stream or with events.
+ *    contents. Every partial read is first written by the same call; the
+ *    split-merge counters, which must start at zero, are cleared by each call
+ *    with an asynchronous memset on `stream` before its launch. Two calls that
+ *    overlap on the GPU race on the array: order them on one stream or with
+ *    events.
  */
 SE_API se_status_t se_sparse_paged_decode_noalloc(const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
                                                   const int32_t* block_table, int32_t bt_stride,

@@ -27,7 +27,7 @@ __all__ = [
     "se_sparse_decode_workspace_size", "se_sparse_decode_plan", "se_sparse_paged_decode",
     "se_sparse_paged_decode_noalloc", "se_snapkv_workspace_size", "se_snapkv_window_scores", "se_snapkv_select",
     "se_snapkv_compact", "se_snapkv_score_and_compact", "se_snapkv_select_windowed",
-    "se_snapkv_score_and_compact_windowed", "exported_symbols",
+    "se_snapkv_score_and_compact_windowed", "se_debug_snapkv_wait_probe", "exported_symbols",
 ]
 
 SE_OK = 0
@@ -85,6 +85,7 @@ _SIGNATURES = {
     "se_snapkv_workspace_size": (_Z, [_I, _I, _I, _I]),
     "se_snapkv_window_scores": (ctypes.c_int, [_KV, _P, _I, _I, _P, _I, _P, _I, _I, _F, _P, _I, _P, _P, _Z, _P]),
     "se_snapkv_select": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
+    "se_debug_snapkv_wait_probe": (ctypes.c_int, [ctypes.c_uint32]),
     "se_snapkv_select_windowed": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
     "se_snapkv_compact": (ctypes.c_int, [_KV, _P, _I, _P, _I, _KV, _P, _I, _P, _I, _P, _P]),
     "se_snapkv_score_and_compact": (ctypes.c_int, [_KV, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _F, _KV, _P, _I, _P,
@@ -335,6 +336,12 @@ def se_sparse_paged_decode_noalloc(kv: SEPagedKV, q, block_table, seq_lens, sel_
 # ---------------------------------------------------------------- SnapKV
 def se_snapkv_workspace_size(batch: int, num_kv_heads: int, window: int, max_prompt_len: int) -> int:
     return int(load_library().se_snapkv_workspace_size(batch, num_kv_heads, window, max_prompt_len))
+
+
+def se_debug_snapkv_wait_probe(limit_us: int):
+    """Test hook: the next SnapKV window-score launch of this thread waits for a count that
+    no CTA reaches and gives up after ``limit_us`` (see the C header)."""
+    _check(load_library().se_debug_snapkv_wait_probe(int(limit_us)))
 
 
 def se_snapkv_window_scores(src: SEPagedKV, q_window, block_table, prompt_lens, max_prompt_len: int, sm_scale: float,

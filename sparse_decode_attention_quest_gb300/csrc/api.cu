@@ -88,6 +88,22 @@ bool encode_page_map(CUtensorMap* map, const void* base, long long rows, int wid
   return r == CUDA_SUCCESS;
 }
 
+// 4-D view of SnapKV window queries bf16 [batch][window][num_q_heads][128]: boxes of
+// 64 dims x `group` heads x `window` positions x 1 request (128-byte swizzle), so one
+// box holds a KV head's window rows r = w * group + g for 64 of the dims.
+bool encode_window_map(CUtensorMap* map, const void* base, int batch, int window, int num_q_heads, int group) {
+  auto fn = encode_tiled();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {128, (cuuint64_t)num_q_heads, (cuuint64_t)window, (cuuint64_t)batch};
+  cuuint64_t strides[3] = {128 * 2, (cuuint64_t)num_q_heads * 128 * 2, (cuuint64_t)window * num_q_heads * 128 * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)group, (cuuint32_t)window, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int pages_of(long long tokens) { return (int)((tokens + se::kPageSize - 1) / se::kPageSize); }
@@ -418,7 +434,7 @@ se_status_t se_sparse_decode_plan(int32_t batch, int32_t num_q_heads, int32_t nu
                                   : se::plan_gqa_decode(batch, num_kv_heads, sel_stride, d->sm_count);
   *nsplit = plan.nsplit;
   *pages_per_split = plan.pages_per_split;
-  *launches = batch == 0 ? 0 : 2;  // the decode kernel and the split merge
+  *launches = batch == 0 ? 0 : (mla ? 2 : 1);  // latent: the decode kernel and the split merge
   return SE_OK;
 }
 
@@ -439,25 +455,11 @@ se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32
                                    int32_t sel_stride, float sm_scale, void* out, float* out_lse,
                                    void* workspace, size_t workspace_bytes, void* stream) {
   static const char* fn = "se_sparse_paged_decode";
-  se_status_t st = check_kv(fn, kv, false);
+  bool mla = false;
+  se_status_t st = se::check_decode_call(fn, kv, q, num_q_heads, block_table, bt_stride, seq_lens, batch, sel_pages,
+                                         sel_counts, sel_stride, sm_scale, out, out_lse, &mla);
   if (st != SE_OK) return st;
-  if (batch < 0) return fail(SE_ERR_INVALID_ARG, fn, "batch < 0");
-  if (num_q_heads < 1 || num_q_heads % kv->num_kv_heads)
-    return fail(SE_ERR_INVALID_ARG, fn, "num_q_heads must be a positive multiple of num_kv_heads");
-  if (sel_stride < 1 || bt_stride < 1) return fail(SE_ERR_INVALID_ARG, fn, "sel_stride/bt_stride < 1");
-  if (batch > 0 && (!q || !block_table || !seq_lens || !sel_pages || !sel_counts || !out))
-    return fail(SE_ERR_INVALID_ARG, fn, "NULL pointer");
-  if (!aligned16(q) || !aligned16(out) || !aligned16(out_lse) || !aligned16(workspace) || !aligned16(sel_pages))
-    return fail(SE_ERR_INVALID_ARG, fn, "pointers must be 16-byte aligned");
-  if (!std::isfinite(sm_scale)) return fail(SE_ERR_INVALID_ARG, fn, "sm_scale not finite");
-  const int group = num_q_heads / kv->num_kv_heads;
-  const bool gqa = kv->head_dim == 128 && kv->head_dim_v == 128 && group <= 16;
-  const bool mla = se::mla_decode_supported(kv->num_kv_heads, kv->head_dim, kv->head_dim_v, num_q_heads);
-  if (!gqa && !mla)
-    return fail(SE_ERR_UNSUPPORTED, fn,
-                "head_dim = head_dim_v = 128 with <= 16 query heads per KV head, or a latent cache (576/512, one "
-                "KV head, 16..64 query heads in multiples of 16)");
-  if (mla && kv->v != kv->k) return fail(SE_ERR_INVALID_ARG, fn, "a latent cache needs kv->v == kv->k");
+  if (!aligned16(workspace)) return fail(SE_ERR_INVALID_ARG, fn, "workspace must be 16-byte aligned");
   DeviceInfo* d = nullptr;
   cudaError_t e = current_device(&d);
   if (e != cudaSuccess) return cuda_fail(fn, e);
@@ -553,15 +555,23 @@ se_status_t se_snapkv_window_scores(const se_paged_kv_t* src, const void* q_wind
   DeviceInfo* d = nullptr;
   cudaError_t e = current_device(&d);
   if (e != cudaSuccess) return cuda_fail(fn, e);
-  CUtensorMap kmap;
+  CUtensorMap kmap, qmap;
   const long long rows = (long long)src->num_pages * src->num_kv_heads * se::kPageSize;
-  if (!encode_page_map(&kmap, src->k, rows > 0 ? rows : 1, src->head_dim, src->row_stride_k))
+  if (!encode_page_map(&kmap, src->k, rows > 0 ? rows : 1, src->head_dim, src->row_stride_k) ||
+      !encode_window_map(&qmap, q_window, batch, window, num_q_heads, num_q_heads / src->num_kv_heads))
     return fail(SE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
-  e = se::launch_snapkv_scores(kmap, view_of(src), static_cast<const uint16_t*>(q_window), num_q_heads, window,
+  e = se::launch_snapkv_scores(kmap, qmap, view_of(src), static_cast<const uint16_t*>(q_window), num_q_heads, window,
                                block_table, bt_stride, prompt_lens, batch, max_prompt_len, sm_scale, scores,
                                score_stride, row_lse, workspace, d->sm_count, d->err,
                                static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SE_OK : cuda_fail(fn, e);
+}
+
+se_status_t se_debug_snapkv_wait_probe(uint32_t limit_us) {
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(SE_ERR_INVALID_ARG, "se_debug_snapkv_wait_probe", "limit_us must be in 1 .. 1000000");
+  se::set_snapkv_wait_probe(limit_us);
+  return SE_OK;
 }
 
 se_status_t se_snapkv_select_windowed(const float* scores, int32_t score_stride, const int32_t* prompt_lens,
@@ -689,5 +699,32 @@ cudaError_t device_context(int* sm_count, unsigned** err) {
 
 
 void set_error_detail(const char* fn, const char* what) { fail(SE_OK, fn, what); }
+
+se_status_t check_decode_call(const char* fn, const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                              const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens, int32_t batch,
+                              const int32_t* sel_pages, const int32_t* sel_counts, int32_t sel_stride,
+                              float sm_scale, const void* out, const float* out_lse, bool* latent) {
+  se_status_t st = check_kv(fn, kv, false);
+  if (st != SE_OK) return st;
+  if (batch < 0) return fail(SE_ERR_INVALID_ARG, fn, "batch < 0");
+  if (num_q_heads < 1 || num_q_heads % kv->num_kv_heads)
+    return fail(SE_ERR_INVALID_ARG, fn, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (sel_stride < 1 || bt_stride < 1) return fail(SE_ERR_INVALID_ARG, fn, "sel_stride/bt_stride < 1");
+  if (batch > 0 && (!q || !block_table || !seq_lens || !sel_pages || !sel_counts || !out))
+    return fail(SE_ERR_INVALID_ARG, fn, "NULL pointer");
+  if (!aligned16(q) || !aligned16(out) || !aligned16(out_lse) || !aligned16(sel_pages))
+    return fail(SE_ERR_INVALID_ARG, fn, "pointers must be 16-byte aligned");
+  if (!std::isfinite(sm_scale)) return fail(SE_ERR_INVALID_ARG, fn, "sm_scale not finite");
+  const int group = num_q_heads / kv->num_kv_heads;
+  const bool gqa = kv->head_dim == 128 && kv->head_dim_v == 128 && group <= 16;
+  const bool mla = mla_decode_supported(kv->num_kv_heads, kv->head_dim, kv->head_dim_v, num_q_heads);
+  if (!gqa && !mla)
+    return fail(SE_ERR_UNSUPPORTED, fn,
+                "head_dim = head_dim_v = 128 with <= 16 query heads per KV head, or a latent cache (576/512, one "
+                "KV head, 16..64 query heads in multiples of 16)");
+  if (mla && kv->v != kv->k) return fail(SE_ERR_INVALID_ARG, fn, "a latent cache needs kv->v == kv->k");
+  *latent = mla;
+  return SE_OK;
+}
 
 }  // namespace se

@@ -14,10 +14,14 @@
 // Every GPU that loads the library holds it until the process exits. Its device
 // address is looked up once per device, by the first call made on that device
 // (with that device current); make that first call before any stream capture.
-// All calls on a device share the array and it keeps the last call's contents:
-// the decode writes every partial it later reads, so nothing needs clearing,
-// but two calls that overlap on the GPU (different streams, no ordering) race
-// on it and both results are undefined.
+// All calls on a device share the array and it keeps the last call's contents.
+// The decode writes every partial it later reads; its per-item arrival counters
+// must start at zero, so each call clears them (an asynchronous memset on the
+// caller's stream, no allocation) before its launch. Two calls that overlap on
+// the GPU (different streams, no ordering) race on the array and both results
+// are undefined. The looked-up address stays valid for the life of the device's
+// primary context: after cudaDeviceReset the library must not be called on that
+// device again in the same process.
 #include <mutex>
 
 #include "se_internal.h"
@@ -52,8 +56,6 @@ cudaError_t scratch_address(void** out) {
   return cudaSuccess;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 se_status_t reject(se_status_t st, const char* what) {
   se::set_error_detail("se_sparse_paged_decode_noalloc", what);
   return st;
@@ -67,26 +69,14 @@ extern "C" se_status_t se_sparse_paged_decode_noalloc(const se_paged_kv_t* kv, c
                                                       const int32_t* sel_pages, const int32_t* sel_counts,
                                                       int32_t sel_stride, float sm_scale, void* out, float* out_lse,
                                                       void* stream) {
-  if (!kv || !kv->k || !kv->v) return reject(SE_ERR_INVALID_ARG, "kv, kv->k or kv->v is NULL");
-  if (!aligned16(kv->k) || !aligned16(kv->v)) return reject(SE_ERR_INVALID_ARG, "cache not 16-byte aligned");
-  if (kv->page_size != se::kPageSize || kv->num_pages < 0 || kv->num_kv_heads < 1)
-    return reject(SE_ERR_INVALID_ARG, "bad page_size / num_pages / num_kv_heads");
-  if (kv->row_stride_k < kv->head_dim || kv->row_stride_v < kv->head_dim_v || (kv->row_stride_k % 8) ||
-      (kv->row_stride_v % 8))
-    return reject(SE_ERR_INVALID_ARG, "row strides must cover the head dims and be multiples of 8");
-  if ((long long)kv->num_pages * kv->num_kv_heads * se::kPageSize >= (1ll << 31))
-    return reject(SE_ERR_UNSUPPORTED, "cache holds 2^31 or more token rows");
-  if (batch < 0 || sel_stride < 1 || bt_stride < 1) return reject(SE_ERR_INVALID_ARG, "bad sizes");
-  if (num_q_heads < 1 || num_q_heads % kv->num_kv_heads)
-    return reject(SE_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
-  if (batch > 0 && (!q || !block_table || !seq_lens || !sel_pages || !sel_counts || !out))
-    return reject(SE_ERR_INVALID_ARG, "NULL pointer");
-  if (!aligned16(q) || !aligned16(out) || !aligned16(out_lse) || !aligned16(sel_pages))
-    return reject(SE_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-  if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
-    return reject(SE_ERR_INVALID_ARG, "sm_scale not finite");
-  if (!(kv->head_dim == 128 && kv->head_dim_v == 128 && num_q_heads / kv->num_kv_heads <= 16))
-    return reject(SE_ERR_UNSUPPORTED, "only head_dim = head_dim_v = 128 with <= 16 query heads per KV head");
+  bool latent = false;
+  const se_status_t st = se::check_decode_call("se_sparse_paged_decode_noalloc", kv, q, num_q_heads, block_table,
+                                               bt_stride, seq_lens, batch, sel_pages, sel_counts, sel_stride,
+                                               sm_scale, out, out_lse, &latent);
+  if (st != SE_OK) return st;
+  if (latent)
+    return reject(SE_ERR_UNSUPPORTED, "a latent cache needs se_sparse_paged_decode with a caller workspace; this "
+                                      "entry covers head_dim = head_dim_v = 128 with <= 16 query heads per KV head");
 
   int sm_count = 0;
   unsigned* err = nullptr;
@@ -97,9 +87,17 @@ extern "C" se_status_t se_sparse_paged_decode_noalloc(const se_paged_kv_t* kv, c
   if (need > kNoAllocScratchBytes)
     return reject(SE_ERR_WORKSPACE, "these sizes need more split scratch than the built-in 8 MiB array; "
                                     "use se_sparse_paged_decode with a caller workspace");
+  if ((size_t)batch * kv->num_kv_heads > se::gqa_decode_max_items())
+    return reject(SE_ERR_UNSUPPORTED, "too many (request, KV head) items for one launch");
   if (batch == 0) return SE_OK;
   void* scratch = nullptr;
   e = scratch_address(&scratch);
+  if (e != cudaSuccess) return reject(SE_ERR_CUDA, cudaGetErrorString(e));
+
+  // The arrival counters of the split merge start at zero on every call.
+  const size_t counters = se::gqa_decode_arrivals_offset(batch, num_q_heads, kv->head_dim_v, plan);
+  e = cudaMemsetAsync(static_cast<unsigned char*>(scratch) + counters, 0,
+                      (size_t)batch * kv->num_kv_heads * sizeof(uint32_t), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return reject(SE_ERR_CUDA, cudaGetErrorString(e));
 
   se::KvView view;
@@ -112,8 +110,6 @@ extern "C" se_status_t se_sparse_paged_decode_noalloc(const se_paged_kv_t* kv, c
   view.head_dim_v = kv->head_dim_v;
   view.row_stride_k = kv->row_stride_k;
   view.row_stride_v = kv->row_stride_v;
-  if ((size_t)batch * kv->num_kv_heads > se::gqa_decode_max_items())
-    return reject(SE_ERR_UNSUPPORTED, "too many (request, KV head) items for one launch");
   e = se::launch_gqa_decode(view, static_cast<const uint16_t*>(q), num_q_heads, block_table, bt_stride, seq_lens,
                             batch, sel_pages, sel_counts, sel_stride, sm_scale, static_cast<uint16_t*>(out), out_lse,
                             scratch, plan, err, static_cast<cudaStream_t>(stream));

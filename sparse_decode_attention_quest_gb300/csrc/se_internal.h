@@ -89,6 +89,9 @@ struct DecodePlan {
 };
 DecodePlan plan_gqa_decode(int32_t batch, int32_t num_kv_heads, int32_t sel_stride, int sm_count);
 size_t gqa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim_v, const DecodePlan& plan);
+// Byte offset in the workspace of the per-item arrival counters (batch x KV heads
+// uint32, zero between calls: every call leaves them as it found them).
+size_t gqa_decode_arrivals_offset(int32_t batch, int32_t num_q_heads, int32_t head_dim_v, const DecodePlan& plan);
 size_t gqa_decode_max_items();
 cudaError_t launch_gqa_decode(const KvView& kv, const uint16_t* q, int32_t num_q_heads, const int32_t* block_table,
                               int32_t bt_stride, const int32_t* seq_lens, int32_t batch, const int32_t* sel_pages,
@@ -125,10 +128,16 @@ cudaError_t launch_quest_fused(const KvView& kv, uint16_t* k_mut, uint16_t* v_mu
 int snapkv_max_slices(int max_len);
 size_t snapkv_part_bytes(int pairs, int max_len);
 int snapkv_select_max_candidates();
-cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const KvView& kv, const uint16_t* qwin, int32_t num_q_heads,
+// kmap: the key cache as rows of 128 bf16, boxes of 64 x 16; qmap: the window
+// queries as [B][W][Hq][128], boxes of 64 dims x G heads x W positions x 1
+// (both 128-byte swizzle).
+cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const CUtensorMap& qmap, const KvView& kv, const uint16_t* qwin,
+                                 int32_t num_q_heads,
                                  int32_t window, const int32_t* bt, int32_t bt_stride, const int32_t* lens,
                                  int32_t batch, int32_t max_len, float sm_scale, float* scores, int32_t score_stride,
                                  float* row_lse, void* part_ws, int sm_count, unsigned* err, cudaStream_t stream);
+// The next launch_snapkv_scores of this host thread runs as a wait probe (limit in us).
+void set_snapkv_wait_probe(uint32_t limit_us);
 // Keeps positions 0 .. sink - 1 and n - recent .. n - 1 (recent >= window) and the keep best
 // pooled candidates between them.
 cudaError_t launch_snapkv_select(const float* scores, int32_t score_stride, const int32_t* lens, int32_t batch,
@@ -143,5 +152,11 @@ cudaError_t launch_snapkv_gather(const KvView& src, uint16_t* dk, uint16_t* dv, 
 // ---- api.cu: per-device context and helpers shared with other entry points
 cudaError_t device_context(int* sm_count, unsigned** err);
 void set_error_detail(const char* fn, const char* what);
+// Argument checks of a sparse paged decode call (everything but the workspace),
+// before any launch; *latent tells which kernel serves the shape.
+se_status_t check_decode_call(const char* fn, const se_paged_kv_t* kv, const void* q, int32_t num_q_heads,
+                              const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens, int32_t batch,
+                              const int32_t* sel_pages, const int32_t* sel_counts, int32_t sel_stride,
+                              float sm_scale, const void* out, const float* out_lse, bool* latent);
 
 }  // namespace se

@@ -14,22 +14,43 @@
 //
 // The logits are the one dense contraction of the path: 128 query rows x 128
 // keys x 128 dims per tile, on the 5th-generation tensor cores. Warp roles:
-//   warp 0      TMA producer: the 8 pages of a 128-key tile, two 64-column
-//               boxes each with 128-byte swizzle, into a 4-stage ring;
+//   warp 0      TMA producer: per segment the pair's window queries (two 4-D
+//               boxes), then the 8 pages of each 128-key tile (two 64-column
+//               boxes each, 128-byte swizzle) into a 4-stage ring;
 //   warp 1      allocates 256 TMEM columns (two fp32 128x128 accumulators)
 //               and issues the tcgen05.mma (M 128, N 128, K 16) x 8 per tile;
-//   warps 2-9   epilogue, two warps per TMEM lane quarter: a thread owns query
-//               row r (TMEM lane r) and 64 of the tile's 128 columns; it applies
-//               the causal mask (boundary tiles only) and the online max/sum
-//               (pass 1) or exp(z - LSE) (pass 2). Pass 2 sums the columns with
-//               a warp transpose-reduce and a fixed-order merge of the four lane
-//               quarters through shared memory (deterministic).
-// The tiles of all (request, KV head) pairs form one flattened range; every
-// CTA takes an equal slice. Pass 1 writes per-slice partial (max, sum) per row
-// that pass 2 merges.
+//   warps 2-9   epilogue, two warps per TMEM lane quarter, each thread with 64
+//               of the tile's 128 accumulator columns.
+// Pass 1 computes S = Q K^T: TMEM lane = query row, so a thread keeps its
+// row's running max and sum (causal mask on the last tiles only). Pass 2
+// computes S^T = K Q^T: TMEM lane = key, so a thread sums exp(z - LSE) over
+// its 64 query rows and the two halves meet in shared memory; no shuffles.
+// Element-wise work runs on paired fp32 instructions (f32x2 fma / add).
+//
+// The (request, KV head) pairs are cut into chunks (at most 2,048 pairs, and
+// about SE_SNAPKV_CHUNK_BYTES of keys), and the passes run chunk by chunk:
+// pass 1 of chunk c, pass 2 of chunk c, pass 1 of chunk c + 1, ..., one launch
+// each. A pass-1 launch after the first does not wait for the pass-2 launch
+// before it (it touches nothing that launch reads or writes), so the two
+// overlap; it waits for it before it exits. Smaller chunks would let pass 2
+// read keys that pass 1 of the chunk has just brought into L2, but on GB300 the
+// fill and drain of the extra launches cost more than the re-read from HBM
+// (4 x 32K prompts: 0.255 ms per eviction with 32 MiB chunks, 0.195 with 64,
+// 0.182 with 96, 0.152 with one chunk), so the default keeps one chunk up to
+// 256 MiB of keys. In a launch the chunk's tiles form one flattened range that
+// every CTA shares equally. Every pass-1 share writes its rows' (max, sum) and
+// counts itself in on the pair's counter (zeroed before the first launch); the
+// share that completes the count merges them into the rows' final
+// log-sum-exps, which pass 2 reads.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include "se_ptx.cuh"
+
+#ifndef SE_SNAPKV_CHUNK_BYTES
+#define SE_SNAPKV_CHUNK_BYTES (256u << 20)  // keys of one chunk of pairs
+#endif
 
 namespace se {
 namespace {
@@ -40,37 +61,87 @@ constexpr int kPagesPerTile = kTileN / kPageSize;
 constexpr int kHalfBytes = kTileN * 128;      // 128 rows x 128 bytes (64 dims)
 constexpr int kTileBytes = 2 * kHalfBytes;    // 32 KB
 constexpr int kStages = 4;
-constexpr int kThreads = 320;
+constexpr int kThreads = 320;                 // producer, MMA issuer, 8 epilogue warps
 constexpr int kEpiThreads = 256;
 constexpr int kMinTilesPerCta = 4;
 constexpr int kTmemCols = 256;
+constexpr int kMaxPairsPerChunk = 2048;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Dynamic shared memory: [K ring 4 x 32 KB][Q 2 x 32 KB][colsum 2 x 4 x 128 fp32][prefix][barriers]
+// Dynamic shared memory: [K ring 4 x 32 KB][Q 2 x 32 KB][column partials 2 x 2 x 128 fp32]
+// [final -LSE 2 x 128 fp32][row stats 2 x 128 x 2 fp32][flag][prefix][barriers]
 constexpr int kRingOff = 0;
 constexpr int kQOff = kStages * kTileBytes;
 constexpr int kColOff = kQOff + 2 * kTileBytes;
-constexpr int kStatOff = kColOff + 2 * 4 * 128 * 4;   // pass 1: [128 rows][2] (max, sum) of column half 1
-constexpr int kPrefixOff = kStatOff + 128 * 2 * 4;
+constexpr int kNegLseOff = kColOff + 2 * 2 * 128 * 4;
+constexpr int kStatOff = kNegLseOff + 2 * 128 * 4;
+constexpr int kFlagOff = kStatOff + 2 * 128 * 2 * 4;
+constexpr int kPrefixOff = kFlagOff + 16;
 
 struct SnapArgs {
-  const uint16_t* qwin;  // [B][W][Hq][D]
-  int32_t W, G, H, B;
+  int32_t W, G, H;
+  int32_t pair0;         // first pair (b * H + h) of this launch
+  int32_t pairs;         // pairs of this launch
+  int32_t wait_previous; // wait for the previous launch of the stream before the first access
   const int32_t* bt;
   int32_t bt_stride;
   const int32_t* lens;
   int32_t max_len;
   int32_t num_pages;
   float scale_log2;
-  float* part;         // pass 1: [pairs][max_slices][128] x (max, sum), log2 domain
-  int32_t* pair_ns;    // pass 1: slices per pair
+  float* part;           // pass 1: [pairs][max_slices][128] x (max, sum), log2 domain
+  uint32_t* done;        // pass-1 shares counted in per pair (zero before the first launch)
+  float* final_nlse;     // [pairs][128]: -LSE_r (log2 domain) of every row, merged by the pair's last share
   int32_t max_slices;
-  float* row_lse;      // pass 2, optional: [pairs][R] natural log
-  float* scores;       // pass 2: [pairs][score_stride]
+  uint64_t probe_limit_ns;  // 0; in a wait probe, the limit of the MMA issuer's wait on a barrier nothing arrives at
+  float* row_lse;        // optional: [pairs][R] natural log
+  float* scores;         // [pairs][score_stride]
   int32_t score_stride;
   unsigned* err;
 };
 
+// ---------------------------------------------------------------- paired fp32
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Sum of exp2(x_c * s + bias_c) over 64 values (two packed lanes at a time, four
+// independent packed accumulators).
+__device__ __forceinline__ float sum_exp2_64(const uint32_t (&raw)[2][32], uint64_t s2, const uint64_t (&bias)[32]) {
+  uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    float x0, x1;
+    f2_split(ffma2(f2(__uint_as_float(raw[c >> 4][(2 * c) & 31]), __uint_as_float(raw[c >> 4][(2 * c + 1) & 31])),
+                   s2, bias[c]),
+             x0, x1);
+    acc[c & 3] = fadd2(acc[c & 3], f2(fast_exp2(x0), fast_exp2(x1)));
+  }
+  float a0, a1;
+  f2_split(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
+  return a0 + a1;
+}
+
+// ---------------------------------------------------------------- schedule
 __device__ __forceinline__ int find_pair(const int* prefix, int n, int x) {
   int lo = 0, hi = n;
   while (hi - lo > 1) {
@@ -80,35 +151,33 @@ __device__ __forceinline__ int find_pair(const int* prefix, int n, int x) {
   return lo;
 }
 
-__device__ __forceinline__ void named_barrier_epi() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-// Row r's log2-domain log-sum-exp of pair p from pass 1's per-slice (max, sum); +inf when the row saw no key.
-__device__ __forceinline__ float merged_lse2(const SnapArgs& a, int p, int r) {
-  const int ns = min(a.pair_ns[p], a.max_slices);
-  const float* pr = a.part + ((size_t)p * a.max_slices * 128 + r) * 2;
-  float M = -INFINITY;
-  for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, pr[(size_t)s2 * 256]);
-  float L = 0.f;
-  for (int s2 = 0; s2 < ns; ++s2) {
-    const float mm = pr[(size_t)s2 * 256];
-    if (mm != -INFINITY) L += pr[(size_t)s2 * 256 + 1] * exp2f(mm - M);
-  }
-  return (L > 0.f) ? M + log2f(L) : INFINITY;
+// A flattened range of T tiles is shared by min(grid, T / kMinTilesPerCta) CTAs
+// (at least one), share i holding tiles [floor(i T / n), floor((i + 1) T / n)):
+// every share has at least kMinTilesPerCta tiles when T does.
+__device__ __forceinline__ int share_count(int T, int grid) { return max(1, min(grid, T / kMinTilesPerCta)); }
+__device__ __forceinline__ int share_start(int T, int n, int i) { return (int)(((long long)i * T) / n); }
+__device__ __forceinline__ int share_of_tile(int T, int n, int u) {
+  return (int)(((long long)(u + 1) * n + T - 1) / T) - 1;
 }
 
-// Tiles of pair (b, h) for the pass: all keys (pass 1) or the candidates only (pass 2).
+__device__ __forceinline__ void named_barrier_epi() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Tiles of a pair with n keys for the pass: all keys (pass 1) or the candidates only (pass 2).
 __device__ __forceinline__ int pair_tiles(int n, int W, int pass) {
   const int cols = pass == 1 ? n : max(n - W, 0);
   return (cols + kTileN - 1) / kTileN;
 }
 
+// One pass over the tiles of one chunk of pairs (see the file comment).
 template <int PASS>
-__global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                   const SnapArgs a) {
-  pdl_enter();
+__global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                 const __grid_constant__ CUtensorMap qmap,
+                                                                 const SnapArgs a) {
+  if (a.wait_previous) pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int pairs = a.B * a.H;
+  const int pairs = a.pairs;
   int* prefix = reinterpret_cast<int*>(smem + kPrefixOff);  // [pairs + 1]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPrefixOff + ((pairs + 2) & ~1) * 4);
   uint64_t* full = bars;                 // [4]
@@ -117,20 +186,26 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
   uint64_t* acc_empty = acc_full + 2;    // [2]
   uint64_t* q_full = acc_empty + 2;      // [2]
   uint64_t* q_empty = q_full + 2;        // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_empty + 2);
-  float* colsum = reinterpret_cast<float*>(smem + kColOff);  // [2][4][128]
+  uint64_t* mma_fin = q_empty + 2;       // every MMA of the CTA has completed
+  uint64_t* probe = mma_fin + 1;         // wait probe: a barrier nothing arrives at
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(probe + 1);
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + kFlagOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = a.W * a.G;
 
-  // Tiles per pair and their exclusive prefix.
+  // Tiles per pair and their exclusive prefix; zero query buffers (the copies
+  // write rows 0 .. R - 1 only).
   for (int p = threadIdx.x; p < pairs; p += kThreads) {
-    int n = a.lens[p / a.H];
+    int n = a.lens[(a.pair0 + p) / a.H];
     if (n < a.W || n > a.max_len) {
-      raise_error(a.err, SE_DEVERR_LENGTH);
+      if (PASS == 1) raise_error(a.err, SE_DEVERR_LENGTH);
       n = n < a.W ? 0 : a.max_len;
     }
     prefix[p + 1] = pair_tiles(n, a.W, PASS);
   }
+  for (int i = threadIdx.x; i < 2 * kTileBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + kQOff)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -139,9 +214,11 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kEpiThreads);
-      mbar_init(&q_full[i], kEpiThreads);
+      mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
+    mbar_init(mma_fin, 1);
+    mbar_init(probe, 1);
     mbar_fence_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -168,183 +245,216 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
   __syncthreads();
   tc05_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = prefix[pairs];
-  const int per_cta = max(kMinTilesPerCta, (total + (int)gridDim.x - 1) / (int)gridDim.x);
-  if (PASS == 1 && blockIdx.x == 0) {
-    for (int p = threadIdx.x; p < pairs; p += kThreads) {
-      const int p0 = prefix[p], cnt = prefix[p + 1] - p0;
-      a.pair_ns[p] = cnt == 0 ? 0 : (p0 + cnt - 1) / per_cta - p0 / per_cta + 1;
+  const int T = prefix[pairs];
+  const int nsh = share_count(T, (int)gridDim.x);
+  const int lo = (int)blockIdx.x < nsh ? share_start(T, nsh, blockIdx.x) : T;
+  const int hi = (int)blockIdx.x < nsh ? share_start(T, nsh, blockIdx.x + 1) : T;
+  // Calls fn(p, t0, t1) for every segment (one pair's tiles [t0, t1)) of this CTA's share.
+  auto for_each_segment = [&](auto&& fn) {
+    if (lo >= hi) return;
+    const int pf = find_pair(prefix, pairs, lo), pl = find_pair(prefix, pairs, hi - 1);
+    for (int p = pf; p <= pl; ++p) {
+      const int t0 = max(lo, prefix[p]) - prefix[p], t1 = min(hi, prefix[p + 1]) - prefix[p];
+      if (t0 < t1) fn(p, t0, t1);
     }
-  }
-  const int start = blockIdx.x * per_cta;
-  const int end = min(total, start + per_cta);
+  };
   bool dead = false;  // a bounded wait gave up: finish without further waits
 
-  if (start < end) {
-    const int p_first = find_pair(prefix, pairs, start);
-    const int p_last = find_pair(prefix, pairs, end - 1);
-    if (warp == 0) {
-      // ------------------------------------------------------------ producer
-      const uint64_t policy = l2_evict_first_policy();
-      int it = 0;
-      for (int p = p_first; p <= p_last; ++p) {
-        const int t0 = max(start, prefix[p]) - prefix[p], t1 = min(end, prefix[p + 1]) - prefix[p];
-        const int b = p / a.H, h = p % a.H;
-        const int n = min(a.lens[b], a.max_len);
-        const int npages = (n + kPageSize - 1) / kPageSize;
-        // Block-table entries of 4 tiles per window (lane l: page l % 8 of tile
-        // wb + l / 8); the next window is read 4 tiles before it is needed, so no
-        // tile waits on a table lookup.
-        const int32_t* bt_row = a.bt + (size_t)b * a.bt_stride;
-        auto load_window = [&](int wt) {
-          const int tt = wt + (lane >> 3), page = tt * kPagesPerTile + (lane & 7);
-          int ph = -1;
-          if (tt < t1 && page < npages) {
-            ph = bt_row[page];
-            if (ph < 0 || ph >= a.num_pages) {
-              raise_error(a.err, SE_DEVERR_PAGE_RANGE);
-              ph = -1;
-            }
-          }
-          return ph;
-        };
-        int wb = t0, win_cur = load_window(t0), win_nxt = load_window(t0 + 4);
-        for (int t = t0; t < t1; ++t, ++it) {
-          const int s = it % kStages;
-          if (t == wb + 4) {
-            wb += 4;
-            win_cur = win_nxt;
-            win_nxt = load_window(wb + 4);
-          }
-          int phys = __shfl_sync(0xffffffffu, win_cur, (t - wb) * kPagesPerTile + (lane & 7));
-          if (lane >= kPagesPerTile) phys = -1;
-          if (it >= kStages && !dead && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1)) {
-            if (lane == 0) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
-            dead = true;
-          }
-          const unsigned live = __ballot_sync(0xffffffffu, phys >= 0);
-          if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(live) * 2 * kPageSize * 128);
-          __syncwarp();
-          if (phys >= 0 && !dead) {
-            uint8_t* st = smem + kRingOff + s * kTileBytes + lane * kPageSize * 128;
-            const int y = (phys * a.H + h) * kPageSize;
-            tma_load_2d(st, &kmap, 0, y, &full[s], policy);
-            tma_load_2d(st + kHalfBytes, &kmap, 64, y, &full[s], policy);
-          }
-        }
-      }
-      // Drain: every copy issued by this CTA has landed.
-      if (lane == 0)
-        for (int i = max(0, it - kStages); i < it && !dead; ++i)
-          if (!mbar_wait(&full[i % kStages], (i / kStages) & 1)) dead = true;
-    } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
-      // Lane 0 alone: descriptors built once per Q buffer and stage, advanced by
-      // constant offsets ((bytes >> 4) in the address field, no carry: every
-      // shared address is below 256 KB).
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Per segment: the pair's window queries (two 4-D boxes: 64 dims x G heads
+    // x W positions, rows r = w G + g), then its key tiles.
+    const uint64_t q_policy = l2_evict_normal_policy();
+    // pass 1: the keys are read again by pass 2 of the chunk; pass 2: last use
+    const uint64_t policy = PASS == 1 ? l2_evict_normal_policy() : l2_evict_first_policy();
+    int it = 0, seg = 0;
+    for_each_segment([&](int p, int t0, int t1) {
+      const int g = a.pair0 + p;
+      const int b = g / a.H, h = g % a.H;
+      const int n = min(a.lens[b], a.max_len);
+      const int npages = (n + kPageSize - 1) / kPageSize;
+      const int qb = seg & 1;
       if (lane == 0) {
-        const uint32_t idesc = umma_idesc_bf16(128, kTileN);
-        int it = 0, acc_it = 0, seg = 0;
-        // After a failed wait the loop goes on without MMAs but keeps committing,
-        // so that the other roles' waits still complete.
-        for (int p = p_first; p <= p_last; ++p) {
-          const int t0 = max(start, prefix[p]) - prefix[p], t1 = min(end, prefix[p + 1]) - prefix[p];
-          if (t0 >= t1) continue;
-          const int qb = seg & 1;
-          if (!dead && !mbar_wait(&q_full[qb], (seg >> 1) & 1)) {
-            raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
-            dead = true;
-          }
-          tc05_fence_after();
-          const uint64_t dq = umma_desc_sw128(smem_addr(smem + kQOff + qb * kTileBytes));
-          for (int t = t0; t < t1; ++t, ++it, ++acc_it) {
-            const int s = it % kStages, ab = acc_it & 1;
-            if (!dead && (!mbar_wait(&full[s], (it / kStages) & 1) ||
-                          (acc_it >= 2 && !mbar_wait(&acc_empty[ab], ((acc_it >> 1) - 1) & 1)))) {
-              raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
-              dead = true;
-            }
-            tc05_fence_after();
-            if (!dead) {
-              const uint64_t dk = umma_desc_sw128(smem_addr(smem + kRingOff + s * kTileBytes));
-              const uint32_t d = tmem + ab * kTileN;
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                constexpr uint64_t kHalfDesc = kHalfBytes >> 4;
-                const uint64_t off = (uint64_t)(kk >> 2) * kHalfDesc + (uint64_t)(kk & 3) * 2;  // 32 bytes = 2
-                tc05_mma_bf16(d, dq + off, dk + off, idesc, kk > 0 ? 1u : 0u);
-              }
-            }
-            tc05_commit(&empty[s]);
-            tc05_commit(&acc_full[ab]);
-            if (t == t1 - 1) tc05_commit(&q_empty[qb]);
-          }
-          ++seg;
-        }
-      }
-      __syncwarp();
-    } else {
-      // ------------------------------------------------------------ epilogue
-      const int wg = warp & 3;              // TMEM lane quarter of this warp
-      const int chalf = (warp - 2) >> 2;    // which 64 of the tile's 128 columns
-      const int r = wg * 32 + lane;         // query row = TMEM lane
-      const int w_pos = r / a.G, g = r % a.G;
-      const bool row_live = r < R;
-      float* stat = reinterpret_cast<float*>(smem + kStatOff);
-      int acc_it = 0, seg = 0, tile_ctr = 0;
-      for (int p = p_first; p <= p_last; ++p) {
-        const int t0 = max(start, prefix[p]) - prefix[p], t1 = min(end, prefix[p + 1]) - prefix[p];
-        if (t0 >= t1) continue;
-        const int b = p / a.H, h = p % a.H;
-        const int n = min(a.lens[b], a.max_len);
-        const int qb = seg & 1;
-        // Query row r, dims [64 chalf, 64 chalf + 64), into Q buffer qb (swizzled, zero past R).
         if (seg >= 2 && !dead && !mbar_wait(&q_empty[qb], ((seg >> 1) - 1) & 1)) {
           raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
           dead = true;
         }
-        {
-          uint8_t* qt = smem + kQOff + qb * kTileBytes + chalf * kHalfBytes;
-          const uint16_t* qrow = a.qwin + (((size_t)b * a.W + w_pos) * (a.H * a.G) + h * a.G + g) * kD + chalf * 64;
-#pragma unroll
-          for (int q8 = 0; q8 < 8; ++q8) {
-            const uint4 v = row_live ? *reinterpret_cast<const uint4*>(qrow + q8 * 8) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(qt + swz128(r, q8)) = v;
+        mbar_arrive_expect_tx(&q_full[qb], dead ? 0u : (uint32_t)(2 * R * 128));
+        if (!dead) {
+          uint8_t* qt = smem + kQOff + qb * kTileBytes;
+          tma_load_4d(qt, &qmap, 0, h * a.G, 0, b, &q_full[qb], q_policy);
+          tma_load_4d(qt + kHalfBytes, &qmap, 64, h * a.G, 0, b, &q_full[qb], q_policy);
+        }
+      }
+      dead = __shfl_sync(0xffffffffu, (int)dead, 0) != 0;
+      ++seg;
+      // Block-table entries of 4 tiles per window (lane l: page l % 8 of tile
+      // wb + l / 8); the next window is read 4 tiles before it is needed.
+      const int32_t* bt_row = a.bt + (size_t)b * a.bt_stride;
+      auto load_window = [&](int wt) {
+        const int tt = wt + (lane >> 3), page = tt * kPagesPerTile + (lane & 7);
+        int ph = -1;
+        if (tt < t1 && page < npages) {
+          ph = bt_row[page];
+          if (ph < 0 || ph >= a.num_pages) {
+            raise_error(a.err, SE_DEVERR_PAGE_RANGE);
+            ph = -1;
           }
-          fence_proxy_async_smem();
-          mbar_arrive(&q_full[qb]);
         }
-        float m_run = -INFINITY, l_run = 0.f, lse2 = INFINITY;
-        if (PASS == 2) {
-          lse2 = merged_lse2(a, p, r);  // +inf: the row contributes nothing
-          if (a.row_lse && t0 == 0 && row_live && chalf == 0)
-            a.row_lse[(size_t)p * R + r] = lse2 != INFINITY ? lse2 * kLn2 : -INFINITY;
+        return ph;
+      };
+      int wb = t0, win_cur = load_window(t0), win_nxt = load_window(t0 + 4);
+      for (int t = t0; t < t1; ++t, ++it) {
+        const int s = it % kStages;
+        if (t == wb + 4) {
+          wb += 4;
+          win_cur = win_nxt;
+          win_nxt = load_window(wb + 4);
         }
-        const int limit = n - a.W + w_pos;  // last key this row sees
-        for (int t = t0; t < t1; ++t, ++acc_it, ++tile_ctr) {
-          const int ab = acc_it & 1;
-          if (!dead && !mbar_wait(&acc_full[ab], (acc_it >> 1) & 1)) {
+        int phys = __shfl_sync(0xffffffffu, win_cur, (t - wb) * kPagesPerTile + (lane & 7));
+        if (lane >= kPagesPerTile) phys = -1;
+        if (it >= kStages && !dead && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1)) {
+          if (lane == 0) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+          dead = true;
+        }
+        const unsigned live = __ballot_sync(0xffffffffu, phys >= 0 && !dead);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(live) * 2 * kPageSize * 128);
+        __syncwarp();
+        if (phys >= 0 && !dead) {
+          uint8_t* st = smem + kRingOff + s * kTileBytes + lane * kPageSize * 128;
+          const int y = (phys * a.H + h) * kPageSize;
+          tma_load_2d(st, &kmap, 0, y, &full[s], policy);
+          tma_load_2d(st + kHalfBytes, &kmap, 64, y, &full[s], policy);
+        }
+      }
+    });
+    // Drain: every copy this CTA issued has landed before it exits.
+    if (lane == 0) {
+      for (int i = max(0, it - kStages); i < it; ++i)
+        if (!mbar_wait(&full[i % kStages], (i / kStages) & 1)) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+      for (int i = max(0, seg - 2); i < seg; ++i)
+        if (!mbar_wait(&q_full[i & 1], (i >> 1) & 1)) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // Lane 0 alone: descriptors advanced by constant offsets ((bytes >> 4) in the
+    // address field, no carry: every shared address is below 256 KB). Pass 1
+    // multiplies Q (A, M = query rows) by K (B, N = keys); pass 2 swaps them.
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16(128, kTileN);
+      int it = 0, seg = 0;
+      if (a.probe_limit_ns && !mbar_wait_ns(probe, 0, a.probe_limit_ns)) {
+        // the probe's wait ran out, as it must: no MMA from here on
+        raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+        dead = true;
+      }
+      // After a failed wait the loop goes on without MMAs but keeps committing,
+      // so that the other roles' waits still complete.
+      for_each_segment([&](int p, int t0, int t1) {
+        const int qb = seg & 1;
+        if (!dead && !mbar_wait(&q_full[qb], (seg >> 1) & 1)) {
+          raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+          dead = true;
+        }
+        tc05_fence_after();
+        const uint64_t dq = umma_desc_sw128(smem_addr(smem + kQOff + qb * kTileBytes));
+        for (int t = t0; t < t1; ++t, ++it) {
+          const int s = it % kStages, ab = it & 1;
+          if (!dead && (!mbar_wait(&full[s], (it / kStages) & 1) ||
+                        (it >= 2 && !mbar_wait(&acc_empty[ab], ((it >> 1) - 1) & 1)))) {
             raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
             dead = true;
           }
           tc05_fence_after();
-          const int jc = t * kTileN + chalf * 64;  // first column of this thread's half
+          if (!dead) {
+            const uint64_t dk = umma_desc_sw128(smem_addr(smem + kRingOff + s * kTileBytes));
+            const uint64_t da = PASS == 1 ? dq : dk, db = PASS == 1 ? dk : dq;
+            const uint32_t d = tmem + ab * kTileN;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              constexpr uint64_t kHalfDesc = kHalfBytes >> 4;
+              const uint64_t off = (uint64_t)(kk >> 2) * kHalfDesc + (uint64_t)(kk & 3) * 2;  // 32 bytes = 2
+              tc05_mma_bf16(d, da + off, db + off, idesc, kk > 0 ? 1u : 0u);
+            }
+          }
+          tc05_commit(&empty[s]);
+          tc05_commit(&acc_full[ab]);
+          if (t == t1 - 1) tc05_commit(&q_empty[qb]);
+        }
+        ++seg;
+      });
+      // Every MMA issued has completed before the CTA frees its tensor memory.
+      tc05_commit(mma_fin);
+      if (!mbar_wait(mma_fin, 0)) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wg = warp & 3;              // TMEM lane quarter of this warp
+    const int chalf = (warp - 2) >> 2;    // which 64 of the tile's 128 columns
+    const int lq = wg * 32 + lane;        // this thread's TMEM lane
+    const int et = threadIdx.x - 64;      // 0 .. 255
+    float* stat = reinterpret_cast<float*>(smem + kStatOff);        // [2][128 rows][2]
+    float* colpart = reinterpret_cast<float*>(smem + kColOff);      // [2 tiles][2 halves][128 keys]
+    float* neglse = reinterpret_cast<float*>(smem + kNegLseOff);    // [2 segments][128 rows]
+    const uint64_t s2 = f2(a.scale_log2, a.scale_log2);
+    int it = 0, seg = 0;
+    for_each_segment([&](int p, int t0, int t1) {
+      const int g = a.pair0 + p;
+      const int b = g / a.H;
+      const int n = min(a.lens[b], a.max_len);
+      if (PASS == 1) {
+        // ---------------------------------------------------- pass 1: row max / sum
+        const int r = lq, w_pos = r / a.G;
+        const bool row_live = r < R;
+        const int limit = n - a.W + w_pos;  // last key this row sees
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int t = t0; t < t1; ++t, ++it) {
+          const int ab = it & 1;
+          if (!dead && !mbar_wait(&acc_full[ab], (it >> 1) & 1)) {
+            raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+            dead = true;
+          }
+          tc05_fence_after();
+          const int jc = t * kTileN + chalf * 64;  // first key of this thread's half
           uint32_t raw[2][32];
           {
-            const uint32_t row_addr = tmem + ((uint32_t)(wg * 32) << 16) + ab * kTileN + chalf * 64;
-            tmem_ld32(row_addr, raw[0]);
-            tmem_ld32(row_addr + 32, raw[1]);
+            const uint32_t addr = tmem + ((uint32_t)(wg * 32) << 16) + ab * kTileN + chalf * 64;
+            tmem_ld32(addr, raw[0]);
+            tmem_ld32(addr + 32, raw[1]);
             tmem_ld_wait();
           }
           tc05_fence_before();
           mbar_arrive(&acc_empty[ab]);  // the accumulator can take the next tile's MMA
-          if (PASS == 1) {
-            const bool interior = row_live && jc + 63 <= limit;  // every column visible
+          if (!row_live) continue;
+          if (jc + 63 <= limit) {
+            // Every key visible: max of the raw logits (scale > 0), then the sum.
+            float m21[22];
+#pragma unroll
+            for (int i = 0; i < 21; ++i)
+              m21[i] = fmax3(__uint_as_float(raw[(3 * i) >> 5][(3 * i) & 31]),
+                             __uint_as_float(raw[(3 * i + 1) >> 5][(3 * i + 1) & 31]),
+                             __uint_as_float(raw[(3 * i + 2) >> 5][(3 * i + 2) & 31]));
+            m21[21] = __uint_as_float(raw[1][31]);
+            float m8[8];
+#pragma unroll
+            for (int i = 0; i < 7; ++i) m8[i] = fmax3(m21[3 * i], m21[3 * i + 1], m21[3 * i + 2]);
+            m8[7] = m21[21];
+            const float zmax = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+            const float mn = fmaxf(m_run, zmax * a.scale_log2);
+            uint64_t bias[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) bias[c] = f2(-mn, -mn);
+            const float sum = sum_exp2_64(raw, s2, bias);
+            l_run = l_run * fast_exp2(m_run - mn) + sum;
+            m_run = mn;
+          } else {
+            // Causal boundary: keys past `limit` (and past the prompt) are masked.
             float x[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
               const float z = __uint_as_float(raw[c >> 5][c & 31]) * a.scale_log2;
-              x[c] = (interior || (row_live && jc + c <= limit)) ? z : -INFINITY;
+              x[c] = jc + c <= limit ? z : -INFINITY;
             }
             float mx = -INFINITY;
 #pragma unroll
@@ -360,81 +470,126 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_scores_kernel(const __grid
               l_run = l_run * fast_exp2(m_run - mn) + (s0 + s1);
               m_run = mn;
             }
-          } else {
-            float* cs = colsum + (tile_ctr & 1) * 4 * 128 + wg * 128 + chalf * 64;
-            const bool interior = jc + 63 < n - a.W;  // every column a candidate
-#pragma unroll
-            for (int chk = 0; chk < 2; ++chk) {
-              float e[32];
-#pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const float v = fast_exp2(__uint_as_float(raw[chk][c]) * a.scale_log2 - lse2);
-                e[c] = (interior || jc + chk * 32 + c < n - a.W) ? v : 0.f;
-              }
-              // Warp transpose-reduce: afterwards lane l holds column (32 chk + l) summed over the warp's rows.
-#pragma unroll
-              for (int k = 0; k < 5; ++k) {
-                const int off = 16 >> k, half = 16 >> k;
-                const bool upper = (lane & off) != 0;
-#pragma unroll
-                for (int i = 0; i < half; ++i) {
-                  const float lo_v = e[i], hi_v = e[i + half];
-                  const float send = upper ? lo_v : hi_v;
-                  e[i] = (upper ? hi_v : lo_v) + __shfl_xor_sync(0xffffffffu, send, off);
-                }
-              }
-              cs[chk * 32 + lane] = e[0];
-            }
-            named_barrier_epi();  // the lane quarters' column partials of this tile are in
-            const int et = threadIdx.x - 64;  // 0 .. 255
-            if (et < kTileN) {
-              const float* cb = colsum + (tile_ctr & 1) * 4 * 128;
-              const float v = ((cb[et] + cb[128 + et]) + cb[256 + et]) + cb[384 + et];
-              const int j = t * kTileN + et;
-              if (j < n - a.W) a.scores[(size_t)p * a.score_stride + j] = v;
-            }
           }
         }
-        if (PASS == 1) {
-          // Merge the two column halves of each row, then write this slice's partial.
-          if (chalf == 1) {
-            stat[r * 2] = m_run;
-            stat[r * 2 + 1] = l_run;
+        // Merge the two column halves of each row (double-buffered by segment),
+        // write this share's partial and count it in on the pair's counter.
+        float* st = stat + (seg & 1) * 256;
+        if (chalf == 1) {
+          st[lq * 2] = m_run;
+          st[lq * 2 + 1] = l_run;
+        }
+        named_barrier_epi();
+        const int Tp = prefix[p + 1] - prefix[p];  // tiles of the pair; its shares:
+        const int first = share_of_tile(T, nsh, prefix[p]);
+        const int ns = share_of_tile(T, nsh, prefix[p] + Tp - 1) - first + 1;
+        if (chalf == 0) {
+          const float m1 = st[lq * 2], l1 = st[lq * 2 + 1];
+          const float M = fmaxf(m_run, m1);
+          float L = 0.f;
+          if (M != -INFINITY) L = l_run * fast_exp2(m_run - M) + l1 * fast_exp2(m1 - M);
+          const int slot = (int)blockIdx.x - first;
+          if (slot >= 0 && slot < a.max_slices) {
+            float* dst = a.part + (((size_t)g * a.max_slices + slot) * 128 + lq) * 2;
+            *reinterpret_cast<float2*>(dst) = make_float2(M, L);
           }
+        }
+        named_barrier_epi();
+        if (et == 0) {
+          __threadfence();
+          const uint32_t before = atomicAdd(a.done + g, 1u);
+          *flag = (int)before == ns - 1 ? 1 : 0;
+        }
+        named_barrier_epi();
+        if (*flag) {
+          // The pair's last share: merge every share's (max, sum) per row (two
+          // threads per row over alternate shares, 8 loads in flight each), then
+          // write the rows' final -LSE and log-sum-exp.
+          __threadfence();
+          const int r = et & 127, hs = et >> 7;
+          const float* pr = a.part + ((size_t)g * a.max_slices * 128 + r) * 2;
+          const int nsc = min(ns, a.max_slices);
+          float m = -INFINITY, l = 0.f;
+          for (int s0 = hs; s0 < nsc; s0 += 16) {
+            float2 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              v[u] = s0 + 2 * u < nsc ? __ldcg(reinterpret_cast<const float2*>(pr + (size_t)(s0 + 2 * u) * 256))
+                                      : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float mn = fmaxf(m, v[u].x);
+              if (mn != -INFINITY) {
+                l = l * fast_exp2(m - mn) + v[u].y * fast_exp2(v[u].x - mn);
+                m = mn;
+              }
+            }
+          }
+          float* mrg = colpart;  // [2 halves][128 rows][2]
+          mrg[(hs * 128 + r) * 2] = m;
+          mrg[(hs * 128 + r) * 2 + 1] = l;
           named_barrier_epi();
-          if (chalf == 0) {
-            const float m1 = stat[r * 2], l1 = stat[r * 2 + 1];
-            const float M = fmaxf(m_run, m1);
+          if (hs == 0) {
+            const float m1 = mrg[(128 + r) * 2], l1 = mrg[(128 + r) * 2 + 1];
+            const float M = fmaxf(m, m1);
             float L = 0.f;
-            if (M != -INFINITY) L = l_run * fast_exp2(m_run - M) + l1 * fast_exp2(m1 - M);
-            const int first_cta = prefix[p] / per_cta;
-            const int slot = blockIdx.x - first_cta;
-            float* dst = a.part + (((size_t)p * a.max_slices + slot) * 128 + r) * 2;
-            dst[0] = M;
-            dst[1] = L;
+            if (M != -INFINITY) L = l * fast_exp2(m - M) + l1 * fast_exp2(m1 - M);
+            const float lse2 = L > 0.f ? M + log2f(L) : INFINITY;  // +inf: the row saw no key
+            a.final_nlse[(size_t)g * 128 + r] = -lse2;
+            if (a.row_lse && r < R) a.row_lse[(size_t)g * R + r] = lse2 != INFINITY ? lse2 * kLn2 : -INFINITY;
           }
-          named_barrier_epi();  // stat is reused by the next segment
+          named_barrier_epi();  // the merge scratch is free again
         }
-        ++seg;
+      } else {
+        // ---------------------------------------------------- pass 2: column sums
+        // The rows' final -LSE of this pair (written by the pass-1 launch).
+        float* nl = neglse + (seg & 1) * 128;
+        if (et < 128) nl[et] = __ldcg(a.final_nlse + (size_t)g * 128 + et);
+        named_barrier_epi();
+        uint64_t bias[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float4 v = *reinterpret_cast<const float4*>(nl + chalf * 64 + 2 * c);
+          bias[c] = f2(v.x, v.y);
+          bias[c + 1] = f2(v.z, v.w);
+        }
+        const bool half_live = chalf * 64 < R;  // rows past R contribute nothing
+        for (int t = t0; t < t1; ++t, ++it) {
+          const int ab = it & 1;
+          if (!dead && !mbar_wait(&acc_full[ab], (it >> 1) & 1)) {
+            raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
+            dead = true;
+          }
+          tc05_fence_after();
+          uint32_t raw[2][32];
+          {
+            const uint32_t addr = tmem + ((uint32_t)(wg * 32) << 16) + ab * kTileN + chalf * 64;
+            tmem_ld32(addr, raw[0]);
+            tmem_ld32(addr + 32, raw[1]);
+            tmem_ld_wait();
+          }
+          tc05_fence_before();
+          mbar_arrive(&acc_empty[ab]);
+          const float part = (half_live && !dead) ? sum_exp2_64(raw, s2, bias) : 0.f;
+          float* cp = colpart + (it & 1) * 256;
+          cp[chalf * 128 + lq] = part;
+          named_bar_sync(2 + wg, 64);  // the other half of these 32 keys is in (warps w and w + 4)
+          if (chalf == 0) {
+            const int j = t * kTileN + lq;
+            if (j < n - a.W) a.scores[(size_t)g * a.score_stride + j] = cp[lq] + cp[128 + lq];
+          }
+        }
       }
-    }
-  }
-  // Pairs whose prompt holds no candidate (n == window) have no pass-2 tile:
-  // CTA 0 writes their row log-sum-exps.
-  if (PASS == 2 && blockIdx.x == 0 && a.row_lse && warp >= 2 && warp < 6) {
-    const int r = (warp & 3) * 32 + lane;
-    for (int p = 0; p < pairs; ++p) {
-      if (prefix[p + 1] != prefix[p] || r >= R) continue;
-      const int n = a.lens[p / a.H];
-      if (n < a.W || n > a.max_len) continue;
-      const float l2 = merged_lse2(a, p, r);
-      a.row_lse[(size_t)p * R + r] = l2 != INFINITY ? l2 * kLn2 : -INFINITY;
-    }
+      ++seg;
+    });
   }
   tc05_fence_before();
   __syncthreads();
   tc05_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  // A launch that did not wait at its start completes only after the launch
+  // before it, so that a later kernel that waits for this one sees both.
+  if (!a.wait_previous) pdl_wait();
 }
 
 // ------------------------------------------------------------------ selection
@@ -857,8 +1012,8 @@ __global__ void __launch_bounds__(256) snapkv_gather_kernel(KvView src, uint16_t
   }
 }
 
-size_t scores_smem_bytes(int pairs) {
-  return 1024 + (size_t)kPrefixOff + (size_t)((pairs + 2) & ~1) * 4 + 16 * 8 + 16;
+size_t pass_smem_bytes(int pairs) {
+  return 1024 + (size_t)kPrefixOff + (size_t)((pairs + 2) & ~1) * 4 + 18 * 8 + 16;
 }
 
 }  // namespace
@@ -869,23 +1024,32 @@ int snapkv_max_slices(int max_len) {
 }
 
 size_t snapkv_part_bytes(int pairs, int max_len) {
+  // per-share (max, sum) of every row, the pair counters, the rows' final -LSE
   const size_t part = (size_t)pairs * snapkv_max_slices(max_len) * 128 * 2 * sizeof(float);
-  return ((part + 15) & ~size_t(15)) + (((size_t)pairs * sizeof(int32_t) + 15) & ~size_t(15));
+  return ((part + 15) & ~size_t(15)) + (((size_t)pairs * sizeof(int32_t) + 15) & ~size_t(15)) +
+         (size_t)pairs * 128 * sizeof(float);
 }
 
 int snapkv_select_max_candidates() { return kSelMaxCand; }
 
-cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const KvView& kv, const uint16_t* qwin, int32_t num_q_heads,
-                                 int32_t window, const int32_t* bt, int32_t bt_stride, const int32_t* lens,
-                                 int32_t batch, int32_t max_len, float sm_scale, float* scores, int32_t score_stride,
-                                 float* row_lse, void* part_ws, int sm_count, unsigned* err, cudaStream_t stream) {
+namespace {
+// One-shot wait probe of this host thread (se_debug_snapkv_wait_probe): 0 = none.
+thread_local uint32_t t_wait_probe_us = 0;
+}  // namespace
+
+void set_snapkv_wait_probe(uint32_t limit_us) { t_wait_probe_us = limit_us; }
+
+cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const CUtensorMap& qmap, const KvView& kv, const uint16_t* qwin,
+                                 int32_t num_q_heads, int32_t window, const int32_t* bt, int32_t bt_stride,
+                                 const int32_t* lens, int32_t batch, int32_t max_len, float sm_scale, float* scores,
+                                 int32_t score_stride, float* row_lse, void* part_ws, int sm_count, unsigned* err,
+                                 cudaStream_t stream) {
+  (void)qwin;
   if (batch == 0) return cudaSuccess;
   SnapArgs a;
-  a.qwin = qwin;
   a.W = window;
   a.H = kv.num_kv_heads;
   a.G = num_q_heads / kv.num_kv_heads;
-  a.B = batch;
   a.bt = bt;
   a.bt_stride = bt_stride;
   a.lens = lens;
@@ -896,25 +1060,39 @@ cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const KvView& kv, cons
   a.max_slices = snapkv_max_slices(max_len);
   const size_t part = (size_t)pairs * a.max_slices * 128 * 2 * sizeof(float);
   a.part = static_cast<float*>(part_ws);
-  a.pair_ns = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(part_ws) + ((part + 15) & ~size_t(15)));
+  a.done = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(part_ws) + ((part + 15) & ~size_t(15)));
+  a.final_nlse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(a.done) +
+                                          (((size_t)pairs * sizeof(uint32_t) + 15) & ~size_t(15)));
   a.row_lse = row_lse;
   a.scores = scores;
   a.score_stride = score_stride;
   a.err = err;
-  const size_t smem = scores_smem_bytes(pairs);
-  cudaError_t e = cudaFuncSetAttribute(snapkv_scores_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const uint64_t probe_ns = (uint64_t)t_wait_probe_us * 1000u;
+  t_wait_probe_us = 0;
+  // Pairs per chunk: their keys take about SE_SNAPKV_CHUNK_BYTES (at most
+  // kMaxPairsPerChunk pairs: their prefix lives in shared memory).
+  const size_t pair_bytes = (size_t)std::max(max_len, 1) * kD * 2;
+  const int chunk = (int)std::min<size_t>(kMaxPairsPerChunk, std::max<size_t>(1, (size_t)SE_SNAPKV_CHUNK_BYTES / pair_bytes));
+  cudaError_t e = cudaMemsetAsync(a.done, 0, (size_t)pairs * sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(snapkv_scores_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = pass_smem_bytes(std::min(chunk, pairs));
+  e = cudaFuncSetAttribute(snapkv_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  {
-    const cudaError_t le = launch_pdl(snapkv_scores_kernel<1>, dim3(sm_count), dim3(kThreads), smem, stream, kmap, a);
-    if (le != cudaSuccess) return le;
-  }
-  e = cudaGetLastError();
+  e = cudaFuncSetAttribute(snapkv_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  {
-    const cudaError_t le = launch_pdl(snapkv_scores_kernel<2>, dim3(sm_count), dim3(kThreads), smem, stream, kmap, a);
-    if (le != cudaSuccess) return le;
+  for (int p0 = 0; p0 < pairs; p0 += chunk) {
+    a.pair0 = p0;
+    a.pairs = std::min(chunk, pairs - p0);
+    // Pass 1 of a later chunk touches nothing the pass 2 before it reads or
+    // writes: it starts at once and waits for that launch only before it exits.
+    a.wait_previous = p0 == 0 ? 1 : 0;
+    a.probe_limit_ns = p0 == 0 ? probe_ns : 0;
+    e = launch_pdl(snapkv_pass_kernel<1>, dim3(sm_count), dim3(kThreads), smem, stream, kmap, qmap, a);
+    if (e != cudaSuccess) return e;
+    a.wait_previous = 1;
+    a.probe_limit_ns = 0;
+    e = launch_pdl(snapkv_pass_kernel<2>, dim3(sm_count), dim3(kThreads), smem, stream, kmap, qmap, a);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -20,8 +20,11 @@
 //    domain, fp32 accumulation;
 //  * at the end of a segment the four warps' states merge in shared memory. An
 //    item held by one CTA writes its output directly; an item spread over
-//    several CTAs writes normalised partials (output, log-sum-exp) and
-//    combine_kernel merges them: o = sum_s exp(lse_s - LSE) o_s.
+//    several CTAs writes normalised partials (output, log-sum-exp), and the
+//    CTA that publishes the item's last partial merges them:
+//    o = sum_s exp(lse_s - LSE) o_s. Each CTA counts itself in on a per-item
+//    arrival counter in the workspace; the last one resets it to zero, so a
+//    workspace that starts zeroed is left zeroed by every call.
 #include "se_ptx.cuh"
 
 namespace se {
@@ -62,7 +65,7 @@ struct DecodeArgs {
   float* out_lse;
   float* o_part;     // [B * Hq][max_splits][128]
   float* lse_part;   // [B * Hq][max_splits], log2 domain
-  int32_t* item_ns;  // [B * H]: CTAs holding each item's pages
+  uint32_t* arrivals;  // [B * H]: CTAs of a split item that have published their partial (zero between calls)
   unsigned* err;
 };
 
@@ -109,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* red_ml = reinterpret_cast<float*>(ring + kRingBytes);       // [2][kWarps][16]: (m, l) per warp and row
   int* prefix = reinterpret_cast<int*>(red_ml + 2 * kWarps * 16);    // [items + 1]
+  __shared__ int s_last;  // this CTA published the last partial of the segment's item
   const int H = a.num_kv_heads, G = a.group, Hq = H * G;
   const int items = a.batch * H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -144,10 +148,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
   __syncthreads();
   const int total = prefix[items];
   const int per_cta = max(kMinPagesPerCta, (total + (int)gridDim.x - 1) / (int)gridDim.x);
+  // Items with no selected page get a zero output and lse = -inf (the empty sum).
   if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < items; i += kThreads) {
-      const int p0 = prefix[i], cnt = prefix[i + 1] - p0;
-      a.item_ns[i] = cnt == 0 ? 0 : (p0 + cnt - 1) / per_cta - p0 / per_cta + 1;
+    for (int idx = threadIdx.x; idx < items * G; idx += kThreads) {
+      const int i = idx / G;
+      if (prefix[i + 1] != prefix[i]) continue;
+      const size_t row = (size_t)(i / H) * Hq + (i % H) * G + idx % G;
+      for (int d = 0; d < kHeadDim; d += 8) *reinterpret_cast<uint4*>(a.out + row * kHeadDim + d) = make_uint4(0, 0, 0, 0);
+      if (a.out_lse) a.out_lse[row] = -INFINITY;
     }
   }
   const int start = blockIdx.x * per_cta;
@@ -397,50 +405,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
         if (d == 0) a.lse_part[row * a.max_splits + slot] = lse2;
       }
     }
+    if (ns > 1) __threadfence();  // this CTA's partial is visible before it counts itself in
     __syncthreads();  // the staged states are read: the last stages may be refilled
+    if (ns > 1) {
+      if (threadIdx.x == 0) {
+        const uint32_t before = atomicAdd(a.arrivals + cur, 1u);
+        const bool last = before == (uint32_t)ns - 1;
+        if (last) a.arrivals[cur] = 0;  // every CTA of the item is in: zero for the next call
+        s_last = last ? 1 : 0;
+      }
+      __syncthreads();
+      if (s_last) {
+        // The item's last partial: merge all ns of them (written by other CTAs:
+        // read past L1).
+        __threadfence();
+        for (int idx = threadIdx.x; idx < G * (kHeadDim / 4); idx += kThreads) {
+          const int r = idx / (kHeadDim / 4), d = (idx % (kHeadDim / 4)) * 4;
+          const size_t row = (size_t)cur_b * Hq + cur_h * G + r;
+          const float* lp = a.lse_part + row * a.max_splits;
+          float M = -INFINITY;
+          for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(lp + s));
+          float wsum = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int s = 0; s < ns; ++s) {
+            const float ls = __ldcg(lp + s);
+            if (ls == -INFINITY) continue;
+            const float f = fast_exp2(ls - M);
+            wsum += f;
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(a.o_part + (row * a.max_splits + s) * kHeadDim + d));
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
+          }
+          const bool empty_row = !(wsum > 0.f);
+          const float inv = empty_row ? 0.f : 1.f / wsum;
+          uint2 pk;
+          pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+          pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+          *reinterpret_cast<uint2*>(a.out + row * kHeadDim + d) = pk;
+          if (a.out_lse && d == 0) a.out_lse[row] = empty_row ? -INFINITY : (M + log2f(wsum)) * kLn2;
+        }
+      }
+    }
     if (next < 0) break;
     item = next;
   }
-}
-
-// Merge the partials of the items spread over several CTAs; one warp per
-// (request, query head). Items held by one CTA were written directly; items
-// with no selected page get a zero output and lse = -inf.
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ o_part,
-                                                      const float* __restrict__ lse_part,
-                                                      const int32_t* __restrict__ item_ns, int32_t batch, int32_t Hq,
-                                                      int32_t group, int32_t max_splits, uint16_t* __restrict__ out,
-                                                      float* __restrict__ out_lse) {
-  pdl_enter();
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (row >= batch * Hq) return;
-  const int lane = threadIdx.x & 31;
-  const int b = row / Hq, h = (row % Hq) / group, H = Hq / group;
-  const int ns = min(item_ns[b * H + h], max_splits);
-  if (ns == 1) return;
-  const float* lp = lse_part + (size_t)row * max_splits;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, lp[s]);
-  float wsum = 0.f;
-  for (int s = 0; s < ns; ++s) wsum += (lp[s] == -INFINITY) ? 0.f : fast_exp2(lp[s] - M);
-  const bool empty_row = !(wsum > 0.f);
-  const float inv = empty_row ? 0.f : 1.f / wsum;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int d = lane * 4;
-  for (int s = 0; s < ns; ++s) {
-    if (lp[s] == -INFINITY) continue;
-    const float f = fast_exp2(lp[s] - M);
-    const float4 v = *reinterpret_cast<const float4*>(o_part + ((size_t)row * max_splits + s) * kHeadDim + d);
-    acc.x += f * v.x;
-    acc.y += f * v.y;
-    acc.z += f * v.z;
-    acc.w += f * v.w;
-  }
-  uint2 pk;
-  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(out + (size_t)row * kHeadDim + d) = pk;
-  if (out_lse && lane == 0) out_lse[row] = empty_row ? -INFINITY : (M + log2f(wsum)) * kLn2;
 }
 
 size_t decode_smem_bytes(int items) {
@@ -459,10 +469,15 @@ DecodePlan plan_gqa_decode(int32_t batch, int32_t num_kv_heads, int32_t sel_stri
   return p;
 }
 
-size_t gqa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim_v, const DecodePlan& plan) {
+size_t gqa_decode_arrivals_offset(int32_t batch, int32_t num_q_heads, int32_t head_dim_v, const DecodePlan& plan) {
   const size_t rows = (size_t)batch * num_q_heads;
   const size_t part = rows * plan.nsplit * ((size_t)head_dim_v + 1) * sizeof(float);
-  return ((part + 15) & ~size_t(15)) + rows * sizeof(int32_t);  // + item_ns (at most one per row)
+  return (part + 15) & ~size_t(15);
+}
+
+size_t gqa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim_v, const DecodePlan& plan) {
+  // partials, then the arrival counters (one per item; items <= rows)
+  return gqa_decode_arrivals_offset(batch, num_q_heads, head_dim_v, plan) + (size_t)batch * num_q_heads * sizeof(int32_t);
 }
 
 size_t gqa_decode_max_items() { return (227 * 1024 - (size_t)kRingBytes - 1024 - 2 * kWarps * 16 * 4) / 4 - 1; }
@@ -495,11 +510,10 @@ cudaError_t launch_gqa_decode(const KvView& kv, const uint16_t* q, int32_t num_q
   a.out = out;
   a.out_lse = out_lse;
   const size_t rows = (size_t)batch * num_q_heads;
-  const size_t part = rows * plan.nsplit * ((size_t)kHeadDim + 1) * sizeof(float);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.o_part = reinterpret_cast<float*>(ws);
   a.lse_part = a.o_part + rows * plan.nsplit * kHeadDim;
-  a.item_ns = reinterpret_cast<int32_t*>(ws + ((part + 15) & ~size_t(15)));
+  a.arrivals = reinterpret_cast<uint32_t*>(ws + gqa_decode_arrivals_offset(batch, num_q_heads, kHeadDim, plan));
   a.err = err;
   const size_t smem = decode_smem_bytes(batch * H);
   cudaError_t e;
@@ -517,14 +531,6 @@ cudaError_t launch_gqa_decode(const KvView& kv, const uint16_t* q, int32_t num_q
       const cudaError_t le = launch_pdl(gqa_decode_kernel<false>, dim3(plan.grid), dim3(kThreads), smem, stream, a);
       if (le != cudaSuccess) return le;
     }
-  }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int nrows = batch * num_q_heads;
-  {
-    const cudaError_t le = launch_pdl(combine_kernel, dim3((nrows + 3) / 4), dim3(128), 0, stream, a.o_part,
-                                      a.lse_part, a.item_ns, batch, num_q_heads, a.group, plan.nsplit, out, out_lse);
-    if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();
 }

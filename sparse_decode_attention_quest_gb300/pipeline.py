@@ -6,7 +6,7 @@ library's kernels:
     se_quest_score_pages_ws     (upper-bound score of every candidate page; the group's query
                                  sums computed once per request into a workspace)
     se_quest_topk_pages_windowed (top-k pages + the sink/recent windows + the last page, ascending)
-    se_sparse_paged_decode      (split-K flash-decode over the selected pages + merge)
+    se_sparse_paged_decode      (split-K flash-decode over the selected pages, partials merged in the same launch)
 or all four in one launch (se_quest_fused_step, run_fused).
 """
 from __future__ import annotations
@@ -62,14 +62,15 @@ class QuestDecodeStep:
         self.out = torch.empty(self.B, self.Hq, self.Dv, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=dev)
         ws = se_sparse_decode_workspace_size(self.B, self.Hq, self.H, self.Dv, self.sel_stride)
-        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        # zero-filled once: the decode's split-merge counters start at zero and every call leaves them so
+        self.workspace = torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev)
         self.score_ws = None
         if score_workspace:
             sws = se_quest_score_workspace_size(self.B, self.H, self.D)
             self.score_ws = torch.empty(max(sws, 16), dtype=torch.uint8, device=dev)
 
     def launches_per_step(self, append: bool = True) -> int:
-        """Kernels one run() launches: append, (query sums,) score, top-k, decode (+ split merge)."""
+        """Kernels one run() launches: append, (query sums,) score, top-k, decode (+ the latent split merge)."""
         _, _, dec = se_sparse_decode_plan(self.B, self.Hq, self.H, self.D, self.Dv, self.sel_stride)
         return (1 if append else 0) + (3 if self.score_ws is not None else 2) + dec
 

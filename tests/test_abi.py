@@ -171,3 +171,24 @@ def test_update_ex_validation(se_lib):
     assert f(ctypes.byref(kv), FAKE, FAKE, FAKE, 64, FAKE, 2, 0x2, None) == INVALID   # unknown flag
     assert b"flags" in se_lib.se_last_error_detail()
     assert f(ctypes.byref(kv), FAKE, None, FAKE, 64, FAKE, 2, se.APPEND_OVERLAP_PREVIOUS, None) == INVALID  # v_new
+
+
+def test_a_c_caller_compiles_against_the_header_and_links(se_lib, tmp_path):
+    """A plain C program (tests/c_abi_check.c) includes include/sparse_engine.h,
+    links the library and checks host-only paths: status strings, rejection
+    before any launch, workspace sizes."""
+    import os
+    import shutil
+    import subprocess
+    from sparse_decode_attention_quest_gb300 import build as b
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    lib_dir = os.path.dirname(b.lib_path())
+    exe = str(tmp_path / "c_abi_check")
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(root, "include"),
+                    os.path.join(root, "tests", "c_abi_check.c"), "-o", exe, "-L", lib_dir, "-lsparse_engine",
+                    "-Wl,-rpath," + lib_dir], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr

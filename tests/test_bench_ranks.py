@@ -40,7 +40,7 @@ def _rank_main(rank, world, port, out):
 
 def test_two_gloo_ranks():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
     (s0, w0, same0), (s1, w1, same1) = out[0], out[1]
     assert s0 != s1                                      # each replica has its own batch

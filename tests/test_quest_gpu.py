@@ -270,6 +270,33 @@ def test_split_count_does_not_change_the_result(cuda_device):
     assert (s1.lse - s2.lse).abs().max().item() <= 1e-4
 
 
+def test_decode_twice_on_one_workspace_leaves_its_counters_zero(cuda_device):
+    # Items span several CTAs (41 pages each, at least 16 per CTA slice): the CTA that
+    # publishes an item's last partial merges them and resets the item's arrival
+    # counter. Two calls back to back on one workspace give the same output, and the
+    # counters are zero after each.
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=3, context_min=2500, context_max=4000, topk_pages=40,
+                                         append=False, seed=33)
+    x, step, b, a = _prepare(wl, cuda_device)
+    _run(x, step, b, a, cuda_device)
+    out1, lse1 = step.out.clone(), step.lse.clone()
+    nsplit, _, launches = se.se_sparse_decode_plan(wl.batch, wl.num_q_heads, wl.num_kv_heads, 128, 128,
+                                                   step.sel_stride)
+    assert launches == 1
+    rows = wl.batch * wl.num_q_heads
+    off = (rows * nsplit * 129 * 4 + 15) // 16 * 16
+    counters = step.workspace[off:off + 4 * wl.batch * wl.num_kv_heads]
+    assert int(counters.count_nonzero()) == 0
+    for _ in range(2):
+        step.out.fill_(float("nan"))
+        step.attend(x.q.to(cuda_device), a)
+        torch.cuda.synchronize()
+        assert torch.equal(step.out.view(torch.int16), out1.view(torch.int16))
+        assert torch.equal(step.lse, lse1)
+        assert int(counters.count_nonzero()) == 0
+    compare_decode(x, step, list(range(wl.batch)), _scale(wl), "twice")
+
+
 def test_select_pages_entry_point_matches_the_two_calls(cuda_device):
     wl = QWEN3_4B_QUEST_32K.scaled(batch=2, context_min=2000, context_max=2400, topk_pages=16, seed=31)
     x, step, b, a = _prepare(wl, cuda_device)

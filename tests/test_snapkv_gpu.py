@@ -241,6 +241,22 @@ def _full_sampled(wl, dev, pairs):
         _check_pair(x, res, b, h)
 
 
+def test_snapkv_many_chunks_sampled(cuda_device):
+    # 160 (request, KV head) pairs of 1.5K-6K tokens: the score kernel cuts them into
+    # chunks of about 21 pairs (pass 2 of a chunk runs one phase after its pass 1),
+    # so pairs on both sides of several chunk boundaries are checked.
+    wl = SNAPKV_PREFILL_32K.scaled(batch=40, num_q_heads=16, num_kv_heads=4, prompt_min=1500, prompt_max=6000,
+                                   keep_topk=300, seed=16)
+    _full_sampled(wl, cuda_device, ((0, 0), (5, 0), (5, 1), (10, 3), (21, 2), (39, 3)))
+
+
+def test_snapkv_more_pairs_than_one_launch(cuda_device):
+    # 2,056 pairs of short prompts (33-200 tokens, some of them only the window plus one
+    # candidate) take two launches of the score kernel; pairs of both are checked.
+    wl = SNAPKV_PREFILL_32K.scaled(batch=257, prompt_min=33, prompt_max=200, keep_topk=20, seed=17)
+    _full_sampled(wl, cuda_device, ((0, 0), (100, 5), (255, 7), (256, 0), (256, 7)))
+
+
 def test_snapkv_aime_budget_full_32k_sampled(cuda_device):
     # 16-query window, sink 16, recent 64, 4,096 selected
     _full_sampled(SNAPKV_AIME_32K, cuda_device, ((0, 0), (3, 7)))
@@ -314,3 +330,25 @@ def test_periodic_decode_eviction_over_compacted_pages(cuda_device):
                 page = int(cache.block_table[b, t // 16])
                 assert torch.equal(kk[page, h, t % 16].view(torch.int16), rows_k[j].view(torch.int16))
                 assert torch.equal(kv_[page, h, t % 16].view(torch.int16), rows_v[j].view(torch.int16))
+
+
+def test_a_wait_that_runs_out_sets_the_error_word_and_the_next_call_is_correct(cuda_device):
+    """The score kernel's mbarrier waits are bounded. With the wait probe, the MMA issuer
+    of every CTA waits on a barrier phase that nothing completes; after 200 us it gives
+    up, sets SE_DEVERR_WAIT_TIMEOUT and the kernel finishes (copies drained, tensor
+    memory freed). The next call in the same process is correct."""
+    wl = SNAPKV_PREFILL_32K.scaled(batch=2, prompt_min=1500, prompt_max=3000, keep_topk=100, seed=18)
+    x = make_snapkv_inputs(wl)
+    res = _run(x, cuda_device)
+    se.se_read_device_error(clear=True)
+    se.se_debug_snapkv_wait_probe(200)
+    scores = torch.zeros_like(res["scores"]).to(cuda_device)
+    max_len = max(x.prompt_lens)
+    se.se_snapkv_window_scores(res["src"], res["qw"], res["bt"], res["lens"], max_len, res["scale"], scores, None,
+                               res["ws"])
+    torch.cuda.synchronize()
+    assert se.se_read_device_error(clear=True) & se.DEVERR_WAIT_TIMEOUT
+    again = _run(x, cuda_device)
+    assert torch.equal(again["scores"].view(torch.int32), res["scores"].view(torch.int32))
+    for b, h in ((0, 0), (1, 5)):
+        _check_pair(x, again, b, h)

@@ -6,9 +6,11 @@ framework's allocator, loops that forbid cudaMalloc after start-up. For them
 the decode keeps its split partials in a fixed array inside the library. This
 file checks, through the C ABI, that two calls in a row (the second on other
 queries, so stale array contents would show) give the same output as
-se_sparse_paged_decode with a caller workspace, and that sizes beyond the
-array are refused. It is collected last so that a failure here comes after
-every other test has run.
+se_sparse_paged_decode with a caller workspace and agree with the fp64 oracle,
+that the case really spreads items over several CTAs (so the array's partials
+and counters are used), that a latent cache and sizes beyond the array are
+refused. It is collected last so that a failure here comes after every other
+test has run.
 """
 import math
 
@@ -18,7 +20,7 @@ import torch
 import sparse_decode_attention_quest_gb300 as se
 from sparse_decode_attention_quest_gb300.pipeline import QuestDecodeStep, new_summary
 from synth import QWEN3_30B_A3B_QUEST_128K, make_quest_decode_inputs
-from tests.parity import LSE_ATOL, OUT_ATOL
+from tests.parity import LSE_ATOL, OUT_ATOL, compare_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -37,13 +39,20 @@ def _case(dev):
 
 def test_noalloc_decode_matches_the_workspace_decode(se_lib, cuda_device):
     wl, x, step, lens = _case(cuda_device)
-    nsplit, _, _ = se.se_sparse_decode_plan(wl.batch, wl.num_q_heads, wl.num_kv_heads, 128, 128, step.sel_stride)
-    assert nsplit > 1  # the split partials (the scratch) are in use
+    _, per_split, _ = se.se_sparse_decode_plan(wl.batch, wl.num_q_heads, wl.num_kv_heads, 128, 128,
+                                               step.sel_stride)
     gen = torch.Generator().manual_seed(5)
     for call in range(2):
         q = x.q if call == 0 else torch.randn(x.q.shape, generator=gen).to(torch.bfloat16)
         q = q.to(cuda_device)
         step.select(q, lens)
+        # A CTA slice holds max(per_split, ceil(pages / CTAs)) selected pages, with at
+        # least one CTA per SM; an item with more pages than that spans two or more
+        # slices, so its partials go through the array and are merged there.
+        counts = step.counts.flatten().tolist()
+        sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+        per_cta_max = max(per_split, -(-sum(counts) // sms))
+        assert max(counts) > per_cta_max, (counts, per_cta_max)
         se.se_sparse_paged_decode(step.kv, q, step.block_table, lens, step.sel, step.counts, step.sm_scale,
                                   step.out, step.lse, step.workspace)
         out = torch.full_like(step.out, float("nan"))
@@ -54,7 +63,27 @@ def test_noalloc_decode_matches_the_workspace_decode(se_lib, cuda_device):
         assert bool(torch.isfinite(out.float()).all())
         assert (out.float() - step.out.float()).abs().max().item() <= OUT_ATOL, call
         assert (lse - step.lse).abs().max().item() <= LSE_ATOL, call
+        # and against the fp64 oracle on the same queries and selection
+        step.out.copy_(out)
+        step.lse.copy_(lse)
+        x.q = q.cpu()
+        compare_decode(x, step, list(range(wl.batch)), step.sm_scale, f"noalloc call {call}")
     assert se.se_read_device_error(clear=True) == 0
+
+
+def test_noalloc_decode_refuses_a_latent_cache(se_lib, cuda_device):
+    dev = cuda_device
+    cache = torch.zeros(4, 1, 16, 576, dtype=torch.bfloat16, device=dev)
+    kv = se.paged_kv(cache, None, None, 512)
+    q = torch.zeros(2, 64, 576, dtype=torch.bfloat16, device=dev)
+    bt = torch.zeros(2, 4, dtype=torch.int32, device=dev)
+    lens = torch.zeros(2, dtype=torch.int32, device=dev)
+    sel = torch.zeros(2, 1, 8, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(2, 1, dtype=torch.int32, device=dev)
+    out = torch.empty(2, 64, 512, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(se.SparseEngineError) as e:
+        se.se_sparse_paged_decode_noalloc(kv, q, bt, lens, sel, cnt, 1 / math.sqrt(576), out)
+    assert e.value.status == 2 and "workspace" in str(e.value)
 
 
 def test_noalloc_decode_refuses_sizes_beyond_its_array(se_lib, cuda_device):
