@@ -150,6 +150,20 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
   __shared__ int s_info[4];  // bucket B, keys above B, members collected
   const int bh = blockIdx.x, b = bh / H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The scores are loaded from the first candidate of a request of at least
+  // `sink` tokens before the length arrives, so that the two loads overlap;
+  // a shorter request (another first candidate) loads them again below.
+  const int c0_guess = min((sink + kPageSize - 1) / kPageSize, score_stride);
+  const int guess_lim = min(kRegMaxCand, score_stride - c0_guess);
+  float x[kKeysPerThread];
+  {
+    const float* sg = scores + (size_t)bh * score_stride + c0_guess;
+#pragma unroll
+    for (int e = 0; e < kKeysPerThread; ++e) {
+      const int i = tid * kKeysPerThread + e;
+      x[e] = i < guess_lim ? sg[i] : -INFINITY;
+    }
+  }
   const int L = clamp_len(seq_lens[b], max_seq_len, err);
   const int n = (L + kPageSize - 1) / kPageSize;
   int c0, c1;
@@ -162,13 +176,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_reg_kernel(
     return;
   }
   write_kept_windows(out, c0, c1, n, k, tid);
-  const float* sc = scores + (size_t)bh * score_stride + c0;
-  float x[kKeysPerThread];
+  if (c0 != c0_guess) {
+    const float* sc = scores + (size_t)bh * score_stride + c0;
+#pragma unroll
+    for (int e = 0; e < kKeysPerThread; ++e) {
+      const int i = tid * kKeysPerThread + e;
+      x[e] = i < C ? sc[i] : -INFINITY;
+    }
+  }
   float lmin = INFINITY, lmax = -INFINITY;
 #pragma unroll
   for (int e = 0; e < kKeysPerThread; ++e) {
     const int i = tid * kKeysPerThread + e;
-    x[e] = i < C ? sc[i] : -INFINITY;
+    if (i >= C) x[e] = -INFINITY;
     if (i < C && isfinite(x[e])) {
       lmin = fminf(lmin, x[e]);
       lmax = fmaxf(lmax, x[e]);

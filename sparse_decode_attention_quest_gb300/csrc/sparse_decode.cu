@@ -137,16 +137,41 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
   const int items = a.batch * H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // A guess made before the counts arrive: every item has sel_stride selected
+  // pages (a top-k that fills its budget). Under it, the page ids and lengths
+  // of this warp's first 32 pages are loaded beside the counts, and their
+  // block-table entries while the prefix is summed; the guess is checked
+  // below and the values are used only if it holds.
+  const int total_g = items * a.sel_stride;
+  const int per_cta_g = max(kMinPagesPerCta, (total_g + (int)gridDim.x - 1) / (int)gridDim.x);
+  const int start_g = blockIdx.x * per_cta_g, end_g = min(total_g, start_g + per_cta_g);
+  const bool lane_g = start_g + warp + kWarps * lane < end_g;
+  int g_it = 0, g_logical = -1, g_L = 0;
+  if (lane_g) {
+    const int p = start_g + warp + kWarps * lane;
+    g_it = p / a.sel_stride;
+    g_logical = a.sel[(size_t)g_it * a.sel_stride + (p - g_it * a.sel_stride)];
+    g_L = a.seq_lens[g_it / a.num_kv_heads];
+  }
+
   // Selected pages per item, then an exclusive prefix.
+  bool full = true;
   for (int i = threadIdx.x; i < items; i += kThreads) {
     int c = a.sel_counts[i];
+    full = full && c == a.sel_stride;
     if (c < 0 || c > a.sel_stride) {
       raise_error(a.err, SE_DEVERR_LENGTH);
       c = c < 0 ? 0 : a.sel_stride;
     }
     prefix[i + 1] = c;
   }
-  __syncthreads();
+  int g_ph = -1;
+  if (lane_g) {
+    const int L = max(g_L, 0);
+    const int n_b = min((L + kPageSize - 1) / kPageSize, a.bt_stride);
+    if (g_logical >= 0 && g_logical < n_b) g_ph = a.block_table[(size_t)(g_it / a.num_kv_heads) * a.bt_stride + g_logical];
+  }
+  const bool guess_ok = __syncthreads_and(full);
   if (warp == 0) {
     const int per = (items + 31) / 32;
     const int lo = min(items, lane * per), hi = min(items, lo + per);
@@ -231,8 +256,36 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
   // Two windows of 32 pages, one page per lane: [base, base + 32) in *_cur,
   // the next 32 in *_nxt (read only once the copies reach them, so that their
   // loads stay in flight meanwhile).
-  int base = 0, ph_cur, vh_cur, ph_nxt = 0, vh_nxt = 0;
-  meta(lane, ph_cur, vh_cur);
+  int base = 0, ph_cur = 0, vh_cur = 0, ph_nxt = 0, vh_nxt = 0;
+  if (guess_ok) {
+    // The first window from the values loaded under the guess (which held),
+    // with the checks of meta().
+    if (lane < np) {
+      int L = g_L;
+      if (L < 0) {
+        raise_error(a.err, SE_DEVERR_LENGTH);
+        L = 0;
+      }
+      int n_b = (L + kPageSize - 1) / kPageSize;
+      if (n_b > a.bt_stride) {
+        raise_error(a.err, SE_DEVERR_LENGTH);
+        n_b = a.bt_stride;
+        L = n_b * kPageSize;
+      }
+      if (g_logical >= 0 && g_logical < n_b) {
+        if (g_ph >= 0 && g_ph < a.num_pages) {
+          ph_cur = g_ph;
+          vh_cur = min(kPageSize, L - g_logical * kPageSize) | ((g_it % H) << 8);
+        } else {
+          raise_error(a.err, SE_DEVERR_PAGE_RANGE);
+        }
+      } else {
+        raise_error(a.err, SE_DEVERR_LENGTH);
+      }
+    }
+  } else {
+    meta(lane, ph_cur, vh_cur);
+  }
   auto lookup = [&](int kk, int& phys, int& vh) {
     if (kk < base + 32) {
       phys = __shfl_sync(0xffffffffu, ph_cur, kk & 31);
