@@ -180,7 +180,9 @@ SE_API se_status_t se_quest_score_pages(const se_paged_kv_t* kv, const void* q, 
 /*
  * se_quest_score_workspace_size -- bytes of the workspace of
  * se_quest_score_pages_ws: the group sums P_c and N_c of every request and KV
- * head (fp32, batch * num_kv_heads * 2 * head_dim values). 0 for negative sizes.
+ * head (fp32, batch * num_kv_heads * 2 * head_dim values), then 16 bytes for
+ * the counter of the scoring kernel's page pool (reset by every call).
+ * 0 for negative sizes.
  */
 SE_API size_t se_quest_score_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t head_dim);
 
@@ -192,7 +194,10 @@ SE_API size_t se_quest_score_workspace_size(int32_t batch, int32_t num_kv_heads,
  * of it. That summing waits on the memory latency of the query loads while the
  * summary reads keep HBM busy; with the workspace, a CTA's switch to another
  * request costs one read of the sums. The largest gain is for the latent cache
- * (64 query heads of 576 channels per request).
+ * (64 query heads of 576 channels per request). With the workspace the
+ * scoring kernel also balances its end: every CTA scores an equal static
+ * slice of three quarters of the pages, and the rest go in units of 8 pages
+ * to whichever warp is free (the scores do not depend on who computes them).
  *   workspace: device memory the caller owns, 16-byte aligned, at least
  *   se_quest_score_workspace_size(batch, kv->num_kv_heads, kv->head_dim) bytes
  *   (SE_ERR_WORKSPACE when smaller, SE_ERR_INVALID_ARG when NULL or

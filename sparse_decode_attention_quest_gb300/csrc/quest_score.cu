@@ -37,6 +37,12 @@
 // reads of the other CTAs: measured on GB300, 12.7 us at the start of the
 // latent kernel (64 query heads x 576 channels per request) and 15 us again in
 // the CTAs whose slice reaches a second request, which then finish last.
+// With the workspace the equal slices hold only kStaticPct percent of the
+// pages: the SMs of a GB300 gather at different speeds (steadily, from launch
+// to launch), so the rest is a pool of kUnit-page units that each warp takes
+// from, one atomic ticket per unit, once its own pages are scored. A unit is
+// streamed by one warp through the same ring (a unit that crosses a request
+// boundary is two runs). The scores do not depend on which warp computes them.
 #include "se_ptx.cuh"
 
 namespace se {
@@ -44,6 +50,9 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+constexpr int kStaticPct = 75;  // share of the pages in the equal static slices (with precomputed multipliers)
+constexpr int kUnit = 8;        // pages per unit of the pool that follows them
+constexpr int kPoolMinPages = 128;  // fair share per CTA below which every page is in the static slices
 
 struct ScoreArgs {
   KvView kv;
@@ -57,6 +66,7 @@ struct ScoreArgs {
   float* scores;
   int32_t score_stride;
   const float* pn_pre;  // P and N per request, [batch][H][2][D], from pn_kernel (or null)
+  unsigned* units;      // units of the pool taken so far (zeroed by pn_kernel; null without pn_pre)
   unsigned* err;
 };
 
@@ -199,25 +209,60 @@ __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArg
   }
   __syncthreads();
   const int total = prefix[a.batch];
-  const int per_cta = (total + gridDim.x - 1) / gridDim.x;
-  const int start = blockIdx.x * per_cta;
+  // With the precomputed multipliers (kPre) the kernel balances its end: each
+  // CTA takes an equal static slice of kStaticPct percent of the pages, and a
+  // warp that has finished its part takes units of kUnit consecutive pages
+  // from the rest, one atomic ticket per unit (pn_kernel zeroes the counter).
+  // The SMs of a GB300 stream at different speeds, steadily so from launch to
+  // launch; with equal slices the last CTA ended 11 us after the mean one.
+  // Small launches (under kPoolMinPages per CTA) keep equal slices: there the
+  // units' ticket and block-table round trips cost more than the balance wins.
+  const bool pool = kPre && a.units != nullptr && total >= kPoolMinPages * (int)gridDim.x;
+  const int per_cta = pool ? (int)((long long)total * kStaticPct / 100 / gridDim.x)
+                           : (int)((total + gridDim.x - 1) / gridDim.x);
+  const int start = min(total, (int)blockIdx.x * per_cta);
   const int end = min(total, start + per_cta);
-  if (start >= end) return;
 
-  const int b_first = find_request(prefix, a.batch, start);
-  const int b_last = find_request(prefix, a.batch, end - 1);
-  int seg = 0;
-  for (int b = b_first; b <= b_last; ++b) {
-    const int lo = max(start, prefix[b]), hi = min(end, prefix[b + 1]);  // flattened ids
-    if (lo >= hi) continue;
+  // A fragments of the m16n8k16 MMA: row n < 8 holds the high parts and row
+  // n + 8 the low parts of the multipliers of channels chan(k, n); k-step s
+  // of head h covers the head's channels 128 s .. 128 s + 127.
+  uint32_t afrag[kHeads * kKsPerHead][4];
+  int afrag_b = -1;  // request whose multipliers afrag holds (kPre)
+  auto multipliers_from = [&](const float* buf) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int h = 0; h < kHeads; ++h)
+#pragma unroll
+      for (int s = 0; s < kKsPerHead; ++s) {
+        const float* mh = buf + h * 2 * D;
+        float hi[4], lo[4];
+        const int k0 = 16 * s + 2 * t;
+        split_bf16(mh[chan(k0, g)], hi[0], lo[0]);
+        split_bf16(mh[chan(k0 + 1, g)], hi[1], lo[1]);
+        split_bf16(mh[chan(k0 + 8, g)], hi[2], lo[2]);
+        split_bf16(mh[chan(k0 + 9, g)], hi[3], lo[3]);
+        uint32_t* f = afrag[h * kKsPerHead + s];
+        f[0] = pack_bf16x2(hi[0], hi[1]);
+        f[1] = pack_bf16x2(lo[0], lo[1]);
+        f[2] = pack_bf16x2(hi[2], hi[3]);
+        f[3] = pack_bf16x2(lo[2], lo[3]);
+      }
+  };
+  auto precomputed = [&](int b) {
+    if (b != afrag_b) {
+      multipliers_from(a.pn_pre + (size_t)b * H * 2 * D);
+      afrag_b = b;
+    }
+  };
 
-    // ---- this warp's pages of the segment: lo + warp, lo + warp + 8, ...;
-    // their physical ids sit in lanes, two windows of 32 pages.
-    const int first = lo + warp;
-    const int npages = first < hi ? (hi - first + kWarps - 1) / kWarps : 0;
+  // This warp's pages first, first + stride, ... (npages of them, all of
+  // request b): their physical ids sit in lanes, two windows of 32 pages; the
+  // blocks stream through the warp's ring and the scores are stored.
+  // `prepare` runs once the first R - 1 copies are out and sets up afrag.
+  auto stream_pages = [&](int b, int first, int npages, int stride, auto&& prepare) {
     const int32_t* bt_row = a.block_table + (size_t)b * a.bt_stride;
     const int p_first = first - prefix[b];  // page id of this warp's first page
-    auto phys_of = [&](int i) { return i < npages ? bt_row[p_first + kWarps * i] : -1; };
+    auto phys_of = [&](int i) { return i < npages ? bt_row[p_first + stride * i] : -1; };
     int base = 0;
     int ph_cur = phys_of(lane), ph_nxt = phys_of(lane + 32);
     auto lookup = [&](int i) {
@@ -237,91 +282,12 @@ __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArg
         }
       }
     };
-    // The first R - 1 pages go out before the pre-reduction below.
 #pragma unroll 1
     for (int i = 0; i < R - 1; ++i) {
       if (i < npages) issue(i);
       cp_async_commit();
     }
-
-    // ---- P and N of request b: precomputed (kPre), or reduced here into
-    // buffer seg & 1. Each (KV head, 8 channels) item is summed by S adjacent
-    // lanes over S runs of the group's query heads and the runs are added with
-    // a fixed butterfly (the result does not depend on timing). The other
-    // buffer may still be read by nobody: each lane copies its multipliers
-    // into registers right after the barrier below.
-    const float* buf;
-    if (kPre) {
-      buf = a.pn_pre + (size_t)b * H * 2 * D;
-    } else {
-      float* wbuf = pn + (seg & 1) * H * 2 * D;
-      buf = wbuf;
-      const uint16_t* qb = a.q + (size_t)b * H * a.group * D;
-      const int S = pn_lanes(a.group);
-      const int tasks = H * (D / 8) * S;
-      for (int t0 = warp * 32; t0 < tasks; t0 += kThreads) {  // warp-uniform
-        const int task = t0 + lane;
-        const bool live = task < tasks;
-        const int it = task / S, sl = task % S;
-        const int h = it / (D / 8), c0 = (it % (D / 8)) * 8;
-        float P[8], N[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) P[e] = N[e] = 0.f;
-        if (live) {
-          const int g0 = sl * a.group / S, g1 = (sl + 1) * a.group / S;
-          const uint16_t* qh = qb + (size_t)h * a.group * D + c0;
-          int g = g0;
-          for (; g + 4 <= g1; g += 4) {
-            uint4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const uint4*>(qh + (size_t)(g + u) * D);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) add_pos_neg(v[u], P, N);
-          }
-          for (; g < g1; ++g) add_pos_neg(*reinterpret_cast<const uint4*>(qh + (size_t)g * D), P, N);
-        }
-        for (int o = 1; o < S; o <<= 1) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            P[e] += __shfl_xor_sync(0xffffffffu, P[e], o);
-            N[e] += __shfl_xor_sync(0xffffffffu, N[e], o);
-          }
-        }
-        if (live && sl == 0) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            wbuf[(h * 2 + 0) * D + c0 + e] = N[e];  // multiplies the min row
-            wbuf[(h * 2 + 1) * D + c0 + e] = P[e];  // multiplies the max row
-          }
-        }
-      }
-      __syncthreads();
-    }
-    // A fragments of the m16n8k16 MMA: row n < 8 holds the high parts and row
-    // n + 8 the low parts of the multipliers of channels chan(k, n); k-step s
-    // of head h covers the head's channels 128 s .. 128 s + 127.
-    uint32_t afrag[kHeads * kKsPerHead][4];
-    {
-      const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-      for (int h = 0; h < kHeads; ++h)
-#pragma unroll
-        for (int s = 0; s < kKsPerHead; ++s) {
-          const float* mh = buf + h * 2 * D;
-          float hi[4], lo[4];
-          const int k0 = 16 * s + 2 * t;
-          split_bf16(mh[chan(k0, g)], hi[0], lo[0]);
-          split_bf16(mh[chan(k0 + 1, g)], hi[1], lo[1]);
-          split_bf16(mh[chan(k0 + 8, g)], hi[2], lo[2]);
-          split_bf16(mh[chan(k0 + 9, g)], hi[3], lo[3]);
-          uint32_t* f = afrag[h * kKsPerHead + s];
-          f[0] = pack_bf16x2(hi[0], hi[1]);
-          f[1] = pack_bf16x2(lo[0], lo[1]);
-          f[2] = pack_bf16x2(hi[2], hi[3]);
-          f[3] = pack_bf16x2(lo[2], lo[3]);
-        }
-    }
-    ++seg;
+    prepare();
 
     float* out_b = a.scores + (size_t)b * H * a.score_stride;
     for (int i = 0; i < npages; ++i) {
@@ -367,11 +333,100 @@ __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArg
         acc[h] = (2 * t == g ? d[0] + d[2] : 0.f) + (2 * t + 1 == g ? d[1] + d[3] : 0.f);
       }
       __syncwarp();  // every lane has read stage i % R before it is refilled
-      float* out = out_b + p_first + kWarps * i;
+      float* out = out_b + p_first + stride * i;
       reduce_and_store<kHeads>(acc, lane, out, a.score_stride, good);
     }
-    cp_async_wait<0>();  // nothing of this segment is in flight when the ring is reused
+    cp_async_wait<0>();  // nothing of these pages is in flight when the ring is reused
     __syncwarp();
+  };
+
+  // ---- the static slice, cut at request boundaries into segments; each of
+  // the 8 warps takes every eighth page of a segment.
+  if (start < end) {
+    const int b_first = find_request(prefix, a.batch, start);
+    const int b_last = find_request(prefix, a.batch, end - 1);
+    int seg = 0;
+    for (int b = b_first; b <= b_last; ++b) {
+      const int lo = max(start, prefix[b]), hi = min(end, prefix[b + 1]);  // flattened ids
+      if (lo >= hi) continue;
+      const int first = lo + warp;
+      const int npages = first < hi ? (hi - first + kWarps - 1) / kWarps : 0;
+      stream_pages(b, first, npages, kWarps, [&]() {
+        if (kPre) {
+          precomputed(b);
+        } else {
+          // P and N of request b reduced here into buffer seg & 1. Each
+          // (KV head, 8 channels) item is summed by S adjacent lanes over S
+          // runs of the group's query heads and the runs are added with a
+          // fixed butterfly (the result does not depend on timing). The other
+          // buffer may still be read by nobody: each lane copies its
+          // multipliers into registers right after the barrier below.
+          float* wbuf = pn + (seg & 1) * H * 2 * D;
+          const uint16_t* qb = a.q + (size_t)b * H * a.group * D;
+          const int S = pn_lanes(a.group);
+          const int tasks = H * (D / 8) * S;
+          for (int t0 = warp * 32; t0 < tasks; t0 += kThreads) {  // warp-uniform
+            const int task = t0 + lane;
+            const bool live = task < tasks;
+            const int it = task / S, sl = task % S;
+            const int h = it / (D / 8), c0 = (it % (D / 8)) * 8;
+            float P[8], N[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) P[e] = N[e] = 0.f;
+            if (live) {
+              const int g0 = sl * a.group / S, g1 = (sl + 1) * a.group / S;
+              const uint16_t* qh = qb + (size_t)h * a.group * D + c0;
+              int g = g0;
+              for (; g + 4 <= g1; g += 4) {
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const uint4*>(qh + (size_t)(g + u) * D);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) add_pos_neg(v[u], P, N);
+              }
+              for (; g < g1; ++g) add_pos_neg(*reinterpret_cast<const uint4*>(qh + (size_t)g * D), P, N);
+            }
+            for (int o = 1; o < S; o <<= 1) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                P[e] += __shfl_xor_sync(0xffffffffu, P[e], o);
+                N[e] += __shfl_xor_sync(0xffffffffu, N[e], o);
+              }
+            }
+            if (live && sl == 0) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                wbuf[(h * 2 + 0) * D + c0 + e] = N[e];  // multiplies the min row
+                wbuf[(h * 2 + 1) * D + c0 + e] = P[e];  // multiplies the max row
+              }
+            }
+          }
+          __syncthreads();
+          multipliers_from(wbuf);
+        }
+      });
+      ++seg;
+    }
+  }
+
+  // ---- the pool: units of kUnit consecutive pages, taken by whichever warp
+  // is free (a unit that crosses a request boundary is two runs).
+  if (pool) {
+    const int dyn0 = per_cta * (int)gridDim.x;
+    while (true) {
+      unsigned u = 0;
+      if (lane == 0) u = atomicAdd(a.units, 1u);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      const long long u_lo = (long long)dyn0 + (long long)u * kUnit;
+      if (u_lo >= total) break;
+      const int p_hi = min(total, (int)u_lo + kUnit);
+      for (int p = (int)u_lo; p < p_hi;) {
+        const int b = find_request(prefix, a.batch, p);
+        const int r_hi = min(p_hi, prefix[b + 1]);
+        stream_pages(b, p, r_hi - p, 1, [&]() { precomputed(b); });
+        p = r_hi;
+      }
+    }
   }
 }
 
@@ -383,9 +438,10 @@ constexpr int kPnThreads = 640;  // up to 640 tasks in one round (d 128 with 5 K
 // task's run are issued before the first is summed.
 template <int D>
 __global__ void __launch_bounds__(kPnThreads) pn_kernel(const uint16_t* __restrict__ q, int32_t H, int32_t group,
-                                                  float* __restrict__ pn_out) {
+                                                  float* __restrict__ pn_out, unsigned* __restrict__ units) {
   pdl_enter();
   const int b = blockIdx.x;
+  if (b == 0 && threadIdx.x == 0) *units = 0u;  // the scoring kernel's pool starts empty
   const int lane = threadIdx.x & 31;
   const int S = pn_lanes(group);
   const int tasks = H * (D / 8) * S;
@@ -454,7 +510,7 @@ cudaError_t launch_t(const ScoreArgs& a, int sm_count, cudaStream_t stream) {
   const int threads = min(kPnThreads, (tasks + 31) / 32 * 32);
   {
     const cudaError_t le = launch_pdl(pn_kernel<D>, dim3(a.batch), dim3(threads), 0, stream, a.q, H, a.group,
-                                      const_cast<float*>(a.pn_pre));
+                                      const_cast<float*>(a.pn_pre), a.units);
     if (le != cudaSuccess) return le;
   }
   return launch_score<D, T, R, true>(a, sm_count, stream);
@@ -463,7 +519,8 @@ cudaError_t launch_t(const ScoreArgs& a, int sm_count, cudaStream_t stream) {
 }  // namespace
 
 size_t score_pn_bytes(int32_t batch, int32_t num_kv_heads, int32_t head_dim) {
-  return (size_t)batch * num_kv_heads * 2 * head_dim * sizeof(float);
+  // P and N, then the pool's unit counter (16 bytes)
+  return (size_t)batch * num_kv_heads * 2 * head_dim * sizeof(float) + 16;
 }
 
 bool score_pages_supported(int num_kv_heads, int head_dim) {
@@ -488,6 +545,7 @@ cudaError_t launch_score_pages(const KvView& kv, const uint16_t* q, int32_t num_
   a.scores = scores;
   a.score_stride = score_stride;
   a.pn_pre = pn_ws;
+  a.units = pn_ws ? reinterpret_cast<unsigned*>(pn_ws + (size_t)batch * kv.num_kv_heads * 2 * kv.head_dim) : nullptr;
   a.err = err;
   // Ring depth per head count: about 96 KB of summary blocks in flight per CTA,
   // two CTAs per SM.

@@ -90,8 +90,8 @@ def test_score_validation(se_lib):
 
 def test_score_workspace_validation(se_lib):
     # the group sums P and N: batch x KV heads x 2 x head_dim floats
-    assert se_lib.se_quest_score_workspace_size(2, 4, 128) == 2 * 4 * 2 * 128 * 4
-    assert se_lib.se_quest_score_workspace_size(64, 1, 576) == 64 * 2 * 576 * 4
+    assert se_lib.se_quest_score_workspace_size(2, 4, 128) == 2 * 4 * 2 * 128 * 4 + 16
+    assert se_lib.se_quest_score_workspace_size(64, 1, 576) == 64 * 2 * 576 * 4 + 16
     assert se_lib.se_quest_score_workspace_size(-1, 4, 128) == 0
     f = se_lib.se_quest_score_pages_ws
     kv = _kv()
