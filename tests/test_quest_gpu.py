@@ -334,6 +334,54 @@ def test_short_workspace_is_rejected(cuda_device):
 
 
 # ---------------------------------------------------------------- full size, sampled requests
+@pytest.mark.parametrize("kind", ["h4", "h8", "latent"])
+def test_score_unit_pool_gives_the_same_scores(cuda_device, kind):
+    # At least 128 candidate pages per CTA: with the workspace the scoring kernel
+    # puts a quarter of the pages in a pool of 8-page units that free warps take,
+    # so which warp scores a page depends on timing. Every score must still equal,
+    # bit for bit, the one of the call without the workspace (equal slices only).
+    if kind == "latent":
+        wl = MLA_GLM_QUEST_32K.scaled(batch=22, seed=81)
+    else:
+        hkv = 4 if kind == "h4" else 8
+        wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=6, num_kv_heads=hkv, num_q_heads=4 * hkv,
+                                             context_min=120000, context_max=131072, append=False,
+                                             seed=80 + hkv)
+    x, plain, pre = _scores_both_ways_dev(wl, cuda_device)
+    total = sum(max(n - 1, 0) for n in x.pages_per_request)
+    assert total >= 128 * 2 * torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    _check_same_scores(x, plain, pre)
+
+
+def _scores_both_ways_dev(wl, dev):
+    """_scores_both_ways with the inputs generated on the device (large workloads)."""
+    x, step, b, a = _prepare(wl, dev, device_gen=True)
+    q = x.q.to(dev)
+    plain = torch.full_like(step.scores, float("nan"))
+    pre = torch.full_like(step.scores, float("nan"))
+    se.se_quest_score_pages(step.kv, q, step.block_table, a, step.max_seq_len, plain)
+    ws = torch.empty(se.se_quest_score_workspace_size(wl.batch, wl.num_kv_heads, wl.head_dim), dtype=torch.uint8,
+                     device=dev)
+    for _ in range(2):  # the second call finds the pool counter as the first left it
+        pre.fill_(float("nan"))
+        se.se_quest_score_pages_ws(step.kv, q, step.block_table, a, step.max_seq_len, pre, ws)
+    torch.cuda.synchronize()
+    return x, plain.cpu(), pre.cpu()
+
+
+@pytest.mark.parametrize("hq,hkv,topk", [(32, 2, 600), (32, 4, 400)])
+def test_decode_items_over_many_slices(cuda_device, hq, hkv, topk):
+    # One request whose items (KV heads) hold hundreds of selected pages: at 16
+    # pages per CTA slice each item spans 25-40 CTAs, so the CTA that completes an
+    # item's count merges its partials in many batches of four, and every CTA's
+    # slice ends mid-item. Groups of 16 (the two-row MMA states) and 8 query heads.
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=1, num_q_heads=hq, num_kv_heads=hkv, context_min=40000,
+                                         context_max=40000, topk_pages=topk, append=False, seed=90 + hkv)
+    x, step, b, a = _prepare(wl, cuda_device)
+    _run(x, step, b, a, cuda_device)
+    compare_decode(x, step, [0], _scale(wl), f"many slices G={hq // hkv}")
+
+
 def test_full_qwen3_4b_32k_sampled(cuda_device):
     wl = QWEN3_4B_QUEST_32K
     x, step, b, a = _prepare(wl, cuda_device, device_gen=True)
