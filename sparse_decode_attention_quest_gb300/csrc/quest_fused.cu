@@ -13,8 +13,9 @@
 //      scores 4 pages per iteration (8 lanes per 512 B summary block of the KV
 //      head), streamed through an 8-stage cp.async ring, and stores the scores'
 //      order keys straight into rank 0's shared memory;
-//   2. select (rank 0): radix-selects the topk best (ties to the lower page;
-//      warp-aggregated histogram atomics) and writes the kept
+//   2. select (rank 0): bucket-selects the topk best (1,024 linear score
+//      buckets, the threshold bucket's members ranked exactly, ties to the
+//      lower page; a radix select when that bucket is crowded) and writes the kept
 //      pages, ascending (sink window, selected, recent window), to its shared
 //      memory and to the caller's selection arrays;
 //   3. decode: rank r takes the kept pages r, r + C, ...; its 8 warps stream
@@ -46,6 +47,8 @@ constexpr int kPageBytes = 2 * kTileBytes;            // K then V
 constexpr int kDecStages = 3;
 constexpr int kMaxCand = 8192;                        // candidate pages per request
 constexpr int kMaxKept = 2048;                        // kept pages per (request, KV head)
+constexpr int kSelBuckets = 1024;                     // linear score buckets of the selection
+constexpr int kSelMaxMembers = 512;                   // members of the threshold bucket ranked one by one
 constexpr int kRegionA = kWarps * kDecStages * kPageBytes;  // 192 KB, reused phase by phase
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -53,6 +56,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kScoreRingOff = 0;                                                    // [8][8][4][512]
 constexpr int kKeysOff = kScoreRingOff + kWarps * kScoreStages * kPagesPerIter * kBlk;  // uint32 [kMaxCand]
 static_assert(kKeysOff + kMaxCand * 4 <= kRegionA, "phase-1/2 storage fits region A");
+static_assert(kSelBuckets * 4 + kSelMaxMembers * 8 + kMaxCand / 8 + 2 * kWarps * 4 + 16 <= kKeysOff,
+              "the selection's scratch fits the idle score ring");
 static_assert(kWarps * 16 * kD * 4 <= kRegionA, "warp states fit region A");
 
 struct FusedArgs {
@@ -95,6 +100,10 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// The score whose order key is u (order_key's inverse).
+__device__ __forceinline__ float key_value(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
 
 // Candidate pages [c0, c1): none of the first `sink` tokens, none of the last
@@ -309,75 +318,203 @@ __global__ void __launch_bounds__(kThreads, 1) quest_fused_kernel(const FusedArg
       cnt = n;
       for (int i = tid; i < n; i += kThreads) sel_s[i] = i;
     } else {
-      // radix select of the topk-th largest key T (4 passes of 8 bits)
-      uint32_t prefix = 0, mask = 0;
-      int remaining = a.topk;
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
-        __syncthreads();
-        for (int j0 = 0; j0 < Cn; j0 += kThreads) {  // warp-uniform: one atomic per distinct digit and warp
-          const int j = j0 + tid;
-          int digit = 256;
-          if (j < Cn) {
-            const uint32_t u = keys[j];
-            if ((u & mask) == prefix) digit = (int)((u >> shift) & 255u);
+      // Bucket select (one pass over the keys): the scores' min and max over
+      // the finite ones, kSelBuckets linear buckets between them (monotone in
+      // the score), the bucket B that holds the topk-th largest (every key in a
+      // higher bucket is selected), and an exact ranking of B's members by
+      // order key, then lower index. Warp w owns the contiguous candidates
+      // [32 E w, 32 E (w + 1)), its lane l the candidates 32 E w + 32 i + l
+      // (conflict-free reads), and a ballot scan per warp keeps the output
+      // ascending. A crowded B
+      // (near-identical scores) falls back to a radix select over all keys.
+      // Scratch: the score ring of region A, idle once the scores are in.
+      int* bhist = reinterpret_cast<int*>(regA + kScoreRingOff);                  // [kSelBuckets]
+      uint32_t* mkey = reinterpret_cast<uint32_t*>(bhist + kSelBuckets);          // [kSelMaxMembers]
+      int* midx = reinterpret_cast<int*>(mkey + kSelMaxMembers);                  // [kSelMaxMembers]
+      uint32_t* selbits = reinterpret_cast<uint32_t*>(midx + kSelMaxMembers);     // [kMaxCand / 32]
+      float* wmm = reinterpret_cast<float*>(selbits + kMaxCand / 32);             // [2][kWarps]
+      int* sinfo = reinterpret_cast<int*>(wmm + 2 * kWarps);                      // [4]
+      const int E = (Cn + kThreads - 1) / kThreads;  // candidates per lane
+      const int wbase = warp * 32 * E;
+      float lmin = INFINITY, lmax = -INFINITY;
+      for (int i = 0; i < E; ++i) {
+        const int j = wbase + 32 * i + lane;
+        if (j >= Cn) break;
+        const float v = key_value(keys[j]);
+        if (isfinite(v)) {
+          lmin = fminf(lmin, v);
+          lmax = fmaxf(lmax, v);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        lmin = fminf(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
+        lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+      }
+      if (lane == 0) {
+        wmm[warp] = lmin;
+        wmm[kWarps + warp] = lmax;
+      }
+      for (int i = tid; i < kSelBuckets; i += kThreads) bhist[i] = 0;
+      for (int i = tid; i < kMaxCand / 32; i += kThreads) selbits[i] = 0u;
+      if (tid == 0) sinfo[2] = 0;
+      __syncthreads();
+      float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        mn = fminf(mn, wmm[w]);
+        mx = fmaxf(mx, wmm[kWarps + w]);
+      }
+      const float scale = (mx > mn) ? (float)kSelBuckets / (mx - mn) : 0.f;
+      auto bucket_of = [&](float v) {
+        if (isfinite(v)) return min(kSelBuckets - 1, max(0, (int)((v - mn) * scale)));
+        return v > 0.f ? kSelBuckets - 1 : 0;  // +inf on top; -inf and NaN in bucket 0
+      };
+      for (int i = 0; i < E; ++i) {
+        const int j = wbase + 32 * i + lane;
+        if (j >= Cn) break;
+        atomicAdd(&bhist[bucket_of(key_value(keys[j]))], 1);
+      }
+      __syncthreads();
+      {
+        // thread t owns buckets [4 t, 4 t + 4); the bucket of the topk-th largest
+        static_assert(kSelBuckets == 4 * kThreads, "four buckets per thread");
+        int hc[4], sum = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          hc[q] = bhist[4 * tid + q];
+          sum += hc[q];
+        }
+        int tot;
+        const int below = block_scan(sum, wtot, warp, lane, tot);
+        int cum = tot - below - sum;  // keys in the buckets above this thread's
+#pragma unroll
+        for (int q = 3; q >= 0; --q) {
+          if (cum < a.topk && a.topk <= cum + hc[q]) {
+            sinfo[0] = 4 * tid + q;
+            sinfo[1] = cum;
           }
-          const unsigned peers = __match_any_sync(0xffffffffu, digit);
-          if (digit < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+          cum += hc[q];
+        }
+      }
+      __syncthreads();
+      const int B = sinfo[0];
+      const int need = a.topk - sinfo[1];  // members of bucket B to take, >= 1
+      const int m = bhist[B];
+      if (m <= kSelMaxMembers) {
+        for (int i = 0; i < E; ++i) {
+          const int j = wbase + 32 * i + lane;
+          if (j >= Cn) break;
+          const uint32_t u = keys[j];
+          if (bucket_of(key_value(u)) == B) {
+            const int slot = atomicAdd(&sinfo[2], 1);
+            mkey[slot] = u;
+            midx[slot] = j;
+          }
         }
         __syncthreads();
-        if (warp == 0) {
-          int g8[8], gsum = 0;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            g8[q] = hist[lane * 8 + q];
-            gsum += g8[q];
+        for (int i = tid; i < m; i += kThreads) {
+          const uint32_t ku = mkey[i];
+          const int ji = midx[i];
+          int rank = 0;
+          for (int x = 0; x < m; ++x) {
+            const uint32_t kx = mkey[x];
+            rank += (kx > ku || (kx == ku && midx[x] < ji)) ? 1 : 0;
           }
-          int incl = gsum;  // keys in bins >= lane * 8
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_down_sync(0xffffffffu, incl, o);
-            if (lane + o < 32) incl += t;
+          if (rank < need) atomicOr(&selbits[ji >> 5], 1u << (ji & 31));
+        }
+        __syncthreads();
+        auto selected = [&](int j) {
+          if (j >= Cn) return false;
+          const int bk = bucket_of(key_value(keys[j]));
+          return bk > B || (bk == B && ((selbits[j >> 5] >> (j & 31)) & 1u));
+        };
+        int n_warp = 0;  // this warp's selected candidates
+        for (int i = 0; i < E; ++i) n_warp += __popc(__ballot_sync(0xffffffffu, selected(wbase + 32 * i + lane)));
+        if (lane == 0) wtot[warp] = n_warp;
+        __syncthreads();
+        int pos = 0;
+        for (int w = 0; w < warp; ++w) pos += wtot[w];
+        const unsigned below = (1u << lane) - 1u;
+        for (int i = 0; i < E; ++i) {
+          const int j = wbase + 32 * i + lane;
+          const bool take = selected(j);
+          const unsigned bal = __ballot_sync(0xffffffffu, take);
+          const int at = pos + __popc(bal & below);
+          if (take && at < a.topk) sel_s[c0 + at] = c0 + j;
+          pos += __popc(bal);
+        }
+      } else {
+        // radix select of the topk-th largest key T (4 passes of 8 bits)
+        uint32_t prefix = 0, mask = 0;
+        int remaining = a.topk;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+          for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+          __syncthreads();
+          for (int j0 = 0; j0 < Cn; j0 += kThreads) {  // warp-uniform: one atomic per distinct digit and warp
+            const int j = j0 + tid;
+            int digit = 256;
+            if (j < Cn) {
+              const uint32_t u = keys[j];
+              if ((u & mask) == prefix) digit = (int)((u >> shift) & 255u);
+            }
+            const unsigned peers = __match_any_sync(0xffffffffu, digit);
+            if (digit < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
           }
-          const int above = incl - gsum;
-          if (above < remaining && remaining <= incl) {
-            int cum = above;
-            for (int q = 7; q >= 0; --q) {
-              if (cum + g8[q] >= remaining) {
-                misc[1] = lane * 8 + q;
-                misc[2] = cum;
-                break;
+          __syncthreads();
+          if (warp == 0) {
+            int g8[8], gsum = 0;
+  #pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              g8[q] = hist[lane * 8 + q];
+              gsum += g8[q];
+            }
+            int incl = gsum;  // keys in bins >= lane * 8
+  #pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int t = __shfl_down_sync(0xffffffffu, incl, o);
+              if (lane + o < 32) incl += t;
+            }
+            const int above = incl - gsum;
+            if (above < remaining && remaining <= incl) {
+              int cum = above;
+              for (int q = 7; q >= 0; --q) {
+                if (cum + g8[q] >= remaining) {
+                  misc[1] = lane * 8 + q;
+                  misc[2] = cum;
+                  break;
+                }
+                cum += g8[q];
               }
-              cum += g8[q];
             }
           }
+          __syncthreads();
+          remaining -= misc[2];
+          prefix |= (uint32_t)misc[1] << shift;
+          mask |= 255u << shift;
+          __syncthreads();
         }
-        __syncthreads();
-        remaining -= misc[2];
-        prefix |= (uint32_t)misc[1] << shift;
-        mask |= 255u << shift;
-        __syncthreads();
-      }
-      // selected: keys above T, then the lowest-index keys equal to T; thread t owns
-      // the contiguous candidates [t E, t E + E) so the output comes out ascending
-      const int E = (Cn + kThreads - 1) / kThreads;
-      const int j0 = min(Cn, tid * E), j1 = min(Cn, j0 + E);
-      int n_eq = 0;
-      for (int j = j0; j < j1; ++j) n_eq += keys[j] == prefix ? 1 : 0;
-      int tot;
-      int eq_rank = block_scan(n_eq, wtot, warp, lane, tot);
-      int n_sel = 0;
-      for (int j = j0; j < j1; ++j) {
-        const uint32_t u = keys[j];
-        if (u > prefix || (u == prefix && eq_rank++ < remaining)) ++n_sel;
-      }
-      int pos = block_scan(n_sel, wtot, warp, lane, tot);
-      eq_rank -= n_eq;  // back to this thread's first equal key
-      for (int j = j0; j < j1; ++j) {
-        const uint32_t u = keys[j];
-        if (u > prefix || (u == prefix && eq_rank++ < remaining)) {
-          if (pos < a.topk) sel_s[c0 + pos] = c0 + j;
-          ++pos;
+        // selected: keys above T, then the lowest-index keys equal to T; thread t owns
+        // the contiguous candidates [t E, t E + E) so the output comes out ascending
+        const int E = (Cn + kThreads - 1) / kThreads;
+        const int j0 = min(Cn, tid * E), j1 = min(Cn, j0 + E);
+        int n_eq = 0;
+        for (int j = j0; j < j1; ++j) n_eq += keys[j] == prefix ? 1 : 0;
+        int tot;
+        int eq_rank = block_scan(n_eq, wtot, warp, lane, tot);
+        int n_sel = 0;
+        for (int j = j0; j < j1; ++j) {
+          const uint32_t u = keys[j];
+          if (u > prefix || (u == prefix && eq_rank++ < remaining)) ++n_sel;
+        }
+        int pos = block_scan(n_sel, wtot, warp, lane, tot);
+        eq_rank -= n_eq;  // back to this thread's first equal key
+        for (int j = j0; j < j1; ++j) {
+          const uint32_t u = keys[j];
+          if (u > prefix || (u == prefix && eq_rank++ < remaining)) {
+            if (pos < a.topk) sel_s[c0 + pos] = c0 + j;
+            ++pos;
+          }
         }
       }
       for (int i = tid; i < c0; i += kThreads) sel_s[i] = i;

@@ -127,3 +127,39 @@ def test_fused_step_is_repeatable(cuda_device):
                 assert torch.equal(step.sel[b, h, :n], sel0[b, h, :n])
         assert torch.equal(step.out.view(torch.int16), out0.view(torch.int16))
         assert torch.equal(step.lse, lse0)
+
+
+@pytest.mark.parametrize("context,topk,period", [(4096, 32, 5), (131072, 256, 20)])
+def test_fused_selection_with_tied_pages(cuda_device, context, topk, period):
+    # Every page of a request repeats the keys of one of its first `period`
+    # pages, so the page scores take `period` values, each on many pages, and the
+    # k-th largest sits inside a tied level. The selection must take the tied
+    # pages with the lowest ids, in the one-launch step (bucket select over the
+    # cluster's scores; 8 candidates per thread at 4K, 32 at 128K) and in the
+    # four-call path alike; both read their scores off equal keys, so equal
+    # pages score equally on each side.
+    wl = QWEN3_4B_QUEST_32K.scaled(batch=1, num_q_heads=16, num_kv_heads=4, context_min=context,
+                                   context_max=context, topk_pages=topk, append=False, seed=95)
+    x, fused, a = _prepare(wl, cuda_device, device_gen=context > 8192)
+    n = context // wl.page_size
+    bt = x.block_table[0].long().to(cuda_device)
+    src = bt[torch.arange(n, device=cuda_device) % period]
+    fused.k_cache[bt[:n]] = fused.k_cache[src]
+    fused.build_summaries(a)
+    sep = QuestDecodeStep(fused.k_cache, fused.v_cache, new_summary(fused.k_cache), x.block_table.to(cuda_device),
+                          wl.num_q_heads, wl.topk_pages, context)
+    sep.build_summaries(a)
+    q = x.q.to(cuda_device)
+    fused.run_fused(q, a)
+    sep.run(q, a)
+    torch.cuda.synchronize()
+    scores = sep.scores[0].cpu()
+    for h in range(wl.num_kv_heads):
+        s = scores[h, :n - 1]
+        order = sorted(range(n - 1), key=lambda p: (-float(s[p]), p))
+        want = sorted(order[:topk]) + [n - 1]
+        level = float(s[order[topk - 1]])
+        assert sum(1 for p in range(n - 1) if float(s[p]) == level) > 1, "the k-th score must be tied"
+        assert int(sep.counts[0, h]) == topk + 1 and int(fused.counts[0, h]) == topk + 1
+        assert sep.sel[0, h, :topk + 1].tolist() == want, h
+        assert fused.sel[0, h, :topk + 1].tolist() == want, h
