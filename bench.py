@@ -651,9 +651,14 @@ def _snapkv_wl(name):
 
 def _e2e(args, step, x, before, after, stream, flush, dev):
     """The step as a server runs it: the step's inputs (q, k_new, v_new and both lengths)
-    packed in one pinned host buffer and copied to the device in one transfer, the four
-    C-ABI calls, the output copied back to pinned host memory."""
+    packed in one pinned host buffer and copied to the device in one transfer, the step
+    through the library, the output copied back to pinned host memory. The step is the
+    four C-ABI calls recorded once with se_capture_begin / se_capture_end and replayed
+    with se_graph_launch every step; the same path with the four calls made live every
+    step is timed too (``calls_ms_per_step``)."""
     import torch
+
+    import sparse_decode_attention_quest_gb300 as se
     wl = x.workload
     parts = [x.q, x.k_new, x.v_new, before, after]
     offs, size = [], 0
@@ -672,42 +677,58 @@ def _e2e(args, step, x, before, after, stream, flush, dev):
     h2d = size
     d2h = h_out.numel() * h_out.element_size()
 
-    def e2e_step(ev0=None, ev1=None):
+    def live(s):
+        step.run(d_q, d_after, d_kn, d_vn, d_before, stream=s)
+
+    se.se_capture_begin(stream)
+    live(stream)
+    graph = se.se_capture_end(stream)
+
+    def e2e_step(replay, ev0=None, ev1=None):
         with torch.cuda.stream(stream):
             if ev0 is not None:
                 ev0.record(stream)
             d_buf.copy_(h_buf, non_blocking=True)
-            step.run(d_q, d_after, d_kn, d_vn, d_before, stream=stream)
+            if replay:
+                graph.launch(stream)
+            else:
+                live(stream)
             h_out.copy_(step.out, non_blocking=True)
             if ev1 is not None:
                 ev1.record(stream)
 
-    for _ in range(args.warmup):
-        flush(1.0)
-        e2e_step()
-    torch.cuda.synchronize()
-    n = max(10, args.steps // 4)
-    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    host_ms = []
-    for i in range(n):
-        with torch.cuda.stream(stream):
-            flush(float(i))
-        stream.synchronize()  # the flush is done before the clock starts
-        t0 = time.perf_counter()
-        e2e_step(*pairs[i])
-        stream.synchronize()  # the output is in host memory
-        host_ms.append((time.perf_counter() - t0) * 1e3)
-    torch.cuda.synchronize()
-    ms = statistics.mean(host_ms)
-    stream_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    def timed(replay):
+        for _ in range(args.warmup):
+            flush(1.0)
+            e2e_step(replay)
+        torch.cuda.synchronize()
+        n = max(10, args.steps // 4)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        host_ms = []
+        for i in range(n):
+            with torch.cuda.stream(stream):
+                flush(float(i))
+            stream.synchronize()  # the flush is done before the clock starts
+            t0 = time.perf_counter()
+            e2e_step(replay, *pairs[i])
+            stream.synchronize()  # the output is in host memory
+            host_ms.append((time.perf_counter() - t0) * 1e3)
+        torch.cuda.synchronize()
+        return n, statistics.mean(host_ms), statistics.mean(a.elapsed_time(b) for a, b in pairs)
+
+    n, ms, stream_ms = timed(True)
+    _, calls_ms, calls_stream_ms = timed(False)
+    graph.destroy()
     return {"value": wl.batch / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": n,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "timing": "host wall clock per step: from before the host-to-device copy is enqueued to the return of "
-                      "a stream synchronize after the device-to-host copy of the output (argument marshalling, "
-                      "launches, copies and kernels included; the L2 flush before it excluded)",
+                      "a stream synchronize after the device-to-host copy of the output (launches, copies and "
+                      "kernels included; the L2 flush before it excluded)",
             "stream_ms_per_step": stream_ms,
-            "path": "pinned host q/k_new/v_new/lengths (one packed buffer, one copy) -> device, the four C-ABI "
-                    "calls, output -> pinned host"}
+            "calls_ms_per_step": calls_ms, "calls_stream_ms_per_step": calls_stream_ms,
+            "path": "pinned host q/k_new/v_new/lengths (one packed buffer, one copy) -> device, the step's four "
+                    "C-ABI calls recorded once (se_capture_begin / se_capture_end) and replayed with "
+                    "se_graph_launch, output -> pinned host; calls_ms_per_step: the four calls made live instead"}
 
 
 # --------------------------------------------------------------------------- reference arm

@@ -428,6 +428,43 @@ SE_API se_status_t se_snapkv_score_and_compact_windowed(const se_paged_kv_t* src
                                                         size_t workspace_bytes, void* stream);
 
 /*
+ * Replayable steps. A decode loop makes the same library calls every step on
+ * the same buffers; only the values in device memory change (queries, new K/V
+ * rows, lengths, selections), and every kernel of the library reads those
+ * values from device memory. These calls record the asynchronous work of a
+ * sequence of library calls into a CUDA graph once, so that each later step
+ * costs one launch instead of the calls' host-side checks and launches. The
+ * pages have no counterpart: this is host plumbing around their hot path.
+ *
+ * se_capture_begin -- starts recording the work issued on `stream` (a stream
+ *   the caller created, not the legacy default stream; thread-local capture
+ *   mode). It first sets up this device's library context, so that no call
+ *   made while recording allocates. Between begin and end, make the library
+ *   calls of one step on `stream`, each exactly as it would be made live:
+ *   their argument checks run now, once, and only their kernels and
+ *   asynchronous copies and sets are recorded. A call that fails while
+ *   recording leaves the capture to be ended and its graph discarded.
+ *   se_sparse_paged_decode_noalloc may be recorded after one live call of it
+ *   on the device (that call looks up the address of its built-in array).
+ * se_capture_end -- ends the recording on `stream` and instantiates it into
+ *   *graph (host handle; owned by the caller, freed with se_graph_destroy).
+ * se_graph_launch -- runs the recorded step on `stream` (any stream of the
+ *   device it was recorded on). Every buffer the recorded calls named must
+ *   still exist, and the sizes passed to them (batch, strides, maximum
+ *   lengths) still hold; the values in the buffers may change freely between
+ *   launches, as in the live calls.
+ * se_graph_destroy -- frees a recorded step (NULL: no-op).
+ * Errors: SE_ERR_INVALID_ARG for a NULL stream, graph or handle; SE_ERR_CUDA
+ * for a failing CUDA call (begin, end, instantiate or launch), with the CUDA
+ * error in se_last_error_detail().
+ */
+typedef struct se_graph_s* se_graph_t;
+SE_API se_status_t se_capture_begin(void* stream);
+SE_API se_status_t se_capture_end(void* stream, se_graph_t* graph);
+SE_API se_status_t se_graph_launch(se_graph_t graph, void* stream);
+SE_API void se_graph_destroy(se_graph_t graph);
+
+/*
  * se_debug_snapkv_wait_probe -- test hook for the bounded waits; it computes
  * nothing (the pages have no counterpart). In the next se_snapkv_window_scores
  * call issued from this host thread (also inside se_snapkv_score_and_compact*),

@@ -27,7 +27,8 @@ __all__ = [
     "se_sparse_decode_workspace_size", "se_sparse_decode_plan", "se_sparse_paged_decode",
     "se_sparse_paged_decode_noalloc", "se_snapkv_workspace_size", "se_snapkv_window_scores", "se_snapkv_select",
     "se_snapkv_compact", "se_snapkv_score_and_compact", "se_snapkv_select_windowed",
-    "se_snapkv_score_and_compact_windowed", "se_debug_snapkv_wait_probe", "exported_symbols",
+    "se_snapkv_score_and_compact_windowed", "se_debug_snapkv_wait_probe", "SEGraph", "se_capture_begin",
+    "se_capture_end", "exported_symbols",
 ]
 
 SE_OK = 0
@@ -86,6 +87,10 @@ _SIGNATURES = {
     "se_snapkv_window_scores": (ctypes.c_int, [_KV, _P, _I, _I, _P, _I, _P, _I, _I, _F, _P, _I, _P, _P, _Z, _P]),
     "se_snapkv_select": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
     "se_debug_snapkv_wait_probe": (ctypes.c_int, [ctypes.c_uint32]),
+    "se_capture_begin": (ctypes.c_int, [_P]),
+    "se_capture_end": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
+    "se_graph_launch": (ctypes.c_int, [_P, _P]),
+    "se_graph_destroy": (None, [_P]),
     "se_snapkv_select_windowed": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
     "se_snapkv_compact": (ctypes.c_int, [_KV, _P, _I, _P, _I, _KV, _P, _I, _P, _I, _P, _P]),
     "se_snapkv_score_and_compact": (ctypes.c_int, [_KV, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _F, _KV, _P, _I, _P,
@@ -162,6 +167,42 @@ def paged_kv(k_cache: torch.Tensor, v_cache: Optional[torch.Tensor], summary: Op
         _ptr(summary, torch.bfloat16, "summary")
     return SEPagedKV(k_cache.data_ptr(), v_ptr, None if summary is None else summary.data_ptr(),
                      P, H, ps, row_k, dv, row_k, row_v)
+
+
+class SEGraph:
+    """A recorded step (se_capture_begin ... se_capture_end): launch() replays it
+    with se_graph_launch; the handle is freed with se_graph_destroy."""
+
+    def __init__(self, handle: int):
+        self._h = handle
+
+    def launch(self, stream=None):
+        if not self._h:
+            raise ValueError("the recorded step has been destroyed")
+        _check(load_library().se_graph_launch(self._h, _stream(stream)))
+
+    def destroy(self):
+        if self._h:
+            load_library().se_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def se_capture_begin(stream=None):
+    """Start recording the library calls made on ``stream`` (not the legacy default stream)."""
+    _check(load_library().se_capture_begin(_stream(stream)))
+
+
+def se_capture_end(stream=None) -> SEGraph:
+    """End the recording on ``stream``; returns the recorded step."""
+    h = ctypes.c_void_p(None)
+    _check(load_library().se_capture_end(_stream(stream), ctypes.byref(h)))
+    return SEGraph(h.value)
 
 
 def se_read_device_error(clear: bool = True) -> int:

@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB_NAME = "libsparse_engine.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "quest_summary.cu", "quest_score.cu", "quest_topk.cu", "sparse_decode.cu", "mla_decode.cu", "quest_fused.cu",
-           "decode_noalloc.cu", "snapkv.cu"]
+           "decode_noalloc.cu", "snapkv.cu", "graph.cu"]
 
 
 def _nvcc():

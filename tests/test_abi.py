@@ -192,3 +192,14 @@ def test_a_c_caller_compiles_against_the_header_and_links(se_lib, tmp_path):
                     "-Wl,-rpath," + lib_dir], check=True)
     r = subprocess.run([exe], capture_output=True, text=True)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+def test_replayable_step_calls_reject_missing_handles(se_lib):
+    # host checks only: a NULL stream (the legacy default stream cannot be
+    # recorded), a NULL graph handle; destroying NULL is a no-op
+    assert se_lib.se_capture_begin(None) == INVALID
+    h = ctypes.c_void_p(None)
+    assert se_lib.se_capture_end(None, ctypes.byref(h)) == INVALID
+    assert se_lib.se_capture_end(ctypes.c_void_p(FAKE), None) == INVALID
+    assert se_lib.se_graph_launch(None, None) == INVALID
+    se_lib.se_graph_destroy(None)
