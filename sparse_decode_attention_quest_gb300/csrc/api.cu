@@ -88,6 +88,23 @@ bool encode_page_map(CUtensorMap* map, const void* base, long long rows, int wid
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view of a 128-wide bf16 cache with `rows` rows, `row_stride` elements apart:
+// (64 dims, row, 64-dim half), the halves 128 bytes apart. A box of 64 x 16 x 2
+// copies one page of one head (both halves, 4 KB) with a single request, into
+// [half][16 rows][128 bytes] with 128-byte swizzle.
+bool encode_page_halves_map(CUtensorMap* map, const void* base, long long rows, int row_stride) {
+  auto fn = encode_tiled();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, 2};
+  cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)se::kPageSize, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 4-D view of SnapKV window queries bf16 [batch][window][num_q_heads][128]: boxes of
 // 64 dims x `group` heads x `window` positions x 1 request (128-byte swizzle), so one
 // box holds a KV head's window rows r = w * group + g for 64 of the dims.
@@ -557,7 +574,7 @@ se_status_t se_snapkv_window_scores(const se_paged_kv_t* src, const void* q_wind
   if (e != cudaSuccess) return cuda_fail(fn, e);
   CUtensorMap kmap, qmap;
   const long long rows = (long long)src->num_pages * src->num_kv_heads * se::kPageSize;
-  if (!encode_page_map(&kmap, src->k, rows > 0 ? rows : 1, src->head_dim, src->row_stride_k) ||
+  if (!encode_page_halves_map(&kmap, src->k, rows > 0 ? rows : 1, src->row_stride_k) ||
       !encode_window_map(&qmap, q_window, batch, window, num_q_heads, num_q_heads / src->num_kv_heads))
     return fail(SE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
   e = se::launch_snapkv_scores(kmap, qmap, view_of(src), static_cast<const uint16_t*>(q_window), num_q_heads, window,

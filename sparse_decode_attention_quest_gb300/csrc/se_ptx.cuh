@@ -115,6 +115,16 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Tiled 3-D tensor copy of the box at (x, y, z) described by `map`.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // Tiled 4-D tensor copy of the box at (x, y, z, w) described by `map`.
 __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
                                             int32_t w, uint64_t* bar, uint64_t policy) {
@@ -328,6 +338,15 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_byte_addr) {
   d |= (uint64_t)(1024 >> 4) << 32;                            // stride offset: next 8-row group
   d |= (uint64_t)1 << 46;                                      // descriptor version
   d |= (uint64_t)2 << 61;                                      // 128-byte swizzle
+  return d;
+}
+// The same with the 8-row groups `group_stride` bytes apart (a multiple of 1024).
+__device__ __forceinline__ uint64_t umma_desc_sw128_groups(uint32_t smem_byte_addr, uint32_t group_stride) {
+  uint64_t d = (uint64_t)((smem_byte_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)((group_stride >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
   return d;
 }
 

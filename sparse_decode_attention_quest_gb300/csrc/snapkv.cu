@@ -12,15 +12,20 @@
 //            keep the top k of s' (ties: lower j) ascending, then n - W .. n - 1
 //   compact  kept token t -> page t / 16, slot t % 16 of the destination table
 //
-// The logits are the one dense contraction of the path: 128 query rows x 128
+// The logits are the one dense contraction of the path: 128 query rows x 256
 // keys x 128 dims per tile, on the 5th-generation tensor cores. Warp roles:
 //   warp 0      TMA producer: per segment the pair's window queries (two 4-D
-//               boxes), then the 8 pages of each 128-key tile (two 64-column
-//               boxes each, 128-byte swizzle) into a 4-stage ring;
-//   warp 1      allocates 256 TMEM columns (two fp32 128x128 accumulators)
-//               and issues the tcgen05.mma (M 128, N 128, K 16) x 8 per tile;
+//               boxes), then the 16 pages of each 256-key tile, one 3-D box
+//               per page (both 64-dim halves, 4 KB, 128-byte swizzle) into a
+//               2-stage ring. Streaming random 4 KB pages, 4 KB boxes reach
+//               about a fifth more HBM bandwidth than two 2 KB boxes per page,
+//               hence one box per page and the page-major tile;
+//   warp 1      allocates all 512 TMEM columns (two tiles x two fp32 128x128
+//               accumulators) and issues the tcgen05.mma (M 128, N 128, K 16):
+//               rows 0-7 of the tile's 16 pages (8-row groups 4 KB apart) into
+//               accumulator 0, rows 8-15 into accumulator 1, 8 K steps each;
 //   warps 2-9   epilogue, two warps per TMEM lane quarter, each thread with 64
-//               of the tile's 128 accumulator columns.
+//               of each accumulator's 128 columns.
 // Pass 1 computes S = Q K^T: TMEM lane = query row, so a thread keeps its
 // row's running max and sum (causal mask on the last tiles only). Pass 2
 // computes S^T = K Q^T: TMEM lane = key, so a thread sums exp(z - LSE) over
@@ -56,23 +61,26 @@ namespace se {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kTileN = 128;                   // keys per tile
+constexpr int kTileN = 256;                   // keys per tile: 16 pages
 constexpr int kPagesPerTile = kTileN / kPageSize;
-constexpr int kHalfBytes = kTileN * 128;      // 128 rows x 128 bytes (64 dims)
-constexpr int kTileBytes = 2 * kHalfBytes;    // 32 KB
-constexpr int kStages = 4;
+constexpr int kPageHalfBytes = kPageSize * 128;  // 16 rows x 128 bytes (64 dims)
+constexpr int kPageBytes = 2 * kPageHalfBytes;   // one page of one head: 4 KB
+constexpr int kTileBytes = kPagesPerTile * kPageBytes;  // 64 KB
+constexpr int kQHalfBytes = 128 * 128;        // 128 query rows x 128 bytes (64 dims)
+constexpr int kQBytes = 2 * kQHalfBytes;      // 32 KB
+constexpr int kStages = 2;
 constexpr int kThreads = 320;                 // producer, MMA issuer, 8 epilogue warps
 constexpr int kEpiThreads = 256;
 constexpr int kMinTilesPerCta = 4;
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 512;                // two tiles x two 128 x 128 fp32 accumulators
 constexpr int kMaxPairsPerChunk = 2048;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Dynamic shared memory: [K ring 4 x 32 KB][Q 2 x 32 KB][column partials 2 x 2 x 128 fp32]
+// Dynamic shared memory: [K ring 2 x 64 KB][Q 2 x 32 KB][column partials 2 x 2 x 128 fp32]
 // [final -LSE 2 x 128 fp32][row stats 2 x 128 x 2 fp32][flag][prefix][barriers]
 constexpr int kRingOff = 0;
 constexpr int kQOff = kStages * kTileBytes;
-constexpr int kColOff = kQOff + 2 * kTileBytes;
+constexpr int kColOff = kQOff + 2 * kQBytes;
 constexpr int kNegLseOff = kColOff + 2 * 2 * 128 * 4;
 constexpr int kStatOff = kNegLseOff + 2 * 128 * 4;
 constexpr int kFlagOff = kStatOff + 2 * 128 * 2 * 4;
@@ -203,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
     }
     prefix[p + 1] = pair_tiles(n, a.W, PASS);
   }
-  for (int i = threadIdx.x; i < 2 * kTileBytes / 16; i += kThreads)
+  for (int i = threadIdx.x; i < 2 * kQBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(smem + kQOff)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
@@ -281,18 +289,18 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
         }
         mbar_arrive_expect_tx(&q_full[qb], dead ? 0u : (uint32_t)(2 * R * 128));
         if (!dead) {
-          uint8_t* qt = smem + kQOff + qb * kTileBytes;
+          uint8_t* qt = smem + kQOff + qb * kQBytes;
           tma_load_4d(qt, &qmap, 0, h * a.G, 0, b, &q_full[qb], q_policy);
-          tma_load_4d(qt + kHalfBytes, &qmap, 64, h * a.G, 0, b, &q_full[qb], q_policy);
+          tma_load_4d(qt + kQHalfBytes, &qmap, 64, h * a.G, 0, b, &q_full[qb], q_policy);
         }
       }
       dead = __shfl_sync(0xffffffffu, (int)dead, 0) != 0;
       ++seg;
-      // Block-table entries of 4 tiles per window (lane l: page l % 8 of tile
-      // wb + l / 8); the next window is read 4 tiles before it is needed.
+      // Block-table entries of 2 tiles per window (lane l: page l % 16 of tile
+      // wb + l / 16); the next window is read 2 tiles before it is needed.
       const int32_t* bt_row = a.bt + (size_t)b * a.bt_stride;
       auto load_window = [&](int wt) {
-        const int tt = wt + (lane >> 3), page = tt * kPagesPerTile + (lane & 7);
+        const int tt = wt + (lane >> 4), page = tt * kPagesPerTile + (lane & 15);
         int ph = -1;
         if (tt < t1 && page < npages) {
           ph = bt_row[page];
@@ -303,29 +311,27 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
         }
         return ph;
       };
-      int wb = t0, win_cur = load_window(t0), win_nxt = load_window(t0 + 4);
+      int wb = t0, win_cur = load_window(t0), win_nxt = load_window(t0 + 2);
       for (int t = t0; t < t1; ++t, ++it) {
         const int s = it % kStages;
-        if (t == wb + 4) {
-          wb += 4;
+        if (t == wb + 2) {
+          wb += 2;
           win_cur = win_nxt;
-          win_nxt = load_window(wb + 4);
+          win_nxt = load_window(wb + 2);
         }
-        int phys = __shfl_sync(0xffffffffu, win_cur, (t - wb) * kPagesPerTile + (lane & 7));
+        // Lane l < 16 copies page l of the tile: [64-dim half][16 rows][128 bytes].
+        int phys = __shfl_sync(0xffffffffu, win_cur, (t - wb) * kPagesPerTile + (lane & 15));
         if (lane >= kPagesPerTile) phys = -1;
         if (it >= kStages && !dead && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1)) {
           if (lane == 0) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
           dead = true;
         }
         const unsigned live = __ballot_sync(0xffffffffu, phys >= 0 && !dead);
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(live) * 2 * kPageSize * 128);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(live) * kPageBytes);
         __syncwarp();
-        if (phys >= 0 && !dead) {
-          uint8_t* st = smem + kRingOff + s * kTileBytes + lane * kPageSize * 128;
-          const int y = (phys * a.H + h) * kPageSize;
-          tma_load_2d(st, &kmap, 0, y, &full[s], policy);
-          tma_load_2d(st + kHalfBytes, &kmap, 64, y, &full[s], policy);
-        }
+        if (phys >= 0 && !dead)
+          tma_load_3d(smem + kRingOff + s * kTileBytes + lane * kPageBytes, &kmap, 0, (phys * a.H + h) * kPageSize, 0,
+                      &full[s], policy);
       }
     });
     // Drain: every copy this CTA issued has landed before it exits.
@@ -341,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
     // address field, no carry: every shared address is below 256 KB). Pass 1
     // multiplies Q (A, M = query rows) by K (B, N = keys); pass 2 swaps them.
     if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16(128, kTileN);
+      const uint32_t idesc = umma_idesc_bf16(128, 128);
       int it = 0, seg = 0;
       if (a.probe_limit_ns && !mbar_wait_ns(probe, 0, a.probe_limit_ns)) {
         // the probe's wait ran out, as it must: no MMA from here on
@@ -357,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
           dead = true;
         }
         tc05_fence_after();
-        const uint64_t dq = umma_desc_sw128(smem_addr(smem + kQOff + qb * kTileBytes));
+        const uint64_t dq = umma_desc_sw128(smem_addr(smem + kQOff + qb * kQBytes));
         for (int t = t0; t < t1; ++t, ++it) {
           const int s = it % kStages, ab = it & 1;
           if (!dead && (!mbar_wait(&full[s], (it / kStages) & 1) ||
@@ -367,14 +373,21 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
           }
           tc05_fence_after();
           if (!dead) {
-            const uint64_t dk = umma_desc_sw128(smem_addr(smem + kRingOff + s * kTileBytes));
-            const uint64_t da = PASS == 1 ? dq : dk, db = PASS == 1 ? dk : dq;
-            const uint32_t d = tmem + ab * kTileN;
+            const uint32_t kt = smem_addr(smem + kRingOff + s * kTileBytes);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              constexpr uint64_t kHalfDesc = kHalfBytes >> 4;
-              const uint64_t off = (uint64_t)(kk >> 2) * kHalfDesc + (uint64_t)(kk & 3) * 2;  // 32 bytes = 2
-              tc05_mma_bf16(d, da + off, db + off, idesc, kk > 0 ? 1u : 0u);
+            for (int q = 0; q < 2; ++q) {
+              const uint64_t dk = umma_desc_sw128_groups(kt + q * 1024, kPageBytes);
+              const uint32_t d = tmem + ab * 256 + q * 128;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                // K step kk: 64-dim half kk / 4, 32 bytes (2 in the address field) per step inside it.
+                const uint64_t oq = (uint64_t)(kk >> 2) * (kQHalfBytes >> 4) + (uint64_t)(kk & 3) * 2;
+                const uint64_t ok = (uint64_t)(kk >> 2) * (kPageHalfBytes >> 4) + (uint64_t)(kk & 3) * 2;
+                if (PASS == 1)
+                  tc05_mma_bf16(d, dq + oq, dk + ok, idesc, kk > 0 ? 1u : 0u);
+                else
+                  tc05_mma_bf16(d, dk + ok, dq + oq, idesc, kk > 0 ? 1u : 0u);
+              }
             }
           }
           tc05_commit(&empty[s]);
@@ -416,59 +429,66 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
             dead = true;
           }
           tc05_fence_after();
-          const int jc = t * kTileN + chalf * 64;  // first key of this thread's half
-          uint32_t raw[2][32];
-          {
-            const uint32_t addr = tmem + ((uint32_t)(wg * 32) << 16) + ab * kTileN + chalf * 64;
-            tmem_ld32(addr, raw[0]);
-            tmem_ld32(addr + 32, raw[1]);
-            tmem_ld_wait();
-          }
-          tc05_fence_before();
-          mbar_arrive(&acc_empty[ab]);  // the accumulator can take the next tile's MMA
-          if (!row_live) continue;
-          if (jc + 63 <= limit) {
-            // Every key visible: max of the raw logits (scale > 0), then the sum.
-            float m21[22];
-#pragma unroll
-            for (int i = 0; i < 21; ++i)
-              m21[i] = fmax3(__uint_as_float(raw[(3 * i) >> 5][(3 * i) & 31]),
-                             __uint_as_float(raw[(3 * i + 1) >> 5][(3 * i + 1) & 31]),
-                             __uint_as_float(raw[(3 * i + 2) >> 5][(3 * i + 2) & 31]));
-            m21[21] = __uint_as_float(raw[1][31]);
-            float m8[8];
-#pragma unroll
-            for (int i = 0; i < 7; ++i) m8[i] = fmax3(m21[3 * i], m21[3 * i + 1], m21[3 * i + 2]);
-            m8[7] = m21[21];
-            const float zmax = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-            const float mn = fmaxf(m_run, zmax * a.scale_log2);
-            uint64_t bias[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) bias[c] = f2(-mn, -mn);
-            const float sum = sum_exp2_64(raw, s2, bias);
-            l_run = l_run * fast_exp2(m_run - mn) + sum;
-            m_run = mn;
-          } else {
-            // Causal boundary: keys past `limit` (and past the prompt) are masked.
-            float x[64];
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const float z = __uint_as_float(raw[c >> 5][c & 31]) * a.scale_log2;
-              x[c] = jc + c <= limit ? z : -INFINITY;
+#pragma unroll 1
+          for (int q = 0; q < 2; ++q) {
+            uint32_t raw[2][32];
+            {
+              const uint32_t addr = tmem + ((uint32_t)(wg * 32) << 16) + ab * 256 + q * 128 + chalf * 64;
+              tmem_ld32(addr, raw[0]);
+              tmem_ld32(addr + 32, raw[1]);
+              tmem_ld_wait();
             }
-            float mx = -INFINITY;
+            if (q == 1) {
+              tc05_fence_before();
+              mbar_arrive(&acc_empty[ab]);  // both accumulators read: the slot can take the next tile
+            }
+            if (!row_live) continue;
+            // Column c of this thread's 64 holds key kb + 16 (c / 8) + c % 8 (page
+            // 8 chalf + c / 8 of the tile, row 8 q + c % 8); the last is kb + 119.
+            const int kb = t * kTileN + chalf * 128 + q * 8;
+            if (kb + 119 <= limit) {
+              // Every key visible: max of the raw logits (scale > 0), then the sum.
+              float m21[22];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
-            const float mn = fmaxf(m_run, mx);
-            if (mn != -INFINITY) {
-              float s0 = 0.f, s1 = 0.f;
+              for (int i = 0; i < 21; ++i)
+                m21[i] = fmax3(__uint_as_float(raw[(3 * i) >> 5][(3 * i) & 31]),
+                               __uint_as_float(raw[(3 * i + 1) >> 5][(3 * i + 1) & 31]),
+                               __uint_as_float(raw[(3 * i + 2) >> 5][(3 * i + 2) & 31]));
+              m21[21] = __uint_as_float(raw[1][31]);
+              float m8[8];
 #pragma unroll
-              for (int c = 0; c < 64; c += 2) {
-                s0 += fast_exp2(x[c] - mn);
-                s1 += fast_exp2(x[c + 1] - mn);
-              }
-              l_run = l_run * fast_exp2(m_run - mn) + (s0 + s1);
+              for (int i = 0; i < 7; ++i) m8[i] = fmax3(m21[3 * i], m21[3 * i + 1], m21[3 * i + 2]);
+              m8[7] = m21[21];
+              const float zmax = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+              const float mn = fmaxf(m_run, zmax * a.scale_log2);
+              uint64_t bias[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) bias[c] = f2(-mn, -mn);
+              const float sum = sum_exp2_64(raw, s2, bias);
+              l_run = l_run * fast_exp2(m_run - mn) + sum;
               m_run = mn;
+            } else {
+              // Causal boundary: keys past `limit` (and past the prompt) are masked.
+              float x[64];
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                const float z = __uint_as_float(raw[c >> 5][c & 31]) * a.scale_log2;
+                x[c] = kb + (c >> 3) * 16 + (c & 7) <= limit ? z : -INFINITY;
+              }
+              float mx = -INFINITY;
+#pragma unroll
+              for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
+              const float mn = fmaxf(m_run, mx);
+              if (mn != -INFINITY) {
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                  s0 += fast_exp2(x[c] - mn);
+                  s1 += fast_exp2(x[c + 1] - mn);
+                }
+                l_run = l_run * fast_exp2(m_run - mn) + (s0 + s1);
+                m_run = mn;
+              }
             }
           }
         }
@@ -561,22 +581,28 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
             dead = true;
           }
           tc05_fence_after();
-          uint32_t raw[2][32];
-          {
-            const uint32_t addr = tmem + ((uint32_t)(wg * 32) << 16) + ab * kTileN + chalf * 64;
-            tmem_ld32(addr, raw[0]);
-            tmem_ld32(addr + 32, raw[1]);
-            tmem_ld_wait();
-          }
-          tc05_fence_before();
-          mbar_arrive(&acc_empty[ab]);
-          const float part = (half_live && !dead) ? sum_exp2_64(raw, s2, bias) : 0.f;
-          float* cp = colpart + (it & 1) * 256;
-          cp[chalf * 128 + lq] = part;
-          named_bar_sync(2 + wg, 64);  // the other half of these 32 keys is in (warps w and w + 4)
-          if (chalf == 0) {
-            const int j = t * kTileN + lq;
-            if (j < n - a.W) a.scores[(size_t)g * a.score_stride + j] = cp[lq] + cp[128 + lq];
+#pragma unroll 1
+          for (int q = 0; q < 2; ++q) {
+            uint32_t raw[2][32];
+            {
+              const uint32_t addr = tmem + ((uint32_t)(wg * 32) << 16) + ab * 256 + q * 128 + chalf * 64;
+              tmem_ld32(addr, raw[0]);
+              tmem_ld32(addr + 32, raw[1]);
+              tmem_ld_wait();
+            }
+            if (q == 1) {
+              tc05_fence_before();
+              mbar_arrive(&acc_empty[ab]);
+            }
+            const float part = (half_live && !dead) ? sum_exp2_64(raw, s2, bias) : 0.f;
+            float* cp = colpart + q * 256;
+            cp[chalf * 128 + lq] = part;
+            named_bar_sync(2 + wg, 64);  // the other half of these 32 keys is in (warps w and w + 4)
+            if (chalf == 0) {
+              // TMEM lane m holds key 16 (m / 8) + 8 q + m % 8 of the tile.
+              const int j = t * kTileN + (lq >> 3) * 16 + q * 8 + (lq & 7);
+              if (j < n - a.W) a.scores[(size_t)g * a.score_stride + j] = cp[lq] + cp[128 + lq];
+            }
           }
         }
       }
