@@ -47,6 +47,7 @@
 // counts itself in on the pair's counter (zeroed before the first launch); the
 // share that completes the count merges them into the rows' final
 // log-sum-exps, which pass 2 reads.
+
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -628,38 +629,23 @@ constexpr int kPoolHalfMax = 8;                      // pooling windows up to 17
 constexpr int kPoolUnroll = 4;                       // chunks of 32 positions a warp loads at once
 constexpr int kSelCluster = 4;                       // CTAs per (request, KV head): the pooling is shared
 constexpr int kSelMaxCand = kSelThreads * kSelPer;   // 45056
+constexpr int kSelWords = kSelMaxCand / 32;          // one bit per candidate
 
+// Monotone map of a float to an unsigned key (a < b <=> key(a) < key(b)).
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix, in index order, of flagged candidates. Thread t owns
-// candidates t + 1024 e, so index order is (e, warp, lane): per (e, warp)
-// counts from ballots, one prefix over them (warp 0). Afterwards the rank of
-// owned candidate e is cnt[e * 32 + warp] + popc(ballot(flag) & lanes below).
 __device__ __forceinline__ int sel_warp_sum(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-// Per-candidate flags (bit e of thread t: candidate t + 1024 e) to the exclusive
-// count, in candidate order, of the flagged candidates before each warp's group
-// of 32: cnt[e * 32 + warp]. Every thread scans up to two of the E x 32 group
-// counts, then the block adds the threads' sums with two warp-level scans.
-__device__ __forceinline__ void index_order_prefix(uint64_t flags, int E, int* cnt, int* wtot, int warp,
-                                                   int lane) {
-  for (int e = 0; e < E; ++e) {
-    const unsigned ball = __ballot_sync(0xffffffffu, (flags >> e) & 1ull);
-    if (lane == 0) cnt[e * 32 + warp] = __popc(ball);
-  }
-  __syncthreads();
-  const int N = E * 32;               // <= 2 * kSelThreads
-  const int tid = warp * 32 + lane;
-  const int i0 = 2 * tid;
-  const int c0 = i0 < N ? cnt[i0] : 0, c1 = i0 + 1 < N ? cnt[i0 + 1] : 0;
-  const int v = c0 + c1;
+// Exclusive prefix over the block's threads (in thread order) of v; `wtot`
+// holds kSelWarps ints. Every thread of the block calls it.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* wtot, int warp, int lane) {
   int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -668,19 +654,37 @@ __device__ __forceinline__ void index_order_prefix(uint64_t flags, int E, int* c
   }
   if (lane == 31) wtot[warp] = incl;
   __syncthreads();
-  const int x = wtot[lane];
-  const int before = incl - v + sel_warp_sum(lane < warp ? x : 0);
-  if (i0 < N) cnt[i0] = before;
-  if (i0 + 1 < N) cnt[i0 + 1] = before + c0;
-  __syncthreads();
+  int x = wtot[lane], xs = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, xs, o);
+    if (lane >= o) xs += t;
+  }
+  const int base = __shfl_sync(0xffffffffu, xs - x, warp);  // totals of the warps before this one
+  __syncthreads();                                          // wtot is free again
+  return base + incl - v;
 }
 
 // Max-pool of the scores, then the top `keep` candidates by pooled score (ties:
 // lower position) in ascending order, then the window positions. A cluster of
 // kSelCluster CTAs per (request, KV head) pools the positions into rank 0's
-// shared memory, and rank 0 selects: its thread t owns candidates t + 1024 e
-// (conflict-free shared-memory accesses); per-candidate flags sit in a 64-bit
-// mask.
+// shared memory, and rank 0 alone selects. Its thread t owns candidates
+// t + 1024 e, so that a warp's ballot over its e-th candidates is bit word
+// e * 32 + warp of the candidate bitmap, which covers candidates 32 w .. 32 w + 31
+// (index order = word order).
+//   1. pool into rank 0's shared memory, with the range [kmin, kmax] of the
+//      candidates' order keys;
+//   2. histogram of the keys in 1,024 log-linear buckets (key - kmin) >> shift,
+//      shift the smallest that fits the range: a bucket spans a fixed fraction
+//      of an octave, so heavy-tailed scores spread over many buckets;
+//   3. the bucket B that holds the keep-th largest; one pass sets the bitmap
+//      bits of every candidate above B and lists B's members;
+//   4. each member's rank (key descending, position ascending) among them
+//      decides it: the first keep - (candidates above B) are kept. A bucket with
+//      more than kMaxMembers members is settled by an 8-bit radix select of
+//      its keys instead (threshold key T, then the first equal keys by
+//      position);
+//   5. the kept positions leave in index order from a prefix over the bitmap.
 __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ lens, int32_t H, int32_t W,
     int32_t max_len, int32_t pool, int32_t keep, int32_t sink, int32_t recent, int32_t* __restrict__ kept,
@@ -688,20 +692,20 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   pdl_enter();
   extern __shared__ float pooled[];  // [n - W]
   __shared__ int hist[kBuckets];
-  __shared__ float s_min[kSelWarps], s_max[kSelWarps];
+  __shared__ uint32_t s_kmin[kSelWarps], s_kmax[kSelWarps];
   __shared__ int wtot[kSelWarps];
-  __shared__ float mem_val[kMaxMembers];
+  __shared__ uint32_t mem_key[kMaxMembers];
   __shared__ int mem_idx[kMaxMembers];
-  __shared__ int cnt[kSelPer * 32];
-  __shared__ int s_info[4];  // bucket B, keys above B, members collected, keys equal to the threshold
+  __shared__ uint32_t selw[kSelWords];  // bit j % 32 of word j / 32: candidate j is kept
+  __shared__ uint32_t eqw[kSelWords];   // radix path: candidate j has the threshold key
+  __shared__ int s_info[4];             // bucket B, candidates above B, members listed, -
   __shared__ int rhist[3][257];
-  __shared__ float cl_mm[2 * kSelCluster];  // rank 0: every rank's min and max of its pooled candidates
+  __shared__ uint32_t cl_range[2 * kSelCluster];  // rank 0: every rank's key range
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int pair = blockIdx.x / kSelCluster, b = pair / H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const unsigned lt = (1u << lane) - 1u;
   const int n = lens[b];
   if (n < W || n > max_len) {  // the same decision in every rank of the cluster
     if (tid == 0 && rank == 0) {
@@ -723,16 +727,13 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     }
     return;
   }
-  // The ranks of the cluster pool the positions together, into rank 0's shared
-  // memory; rank 0 alone then selects. Every rank has started before any writes
-  // into rank 0's shared memory.
+  // Every rank has started before any writes into rank 0's shared memory.
   cluster.sync();
   float* pooled0 = cluster.map_shared_rank(pooled, 0);
   const float* sc = scores + (size_t)pair * score_stride;
   const int half = pool / 2;
-  float lmin = INFINITY, lmax = -INFINITY;  // over the finite pooled scores of the candidates
-  // Max-pool over the scored positions (window clipped to them), and the min and
-  // max of the candidates' pooled scores on the way. A warp takes 32
+  uint32_t kmin = 0xffffffffu, kmax = 0u;  // over the candidates' pooled order keys
+  // Max-pool over the scored positions (window clipped to them). A warp takes 32
   // consecutive positions; a lane reads its own score, the `half` lanes at each
   // end also the score `half` places beyond the warp's range, and the window
   // comes from the neighbouring lanes by shuffles.
@@ -768,9 +769,10 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
             }
           }
           if (p < CS) pooled0[p] = m;
-          if (p >= c0 && p < c1 && isfinite(m)) {
-            lmin = fminf(lmin, m);
-            lmax = fmaxf(lmax, m);
+          if (p >= c0 && p < c1) {
+            const uint32_t k = order_key(m);
+            kmin = min(kmin, k);
+            kmax = max(kmax, k);
           }
         }
       }
@@ -780,123 +782,121 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
       float m = -INFINITY;
       for (int t = max(0, i - half); t <= min(CS - 1, i + half); ++t) m = fmaxf(m, sc[t]);
       pooled0[i] = m;
-      if (i >= c0 && i < c1 && isfinite(m)) {
-        lmin = fminf(lmin, m);
-        lmax = fmaxf(lmax, m);
+      if (i >= c0 && i < c1) {
+        const uint32_t k = order_key(m);
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
       }
     }
   }
-  __syncthreads();
-  const float* pc = pooled + c0;  // pooled score of candidate j
-  const int E = (C + kSelThreads - 1) / kSelThreads;
-  hist[tid] = 0;
-  if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
-  if (tid == 0) s_info[2] = s_info[3] = 0;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    lmin = fminf(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
-    lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
   if (lane == 0) {
-    s_min[warp] = lmin;
-    s_max[warp] = lmax;
+    s_kmin[warp] = kmin;
+    s_kmax[warp] = kmax;
   }
   __syncthreads();
-  float mn = s_min[lane], mx = s_max[lane];  // min and max over the warps, by shuffles
+  kmin = s_kmin[lane];
+  kmax = s_kmax[lane];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
   if (tid == 0) {
-    float* mm0 = cluster.map_shared_rank(cl_mm, 0);
-    mm0[2 * rank] = mn;
-    mm0[2 * rank + 1] = mx;
+    uint32_t* r0 = cluster.map_shared_rank(cl_range, 0);
+    r0[2 * rank] = kmin;
+    r0[2 * rank + 1] = kmax;
   }
-  cluster.sync();  // rank 0 holds every pooled score and every rank's min and max
+  cluster.sync();  // rank 0 holds every pooled score and every rank's key range
   if (rank != 0) return;
+  hist[tid] = 0;
+  for (int i = tid; i < kSelWords; i += kSelThreads) selw[i] = 0u;
+  if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
+  if (tid == 0) s_info[2] = 0;
 #pragma unroll
   for (int r = 0; r < kSelCluster; ++r) {
-    mn = fminf(mn, cl_mm[2 * r]);
-    mx = fmaxf(mx, cl_mm[2 * r + 1]);
+    kmin = min(kmin, cl_range[2 * r]);
+    kmax = max(kmax, cl_range[2 * r + 1]);
   }
-  const float scale = (mx > mn) ? (float)kBuckets / (mx - mn) : 0.f;
-  auto bucket = [&](float v) {
-    if (isfinite(v)) return min(kBuckets - 1, max(0, (int)((v - mn) * scale)));
-    return v > 0.f ? kBuckets - 1 : 0;
-  };
+  __syncthreads();
+  int shift = 0;  // block-uniform
+  while (((kmax - kmin) >> shift) >= (uint32_t)kBuckets) ++shift;
+  const float* pc = pooled + c0;  // pooled score of candidate j
+  const int E = (C + kSelThreads - 1) / kSelThreads;
   for (int e = 0; e < E; ++e) {
     const int i = tid + e * kSelThreads;
-    if (i < C) atomicAdd(&hist[bucket(pc[i])], 1);
+    if (i < C) atomicAdd(&hist[(order_key(pc[i]) - kmin) >> shift], 1);
   }
   __syncthreads();
-  const int hc = hist[tid];
-  int incl = hc;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_down_sync(0xffffffffu, incl, o);
-    if (lane + o < 32) incl += t;
-  }
-  if (lane == 0) wtot[warp] = incl;
-  __syncthreads();
+  // The bucket B holding the keep-th largest: thread t sums the buckets >= t.
   {
+    const int hc = hist[tid];
+    int incl = hc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += t;
+    }
+    if (lane == 0) wtot[warp] = incl;
+    __syncthreads();
     const int x = wtot[lane];
     incl += sel_warp_sum(lane > warp ? x : 0);  // candidates in the buckets of the warps above
+    if (incl - hc < keep && keep <= incl) {
+      s_info[0] = tid;
+      s_info[1] = incl - hc;
+    }
+    __syncthreads();
   }
-  if (incl - hc < keep && keep <= incl) {
-    s_info[0] = tid;
-    s_info[1] = incl - hc;
+  const int B = s_info[0];
+  const int need = keep - s_info[1];  // members of B to keep, >= 1
+  const int m = hist[B];
+  // Candidates above B are kept; B's members are listed (when they fit).
+  for (int e = 0; e < E; ++e) {
+    const int i = tid + e * kSelThreads;
+    const bool valid = i < C;
+    const uint32_t k = valid ? order_key(pc[i]) : 0u;
+    const int bb = valid ? (int)((k - kmin) >> shift) : -1;
+    const unsigned above = __ballot_sync(0xffffffffu, bb > B);
+    if (lane == 0) selw[e * 32 + warp] = above;
+    if (bb == B && m <= kMaxMembers) {
+      const int slot = atomicAdd(&s_info[2], 1);
+      mem_key[slot] = k;
+      mem_idx[slot] = i;
+    }
   }
   __syncthreads();
-  const int B = s_info[0];
-  const int need = keep - s_info[1];
-  const int m = hist[B];
-  __syncthreads();  // s_info is rewritten below
-  uint32_t T;
-  int need_eq;
   if (m <= kMaxMembers) {
-    for (int e = 0; e < E; ++e) {
-      const int i = tid + e * kSelThreads;
-      if (i < C && bucket(pc[i]) == B) {
-        const int slot = atomicAdd(&s_info[2], 1);
-        mem_val[slot] = pc[i];
-        mem_idx[slot] = i;
-      }
-    }
-    __syncthreads();
-    // The member of rank need - 1 (score desc, position asc) fixes the threshold.
-    if (tid < m) {
-      const uint32_t kv = order_key(mem_val[tid]);
-      const int id = mem_idx[tid];
-      int rank = 0, above = 0;
+    // A member is kept when fewer than `need` members rank before it.
+    for (int s = tid; s < m; s += kSelThreads) {
+      const uint32_t k = mem_key[s];
+      const int id = mem_idx[s];
+      int r = 0;
       for (int j = 0; j < m; ++j) {
-        const uint32_t kj = order_key(mem_val[j]);
-        rank += (kj > kv || (kj == kv && mem_idx[j] < id)) ? 1 : 0;
-        above += kj > kv ? 1 : 0;
+        const uint32_t kj = mem_key[j];
+        r += (kj > k || (kj == k && mem_idx[j] < id)) ? 1 : 0;
       }
-      if (rank == need - 1) {
-        s_info[0] = (int)kv;
-        s_info[1] = need - above;
-      }
+      if (r < need) atomicOr(&selw[id >> 5], 1u << (id & 31));
     }
-    __syncthreads();
-    T = (uint32_t)s_info[0];
-    need_eq = s_info[1];
   } else {
+    // Radix select of the need-th largest key in B, 8 bits at a time: the
+    // threshold key T and how many of the keys equal to T are kept.
     uint32_t prefix = 0, mask = 0;
     int remaining = need;
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
+      const int shift8 = 24 - 8 * pass;
       int* hh = rhist[pass % 3];
       if (pass >= 1)
         for (int i = tid; i < 257; i += kSelThreads) rhist[(pass + 1) % 3][i] = 0;
       for (int e = 0; e < E; ++e) {
         const int i = tid + e * kSelThreads;
         if (i < C) {
-          const float v = pc[i];
-          const uint32_t key = order_key(v);
-          if (bucket(v) == B && (key & mask) == prefix) atomicAdd(&hh[(key >> shift) & 255u], 1);
+          const uint32_t key = order_key(pc[i]);
+          if ((int)((key - kmin) >> shift) == B && (key & mask) == prefix) atomicAdd(&hh[(key >> shift8) & 255u], 1);
         }
       }
       __syncthreads();
@@ -931,47 +931,42 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
       d = __shfl_sync(0xffffffffu, d, src);
       ab = __shfl_sync(0xffffffffu, ab, src);
       remaining -= ab;
-      prefix |= (uint32_t)d << shift;
-      mask |= 255u << shift;
+      prefix |= (uint32_t)d << shift8;
+      mask |= 255u << shift8;
     }
-    T = prefix;
-    need_eq = remaining;
-  }
-  // Selected: pooled key above T, or equal to T among the first need_eq by position.
-  uint64_t self = 0, eqf = 0;
-  int n_eq = 0;
-  for (int e = 0; e < E; ++e) {
-    const int i = tid + e * kSelThreads;
-    if (i < C) {
-      const uint32_t key = order_key(pc[i]);
-      if (key > T) {
-        self |= 1ull << e;
-      } else if (key == T) {
-        eqf |= 1ull << e;
-        ++n_eq;
+    const uint32_t T = prefix;
+    const int need_eq = remaining;  // keys equal to T to keep, the first by position
+    for (int e = 0; e < E; ++e) {
+      const int i = tid + e * kSelThreads;
+      const bool valid = i < C;
+      const uint32_t k = valid ? order_key(pc[i]) : 0u;
+      const bool inb = valid && (int)((k - kmin) >> shift) == B;
+      const unsigned gt = __ballot_sync(0xffffffffu, inb && k > T);
+      const unsigned eq = __ballot_sync(0xffffffffu, inb && k == T);
+      if (lane == 0) {
+        selw[e * 32 + warp] |= gt;
+        eqw[e * 32 + warp] = eq;
       }
     }
+    __syncthreads();
+    // Thread t: equal-key words 2t, 2t + 1 (index order).
+    const int nw = E * 32;
+    const uint32_t e0 = 2 * tid < nw ? eqw[2 * tid] : 0u, e1 = 2 * tid + 1 < nw ? eqw[2 * tid + 1] : 0u;
+    int before = block_exclusive_scan(__popc(e0) + __popc(e1), wtot, warp, lane);
+    uint32_t take0 = 0, take1 = 0;
+    for (uint32_t v = e0; v && before < need_eq; v &= v - 1, ++before) take0 |= v & (~v + 1u);
+    for (uint32_t v = e1; v && before < need_eq; v &= v - 1, ++before) take1 |= v & (~v + 1u);
+    if (take0) selw[2 * tid] |= take0;
+    if (take1) selw[2 * tid + 1] |= take1;
   }
-  if (n_eq) atomicAdd(&s_info[3], n_eq);
   __syncthreads();
-  if (s_info[3] <= need_eq) {  // block-uniform: every key equal to T is taken (the usual case)
-    self |= eqf;
-  } else {                     // more ties than places: the first need_eq by position
-    index_order_prefix(eqf, E, cnt, wtot, warp, lane);
-    for (int e = 0; e < E; ++e) {
-      const unsigned ball = __ballot_sync(0xffffffffu, (eqf >> e) & 1ull);
-      const int eq_rank = cnt[e * 32 + warp] + __popc(ball & lt);
-      if (((eqf >> e) & 1ull) && eq_rank < need_eq) self |= 1ull << e;
-    }
-    __syncthreads();  // cnt is reused
-  }
-  index_order_prefix(self, E, cnt, wtot, warp, lane);
-  for (int e = 0; e < E; ++e) {
-    const unsigned ball = __ballot_sync(0xffffffffu, (self >> e) & 1ull);
-    if ((self >> e) & 1ull) {
-      const int pos = cnt[e * 32 + warp] + __popc(ball & lt);
-      if (pos < keep) out[c0 + pos] = c0 + tid + e * kSelThreads;
-    }
+  // Kept candidates in index order: thread t holds bitmap words 2t, 2t + 1.
+  {
+    const int nw = E * 32;
+    const uint32_t w0 = 2 * tid < nw ? selw[2 * tid] : 0u, w1 = 2 * tid + 1 < nw ? selw[2 * tid + 1] : 0u;
+    int pos = block_exclusive_scan(__popc(w0) + __popc(w1), wtot, warp, lane);
+    for (uint32_t v = w0; v; v &= v - 1) out[c0 + pos++] = c0 + 64 * tid + __ffs(v) - 1;
+    for (uint32_t v = w1; v; v &= v - 1) out[c0 + pos++] = c0 + 64 * tid + 32 + __ffs(v) - 1;
   }
   for (int i = tid; i < c0; i += kSelThreads) out[i] = i;
   for (int w = tid; w < n - c1; w += kSelThreads) out[c0 + keep + w] = c1 + w;
