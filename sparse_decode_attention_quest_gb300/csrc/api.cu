@@ -88,16 +88,19 @@ bool encode_page_map(CUtensorMap* map, const void* base, long long rows, int wid
   return r == CUDA_SUCCESS;
 }
 
-// 3-D view of a 128-wide bf16 cache with `rows` rows, `row_stride` elements apart:
-// (64 dims, row, 64-dim half), the halves 128 bytes apart. A box of 64 x 16 x 2
-// copies one page of one head (both halves, 4 KB) with a single request, into
-// [half][16 rows][128 bytes] with 128-byte swizzle.
-bool encode_page_halves_map(CUtensorMap* map, const void* base, long long rows, int row_stride) {
+// 3-D view of a bf16 cache of `rows` rows, `row_stride` elements apart, as
+// (64 dims, row, 64-dim chunk) with the chunks 128 bytes apart. A box of
+// 64 x box_rows x chunks copies box_rows rows, every chunk, with a single
+// request, into [chunk][row][128 bytes] with 128-byte swizzle: a SnapKV page
+// of one head (16 rows x 2 chunks, 4 KB), or half a latent page (8 rows x 9
+// chunks, 9 KB).
+bool encode_row_chunks_map(CUtensorMap* map, const void* base, long long rows, int row_stride, int chunks,
+                           int box_rows) {
   auto fn = encode_tiled();
   if (!fn) return false;
-  cuuint64_t dims[3] = {64, (cuuint64_t)rows, 2};
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)chunks};
   cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, 128};
-  cuuint32_t box[3] = {64, (cuuint32_t)se::kPageSize, 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)chunks};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -488,9 +491,11 @@ se_status_t se_sparse_paged_decode(const se_paged_kv_t* kv, const void* q, int32
     if ((size_t)batch > se::mla_decode_max_items())
       return fail(SE_ERR_UNSUPPORTED, fn, "too many requests for one launch");
     if (batch == 0) return SE_OK;
-    // Tile copies: 64 dims x 16 rows (one page) of the cache, 64 dims x all heads of the queries.
+    // Tile copies: 8 rows x all 9 chunks of 64 dims (half a page) of the cache,
+    // 64 dims x all heads of the queries.
     CUtensorMap kvmap, qmap;
-    if (!encode_page_map(&kvmap, kv->k, (long long)kv->num_pages * se::kPageSize, kv->head_dim, kv->row_stride_k) ||
+    if (!encode_row_chunks_map(&kvmap, kv->k, (long long)kv->num_pages * se::kPageSize, kv->row_stride_k,
+                               kv->head_dim / 64, se::kPageSize / 2) ||
         !encode_page_map(&qmap, q, (long long)batch * num_q_heads, kv->head_dim, kv->head_dim, num_q_heads))
       return fail(SE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
     e = se::launch_mla_decode(kvmap, qmap, view_of(kv), static_cast<const uint16_t*>(q), num_q_heads, block_table,
@@ -574,7 +579,7 @@ se_status_t se_snapkv_window_scores(const se_paged_kv_t* src, const void* q_wind
   if (e != cudaSuccess) return cuda_fail(fn, e);
   CUtensorMap kmap, qmap;
   const long long rows = (long long)src->num_pages * src->num_kv_heads * se::kPageSize;
-  if (!encode_page_halves_map(&kmap, src->k, rows > 0 ? rows : 1, src->row_stride_k) ||
+  if (!encode_row_chunks_map(&kmap, src->k, rows > 0 ? rows : 1, src->row_stride_k, 2, se::kPageSize) ||
       !encode_window_map(&qmap, q_window, batch, window, num_q_heads, num_q_heads / src->num_kv_heads))
     return fail(SE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
   e = se::launch_snapkv_scores(kmap, qmap, view_of(src), static_cast<const uint16_t*>(q_window), num_q_heads, window,

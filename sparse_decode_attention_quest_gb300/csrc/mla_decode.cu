@@ -11,11 +11,15 @@
 //
 //  * Work split as in the GQA decode: the selected pages of all requests form
 //    one flattened range and every CTA takes an equal slice (>= 16 pages).
-//  * A tile is 64 tokens (4 pages) in nine 64-dim chunks of 64 rows x 128 bytes,
-//    128-byte swizzled; two tiles are in flight. One thread copies each page of
-//    a tile with nine TMA boxes (64 dims x 16 rows); pages not selected are not
-//    copied, and the value dims of rows at or past the request's length are
-//    zeroed in shared memory by the softmax warps before the PV MMAs read them.
+//  * A tile is 64 tokens (4 pages) in eight groups of 8 rows (group g: rows
+//    8 g .. 8 g + 7, i.e. rows 0-7 or 8-15 of page g / 2), each group nine 64-dim
+//    chunks of 8 rows x 128 bytes, 128-byte swizzled; two tiles are in flight.
+//    One thread copies a group with one 3-D TMA box (64 dims x 8 rows x 9
+//    chunks, 9 KiB): 8 boxes per tile instead of 36 of 2 KiB, since the TMA rate
+//    goes with the number of boxes. A product's 8-row groups are then 9 KiB
+//    apart, in token order. Pages not selected are not copied, and the value
+//    dims of rows at or past the request's length are zeroed in shared memory
+//    by the softmax warps before the PV MMAs read them.
 //  * Two threads issue the MMAs: one the S^T MMAs of each tile chunk by chunk as
 //    the chunks land, the other the PV MMAs of each tile once its P is written.
 //  * S^T = K Q^T: one M = 64 tcgen05.mma per 16 dims (36 per tile) with the tile
@@ -25,7 +29,8 @@
 //    token x 16 heads), take per-head tile maxima, keep a running maximum per
 //    head that moves only when a tile exceeds it by 2^8 (then the output
 //    accumulator columns of the heads that moved are rescaled in TMEM), and
-//    write P as bf16 over the tile's RoPE chunk, which S^T no longer needs.
+//    write P as bf16 over the tile's RoPE chunks (one per group), which S^T no
+//    longer needs.
 //  * O^T += V^T P^T: four M = 128 MMAs per 16 tokens (dims 128 mt ..), A = the
 //    tile's first 512 dims read MN-major, B = P read MN-major; O^T of all 64
 //    heads is 4 x 64 TMEM columns. The epilogue divides by the softmax sums
@@ -43,12 +48,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 constexpr int kTileTok = 64;                            // 4 pages per tile
 constexpr int kTilePages = kTileTok / kPageSize;
-constexpr int kChunkBytes = kTileTok * 128;             // 64 rows x 64 dims
-constexpr int kStageBytes = kChunks * kChunkBytes;      // 72 KB
+constexpr int kGroupRows = 8;                           // rows of a copy group (half a page)
+constexpr int kChunkBytes = kGroupRows * 128;           // 8 rows x 64 dims
+constexpr int kGroupBytes = kChunks * kChunkBytes;      // 9 KB: one TMA box
+constexpr int kStageBytes = (kTileTok / kGroupRows) * kGroupBytes;  // 72 KB
 constexpr int kStages = 2;
 constexpr int kQRows = 64;
 constexpr int kQBytes = kChunks * kQRows * 128;         // 64 heads x 576 dims
-constexpr int kPOff = 8 * kChunkBytes;                  // P of a tile: over its RoPE chunk
+constexpr int kPOff = 8 * kChunkBytes;                  // P of a group: over its RoPE chunk
 constexpr int kQOff = kStages * kStageBytes;
 constexpr int kMiscOff = kQOff + kQBytes;
 constexpr int kThreads = 352;
@@ -179,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* misc = smem + kMiscOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc + kBarOff);
-  uint64_t* full = bars;          // [2 stages][9 chunks] a chunk of a tile landed (TMA transaction count)
+  uint64_t* full = bars;          // [2 stages] a tile landed (TMA transaction count)
   uint64_t* empty = bars + 18;    // [2] the PV MMAs of the stage's tile are done
   uint64_t* s_full = bars + 20;   // [2] S^T of a tile is in TMEM
   uint64_t* s_free = bars + 22;   // [2] S^T read by the softmax threads
@@ -247,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
   if (start >= end) return;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages * kChunks; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&empty[s], 1);
       mbar_init(&s_full[s], 1);
@@ -275,9 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
-    // Lane 0 issues the copies, chunk by chunk (each chunk signals its own
-    // barrier, so that the S^T MMAs of a chunk start as soon as it is in); the
-    // lanes hold the page metadata.
+    // Lane 0 issues the copies, two groups (one box each) per selected page, all
+    // signalling the stage's barrier; the lanes hold the page metadata.
     const uint64_t policy = l2_evict_first_policy();
     TileCursor c;
     c.init(prefix, start, end, i_first, i_last);
@@ -347,15 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
 #pragma unroll
           for (int pg = 0; pg < kTilePages; ++pg) tile_valid[s * kTilePages + pg] = valid[pg];
           uint8_t* st = smem + s * kStageBytes;
-#pragma unroll 1
-          for (int ch = 0; ch < kChunks; ++ch) {
-            mbar_arrive_expect_tx(&full[s * kChunks + ch], (uint32_t)live * kPageSize * 128);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)live * 2 * kGroupBytes);
 #pragma unroll
-            for (int pg = 0; pg < kTilePages; ++pg)
-              if (valid[pg] > 0)
-                tma_load_2d(st + ch * kChunkBytes + pg * kPageSize * 128, &kvmap, ch * 64, phys[pg] * kPageSize,
-                            &full[s * kChunks + ch], policy);
-          }
+          for (int pg = 0; pg < kTilePages; ++pg)
+            if (valid[pg] > 0)
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf)
+                tma_load_3d(st + (2 * pg + hf) * kGroupBytes, &kvmap, 0, phys[pg] * kPageSize + hf * kGroupRows, 0,
+                            &full[s], policy);
           if (c.t == 0) {
             // The request's queries, once the previous segment's S^T MMAs are done with the buffer.
             if (c.seg >= 1 && !mbar_wait(q_empty, (c.seg - 1) & 1)) dead = true;
@@ -376,13 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     if (dead && lane == 0) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ S^T issuer
-    // The score MMAs of each tile, chunk by chunk as the chunks land.
+    // The score MMAs of each tile once it has landed.
     if (lane == 0) {
       const uint32_t idesc_s = umma_idesc_bf16(64, Hq);
       // Operand descriptors of the bases; an MMA adds a constant offset (the
       // address field is bits 0-13 of (address >> 4), and every shared address
       // here is below 256 KB, so the additions never carry out of it).
-      const uint64_t desc_k0 = umma_desc_sw128(smem0);
+      const uint64_t desc_k0 = umma_desc_sw128_groups(smem0, kGroupBytes);
       const uint64_t desc_q = umma_desc_sw128(smem0 + kQOff);
       constexpr uint64_t kStageDesc = kStageBytes >> 4;
       TileCursor c;
@@ -396,12 +401,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
         tc05_fence_after();  // after the softmax's read of this S^T buffer
         const uint32_t d_s = tmem + kSCol + s * 64;
         const uint64_t dk = desc_k0 + (s ? kStageDesc : 0);
+        if (!mbar_wait(&full[s], (c.j >> 1) & 1)) {
+          dead = true;
+          break;
+        }
 #pragma unroll 1
         for (int ch = 0; ch < kChunks; ++ch) {
-          if (!mbar_wait(&full[s * kChunks + ch], (c.j >> 1) & 1)) {
-            dead = true;
-            break;
-          }
           // 16 dims = 32 bytes = 2 per K step; a chunk is (chunk bytes >> 4) further.
           const uint64_t da = dk + (uint64_t)(ch * (kChunkBytes >> 4));
           const uint64_t dq = desc_q + (uint64_t)(ch * ((kQRows * 128) >> 4));
@@ -423,7 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     // O^T += V^T P^T of each tile once its P is written.
     if (lane == 0) {
       const uint32_t idesc_o = umma_idesc_bf16_mn(128, 64);
-      const uint64_t desc_v0 = umma_desc_sw128_mn(smem0, kChunkBytes);
+      // V^T and P^T read MN-major: 64 elements of M (dims, or heads) per 128-byte
+      // row, the next 64 dims one chunk further, the next 8 tokens one group further.
+      const uint64_t desc_v0 = umma_desc_sw128_mn_groups(smem0, kChunkBytes, kGroupBytes);
       constexpr uint64_t kStageDesc = kStageBytes >> 4, kPDesc = kPOff >> 4;
       TileCursor c;
       c.init(prefix, start, end, i_first, i_last);
@@ -435,16 +442,18 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
           break;
         }
         tc05_fence_after();
-        // 16 tokens = 2048 bytes = 128 per K step; 128 dims = 2 chunks = 1024 per M-tile.
+        // 16 tokens = 2 groups = (2 group bytes >> 4) per K step; 128 dims = 2
+        // chunks = (2 chunk bytes >> 4) per M-tile.
+        constexpr uint64_t kStep = (2 * kGroupBytes) >> 4, kMt = (2 * kChunkBytes) >> 4;
         const uint64_t dv = desc_v0 + (s ? kStageDesc : 0), dp = dv + kPDesc;
         const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           const uint32_t d_o = tmem + kOCol + mt * 64;
-          tc05_mma_bf16(d_o, dv + mt * 1024, dp, idesc_o, acc0);
-          tc05_mma_bf16(d_o, dv + mt * 1024 + 128, dp + 128, idesc_o, 1u);
-          tc05_mma_bf16(d_o, dv + mt * 1024 + 256, dp + 256, idesc_o, 1u);
-          tc05_mma_bf16(d_o, dv + mt * 1024 + 384, dp + 384, idesc_o, 1u);
+          tc05_mma_bf16(d_o, dv + mt * kMt, dp, idesc_o, acc0);
+          tc05_mma_bf16(d_o, dv + mt * kMt + kStep, dp + kStep, idesc_o, 1u);
+          tc05_mma_bf16(d_o, dv + mt * kMt + 2 * kStep, dp + 2 * kStep, idesc_o, 1u);
+          tc05_mma_bf16(d_o, dv + mt * kMt + 3 * kStep, dp + 3 * kStep, idesc_o, 1u);
         }
         tc05_commit(&empty[s]);
         tc05_commit(o_done);
@@ -482,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
       }
       tc05_fence_before();
       mbar_arrive(&s_free[s]);
-      const bool ok_f = mbar_wait(&full[s * kChunks], (j >> 1) & 1);  // valid rows of the tile
+      const bool ok_f = mbar_wait(&full[s], (j >> 1) & 1);  // valid rows of the tile
       dead = dead || !ok_s || !ok_f;
       const bool tok_ok = tok < tile_valid[s * kTilePages + q4];
       float x[16], v[16];
@@ -494,11 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
       if (!tok_ok && (warp >> 2) == 0) {
         // Rows past the request's length (or of pages not copied) hold stale
         // data: zero their value dims so that P = 0 times them stays 0.
-        const uint32_t st = smem0 + s * kStageBytes;
+        const uint32_t st = smem0 + s * kStageBytes + (row / kGroupRows) * kGroupBytes;
 #pragma unroll 1
         for (int ch = 4 * (lane >> 4); ch < 4 * (lane >> 4) + 4; ++ch)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) st_shared_v4(st + ch * kChunkBytes + swz128(row, k), 0u, 0u, 0u, 0u);
+          for (int k = 0; k < 8; ++k) st_shared_v4(st + ch * kChunkBytes + swz128(row % kGroupRows, k), 0u, 0u, 0u, 0u);
       }
       // Fast path: after the segment's first tile, a tile whose scores all stay
       // within 2^8 of the running maxima changes nothing but P and l. Otherwise
@@ -566,8 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
           }
         }
       }
-      // P of this token for heads hh .. hh + 15 into row `row` of the tile's
-      // RoPE chunk (64 heads per 128-byte row).
+      // P of this token for heads hh .. hh + 15 into its row of its group's RoPE
+      // chunk (64 heads per 128-byte row).
       uint32_t pk[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -578,9 +587,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
         l_h[2 * i + 1] += pb;
         pk[i] = pack_bf16x2(pa, pb);
       }
-      const uint32_t prow = smem0 + s * kStageBytes + kPOff;
-      st_shared_v4(prow + swz128(row, hh >> 3), pk[0], pk[1], pk[2], pk[3]);
-      st_shared_v4(prow + swz128(row, (hh >> 3) + 1), pk[4], pk[5], pk[6], pk[7]);
+      const uint32_t prow = smem0 + s * kStageBytes + (row / kGroupRows) * kGroupBytes + kPOff;
+      st_shared_v4(prow + swz128(row % kGroupRows, hh >> 3), pk[0], pk[1], pk[2], pk[3]);
+      st_shared_v4(prow + swz128(row % kGroupRows, (hh >> 3) + 1), pk[4], pk[5], pk[6], pk[7]);
       fence_proxy_async_smem();
       tc05_fence_before();
       mbar_arrive(&p_full[s]);

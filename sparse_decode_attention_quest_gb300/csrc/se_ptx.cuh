@@ -315,6 +315,17 @@ __device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t smem_byte_addr, 
   return d;
 }
 
+// The same with the 8-row groups of K `k_group_stride` bytes apart (a multiple of 1024).
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn_groups(uint32_t smem_byte_addr, uint32_t mn_stride,
+                                                              uint32_t k_group_stride) {
+  uint64_t d = (uint64_t)((smem_byte_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((k_group_stride >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D, shape M x N.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
   return (1u << 4)                          // D format: fp32
