@@ -24,7 +24,9 @@
 //    the chunks land, the other the PV MMAs of each tile once its P is written.
 //  * S^T = K Q^T: one M = 64 tcgen05.mma per 16 dims (36 per tile) with the tile
 //    as the K-major A operand and the request's queries (64 rows x 576 dims in
-//    shared memory) as B; S^T lands in TMEM, token r in lane 32 (r / 16) + r % 16.
+//    shared memory) as B; S^T lands in TMEM, token r in lane 32 (r / 16) + r % 16,
+//    as two accumulators (the even and the odd K steps) that the softmax adds:
+//    a chain of small MMAs into one accumulator waits on each one's result.
 //  * Eight softmax warps, two per page of the tile, read S^T (each thread one
 //    token x 16 heads), take per-head tile maxima, keep a running maximum per
 //    head that moves only when a tile exceeds it by 2^8 (then the output
@@ -64,8 +66,11 @@ constexpr int kMmaWarp = 8;                             // lane 0 issues the S^T
 constexpr int kLoadWarp = 9;                            // lane 0 issues the TMA copies
 constexpr int kPvWarp = 10;                             // lane 0 issues the PV MMAs
 constexpr int kTmemCols = 512;
-constexpr int kSCol = 0;                                // S^T buffers: columns 0, 64
-constexpr int kOCol = 128;                              // O^T M-tile mt: columns 128 + 64 mt
+// S^T of tile parity s is the sum of two accumulators (the even and the odd K
+// steps, so that consecutive MMAs do not wait on one another): columns
+// 128 s + 64 h, h = 0, 1.
+constexpr int kSCol = 0;
+constexpr int kOCol = 256;                              // O^T M-tile mt: columns 256 + 64 mt
 constexpr float kRescaleLog2 = 8.f;                     // running max moves when exceeded by 2^8
 constexpr uint32_t kSoftBar = 1;                        // named barrier of the softmax warps
 
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
           break;
         }
         tc05_fence_after();  // after the softmax's read of this S^T buffer
-        const uint32_t d_s = tmem + kSCol + s * 64;
+        const uint32_t d_s = tmem + kSCol + s * 128, d_s2 = d_s + 64;
         const uint64_t dk = desc_k0 + (s ? kStageDesc : 0);
         if (!mbar_wait(&full[s], (c.j >> 1) & 1)) {
           dead = true;
@@ -411,9 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
           const uint64_t da = dk + (uint64_t)(ch * (kChunkBytes >> 4));
           const uint64_t dq = desc_q + (uint64_t)(ch * ((kQRows * 128) >> 4));
           tc05_mma_bf16(d_s, da, dq, idesc_s, ch != 0 ? 1u : 0u);
-          tc05_mma_bf16(d_s, da + 2, dq + 2, idesc_s, 1u);
+          tc05_mma_bf16(d_s2, da + 2, dq + 2, idesc_s, ch != 0 ? 1u : 0u);
           tc05_mma_bf16(d_s, da + 4, dq + 4, idesc_s, 1u);
-          tc05_mma_bf16(d_s, da + 6, dq + 6, idesc_s, 1u);
+          tc05_mma_bf16(d_s2, da + 6, dq + 6, idesc_s, 1u);
         }
         if (dead) break;
         tc05_commit(&s_full[s]);
@@ -447,14 +452,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
         constexpr uint64_t kStep = (2 * kGroupBytes) >> 4, kMt = (2 * kChunkBytes) >> 4;
         const uint64_t dv = desc_v0 + (s ? kStageDesc : 0), dp = dv + kPDesc;
         const uint32_t acc0 = first ? 0u : 1u;
+        // K step outer, M-tile inner: consecutive MMAs go to different accumulators.
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          const uint32_t d_o = tmem + kOCol + mt * 64;
-          tc05_mma_bf16(d_o, dv + mt * kMt, dp, idesc_o, acc0);
-          tc05_mma_bf16(d_o, dv + mt * kMt + kStep, dp + kStep, idesc_o, 1u);
-          tc05_mma_bf16(d_o, dv + mt * kMt + 2 * kStep, dp + 2 * kStep, idesc_o, 1u);
-          tc05_mma_bf16(d_o, dv + mt * kMt + 3 * kStep, dp + 3 * kStep, idesc_o, 1u);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt)
+            tc05_mma_bf16(tmem + kOCol + mt * 64, dv + mt * kMt + ks * kStep, dp + ks * kStep, idesc_o,
+                          ks > 0 ? 1u : acc0);
         tc05_commit(&empty[s]);
         tc05_commit(o_done);
         if (c.last()) tc05_commit(o_last);
@@ -483,8 +487,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
       uint32_t r[16];
       if (ok_s) {
         tc05_fence_after();
-        tmem_ld16x2_16(tmem + lane_base + kSCol + s * 64 + 32 * (warp >> 2), r);
+        uint32_t r2[16];
+        tmem_ld16x2_16(tmem + lane_base + kSCol + s * 128 + 32 * (warp >> 2), r);
+        tmem_ld16x2_16(tmem + lane_base + kSCol + s * 128 + 64 + 32 * (warp >> 2), r2);
         tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) r[i] = 0u;
