@@ -324,9 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1) quest_fused_kernel(const FusedArg
       // higher bucket is selected), and an exact ranking of B's members by
       // order key, then lower index. Warp w owns the contiguous candidates
       // [32 E w, 32 E (w + 1)), its lane l the candidates 32 E w + 32 i + l
-      // (conflict-free reads), and a ballot scan per warp keeps the output
-      // ascending. A crowded B
-      // (near-identical scores) falls back to a radix select over all keys.
+      // (conflict-free reads); the kept ones are bits of a candidate bitmap set
+      // by warp ballots, whose words leave in order behind a popcount prefix. A
+      // crowded B (near-identical scores) falls back to a radix select over all
+      // keys.
       // Scratch: the score ring of region A, idle once the scores are in.
       int* bhist = reinterpret_cast<int*>(regA + kScoreRingOff);                  // [kSelBuckets]
       uint32_t* mkey = reinterpret_cast<uint32_t*>(bhist + kSelBuckets);          // [kSelMaxMembers]
@@ -402,17 +403,25 @@ __global__ void __launch_bounds__(kThreads, 1) quest_fused_kernel(const FusedArg
       const int need = a.topk - sinfo[1];  // members of bucket B to take, >= 1
       const int m = bhist[B];
       if (m <= kSelMaxMembers) {
+        // One pass: every candidate above B sets its bit of the candidate bitmap
+        // (a warp's ballot over its i-th candidates is word 32 E w / 32 + i, as the
+        // warp owns candidates [32 E w, 32 E (w + 1))), and B's members are listed.
         for (int i = 0; i < E; ++i) {
           const int j = wbase + 32 * i + lane;
-          if (j >= Cn) break;
-          const uint32_t u = keys[j];
-          if (bucket_of(key_value(u)) == B) {
+          const bool in = j < Cn;
+          const uint32_t u = in ? keys[j] : 0u;
+          const int bk = in ? bucket_of(key_value(u)) : -1;
+          const unsigned above = __ballot_sync(0xffffffffu, bk > B);
+          if (lane == 0) selbits[(wbase >> 5) + i] = above;
+          if (bk == B) {
             const int slot = atomicAdd(&sinfo[2], 1);
             mkey[slot] = u;
             midx[slot] = j;
           }
         }
         __syncthreads();
+        // A member is kept when fewer than `need` members rank before it (key
+        // descending, then lower index).
         for (int i = tid; i < m; i += kThreads) {
           const uint32_t ku = mkey[i];
           const int ji = midx[i];
@@ -424,26 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1) quest_fused_kernel(const FusedArg
           if (rank < need) atomicOr(&selbits[ji >> 5], 1u << (ji & 31));
         }
         __syncthreads();
-        auto selected = [&](int j) {
-          if (j >= Cn) return false;
-          const int bk = bucket_of(key_value(keys[j]));
-          return bk > B || (bk == B && ((selbits[j >> 5] >> (j & 31)) & 1u));
-        };
-        int n_warp = 0;  // this warp's selected candidates
-        for (int i = 0; i < E; ++i) n_warp += __popc(__ballot_sync(0xffffffffu, selected(wbase + 32 * i + lane)));
-        if (lane == 0) wtot[warp] = n_warp;
-        __syncthreads();
-        int pos = 0;
-        for (int w = 0; w < warp; ++w) pos += wtot[w];
-        const unsigned below = (1u << lane) - 1u;
-        for (int i = 0; i < E; ++i) {
-          const int j = wbase + 32 * i + lane;
-          const bool take = selected(j);
-          const unsigned bal = __ballot_sync(0xffffffffu, take);
-          const int at = pos + __popc(bal & below);
-          if (take && at < a.topk) sel_s[c0 + at] = c0 + j;
-          pos += __popc(bal);
-        }
+        // Output in candidate order: thread t holds bitmap word t.
+        static_assert(kMaxCand / 32 == kThreads, "one bitmap word per thread");
+        const uint32_t wv = tid < (Cn + 31) / 32 ? selbits[tid] : 0u;
+        int tot;
+        int pos = block_scan(__popc(wv), wtot, warp, lane, tot);
+        for (uint32_t v = wv; v; v &= v - 1, ++pos)
+          if (pos < a.topk) sel_s[c0 + pos] = c0 + 32 * tid + __ffs(v) - 1;
       } else {
         // radix select of the topk-th largest key T (4 passes of 8 bits)
         uint32_t prefix = 0, mask = 0;
