@@ -25,8 +25,8 @@
 //  * S^T = K Q^T: one M = 64 tcgen05.mma per 16 dims (36 per tile) with the tile
 //    as the K-major A operand and the request's queries (64 rows x 576 dims in
 //    shared memory) as B; S^T lands in TMEM, token r in lane 32 (r / 16) + r % 16,
-//    as two accumulators (the even and the odd K steps) that the softmax adds:
-//    a chain of small MMAs into one accumulator waits on each one's result.
+//    as two accumulators that the softmax adds (chunks 0-4 and 5-8, issued by
+//    two threads: one thread issuing all 36 small MMAs of a tile takes 1.5 us).
 //  * Eight softmax warps, two per page of the tile, read S^T (each thread one
 //    token x 16 heads), take per-head tile maxima, keep a running maximum per
 //    head that moves only when a tile exceeds it by 2^8 (then the output
@@ -60,15 +60,15 @@ constexpr int kQBytes = kChunks * kQRows * 128;         // 64 heads x 576 dims
 constexpr int kPOff = 8 * kChunkBytes;                  // P of a group: over its RoPE chunk
 constexpr int kQOff = kStages * kStageBytes;
 constexpr int kMiscOff = kQOff + kQBytes;
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kSoftThreads = 256;                       // warps 0-7: softmax + epilogue
 constexpr int kMmaWarp = 8;                             // lane 0 issues the S^T MMAs (and owns TMEM)
 constexpr int kLoadWarp = 9;                            // lane 0 issues the TMA copies
 constexpr int kPvWarp = 10;                             // lane 0 issues the PV MMAs
+constexpr int kMmaWarp2 = 11;                           // lane 0 issues the S^T MMAs of chunks 5-8
 constexpr int kTmemCols = 512;
-// S^T of tile parity s is the sum of two accumulators (the even and the odd K
-// steps, so that consecutive MMAs do not wait on one another): columns
-// 128 s + 64 h, h = 0, 1.
+// S^T of tile parity s is the sum of two accumulators (chunks 0-4 and 5-8, from
+// two issuing threads): columns 128 s + 64 h, h = 0, 1.
 constexpr int kSCol = 0;
 constexpr int kOCol = 256;                              // O^T M-tile mt: columns 256 + 64 mt
 constexpr float kRescaleLog2 = 8.f;                     // running max moves when exceeded by 2^8
@@ -262,15 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&empty[s], 1);
-      mbar_init(&s_full[s], 1);
+      mbar_init(&s_full[s], 2);  // both S^T issuers commit
       mbar_init(&s_free[s], kSoftThreads);
       mbar_init(&p_full[s], kSoftThreads);
     }
     mbar_init(o_done, 1);
     mbar_init(o_free, kSoftThreads);
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    mbar_init(fin, 2);
+    mbar_init(q_empty, 2);
+    mbar_init(fin, 3);
     mbar_init(o_last, 1);
     mbar_fence_init();
   }
@@ -384,10 +384,15 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
       }
     }
     if (dead && lane == 0) raise_error(a.err, SE_DEVERR_WAIT_TIMEOUT);
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ S^T issuer
-    // The score MMAs of each tile once it has landed.
+  } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+    // ------------------------------------------------------------ S^T issuers
+    // The score MMAs of each tile once it has landed: warp kMmaWarp the 64-dim
+    // chunks 0-4 into the first accumulator, warp kMmaWarp2 chunks 5-8 into the
+    // second (one thread issuing all 36 back to back takes 1.5 us a tile, two
+    // take 1.0; splitting the 36 K steps 18 / 18 instead was slower).
     if (lane == 0) {
+      const int hf = warp == kMmaWarp2 ? 1 : 0;
+      const int ch0 = hf ? 5 : 0, ch1 = hf ? kChunks : 5;
       const uint32_t idesc_s = umma_idesc_bf16(64, Hq);
       // Operand descriptors of the bases; an MMA adds a constant offset (the
       // address field is bits 0-13 of (address >> 4), and every shared address
@@ -404,21 +409,21 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
           break;
         }
         tc05_fence_after();  // after the softmax's read of this S^T buffer
-        const uint32_t d_s = tmem + kSCol + s * 128, d_s2 = d_s + 64;
+        const uint32_t d_s = tmem + kSCol + s * 128 + hf * 64;
         const uint64_t dk = desc_k0 + (s ? kStageDesc : 0);
         if (!mbar_wait(&full[s], (c.j >> 1) & 1)) {
           dead = true;
           break;
         }
 #pragma unroll 1
-        for (int ch = 0; ch < kChunks; ++ch) {
+        for (int ch = ch0; ch < ch1; ++ch) {
           // 16 dims = 32 bytes = 2 per K step; a chunk is (chunk bytes >> 4) further.
           const uint64_t da = dk + (uint64_t)(ch * (kChunkBytes >> 4));
           const uint64_t dq = desc_q + (uint64_t)(ch * ((kQRows * 128) >> 4));
-          tc05_mma_bf16(d_s, da, dq, idesc_s, ch != 0 ? 1u : 0u);
-          tc05_mma_bf16(d_s2, da + 2, dq + 2, idesc_s, ch != 0 ? 1u : 0u);
+          tc05_mma_bf16(d_s, da, dq, idesc_s, ch != ch0 ? 1u : 0u);
+          tc05_mma_bf16(d_s, da + 2, dq + 2, idesc_s, 1u);
           tc05_mma_bf16(d_s, da + 4, dq + 4, idesc_s, 1u);
-          tc05_mma_bf16(d_s2, da + 6, dq + 6, idesc_s, 1u);
+          tc05_mma_bf16(d_s, da + 6, dq + 6, idesc_s, 1u);
         }
         if (dead) break;
         tc05_commit(&s_full[s]);
