@@ -727,9 +727,8 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     }
     return;
   }
-  // Every rank has started before any writes into rank 0's shared memory.
+  // Every rank has started before any writes into another rank's shared memory.
   cluster.sync();
-  float* pooled0 = cluster.map_shared_rank(pooled, 0);
   const float* sc = scores + (size_t)pair * score_stride;
   const int half = pool / 2;
   uint32_t kmin = 0xffffffffu, kmax = 0u;  // over the candidates' pooled order keys
@@ -768,7 +767,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
               m = fmaxf(m, up < 32 ? bu : bh);
             }
           }
-          if (p < CS) pooled0[p] = m;
+          if (p < CS) pooled[p] = m;
           if (p >= c0 && p < c1) {
             const uint32_t k = order_key(m);
             kmin = min(kmin, k);
@@ -781,7 +780,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     for (int i = rank * kSelThreads + tid; i < CS; i += kSelCluster * kSelThreads) {
       float m = -INFINITY;
       for (int t = max(0, i - half); t <= min(CS - 1, i + half); ++t) m = fmaxf(m, sc[t]);
-      pooled0[i] = m;
+      pooled[i] = m;
       if (i >= c0 && i < c1) {
         const uint32_t k = order_key(m);
         kmin = min(kmin, k);
@@ -798,6 +797,10 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     s_kmin[warp] = kmin;
     s_kmax[warp] = kmax;
   }
+  hist[tid] = 0;  // this rank's histogram; rank 0's is the pair's
+  for (int i = tid; i < kSelWords; i += kSelThreads) selw[i] = 0u;
+  if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
+  if (tid == 0) s_info[2] = 0;
   __syncthreads();
   kmin = s_kmin[lane];
   kmax = s_kmax[lane];
@@ -806,35 +809,38 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
     kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
-  if (tid == 0) {
-    uint32_t* r0 = cluster.map_shared_rank(cl_range, 0);
-    r0[2 * rank] = kmin;
-    r0[2 * rank + 1] = kmax;
+  if (tid < kSelCluster) {  // this rank's key range to every rank
+    uint32_t* r = cluster.map_shared_rank(cl_range, tid);
+    r[2 * rank] = kmin;
+    r[2 * rank + 1] = kmax;
   }
-  cluster.sync();  // rank 0 holds every pooled score and every rank's key range
-  if (rank != 0) return;
-  hist[tid] = 0;
-  for (int i = tid; i < kSelWords; i += kSelThreads) selw[i] = 0u;
-  if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
-  if (tid == 0) s_info[2] = 0;
+  cluster.sync();  // every rank holds every rank's key range; rank 0's histogram and bitmap are zero
 #pragma unroll
   for (int r = 0; r < kSelCluster; ++r) {
     kmin = min(kmin, cl_range[2 * r]);
     kmax = max(kmax, cl_range[2 * r + 1]);
   }
-  __syncthreads();
   int shift = 0;  // block-uniform
   while (((kmax - kmin) >> shift) >= (uint32_t)kBuckets) ++shift;
-  const float* pc = pooled + c0;  // pooled score of candidate j
-  const int E = (C + kSelThreads - 1) / kSelThreads;
-  for (int e = 0; e < E; ++e) {
-    const int i = tid + e * kSelThreads;
-    if (i < C) atomicAdd(&hist[(order_key(pc[i]) - kmin) >> shift], 1);
+  // This rank's positions come in chunks of 32: chunk k (positions 32 k ..
+  // 32 k + 31) belongs to rank (k mod 128) / 32 and its warp k mod 32, in both
+  // pooling loops above.
+  constexpr int kChunkStep = kSelCluster * kSelWarps;
+  for (int k = rank * kSelWarps + warp; 32 * k < CS; k += kChunkStep) {
+    const int p = 32 * k + lane;
+    if (p >= c0 && p < c1) atomicAdd(&hist[(order_key(pooled[p]) - kmin) >> shift], 1);
   }
   __syncthreads();
-  // The bucket B holding the keep-th largest: thread t sums the buckets >= t.
+  int* hist0 = cluster.map_shared_rank(hist, 0);
+  if (rank != 0) {
+    const int h = hist[tid];
+    if (h) atomicAdd(hist0 + tid, h);
+  }
+  cluster.sync();  // rank 0's histogram is the pair's
+  // The bucket B holding the keep-th largest (every rank finds the same):
+  // thread t sums the buckets >= t.
   {
-    const int hc = hist[tid];
+    const int hc = hist0[tid];
     int incl = hc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -853,24 +859,36 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   }
   const int B = s_info[0];
   const int need = keep - s_info[1];  // members of B to keep, >= 1
-  const int m = hist[B];
-  // Candidates above B are kept; B's members are listed (when they fit).
-  for (int e = 0; e < E; ++e) {
-    const int i = tid + e * kSelThreads;
-    const bool valid = i < C;
-    const uint32_t k = valid ? order_key(pc[i]) : 0u;
-    const int bb = valid ? (int)((k - kmin) >> shift) : -1;
-    const unsigned above = __ballot_sync(0xffffffffu, bb > B);
-    if (lane == 0) selw[e * 32 + warp] = above;
-    if (bb == B && m <= kMaxMembers) {
-      const int slot = atomicAdd(&s_info[2], 1);
-      mem_key[slot] = k;
-      mem_idx[slot] = i;
+  const int m = hist0[B];
+  // Every rank: its candidates above B set their bits of rank 0's bitmap (by
+  // position: chunk k is word k, one ballot), and B's members are listed in rank 0.
+  {
+    uint32_t* selw0 = cluster.map_shared_rank(selw, 0);
+    int* info0 = cluster.map_shared_rank(s_info, 0);
+    uint32_t* key0 = cluster.map_shared_rank(mem_key, 0);
+    int* idx0 = cluster.map_shared_rank(mem_idx, 0);
+    for (int k = rank * kSelWarps + warp; 32 * k < CS; k += kChunkStep) {
+      const int p = 32 * k + lane;
+      const bool cand = p >= c0 && p < c1;
+      const uint32_t key = cand ? order_key(pooled[p]) : 0u;
+      const int bb = cand ? (int)((key - kmin) >> shift) : -1;
+      const unsigned above = __ballot_sync(0xffffffffu, bb > B);
+      if (lane == 0 && above) selw0[k] = above;
+      if (bb == B && m <= kMaxMembers) {
+        const int slot = atomicAdd(info0 + 2, 1);
+        key0[slot] = key;
+        idx0[slot] = p;
+      }
     }
   }
-  __syncthreads();
+  cluster.sync();  // rank 0 holds the bitmap of the candidates above B and B's members
+  if (rank != 0) {
+    if (m > kMaxMembers) cluster.sync();  // rank 0's radix select reads this rank's pooled scores
+    return;
+  }
   if (m <= kMaxMembers) {
-    // A member is kept when fewer than `need` members rank before it.
+    // A member is kept when fewer than `need` members rank before it (key
+    // descending, then position).
     for (int s = tid; s < m; s += kSelThreads) {
       const uint32_t k = mem_key[s];
       const int id = mem_idx[s];
@@ -882,8 +900,14 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
       if (r < need) atomicOr(&selw[id >> 5], 1u << (id & 31));
     }
   } else {
-    // Radix select of the need-th largest key in B, 8 bits at a time: the
-    // threshold key T and how many of the keys equal to T are kept.
+    // Radix select of the need-th largest key in B, 8 bits at a time, over
+    // every rank's pooled scores (read across the cluster): the threshold key
+    // T and how many of the keys equal to T are kept.
+    auto key_at = [&](int p) {
+      const int owner = ((p >> 5) & (kChunkStep - 1)) / kSelWarps;
+      const float v = owner == 0 ? pooled[p] : cluster.map_shared_rank(pooled, owner)[p];
+      return order_key(v);
+    };
     uint32_t prefix = 0, mask = 0;
     int remaining = need;
 #pragma unroll 1
@@ -892,12 +916,9 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
       int* hh = rhist[pass % 3];
       if (pass >= 1)
         for (int i = tid; i < 257; i += kSelThreads) rhist[(pass + 1) % 3][i] = 0;
-      for (int e = 0; e < E; ++e) {
-        const int i = tid + e * kSelThreads;
-        if (i < C) {
-          const uint32_t key = order_key(pc[i]);
-          if ((int)((key - kmin) >> shift) == B && (key & mask) == prefix) atomicAdd(&hh[(key >> shift8) & 255u], 1);
-        }
+      for (int p = c0 + tid; p < c1; p += kSelThreads) {
+        const uint32_t key = key_at(p);
+        if ((int)((key - kmin) >> shift) == B && (key & mask) == prefix) atomicAdd(&hh[(key >> shift8) & 255u], 1);
       }
       __syncthreads();
       int g8[8], gsum = 0;
@@ -936,21 +957,22 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     }
     const uint32_t T = prefix;
     const int need_eq = remaining;  // keys equal to T to keep, the first by position
-    for (int e = 0; e < E; ++e) {
-      const int i = tid + e * kSelThreads;
-      const bool valid = i < C;
-      const uint32_t k = valid ? order_key(pc[i]) : 0u;
-      const bool inb = valid && (int)((k - kmin) >> shift) == B;
-      const unsigned gt = __ballot_sync(0xffffffffu, inb && k > T);
-      const unsigned eq = __ballot_sync(0xffffffffu, inb && k == T);
+    for (int k = warp; 32 * k < CS; k += kSelWarps) {
+      const int p = 32 * k + lane;
+      const bool cand = p >= c0 && p < c1;
+      const uint32_t key = cand ? key_at(p) : 0u;
+      const bool inb = cand && (int)((key - kmin) >> shift) == B;
+      const unsigned gt = __ballot_sync(0xffffffffu, inb && key > T);
+      const unsigned eq = __ballot_sync(0xffffffffu, inb && key == T);
       if (lane == 0) {
-        selw[e * 32 + warp] |= gt;
-        eqw[e * 32 + warp] = eq;
+        selw[k] |= gt;
+        eqw[k] = eq;
       }
     }
     __syncthreads();
-    // Thread t: equal-key words 2t, 2t + 1 (index order).
-    const int nw = E * 32;
+    cluster.sync();  // the other ranks' pooled scores are no longer read
+    // Thread t: equal-key words 2t, 2t + 1 (position order).
+    const int nw = (CS + 31) / 32;
     const uint32_t e0 = 2 * tid < nw ? eqw[2 * tid] : 0u, e1 = 2 * tid + 1 < nw ? eqw[2 * tid + 1] : 0u;
     int before = block_exclusive_scan(__popc(e0) + __popc(e1), wtot, warp, lane);
     uint32_t take0 = 0, take1 = 0;
@@ -960,13 +982,13 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     if (take1) selw[2 * tid + 1] |= take1;
   }
   __syncthreads();
-  // Kept candidates in index order: thread t holds bitmap words 2t, 2t + 1.
+  // Kept candidates in position order: thread t holds bitmap words 2t, 2t + 1.
   {
-    const int nw = E * 32;
+    const int nw = (CS + 31) / 32;
     const uint32_t w0 = 2 * tid < nw ? selw[2 * tid] : 0u, w1 = 2 * tid + 1 < nw ? selw[2 * tid + 1] : 0u;
     int pos = block_exclusive_scan(__popc(w0) + __popc(w1), wtot, warp, lane);
-    for (uint32_t v = w0; v; v &= v - 1) out[c0 + pos++] = c0 + 64 * tid + __ffs(v) - 1;
-    for (uint32_t v = w1; v; v &= v - 1) out[c0 + pos++] = c0 + 64 * tid + 32 + __ffs(v) - 1;
+    for (uint32_t v = w0; v; v &= v - 1) out[c0 + pos++] = 64 * tid + __ffs(v) - 1;
+    for (uint32_t v = w1; v; v &= v - 1) out[c0 + pos++] = 64 * tid + 32 + __ffs(v) - 1;
   }
   for (int i = tid; i < c0; i += kSelThreads) out[i] = i;
   for (int w = tid; w < n - c1; w += kSelThreads) out[c0 + keep + w] = c1 + w;
