@@ -37,7 +37,11 @@
 // pass 1 of chunk c, pass 2 of chunk c, pass 1 of chunk c + 1, ..., one launch
 // each. A pass-1 launch after the first does not wait for the pass-2 launch
 // before it (it touches nothing that launch reads or writes), so the two
-// overlap; it waits for it before it exits. Smaller chunks would let pass 2
+// overlap; it waits for it before it exits. A pass-2 launch starts its copies
+// and products as soon as its CTAs are resident, and only its epilogue waits
+// for the pass-1 launch, before reading the rows' -LSE (each CTA of it waited
+// about 10 us for its first accumulator when the whole launch waited at its
+// start). Smaller chunks would let pass 2
 // read keys that pass 1 of the chunk has just brought into L2, but on GB300 the
 // fill and drain of the extra launches cost more than the re-read from HBM
 // (4 x 32K prompts: 0.255 ms per eviction with 32 MiB chunks, 0.195 with 64,
@@ -92,6 +96,7 @@ struct SnapArgs {
   int32_t pair0;         // first pair (b * H + h) of this launch
   int32_t pairs;         // pairs of this launch
   int32_t wait_previous; // wait for the previous launch of the stream before the first access
+  int32_t late_wait;     // pass 2: only the epilogue waits (for the -LSE), every thread before it exits
   const int32_t* bt;
   int32_t bt_stride;
   const int32_t* lens;
@@ -182,7 +187,7 @@ template <int PASS>
 __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                  const __grid_constant__ CUtensorMap qmap,
                                                                  const SnapArgs a) {
-  if (a.wait_previous) pdl_wait();
+  if (a.wait_previous && !a.late_wait) pdl_wait();
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -563,8 +568,11 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
         }
       } else {
         // ---------------------------------------------------- pass 2: column sums
-        // The rows' final -LSE of this pair (written by the pass-1 launch).
+        // The rows' final -LSE of this pair (written by the pass-1 launch: with
+        // a late wait, the copies and products of this launch have started
+        // before it completed).
         float* nl = neglse + (seg & 1) * 128;
+        if (a.late_wait) pdl_wait();
         if (et < 128) nl[et] = __ldcg(a.final_nlse + (size_t)g * 128 + et);
         named_barrier_epi();
         uint64_t bias[32];
@@ -616,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   // A launch that did not wait at its start completes only after the launch
   // before it, so that a later kernel that waits for this one sees both.
-  if (!a.wait_previous) pdl_wait();
+  if (!a.wait_previous || a.late_wait) pdl_wait();
 }
 
 // ------------------------------------------------------------------ selection
@@ -1129,10 +1137,15 @@ cudaError_t launch_snapkv_scores(const CUtensorMap& kmap, const CUtensorMap& qma
     // Pass 1 of a later chunk touches nothing the pass 2 before it reads or
     // writes: it starts at once and waits for that launch only before it exits.
     a.wait_previous = p0 == 0 ? 1 : 0;
+    a.late_wait = 0;
     a.probe_limit_ns = p0 == 0 ? probe_ns : 0;
     e = launch_pdl(snapkv_pass_kernel<1>, dim3(sm_count), dim3(kThreads), smem, stream, kmap, qmap, a);
     if (e != cudaSuccess) return e;
+    // Pass 2 reads keys and queries (the inputs, complete once pass 1 has
+    // started) and pass 1's -LSE: its copies and products start at once, its
+    // epilogue waits for pass 1 before reading the -LSE.
     a.wait_previous = 1;
+    a.late_wait = 1;
     a.probe_limit_ns = 0;
     e = launch_pdl(snapkv_pass_kernel<2>, dim3(sm_count), dim3(kThreads), smem, stream, kmap, qmap, a);
     if (e != cudaSuccess) return e;
