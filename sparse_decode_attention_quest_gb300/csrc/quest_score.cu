@@ -163,7 +163,12 @@ __host__ __device__ __forceinline__ int pn_lanes(int group) { return group >= 8 
 // reducing the group's queries itself, and no CTA barrier is needed.
 template <int D, int T, int R, bool kPre>
 __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArgs a) {
-  pdl_enter();
+  // With the multipliers from pn_kernel (kPre), the launch before this one, the
+  // lengths, block table and summaries were complete when it started: the
+  // copies start at once and a thread waits for pn_kernel only before it first
+  // reads the multipliers or takes a unit of the pool, and before it exits.
+  if (!kPre) pdl_wait();
+  pdl_launch_dependents();
   // Page i + R - 1 is looked up while page i is consumed, inside the two
   // 32-page block-table windows [base, base + 64) a warp holds.
   static_assert(R >= 2 && R <= 17, "ring depth");
@@ -250,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArg
   };
   auto precomputed = [&](int b) {
     if (b != afrag_b) {
+      if (afrag_b < 0) pdl_wait();  // pn_kernel's multipliers
       multipliers_from(a.pn_pre + (size_t)b * H * 2 * D);
       afrag_b = b;
     }
@@ -412,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArg
   // ---- the pool: units of kUnit consecutive pages, taken by whichever warp
   // is free (a unit that crosses a request boundary is two runs).
   if (pool) {
+    pdl_wait();  // pn_kernel zeroes the unit counter
     const int dyn0 = per_cta * (int)gridDim.x;
     while (true) {
       unsigned u = 0;
@@ -428,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 2) score_pages_kernel(const ScoreArg
       }
     }
   }
+  pdl_wait();  // completes after pn_kernel, like every other launch
 }
 
 constexpr int kPnThreads = 640;  // up to 640 tasks in one round (d 128 with 5 KV heads; the latent 576)
