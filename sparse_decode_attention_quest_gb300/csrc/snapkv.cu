@@ -264,10 +264,15 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
   const int lo = (int)blockIdx.x < nsh ? share_start(T, nsh, blockIdx.x) : T;
   const int hi = (int)blockIdx.x < nsh ? share_start(T, nsh, blockIdx.x + 1) : T;
   // Calls fn(p, t0, t1) for every segment (one pair's tiles [t0, t1)) of this CTA's share.
+  // Pass 2 walks its share backwards (segments and tiles): its first tiles are the
+  // ones pass 1 read last, still in L2. Loops run over t in [t0, t1) either way;
+  // iteration t of pass 2 reads tile t0 + t1 - 1 - t.
+  constexpr bool kBackwards = PASS == 2;
   auto for_each_segment = [&](auto&& fn) {
     if (lo >= hi) return;
     const int pf = find_pair(prefix, pairs, lo), pl = find_pair(prefix, pairs, hi - 1);
-    for (int p = pf; p <= pl; ++p) {
+    for (int i = 0; i <= pl - pf; ++i) {
+      const int p = kBackwards ? pl - i : pf + i;
       const int t0 = max(lo, prefix[p]) - prefix[p], t1 = min(hi, prefix[p + 1]) - prefix[p];
       if (t0 < t1) fn(p, t0, t1);
     }
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
     // Per segment: the pair's window queries (two 4-D boxes: 64 dims x G heads
     // x W positions, rows r = w G + g), then its key tiles.
     const uint64_t q_policy = l2_evict_normal_policy();
-    // pass 1: the keys are read again by pass 2 of the chunk; pass 2: last use
+    // pass 1: the keys are read again by pass 2 (its first tiles from L2); pass 2: last use
     const uint64_t policy = PASS == 1 ? l2_evict_normal_policy() : l2_evict_first_policy();
     int it = 0, seg = 0;
     for_each_segment([&](int p, int t0, int t1) {
@@ -306,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
       // wb + l / 16); the next window is read 2 tiles before it is needed.
       const int32_t* bt_row = a.bt + (size_t)b * a.bt_stride;
       auto load_window = [&](int wt) {
-        const int tt = wt + (lane >> 4), page = tt * kPagesPerTile + (lane & 15);
+        const int tt = wt + (lane >> 4);
+        const int page = (kBackwards ? t0 + t1 - 1 - tt : tt) * kPagesPerTile + (lane & 15);
         int ph = -1;
         if (tt < t1 && page < npages) {
           ph = bt_row[page];
@@ -609,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) snapkv_pass_kernel(const __grid_c
             named_bar_sync(2 + wg, 64);  // the other half of these 32 keys is in (warps w and w + 4)
             if (chalf == 0) {
               // TMEM lane m holds key 16 (m / 8) + 8 q + m % 8 of the tile.
-              const int j = t * kTileN + (lq >> 3) * 16 + q * 8 + (lq & 7);
+              const int j = (kBackwards ? t0 + t1 - 1 - t : t) * kTileN + (lq >> 3) * 16 + q * 8 + (lq & 7);
               if (j < n - a.W) a.scores[(size_t)g * a.score_stride + j] = cp[lq] + cp[128 + lq];
             }
           }
