@@ -139,6 +139,15 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Atomic add at GPU scope with acquire and release semantics: what the caller
+// wrote before (and what a CTA barrier ordered before it) is visible to a later
+// adder that acquires the counter, and the caller sees what earlier adders wrote.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // L2 policy for data read once per step: evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;

@@ -615,98 +615,109 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gqa_decode_kernel(const 
 
   // ---- Publish this CTA's partials: count the CTA in on each split item it
   // holds; the CTA that completes an item's count merges its partials
-  // (written by other CTAs: read past L1) and resets the counter.
+  // (written by other CTAs: read past L1) and resets the counter. The count is
+  // an acquire-release atomic, so the merging CTA needs no further fence, and
+  // every item it completes is merged in one pass (their loads in flight together).
+  __shared__ int s_nfl[2];  // items listed for merging, per round (two rounds alternate)
+  if (threadIdx.x == 0) {
+    s_nfl[0] = 0;
+    s_nfl[1] = 0;
+  }
   __threadfence();  // this thread's partials are visible before any counter moves
   __syncthreads();
-  for (int it0 = i_first; it0 <= i_last; it0 += kThreads) {
+  int par = 0;
+  for (int it0 = i_first; it0 <= i_last; it0 += kThreads, par ^= 1) {
     const int it = it0 + threadIdx.x;
-    int mine = -1;
     if (it <= i_last) {
       const int q0 = prefix[it], q1 = prefix[it + 1];
       if (max(start, q0) < min(end, q1)) {
         const int nsi = (q1 - 1) / per_cta - q0 / per_cta + 1;
         if (nsi > 1) {
-          const uint32_t before = atomicAdd(a.arrivals + it, 1u);
+          const uint32_t before = atomic_add_acq_rel_gpu(a.arrivals + it, 1u);
           if (before == (uint32_t)nsi - 1) {
             a.arrivals[it] = 0;  // every CTA of the item is in: zero for the next call
-            mine = it;
+            flags[atomicAdd(&s_nfl[par], 1)] = it;
           }
         }
       }
     }
-    flags[threadIdx.x] = mine;
     __syncthreads();
-    const int nflags = min(kThreads, i_last - it0 + 1);
-    for (int f = 0; f < nflags; ++f) {
-      const int it2 = flags[f];
-      if (it2 < 0) continue;
-      __threadfence();
-      const int q0 = prefix[it2];
-      const int nsi = (prefix[it2 + 1] - 1) / per_cta - q0 / per_cta + 1;
-      const size_t rbase = (size_t)(it2 / H) * Hq + (it2 % H) * G;
-      // Each thread takes two (row, 4 columns) elements and issues every load
-      // of a batch of four partials at once (one L2 round trip per batch),
-      // folding the batches in with an online rescale.
-      for (int e0 = threadIdx.x; e0 < G * (kHeadDim / 4); e0 += 2 * kThreads) {
-        float M[2] = {-INFINITY, -INFINITY}, wsum[2] = {0.f, 0.f};
-        float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-        size_t row[2];
-        int d[2];
-        bool on[2];
+    const int nfl = s_nfl[par];
+    if (threadIdx.x == 0) s_nfl[par ^ 1] = 0;  // the next round's list; untouched until the barrier below
+    // Elements (item of the list, query row, 4 columns); each thread takes up to
+    // kMergeU of them at once and issues every load of a batch of four partials
+    // of each at once (one L2 round trip per batch), folding the batches in with
+    // an online rescale.
+    constexpr int kMergeU = 4;
+    const int per_item = G * (kHeadDim / 4);
+    const int E = nfl * per_item;
+    for (int e0 = threadIdx.x; e0 < E; e0 += kMergeU * kThreads) {
+      float M[kMergeU], wsum[kMergeU];
+      float4 acc[kMergeU];
+      size_t row[kMergeU];
+      int d[kMergeU], nsu[kMergeU];
+      bool on[kMergeU];
+      int nmax = 0;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int e = e0 + u * kThreads;
-          on[u] = e < G * (kHeadDim / 4);
-          const int ee = on[u] ? e : e0;
-          row[u] = rbase + ee / (kHeadDim / 4);
-          d[u] = (ee % (kHeadDim / 4)) * 4;
-        }
-        for (int s0 = 0; s0 < nsi; s0 += 4) {
-          float ls[2][4];
-          float4 v[2][4];
+      for (int u = 0; u < kMergeU; ++u) {
+        const int e = e0 + u * kThreads;
+        on[u] = e < E;
+        const int ee = on[u] ? e : e0;
+        const int it2 = flags[ee / per_item], r = ee % per_item;
+        const int q0 = prefix[it2];
+        nsu[u] = (prefix[it2 + 1] - 1) / per_cta - q0 / per_cta + 1;
+        row[u] = (size_t)(it2 / H) * Hq + (it2 % H) * G + r / (kHeadDim / 4);
+        d[u] = (r % (kHeadDim / 4)) * 4;
+        M[u] = -INFINITY;
+        wsum[u] = 0.f;
+        acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (on[u]) nmax = max(nmax, nsu[u]);
+      }
+      for (int s0 = 0; s0 < nmax; s0 += 4) {
+        float ls[kMergeU][4];
+        float4 v[kMergeU][4];
 #pragma unroll
-          for (int u = 0; u < 2; ++u)
+        for (int u = 0; u < kMergeU; ++u)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int sl = min(s0 + k, nsi - 1);
-              ls[u][k] = __ldcg(a.lse_part + row[u] * a.max_splits + sl);
-              v[u][k] = __ldcg(reinterpret_cast<const float4*>(a.o_part + (row[u] * a.max_splits + sl) * kHeadDim + d[u]));
-              if (s0 + k >= nsi) ls[u][k] = -INFINITY;  // past the last partial: no weight
-            }
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float mn = M[u];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mn = fmaxf(mn, ls[u][k]);
-            const float sc = (M[u] == -INFINITY) ? 0.f : fast_exp2(M[u] - mn);
-            wsum[u] *= sc;
-            acc[u].x *= sc;
-            acc[u].y *= sc;
-            acc[u].z *= sc;
-            acc[u].w *= sc;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float fs = (ls[u][k] == -INFINITY) ? 0.f : fast_exp2(ls[u][k] - mn);
-              wsum[u] += fs;
-              acc[u].x += fs * v[u][k].x;
-              acc[u].y += fs * v[u][k].y;
-              acc[u].z += fs * v[u][k].z;
-              acc[u].w += fs * v[u][k].w;
-            }
-            M[u] = mn;
+          for (int k = 0; k < 4; ++k) {
+            const int sl = min(s0 + k, nsu[u] - 1);
+            ls[u][k] = __ldcg(a.lse_part + row[u] * a.max_splits + sl);
+            v[u][k] = __ldcg(reinterpret_cast<const float4*>(a.o_part + (row[u] * a.max_splits + sl) * kHeadDim + d[u]));
+            if (s0 + k >= nsu[u]) ls[u][k] = -INFINITY;  // past the item's last partial: no weight
           }
-        }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (!on[u]) continue;
-          const bool empty_row = !(wsum[u] > 0.f);
-          const float inv = empty_row ? 0.f : 1.f / wsum[u];
-          uint2 pk;
-          pk.x = pack_bf16x2(acc[u].x * inv, acc[u].y * inv);
-          pk.y = pack_bf16x2(acc[u].z * inv, acc[u].w * inv);
-          *reinterpret_cast<uint2*>(a.out + row[u] * kHeadDim + d[u]) = pk;
-          if (a.out_lse && d[u] == 0) a.out_lse[row[u]] = empty_row ? -INFINITY : (M[u] + log2f(wsum[u])) * kLn2;
+        for (int u = 0; u < kMergeU; ++u) {
+          float mn = M[u];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mn = fmaxf(mn, ls[u][k]);
+          const float sc = (M[u] == -INFINITY) ? 0.f : fast_exp2(M[u] - mn);
+          wsum[u] *= sc;
+          acc[u].x *= sc;
+          acc[u].y *= sc;
+          acc[u].z *= sc;
+          acc[u].w *= sc;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float fs = (ls[u][k] == -INFINITY) ? 0.f : fast_exp2(ls[u][k] - mn);
+            wsum[u] += fs;
+            acc[u].x += fs * v[u][k].x;
+            acc[u].y += fs * v[u][k].y;
+            acc[u].z += fs * v[u][k].z;
+            acc[u].w += fs * v[u][k].w;
+          }
+          M[u] = mn;
         }
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeU; ++u) {
+        if (!on[u]) continue;
+        const bool empty_row = !(wsum[u] > 0.f);
+        const float inv = empty_row ? 0.f : 1.f / wsum[u];
+        uint2 pk;
+        pk.x = pack_bf16x2(acc[u].x * inv, acc[u].y * inv);
+        pk.y = pack_bf16x2(acc[u].z * inv, acc[u].w * inv);
+        *reinterpret_cast<uint2*>(a.out + row[u] * kHeadDim + d[u]) = pk;
+        if (a.out_lse && d[u] == 0) a.out_lse[row[u]] = empty_row ? -INFINITY : (M[u] + log2f(wsum[u])) * kLn2;
       }
     }
     __syncthreads();
