@@ -703,7 +703,10 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     const float* __restrict__ scores, int32_t score_stride, const int32_t* __restrict__ lens, int32_t H, int32_t W,
     int32_t max_len, int32_t pool, int32_t keep, int32_t sink, int32_t recent, int32_t* __restrict__ kept,
     int32_t kept_stride, int32_t* __restrict__ kept_counts, unsigned* err) {
-  pdl_enter();
+  // The scores are the previous kernel's output: everything before the first
+  // score load (lengths, the cluster's start, zeroing its shared memory) runs
+  // before that kernel has completed; every thread waits for it before it reads
+  // a score or exits.
   extern __shared__ float pooled[];  // [n - W]
   __shared__ int hist[kBuckets];
   __shared__ uint32_t s_kmin[kSelWarps], s_kmax[kSelWarps];
@@ -722,6 +725,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = lens[b];
   if (n < W || n > max_len) {  // the same decision in every rank of the cluster
+    pdl_wait();
     if (tid == 0 && rank == 0) {
       raise_error(err, SE_DEVERR_LENGTH);
       kept_counts[pair] = 0;
@@ -735,14 +739,21 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
   const int C = c1 - c0;  // candidate j is position c0 + j
   int32_t* out = kept + (size_t)pair * kept_stride;
   if (C <= keep) {
+    pdl_wait();
     if (rank == 0) {
       for (int i = tid; i < n; i += kSelThreads) out[i] = i;
       if (tid == 0) kept_counts[pair] = n;
     }
     return;
   }
-  // Every rank has started before any writes into another rank's shared memory.
+  hist[tid] = 0;  // this rank's histogram; rank 0's is the pair's
+  for (int i = tid; i < kSelWords; i += kSelThreads) selw[i] = 0u;
+  if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
+  if (tid == 0) s_info[2] = 0;
+  // Every rank has started and zeroed its shared memory before any rank writes
+  // into another's.
   cluster.sync();
+  pdl_enter();
   const float* sc = scores + (size_t)pair * score_stride;
   const int half = pool / 2;
   uint32_t kmin = 0xffffffffu, kmax = 0u;  // over the candidates' pooled order keys
@@ -811,10 +822,6 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(
     s_kmin[warp] = kmin;
     s_kmax[warp] = kmax;
   }
-  hist[tid] = 0;  // this rank's histogram; rank 0's is the pair's
-  for (int i = tid; i < kSelWords; i += kSelThreads) selw[i] = 0u;
-  if (tid < 2 * 257) (&rhist[0][0])[tid] = 0;
-  if (tid == 0) s_info[2] = 0;
   __syncthreads();
   kmin = s_kmin[lane];
   kmax = s_kmax[lane];
@@ -1022,17 +1029,28 @@ __global__ void __launch_bounds__(256) snapkv_gather_kernel(KvView src, uint16_t
                                                             const int32_t* __restrict__ lens, int32_t pairs,
                                                             const int32_t* __restrict__ kept, int32_t kept_stride,
                                                             const int32_t* __restrict__ kept_counts, unsigned* err) {
-  pdl_enter();
+  // The lengths and the destination pages of these slots do not depend on the
+  // selection (the previous kernel): they are read before it has completed.
   const long long unit = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);  // (pair, group of kGatherTok tokens)
   const int sub = threadIdx.x & 15;
   const int groups = (kept_stride + kGatherTok - 1) / kGatherTok;
-  if (unit >= (long long)pairs * groups) return;
+  if (unit >= (long long)pairs * groups) {
+    pdl_wait();
+    return;
+  }
   const int pair = (int)(unit / groups), t0 = (int)(unit % groups) * kGatherTok;
   const int H = src.num_kv_heads;
   const int b = pair / H, h = pair % H;
+  const int n = lens[b];
+  int dpg[kGatherTok];
+#pragma unroll
+  for (int u = 0; u < kGatherTok; ++u) {
+    const int t = t0 + u;
+    dpg[u] = (t < kept_stride && t / kPageSize < dst_bt_stride) ? dst_bt[(size_t)b * dst_bt_stride + t / kPageSize] : -1;
+  }
+  pdl_enter();
   const int cnt = kept_counts[pair];
   if (cnt > kept_stride) return;
-  const int n = lens[b];
   // (page, head, slot) row of each token in the source and the destination cache; -1: not copied
   long long srow[kGatherTok], drow[kGatherTok];
 #pragma unroll
@@ -1046,7 +1064,7 @@ __global__ void __launch_bounds__(256) snapkv_gather_kernel(KvView src, uint16_t
       continue;
     }
     const int sp = src_bt[(size_t)b * src_bt_stride + pos / kPageSize];
-    const int dp = dst_bt[(size_t)b * dst_bt_stride + t / kPageSize];
+    const int dp = dpg[u];
     if (sp < 0 || sp >= src.num_pages || dp < 0 || dp >= dst_num_pages) {
       if (sub == 0) raise_error(err, SE_DEVERR_PAGE_RANGE);
       continue;
