@@ -652,10 +652,12 @@ def _snapkv_wl(name):
 def _e2e(args, step, x, before, after, stream, flush, dev):
     """The step as a server runs it: the step's inputs (q, k_new, v_new and both lengths)
     packed in one pinned host buffer and copied to the device in one transfer, the step
-    through the library, the output copied back to pinned host memory. The step is the
-    four C-ABI calls recorded once with se_capture_begin / se_capture_end and replayed
-    with se_graph_launch every step; the same path with the four calls made live every
-    step is timed too (``calls_ms_per_step``)."""
+    through the library, the output copied back to pinned host memory. The upload
+    (se_copy_async), the four C-ABI calls and the download (se_copy_async) are recorded
+    once with se_capture_begin / se_capture_end and replayed with one se_graph_launch per
+    step. Timed too: the copies made by torch around a replay of the four recorded calls
+    (``split_ms_per_step``), and the four calls made live every step
+    (``calls_ms_per_step``)."""
     import torch
 
     import sparse_decode_attention_quest_gb300 as se
@@ -681,54 +683,77 @@ def _e2e(args, step, x, before, after, stream, flush, dev):
         step.run(d_q, d_after, d_kn, d_vn, d_before, stream=s)
 
     se.se_capture_begin(stream)
+    se.se_copy_async(d_buf, h_buf, stream)
+    live(stream)
+    se.se_copy_async(h_out, step.out, stream)
+    graph_io = se.se_capture_end(stream)
+    se.se_capture_begin(stream)
     live(stream)
     graph = se.se_capture_end(stream)
 
-    def e2e_step(replay, ev0=None, ev1=None):
+    def e2e_step(mode, ev0=None, ev1=None):
+        if mode == "one" and ev0 is None:
+            graph_io.launch(stream)  # the whole step: one call
+            return
         with torch.cuda.stream(stream):
             if ev0 is not None:
                 ev0.record(stream)
-            d_buf.copy_(h_buf, non_blocking=True)
-            if replay:
-                graph.launch(stream)
+            if mode == "one":
+                graph_io.launch(stream)
             else:
-                live(stream)
-            h_out.copy_(step.out, non_blocking=True)
+                d_buf.copy_(h_buf, non_blocking=True)
+                if mode == "split":
+                    graph.launch(stream)
+                else:
+                    live(stream)
+                h_out.copy_(step.out, non_blocking=True)
             if ev1 is not None:
                 ev1.record(stream)
 
-    def timed(replay):
+    def timed(mode):
+        """Host wall clock per step (no events in the clocked region), then the
+        same steps again with events around each for the stream time."""
         for _ in range(args.warmup):
             flush(1.0)
-            e2e_step(replay)
+            e2e_step(mode)
         torch.cuda.synchronize()
         n = max(10, args.steps // 4)
-        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         host_ms = []
         for i in range(n):
             with torch.cuda.stream(stream):
                 flush(float(i))
             stream.synchronize()  # the flush is done before the clock starts
             t0 = time.perf_counter()
-            e2e_step(replay, *pairs[i])
+            e2e_step(mode)
             stream.synchronize()  # the output is in host memory
             host_ms.append((time.perf_counter() - t0) * 1e3)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            with torch.cuda.stream(stream):
+                flush(float(i))
+            e2e_step(mode, *pairs[i])
         torch.cuda.synchronize()
         return n, statistics.mean(host_ms), statistics.mean(a.elapsed_time(b) for a, b in pairs)
 
-    n, ms, stream_ms = timed(True)
-    _, calls_ms, calls_stream_ms = timed(False)
+    n, ms, stream_ms = timed("one")
+    _, split_ms, split_stream_ms = timed("split")
+    _, calls_ms, calls_stream_ms = timed("calls")
+    graph_io.destroy()
     graph.destroy()
     return {"value": wl.batch / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": n,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "timing": "host wall clock per step: from before the host-to-device copy is enqueued to the return of "
-                      "a stream synchronize after the device-to-host copy of the output (launches, copies and "
-                      "kernels included; the L2 flush before it excluded)",
+            "timing": "host wall clock per step: from before the step's launch (the upload first) to the return of "
+                      "a stream synchronize after the download of the output (launches, copies and kernels "
+                      "included; the L2 flush before it excluded); stream_ms_per_step: CUDA events around the "
+                      "same steps in a second pass",
             "stream_ms_per_step": stream_ms,
+            "split_ms_per_step": split_ms, "split_stream_ms_per_step": split_stream_ms,
             "calls_ms_per_step": calls_ms, "calls_stream_ms_per_step": calls_stream_ms,
-            "path": "pinned host q/k_new/v_new/lengths (one packed buffer, one copy) -> device, the step's four "
-                    "C-ABI calls recorded once (se_capture_begin / se_capture_end) and replayed with "
-                    "se_graph_launch, output -> pinned host; calls_ms_per_step: the four calls made live instead"}
+            "path": "pinned host q/k_new/v_new/lengths (one packed buffer) -> device with se_copy_async, the step's "
+                    "four C-ABI calls, output -> pinned host with se_copy_async, all recorded once "
+                    "(se_capture_begin / se_capture_end) and replayed with one se_graph_launch per step; "
+                    "split_ms_per_step: torch copies around a replay of the four recorded calls; "
+                    "calls_ms_per_step: torch copies around the four calls made live"}
 
 
 # --------------------------------------------------------------------------- reference arm

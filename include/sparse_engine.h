@@ -465,6 +465,27 @@ SE_API se_status_t se_graph_launch(se_graph_t graph, void* stream);
 SE_API void se_graph_destroy(se_graph_t graph);
 
 /*
+ * se_copy_async -- copies `bytes` bytes from src to dst on `stream`,
+ * asynchronously: device memory to or from page-locked host memory, or device
+ * to device (the direction follows from the addresses). Up to 8 MiB between
+ * device memory and page-locked host memory, the copy is a kernel of the
+ * library whose loads or stores reach the host side directly (a decode step's
+ * few hundred KB move in a fraction of a copy engine's start-up); it waits for
+ * the previous kernel on `stream` like every kernel of the library. Other
+ * copies use the copy engine (cudaMemcpyAsync). Made between
+ * se_capture_begin and se_capture_end it is recorded too, so that a step's
+ * input upload and result download replay with its kernels in one launch. The
+ * pages have no counterpart: this is host plumbing around their hot path.
+ * Pageable host memory is not allowed while recording (CUDA refuses it) and
+ * makes a live copy synchronous. Ownership: both buffers stay the caller's and
+ * must outlive the copy (and every replay of a recording that holds it).
+ * Errors: SE_ERR_INVALID_ARG for a NULL dst or src with bytes > 0 (bytes = 0
+ * is a no-op); SE_ERR_CUDA for a failing copy, with the CUDA error in
+ * se_last_error_detail().
+ */
+SE_API se_status_t se_copy_async(void* dst, const void* src, size_t bytes, void* stream);
+
+/*
  * se_debug_snapkv_wait_probe -- test hook for the bounded waits; it computes
  * nothing (the pages have no counterpart). In the next se_snapkv_window_scores
  * call issued from this host thread (also inside se_snapkv_score_and_compact*),

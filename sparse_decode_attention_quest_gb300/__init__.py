@@ -91,6 +91,7 @@ _SIGNATURES = {
     "se_capture_end": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     "se_graph_launch": (ctypes.c_int, [_P, _P]),
     "se_graph_destroy": (None, [_P]),
+    "se_copy_async": (ctypes.c_int, [_P, _P, _Z, _P]),
     "se_snapkv_select_windowed": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
     "se_snapkv_compact": (ctypes.c_int, [_KV, _P, _I, _P, _I, _KV, _P, _I, _P, _I, _P, _P]),
     "se_snapkv_score_and_compact": (ctypes.c_int, [_KV, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _F, _KV, _P, _I, _P,
@@ -203,6 +204,25 @@ def se_capture_end(stream=None) -> SEGraph:
     h = ctypes.c_void_p(None)
     _check(load_library().se_capture_end(_stream(stream), ctypes.byref(h)))
     return SEGraph(h.value)
+
+
+def _copy_ptr(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name}: a host tensor must be in page-locked memory (pin_memory())")
+    return t.data_ptr()
+
+
+def se_copy_async(dst: torch.Tensor, src: torch.Tensor, stream=None):
+    """Copy ``src`` into ``dst`` (same number of bytes; device or pinned host memory)
+    asynchronously on ``stream``; recordable between se_capture_begin and se_capture_end."""
+    nb = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nb:
+        raise ValueError("se_copy_async: dst and src differ in size")
+    _check(load_library().se_copy_async(_copy_ptr(dst, "dst"), _copy_ptr(src, "src"), nb, _stream(stream)))
 
 
 def se_read_device_error(clear: bool = True) -> int:

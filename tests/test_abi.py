@@ -203,3 +203,10 @@ def test_replayable_step_calls_reject_missing_handles(se_lib):
     assert se_lib.se_capture_end(ctypes.c_void_p(FAKE), None) == INVALID
     assert se_lib.se_graph_launch(None, None) == INVALID
     se_lib.se_graph_destroy(None)
+
+
+def test_copy_async_host_checks(se_lib):
+    # an empty copy is a no-op (no CUDA call); a NULL buffer with bytes to copy is refused
+    assert se_lib.se_copy_async(None, None, 0, None) == 0
+    assert se_lib.se_copy_async(None, ctypes.c_void_p(FAKE), 16, None) == INVALID
+    assert se_lib.se_copy_async(ctypes.c_void_p(FAKE), None, 16, None) == INVALID

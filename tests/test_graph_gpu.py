@@ -80,3 +80,70 @@ def test_replayed_step_follows_its_buffers(cuda_device):
         assert torch.equal(rec.summary.view(torch.int16), live.summary.view(torch.int16))
     finally:
         graph.destroy()
+
+
+def test_replayed_step_with_its_copies(cuda_device):
+    """The input upload (pinned host -> device), the four calls and the result
+    download recorded in one step: each replay computes what the live calls do
+    on the values the host buffer holds at that launch."""
+    dev = cuda_device
+    wl = QWEN3_30B_A3B_QUEST_128K.scaled(batch=3, context_min=1500, context_max=4000, topk_pages=16, seed=41)
+    x = make_quest_decode_inputs(wl, device="cpu", poison_tail=True)
+    live, rec = _make(x, wl, dev), _make(x, wl, dev)
+    B, Hq, H, D = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    start = torch.tensor(x.seq_lens, dtype=torch.int32) - 2
+    assert int(start.min()) >= 0
+    shapes = [((B, Hq, D), torch.bfloat16), ((B, H, D), torch.bfloat16), ((B, H, D), torch.bfloat16),
+              ((B,), torch.int32), ((B,), torch.int32)]
+    offs, size = [], 0
+    for shp, dt in shapes:
+        offs.append(size)
+        n = 1
+        for v in shp:
+            n *= v
+        size += (n * torch.empty((), dtype=dt).element_size() + 15) // 16 * 16
+    h_in = torch.zeros(size, dtype=torch.uint8).pin_memory()
+    d_in = torch.zeros(size, dtype=torch.uint8, device=dev)
+
+    def views(buf):
+        out = []
+        for (shp, dt), o in zip(shapes, offs):
+            n = 1
+            for v in shp:
+                n *= v
+            nb = n * torch.empty((), dtype=dt).element_size()
+            out.append(buf[o:o + nb].view(dt).view(shp))
+        return out
+
+    hq, hkn, hvn, hbefore, hafter = views(h_in)
+    dq, dkn, dvn, dbefore, dafter = views(d_in)
+    h_out = torch.zeros(rec.out.shape, dtype=rec.out.dtype).pin_memory()
+    stream = torch.cuda.Stream(device=dev)
+    se.se_capture_begin(stream)
+    se.se_copy_async(d_in, h_in, stream)
+    rec.run(dq, dafter, dkn, dvn, dbefore, stream=stream)
+    se.se_copy_async(h_out, rec.out, stream)
+    graph = se.se_capture_end(stream)
+    g = torch.Generator().manual_seed(6)
+    try:
+        for t in range(3):
+            q = torch.randn(B, Hq, D, generator=g).bfloat16()
+            kn = torch.randn(B, H, D, generator=g).bfloat16()
+            vn = torch.randn(B, H, D, generator=g).bfloat16()
+            before = start + t
+            after = before + 1
+            stream.synchronize()
+            hq.copy_(q)
+            hkn.copy_(kn)
+            hvn.copy_(vn)
+            hbefore.copy_(before)
+            hafter.copy_(after)
+            graph.launch(stream)
+            stream.synchronize()
+            live.run(q.to(dev), after.to(dev), kn.to(dev), vn.to(dev), before.to(dev))
+            torch.cuda.synchronize()
+            assert torch.equal(rec.counts, live.counts), t
+            assert torch.equal(h_out.view(torch.int16), live.out.cpu().view(torch.int16)), t
+            assert torch.equal(rec.lse, live.lse), t
+    finally:
+        graph.destroy()
