@@ -102,7 +102,7 @@ struct MlaArgs {
   float scale_log2;
   uint16_t* out;     // [B][Hq][512]
   float* out_lse;
-  float* o_part;     // [B * Hq][max_splits][512]
+  float* o_part;     // [B * Hq / 4][max_splits][512][4]: four heads' partials per dim
   float* lse_part;   // [B * Hq][max_splits], log2 domain
   int32_t* item_ns;  // [B]
   unsigned* err;
@@ -640,16 +640,29 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
             tmem_ld32(tmem + lane_base + kOCol + mt * 64 + 32 * (warp >> 2), o);
             tmem_ld_wait();
             const int d = mt * 128 + 32 * q4 + lane;
+            if (ns == 1) {
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-              const int h = 32 * (warp >> 2) + cc;
-              if (h < Hq) {
-                const float val = __uint_as_float(o[cc]) * linv[h];
-                const size_t orow = (size_t)b * Hq + h;
-                if (ns == 1)
-                  a.out[orow * kDv + d] = (uint16_t)(pack_bf16x2(val, 0.f) & 0xffffu);
-                else
-                  a.o_part[(orow * a.max_splits + slot) * kDv + d] = val;
+              for (int cc = 0; cc < 32; ++cc) {
+                const int h = 32 * (warp >> 2) + cc;
+                if (h < Hq) {
+                  const float val = __uint_as_float(o[cc]) * linv[h];
+                  a.out[((size_t)b * Hq + h) * kDv + d] = (uint16_t)(pack_bf16x2(val, 0.f) & 0xffffu);
+                }
+              }
+            } else {
+              // A partial: the thread's four heads 4 k .. 4 k + 3 at its dim d in
+              // one 16-byte store (four 4-byte stores per value run at a
+              // fraction of the rate and hold up the softmax warps).
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int h = 32 * (warp >> 2) + 4 * k;
+                if (h < Hq) {
+                  const float4 val =
+                      make_float4(__uint_as_float(o[4 * k]) * linv[h], __uint_as_float(o[4 * k + 1]) * linv[h + 1],
+                                  __uint_as_float(o[4 * k + 2]) * linv[h + 2], __uint_as_float(o[4 * k + 3]) * linv[h + 3]);
+                  const size_t blk = ((size_t)b * Hq + h) / 4;
+                  *reinterpret_cast<float4*>(a.o_part + ((blk * a.max_splits + slot) * kDv + d) * 4) = val;
+                }
               }
             }
           }
@@ -674,67 +687,105 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Merge the partials of the items spread over several CTAs; one warp per
-// (request, query head) row. The log-sum-exps of up to 32 splits come in one
-// round trip (lane s reads split s); the partial outputs are read split by
-// split, the 4 column chunks of a lane and two splits at a time in flight, and
-// added in split order. Items held by one CTA were written directly; rows of
-// requests with no selected page get 0 and lse = -inf.
+// Merge the partials of the items spread over several CTAs; one warp per four
+// query heads of a request (the partials hold four heads per dim). Splits come
+// in chunks of 32: lane s holds the four heads' log-sum-exps of split s of the
+// chunk (one round trip);
+// lane l takes dims 4 l + 128 j (j = 0..3, 4 consecutive dims each) of the four
+// heads, and the splits are added in split order, two at a time in flight.
+// Items held by one CTA were written directly; rows of requests with no
+// selected page get 0 and lse = -inf.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restrict__ o_part,
                                                           const float* __restrict__ lse_part,
                                                           const int32_t* __restrict__ item_ns, int32_t batch,
                                                           int32_t Hq, int32_t max_splits, uint16_t* __restrict__ out,
                                                           float* __restrict__ out_lse) {
   pdl_enter();
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (row >= batch * Hq) return;
+  const int blk = blockIdx.x * 4 + (threadIdx.x >> 5);  // four heads: rows 4 blk .. 4 blk + 3
+  if (blk * 4 >= batch * Hq) return;
   const int lane = threadIdx.x & 31;
-  const int ns = min(item_ns[row / Hq], max_splits);
+  const int ns = min(item_ns[(blk * 4) / Hq], max_splits);
   if (ns == 1) return;
-  const float* lp = lse_part + (size_t)row * max_splits;
-  const float* op = o_part + (size_t)row * max_splits * kDv + lane * 4;
-  float M = -INFINITY;
-  for (int s0 = 0; s0 < ns; s0 += 32) M = fmaxf(M, s0 + lane < ns ? lp[s0 + lane] : -INFINITY);
+  float ls[4], M[4], wsum[4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float wsum = 0.f;
-  float4 acc[4];
+  for (int hh = 0; hh < 4; ++hh) {
+    const float* lp = lse_part + (size_t)(blk * 4 + hh) * max_splits;
+    ls[hh] = lane < ns ? lp[lane] : -INFINITY;  // the first chunk
+    float m = ls[hh];
+    for (int c0 = 32; c0 < ns; c0 += 32) m = fmaxf(m, c0 + lane < ns ? lp[c0 + lane] : -INFINITY);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  auto add = [&](float l, const float4 (&v)[4]) {
-    if (l == -INFINITY) return;
-    const float f = fast_exp2(l - M);
-    wsum += f;
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    M[hh] = m;
+    wsum[hh] = 0.f;
+  }
+  // acc[j][e]: dim 4 lane + 128 j + e, the four heads in x, y, z, w
+  float4 acc[4][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[j].x += f * v[j].x;
-      acc[j].y += f * v[j].y;
-      acc[j].z += f * v[j].z;
-      acc[j].w += f * v[j].w;
-    }
-  };
-  for (int s = 0; s < ns; s += 2) {
-    const bool two = s + 1 < ns;
-    float4 v0[4], v1[4];
+  for (int j = 0; j < 4; ++j)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) v0[j] = *reinterpret_cast<const float4*>(op + (size_t)s * kDv + 128 * j);
+    for (int e = 0; e < 4; ++e) acc[j][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float* op = o_part + (size_t)blk * max_splits * kDv * 4;
+  auto load = [&](int sp, float4 (&v)[4][4]) {
+    const float* p = op + (size_t)sp * kDv * 4;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      v1[j] = two ? *reinterpret_cast<const float4*>(op + (size_t)(s + 1) * kDv + 128 * j)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    add(lp[s], v0);
-    if (two) add(lp[s + 1], v1);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[j][e] = *reinterpret_cast<const float4*>(p + (size_t)(4 * lane + 128 * j + e) * 4);
+  };
+  auto add = [&](int sp, const float4 (&v)[4][4]) {
+    float f[4];
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      const float l = __shfl_sync(0xffffffffu, ls[hh], sp & 31);
+      f[hh] = l == -INFINITY ? 0.f : fast_exp2(l - M[hh]);
+      wsum[hh] += f[hh];
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[j][e].x += f[0] * v[j][e].x;
+        acc[j][e].y += f[1] * v[j][e].y;
+        acc[j][e].z += f[2] * v[j][e].z;
+        acc[j][e].w += f[3] * v[j][e].w;
+      }
+  };
+  for (int sp = 0; sp < ns; sp += 2) {  // warp-uniform
+    if (sp > 0 && (sp & 31) == 0)  // the next chunk's log-sum-exps
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh)
+        ls[hh] = sp + lane < ns ? lse_part[(size_t)(blk * 4 + hh) * max_splits + sp + lane] : -INFINITY;
+    float4 v0[4][4], v1[4][4];
+    load(sp, v0);
+    if (sp + 1 < ns) load(sp + 1, v1);
+    add(sp, v0);
+    if (sp + 1 < ns) add(sp + 1, v1);
   }
-  const bool empty_row = !(wsum > 0.f);
-  const float inv = empty_row ? 0.f : 1.f / wsum;
+  float inv[4], lse[4];
+#pragma unroll
+  for (int hh = 0; hh < 4; ++hh) {
+    const bool empty_row = !(wsum[hh] > 0.f);
+    inv[hh] = empty_row ? 0.f : 1.f / wsum[hh];
+    lse[hh] = empty_row ? -INFINITY : (M[hh] + log2f(wsum[hh])) * kLn2;
+  }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    uint2 pk;
-    pk.x = pack_bf16x2(acc[j].x * inv, acc[j].y * inv);
-    pk.y = pack_bf16x2(acc[j].z * inv, acc[j].w * inv);
-    *reinterpret_cast<uint2*>(out + (size_t)row * kDv + lane * 4 + 128 * j) = pk;
+    const int d = 4 * lane + 128 * j;
+    uint2 pk[4];
+    pk[0].x = pack_bf16x2(acc[j][0].x * inv[0], acc[j][1].x * inv[0]);
+    pk[0].y = pack_bf16x2(acc[j][2].x * inv[0], acc[j][3].x * inv[0]);
+    pk[1].x = pack_bf16x2(acc[j][0].y * inv[1], acc[j][1].y * inv[1]);
+    pk[1].y = pack_bf16x2(acc[j][2].y * inv[1], acc[j][3].y * inv[1]);
+    pk[2].x = pack_bf16x2(acc[j][0].z * inv[2], acc[j][1].z * inv[2]);
+    pk[2].y = pack_bf16x2(acc[j][2].z * inv[2], acc[j][3].z * inv[2]);
+    pk[3].x = pack_bf16x2(acc[j][0].w * inv[3], acc[j][1].w * inv[3]);
+    pk[3].y = pack_bf16x2(acc[j][2].w * inv[3], acc[j][3].w * inv[3]);
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh)
+      *reinterpret_cast<uint2*>(out + (size_t)(blk * 4 + hh) * kDv + d) = pk[hh];
   }
-  if (out_lse && lane == 0) out_lse[row] = empty_row ? -INFINITY : (M + log2f(wsum)) * kLn2;
+  if (out_lse && lane < 4)
+    out_lse[blk * 4 + lane] = lane == 0 ? lse[0] : lane == 1 ? lse[1] : lane == 2 ? lse[2] : lse[3];
 }
 
 size_t smem_bytes(int32_t batch) { return 1024 + (size_t)kMiscOff + kPrefixOff + (size_t)(batch + 1) * 4; }
@@ -800,7 +851,7 @@ cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const CUtensorMap& qmap,
   if (e != cudaSuccess) return e;
   e = launch_pdl(mla_decode_kernel, dim3(plan.grid), dim3(kThreads), smem, stream, kvmap, qmap, a);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(mla_combine_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, stream, a.o_part, a.lse_part,
+  e = launch_pdl(mla_combine_kernel, dim3((unsigned)((rows / 4 + 3) / 4)), dim3(128), 0, stream, a.o_part, a.lse_part,
                  a.item_ns, batch, num_q_heads, plan.nsplit, out, out_lse);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

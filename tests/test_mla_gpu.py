@@ -87,6 +87,16 @@ def test_latent_many_pages_per_slice(cuda_device):
     compare_decode(x, step, range(wl.batch), _scale(wl), "latent long slices")
 
 
+def test_latent_one_request_over_many_splits(cuda_device):
+    """One request's 1,101 selected pages over 16-page slices: about 70 decode
+    splits, so the combine takes their log-sum-exps in several chunks of 32."""
+    wl = MLA_GLM_QUEST_32K.scaled(batch=1, num_q_heads=16, context_min=18000, context_max=18000,
+                                  topk_pages=1100, seed=71)
+    x, step, lens = _prepare(wl, cuda_device)
+    _run(x, step, lens, cuda_device)
+    compare_decode(x, step, range(wl.batch), _scale(wl), "latent many splits")
+
+
 def test_latent_decode_on_the_oracle_selection(cuda_device):
     wl = MLA_GLM_QUEST_32K.scaled(batch=3, context_min=2000, context_max=2600, topk_pages=30, seed=53)
     x, step, lens = _prepare(wl, cuda_device)
