@@ -147,3 +147,24 @@ def test_replayed_step_with_its_copies(cuda_device):
             assert torch.equal(rec.lse, live.lse), t
     finally:
         graph.destroy()
+
+
+@pytest.mark.parametrize("nbytes, offset", [(16, 0), (4096, 0), (328_000, 0), (1000, 0), (777, 3),
+                                            (9 << 20, 0), ((9 << 20) + 5, 1)])
+def test_copy_async_every_path(cuda_device, nbytes, offset):
+    """se_copy_async host -> device -> device -> host on one stream: the kernel
+    (16-byte pieces, or bytes for unaligned sizes and offsets) up to 8 MiB, the
+    copy engine above, and device to device; the bytes come back unchanged."""
+    dev = cuda_device
+    g = torch.Generator().manual_seed(nbytes + offset)
+    src = torch.randint(0, 256, (nbytes + offset,), dtype=torch.uint8, generator=g).pin_memory()
+    d1 = torch.zeros(nbytes + offset, dtype=torch.uint8, device=dev)
+    d2 = torch.zeros(nbytes + offset, dtype=torch.uint8, device=dev)
+    back = torch.zeros(nbytes + offset, dtype=torch.uint8).pin_memory()
+    stream = torch.cuda.Stream(device=dev)
+    se.se_copy_async(d1[offset:], src[offset:], stream)
+    se.se_copy_async(d2[offset:], d1[offset:], stream)
+    se.se_copy_async(back[offset:], d2[offset:], stream)
+    stream.synchronize()
+    assert torch.equal(back[offset:], src[offset:])
+    assert int(back[:offset].sum()) == 0
