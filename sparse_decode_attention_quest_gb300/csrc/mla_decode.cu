@@ -36,7 +36,10 @@
 //  * O^T += V^T P^T: four M = 128 MMAs per 16 tokens (dims 128 mt ..), A = the
 //    tile's first 512 dims read MN-major, B = P read MN-major; O^T of all 64
 //    heads is 4 x 64 TMEM columns. The epilogue divides by the softmax sums
-//    and writes the output (one slice) or a partial for the combine kernel.
+//    and writes the output (one slice) or a partial for the combine kernel:
+//    four heads per dim, one 16-byte store each (the softmax warps serve no
+//    tile meanwhile; one 4-byte store per head and dim took three times as
+//    long at every segment switch).
 #include "se_ptx.cuh"
 
 namespace se {

@@ -47,7 +47,8 @@
 // (4 x 32K prompts: 0.255 ms per eviction with 32 MiB chunks, 0.195 with 64,
 // 0.182 with 96, 0.152 with one chunk), so the default keeps one chunk up to
 // 256 MiB of keys. In a launch the chunk's tiles form one flattened range that
-// every CTA shares equally. Every pass-1 share writes its rows' (max, sum) and
+// every CTA shares equally; pass 2 walks its share backwards, so that its first
+// tiles are the ones pass 1 read last, still in L2. Every pass-1 share writes its rows' (max, sum) and
 // counts itself in on the pair's counter (zeroed before the first launch); the
 // share that completes the count merges them into the rows' final
 // log-sum-exps, which pass 2 reads.
