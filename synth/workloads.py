@@ -57,6 +57,7 @@ class QuestDecodeWorkload:
     outlier_channels: int = 4
     outlier_scale: float = 8.0
     latent: bool = False     # one cache row holds the key; the value is its first head_dim_v dims
+    outliers_in_value: bool = False  # latent cache: outlier channels drawn over all dims, the value's too
     page_size: int = PAGE_SIZE
     lengths: tuple = ()      # explicit per-request lengths (override the uniform draw)
 
@@ -162,8 +163,9 @@ def make_quest_decode_inputs(wl: QuestDecodeWorkload, device="cpu", poison_tail=
     bt, num_pages = _block_table(ppr, wl.permuted_table, cpu_g)
 
     # Outlier key channels, per KV head. For a latent cache the outliers sit in the
-    # RoPE part of the row (dims head_dim_v .. head_dim-1), which is not part of the value.
-    lo = wl.head_dim_v if wl.latent else 0
+    # RoPE part of the row (dims head_dim_v .. head_dim-1), which is not part of the
+    # value, unless outliers_in_value draws them over the whole row.
+    lo = wl.head_dim_v if wl.latent and not wl.outliers_in_value else 0
     width = wl.head_dim - lo
     outliers = []
     scale = torch.ones(wl.num_kv_heads, 1, wl.head_dim)

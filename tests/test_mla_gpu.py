@@ -97,6 +97,19 @@ def test_latent_one_request_over_many_splits(cuda_device):
     compare_decode(x, step, range(wl.batch), _scale(wl), "latent many splits")
 
 
+def test_latent_value_outlier_channels(cuda_device):
+    """Outlier channels (x3) drawn over the whole 576-dim row, so that some fall
+    in the value part: the output stays below 4 in magnitude, where bf16
+    rounding is well inside the absolute tolerance."""
+    wl = MLA_GLM_QUEST_32K.scaled(batch=3, context_min=1800, context_max=3000, topk_pages=30, seed=73,
+                                  outliers_in_value=True, outlier_channels=12, outlier_scale=3.0)
+    x, step, lens = _prepare(wl, cuda_device)
+    assert any(c < wl.head_dim_v for c in x.outlier_channels[0])  # some outliers are value dims
+    _run(x, step, lens, cuda_device)
+    assert float(step.out.float().abs().max()) < 4.0
+    compare_decode(x, step, range(wl.batch), _scale(wl), "latent value outliers")
+
+
 def test_latent_decode_on_the_oracle_selection(cuda_device):
     wl = MLA_GLM_QUEST_32K.scaled(batch=3, context_min=2000, context_max=2600, topk_pages=30, seed=53)
     x, step, lens = _prepare(wl, cuda_device)
