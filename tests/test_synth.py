@@ -54,6 +54,18 @@ def test_latent_outliers_outside_the_value():
     assert all(512 <= c < 576 for c in x.outlier_channels[0])
 
 
+def test_latent_outliers_over_the_whole_row():
+    # outliers_in_value draws the outlier channels over all 576 dims, the value's
+    # too, and scales them by outlier_scale
+    wl = MLA_GLM_QUEST_32K.scaled(batch=2, context_min=512, context_max=512, outliers_in_value=True,
+                                  outlier_channels=12, outlier_scale=3.0, seed=73)
+    x = make_quest_decode_inputs(wl)
+    ch = x.outlier_channels[0]
+    assert len(ch) == 12 and any(c < 512 for c in ch) and all(0 <= c < 576 for c in ch)
+    std = x.k_cache.float()[:, 0].reshape(-1, 576).std(dim=0)
+    assert bool((std[ch] > 2.5).all()) and float(std[[c for c in range(576) if c not in ch]].max()) < 1.2
+
+
 def test_snapkv_inputs():
     wl = SNAPKV_PREFILL_32K.scaled(batch=2, prompt_min=100, prompt_max=300)
     x = make_snapkv_inputs(wl)
